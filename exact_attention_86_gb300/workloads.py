@@ -1,0 +1,116 @@
+"""Seeded synthetic workloads for the attention forward.
+
+This module only draws inputs; it holds none of the attention arithmetic.
+Tests, the benchmark and the smoke check draw the SAME bf16 tensors from it,
+and both the CUDA path and the CPU oracle read those tensors.
+
+Recipe (identical for every workload): a CPU ``torch.Generator`` seeded with
+the workload's seed draws ``q``, ``k``, ``v`` in that order with
+``torch.randn(..., dtype=float32)``, multiplied by the workload's standard
+deviation and rounded to bfloat16.  A padded-batch workload then draws
+``kv_lens`` with ``torch.randint(0, Sk + 1, (B,))`` and forces the entry at
+``kv_zero_index`` to 0 (one sequence with no valid key).  A second draw of a
+workload continues the same generator after the first draw (q, k, v again,
+then kv_lens if the workload has them), scaled by ``second_std``.
+"""
+
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+from typing import Optional
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    Sq: int
+    Sk: int
+    D: int
+    causal: bool
+    seed: int
+    std: float = 1.0
+    padded: bool = False          # draws per-sequence kv_lens in [0, Sk]
+    kv_zero_index: int = 0        # which sequence is forced to kv_len = 0
+    second_std: Optional[float] = None  # std of an optional second draw
+
+    @property
+    def scale(self) -> float:
+        """Softmax scale passed to the kernel: 1/sqrt(D)."""
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def flops(self) -> float:
+        """4*B*H*Sq*Sk*D, halved when causal (the headline FLOP count)."""
+        f = 4.0 * self.B * self.H * self.Sq * self.Sk * self.D
+        return f / 2 if self.causal else f
+
+    @property
+    def min_bytes(self) -> int:
+        """Read Q, K, V once (bf16), write O (bf16) and LSE (fp32) once."""
+        return (2 * self.B * self.H * self.D * (2 * self.Sq + 2 * self.Sk)
+                + 4 * self.B * self.H * self.Sq)
+
+    def label(self) -> str:
+        s = (f"B{self.B} H{self.H} Sq{self.Sq} Sk{self.Sk} D{self.D} "
+             f"{'causal' if self.causal else 'non-causal'}")
+        if self.padded:
+            s += " kv_len~U[0,Sk] (one 0)"
+        return s
+
+
+# The five workloads of the attention forward (one per line of the benchmark
+# table), plus the causal run of the S=8192 workload.
+WORKLOADS = {
+    "s128_d64": Workload("s128_d64", 1, 1, 128, 128, 64, False, seed=0),
+    "s1024_d64_causal": Workload("s1024_d64_causal", 4, 8, 1024, 1024, 64, True, seed=1),
+    "s2048_d128_padded": Workload("s2048_d128_padded", 8, 16, 2048, 2048, 128, False, seed=2,
+                                  padded=True, kv_zero_index=0),
+    "s8192_d128": Workload("s8192_d128", 2, 16, 8192, 8192, 128, False, seed=3, second_std=2.0),
+    "s8192_d128_causal": Workload("s8192_d128_causal", 2, 16, 8192, 8192, 128, True, seed=3,
+                                  second_std=2.0),
+    "s32768_d128_causal": Workload("s32768_d128_causal", 1, 8, 32768, 32768, 128, True, seed=4),
+}
+
+HEADLINE = "s8192_d128"
+
+
+def _draw(g: torch.Generator, w: Workload, std: float):
+    shape_q = (w.B, w.H, w.Sq, w.D)
+    shape_kv = (w.B, w.H, w.Sk, w.D)
+    q = (torch.randn(shape_q, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+    k = (torch.randn(shape_kv, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+    v = (torch.randn(shape_kv, generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+    kv = None
+    if w.padded:
+        kv = torch.randint(0, w.Sk + 1, (w.B,), generator=g, dtype=torch.int64).to(torch.int32)
+        kv[w.kv_zero_index] = 0
+    return q, k, v, kv
+
+
+def generate(w: Workload, draw: int = 0):
+    """Return ``(q, k, v, kv_lens)`` on the CPU: bf16 ``[B,H,S,D]`` contiguous
+    tensors and an int32 ``[B]`` tensor or ``None``.  ``draw=1`` is the
+    workload's second draw (std ``second_std``)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    out = _draw(g, w, w.std)
+    if draw == 0:
+        return out
+    if draw != 1 or w.second_std is None:
+        raise ValueError(f"workload {w.name} has no draw {draw}")
+    return _draw(g, w, w.second_std)
+
+
+def small(name: str, B: int, H: int, Sq: int, Sk: int, D: int, causal: bool, seed: int,
+          padded: bool = False, std: float = 1.0) -> Workload:
+    """A reduced workload with the same recipe (for oracle-sized parity cases)."""
+    return Workload(name, B, H, Sq, Sk, D, causal, seed, std=std, padded=padded)
+
+
+def shrink(w: Workload, **kw) -> Workload:
+    return replace(w, **kw)

@@ -1,0 +1,28 @@
+"""CPU oracle for the fused attention forward — TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The
+product path (``exact_attention_86_gb300``) never imports it and has no CPU
+fallback: if the CUDA library is missing, the product raises.
+
+Contents:
+
+* ``attention.attention_ref`` — the plain definition of exact attention,
+  ``softmax(Q K^T * scale + mask) V`` with the per-row log-sum-exp, in float64,
+  with every score row materialised in full ("Kernel Fusion and the Memory
+  Wall", section "FlashAttention: avoid the full score matrix"; the stable
+  softmax of section "Softmax needs a global row statistic").
+* ``attention.attention_rows`` — the same definition for a chosen set of query
+  rows of one head, used for sampled parity at full size.
+* ``online.online_softmax_attention`` — the tiled online-softmax recurrence
+  (running max, normaliser, numerator, each corrected by exp(m_old - m_new))
+  from "Attention softmax fusion", section "The tile loop", and "Kernel Fusion
+  and the Memory Wall", section "FlashAttention: avoid the full score matrix".
+  It exists only so the tests can pin the materialised form against it.
+
+The oracle shares no code with the CUDA path: it reads float64 NumPy arrays
+and nothing else.
+"""
+
+from .attention import attention_ref, attention_rows, valid_key_count  # noqa: F401
+from .online import online_softmax_attention  # noqa: F401

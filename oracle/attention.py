@@ -1,0 +1,149 @@
+"""Materialised fp64 attention oracle — TEST INFRASTRUCTURE ONLY.
+
+Only tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline legs
+may import this module.  It never calls into the CUDA library.
+
+What it computes (one head ``(b, h)``, one query row ``i``):
+
+* scores ``s_ij = scale * sum_d q_id k_jd`` — the dense attention
+  ``softmax(Q K^T / sqrt(d)) V`` of "Kernel Fusion and the Memory Wall",
+  section "FlashAttention: avoid the full score matrix", with the caller's
+  ``scale`` in place of ``1/sqrt(d)``;
+* the valid key set ``V_i = {j : j < kv_len[b] and (not causal or j <= i)}``
+  (causal masking: "Kernel Fusion and the Memory Wall", the paragraph after
+  "A small executable reference"; per-sequence key lengths for the ragged,
+  padded batches of "Fused Multi-Head Attention", the continuous-batching
+  item);
+* the stable softmax over the WHOLE row ("Softmax needs a global row
+  statistic": the denominator must include every valid key):
+  ``M = max_{j in V_i} s_ij``, ``p_ij = exp(s_ij - M)``, ``L = sum_j p_ij``,
+  ``O_i = sum_j p_ij v_j / L`` and ``LSE_i = M + ln L`` (natural log, over the
+  scaled scores);
+* a row with no valid key ("Attention softmax fusion", section "Things that
+  break": a fully masked tile must not poison the result with NaN) has
+  ``O_i = +0.0`` in every column and ``LSE_i = -inf``.
+
+Readings where the pages are silent (each one is listed in the design doc):
+
+* causal alignment is top-left: key ``j`` is masked for query ``i`` when
+  ``j > i``, for any ``Sq`` and ``Sk``;
+* ``kv_lens`` entries are clamped to ``[0, Sk]``; ``None`` means ``Sk`` for
+  every batch entry; causal and key-length masks combine by AND on validity;
+* ``LSE`` uses the natural logarithm of the scaled scores.
+
+Implementation: float64 NumPy; query rows are processed in blocks of
+``block`` rows so that memory stays bounded at long sequence lengths; within a
+block each score row is materialised in full over all ``Sk`` keys (no online
+recurrence, no tiling over keys).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+def _as_f64(x) -> np.ndarray:
+    a = np.asarray(x)
+    if a.dtype != np.float64:
+        a = a.astype(np.float64)
+    return a
+
+
+def valid_key_count(i: int, Sk: int, causal: bool, kv_len: int) -> int:
+    """Number of valid keys of query row ``i``: ``|{j : j < kv_len, (not causal or j <= i)}|``.
+
+    ``kv_len`` is clamped to ``[0, Sk]`` first (reading of the pages' silence
+    on out-of-range key lengths)."""
+    lim = min(max(int(kv_len), 0), Sk)
+    if causal:
+        lim = min(lim, i + 1)
+    return max(lim, 0)
+
+
+def _head_rows(q_rows: np.ndarray, row_index: np.ndarray, k: np.ndarray, v: np.ndarray,
+               scale: float, causal: bool, kv_len: int):
+    """Exact attention for the query rows ``q_rows`` (their positions are
+    ``row_index``) against all keys ``k`` / values ``v`` of one head.
+
+    Returns ``(O [n, Dv] float64, LSE [n] float64)``."""
+    Sk = k.shape[0]
+    n = q_rows.shape[0]
+    Dv = v.shape[1]
+    out = np.zeros((n, Dv), dtype=np.float64)
+    lse = np.full((n,), -np.inf, dtype=np.float64)
+    if n == 0:
+        return out, lse
+    # s_ij = scale * <q_i, k_j>, one full row per query
+    s = (q_rows @ k.T) * np.float64(scale)
+    # validity: j < kv_len (clamped), and j <= i when causal
+    lim = np.full((n,), min(max(int(kv_len), 0), Sk), dtype=np.int64)
+    if causal:
+        lim = np.minimum(lim, row_index.astype(np.int64) + 1)
+    cols = np.arange(Sk, dtype=np.int64)
+    valid = cols[None, :] < lim[:, None]
+    has_key = lim > 0
+    if not np.any(has_key):
+        return out, lse
+    s = np.where(valid, s, -np.inf)
+    sv = s[has_key]
+    # stable softmax over the whole row: subtract the row maximum of the valid scores
+    m = np.max(sv, axis=1)
+    p = np.exp(sv - m[:, None])  # masked entries: exp(-inf) = 0
+    total = np.sum(p, axis=1)
+    out[has_key] = (p @ v) / total[:, None]
+    lse[has_key] = m + np.log(total)
+    return out, lse
+
+
+def attention_ref(q, k, v, scale: float, causal: bool = False, kv_lens=None, block: int = 256):
+    """Exact attention forward over a padded batch.
+
+    Arguments: ``q [B,H,Sq,D]``, ``k [B,H,Sk,D]``, ``v [B,H,Sk,Dv]`` (any real
+    dtype; widened to float64), ``scale`` (the caller's float, widened to
+    float64), ``causal`` (top-left aligned), ``kv_lens`` (``None`` or ``B``
+    integers, clamped to ``[0, Sk]``).
+
+    Returns ``(O [B,H,Sq,Dv], LSE [B,H,Sq])`` in float64; rows with no valid
+    key hold ``O = 0`` and ``LSE = -inf``."""
+    q = _as_f64(q)
+    k = _as_f64(k)
+    v = _as_f64(v)
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    assert k.shape[:2] == (B, H) and k.shape[3] == D
+    assert v.shape[:3] == (B, H, Sk)
+    Dv = v.shape[3]
+    if kv_lens is None:
+        kvl = [Sk] * B
+    else:
+        kvl = [int(x) for x in np.asarray(kv_lens).reshape(-1)]
+        assert len(kvl) == B
+    out = np.zeros((B, H, Sq, Dv), dtype=np.float64)
+    lse = np.full((B, H, Sq), -np.inf, dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            for r0 in range(0, Sq, block):
+                r1 = min(r0 + block, Sq)
+                rows = np.arange(r0, r1)
+                o_blk, l_blk = _head_rows(q[b, h, r0:r1], rows, k[b, h], v[b, h],
+                                          scale, causal, kvl[b])
+                out[b, h, r0:r1] = o_blk
+                lse[b, h, r0:r1] = l_blk
+    return out, lse
+
+
+def attention_rows(q_head, k_head, v_head, rows, scale: float, causal: bool = False,
+                   kv_len=None):
+    """Exact attention for selected query ``rows`` of ONE head.
+
+    ``q_head [Sq,D]``, ``k_head [Sk,D]``, ``v_head [Sk,Dv]``; ``rows`` is a
+    sequence of query positions; ``kv_len`` is that head's batch entry's key
+    length (``None`` = ``Sk``).  Returns ``(O [len(rows), Dv], LSE [len(rows)])``
+    in float64.  Used to check full-size outputs one sampled row at a time."""
+    q_head = _as_f64(q_head)
+    k_head = _as_f64(k_head)
+    v_head = _as_f64(v_head)
+    rows = np.asarray(rows, dtype=np.int64)
+    Sk = k_head.shape[0]
+    return _head_rows(q_head[rows], rows, k_head, v_head, scale, causal,
+                      Sk if kv_len is None else kv_len)
