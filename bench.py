@@ -1,0 +1,389 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward on GB300.
+
+``python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+[--workload NAME]`` prints ONE JSON line.
+
+A step is one ``attn_fwd`` call over the whole workload (default: B=2, H=16,
+Sq=Sk=8192, D=128, non-causal, bf16 N(0,1) inputs from seed 3).  ``value`` is
+whole-job TFLOP/s (4*B*H*Sq*Sk*D per step, halved when causal) with inputs
+resident in HBM; every step re-reads 192 MiB of Q/K/V (plus 64 MiB of O
+written), more than the 129 MB L2, so no explicit flush is needed.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (weak
+scaling: the attention units shard with no exchange step); the barrier and the
+max over ranks use torch.distributed, never the data path.
+
+``--impl reference`` times the CPU oracle (fp64, materialised softmax) on the
+host cores instead: each step is one 256-row query block of one head against
+all keys, cycling over the workload's blocks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor peak"
+FALLBACK_PEAK_TFLOPS = 1900.0
+KERNEL_SOURCES = ["exact_attention_86_gb300/csrc/attn_fwd.cu", "exact_attention_86_gb300/csrc/sm103_ptx.cuh"]
+TRAFFIC_FILE = "profiles/attn_fwd_kernel_s8192_d128_traffic.md"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source and this workload; else None."""
+    path = os.path.join(ROOT, TRAFFIC_FILE)
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    wl = re.search(r"workload:\s*(\S+)", text)
+    val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not (src and wl and val) or src.group(1) != kernel_source_hash() or wl.group(1) != workload:
+        return None
+    return float(val.group(1))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            rows.append((ts, parts))
+        window = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for _, p in window if num(p[1]) is not None]
+        mx = [num(p[2]) for _, p in window if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, p in window:
+            for name, val in zip(names, p[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(window),
+                "power_w_max": max((num(p[3]) or 0.0) for _, p in window)}
+
+
+def cpu_oracle_steps(w, q, k, v, kv, n_steps: int, budget_s: float | None):
+    """Runs the fp64 oracle on successive 256-row query blocks of head (0, 0).
+    Returns (flops, seconds, blocks)."""
+    import numpy as np
+    from oracle import attention_rows
+
+    qh = q[0, 0].float().numpy().astype(np.float64)
+    kh = k[0, 0].float().numpy().astype(np.float64)
+    vh = v[0, 0].float().numpy().astype(np.float64)
+    kvb = None if kv is None else int(kv[0])
+    n_blocks = (w.Sq + 255) // 256
+    flops = 0.0
+    t0 = time.perf_counter()
+    i = 0
+    while True:
+        blk = i % n_blocks
+        rows = list(range(blk * 256, min(w.Sq, blk * 256 + 256)))
+        attention_rows(qh, kh, vh, rows, w.scale, causal=w.causal, kv_len=kvb)
+        keys = w.Sk if kvb is None else min(max(kvb, 0), w.Sk)
+        for r in rows:
+            n = min(keys, r + 1) if w.causal else keys
+            flops += 4.0 * n * w.D
+        i += 1
+        el = time.perf_counter() - t0
+        if n_steps is not None and i >= n_steps:
+            break
+        if budget_s is not None and el >= budget_s:
+            break
+    return flops, time.perf_counter() - t0, i
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        n = [d.get("num_threads") for d in info if d.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def run_reference(args, w):
+    """The CPU oracle as the reference arm."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from exact_attention_86_gb300 import workloads
+    q, k, v, kv = workloads.generate(w)
+    cpu_oracle_steps(w, q, k, v, kv, n_steps=args.warmup, budget_s=None) if args.warmup > 0 else None
+    flops, secs, blocks = cpu_oracle_steps(w, q, k, v, kv, n_steps=args.steps, budget_s=None)
+    tflops = flops / secs / 1e12
+    sample = (f"{blocks} steps; each one 256-row query block of head (0,0) against all "
+              f"{w.Sk} keys, fp64 NumPy/BLAS")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / max(blocks, 1) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "shape": w.label(), "oracle": "fp64 materialised softmax (CPU)"},
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--draw", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    from exact_attention_86_gb300 import workloads
+    w = workloads.WORKLOADS[args.workload or workloads.HEADLINE]
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+    from exact_attention_86_gb300 import attn
+    from exact_attention_86_gb300.build import build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+
+    if rank == 0:
+        build()
+    if world > 1:
+        dist.barrier()
+    attn.lib()
+
+    q, k, v, kv = workloads.generate(w, args.draw)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    kvd = kv.to(dev) if kv is not None else None
+    o = torch.empty_like(qd)
+    lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    kv_ptr = kvd.data_ptr() if kvd is not None else None
+
+    def step():
+        st = attn.attn_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                           w.B, w.H, w.Sq, w.Sk, w.D, w.scale, int(w.causal), kv_ptr, sptr)
+        if st != attn.ATTN_OK:
+            raise attn.AttnError(st, "attn_fwd")
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    st, site = attn.attn_check_device_status(sptr)
+    if st != attn.ATTN_OK:
+        raise attn.AttnError(st, f"warm-up (site {site})")
+
+    # ---------------------------------------------------------- device-timed
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(max(args.warmup, 20)):
+        step()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_all0 = torch.cuda.Event(enable_timing=True)
+    t_all1 = torch.cuda.Event(enable_timing=True)
+    barrier()
+    wall0 = time.time()
+    t_all0.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    t_all1.record(stream)
+    barrier()
+    wall1 = time.time()
+    sampler.stop()
+    st, site = attn.attn_check_device_status(sptr)
+    if st != attn.ATTN_OK:
+        raise attn.AttnError(st, f"timed region (site {site})")
+    elapsed_ms = t_all0.elapsed_time(t_all1)
+    launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        t = torch.tensor([elapsed_ms, launch_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms, launch_ms = float(t[0]), float(t[1])
+    ms_per_step = elapsed_ms / args.steps
+    value = w.flops * world / (ms_per_step * 1e-3) / 1e12
+    clocks = sampler.summary(wall0, wall1)
+
+    # ------------------------------------------------------------ end to end
+    qh = q.pin_memory()
+    kh = k.pin_memory()
+    vh = v.pin_memory()
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        step()
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    h2d = (q.numel() + k.numel() + v.numel()) * 2
+    d2h = o.numel() * 2 + lse.numel() * 4
+
+    # -------------------------------------------------------------- roofline
+    peaks = measured_peaks()
+    if peaks and peaks.get("bf16_tflops"):
+        peak = float(peaks["bf16_tflops"])
+        peak_src = "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
+    else:
+        peak = FALLBACK_PEAK_TFLOPS
+        peak_src = "fallback (1.9 PFLOP/s bf16 burst)"
+    achieved = w.flops / (launch_ms * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": recorded_traffic(w.name), "kernel": "attn_fwd_kernel", "peak_source": peak_src,
+                "launch_ms": launch_ms, "algorithmic_flops_per_launch": w.flops,
+                "algorithmic_bytes_per_launch": w.min_bytes}
+
+    # ----------------------------------------------------------- CPU oracle
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        flops, secs, blocks = cpu_oracle_steps(w, q, k, v, kv, n_steps=None, budget_s=args.cpu_budget_s)
+        cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": f"{blocks} query blocks of 256 rows of head (0,0) against all {w.Sk} keys "
+                         f"({secs:.1f} s of fp64 NumPy/BLAS)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "shape": w.label(), "draw": args.draw,
+                       "inputs": f"bf16 N(0,{(w.std if args.draw == 0 else w.second_std) ** 2:g}) seed {w.seed}",
+                       "l2": "no flush: each step reads 192 MiB of Q/K/V and writes 64 MiB of O, more than the "
+                             "129 MB L2",
+                       "parallelism": f"weak: {world} replica(s) of the workload, one per GPU"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "clocks": clocks,
+            "gpu_launches": args.steps,
+            "pct_of_peak": 100.0 * value / world / peak,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,136 @@
+"""Python binding of the C-ABI attention library (argument marshalling only).
+
+The functions with the C names (``attn_fwd``, ``attn_get_error_string``,
+``attn_check_device_status``, ``attn_selftest_wait_timeout``,
+``attn_abi_version``) take raw device addresses and sizes exactly like
+``include/attn.h``.  ``forward`` is the torch-facing convenience: it checks
+dtypes / devices / contiguity, allocates ``o`` and ``lse`` with torch, and calls
+``attn_fwd`` on the current CUDA stream.  Every step of the computation runs in
+the library's CUDA kernel; there is no CPU fallback, and a missing library is
+an error.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional, Tuple
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libattn.so")
+_lib = None
+
+ATTN_OK = 0
+ATTN_ERR_NULLPTR = 1
+ATTN_ERR_ALIGN = 2
+ATTN_ERR_SHAPE = 3
+ATTN_ERR_UNSUPPORTED_D = 4
+ATTN_ERR_SCALE = 5
+ATTN_ERR_CUDA = 6
+ATTN_ERR_DEVICE_TIMEOUT = 7
+ATTN_ERR_UNSUPPORTED_DEVICE = 8
+
+#: Functions declared in include/attn.h, with their ctypes signatures.
+SIGNATURES = {
+    "attn_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "attn_get_error_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "attn_check_device_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
+    "attn_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
+    "attn_abi_version": (ctypes.c_int, []),
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {attn_get_error_string(status)} (status {status})" if what
+                         else f"{attn_get_error_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """Load ``libattn.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                               "`python -m exact_attention_86_gb300.build` (needs nvcc)")
+        handle = ctypes.CDLL(_LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+# ----------------------------------------------------------------- raw C ABI
+
+def attn_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
+             scale: float, causal: int, kv_lens: Optional[int], stream: Optional[int]) -> int:
+    return lib().attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, stream)
+
+
+def attn_get_error_string(status: int) -> str:
+    return lib().attn_get_error_string(status).decode()
+
+
+def attn_check_device_status(stream: Optional[int] = None) -> Tuple[int, int]:
+    site = ctypes.c_uint32(0)
+    st = lib().attn_check_device_status(stream, ctypes.byref(site))
+    return st, site.value
+
+
+def attn_selftest_wait_timeout(limit_ns: int, stream: Optional[int] = None) -> int:
+    return lib().attn_selftest_wait_timeout(limit_ns, stream)
+
+
+def attn_abi_version() -> int:
+    return lib().attn_abi_version()
+
+
+# -------------------------------------------------------------- torch facing
+
+def forward(q, k, v, scale: Optional[float] = None, causal: bool = False, kv_lens=None,
+            out=None, lse=None):
+    """Fused attention forward on torch CUDA tensors.
+
+    ``q [B,H,Sq,D]``, ``k``/``v [B,H,Sk,D]``: bf16, contiguous, same device.
+    ``kv_lens``: ``None`` or an int32 CUDA tensor ``[B]``.  ``scale`` defaults to
+    ``1/sqrt(D)``.  Returns ``(o bf16 [B,H,Sq,D], lse fp32 [B,H,Sq])``.  The call
+    is asynchronous on the current stream."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-d bf16 CUDA tensor")
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    if tuple(k.shape) != (B, H, Sk, D) or tuple(v.shape) != (B, H, Sk, D):
+        raise ValueError("k and v must be [B, H, Sk, D] with q's B, H, D")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on one device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    kv_ptr = None
+    if kv_lens is not None:
+        if kv_lens.dtype != torch.int32 or kv_lens.device != q.device or kv_lens.numel() != B \
+                or not kv_lens.is_contiguous():
+            raise ValueError("kv_lens must be a contiguous int32 tensor [B] on q's device")
+        kv_ptr = kv_lens.data_ptr()
+    if out is None:
+        out = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                      B, H, Sq, Sk, D, float(scale), int(bool(causal)), kv_ptr, stream)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+    return out, lse

@@ -1,0 +1,114 @@
+/*
+ * attn.h — C ABI of the GB300 (sm_103a) exact fused attention forward.
+ *
+ * The operation is dense exact attention with a per-row log-sum-exp:
+ *
+ *   O[b,h,i,:] = sum_j softmax_j( scale * <Q[b,h,i,:], K[b,h,j,:]> + mask[b,i,j] ) * V[b,h,j,:]
+ *   LSE[b,h,i] = ln sum_{j valid} exp( scale * <Q[b,h,i,:], K[b,h,j,:]> )
+ *
+ * as defined in "Kernel Fusion and the Memory Wall" (thegustafson.com), section
+ * "FlashAttention: avoid the full score matrix" (softmax(QK^T/sqrt(d))V, with
+ * the caller's `scale` in place of 1/sqrt(d)); the softmax is the stable,
+ * whole-row one of section "Softmax needs a global row statistic".  It is
+ * computed tile by tile with the online max/sum correction of "Attention
+ * softmax fusion" (roadmapper-2x4.pages.dev), section "The tile loop", so the
+ * Sq x Sk score and probability matrices never exist in device memory.
+ *
+ * The mask takes only the values 0 and -inf:
+ *   - key j is valid for query row i iff  j < kv_len[b]  and  (!causal || j <= i);
+ *     the causal mask is top-left aligned for any Sq, Sk;
+ *   - a row with no valid key (e.g. kv_len[b] == 0) yields O = +0.0 in every
+ *     column and LSE = -inf, never NaN ("Attention softmax fusion", section
+ *     "Things that break"; "Kernel Fusion and the Memory Wall", the paragraph on
+ *     causal kernels after "A small executable reference").
+ *
+ * All entry points are host functions; device pointers are plain CUDA device
+ * (or managed) addresses on the CURRENT device.  The caller allocates and owns
+ * every buffer.  The library allocates no device memory: its only device state
+ * is one status word per device, a static __device__ variable in the library.
+ */
+#ifndef EXACT_ATTENTION_86_GB300_ATTN_H
+#define EXACT_ATTENTION_86_GB300_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* attn_stream_t;
+
+typedef enum attn_status {
+  ATTN_OK = 0,
+  ATTN_ERR_NULLPTR = 1,            /* a required pointer is NULL                         */
+  ATTN_ERR_ALIGN = 2,              /* q/k/v/o not 16-byte aligned, lse/kv_lens not 4-byte */
+  ATTN_ERR_SHAPE = 3,              /* negative or too large B/H/Sq/Sk                   */
+  ATTN_ERR_UNSUPPORTED_D = 4,      /* D is not 64 or 128                                */
+  ATTN_ERR_SCALE = 5,              /* scale is NaN or infinite                          */
+  ATTN_ERR_CUDA = 6,               /* a CUDA runtime/driver call failed                 */
+  ATTN_ERR_DEVICE_TIMEOUT = 7,     /* a kernel wait gave up (see attn_check_device_status) */
+  ATTN_ERR_UNSUPPORTED_DEVICE = 8  /* the current device is not sm_103 (GB300)          */
+} attn_status;
+
+/*
+ * attn_fwd — fused attention forward, asynchronous on `stream`.
+ *
+ * q       bf16 [B, H, Sq, D], contiguous (D innermost), device, 16-byte aligned.
+ * k, v    bf16 [B, H, Sk, D], contiguous, device, 16-byte aligned.
+ * o       bf16 [B, H, Sq, D], contiguous, device, 16-byte aligned; written.
+ * lse     fp32 [B, H, Sq], contiguous, device, 4-byte aligned; written
+ *         (natural log over the scaled scores; -inf on rows with no valid key).
+ * B, H    batch and heads, >= 0.  Sq, Sk: query and key lengths, >= 0.
+ *         B*H*max(Sq,Sk)*D must stay below 2^31 elements per tensor dimension
+ *         set the TMA descriptor can address (checked: ATTN_ERR_SHAPE).
+ * D       head dimension: 64 or 128 (else ATTN_ERR_UNSUPPORTED_D).
+ * scale   multiplier of QK^T, any finite value (usually 1/sqrt(D)).
+ * causal  0 or non-zero.
+ * kv_lens NULL (every sequence has Sk keys) or device int32 [B]; entries are
+ *         clamped to [0, Sk].
+ *
+ * Sq == 0, B == 0 or H == 0: nothing to compute, returns ATTN_OK without a
+ * launch.  Sk == 0: every row has no valid key (O = 0, LSE = -inf).
+ *
+ * Errors: argument errors return before anything is launched.  A failed
+ * launch returns ATTN_ERR_CUDA.  The call never synchronises; a device-side
+ * wait that gave up (a kernel bug, never expected) is reported later by
+ * attn_check_device_status.  q/k/v must not overlap o/lse.
+ */
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
+                     int Sk, int D, float scale, int causal, const int32_t* kv_lens, attn_stream_t stream);
+
+/* Static, human-readable description of a status code. */
+const char* attn_get_error_string(attn_status status);
+
+/*
+ * attn_check_device_status — synchronises `stream`, then reads and clears the
+ * current device's status word.  Returns ATTN_ERR_DEVICE_TIMEOUT if any kernel
+ * of this library gave up on a bounded wait since the last check (the kernel
+ * then skipped the rest of its work and released its resources), ATTN_ERR_CUDA
+ * if the synchronisation failed, else ATTN_OK.  If `site` is not NULL it
+ * receives the code of the first wait that gave up (0 if none).
+ */
+attn_status attn_check_device_status(attn_stream_t stream, uint32_t* site);
+
+/*
+ * attn_selftest_wait_timeout — failure-detection self test.  Launches one
+ * 32-thread block that waits on a shared-memory mbarrier that nothing ever
+ * arrives on, with the same bounded wait the attention kernel uses but a limit
+ * of `limit_ns` nanoseconds (1 .. 2e9).  The wait gives up, sets the status
+ * word and the block exits normally; attn_check_device_status then returns
+ * ATTN_ERR_DEVICE_TIMEOUT.  No fault, trap or unbounded spin is involved.
+ */
+attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream);
+
+/* ABI version of this header (incremented on any signature change). */
+int attn_abi_version(void);
+
+#define ATTN_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_86_GB300_ATTN_H */

@@ -1,0 +1,117 @@
+"""CPU checks of the C-ABI library: it builds, loads without a GPU, exports every
+function include/attn.h declares, and its host-side argument checks return the
+documented codes before touching CUDA."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_86_gb300 import attn
+from exact_attention_86_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return attn.lib()
+
+
+def _declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(attn_[a-z0-9_]+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    assert {"attn_fwd", "attn_get_error_string", "attn_check_device_status",
+            "attn_selftest_wait_timeout", "attn_abi_version"} <= set(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert set(_declared_functions()) <= set(attn.SIGNATURES)
+
+
+def test_abi_version(lib):
+    src = open(os.path.join(ROOT, "include", "attn.h")).read()
+    ver = int(re.search(r"#define ATTN_ABI_VERSION (\d+)", src).group(1))
+    assert attn.attn_abi_version() == ver
+
+
+def test_error_strings(lib):
+    for code in range(9):
+        assert attn.attn_get_error_string(code) not in ("", "unknown status")
+    assert attn.attn_get_error_string(99) == "unknown status"
+
+
+A = 1 << 20  # a 16-byte-aligned dummy address: argument checks never dereference
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(D=96), attn.ATTN_ERR_UNSUPPORTED_D),
+    (dict(D=32), attn.ATTN_ERR_UNSUPPORTED_D),
+    (dict(B=-1), attn.ATTN_ERR_SHAPE),
+    (dict(Sq=-5), attn.ATTN_ERR_SHAPE),
+    (dict(Sk=-1), attn.ATTN_ERR_SHAPE),
+    (dict(scale=float("nan")), attn.ATTN_ERR_SCALE),
+    (dict(scale=float("inf")), attn.ATTN_ERR_SCALE),
+    (dict(q=0), attn.ATTN_ERR_NULLPTR),
+    (dict(o=0), attn.ATTN_ERR_NULLPTR),
+    (dict(lse=0), attn.ATTN_ERR_NULLPTR),
+    (dict(k=0), attn.ATTN_ERR_NULLPTR),
+    (dict(q=A + 8), attn.ATTN_ERR_ALIGN),
+    (dict(v=A + 2), attn.ATTN_ERR_ALIGN),
+    (dict(lse=A + 2), attn.ATTN_ERR_ALIGN),
+    (dict(kv=A + 1), attn.ATTN_ERR_ALIGN),
+    (dict(H=1 << 20, Sq=1 << 20, Sk=1 << 20), attn.ATTN_ERR_SHAPE),
+    (dict(B=0), attn.ATTN_OK),      # nothing to compute, no launch
+    (dict(Sq=0), attn.ATTN_OK),
+    (dict(H=0, q=0, o=0), attn.ATTN_OK),
+])
+def test_argument_checks(lib, args, code):
+    a = dict(q=A, k=A, v=A, o=A, lse=A, B=2, H=2, Sq=256, Sk=256, D=128, scale=0.088, causal=0, kv=None)
+    a.update(args)
+    st = attn.attn_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Sq"], a["Sk"], a["D"],
+                       a["scale"], a["causal"], a["kv"], None)
+    assert st == code
+
+
+def test_no_silent_success_without_gpu(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = attn.attn_fwd(A, A, A, A, A, 1, 1, 128, 128, 64, 0.125, 0, None, None)
+    assert st in (attn.ATTN_ERR_CUDA, attn.ATTN_ERR_UNSUPPORTED_DEVICE)
+    assert attn.attn_selftest_wait_timeout(1000, None) in (attn.ATTN_ERR_CUDA, attn.ATTN_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_selftest_limit_checked(lib):
+    assert attn.attn_selftest_wait_timeout(0, None) == attn.ATTN_ERR_SHAPE
+    assert attn.attn_selftest_wait_timeout(3_000_000_000, None) == attn.ATTN_ERR_SHAPE
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "exact_attention_86_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert not re.search(r"^\s*(from|import)\s+oracle", src, flags=re.M), fn
+                assert "oracle/" not in src, fn
+
+
+def test_missing_library_is_an_error(monkeypatch, tmp_path):
+    monkeypatch.setattr(attn, "_LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(attn, "_lib", None)
+    with pytest.raises(RuntimeError):
+        attn.lib()

@@ -1,0 +1,287 @@
+"""GPU parity: the sm_103a kernel (through the C ABI) against the fp64 oracle on
+the same seeded bf16 inputs.
+
+Small cases are compared element by element over the whole output; they span
+several 128-row tiles and a ragged tail.  The full-size workloads are run in
+exactly the launch configuration the benchmark times and compared on sampled
+rows that the oracle computes one by one, plus whole-output properties (no
+NaN, exact empty rows, determinism, no score-sized allocation)."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_86_gb300 import attn, workloads
+from exact_attention_86_gb300.build import build
+from oracle import attention_ref, attention_rows
+
+from parity import check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build()
+    attn.lib()
+    torch.cuda.init()
+
+
+def _run(q, k, v, scale, causal, kv_lens):
+    dev = torch.device("cuda:0")
+    qd, kd, vd = (t.to(dev).contiguous() for t in (q, k, v))
+    kvd = kv_lens.to(dev) if kv_lens is not None else None
+    o, lse = attn.forward(qd, kd, vd, scale=scale, causal=causal, kv_lens=kvd)
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, (st, site)
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _np(t):
+    return t.float().numpy().astype(np.float64)
+
+
+def _inputs(B, H, Sq, Sk, D, seed, std=1.0, kv=None):
+    g = torch.Generator().manual_seed(seed)
+    q = (torch.randn(B, H, Sq, D, generator=g) * std).to(torch.bfloat16)
+    k = (torch.randn(B, H, Sk, D, generator=g) * std).to(torch.bfloat16)
+    v = (torch.randn(B, H, Sk, D, generator=g) * std).to(torch.bfloat16)
+    kvt = None if kv is None else torch.tensor(kv, dtype=torch.int32)
+    return q, k, v, kvt
+
+
+def _full_check(q, k, v, scale, causal, kv_lens, what):
+    o, lse = _run(q, k, v, scale, causal, kv_lens)
+    o_ref, lse_ref = attention_ref(_np(q), _np(k), _np(v), scale, causal=causal,
+                                   kv_lens=None if kv_lens is None else kv_lens.numpy())
+    return check(o, lse, o_ref, lse_ref, what)
+
+
+# ---------------------------------------------------------------- small cases
+
+SMALL = [
+    # B, H, Sq, Sk, D, causal
+    (1, 2, 300, 300, 64, False),
+    (1, 2, 300, 300, 128, False),
+    (2, 1, 600, 600, 64, True),
+    (2, 1, 600, 600, 128, True),
+    (1, 1, 1, 1, 64, False),
+    (1, 1, 1, 1, 128, True),
+    (1, 2, 127, 129, 128, False),
+    (1, 2, 129, 127, 64, False),
+    (2, 3, 257, 385, 128, False),
+    (1, 1, 200, 700, 64, False),
+    (1, 1, 700, 200, 128, False),
+    (1, 2, 300, 520, 128, True),   # causal with Sq != Sk: top-left aligned
+    (1, 2, 520, 300, 64, True),
+    (1, 1, 4097, 130, 64, False),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "B{}H{}q{}k{}d{}{}".format(*s[:5], "c" if s[5] else ""))
+def test_small_shapes(shape):
+    B, H, Sq, Sk, D, causal = shape
+    q, k, v, _ = _inputs(B, H, Sq, Sk, D, seed=(B * 131 + H * 71 + Sq * 7 + Sk * 13 + D + int(causal)) % 997)
+    _full_check(q, k, v, 1.0 / math.sqrt(D), causal, None, str(shape))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_kv_lens_edges(D, causal):
+    Sk = 400
+    kv = [0, 1, 127, 128, 129, Sk, 255, 257]
+    q, k, v, kvt = _inputs(len(kv), 2, 384, Sk, D, seed=7 + D, kv=kv)
+    _full_check(q, k, v, 1.0 / math.sqrt(D), causal, kvt, f"kv edges D{D} causal{causal}")
+
+
+def test_kv_lens_out_of_range_are_clamped():
+    q, k, v, kvt = _inputs(3, 1, 256, 300, 128, seed=3, kv=[-7, 1000, 300])
+    o, lse = _run(q, k, v, 0.1, False, kvt)
+    o_ref, lse_ref = attention_ref(_np(q), _np(k), _np(v), 0.1, kv_lens=[0, 300, 300])
+    check(o, lse, o_ref, lse_ref, "clamped kv_lens")
+
+
+@pytest.mark.parametrize("std", [2.0, 4.0])
+@pytest.mark.parametrize("causal", [False, True])
+def test_large_scores_stress_rescale(std, causal):
+    # Scores with std ~ std^2 * sqrt(D) * scale: the running max moves often.
+    q, k, v, _ = _inputs(1, 2, 512, 1024, 128, seed=11, std=std)
+    _full_check(q, k, v, 1.0 / math.sqrt(128), causal, None, f"std {std}")
+
+
+def test_increasing_scores_force_rescale_every_tile():
+    # Keys grow along the sequence so that every K tile raises the row max by
+    # more than the lazy-rescale threshold.
+    B, H, S, D = 1, 1, 256, 64
+    g = torch.Generator().manual_seed(5)
+    q = torch.ones(B, H, S, D)
+    k = torch.linspace(0, 1, S).view(1, 1, S, 1).expand(B, H, S, D) * 0.5 + torch.randn(B, H, S, D, generator=g) * 0.01
+    v = torch.randn(B, H, S, D, generator=g)
+    q, k, v = (t.to(torch.bfloat16).contiguous() for t in (q, k, v))
+    _full_check(q, k, v, 2.0, False, None, "rescale every tile")
+    _full_check(q, k, v, 2.0, True, None, "rescale every tile, causal")
+
+
+@pytest.mark.parametrize("scale", [-0.125, 0.0, 1e-3, 0.5])
+def test_scale_values(scale):
+    q, k, v, _ = _inputs(1, 2, 300, 300, 64, seed=21)
+    _full_check(q, k, v, scale, True, None, f"scale {scale}")
+
+
+def test_no_keys_at_all():
+    q, k, v, _ = _inputs(2, 2, 200, 1, 128, seed=1)
+    k = k[:, :, :0].contiguous()
+    v = v[:, :, :0].contiguous()
+    dev = torch.device("cuda:0")
+    o, lse = attn.forward(q.to(dev), torch.empty(2, 2, 0, 128, dtype=torch.bfloat16, device=dev),
+                          torch.empty(2, 2, 0, 128, dtype=torch.bfloat16, device=dev))
+    torch.cuda.synchronize()
+    assert torch.all(o == 0) and not torch.any(torch.signbit(o.float()))
+    assert torch.all(lse == float("-inf"))
+
+
+def test_empty_query_is_a_no_op():
+    dev = torch.device("cuda:0")
+    q = torch.empty(1, 1, 0, 64, dtype=torch.bfloat16, device=dev)
+    k = torch.randn(1, 1, 16, 64, device=dev).to(torch.bfloat16)
+    o, lse = attn.forward(q, k, k)
+    torch.cuda.synchronize()
+    assert o.numel() == 0 and lse.numel() == 0
+
+
+def test_output_guard_bands_untouched():
+    # Canary words around O and LSE catch out-of-bounds writes.
+    B, H, Sq, Sk, D = 2, 3, 300, 333, 128
+    q, k, v, kvt = _inputs(B, H, Sq, Sk, D, seed=9, kv=[333, 100])
+    dev = torch.device("cuda:0")
+    pad = 4096
+    o_buf = torch.full((2 * pad + B * H * Sq * D,), 12345, dtype=torch.int16, device=dev)
+    l_buf = torch.full((2 * pad + B * H * Sq,), 7.25, dtype=torch.float32, device=dev)
+    o_view = o_buf[pad:pad + B * H * Sq * D].view(torch.bfloat16).view(B, H, Sq, D)
+    l_view = l_buf[pad:pad + B * H * Sq].view(B, H, Sq)
+    attn.forward(q.to(dev), k.to(dev), v.to(dev), causal=True, kv_lens=kvt.to(dev), out=o_view, lse=l_view)
+    torch.cuda.synchronize()
+    assert torch.all(o_buf[:pad] == 12345) and torch.all(o_buf[-pad:] == 12345)
+    assert torch.all(l_buf[:pad] == 7.25) and torch.all(l_buf[-pad:] == 7.25)
+    o_ref, lse_ref = attention_ref(_np(q), _np(k), _np(v), 1 / math.sqrt(D), causal=True, kv_lens=[333, 100])
+    check(o_view.float().cpu().numpy(), l_view.cpu().numpy(), o_ref, lse_ref, "guard bands")
+
+
+def test_deterministic():
+    q, k, v, _ = _inputs(2, 4, 1000, 1000, 128, seed=13)
+    dev = torch.device("cuda:0")
+    a = attn.forward(q.to(dev), k.to(dev), v.to(dev), causal=True)
+    b = attn.forward(q.to(dev), k.to(dev), v.to(dev), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
+
+
+def test_wait_timeout_selftest_reports_and_recovers():
+    stream = torch.cuda.current_stream().cuda_stream
+    assert attn.attn_check_device_status(stream)[0] == attn.ATTN_OK
+    assert attn.attn_selftest_wait_timeout(1_000_000, stream) == attn.ATTN_OK
+    st, site = attn.attn_check_device_status(stream)
+    assert st == attn.ATTN_ERR_DEVICE_TIMEOUT and site == 8
+    assert attn.attn_check_device_status(stream)[0] == attn.ATTN_OK  # cleared
+    # the context is still healthy: a normal call works and matches the oracle
+    q, k, v, _ = _inputs(1, 1, 130, 130, 64, seed=2)
+    _full_check(q, k, v, 0.125, False, None, "after selftest")
+
+
+# ------------------------------------------------------ the five workloads
+
+def _device_inputs(w, draw=0):
+    q, k, v, kv = workloads.generate(w, draw)
+    dev = torch.device("cuda:0")
+    return q, k, v, kv, q.to(dev), k.to(dev), v.to(dev), (kv.to(dev) if kv is not None else None)
+
+
+def _sample_rows(Sq, rng, n):
+    fixed = [0, 1, 127, 128, 129, 255, 256, Sq // 2, Sq - 129, Sq - 128, Sq - 2, Sq - 1]
+    rows = set(r for r in fixed if 0 <= r < Sq)
+    rows.update(int(x) for x in rng.integers(0, Sq, size=n))
+    return sorted(rows)
+
+
+def _sampled_check(w, draw, heads, n_rows):
+    q, k, v, kv, qd, kd, vd, kvd = _device_inputs(w, draw)
+    o, lse = attn.forward(qd, kd, vd, scale=w.scale, causal=w.causal, kv_lens=kvd)
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, (st, site)
+    assert not torch.any(torch.isnan(o)) and not torch.any(torch.isnan(lse))
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    rng = np.random.default_rng(w.seed)
+    for (b, h) in heads:
+        rows = _sample_rows(w.Sq, rng, n_rows)
+        kvb = None if kv is None else int(kv[b])
+        o_ref, l_ref = attention_rows(_np(q[b, h]), _np(k[b, h]), _np(v[b, h]), rows, w.scale,
+                                      causal=w.causal, kv_len=kvb)
+        check(o[b, h, rows], lse[b, h, rows], o_ref, l_ref, f"{w.name} draw{draw} b{b} h{h}")
+    return o, lse, kv
+
+
+def test_workload_s128_d64_full():
+    w = workloads.WORKLOADS["s128_d64"]
+    q, k, v, kv = workloads.generate(w)
+    _full_check(q, k, v, w.scale, w.causal, kv, w.name)
+
+
+def test_workload_s1024_d64_causal_full():
+    w = workloads.WORKLOADS["s1024_d64_causal"]
+    q, k, v, kv = workloads.generate(w)
+    _full_check(q, k, v, w.scale, w.causal, kv, w.name)
+
+
+def test_workload_s2048_d128_padded():
+    w = workloads.WORKLOADS["s2048_d128_padded"]
+    q, k, v, kv = workloads.generate(w)
+    assert int(kv[w.kv_zero_index]) == 0
+    dev = torch.device("cuda:0")
+    o, lse = attn.forward(q.to(dev), k.to(dev), v.to(dev), scale=w.scale, causal=w.causal, kv_lens=kv.to(dev))
+    torch.cuda.synchronize()
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
+    # every batch entry (all key lengths), two heads each, every row
+    for b in range(w.B):
+        for h in (0, w.H - 1):
+            o_ref, l_ref = attention_ref(_np(q[b:b + 1, h:h + 1]), _np(k[b:b + 1, h:h + 1]),
+                                         _np(v[b:b + 1, h:h + 1]), w.scale, kv_lens=[int(kv[b])])
+            check(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], o_ref, l_ref, f"{w.name} b{b} h{h}")
+    # the sequence with kv_len = 0: every head exactly O = 0, LSE = -inf
+    z = w.kv_zero_index
+    assert np.all(o[z] == 0.0) and np.all(lse[z] == -np.inf)
+
+
+@pytest.mark.parametrize("name", ["s8192_d128", "s8192_d128_causal"])
+@pytest.mark.parametrize("draw", [0, 1])
+def test_workload_s8192_sampled(name, draw):
+    w = workloads.WORKLOADS[name]
+    _sampled_check(w, draw, heads=[(0, 0), (1, 7), (1, w.H - 1)], n_rows=40)
+
+
+def test_workload_s32768_causal_sampled_and_memory():
+    w = workloads.WORKLOADS["s32768_d128_causal"]
+    q, k, v, kv, qd, kd, vd, kvd = _device_inputs(w)
+    o = torch.empty_like(qd)
+    lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=qd.device)
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    alloc_before = torch.cuda.max_memory_allocated()
+    attn.forward(qd, kd, vd, scale=w.scale, causal=True, out=o, lse=lse)
+    torch.cuda.synchronize()
+    free_after = torch.cuda.mem_get_info()[0]
+    # no allocation anywhere near one head's score matrix (2 GiB in bf16)
+    assert torch.cuda.max_memory_allocated() == alloc_before
+    assert free_before - free_after < (64 << 20)
+    on = o.float().cpu().numpy()
+    ln = lse.cpu().numpy()
+    assert np.all(np.isfinite(on)) and np.all(np.isfinite(ln))
+    rng = np.random.default_rng(4)
+    for h in (0, 3, 7):
+        rows = _sample_rows(w.Sq, rng, 24)
+        o_ref, l_ref = attention_rows(_np(q[0, h]), _np(k[0, h]), _np(v[0, h]), rows, w.scale, causal=True)
+        check(on[0, h, rows], ln[0, h, rows], o_ref, l_ref, f"{w.name} h{h}")
