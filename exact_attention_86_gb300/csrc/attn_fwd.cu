@@ -10,11 +10,16 @@
 // row maximum (same section, second paragraph).  Nothing of size Sq x Sk is ever
 // written to device memory.
 //
-// CTA layout (320 threads, persistent over work units):
+// CTA layout (384 threads, persistent over work units):
 //   warps 0-3  softmax warpgroup 0: rows 0-127 of the unit (one thread per row)
 //   warps 4-7  softmax warpgroup 1: rows 128-255
 //   warp 8     TMA producer (one elected lane)
 //   warp 9     TMEM owner and tcgen05.mma issuer (one elected lane)
+//   warps 10-11 idle (they complete warpgroup 2 for the register split)
+// The block launches with 168 registers per thread; warpgroup 2 gives most of
+// its registers back (48 each) and the softmax warpgroups take 224 each, so a
+// whole 128-column score row stays in registers:
+//   launch 384 x 168 = 64512 >= 256 x 224 + 128 x 48 = 63488.
 //
 // Tensor Memory (512 columns x 128 lanes, fp32):
 //   [  0,128)  S0: scores of Q tile 0 vs the current K tile; its first 64
@@ -52,7 +57,9 @@ constexpr int kBQ = 128;          // query rows per Q tile (MMA M, TMEM lanes)
 constexpr int kBK = 128;          // keys per K/V tile (MMA N of QK^T)
 constexpr int kQT = 2;            // Q tiles per work unit, sharing each K/V tile
 constexpr int kUnitRows = kQT * kBQ;
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kRegsSoftmax = 192;
+constexpr int kRegsOther = 120;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpMma = 9;
 constexpr float kTau = 8.0f;      // lazy rescale threshold (log2 units)
@@ -236,6 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl.tmem_base;
   const uint64_t limit = p.wait_limit_ns;
 
+  if (warp >= 8) {
+    // ------------------------------------------- warpgroup 2: TMA and MMA
+    regs_decrease<kRegsOther>();
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
@@ -285,11 +295,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       uint32_t ring = 0, qcount = 0;
-      uint32_t pcount[2] = {0u, 0u};
+      uint32_t pcount0 = 0u, pcount1 = 0u;
       bool ok = true;
-      const uint32_t bar_s_full[2] = {smem_addr(&ctl.s_full[0]), smem_addr(&ctl.s_full[1])};
-      const uint32_t bar_p_full[2] = {smem_addr(&ctl.p_full[0]), smem_addr(&ctl.p_full[1])};
-      const uint32_t bar_o_full[2] = {smem_addr(&ctl.o_full[0]), smem_addr(&ctl.o_full[1])};
+      // barrier of Q tile i = barrier of tile 0 + 8 * i (consecutive uint64_t)
+      const uint32_t bar_s_full0 = smem_addr(&ctl.s_full[0]);
+      const uint32_t bar_p_full0 = smem_addr(&ctl.p_full[0]);
+      const uint32_t bar_o_full0 = smem_addr(&ctl.o_full[0]);
 
       // S_i = Q_i K^T: both operands K-major, 128-B swizzled; one MMA per 16 columns of D.
       auto issue_qk = [&](int i, uint32_t slot) {
@@ -331,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
           if (u.n[i] > 0) {
             issue_qk(i, ring % G::kSlots);
-            mma_commit(bar_s_full[i]);
+            mma_commit(bar_s_full0 + 8 * i);
           }
         }
         mma_commit(bar_kv_empty0 + 8 * (ring % G::kSlots));
@@ -342,8 +353,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool kn_ready = false;
           for (int i = 0; i < 2; ++i) {
             if (j >= u.n[i]) continue;
-            if (!wait_phase(bar_p_full[i], pcount[i] & 1u, abort_flag, kSitePFull, limit)) { ok = false; break; }
-            ++pcount[i];
+            uint32_t& pc = i ? pcount1 : pcount0;
+            if (!wait_phase(bar_p_full0 + 8 * i, pc & 1u, abort_flag, kSitePFull, limit)) { ok = false; break; }
+            ++pc;
             tc_fence_after_sync();
             issue_pv(i, v_pos % G::kSlots, j > 0);
             if (j + 1 < u.n[i]) {
@@ -352,9 +364,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kn_ready = true;
               }
               issue_qk(i, kn_pos % G::kSlots);
-              mma_commit(bar_s_full[i]);
+              mma_commit(bar_s_full0 + 8 * i);
             } else {
-              mma_commit(bar_o_full[i]);
+              mma_commit(bar_o_full0 + 8 * i);
             }
           }
           if (!ok) break;
@@ -372,8 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+  }
   } else {
-    // -------------------------------------------------------------- softmax
+    // ------------------------------------------- warpgroups 0, 1: softmax
+    regs_increase<kRegsSoftmax>();
     const int wg = warp >> 2;                      // which Q tile of the unit
     const int r = threadIdx.x & (kBQ - 1);         // row within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -392,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tile_row0 >= p.Sq) continue;
       const int row = tile_row0 + r;
       const size_t row_index = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq) + row;
-      const int n = u.n[wg];
+      const int n = wg ? u.n[1] : u.n[0];
       if (n == 0) {  // no valid key for any row of this tile: O = 0, LSE = -inf
         if (row < p.Sq) {
           uint4* dst = reinterpret_cast<uint4*>(p.o + row_index * D);
@@ -420,22 +434,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         int climit = u.kv - k0;  // columns >= climit are masked for this row
         if (CAUSAL) climit = min(climit, row - k0 + 1);
 
-        // row maximum of the valid raw scores (8 independent chains)
+        // row maximum of the valid raw scores (8 independent chains of 3-input max)
         float mx8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
         if (masked) {
 #pragma unroll
-          for (int col = 0; col < kBK; ++col) {
-            const float x = (col < climit) ? u2f(s[col >> 5][col & 31]) : -INFINITY;
-            mx8[col & 7] = fmaxf(mx8[col & 7], x);
+          for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
+#pragma unroll
+          for (int col = 0; col < kBK; col += 2) {
+            const float x0 = (col < climit) ? u2f(s[col >> 5][col & 31]) : -INFINITY;
+            const float x1 = (col + 1 < climit) ? u2f(s[col >> 5][(col + 1) & 31]) : -INFINITY;
+            mx8[(col >> 1) & 7] = max3(mx8[(col >> 1) & 7], x0, x1);
           }
         } else {
 #pragma unroll
-          for (int col = 0; col < kBK; ++col) mx8[col & 7] = fmaxf(mx8[col & 7], u2f(s[col >> 5][col & 31]));
+          for (int e = 0; e < 8; ++e) mx8[e] = u2f(s[0][e]);
+#pragma unroll
+          for (int col = 8; col < kBK; col += 2)
+            mx8[(col >> 1) & 7] = max3(mx8[(col >> 1) & 7], u2f(s[col >> 5][col & 31]), u2f(s[col >> 5][(col + 1) & 31]));
         }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+        const float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
         const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
         const float m_new = fmaxf(m_used, m_tile);
         // Lazy correction: move the reference max only when it grew by more than
@@ -446,38 +463,58 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
           m_used = m_new;
         }
+        // p = 2^(s*c - mb) on pairs (one packed FMA per pair), packed row sum,
+        // bf16 pairs written back over the first half of the S columns in
+        // 16-column chunks.
+        const float mb = (m_used == -INFINITY) ? 0.0f : m_used;
+        const uint64_t c2 = f2_pack(c, c);
+        const uint64_t nmb2 = f2_pack(-mb, -mb);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int col = q * 32 + 2 * e;
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(u2f(s[q][2 * e]), u2f(s[q][2 * e + 1])), c2, nmb2), x0, x1);
+            float p0 = ex2_approx(x0);
+            float p1 = ex2_approx(x1);
+            if (masked) {
+              p0 = (col < climit) ? p0 : 0.0f;
+              p1 = (col + 1 < climit) ? p1 : 0.0f;
+            }
+            acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+          tmem_st_32x32b_x16(tS + q * 16, pk);
+        }
+        {
+          const uint64_t a01 = f2_add(acc[0], acc[1]);
+          const uint64_t a23 = f2_add(acc[2], acc[3]);
+          float lo, hi;
+          f2_unpack(f2_add(a01, a23), lo, hi);
+          l += lo + hi;
+        }
         if (j > 0 && __any_sync(0xffffffffu, grow)) {
-          // O_i row *= alpha (PV of tile j-1 has retired: S_i(j) was committed after it)
+          // O_i row *= alpha (PV of tile j-1 has retired: S_i(j) was committed after it).
+          // Done after P is written so that the score row is no longer live.
+          const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
           for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];
             tmem_ld_32x32b_x32(tO + q * 32, o);
             tmem_ld_wait_x32(o);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(u2f(o[e]) * alpha);
+            for (int e = 0; e < 16; ++e) {
+              float lo, hi;
+              f2_unpack(f2_mul(f2_pack(u2f(o[2 * e]), u2f(o[2 * e + 1])), a2), lo, hi);
+              o[2 * e] = __float_as_uint(lo);
+              o[2 * e + 1] = __float_as_uint(hi);
+            }
             tmem_st_32x32b_x32(tO + q * 32, o);
           }
         }
-        const float mb = (m_used == -INFINITY) ? 0.0f : m_used;
-        float sum8[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sum8[e] = 0.0f;
-        uint32_t pk[2][32];
-#pragma unroll
-        for (int col = 0; col < kBK; col += 2) {
-          float p0 = ex2_approx(fmaf(u2f(s[col >> 5][col & 31]), c, -mb));
-          float p1 = ex2_approx(fmaf(u2f(s[(col + 1) >> 5][(col + 1) & 31]), c, -mb));
-          if (masked) {
-            p0 = (col < climit) ? p0 : 0.0f;
-            p1 = (col + 1 < climit) ? p1 : 0.0f;
-          }
-          sum8[col & 7] += p0;
-          sum8[(col + 1) & 7] += p1;
-          pk[col >> 6][(col >> 1) & 31] = pack_bf16x2(p0, p1);
-        }
-        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        tmem_st_32x32b_x32(tS, pk[0]);
-        tmem_st_32x32b_x32(tS + 32, pk[1]);
         tmem_st_wait();
         tc_fence_before_sync();
         mbar_arrive(bar_p);
