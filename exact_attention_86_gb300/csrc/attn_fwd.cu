@@ -16,10 +16,11 @@
 //   warp 8     TMA producer (one elected lane)
 //   warp 9     TMEM owner and tcgen05.mma issuer (one elected lane)
 //   warps 10-11 idle (they complete warpgroup 2 for the register split)
-// The block launches with 168 registers per thread; warpgroup 2 gives most of
-// its registers back (48 each) and the softmax warpgroups take 224 each, so a
-// whole 128-column score row stays in registers:
-//   launch 384 x 168 = 64512 >= 256 x 224 + 128 x 48 = 63488.
+// The block launches with 168 registers per thread; warpgroup 2 gives registers
+// back (120 each) and the softmax warpgroups take 192 each, so a whole
+// 128-column score row stays in registers without spills:
+//   launch 384 x 168 = 64512 = 256 x 192 + 128 x 120;
+//   per SM sub-partition (one warp of each warpgroup): (192+192+120) x 32 <= 16384.
 //
 // Tensor Memory (512 columns x 128 lanes, fp32):
 //   [  0,128)  S0: scores of Q tile 0 vs the current K tile; its first 64
