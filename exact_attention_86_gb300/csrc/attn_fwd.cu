@@ -2,37 +2,32 @@
 //
 // Computes O = softmax(scale * Q K^T + mask) V and LSE = ln(sum_j exp(scale * q.k_j))
 // for a padded batch [B, H, S, D] of bf16 tensors ("Kernel Fusion and the Memory
-// Wall", section "FlashAttention: avoid the full score matrix").  Each CTA owns a
-// block of 2 x 128 query rows at a time and streams the K/V tiles of that head
-// past them ("Attention softmax fusion", section "The tile loop"); the score
-// tile lives only in Tensor Memory and registers, and the running max / sum /
-// numerator are corrected by exp(m_old - m_new) whenever a later tile raises the
-// row maximum (same section, second paragraph).  Nothing of size Sq x Sk is ever
-// written to device memory.
+// Wall", section "FlashAttention: avoid the full score matrix").  Each CTA owns
+// one block of 128 query rows at a time and streams the K/V tiles of that head
+// past it ("Attention softmax fusion", section "The tile loop"); the score tile
+// lives only in Tensor Memory and registers, and the running max / sum /
+// numerator are corrected by exp(m_old - m_new) whenever a later tile raises
+// the row maximum (same section, second paragraph).  Nothing of size Sq x Sk is
+// ever written to device memory.
 //
 // CTA layout (384 threads, persistent over work units):
-//   warps 0-3  softmax warpgroup 0: rows 0-127 of the unit (one thread per row)
-//   warps 4-7  softmax warpgroup 1: rows 128-255
-//   warp 8     TMA producer (one elected lane)
-//   warp 9     TMEM owner and tcgen05.mma issuer (one elected lane)
-//   warps 10-11 idle (they complete warpgroup 2 for the register split)
-// The block launches with 168 registers per thread; warpgroup 2 gives registers
-// back (120 each) and the softmax warpgroups take 192 each, so a whole
-// 128-column score row stays in registers without spills:
-//   launch 384 x 168 = 64512 = 256 x 192 + 128 x 120;
-//   per SM sub-partition (one warp of each warpgroup): (192+192+120) x 32 <= 16384.
+//   warps 0-3  softmax, columns 0-63 of every score tile (one thread per row)
+//   warps 4-7  softmax, columns 64-127 (the partner thread of the same row)
+//   warp 8     TMA producer (one lane)
+//   warp 9     TMEM owner; issues S = Q K^T (whole warp, one elected lane)
+//   warp 10    issues O += P V (whole warp, one elected lane)
+//   warp 11    idle
 //
-// Tensor Memory (512 columns x 128 lanes, fp32):
-//   [  0,128)  S0: scores of Q tile 0 vs the current K tile; its first 64
-//              columns are overwritten by P0 (bf16 pairs) once softmax is done
-//   [128,256)  S1 / P1 for Q tile 1
-//   [256,256+D)     O0 accumulator,  [256+D,256+2D) O1 accumulator
-//
-// Per K/V tile j the MMA lane issues, in this order,
-//   O0 += P0(j) V_j ; S0 = Q0 K_{j+1}^T ; O1 += P1(j) V_j ; S1 = Q1 K_{j+1}^T
-// so that softmax of one Q tile overlaps the tensor-core work of the other.
-// tcgen05.mma operations issued by one thread execute in order, so the QK^T of
-// tile j+1 may overwrite the columns that the preceding PV of tile j reads.
+// Tensor Memory (512 columns x 128 lanes, lane = query row):
+//   [  0,128)  S buffer 0      [128,256)  S buffer 1     (fp32 scores)
+//   [256,320)  P buffer 0      [320,384)  P buffer 1     (bf16 pairs)
+//   [384,384+D) O accumulator (fp32)
+// With two S buffers the QK^T of tile j+1 runs while the softmax of tile j
+// works, and with P apart from S the PV of tile j runs while QK^T proceeds:
+// the two issuing warps each feed one independent stream of MMAs.  One warp
+// issues a 128x128x16 MMA no faster than about one per 110 cycles (measured),
+// more than the 64 cycles the tensor core needs for it, so both streams must
+// be in flight to keep the tensor pipe busy.
 //
 // Every mbarrier wait is bounded (global timer); a wait that gives up records
 // the site in a device status word, raises a CTA-wide abort flag, and every
@@ -54,15 +49,13 @@ using namespace attn_sm103;
 
 namespace {
 
-constexpr int kBQ = 128;          // query rows per Q tile (MMA M, TMEM lanes)
+constexpr int kBQ = 128;          // query rows per work unit (MMA M, TMEM lanes)
 constexpr int kBK = 128;          // keys per K/V tile (MMA N of QK^T)
-constexpr int kQT = 2;            // Q tiles per work unit, sharing each K/V tile
-constexpr int kUnitRows = kQT * kBQ;
 constexpr int kThreads = 384;
-constexpr int kRegsSoftmax = 192;
-constexpr int kRegsOther = 120;
+constexpr int kSoftmaxWarps = 8;
 constexpr int kWarpLoad = 8;
-constexpr int kWarpMma = 9;
+constexpr int kWarpQK = 9;
+constexpr int kWarpPV = 10;
 constexpr float kTau = 8.0f;      // lazy rescale threshold (log2 units)
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
@@ -77,6 +70,9 @@ enum WaitSite : uint32_t {
   kSiteSFull = 6,
   kSiteOFull = 7,
   kSiteSelftest = 8,
+  kSiteSFree = 9,
+  kSitePFree = 10,
+  kSiteExchange = 11,
 };
 
 // [0]: 1 once any wait gave up; [1]: site of the first one; [2]: its block.
@@ -88,31 +84,43 @@ struct Geo {
   static constexpr int kTileBytes = 128 * D * 2;     // one Q, K or V tile (128 rows)
   static constexpr int kChunkBytes = 128 * 128;      // 128 rows x 64 bf16 (one 128-B swizzle column)
   static constexpr int kChunks = D / 64;
-  static constexpr int kSlots = (D == 128) ? 4 : 8;  // K/V ring depth (tiles)
-  static __host__ __device__ constexpr uint32_t tmem_s(int i) { return 128u * i; }
-  static __host__ __device__ constexpr uint32_t tmem_o(int i) { return 256u + D * i; }
+  static constexpr int kSlots = (D == 128) ? 5 : 12; // K/V ring depth (tiles)
+  static constexpr uint32_t kTmemS = 0;              // + 128 * buffer
+  static constexpr uint32_t kTmemP = 256;            // + 64 * buffer
+  static constexpr uint32_t kTmemO = 384;
   static constexpr int kTmemCols = 512;
-  static constexpr int kOffQ = 1024;                 // after the control block
-  static constexpr int kOffRing = kOffQ + kQT * kTileBytes;
+  static constexpr int kOffQ = 4096;                 // after control block and exchange buffers
+  static constexpr int kOffRing = kOffQ + kTileBytes;
   static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes + 1024;  // + alignment slack
 };
 
 struct Ctrl {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[8], kv_empty[8];
-  uint64_t s_full[2], p_full[2], o_full[2];
-  uint64_t drain;
+  uint64_t kv_full[12], kv_empty[12];
+  uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
+  uint64_t x_bar[2];       // row-max exchange between the two softmax halves, by tile parity
+  uint64_t e_bar;          // row-sum exchange in the epilogue
+  uint64_t o_full;
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(Ctrl) <= 1024, "control block");
+
+// Exchange buffers (shared memory, after the control block at +1024):
+//   xmax[2][2][128] fp32 (tile parity, half, row), then xsum[2][128].
+struct Xchg {
+  float xmax[2][2][kBQ];
+  float xsum[2][kBQ];
+};
+static_assert(sizeof(Xchg) <= 3072, "exchange buffers");
 
 struct Params {
   uint16_t* o;
   float* lse;
   const int32_t* kv_lens;
   int B, H, Sq, Sk;
-  int n_qpairs;
+  int n_qtiles;
   int total_units;
   float c;                 // |scale| * log2(e)
   uint32_t idesc_qk;       // negate-A set when scale < 0
@@ -123,38 +131,30 @@ struct Params {
 struct Unit {
   int b, h, q0;
   int kv;                  // valid keys of this batch entry (kv_lens clamped to [0, Sk])
-  int n[2];                // K tiles each Q tile needs (0: tile absent or no valid key)
+  int n;                   // K tiles the unit needs (0: no valid key for any row)
 };
 
 template <bool CAUSAL>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int t) {
   Unit u;
   const int bh_count = p.B * p.H;
-  int qp, bh;
+  int qt, bh;
   if (CAUSAL) {  // longest units first: query blocks from the end of the sequence
-    qp = p.n_qpairs - 1 - t / bh_count;
+    qt = p.n_qtiles - 1 - t / bh_count;
     bh = t % bh_count;
   } else {       // consecutive units share a head, so its K/V stay hot in L2
-    qp = t % p.n_qpairs;
-    bh = t / p.n_qpairs;
+    qt = t % p.n_qtiles;
+    bh = t / p.n_qtiles;
   }
   u.b = bh / p.H;
   u.h = bh % p.H;
-  u.q0 = qp * kUnitRows;
+  u.q0 = qt * kBQ;
   int kv = p.Sk;
   if (p.kv_lens != nullptr) kv = min(max(__ldg(p.kv_lens + u.b), 0), p.Sk);
   u.kv = kv;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int r_first = u.q0 + i * kBQ;
-    if (r_first >= p.Sq) {
-      u.n[i] = 0;
-    } else {
-      int lim = kv;
-      if (CAUSAL) lim = min(lim, min(r_first + kBQ, p.Sq));  // last row of the tile + 1
-      u.n[i] = (lim + kBK - 1) / kBK;
-    }
-  }
+  int lim = kv;
+  if (CAUSAL) lim = min(lim, min(u.q0 + kBQ, p.Sq));  // last row of the tile + 1
+  u.n = (lim + kBK - 1) / kBK;
   return u;
 }
 
@@ -183,6 +183,13 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
+// The same wait for a whole warp: every lane waits, and the outcome is made
+// warp-uniform so that warp-collective operations after it never miss a lane.
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t site,
+                                          uint64_t limit_ns) {
+  return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, site, limit_ns));
+}
+
 // Wait used only while draining after an abort: ignores the abort flag.
 __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
@@ -193,6 +200,91 @@ __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) 
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 
+// One warp's arrival on a barrier that counts warps: every lane's tcgen05
+// traffic is ordered before the warp synchronisation, then one lane arrives.
+__device__ __forceinline__ void warp_arrive_after_tc(uint32_t bar, int lane) {
+  tc_fence_before_sync();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+// Row maximum of a thread's 64 raw scores (columns >= climit excluded when
+// MASKED); 4 independent chains of three-input max.
+template <bool MASKED>
+__device__ __forceinline__ float half_row_max(const uint32_t (&s)[2][32], int climit) {
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int col = 0; col < 64; col += 2) {
+    float x0 = u2f(s[col >> 5][col & 31]);
+    float x1 = u2f(s[col >> 5][(col + 1) & 31]);
+    if (MASKED) {
+      x0 = (col < climit) ? x0 : -INFINITY;
+      x1 = (col + 1 < climit) ? x1 : -INFINITY;
+    }
+    m4[(col >> 1) & 3] = max3(m4[(col >> 1) & 3], x0, x1);
+  }
+  return fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
+}
+
+// p = 2^(s*c - mb) for a thread's 64 scores (one packed FMA per pair; masked
+// columns give 0) into 32 bf16 pairs; returns the fp32 sum.  With WITH_MAX it
+// also returns the maximum of the raw valid scores, found in the same pass.
+template <bool MASKED, bool WITH_MAX>
+__device__ __forceinline__ float half_row_exp(const uint32_t (&s)[2][32], float c, float mb, int climit,
+                                              uint32_t (&pk)[32], float& mx) {
+  const uint64_t c2 = f2_pack(c, c);
+  const uint64_t nmb2 = f2_pack(-mb, -mb);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const int col = 2 * e;
+    const float s0 = u2f(s[col >> 5][col & 31]);
+    const float s1 = u2f(s[col >> 5][(col + 1) & 31]);
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(s0, s1), c2, nmb2), x0, x1);
+    float p0 = ex2_approx(x0);
+    float p1 = ex2_approx(x1);
+    if (MASKED) {
+      const bool v0 = col < climit;
+      const bool v1 = col + 1 < climit;
+      p0 = v0 ? p0 : 0.0f;
+      p1 = v1 ? p1 : 0.0f;
+      if (WITH_MAX) m4[e & 3] = max3(m4[e & 3], v0 ? s0 : -INFINITY, v1 ? s1 : -INFINITY);
+    } else if (WITH_MAX) {
+      m4[e & 3] = max3(m4[e & 3], s0, s1);
+    }
+    acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
+    pk[e] = pack_bf16x2(p0, p1);
+  }
+  if (WITH_MAX) mx = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
+  const uint64_t a01 = f2_add(acc[0], acc[1]);
+  const uint64_t a23 = f2_add(acc[2], acc[3]);
+  float lo, hi;
+  f2_unpack(f2_add(a01, a23), lo, hi);
+  return lo + hi;
+}
+
+// A thread's half of its O row (D/2 fp32 columns in TMEM) *= alpha.
+template <int D>
+__device__ __forceinline__ void rescale_o_half(uint32_t tO, float alpha) {
+  const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+  for (int q = 0; q < D / 64; ++q) {
+    uint32_t o[32];
+    tmem_ld_32x32b_x32(tO + q * 32, o);
+    tmem_ld_wait_x32(o);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      float lo, hi;
+      f2_unpack(f2_mul(f2_pack(u2f(o[2 * e]), u2f(o[2 * e + 1])), a2), lo, hi);
+      o[2 * e] = __float_as_uint(lo);
+      o[2 * e + 1] = __float_as_uint(hi);
+    }
+    tmem_st_32x32b_x32(tO + q * 32, o);
+  }
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -201,7 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem_raw + (base - raw));
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  Ctrl& ctl = *reinterpret_cast<Ctrl*>(base_ptr);
+  Xchg& xch = *reinterpret_cast<Xchg*>(base_ptr + 1024);
   volatile int* abort_flag = &ctl.abort_flag;
 
   const int warp = threadIdx.x >> 5;
@@ -211,25 +305,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_q_empty = smem_addr(&ctl.q_empty);
   const uint32_t bar_kv_full0 = smem_addr(&ctl.kv_full[0]);
   const uint32_t bar_kv_empty0 = smem_addr(&ctl.kv_empty[0]);
-  const uint32_t bar_drain = smem_addr(&ctl.drain);
+  // barrier of buffer b = barrier of buffer 0 + 8 * b (consecutive uint64_t)
+  const uint32_t bar_s_full0 = smem_addr(&ctl.s_full[0]);
+  const uint32_t bar_s_free0 = smem_addr(&ctl.s_free[0]);
+  const uint32_t bar_p_full0 = smem_addr(&ctl.p_full[0]);
+  const uint32_t bar_p_free0 = smem_addr(&ctl.p_free[0]);
+  const uint32_t bar_x0 = smem_addr(&ctl.x_bar[0]);
+  const uint32_t bar_e = smem_addr(&ctl.e_bar);
+  const uint32_t bar_o_full = smem_addr(&ctl.o_full);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
     mbar_init(bar_q_empty, 1);
     for (int s = 0; s < G::kSlots; ++s) {
       mbar_init(bar_kv_full0 + 8 * s, 1);
-      mbar_init(bar_kv_empty0 + 8 * s, 1);
+      mbar_init(bar_kv_empty0 + 8 * s, 1);  // K slots: QK issuer; V slots: PV issuer
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_addr(&ctl.s_full[i]), 1);
-      mbar_init(smem_addr(&ctl.p_full[i]), kBQ);
-      mbar_init(smem_addr(&ctl.o_full[i]), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_s_full0 + 8 * b, 1);
+      mbar_init(bar_s_free0 + 8 * b, kSoftmaxWarps);
+      mbar_init(bar_p_full0 + 8 * b, kSoftmaxWarps);
+      mbar_init(bar_p_free0 + 8 * b, 1);
+      mbar_init(bar_x0 + 8 * b, kSoftmaxWarps);
+      mbar_init(smem_addr(&ctl.drain[b]), 1);
     }
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_e, kSoftmaxWarps);
+    mbar_init(bar_o_full, 1);
     ctl.abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kWarpMma) {
+  if (warp == kWarpQK) {
     tmem_alloc(smem_addr(&ctl.tmem_base), G::kTmemCols);
     tmem_relinquish_alloc_permit();
   }
@@ -244,9 +349,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl.tmem_base;
   const uint64_t limit = p.wait_limit_ns;
 
-  if (warp >= 8) {
-    // ------------------------------------------- warpgroup 2: TMA and MMA
-    regs_decrease<kRegsOther>();
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
@@ -256,18 +358,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
         const Unit u = decode_unit<CAUSAL>(p, t);
-        const int N = max(u.n[0], u.n[1]);
-        if (N == 0) continue;
+        if (u.n == 0) continue;
         if (!wait_phase(bar_q_empty, (qcount & 1u) ^ 1u, abort_flag, kSiteQEmpty, limit)) { ok = false; break; }
-        mbar_arrive_expect_tx(bar_q_full, (u.n[0] > 0 ? G::kTileBytes : 0) + (u.n[1] > 0 ? G::kTileBytes : 0));
-        for (int i = 0; i < 2; ++i) {
-          if (u.n[i] == 0) continue;
-          for (int c = 0; c < G::kChunks; ++c)
-            tma_load_4d_hint(base + G::kOffQ + i * G::kTileBytes + c * G::kChunkBytes, &map_q, bar_q_full, c * 64,
-                             u.q0 + i * kBQ, u.h, u.b, pol_once);
-        }
+        mbar_arrive_expect_tx(bar_q_full, G::kTileBytes);
+        for (int c = 0; c < G::kChunks; ++c)
+          tma_load_4d_hint(base + G::kOffQ + c * G::kChunkBytes, &map_q, bar_q_full, c * 64, u.q0, u.h, u.b,
+                           pol_once);
         ++qcount;
-        for (int j = 0; ok && j < N; ++j) {
+        for (int j = 0; ok && j < u.n; ++j) {
           for (int sel = 0; sel < 2; ++sel) {  // K_j, then V_j
             const uint32_t slot = ring % G::kSlots;
             const uint32_t ph = (ring / G::kSlots) & 1u;
@@ -292,244 +390,228 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------------ MMA
-    if (lane == 0) {
-      uint32_t ring = 0, qcount = 0;
-      uint32_t pcount0 = 0u, pcount1 = 0u;
-      bool ok = true;
-      // barrier of Q tile i = barrier of tile 0 + 8 * i (consecutive uint64_t)
-      const uint32_t bar_s_full0 = smem_addr(&ctl.s_full[0]);
-      const uint32_t bar_p_full0 = smem_addr(&ctl.p_full[0]);
-      const uint32_t bar_o_full0 = smem_addr(&ctl.o_full[0]);
-
-      // S_i = Q_i K^T: both operands K-major, 128-B swizzled; one MMA per 16 columns of D.
-      auto issue_qk = [&](int i, uint32_t slot) {
-        const uint32_t qa = base + G::kOffQ + i * G::kTileBytes;
+  } else if (warp == kWarpQK) {
+    // ---------------------------------------------------- S = Q K^T issuer
+    // Runs up to two tiles ahead of the softmax (two S buffers).  Releases
+    // each K slot once its MMAs complete.
+    uint32_t ring = 0, qcount = 0, tcount = 0;
+    bool ok = true;
+    const uint32_t qa = base + G::kOffQ;
+    for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
+      const Unit u = decode_unit<CAUSAL>(p, t);
+      if (u.n == 0) continue;
+      if (!wait_warp(bar_q_full, qcount & 1u, abort_flag, kSiteQFull, limit)) { ok = false; break; }
+      ++qcount;
+      for (int j = 0; j < u.n; ++j, ++tcount) {
+        const uint32_t b = tcount & 1u;
+        const uint32_t use = tcount >> 1;
+        if (tcount >= 2) {  // the softmax has read S of tile tcount-2 out of buffer b
+          if (!wait_warp(bar_s_free0 + 8 * b, (use - 1) & 1u, abort_flag, kSiteSFree, limit)) { ok = false; break; }
+          tc_fence_after_sync();
+        }
+        const uint32_t pos = ring + 2 * j;
+        const uint32_t slot = pos % G::kSlots;
+        if (!wait_warp(bar_kv_full0 + 8 * slot, (pos / G::kSlots) & 1u, abort_flag, kSiteKvFull, limit)) {
+          ok = false;
+          break;
+        }
+        // S_b = Q K_j^T: both operands K-major, 128-B swizzled; one MMA per 16 columns of D.
         const uint32_t ka = base + G::kOffRing + slot * G::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-          mma_ss(tmem + G::tmem_s(i), sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), p.idesc_qk,
-                 kk > 0 ? 1u : 0u);
+          mma_ss_elect(tmem + G::kTmemS + 128u * b, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                       p.idesc_qk, kk > 0 ? 1u : 0u);
         }
-      };
-      // O_i += P_i V: P from TMEM (16 keys = 8 columns per MMA), V MN-major in smem
-      // (LBO = distance between 64-column chunks of D, SBO = 8 keys x 128 B).
-      auto issue_pv = [&](int i, uint32_t slot, bool accumulate) {
+        mma_commit_elect(bar_s_full0 + 8 * b);
+        mma_commit_elect(bar_kv_empty0 + 8 * slot);
+      }
+      if (!ok) break;
+      ring += 2 * u.n;
+      mma_commit_elect(bar_q_empty);
+    }
+    if (!ok) {
+      const uint32_t bar_d = smem_addr(&ctl.drain[0]);
+      mma_commit_elect(bar_d);
+      wait_phase_drain(bar_d, 0);
+    }
+  } else if (warp == kWarpPV) {
+    // ---------------------------------------------------- O += P V issuer
+    uint32_t ring = 0, tcount = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
+      const Unit u = decode_unit<CAUSAL>(p, t);
+      if (u.n == 0) continue;
+      for (int j = 0; j < u.n; ++j, ++tcount) {
+        const uint32_t b = tcount & 1u;
+        const uint32_t use = tcount >> 1;
+        if (!wait_warp(bar_p_full0 + 8 * b, use & 1u, abort_flag, kSitePFull, limit)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t pos = ring + 2 * j + 1;
+        const uint32_t slot = pos % G::kSlots;
+        if (!wait_warp(bar_kv_full0 + 8 * slot, (pos / G::kSlots) & 1u, abort_flag, kSiteKvFull, limit)) {
+          ok = false;
+          break;
+        }
+        // O += P_b V_j: P from TMEM (16 keys = 8 columns per MMA), V MN-major in
+        // smem (LBO = distance between 64-column chunks of D, SBO = 8 keys x 128 B).
         const uint32_t va = base + G::kOffRing + slot * G::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          mma_ts(tmem + G::tmem_o(i), tmem + G::tmem_s(i) + kk * 8,
-                 sdesc_sw128(va + kk * 16 * 128, G::kChunkBytes, 1024), p.idesc_pv,
-                 (accumulate || kk > 0) ? 1u : 0u);
+          mma_ts_elect(tmem + G::kTmemO, tmem + G::kTmemP + 64u * b + kk * 8,
+                       sdesc_sw128(va + kk * 16 * 128, G::kChunkBytes, 1024), p.idesc_pv,
+                       (j > 0 || kk > 0) ? 1u : 0u);
         }
-      };
-      auto wait_kv = [&](uint32_t pos) -> bool {
-        const uint32_t slot = pos % G::kSlots;
-        if (!wait_phase(bar_kv_full0 + 8 * slot, (pos / G::kSlots) & 1u, abort_flag, kSiteKvFull, limit)) return false;
-        tc_fence_after_sync();
-        return true;
-      };
-
-      for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
-        const Unit u = decode_unit<CAUSAL>(p, t);
-        const int N = max(u.n[0], u.n[1]);
-        if (N == 0) continue;
-        if (!wait_phase(bar_q_full, qcount & 1u, abort_flag, kSiteQFull, limit)) { ok = false; break; }
-        ++qcount;
-        tc_fence_after_sync();
-        if (!wait_kv(ring)) { ok = false; break; }
-        for (int i = 0; i < 2; ++i) {
-          if (u.n[i] > 0) {
-            issue_qk(i, ring % G::kSlots);
-            mma_commit(bar_s_full0 + 8 * i);
-          }
-        }
-        mma_commit(bar_kv_empty0 + 8 * (ring % G::kSlots));
-        for (int j = 0; ok && j < N; ++j) {
-          const uint32_t v_pos = ring + 2 * j + 1;
-          const uint32_t kn_pos = ring + 2 * j + 2;
-          if (!wait_kv(v_pos)) { ok = false; break; }
-          bool kn_ready = false;
-          for (int i = 0; i < 2; ++i) {
-            if (j >= u.n[i]) continue;
-            uint32_t& pc = i ? pcount1 : pcount0;
-            if (!wait_phase(bar_p_full0 + 8 * i, pc & 1u, abort_flag, kSitePFull, limit)) { ok = false; break; }
-            ++pc;
-            tc_fence_after_sync();
-            issue_pv(i, v_pos % G::kSlots, j > 0);
-            if (j + 1 < u.n[i]) {
-              if (!kn_ready) {
-                if (!wait_kv(kn_pos)) { ok = false; break; }
-                kn_ready = true;
-              }
-              issue_qk(i, kn_pos % G::kSlots);
-              mma_commit(bar_s_full0 + 8 * i);
-            } else {
-              mma_commit(bar_o_full0 + 8 * i);
-            }
-          }
-          if (!ok) break;
-          if (kn_ready) mma_commit(bar_kv_empty0 + 8 * (kn_pos % G::kSlots));
-          mma_commit(bar_kv_empty0 + 8 * (v_pos % G::kSlots));
-        }
-        if (!ok) break;
-        ring += 2 * N;
-        mma_commit(bar_q_empty);
+        mma_commit_elect(bar_p_free0 + 8 * b);
+        mma_commit_elect(bar_kv_empty0 + 8 * slot);
+        if (j == u.n - 1) mma_commit_elect(bar_o_full);
       }
-      if (!ok) {
-        // Let every MMA this lane issued retire before TMEM is released.
-        mma_commit(bar_drain);
-        wait_phase_drain(bar_drain, 0);
-      }
+      if (!ok) break;
+      ring += 2 * u.n;
     }
-    __syncwarp();
-  }
-  } else {
-    // ------------------------------------------- warpgroups 0, 1: softmax
-    regs_increase<kRegsSoftmax>();
-    const int wg = warp >> 2;                      // which Q tile of the unit
+    if (!ok) {
+      const uint32_t bar_d = smem_addr(&ctl.drain[1]);
+      mma_commit_elect(bar_d);
+      wait_phase_drain(bar_d, 0);
+    }
+  } else if (warp < kSoftmaxWarps) {
+    // -------------------------------------------------------------- softmax
+    // Two threads per query row: half 0 (warps 0-3) owns columns 0-63 of each
+    // score tile, half 1 (warps 4-7) columns 64-127.  Both keep the same
+    // reference max (they exchange their partial maxima every tile) and their
+    // own partial row sums, added in the epilogue.
+    const int half = warp >> 2;
     const int r = threadIdx.x & (kBQ - 1);         // row within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_off + G::tmem_s(wg);
-    const uint32_t tO = tmem + lane_off + G::tmem_o(wg);
-    const uint32_t bar_s = smem_addr(&ctl.s_full[wg]);
-    const uint32_t bar_p = smem_addr(&ctl.p_full[wg]);
-    const uint32_t bar_o = smem_addr(&ctl.o_full[wg]);
+    const uint32_t tO = tmem + lane_off + G::kTmemO + (D / 2) * half;
     const float c = p.c;
-    uint32_t scount = 0, ocount = 0;
+    uint32_t tcount = 0, ocount = 0, ecount = 0;
     bool ok = true;
 
     for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
       const Unit u = decode_unit<CAUSAL>(p, t);
-      const int tile_row0 = u.q0 + wg * kBQ;
-      if (tile_row0 >= p.Sq) continue;
-      const int row = tile_row0 + r;
+      const int row = u.q0 + r;
       const size_t row_index = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq) + row;
-      const int n = wg ? u.n[1] : u.n[0];
-      if (n == 0) {  // no valid key for any row of this tile: O = 0, LSE = -inf
+      uint16_t* o_dst = p.o + row_index * D + (D / 2) * half;
+      if (u.n == 0) {  // no valid key for any row of this unit: O = 0, LSE = -inf
         if (row < p.Sq) {
-          uint4* dst = reinterpret_cast<uint4*>(p.o + row_index * D);
+          uint4* dst = reinterpret_cast<uint4*>(o_dst);
 #pragma unroll
-          for (int q = 0; q < D / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
-          p.lse[row_index] = -INFINITY;
+          for (int q = 0; q < D / 16; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+          if (half == 0) p.lse[row_index] = -INFINITY;
         }
         continue;
       }
 
-      float m_used = -INFINITY;  // stale running max (log2 units, scale folded in)
-      float l = 0.0f;            // running sum of 2^(x - m_used)
-      for (int j = 0; j < n; ++j) {
-        if (!wait_phase(bar_s, scount & 1u, abort_flag, kSiteSFull, limit)) { ok = false; break; }
-        ++scount;
+      float m_used = -INFINITY;  // reference max (log2 units, scale folded in), shared by both halves
+      float l = 0.0f;            // this half's sum of 2^(x - m_used)
+      for (int j = 0; j < u.n; ++j, ++tcount) {
+        const uint32_t b = tcount & 1u;
+        const uint32_t use = tcount >> 1;
+        if (!wait_warp(bar_s_full0 + 8 * b, use & 1u, abort_flag, kSiteSFull, limit)) { ok = false; break; }
         tc_fence_after_sync();
-        uint32_t s[4][32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x32(tS + q * 32, s[q]);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld_wait_x32(s[q]);
+        uint32_t s[2][32];
+        const uint32_t tS = tmem + lane_off + G::kTmemS + 128u * b + 64u * half;
+        tmem_ld_32x32b_x32(tS, s[0]);
+        tmem_ld_32x32b_x32(tS + 32, s[1]);
+        tmem_ld_wait_x32(s[0]);
+        tmem_ld_wait_x32(s[1]);
+        warp_arrive_after_tc(bar_s_free0 + 8 * b, lane);  // the QK issuer may refill buffer b
 
         const int k0 = j * kBK;
-        const bool masked = (k0 + kBK > u.kv) || (CAUSAL && k0 + kBK - 1 > tile_row0);
-        int climit = u.kv - k0;  // columns >= climit are masked for this row
+        const bool masked = (k0 + kBK > u.kv) || (CAUSAL && k0 + kBK - 1 > u.q0);
+        int climit = u.kv - k0;  // columns >= climit of the tile are masked for this row
         if (CAUSAL) climit = min(climit, row - k0 + 1);
+        climit -= 64 * half;     // ... in this half's column numbering
 
-        // row maximum of the valid raw scores (8 independent chains of 3-input max)
-        float mx8[8];
-        if (masked) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) mx8[e] = -INFINITY;
-#pragma unroll
-          for (int col = 0; col < kBK; col += 2) {
-            const float x0 = (col < climit) ? u2f(s[col >> 5][col & 31]) : -INFINITY;
-            const float x1 = (col + 1 < climit) ? u2f(s[col >> 5][(col + 1) & 31]) : -INFINITY;
-            mx8[(col >> 1) & 7] = max3(mx8[(col >> 1) & 7], x0, x1);
-          }
+        uint32_t pk[32];
+        float sum, mx_half;
+        const float m_old = m_used;
+        if (j > 0) {
+          // Exponentiate against the current reference right away; the row max
+          // is found in the same pass and checked after the exchange.
+          sum = masked ? half_row_exp<true, true>(s, c, m_used, climit, pk, mx_half)
+                       : half_row_exp<false, true>(s, c, m_used, climit, pk, mx_half);
         } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) mx8[e] = u2f(s[0][e]);
-#pragma unroll
-          for (int col = 8; col < kBK; col += 2)
-            mx8[(col >> 1) & 7] = max3(mx8[(col >> 1) & 7], u2f(s[col >> 5][col & 31]), u2f(s[col >> 5][(col + 1) & 31]));
+          mx_half = masked ? half_row_max<true>(s, climit) : half_row_max<false>(s, climit);
         }
-        const float mx = max3(max3(mx8[0], mx8[1], mx8[2]), max3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        // exchange the partial maxima of the row (by tile parity, so that a
+        // slow partner still reads the previous tile's value undisturbed)
+        xch.xmax[b][half][r] = mx_half;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_x0 + 8 * b);
+        if (!wait_warp(bar_x0 + 8 * b, use & 1u, abort_flag, kSiteExchange, limit)) { ok = false; break; }
+        const float mx = fmaxf(mx_half, xch.xmax[b][half ^ 1][r]);
         const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
-        const float m_new = fmaxf(m_used, m_tile);
-        // Lazy correction: move the reference max only when it grew by more than
-        // kTau; every term stays <= 2^kTau, and O and l keep one shared reference.
-        const bool grow = m_new > m_used + kTau;
-        const float alpha = grow ? ex2_approx(m_used - m_new) : 1.0f;
-        if (grow) {
+        bool rescale = false;
+        float alpha = 1.0f;
+        if (j == 0) {
+          // First tile: its row max is the reference (every row of a unit with
+          // n > 0 has key 0 valid, so the reference is finite afterwards).
+          m_used = m_tile;
+          const float mb = (m_used == -INFINITY) ? 0.0f : m_used;
+          float unused;
+          sum = masked ? half_row_exp<true, false>(s, c, mb, climit, pk, unused)
+                       : half_row_exp<false, false>(s, c, mb, climit, pk, unused);
+        } else {
+          // Lazy correction: only when the max grew by more than kTau is the
+          // reference moved, this tile recomputed, and l and O rescaled by
+          // alpha = 2^(m_old - m_new); every term stays <= 2^kTau and O and l
+          // always share one reference.  Both halves see the same row max, so
+          // they take the same decision.
+          const bool grow = m_tile > m_used + kTau;
+          if (__any_sync(0xffffffffu, grow)) {
+            rescale = true;
+            if (grow) {
+              alpha = ex2_approx(m_old - m_tile);
+              m_used = m_tile;
+            }
+            float unused;
+            sum = masked ? half_row_exp<true, false>(s, c, m_used, climit, pk, unused)
+                         : half_row_exp<false, false>(s, c, m_used, climit, pk, unused);
+          }
+        }
+        // P buffer b is free once the PV of tile tcount-2 has completed.
+        if (tcount >= 2 && !wait_warp(bar_p_free0 + 8 * b, (use - 1) & 1u, abort_flag, kSitePFree, limit)) {
+          ok = false;
+          break;
+        }
+        if (rescale) {
+          // O is stable once the PV of the previous tile (buffer b^1) completed.
+          const uint32_t tp = tcount - 1;
+          if (!wait_warp(bar_p_free0 + 8 * (tp & 1u), (tp >> 1) & 1u, abort_flag, kSitePFree, limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
           l *= alpha;
-          m_used = m_new;
+          rescale_o_half<D>(tO, alpha);
+        } else {
+          tc_fence_after_sync();
         }
-        // p = 2^(s*c - mb) on pairs (one packed FMA per pair), packed row sum,
-        // bf16 pairs written back over the first half of the S columns in
-        // 16-column chunks.
-        const float mb = (m_used == -INFINITY) ? 0.0f : m_used;
-        const uint64_t c2 = f2_pack(c, c);
-        const uint64_t nmb2 = f2_pack(-mb, -mb);
-        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int col = q * 32 + 2 * e;
-            float x0, x1;
-            f2_unpack(f2_fma(f2_pack(u2f(s[q][2 * e]), u2f(s[q][2 * e + 1])), c2, nmb2), x0, x1);
-            float p0 = ex2_approx(x0);
-            float p1 = ex2_approx(x1);
-            if (masked) {
-              p0 = (col < climit) ? p0 : 0.0f;
-              p1 = (col + 1 < climit) ? p1 : 0.0f;
-            }
-            acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
-            pk[e] = pack_bf16x2(p0, p1);
-          }
-          tmem_st_32x32b_x16(tS + q * 16, pk);
-        }
-        {
-          const uint64_t a01 = f2_add(acc[0], acc[1]);
-          const uint64_t a23 = f2_add(acc[2], acc[3]);
-          float lo, hi;
-          f2_unpack(f2_add(a01, a23), lo, hi);
-          l += lo + hi;
-        }
-        if (j > 0 && __any_sync(0xffffffffu, grow)) {
-          // O_i row *= alpha (PV of tile j-1 has retired: S_i(j) was committed after it).
-          // Done after P is written so that the score row is no longer live.
-          const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-          for (int q = 0; q < D / 32; ++q) {
-            uint32_t o[32];
-            tmem_ld_32x32b_x32(tO + q * 32, o);
-            tmem_ld_wait_x32(o);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              float lo, hi;
-              f2_unpack(f2_mul(f2_pack(u2f(o[2 * e]), u2f(o[2 * e + 1])), a2), lo, hi);
-              o[2 * e] = __float_as_uint(lo);
-              o[2 * e + 1] = __float_as_uint(hi);
-            }
-            tmem_st_32x32b_x32(tO + q * 32, o);
-          }
-        }
+        const uint32_t tP = tmem + lane_off + G::kTmemP + 64u * b + 32u * half;
+        tmem_st_32x32b_x16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+        tmem_st_32x32b_x16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
         tmem_st_wait();
-        tc_fence_before_sync();
-        mbar_arrive(bar_p);
+        warp_arrive_after_tc(bar_p_full0 + 8 * b, lane);
+        l += sum;
       }
       if (!ok) break;
 
       // ------------------------------------------------------------ epilogue
-      if (!wait_phase(bar_o, ocount & 1u, abort_flag, kSiteOFull, limit)) { ok = false; break; }
+      if (!wait_warp(bar_o_full, ocount & 1u, abort_flag, kSiteOFull, limit)) { ok = false; break; }
       ++ocount;
       tc_fence_after_sync();
-      const bool has_key = l > 0.0f;
-      const float inv_l = has_key ? 1.0f / l : 0.0f;
+      xch.xsum[half][r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_e);
+      if (!wait_warp(bar_e, ecount & 1u, abort_flag, kSiteExchange, limit)) { ok = false; break; }
+      ++ecount;
+      const float l_row = l + xch.xsum[half ^ 1][r];
+      const bool has_key = l_row > 0.0f;
+      const float inv_l = has_key ? 1.0f / l_row : 0.0f;
 #pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
+      for (int q = 0; q < D / 64; ++q) {
         uint32_t o[32];
         tmem_ld_32x32b_x32(tO + q * 32, o);
         tmem_ld_wait_x32(o);
@@ -538,18 +620,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             w[e] = has_key ? pack_bf16x2(u2f(o[2 * e]) * inv_l, u2f(o[2 * e + 1]) * inv_l) : 0u;
-          uint4* dst = reinterpret_cast<uint4*>(p.o + row_index * D + q * 32);
+          uint4* dst = reinterpret_cast<uint4*>(o_dst + q * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
         }
       }
-      if (row < p.Sq) p.lse[row_index] = has_key ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      if (row < p.Sq && half == 0) p.lse[row_index] = has_key ? (m_used + log2f(l_row)) * kLn2 : -INFINITY;
+      // The next unit's first PV overwrites O only after every softmax warp has
+      // arrived on p_full for it, which each warp does after this epilogue.
+      tc_fence_before_sync();
     }
   }
 
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == kWarpQK) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, G::kTmemCols);
   }
@@ -673,8 +758,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   // TMA strides must stay below 2^40 bytes; work units must fit an int.
   const uint64_t max_s = static_cast<uint64_t>(Sq > Sk ? Sq : Sk);
   if (static_cast<uint64_t>(H) * max_s * D * 2 >= (1ull << 40)) return ATTN_ERR_SHAPE;
-  const uint64_t n_qpairs = (static_cast<uint64_t>(Sq) + kUnitRows - 1) / kUnitRows;
-  if (static_cast<uint64_t>(B) * H * n_qpairs > 0x7fffffffull) return ATTN_ERR_SHAPE;
+  const uint64_t n_qtiles = (static_cast<uint64_t>(Sq) + kBQ - 1) / kBQ;
+  if (static_cast<uint64_t>(B) * H * n_qtiles > 0x7fffffffull) return ATTN_ERR_SHAPE;
 
   DeviceInfo* dev = nullptr;
   attn_status st = device_info(&dev);
@@ -697,8 +782,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.H = H;
   p.Sq = Sq;
   p.Sk = Sk;
-  p.n_qpairs = static_cast<int>(n_qpairs);
-  p.total_units = static_cast<int>(static_cast<uint64_t>(B) * H * n_qpairs);
+  p.n_qtiles = static_cast<int>(n_qtiles);
+  p.total_units = static_cast<int>(static_cast<uint64_t>(B) * H * n_qtiles);
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634);
   p.idesc_qk = idesc_bf16_f32(kBQ, kBK, scale < 0.0f, false);
   p.idesc_pv = idesc_bf16_f32(kBQ, D, false, true);
