@@ -52,6 +52,12 @@ namespace {
 constexpr int kBQ = 128;          // query rows per work unit (MMA M, TMEM lanes)
 constexpr int kBK = 128;          // keys per K/V tile (MMA N of QK^T)
 constexpr int kThreads = 384;
+// Register split (setmaxnreg): the block launches at 168 per thread; warpgroup 2
+// (producer, issuers) drops to 104 and the two softmax warpgroups rise to 200:
+//   384 x 168 = 64512 = 256 x 200 + 128 x 104; per SM sub-partition
+//   (one warp of each warpgroup) (200 + 200 + 104) x 32 <= 16384.
+constexpr int kRegsSoftmax = 200;
+constexpr int kRegsOther = 104;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpQK = 9;
@@ -72,7 +78,6 @@ enum WaitSite : uint32_t {
   kSiteSelftest = 8,
   kSiteSFree = 9,
   kSitePFree = 10,
-  kSiteExchange = 11,
 };
 
 // [0]: 1 once any wait gave up; [1]: site of the first one; [2]: its block.
@@ -98,8 +103,6 @@ struct Ctrl {
   uint64_t q_full, q_empty;
   uint64_t kv_full[12], kv_empty[12];
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
-  uint64_t x_bar[2];       // row-max exchange between the two softmax halves, by tile parity
-  uint64_t e_bar;          // row-sum exchange in the epilogue
   uint64_t o_full;
   uint64_t drain[2];
   uint32_t tmem_base;
@@ -310,8 +313,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_s_free0 = smem_addr(&ctl.s_free[0]);
   const uint32_t bar_p_full0 = smem_addr(&ctl.p_full[0]);
   const uint32_t bar_p_free0 = smem_addr(&ctl.p_free[0]);
-  const uint32_t bar_x0 = smem_addr(&ctl.x_bar[0]);
-  const uint32_t bar_e = smem_addr(&ctl.e_bar);
   const uint32_t bar_o_full = smem_addr(&ctl.o_full);
 
   if (threadIdx.x == 0) {
@@ -326,10 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_s_free0 + 8 * b, kSoftmaxWarps);
       mbar_init(bar_p_full0 + 8 * b, kSoftmaxWarps);
       mbar_init(bar_p_free0 + 8 * b, 1);
-      mbar_init(bar_x0 + 8 * b, kSoftmaxWarps);
       mbar_init(smem_addr(&ctl.drain[b]), 1);
     }
-    mbar_init(bar_e, kSoftmaxWarps);
     mbar_init(bar_o_full, 1);
     ctl.abort_flag = 0;
     fence_barrier_init();
@@ -349,6 +348,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ctl.tmem_base;
   const uint64_t limit = p.wait_limit_ns;
 
+  if (warp >= kSoftmaxWarps) {
+    regs_decrease<kRegsOther>();
   if (warp == kWarpLoad) {
     // ------------------------------------------------------------------ TMA
     if (lane == 0) {
@@ -474,18 +475,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_elect(bar_d);
       wait_phase_drain(bar_d, 0);
     }
-  } else if (warp < kSoftmaxWarps) {
+  }
+  } else {
+    regs_increase<kRegsSoftmax>();
     // -------------------------------------------------------------- softmax
     // Two threads per query row: half 0 (warps 0-3) owns columns 0-63 of each
     // score tile, half 1 (warps 4-7) columns 64-127.  Both keep the same
-    // reference max (they exchange their partial maxima every tile) and their
-    // own partial row sums, added in the epilogue.
+    // reference max (they exchange their partial maxima every tile through
+    // shared memory and named barrier 1) and their own partial row sums, added
+    // in the epilogue.
+    //
+    // Named barriers cannot time out, so the eight warps keep one discipline:
+    // a wait that fails only marks the warp as failed and skips work; every
+    // warp still executes every named barrier, and right after each one all of
+    // them test the CTA abort flag (raised before the barrier by whoever gave
+    // up) and leave together.
     const int half = warp >> 2;
     const int r = threadIdx.x & (kBQ - 1);         // row within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tO = tmem + lane_off + G::kTmemO + (D / 2) * half;
     const float c = p.c;
-    uint32_t tcount = 0, ocount = 0, ecount = 0;
+    constexpr uint32_t kBarSoftmax = 1;
+    constexpr uint32_t kSoftmaxThreads = kSoftmaxWarps * 32;
+    uint32_t tcount = 0, ocount = 0;
     bool ok = true;
 
     for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
@@ -505,42 +517,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       float m_used = -INFINITY;  // reference max (log2 units, scale folded in), shared by both halves
       float l = 0.0f;            // this half's sum of 2^(x - m_used)
+      bool failed = false;
       for (int j = 0; j < u.n; ++j, ++tcount) {
         const uint32_t b = tcount & 1u;
         const uint32_t use = tcount >> 1;
-        if (!wait_warp(bar_s_full0 + 8 * b, use & 1u, abort_flag, kSiteSFull, limit)) { ok = false; break; }
-        tc_fence_after_sync();
-        uint32_t s[2][32];
-        const uint32_t tS = tmem + lane_off + G::kTmemS + 128u * b + 64u * half;
-        tmem_ld_32x32b_x32(tS, s[0]);
-        tmem_ld_32x32b_x32(tS + 32, s[1]);
-        tmem_ld_wait_x32(s[0]);
-        tmem_ld_wait_x32(s[1]);
-        warp_arrive_after_tc(bar_s_free0 + 8 * b, lane);  // the QK issuer may refill buffer b
-
+        const uint32_t bar_pf = bar_p_free0 + 8 * b;
         const int k0 = j * kBK;
         const bool masked = (k0 + kBK > u.kv) || (CAUSAL && k0 + kBK - 1 > u.q0);
         int climit = u.kv - k0;  // columns >= climit of the tile are masked for this row
         if (CAUSAL) climit = min(climit, row - k0 + 1);
         climit -= 64 * half;     // ... in this half's column numbering
 
+        uint32_t s[2][32];
         uint32_t pk[32];
-        float sum, mx_half;
-        const float m_old = m_used;
-        if (j > 0) {
-          // Exponentiate against the current reference right away; the row max
-          // is found in the same pass and checked after the exchange.
-          sum = masked ? half_row_exp<true, true>(s, c, m_used, climit, pk, mx_half)
-                       : half_row_exp<false, true>(s, c, m_used, climit, pk, mx_half);
-        } else {
-          mx_half = masked ? half_row_max<true>(s, climit) : half_row_max<false>(s, climit);
+        float sum = 0.0f, mx_half = -INFINITY;
+        bool pf_ready = true;
+        if (!failed && !wait_warp(bar_s_full0 + 8 * b, use & 1u, abort_flag, kSiteSFull, limit)) failed = true;
+        if (!failed) {
+          tc_fence_after_sync();
+          const uint32_t tS = tmem + lane_off + G::kTmemS + 128u * b + 64u * half;
+          tmem_ld_32x32b_x32(tS, s[0]);
+          tmem_ld_32x32b_x32(tS + 32, s[1]);
+          tmem_ld_wait_x32(s[0]);
+          tmem_ld_wait_x32(s[1]);
+          warp_arrive_after_tc(bar_s_free0 + 8 * b, lane);  // the QK issuer may refill buffer b
+          // P buffer b is free once the PV of tile tcount-2 has completed: ask
+          // now, use the answer after the exponentials.
+          if (tcount >= 2) pf_ready = mbar_test_wait(bar_pf, (use - 1) & 1u);
+          if (j > 0) {
+            // Exponentiate against the current reference right away; the row
+            // max is found in the same pass and checked after the exchange.
+            sum = masked ? half_row_exp<true, true>(s, c, m_used, climit, pk, mx_half)
+                         : half_row_exp<false, true>(s, c, m_used, climit, pk, mx_half);
+          } else {
+            mx_half = masked ? half_row_max<true>(s, climit) : half_row_max<false>(s, climit);
+          }
+          // by tile parity, so a slow partner still reads the previous value undisturbed
+          xch.xmax[b][half][r] = mx_half;
         }
-        // exchange the partial maxima of the row (by tile parity, so that a
-        // slow partner still reads the previous tile's value undisturbed)
-        xch.xmax[b][half][r] = mx_half;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_x0 + 8 * b);
-        if (!wait_warp(bar_x0 + 8 * b, use & 1u, abort_flag, kSiteExchange, limit)) { ok = false; break; }
+        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+        if (*abort_flag) { ok = false; break; }
         const float mx = fmaxf(mx_half, xch.xmax[b][half ^ 1][r]);
         const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
         bool rescale = false;
@@ -563,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (__any_sync(0xffffffffu, grow)) {
             rescale = true;
             if (grow) {
-              alpha = ex2_approx(m_old - m_tile);
+              alpha = ex2_approx(m_used - m_tile);
               m_used = m_tile;
             }
             float unused;
@@ -571,42 +587,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                          : half_row_exp<false, false>(s, c, m_used, climit, pk, unused);
           }
         }
-        // P buffer b is free once the PV of tile tcount-2 has completed.
-        if (tcount >= 2 && !wait_warp(bar_p_free0 + 8 * b, (use - 1) & 1u, abort_flag, kSitePFree, limit)) {
-          ok = false;
-          break;
-        }
-        if (rescale) {
+        if (!pf_ready && !wait_warp(bar_pf, (use - 1) & 1u, abort_flag, kSitePFree, limit)) failed = true;
+        if (rescale && !failed) {
           // O is stable once the PV of the previous tile (buffer b^1) completed.
           const uint32_t tp = tcount - 1;
           if (!wait_warp(bar_p_free0 + 8 * (tp & 1u), (tp >> 1) & 1u, abort_flag, kSitePFree, limit)) {
-            ok = false;
-            break;
+            failed = true;
+          } else {
+            tc_fence_after_sync();
+            l *= alpha;
+            rescale_o_half<D>(tO, alpha);
           }
-          tc_fence_after_sync();
-          l *= alpha;
-          rescale_o_half<D>(tO, alpha);
-        } else {
-          tc_fence_after_sync();
         }
-        const uint32_t tP = tmem + lane_off + G::kTmemP + 64u * b + 32u * half;
-        tmem_st_32x32b_x16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
-        tmem_st_32x32b_x16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
-        tmem_st_wait();
-        warp_arrive_after_tc(bar_p_full0 + 8 * b, lane);
-        l += sum;
+        if (!failed) {
+          tc_fence_after_sync();
+          const uint32_t tP = tmem + lane_off + G::kTmemP + 64u * b + 32u * half;
+          tmem_st_32x32b_x16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+          tmem_st_32x32b_x16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+          tmem_st_wait();
+          warp_arrive_after_tc(bar_p_full0 + 8 * b, lane);
+          l += sum;
+        }
       }
       if (!ok) break;
 
       // ------------------------------------------------------------ epilogue
-      if (!wait_warp(bar_o_full, ocount & 1u, abort_flag, kSiteOFull, limit)) { ok = false; break; }
+      if (!failed && !wait_warp(bar_o_full, ocount & 1u, abort_flag, kSiteOFull, limit)) failed = true;
       ++ocount;
+      if (!failed) xch.xsum[half][r] = l;
+      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+      if (*abort_flag) { ok = false; break; }
       tc_fence_after_sync();
-      xch.xsum[half][r] = l;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_e);
-      if (!wait_warp(bar_e, ecount & 1u, abort_flag, kSiteExchange, limit)) { ok = false; break; }
-      ++ecount;
       const float l_row = l + xch.xsum[half ^ 1][r];
       const bool has_key = l_row > 0.0f;
       const float inv_l = has_key ? 1.0f / l_row : 0.0f;
