@@ -63,6 +63,7 @@ constexpr int kWarpLoad = 8;
 constexpr int kWarpQK = 9;
 constexpr int kWarpPV = 10;
 constexpr float kTau = 8.0f;      // lazy rescale threshold (log2 units)
+constexpr float kTauPow2 = 256.0f; // 2^kTau
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s for draining after an abort
@@ -530,8 +531,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         uint32_t s[2][32];
         uint32_t pk[32];
-        float sum = 0.0f, mx_half = -INFINITY;
+        float sum = 0.0f;
         bool pf_ready = true;
+        bool suspect = false;  // this thread's part of the row may have grown past the reference
         if (!failed && !wait_warp(bar_s_full0 + 8 * b, use & 1u, abort_flag, kSiteSFull, limit)) failed = true;
         if (!failed) {
           tc_fence_after_sync();
@@ -545,46 +547,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           // now, use the answer after the exponentials.
           if (tcount >= 2) pf_ready = mbar_test_wait(bar_pf, (use - 1) & 1u);
           if (j > 0) {
-            // Exponentiate against the current reference right away; the row
-            // max is found in the same pass and checked after the exchange.
-            sum = masked ? half_row_exp<true, true>(s, c, m_used, climit, pk, mx_half)
-                         : half_row_exp<false, true>(s, c, m_used, climit, pk, mx_half);
-          } else {
-            mx_half = masked ? half_row_max<true>(s, climit) : half_row_max<false>(s, climit);
-          }
-          // by tile parity, so a slow partner still reads the previous value undisturbed
-          xch.xmax[b][half][r] = mx_half;
-        }
-        named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-        if (*abort_flag) { ok = false; break; }
-        const float mx = fmaxf(mx_half, xch.xmax[b][half ^ 1][r]);
-        const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
-        bool rescale = false;
-        float alpha = 1.0f;
-        if (j == 0) {
-          // First tile: its row max is the reference (every row of a unit with
-          // n > 0 has key 0 valid, so the reference is finite afterwards).
-          m_used = m_tile;
-          const float mb = (m_used == -INFINITY) ? 0.0f : m_used;
-          float unused;
-          sum = masked ? half_row_exp<true, false>(s, c, mb, climit, pk, unused)
-                       : half_row_exp<false, false>(s, c, mb, climit, pk, unused);
-        } else {
-          // Lazy correction: only when the max grew by more than kTau is the
-          // reference moved, this tile recomputed, and l and O rescaled by
-          // alpha = 2^(m_old - m_new); every term stays <= 2^kTau and O and l
-          // always share one reference.  Both halves see the same row max, so
-          // they take the same decision.
-          const bool grow = m_tile > m_used + kTau;
-          if (__any_sync(0xffffffffu, grow)) {
-            rescale = true;
-            if (grow) {
-              alpha = ex2_approx(m_used - m_tile);
-              m_used = m_tile;
-            }
+            // Exponentiate against the current reference right away.  Each term
+            // is 2^(x - m_used); if they all stay <= 2^kTau no score of this part
+            // of the row grew past the reference by more than kTau, and a part
+            // sum <= 2^kTau proves it (the test is also false for NaN / inf).
             float unused;
             sum = masked ? half_row_exp<true, false>(s, c, m_used, climit, pk, unused)
                          : half_row_exp<false, false>(s, c, m_used, climit, pk, unused);
+            suspect = !(sum <= kTauPow2);
+          } else {
+            suspect = true;  // first tile: the reference is this tile's row max
+          }
+        }
+        // One barrier per tile for the eight softmax warps; it also tells every
+        // thread whether any row of the tile needs its exact maximum.
+        const bool any_suspect = named_bar_red_or(kBarSoftmax, kSoftmaxThreads, suspect);
+        if (*abort_flag) { ok = false; break; }
+        bool rescale = false;
+        float alpha = 1.0f;
+        if (any_suspect) {
+          // Exact row max: partial maxima of both halves through shared memory
+          // (by tile parity, so a slow partner still reads the previous value
+          // undisturbed).  Taken by all eight warps together.
+          if (!failed) {
+            xch.xmax[b][half][r] = masked ? half_row_max<true>(s, climit) : half_row_max<false>(s, climit);
+          }
+          named_bar_sync(kBarSoftmax, kSoftmaxThreads);
+          if (*abort_flag) { ok = false; break; }
+          const float mx = fmaxf(xch.xmax[b][0][r], xch.xmax[b][1][r]);
+          const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
+          if (j == 0) {
+            // First tile: its row max is the reference (every row of a unit with
+            // n > 0 has key 0 valid, so the reference is finite afterwards).
+            m_used = m_tile;
+            const float mb = (m_used == -INFINITY) ? 0.0f : m_used;
+            float unused;
+            sum = masked ? half_row_exp<true, false>(s, c, mb, climit, pk, unused)
+                         : half_row_exp<false, false>(s, c, mb, climit, pk, unused);
+          } else {
+            // Lazy correction: only when the max grew by more than kTau is the
+            // reference moved, this tile recomputed, and l and O rescaled by
+            // alpha = 2^(m_old - m_new); every term stays <= 2^kTau and O and l
+            // always share one reference.  Both halves see the same row max, so
+            // they take the same decision.
+            const bool grow = m_tile > m_used + kTau;
+            if (__any_sync(0xffffffffu, grow)) {
+              rescale = true;
+              if (grow) {
+                alpha = ex2_approx(m_used - m_tile);
+                m_used = m_tile;
+              }
+              float unused;
+              sum = masked ? half_row_exp<true, false>(s, c, m_used, climit, pk, unused)
+                           : half_row_exp<false, false>(s, c, m_used, climit, pk, unused);
+            }
           }
         }
         if (!pf_ready && !wait_warp(bar_pf, (use - 1) & 1u, abort_flag, kSitePFree, limit)) failed = true;
