@@ -62,8 +62,8 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpQK = 9;
 constexpr int kWarpPV = 10;
-constexpr float kTau = 8.0f;      // lazy rescale threshold (log2 units)
-constexpr float kTauPow2 = 256.0f; // 2^kTau
+constexpr float kTau = 16.0f;     // lazy rescale threshold (log2 units): terms stay <= 2^16
+constexpr float kTauPow2 = 65536.0f;  // 2^kTau
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s for draining after an abort
@@ -160,6 +160,18 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int t) {
   if (CAUSAL) lim = min(lim, min(u.q0 + kBQ, p.Sq));  // last row of the tile + 1
   u.n = (lim + kBK - 1) / kBK;
   return u;
+}
+
+// Unit processed at the t-th step of the persistent loop (t = blockIdx.x +
+// k * gridDim.x).  Causal units come longest first; they are dealt to the CTAs
+// in alternating direction each round ("snake" order), which evens out the
+// per-CTA sums of their lengths.  Values >= total_units are skipped.
+template <bool CAUSAL>
+__device__ __forceinline__ int unit_at(int t) {
+  if (!CAUSAL) return t;
+  const int round = t / static_cast<int>(gridDim.x);
+  const int pos = t - round * static_cast<int>(gridDim.x);
+  return (round & 1) ? round * static_cast<int>(gridDim.x) + (static_cast<int>(gridDim.x) - 1 - pos) : t;
 }
 
 __device__ __noinline__ void record_give_up(uint32_t site) {
@@ -348,6 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem = ctl.tmem_base;
   const uint64_t limit = p.wait_limit_ns;
+  // every role walks the same sequence of units (whole rounds of gridDim.x)
+  const int t_end = (p.total_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) *
+                    static_cast<int>(gridDim.x);
 
   if (warp >= kSoftmaxWarps) {
     regs_decrease<kRegsOther>();
@@ -358,8 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_once = l2_policy_evict_first();  // Q: read once
       uint32_t ring = 0, qcount = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
-        const Unit u = decode_unit<CAUSAL>(p, t);
+      for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
+        const int unit = unit_at<CAUSAL>(t);
+        if (unit >= p.total_units) continue;
+        const Unit u = decode_unit<CAUSAL>(p, unit);
         if (u.n == 0) continue;
         if (!wait_phase(bar_q_empty, (qcount & 1u) ^ 1u, abort_flag, kSiteQEmpty, limit)) { ok = false; break; }
         mbar_arrive_expect_tx(bar_q_full, G::kTileBytes);
@@ -399,8 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t ring = 0, qcount = 0, tcount = 0;
     bool ok = true;
     const uint32_t qa = base + G::kOffQ;
-    for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
-      const Unit u = decode_unit<CAUSAL>(p, t);
+    for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
+      const int unit = unit_at<CAUSAL>(t);
+        if (unit >= p.total_units) continue;
+        const Unit u = decode_unit<CAUSAL>(p, unit);
       if (u.n == 0) continue;
       if (!wait_warp(bar_q_full, qcount & 1u, abort_flag, kSiteQFull, limit)) { ok = false; break; }
       ++qcount;
@@ -441,8 +460,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------- O += P V issuer
     uint32_t ring = 0, tcount = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
-      const Unit u = decode_unit<CAUSAL>(p, t);
+    for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
+      const int unit = unit_at<CAUSAL>(t);
+        if (unit >= p.total_units) continue;
+        const Unit u = decode_unit<CAUSAL>(p, unit);
       if (u.n == 0) continue;
       for (int j = 0; j < u.n; ++j, ++tcount) {
         const uint32_t b = tcount & 1u;
@@ -501,8 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tcount = 0, ocount = 0;
     bool ok = true;
 
-    for (int t = blockIdx.x; ok && t < p.total_units; t += gridDim.x) {
-      const Unit u = decode_unit<CAUSAL>(p, t);
+    for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
+      const int unit = unit_at<CAUSAL>(t);
+        if (unit >= p.total_units) continue;
+        const Unit u = decode_unit<CAUSAL>(p, unit);
       const int row = u.q0 + r;
       const size_t row_index = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq) + row;
       uint16_t* o_dst = p.o + row_index * D + (D / 2) * half;
@@ -786,7 +809,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   const uint64_t max_s = static_cast<uint64_t>(Sq > Sk ? Sq : Sk);
   if (static_cast<uint64_t>(H) * max_s * D * 2 >= (1ull << 40)) return ATTN_ERR_SHAPE;
   const uint64_t n_qtiles = (static_cast<uint64_t>(Sq) + kBQ - 1) / kBQ;
-  if (static_cast<uint64_t>(B) * H * n_qtiles > 0x7fffffffull) return ATTN_ERR_SHAPE;
+  if (static_cast<uint64_t>(B) * H * n_qtiles > 0x7fff0000ull) return ATTN_ERR_SHAPE;  // + room for whole rounds
 
   DeviceInfo* dev = nullptr;
   attn_status st = device_info(&dev);
