@@ -29,12 +29,21 @@ ATTN_ERR_SCALE = 5
 ATTN_ERR_CUDA = 6
 ATTN_ERR_DEVICE_TIMEOUT = 7
 ATTN_ERR_UNSUPPORTED_DEVICE = 8
+ATTN_ERR_WORKSPACE = 9
 
 #: Functions declared in include/attn.h, with their ctypes signatures.
 SIGNATURES = {
     "attn_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "attn_fwd_splitkv_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                          ctypes.c_int]),
+    "attn_fwd_splitkv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "attn_lse_merge": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_void_p]),
     "attn_get_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_check_device_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
     "attn_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
@@ -76,6 +85,22 @@ def attn_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, 
     return lib().attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, stream)
 
 
+def attn_fwd_splitkv_workspace_size(B: int, H: int, Sq: int, D: int, num_splits: int) -> int:
+    return lib().attn_fwd_splitkv_workspace_size(B, H, Sq, D, num_splits)
+
+
+def attn_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
+                     scale: float, causal: int, kv_lens: Optional[int], num_splits: int, workspace: int,
+                     workspace_bytes: int, stream: Optional[int]) -> int:
+    return lib().attn_fwd_splitkv(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, num_splits,
+                                  workspace, workspace_bytes, stream)
+
+
+def attn_lse_merge(o_parts: int, lse_parts: int, num_parts: int, o: int, lse: int, rows: int, D: int,
+                   stream: Optional[int]) -> int:
+    return lib().attn_lse_merge(o_parts, lse_parts, num_parts, o, lse, rows, D, stream)
+
+
 def attn_get_error_string(status: int) -> str:
     return lib().attn_get_error_string(status).decode()
 
@@ -95,6 +120,69 @@ def attn_abi_version() -> int:
 
 
 # -------------------------------------------------------------- torch facing
+
+def _check_qkv(q, k, v, kv_lens):
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-d bf16 CUDA tensor")
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    if tuple(k.shape) != (B, H, Sk, D) or tuple(v.shape) != (B, H, Sk, D):
+        raise ValueError("k and v must be [B, H, Sk, D] with q's B, H, D")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on one device")
+    kv_ptr = None
+    if kv_lens is not None:
+        if kv_lens.dtype != torch.int32 or kv_lens.device != q.device or kv_lens.numel() != B \
+                or not kv_lens.is_contiguous():
+            raise ValueError("kv_lens must be a contiguous int32 tensor [B] on q's device")
+        kv_ptr = kv_lens.data_ptr()
+    return B, H, Sq, Sk, D, kv_ptr
+
+
+def forward_splitkv(q, k, v, num_splits: int, scale: Optional[float] = None, causal: bool = False,
+                    kv_lens=None, workspace=None):
+    """Split-KV forward on torch CUDA tensors (see ``forward``).  ``workspace``
+    (a CUDA tensor of at least ``attn_fwd_splitkv_workspace_size`` bytes) is
+    allocated with torch when not given."""
+    import torch
+
+    B, H, Sq, Sk, D, kv_ptr = _check_qkv(q, k, v, kv_lens)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    need = attn_fwd_splitkv_workspace_size(B, H, Sq, D, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                              B, H, Sq, Sk, D, float(scale), int(bool(causal)), kv_ptr, num_splits,
+                              workspace.data_ptr(), workspace.numel() * workspace.element_size(), stream)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_splitkv")
+    return out, lse
+
+
+def lse_merge(o_parts, lse_parts):
+    """Merge ``o_parts`` (fp32 ``[n, rows, D]``) and ``lse_parts`` (fp32 ``[n, rows]``)
+    CUDA tensors into ``(o bf16 [rows, D], lse fp32 [rows])``."""
+    import torch
+
+    n, rows, D = o_parts.shape
+    out = torch.empty((rows, D), dtype=torch.bfloat16, device=o_parts.device)
+    lse = torch.empty((rows,), dtype=torch.float32, device=o_parts.device)
+    with torch.cuda.device(o_parts.device):
+        stream = torch.cuda.current_stream(o_parts.device).cuda_stream
+        st = attn_lse_merge(o_parts.data_ptr(), lse_parts.data_ptr(), n, out.data_ptr(), lse.data_ptr(), rows, D,
+                            stream)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_lse_merge")
+    return out, lse
+
 
 def forward(q, k, v, scale: Optional[float] = None, causal: bool = False, kv_lens=None,
             out=None, lse=None):

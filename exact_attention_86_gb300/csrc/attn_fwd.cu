@@ -125,7 +125,10 @@ struct Params {
   const int32_t* kv_lens;
   int B, H, Sq, Sk;
   int n_qtiles;
+  int num_splits;          // key ranges per (b, h, query tile); 1 = whole rows
   int total_units;
+  float* o_part;           // split mode: fp32 [num_splits][B*H*Sq][D] normalised partial outputs
+  float* lse_part;         //             fp32 [num_splits][B*H*Sq] partial LSE; nullptr = write o/lse
   float c;                 // |scale| * log2(e)
   uint32_t idesc_qk;       // negate-A set when scale < 0
   uint32_t idesc_pv;
@@ -135,12 +138,18 @@ struct Params {
 struct Unit {
   int b, h, q0;
   int kv;                  // valid keys of this batch entry (kv_lens clamped to [0, Sk])
-  int n;                   // K tiles the unit needs (0: no valid key for any row)
+  int j0;                  // first K tile of the unit
+  int n;                   // K tiles the unit processes (0: no valid key for any row)
+  int split;               // key range index (split mode)
 };
 
 template <bool CAUSAL>
-__device__ __forceinline__ Unit decode_unit(const Params& p, int t) {
+__device__ __forceinline__ Unit decode_unit(const Params& p, int t_in) {
   Unit u;
+  // split mode: the key tiles of a (b, h, query tile) are cut into num_splits
+  // contiguous ranges, consecutive units
+  u.split = t_in % p.num_splits;
+  const int t = t_in / p.num_splits;
   const int bh_count = p.B * p.H;
   int qt, bh;
   if (CAUSAL) {  // longest units first: query blocks from the end of the sequence
@@ -158,7 +167,9 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int t) {
   u.kv = kv;
   int lim = kv;
   if (CAUSAL) lim = min(lim, min(u.q0 + kBQ, p.Sq));  // last row of the tile + 1
-  u.n = (lim + kBK - 1) / kBK;
+  const int n_all = (lim + kBK - 1) / kBK;
+  u.j0 = u.split * n_all / p.num_splits;
+  u.n = (u.split + 1) * n_all / p.num_splits - u.j0;
   return u;
 }
 
@@ -394,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const CUtensorMap* m = sel ? &map_v : &map_k;
             for (int c = 0; c < G::kChunks; ++c)
               tma_load_4d_hint(base + G::kOffRing + slot * G::kTileBytes + c * G::kChunkBytes, m, full, c * 64,
-                               j * kBK, u.h, u.b, pol_keep);
+                               (u.j0 + j) * kBK, u.h, u.b, pol_keep);
             ++ring;
           }
         }
@@ -529,12 +540,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row = u.q0 + r;
       const size_t row_index = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq) + row;
       uint16_t* o_dst = p.o + row_index * D + (D / 2) * half;
+      // split mode: this key range's partial row
+      const size_t prow = static_cast<size_t>(u.split) * p.B * p.H * static_cast<size_t>(p.Sq) + row_index;
+      float* op_dst = (p.o_part != nullptr) ? p.o_part + prow * D + (D / 2) * half : nullptr;
       if (u.n == 0) {  // no valid key for any row of this unit: O = 0, LSE = -inf
         if (row < p.Sq) {
-          uint4* dst = reinterpret_cast<uint4*>(o_dst);
+          if (op_dst == nullptr) {
+            uint4* dst = reinterpret_cast<uint4*>(o_dst);
 #pragma unroll
-          for (int q = 0; q < D / 16; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
-          if (half == 0) p.lse[row_index] = -INFINITY;
+            for (int q = 0; q < D / 16; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+            if (half == 0) p.lse[row_index] = -INFINITY;
+          } else {
+            float4* dst = reinterpret_cast<float4*>(op_dst);
+#pragma unroll
+            for (int q = 0; q < D / 8; ++q) dst[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (half == 0) p.lse_part[prow] = -INFINITY;
+          }
         }
         continue;
       }
@@ -546,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b = tcount & 1u;
         const uint32_t use = tcount >> 1;
         const uint32_t bar_pf = bar_p_free0 + 8 * b;
-        const int k0 = j * kBK;
+        const int k0 = (u.j0 + j) * kBK;
         const bool masked = (k0 + kBK > u.kv) || (CAUSAL && k0 + kBK - 1 > u.q0);
         int climit = u.kv - k0;  // columns >= climit of the tile are masked for this row
         if (CAUSAL) climit = min(climit, row - k0 + 1);
@@ -660,22 +681,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float l_row = l + xch.xsum[half ^ 1][r];
       const bool has_key = l_row > 0.0f;
       const float inv_l = has_key ? 1.0f / l_row : 0.0f;
+      const float lse_row = has_key ? (m_used + log2f(l_row)) * kLn2 : -INFINITY;
 #pragma unroll
       for (int q = 0; q < D / 64; ++q) {
         uint32_t o[32];
         tmem_ld_32x32b_x32(tO + q * 32, o);
         tmem_ld_wait_x32(o);
         if (row < p.Sq) {
-          uint32_t w[16];
+          if (op_dst == nullptr) {
+            uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = has_key ? pack_bf16x2(u2f(o[2 * e]) * inv_l, u2f(o[2 * e + 1]) * inv_l) : 0u;
-          uint4* dst = reinterpret_cast<uint4*>(o_dst + q * 32);
+            for (int e = 0; e < 16; ++e)
+              w[e] = has_key ? pack_bf16x2(u2f(o[2 * e]) * inv_l, u2f(o[2 * e + 1]) * inv_l) : 0u;
+            uint4* dst = reinterpret_cast<uint4*>(o_dst + q * 32);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          } else {  // normalised fp32 partial output
+            float4* dst = reinterpret_cast<float4*>(op_dst + q * 32);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[e] = has_key ? make_float4(u2f(o[4 * e]) * inv_l, u2f(o[4 * e + 1]) * inv_l,
+                                             u2f(o[4 * e + 2]) * inv_l, u2f(o[4 * e + 3]) * inv_l)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
         }
       }
-      if (row < p.Sq && half == 0) p.lse[row_index] = has_key ? (m_used + log2f(l_row)) * kLn2 : -INFINITY;
+      if (row < p.Sq && half == 0) {
+        if (op_dst == nullptr) p.lse[row_index] = lse_row;
+        else p.lse_part[prow] = lse_row;
+      }
       // The next unit's first PV overwrites O only after every softmax warp has
       // arrived on p_full for it, which each warp does after this epilogue.
       tc_fence_before_sync();
@@ -790,31 +824,113 @@ attn_status launch(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CUtens
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-}  // namespace
+// LSE merge of key-range partial results: one warp per row, each lane owns
+// D/32 consecutive columns.  M = max_s LSE_s, w_s = 2^((LSE_s - M) log2 e),
+// O = sum_s w_s O_s / sum_s w_s, LSE = M + ln sum_s w_s; all-empty rows give
+// O = 0 and LSE = -inf.
+template <int D>
+__global__ void __launch_bounds__(256) lse_merge_kernel(const float* __restrict__ o_parts,
+                                                        const float* __restrict__ lse_parts, int n_parts,
+                                                        long long rows, uint16_t* __restrict__ o,
+                                                        float* __restrict__ lse) {
+  constexpr int C = D / 32;
+  constexpr float kLog2e = 1.4426950408889634f;
+  const int lane = threadIdx.x & 31;
+  const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long r = warp_id; r < rows; r += n_warps) {
+    float m = -INFINITY;
+    for (int s = 0; s < n_parts; ++s) m = fmaxf(m, __ldg(lse_parts + s * rows + r));
+    float acc[C];
+#pragma unroll
+    for (int e = 0; e < C; ++e) acc[e] = 0.0f;
+    float total = 0.0f;
+    if (m != -INFINITY) {
+      for (int s = 0; s < n_parts; ++s) {
+        const float ls = __ldg(lse_parts + s * rows + r);
+        if (ls == -INFINITY) continue;
+        const float w = ex2_approx((ls - m) * kLog2e);
+        total += w;
+        const float* src = o_parts + (s * rows + r) * D + lane * C;
+        if constexpr (C == 4) {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(src));
+          acc[0] = fmaf(w, x.x, acc[0]);
+          acc[1] = fmaf(w, x.y, acc[1]);
+          acc[2] = fmaf(w, x.z, acc[2]);
+          acc[3] = fmaf(w, x.w, acc[3]);
+        } else {
+          const float2 x = __ldg(reinterpret_cast<const float2*>(src));
+          acc[0] = fmaf(w, x.x, acc[0]);
+          acc[1] = fmaf(w, x.y, acc[1]);
+        }
+      }
+    }
+    const float inv = total > 0.0f ? 1.0f / total : 0.0f;
+    uint16_t* dst = o + r * D + lane * C;
+    if constexpr (C == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc[0] * inv, acc[1] * inv),
+                                                  pack_bf16x2(acc[2] * inv, acc[3] * inv));
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    }
+    if (lane == 0) lse[r] = total > 0.0f ? m + logf(total) : -INFINITY;
+  }
+}
 
-extern "C" {
+attn_status launch_merge(DeviceInfo& dev, const float* o_parts, const float* lse_parts, int n_parts, long long rows,
+                         int D, void* o, float* lse, cudaStream_t s) {
+  if (rows == 0) return ATTN_OK;
+  const long long warps_needed = rows;
+  long long blocks = (warps_needed + 7) / 8;  // 8 warps per block
+  const long long max_blocks = static_cast<long long>(dev.num_sms) * 8;
+  if (blocks > max_blocks) blocks = max_blocks;
+  if (D == 64)
+    lse_merge_kernel<64><<<static_cast<int>(blocks), 256, 0, s>>>(o_parts, lse_parts, n_parts, rows,
+                                                                   static_cast<uint16_t*>(o), lse);
+  else
+    lse_merge_kernel<128><<<static_cast<int>(blocks), 256, 0, s>>>(o_parts, lse_parts, n_parts, rows,
+                                                                    static_cast<uint16_t*>(o), lse);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
 
-attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk,
-                     int D, float scale, int causal, const int32_t* kv_lens, attn_stream_t stream) {
+constexpr int kMaxSplits = 128;
+
+size_t round_up_256(size_t x) { return (x + 255) / 256 * 256; }
+
+// Bytes of the split-mode workspace: partial O (fp32) then partial LSE (fp32).
+size_t splitkv_bytes(int B, int H, int Sq, int D, int num_splits, size_t* lse_offset) {
+  const size_t rows = static_cast<size_t>(B) * H * Sq;
+  const size_t o_bytes = round_up_256(static_cast<size_t>(num_splits) * rows * D * sizeof(float));
+  if (lse_offset != nullptr) *lse_offset = o_bytes;
+  return o_bytes + round_up_256(static_cast<size_t>(num_splits) * rows * sizeof(float));
+}
+
+attn_status check_args(const void* q, const void* k, const void* v, const void* o, const float* lse, int B, int H,
+                       int Sq, int Sk, int D, float scale, const int32_t* kv_lens, int num_splits) {
   if (B < 0 || H < 0 || Sq < 0 || Sk < 0) return ATTN_ERR_SHAPE;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED_D;
   if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
+  if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_SHAPE;
   if (B == 0 || H == 0 || Sq == 0) return ATTN_OK;
   if (q == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_NULLPTR;
   if (Sk > 0 && (k == nullptr || v == nullptr)) return ATTN_ERR_NULLPTR;
   if (!aligned(q, 16) || !aligned(o, 16) || !aligned(lse, 4)) return ATTN_ERR_ALIGN;
   if (Sk > 0 && (!aligned(k, 16) || !aligned(v, 16))) return ATTN_ERR_ALIGN;
   if (kv_lens != nullptr && !aligned(kv_lens, 4)) return ATTN_ERR_ALIGN;
-  // TMA strides must stay below 2^40 bytes; work units must fit an int.
+  // TMA strides must stay below 2^40 bytes; work units (whole rounds of the
+  // persistent loop included) must fit an int.
   const uint64_t max_s = static_cast<uint64_t>(Sq > Sk ? Sq : Sk);
   if (static_cast<uint64_t>(H) * max_s * D * 2 >= (1ull << 40)) return ATTN_ERR_SHAPE;
   const uint64_t n_qtiles = (static_cast<uint64_t>(Sq) + kBQ - 1) / kBQ;
-  if (static_cast<uint64_t>(B) * H * n_qtiles > 0x7fff0000ull) return ATTN_ERR_SHAPE;  // + room for whole rounds
+  if (static_cast<uint64_t>(B) * H * n_qtiles * num_splits > 0x7fff0000ull) return ATTN_ERR_SHAPE;
+  return ATTN_OK;
+}
 
-  DeviceInfo* dev = nullptr;
-  attn_status st = device_info(&dev);
-  if (st != ATTN_OK) return st;
-
+// Launches the attention kernel.  o_part == nullptr: final bf16 O and LSE;
+// otherwise num_splits key ranges write fp32 partials to o_part / lse_part.
+attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                        int H, int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens, int num_splits,
+                        float* o_part, float* lse_part, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, B, H, Sq, D)) return ATTN_ERR_CUDA;
   if (Sk > 0) {
@@ -823,7 +939,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
     mk = mq;
     mv = mq;
   }
-
+  const uint64_t n_qtiles = (static_cast<uint64_t>(Sq) + kBQ - 1) / kBQ;
   Params p;
   p.o = static_cast<uint16_t*>(o);
   p.lse = lse;
@@ -833,17 +949,72 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   p.Sq = Sq;
   p.Sk = Sk;
   p.n_qtiles = static_cast<int>(n_qtiles);
-  p.total_units = static_cast<int>(static_cast<uint64_t>(B) * H * n_qtiles);
+  p.num_splits = num_splits;
+  p.total_units = static_cast<int>(static_cast<uint64_t>(B) * H * n_qtiles * num_splits);
+  p.o_part = o_part;
+  p.lse_part = lse_part;
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634);
   p.idesc_qk = idesc_bf16_f32(kBQ, kBK, scale < 0.0f, false);
   p.idesc_pv = idesc_bf16_f32(kBQ, D, false, true);
   p.wait_limit_ns = kWaitLimitNs;
-
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (D == 64) {
-    return causal ? launch<64, true>(*dev, 0, mq, mk, mv, p, s) : launch<64, false>(*dev, 1, mq, mk, mv, p, s);
+    return causal ? launch<64, true>(dev, 0, mq, mk, mv, p, s) : launch<64, false>(dev, 1, mq, mk, mv, p, s);
   }
-  return causal ? launch<128, true>(*dev, 2, mq, mk, mv, p, s) : launch<128, false>(*dev, 3, mq, mk, mv, p, s);
+  return causal ? launch<128, true>(dev, 2, mq, mk, mv, p, s) : launch<128, false>(dev, 3, mq, mk, mv, p, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq, int Sk,
+                     int D, float scale, int causal, const int32_t* kv_lens, attn_stream_t stream) {
+  attn_status st = check_args(q, k, v, o, lse, B, H, Sq, Sk, D, scale, kv_lens, 1);
+  if (st != ATTN_OK || B == 0 || H == 0 || Sq == 0) return st;
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  return run_forward(*dev, q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, 1, nullptr, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t attn_fwd_splitkv_workspace_size(int B, int H, int Sq, int D, int num_splits) {
+  if (B < 0 || H < 0 || Sq < 0 || (D != 64 && D != 128) || num_splits < 1 || num_splits > kMaxSplits) return 0;
+  return splitkv_bytes(B, H, Sq, D, num_splits, nullptr);
+}
+
+attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
+                             int Sk, int D, float scale, int causal, const int32_t* kv_lens, int num_splits,
+                             void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  attn_status st = check_args(q, k, v, o, lse, B, H, Sq, Sk, D, scale, kv_lens, num_splits);
+  if (st != ATTN_OK || B == 0 || H == 0 || Sq == 0) return st;
+  size_t lse_off = 0;
+  const size_t need = splitkv_bytes(B, H, Sq, D, num_splits, &lse_off);
+  if (workspace == nullptr) return ATTN_ERR_NULLPTR;
+  if (!aligned(workspace, 256)) return ATTN_ERR_ALIGN;
+  if (workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + lse_off);
+  st = run_forward(*dev, q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, num_splits, o_part, lse_part, s);
+  if (st != ATTN_OK) return st;
+  return launch_merge(*dev, o_part, lse_part, num_splits, static_cast<long long>(B) * H * Sq, D, o, lse, s);
+}
+
+attn_status attn_lse_merge(const float* o_parts, const float* lse_parts, int num_parts, void* o, float* lse,
+                           long long rows, int D, attn_stream_t stream) {
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED_D;
+  if (num_parts < 1 || rows < 0) return ATTN_ERR_SHAPE;
+  if (rows == 0) return ATTN_OK;
+  if (o_parts == nullptr || lse_parts == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_NULLPTR;
+  if (!aligned(o_parts, 16) || !aligned(lse_parts, 4) || !aligned(o, 8) || !aligned(lse, 4)) return ATTN_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  attn_status st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  return launch_merge(*dev, o_parts, lse_parts, num_parts, rows, D, o, lse, reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* attn_get_error_string(attn_status status) {
@@ -851,12 +1022,13 @@ const char* attn_get_error_string(attn_status status) {
     case ATTN_OK: return "ok";
     case ATTN_ERR_NULLPTR: return "a required pointer is NULL";
     case ATTN_ERR_ALIGN: return "q/k/v/o must be 16-byte aligned, lse and kv_lens 4-byte aligned";
-    case ATTN_ERR_SHAPE: return "invalid or too large B/H/Sq/Sk";
+    case ATTN_ERR_SHAPE: return "invalid or too large B/H/Sq/Sk/num_splits";
     case ATTN_ERR_UNSUPPORTED_D: return "head dimension D must be 64 or 128";
     case ATTN_ERR_SCALE: return "scale must be finite";
     case ATTN_ERR_CUDA: return "a CUDA call failed";
     case ATTN_ERR_DEVICE_TIMEOUT: return "a device-side wait gave up (kernel aborted its work)";
     case ATTN_ERR_UNSUPPORTED_DEVICE: return "the current device is not an sm_103 (GB300) GPU";
+    case ATTN_ERR_WORKSPACE: return "workspace smaller than attn_fwd_splitkv_workspace_size()";
   }
   return "unknown status";
 }

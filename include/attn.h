@@ -24,12 +24,14 @@
  *
  * All entry points are host functions; device pointers are plain CUDA device
  * (or managed) addresses on the CURRENT device.  The caller allocates and owns
- * every buffer.  The library allocates no device memory: its only device state
- * is one status word per device, a static __device__ variable in the library.
+ * every buffer (including the split-KV workspace).  The library allocates no
+ * device memory: its only device state is one status word per device, a
+ * static __device__ variable in the library.
  */
 #ifndef EXACT_ATTENTION_86_GB300_ATTN_H
 #define EXACT_ATTENTION_86_GB300_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -48,7 +50,8 @@ typedef enum attn_status {
   ATTN_ERR_SCALE = 5,              /* scale is NaN or infinite                          */
   ATTN_ERR_CUDA = 6,               /* a CUDA runtime/driver call failed                 */
   ATTN_ERR_DEVICE_TIMEOUT = 7,     /* a kernel wait gave up (see attn_check_device_status) */
-  ATTN_ERR_UNSUPPORTED_DEVICE = 8  /* the current device is not sm_103 (GB300)          */
+  ATTN_ERR_UNSUPPORTED_DEVICE = 8, /* the current device is not sm_103 (GB300)          */
+  ATTN_ERR_WORKSPACE = 9           /* workspace smaller than the size the call needs     */
 } attn_status;
 
 /*
@@ -79,6 +82,52 @@ typedef enum attn_status {
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
                      int Sk, int D, float scale, int causal, const int32_t* kv_lens, attn_stream_t stream);
 
+/*
+ * attn_fwd_splitkv — the same forward with the keys of every (b, h, 128-row
+ * query block) cut into `num_splits` contiguous ranges of 128-key tiles that
+ * run as separate units of work, then merged (split-KV).  It raises the
+ * parallelism of shapes with few query blocks (short Sq, few heads, decode)
+ * at the cost of a workspace and one merge pass.
+ *
+ * Each range produces the normalised partial output O_s = sum p_j v_j / sum p_j
+ * and LSE_s over its keys (the tile loop of "Attention softmax fusion",
+ * section "The tile loop", run on the range); the merge applies the running
+ * max / normaliser correction once per range (see attn_lse_merge).
+ *
+ * Arguments as attn_fwd, plus:
+ * num_splits       1 .. 128.  Ranges are whole tiles, so a range may be empty;
+ *                  an empty range contributes nothing.
+ * workspace        device memory, 256-byte aligned, caller-owned, at least
+ *                  attn_fwd_splitkv_workspace_size(B, H, Sq, D, num_splits)
+ *                  bytes (else ATTN_ERR_WORKSPACE).  Its contents on entry are
+ *                  irrelevant; the call overwrites it.  Calls that use one
+ *                  workspace must not overlap on the GPU.
+ * Two kernels are launched on `stream`; the call never synchronises.
+ */
+size_t attn_fwd_splitkv_workspace_size(int B, int H, int Sq, int D, int num_splits);
+
+attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
+                             int Sk, int D, float scale, int causal, const int32_t* kv_lens, int num_splits,
+                             void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * attn_lse_merge — combine attention results computed over disjoint key sets
+ * into the result over their union ("Kernel Fusion and the Memory Wall",
+ * section "FlashAttention: avoid the full score matrix": rescale each part by
+ * exp(m - m') so that all share one denominator; here m is each part's LSE):
+ *
+ *   M = max_s LSE_s,  w_s = exp(LSE_s - M),  O = sum_s w_s O_s / sum_s w_s,
+ *   LSE = M + ln sum_s w_s;   every LSE_s = -inf  ->  O = +0.0, LSE = -inf.
+ *
+ * o_parts    fp32 [num_parts][rows][D] normalised partial outputs, device, 16-B aligned.
+ * lse_parts  fp32 [num_parts][rows] partial LSE (natural log), device, 4-B aligned.
+ * o          bf16 [rows][D] output, device, 8-B aligned.   lse: fp32 [rows] output.
+ * rows >= 0, num_parts >= 1, D in {64, 128}.  Asynchronous on `stream`.
+ * This is the exchange step a key-sharded (context-parallel) forward needs.
+ */
+attn_status attn_lse_merge(const float* o_parts, const float* lse_parts, int num_parts, void* o, float* lse,
+                           long long rows, int D, attn_stream_t stream);
+
 /* Static, human-readable description of a status code. */
 const char* attn_get_error_string(attn_status status);
 
@@ -105,7 +154,7 @@ attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream);
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 1
+#define ATTN_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

@@ -19,6 +19,8 @@ Contents:
   from "Attention softmax fusion", section "The tile loop", and "Kernel Fusion
   and the Memory Wall", section "FlashAttention: avoid the full score matrix".
   It exists only so the tests can pin the materialised form against it.
+* ``merge.lse_merge`` — the combination of per-key-range partial results
+  (normalised partial output and LSE of each range) into the whole-row result.
 
 The oracle shares no code with the CUDA path: it reads float64 NumPy arrays
 and nothing else.
@@ -26,3 +28,4 @@ and nothing else.
 
 from .attention import attention_ref, attention_rows, valid_key_count  # noqa: F401
 from .online import online_softmax_attention  # noqa: F401
+from .merge import lse_merge  # noqa: F401

@@ -49,7 +49,7 @@ def test_abi_version(lib):
 
 
 def test_error_strings(lib):
-    for code in range(9):
+    for code in range(10):
         assert attn.attn_get_error_string(code) not in ("", "unknown status")
     assert attn.attn_get_error_string(99) == "unknown status"
 
@@ -115,3 +115,49 @@ def test_missing_library_is_an_error(monkeypatch, tmp_path):
     monkeypatch.setattr(attn, "_lib", None)
     with pytest.raises(RuntimeError):
         attn.lib()
+
+
+W = 1 << 24  # a 256-byte-aligned dummy workspace address
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(ns=0), attn.ATTN_ERR_SHAPE),
+    (dict(ns=129), attn.ATTN_ERR_SHAPE),
+    (dict(ws=0), attn.ATTN_ERR_NULLPTR),
+    (dict(ws=W + 128), attn.ATTN_ERR_ALIGN),
+    (dict(wsb=1024), attn.ATTN_ERR_WORKSPACE),
+    (dict(D=80), attn.ATTN_ERR_UNSUPPORTED_D),
+    (dict(Sq=0), attn.ATTN_OK),
+])
+def test_splitkv_argument_checks(lib, args, code):
+    a = dict(B=2, H=2, Sq=256, Sk=512, D=128, ns=4, ws=W, wsb=None)
+    a.update(args)
+    need = attn.attn_fwd_splitkv_workspace_size(a["B"], a["H"], a["Sq"], a["D"], a["ns"]) if a["D"] in (64, 128) else 0
+    wsb = need if a["wsb"] is None else a["wsb"]
+    st = attn.attn_fwd_splitkv(A, A, A, A, A, a["B"], a["H"], a["Sq"], a["Sk"], a["D"], 0.1, 0, None, a["ns"],
+                               a["ws"], wsb, None)
+    assert st == code
+
+
+def test_splitkv_workspace_size(lib):
+    # fp32 partial O and LSE for every split, each part rounded up to 256 bytes
+    rows = 2 * 3 * 300
+    o_bytes = -(-(5 * rows * 128 * 4) // 256) * 256
+    l_bytes = -(-(5 * rows * 4) // 256) * 256
+    assert attn.attn_fwd_splitkv_workspace_size(2, 3, 300, 128, 5) == o_bytes + l_bytes
+    assert attn.attn_fwd_splitkv_workspace_size(2, 3, 300, 96, 5) == 0
+    assert attn.attn_fwd_splitkv_workspace_size(2, 3, 300, 128, 0) == 0
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(D=32), attn.ATTN_ERR_UNSUPPORTED_D),
+    (dict(n=0), attn.ATTN_ERR_SHAPE),
+    (dict(rows=-1), attn.ATTN_ERR_SHAPE),
+    (dict(op=0), attn.ATTN_ERR_NULLPTR),
+    (dict(op=A + 4), attn.ATTN_ERR_ALIGN),
+    (dict(rows=0), attn.ATTN_OK),
+])
+def test_merge_argument_checks(lib, args, code):
+    a = dict(op=A, lp=A, n=3, o=A, lse=A, rows=100, D=128)
+    a.update(args)
+    assert attn.attn_lse_merge(a["op"], a["lp"], a["n"], a["o"], a["lse"], a["rows"], a["D"], None) == code

@@ -330,3 +330,52 @@ def test_against_torch_sdpa_key_padding():
     t = torch.nn.functional.scaled_dot_product_attention(
         torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v), attn_mask=mask, scale=0.25)
     np.testing.assert_allclose(O, t.numpy(), rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# LSE merge of key-range partial results (split-KV / context parallel)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("cuts", [[0, 13, 29], [0, 1, 2, 29], [0, 29], [0, 10, 10, 20, 29]])
+def test_merge_of_key_ranges_is_whole_row_attention(causal, cuts):
+    from oracle import lse_merge
+    B, H, Sq, Sk, D = 1, 2, 17, 29, 6
+    q = _rand((B, H, Sq, D), 131)
+    k = _rand((B, H, Sk, D), 132)
+    v = _rand((B, H, Sk, D), 133)
+    scale = 0.45
+    O, L = attention_ref(q, k, v, scale, causal=causal)
+    parts_o, parts_l = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        # keys outside [a, b) are masked for this range: shift causality by giving
+        # the oracle only the range's keys and the row positions relative to it
+        o_s = np.zeros((B, H, Sq, D))
+        l_s = np.full((B, H, Sq), -np.inf)
+        for h in range(H):
+            for i in range(Sq):
+                valid = [j for j in range(a, b) if (not causal or j <= i)]
+                if not valid:
+                    continue
+                s = scale * (k[0, h, valid] @ q[0, h, i])
+                mx = s.max()
+                p = np.exp(s - mx)
+                o_s[0, h, i] = p @ v[0, h, valid] / p.sum()
+                l_s[0, h, i] = mx + math.log(p.sum())
+        parts_o.append(o_s.reshape(-1, D))
+        parts_l.append(l_s.reshape(-1))
+    Om, Lm = lse_merge(np.stack(parts_o), np.stack(parts_l))
+    np.testing.assert_allclose(Om, O.reshape(-1, D), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(Lm, L.reshape(-1), rtol=1e-12, atol=1e-12)
+
+
+def test_merge_of_empty_sets():
+    from oracle import lse_merge
+    o = np.array([[[1.0, 2.0]], [[5.0, 6.0]]])
+    l = np.array([[-np.inf], [-np.inf]])
+    Om, Lm = lse_merge(o, l)
+    assert np.all(Om == 0.0) and Lm[0] == -np.inf
+    l2 = np.array([[-np.inf], [0.3]])
+    Om, Lm = lse_merge(o, l2)       # one empty set: the other passes through unchanged
+    np.testing.assert_array_equal(Om, o[1])
+    assert Lm[0] == 0.3
