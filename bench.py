@@ -218,6 +218,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits", type=int, default=0,
+                    help="use the split-KV forward with this many key ranges (0: the plain forward)")
     args = ap.parse_args()
 
     from exact_attention_86_gb300 import workloads
@@ -256,9 +258,19 @@ def main():
     sptr = stream.cuda_stream
     kv_ptr = kvd.data_ptr() if kvd is not None else None
 
+    ws = None
+    if args.splits > 0:
+        ws_bytes = attn.attn_fwd_splitkv_workspace_size(w.B, w.H, w.Sq, w.D, args.splits)
+        ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+
     def step():
-        st = attn.attn_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                           w.B, w.H, w.Sq, w.Sk, w.D, w.scale, int(w.causal), kv_ptr, sptr)
+        if ws is None:
+            st = attn.attn_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                               w.B, w.H, w.Sq, w.Sk, w.D, w.scale, int(w.causal), kv_ptr, sptr)
+        else:
+            st = attn.attn_fwd_splitkv(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                       w.B, w.H, w.Sq, w.Sk, w.D, w.scale, int(w.causal), kv_ptr, args.splits,
+                                       ws.data_ptr(), ws.numel(), sptr)
         if st != attn.ATTN_OK:
             raise attn.AttnError(st, "attn_fwd")
 
@@ -370,13 +382,14 @@ def main():
                        "inputs": f"bf16 N(0,{(w.std if args.draw == 0 else w.second_std) ** 2:g}) seed {w.seed}",
                        "l2": "no flush: each step reads 192 MiB of Q/K/V and writes 64 MiB of O, more than the "
                              "129 MB L2",
-                       "parallelism": f"weak: {world} replica(s) of the workload, one per GPU"},
+                       "parallelism": f"weak: {world} replica(s) of the workload, one per GPU",
+                       "splits": args.splits},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "clocks": clocks,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if args.splits > 0 else 1),
             "pct_of_peak": 100.0 * value / world / peak,
         }
         print(json.dumps(line), flush=True)

@@ -418,6 +418,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           wait_phase_drain(bar_kv_full0 + 8 * s, (last / G::kSlots) & 1u);
         }
       }
+      // The issuers release slots and the Q buffer with tcgen05.commit, whose
+      // mbarrier arrivals land asynchronously; nothing else waits for the last
+      // ones.  Wait for them here so that none can land after this CTA's shared
+      // memory is gone.
+      if (qcount > 0) wait_phase_drain(bar_q_empty, (qcount - 1) & 1u);
+      for (uint32_t s = 0; s < (uint32_t)G::kSlots && s < ring; ++s) {
+        const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);
+        wait_phase_drain(bar_kv_empty0 + 8 * s, (last / G::kSlots) & 1u);
+      }
     }
     __syncwarp();
   } else if (warp == kWarpQK) {
@@ -713,6 +722,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The next unit's first PV overwrites O only after every softmax warp has
       // arrived on p_full for it, which each warp does after this epilogue.
       tc_fence_before_sync();
+    }
+    // The last p_free arrivals (commits of the last two PVs) land
+    // asynchronously and nothing else waits for them: wait before exiting.
+    for (uint32_t back = 1; back <= 2 && back <= tcount; ++back) {
+      const uint32_t tp = tcount - back;
+      wait_phase_drain(bar_p_free0 + 8 * (tp & 1u), (tp >> 1) & 1u);
     }
   }
 

@@ -74,6 +74,9 @@ WORKLOADS = {
     "s8192_d128_causal": Workload("s8192_d128_causal", 2, 16, 8192, 8192, 128, True, seed=3,
                                   second_std=2.0),
     "s32768_d128_causal": Workload("s32768_d128_causal", 1, 8, 32768, 32768, 128, True, seed=4),
+    # one 128-row query block per head against a long key sequence (the shape
+    # split-KV is for; not one of the five headline workloads)
+    "q128_k32768_d128": Workload("q128_k32768_d128", 1, 8, 128, 32768, 128, False, seed=5),
 }
 
 HEADLINE = "s8192_d128"
