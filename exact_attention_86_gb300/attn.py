@@ -36,6 +36,10 @@ SIGNATURES = {
     "attn_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "attn_fwd_varlen": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                                       ctypes.c_int, ctypes.c_void_p]),
     "attn_fwd_splitkv_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                           ctypes.c_int]),
     "attn_fwd_splitkv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -83,6 +87,13 @@ def lib():
 def attn_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
              scale: float, causal: int, kv_lens: Optional[int], stream: Optional[int]) -> int:
     return lib().attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, stream)
+
+
+def attn_fwd_varlen(q: int, k: int, v: int, o: int, lse: int, cu_q: int, cu_k: int, batch: int,
+                    max_seqlen_q: int, total_q: int, total_k: int, H: int, D: int, scale: float, causal: int,
+                    stream: Optional[int]) -> int:
+    return lib().attn_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, batch, max_seqlen_q, total_q, total_k, H, D, scale,
+                                 int(causal), stream)
 
 
 def attn_fwd_splitkv_workspace_size(B: int, H: int, Sq: int, D: int, num_splits: int) -> int:
@@ -164,6 +175,40 @@ def forward_splitkv(q, k, v, num_splits: int, scale: Optional[float] = None, cau
                               workspace.data_ptr(), workspace.numel() * workspace.element_size(), stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_splitkv")
+    return out, lse
+
+
+def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, scale: Optional[float] = None,
+                   causal: bool = False):
+    """Packed variable-length forward on torch CUDA tensors: ``q [total_q, H, D]``,
+    ``k``/``v [total_k, H, D]`` bf16, ``cu_seqlens_q``/``cu_seqlens_k`` int32
+    ``[batch + 1]`` on the same device.  Returns ``(o [total_q, H, D], lse [H, total_q])``."""
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+            raise ValueError(f"{name} must be a contiguous 3-d bf16 CUDA tensor")
+    total_q, H, D = q.shape
+    total_k = k.shape[0]
+    if tuple(k.shape) != (total_k, H, D) or tuple(v.shape) != (total_k, H, D):
+        raise ValueError("k and v must be [total_k, H, D] with q's H, D")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or t.device != q.device or not t.is_contiguous() or t.dim() != 1:
+            raise ValueError(f"{name} must be a contiguous int32 tensor on q's device")
+    batch = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != batch + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = torch.empty((total_q, H, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                             cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), batch, int(max_seqlen_q), total_q,
+                             total_k, H, D, float(scale), int(bool(causal)), stream)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_varlen")
     return out, lse
 
 

@@ -129,6 +129,13 @@ struct Params {
   int total_units;
   float* o_part;           // split mode: fp32 [num_splits][B*H*Sq][D] normalised partial outputs
   float* lse_part;         //             fp32 [num_splits][B*H*Sq] partial LSE; nullptr = write o/lse
+  // packed variable-length mode (cu_q != nullptr): q/o [total_q, H, D], k/v
+  // [total_k, H, D], lse [H, total_q]; sequence b owns query tokens
+  // [cu_q[b], cu_q[b+1]) and key tokens [cu_k[b], cu_k[b+1]); B = batch and
+  // Sq = the largest query length (it sizes the grid)
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int total_q, total_k;
   float c;                 // |scale| * log2(e)
   uint32_t idesc_qk;       // negate-A set when scale < 0
   uint32_t idesc_pv;
@@ -136,7 +143,9 @@ struct Params {
 };
 
 struct Unit {
-  int b, h, q0;
+  int b, h, q0;            // q0: position of the unit's first query row within its sequence
+  int rows;                // query rows of the unit that exist (<= 128; 0: nothing to do)
+  int q_tok0, k_tok0;      // packed mode: token index of the first query row / first key
   int kv;                  // valid keys of this batch entry (kv_lens clamped to [0, Sk])
   int j0;                  // first K tile of the unit
   int n;                   // K tiles the unit processes (0: no valid key for any row)
@@ -162,12 +171,29 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int t_in) {
   u.b = bh / p.H;
   u.h = bh % p.H;
   u.q0 = qt * kBQ;
-  int kv = p.Sk;
-  if (p.kv_lens != nullptr) kv = min(max(__ldg(p.kv_lens + u.b), 0), p.Sk);
+  int kv, q_len;
+  if (p.cu_q != nullptr) {
+    // packed sequences: offsets clamped so that any content stays in bounds
+    const int qs = min(max(__ldg(p.cu_q + u.b), 0), p.total_q);
+    const int qe = min(max(__ldg(p.cu_q + u.b + 1), qs), p.total_q);
+    const int ks = min(max(__ldg(p.cu_k + u.b), 0), p.total_k);
+    const int ke = min(max(__ldg(p.cu_k + u.b + 1), ks), p.total_k);
+    q_len = qe - qs;
+    kv = ke - ks;
+    u.q_tok0 = qs + u.q0;
+    u.k_tok0 = ks;
+  } else {
+    q_len = p.Sq;
+    kv = p.Sk;
+    if (p.kv_lens != nullptr) kv = min(max(__ldg(p.kv_lens + u.b), 0), p.Sk);
+    u.q_tok0 = 0;
+    u.k_tok0 = 0;
+  }
+  u.rows = max(min(kBQ, q_len - u.q0), 0);
   u.kv = kv;
   int lim = kv;
-  if (CAUSAL) lim = min(lim, min(u.q0 + kBQ, p.Sq));  // last row of the tile + 1
-  const int n_all = (lim + kBK - 1) / kBK;
+  if (CAUSAL) lim = min(lim, u.q0 + u.rows);  // last row of the tile + 1
+  const int n_all = u.rows > 0 ? (lim + kBK - 1) / kBK : 0;
   u.j0 = u.split * n_all / p.num_splits;
   u.n = (u.split + 1) * n_all / p.num_splits - u.j0;
   return u;
@@ -391,9 +417,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u.n == 0) continue;
         if (!wait_phase(bar_q_empty, (qcount & 1u) ^ 1u, abort_flag, kSiteQEmpty, limit)) { ok = false; break; }
         mbar_arrive_expect_tx(bar_q_full, G::kTileBytes);
+        // padded maps are (D, S, H, B); packed maps are (D, H, tokens, 1)
+        const bool packed = p.cu_q != nullptr;
         for (int c = 0; c < G::kChunks; ++c)
-          tma_load_4d_hint(base + G::kOffQ + c * G::kChunkBytes, &map_q, bar_q_full, c * 64, u.q0, u.h, u.b,
-                           pol_once);
+          tma_load_4d_hint(base + G::kOffQ + c * G::kChunkBytes, &map_q, bar_q_full, c * 64,
+                           packed ? u.h : u.q0, packed ? u.q_tok0 : u.h, packed ? 0 : u.b, pol_once);
         ++qcount;
         for (int j = 0; ok && j < u.n; ++j) {
           for (int sel = 0; sel < 2; ++sel) {  // K_j, then V_j
@@ -403,9 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t full = bar_kv_full0 + 8 * slot;
             mbar_arrive_expect_tx(full, G::kTileBytes);
             const CUtensorMap* m = sel ? &map_v : &map_k;
+            const int key0 = (u.j0 + j) * kBK;
             for (int c = 0; c < G::kChunks; ++c)
               tma_load_4d_hint(base + G::kOffRing + slot * G::kTileBytes + c * G::kChunkBytes, m, full, c * 64,
-                               (u.j0 + j) * kBK, u.h, u.b, pol_keep);
+                               packed ? u.h : key0, packed ? u.k_tok0 + key0 : u.h, packed ? 0 : u.b, pol_keep);
             ++ring;
           }
         }
@@ -546,19 +575,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int unit = unit_at<CAUSAL>(t);
         if (unit >= p.total_units) continue;
         const Unit u = decode_unit<CAUSAL>(p, unit);
-      const int row = u.q0 + r;
-      const size_t row_index = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq) + row;
+      const int row = u.q0 + r;     // position of this thread's query row within its sequence
+      const bool row_ok = r < u.rows;
+      size_t row_index, lse_index;  // row of O (in units of D elements) and index into lse
+      if (p.cu_q != nullptr) {      // packed: o [total_q, H, D], lse [H, total_q]
+        const size_t tok = static_cast<size_t>(u.q_tok0) + r;
+        row_index = tok * p.H + u.h;
+        lse_index = static_cast<size_t>(u.h) * p.total_q + tok;
+      } else {                      // padded: o [B, H, Sq, D], lse [B, H, Sq]
+        row_index = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq) + row;
+        lse_index = row_index;
+      }
       uint16_t* o_dst = p.o + row_index * D + (D / 2) * half;
-      // split mode: this key range's partial row
+      // split mode (padded only): this key range's partial row
       const size_t prow = static_cast<size_t>(u.split) * p.B * p.H * static_cast<size_t>(p.Sq) + row_index;
       float* op_dst = (p.o_part != nullptr) ? p.o_part + prow * D + (D / 2) * half : nullptr;
       if (u.n == 0) {  // no valid key for any row of this unit: O = 0, LSE = -inf
-        if (row < p.Sq) {
+        if (row_ok) {
           if (op_dst == nullptr) {
             uint4* dst = reinterpret_cast<uint4*>(o_dst);
 #pragma unroll
             for (int q = 0; q < D / 16; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
-            if (half == 0) p.lse[row_index] = -INFINITY;
+            if (half == 0) p.lse[lse_index] = -INFINITY;
           } else {
             float4* dst = reinterpret_cast<float4*>(op_dst);
 #pragma unroll
@@ -696,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t o[32];
         tmem_ld_32x32b_x32(tO + q * 32, o);
         tmem_ld_wait_x32(o);
-        if (row < p.Sq) {
+        if (row_ok) {
           if (op_dst == nullptr) {
             uint32_t w[16];
 #pragma unroll
@@ -715,8 +753,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (row < p.Sq && half == 0) {
-        if (op_dst == nullptr) p.lse[row_index] = lse_row;
+      if (row_ok && half == 0) {
+        if (op_dst == nullptr) p.lse[lse_index] = lse_row;
         else p.lse_part[prow] = lse_row;
       }
       // The next unit's first PV overwrites O only after every softmax warp has
@@ -820,6 +858,21 @@ bool make_map(CUtensorMap* m, const void* ptr, int B, int H, int S, int D) {
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Rank-4 map over a packed [tokens, H, D] tensor as (D, H, tokens, 1) with a
+// 64 x 1 x 128 box: the box lands in shared memory as the same 128 rows x 128 B
+// tile as the padded map's.  Token rows past the end read as zeros.
+bool make_map_packed(CUtensorMap* m, const void* ptr, int H, int total, int D) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
+  if (encode == nullptr) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total, 1};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)total * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int D, bool CAUSAL>
@@ -968,6 +1021,10 @@ attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const voi
   p.total_units = static_cast<int>(static_cast<uint64_t>(B) * H * n_qtiles * num_splits);
   p.o_part = o_part;
   p.lse_part = lse_part;
+  p.cu_q = nullptr;
+  p.cu_k = nullptr;
+  p.total_q = 0;
+  p.total_k = 0;
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634);
   p.idesc_qk = idesc_bf16_f32(kBQ, kBK, scale < 0.0f, false);
   p.idesc_pv = idesc_bf16_f32(kBQ, D, false, true);
@@ -991,6 +1048,64 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   if (st != ATTN_OK) return st;
   return run_forward(*dev, q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, 1, nullptr, nullptr,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int max_seqlen_q,
+                            int total_q, int total_k, int H, int D, float scale, int causal,
+                            attn_stream_t stream) {
+  if (batch < 0 || max_seqlen_q < 0 || total_q < 0 || total_k < 0 || H < 0) return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED_D;
+  if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
+  if (batch == 0 || H == 0 || total_q == 0 || max_seqlen_q == 0) return ATTN_OK;
+  if (q == nullptr || o == nullptr || lse == nullptr || cu_seqlens_q == nullptr || cu_seqlens_k == nullptr)
+    return ATTN_ERR_NULLPTR;
+  if (total_k > 0 && (k == nullptr || v == nullptr)) return ATTN_ERR_NULLPTR;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(lse, 4) || !aligned(cu_seqlens_q, 4) ||
+      !aligned(cu_seqlens_k, 4))
+    return ATTN_ERR_ALIGN;
+  if (total_k > 0 && (!aligned(k, 16) || !aligned(v, 16))) return ATTN_ERR_ALIGN;
+  const uint64_t max_t = static_cast<uint64_t>(total_q > total_k ? total_q : total_k);
+  if (max_t * H * D * 2 >= (1ull << 40)) return ATTN_ERR_SHAPE;
+  const uint64_t n_qtiles = (static_cast<uint64_t>(max_seqlen_q) + kBQ - 1) / kBQ;
+  if (static_cast<uint64_t>(batch) * H * n_qtiles > 0x7fff0000ull) return ATTN_ERR_SHAPE;
+  DeviceInfo* dev = nullptr;
+  attn_status st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  CUtensorMap mq, mk, mv;
+  if (!make_map_packed(&mq, q, H, total_q, D)) return ATTN_ERR_CUDA;
+  if (total_k > 0) {
+    if (!make_map_packed(&mk, k, H, total_k, D) || !make_map_packed(&mv, v, H, total_k, D)) return ATTN_ERR_CUDA;
+  } else {  // never dereferenced: with no keys every unit has zero K tiles
+    mk = mq;
+    mv = mq;
+  }
+  Params p;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.kv_lens = nullptr;
+  p.B = batch;
+  p.H = H;
+  p.Sq = max_seqlen_q;
+  p.Sk = 0;
+  p.n_qtiles = static_cast<int>(n_qtiles);
+  p.num_splits = 1;
+  p.total_units = static_cast<int>(static_cast<uint64_t>(batch) * H * n_qtiles);
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
+  p.cu_q = cu_seqlens_q;
+  p.cu_k = cu_seqlens_k;
+  p.total_q = total_q;
+  p.total_k = total_k;
+  p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634);
+  p.idesc_qk = idesc_bf16_f32(kBQ, kBK, scale < 0.0f, false);
+  p.idesc_pv = idesc_bf16_f32(kBQ, D, false, true);
+  p.wait_limit_ns = kWaitLimitNs;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (D == 64) {
+    return causal ? launch<64, true>(*dev, 0, mq, mk, mv, p, s) : launch<64, false>(*dev, 1, mq, mk, mv, p, s);
+  }
+  return causal ? launch<128, true>(*dev, 2, mq, mk, mv, p, s) : launch<128, false>(*dev, 3, mq, mk, mv, p, s);
 }
 
 size_t attn_fwd_splitkv_workspace_size(int B, int H, int Sq, int D, int num_splits) {

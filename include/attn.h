@@ -69,7 +69,9 @@ typedef enum attn_status {
  * scale   multiplier of QK^T, any finite value (usually 1/sqrt(D)).
  * causal  0 or non-zero.
  * kv_lens NULL (every sequence has Sk keys) or device int32 [B]; entries are
- *         clamped to [0, Sk].
+ *         clamped to [0, Sk].  Key/value rows past kv_lens[b] that fall in the
+ *         last 128-key tile are read and given weight zero, so they must hold
+ *         finite values (0 * Inf would be NaN).
  *
  * Sq == 0, B == 0 or H == 0: nothing to compute, returns ATTN_OK without a
  * launch.  Sk == 0: every row has no valid key (O = 0, LSE = -inf).
@@ -81,6 +83,30 @@ typedef enum attn_status {
  */
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
                      int Sk, int D, float scale, int causal, const int32_t* kv_lens, attn_stream_t stream);
+
+/*
+ * attn_fwd_varlen — the same forward over a packed batch of variable-length
+ * sequences (the ragged tensors of continuous batching, "Fused Multi-Head
+ * Attention", section on continuous batching): no padding is stored or read.
+ *
+ * q, o         bf16 [total_q, H, D], contiguous, device, 16-byte aligned.
+ * k, v         bf16 [total_k, H, D], contiguous, device, 16-byte aligned.
+ * lse          fp32 [H, total_q], device, 4-byte aligned.
+ * cu_seqlens_q device int32 [batch + 1]: sequence b owns query tokens
+ *              [cu_seqlens_q[b], cu_seqlens_q[b+1]); cu_seqlens_k likewise for
+ *              keys and values.  Entries are clamped to [0, total] and to be
+ *              non-decreasing, so any content keeps every access in bounds.
+ * max_seqlen_q host upper bound of the query lengths (it sizes the grid); rows
+ *              of a longer sequence past it are not computed.
+ * Per sequence the operation is exactly attn_fwd's (causal masking top-left
+ * within the sequence; a sequence with no key gives O = 0, LSE = -inf).  The
+ * last 128-key tile of a sequence also reads the next sequence's first keys
+ * with weight zero (they must be finite); past total_k the tile reads zeros.
+ * Asynchronous on `stream`; argument errors return before any launch.
+ */
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int max_seqlen_q,
+                            int total_q, int total_k, int H, int D, float scale, int causal, attn_stream_t stream);
 
 /*
  * attn_fwd_splitkv — the same forward with the keys of every (b, h, 128-row
@@ -154,7 +180,7 @@ attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream);
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 2
+#define ATTN_ABI_VERSION 3
 
 #ifdef __cplusplus
 }

@@ -147,3 +147,37 @@ def attention_rows(q_head, k_head, v_head, rows, scale: float, causal: bool = Fa
     Sk = k_head.shape[0]
     return _head_rows(q_head[rows], rows, k_head, v_head, scale, causal,
                       Sk if kv_len is None else kv_len)
+
+
+def attention_varlen_ref(q, k, v, cu_q, cu_k, scale: float, causal: bool = False):
+    """Exact attention over a packed batch of variable-length sequences.
+
+    ``q [total_q, H, D]``, ``k``/``v [total_k, H, D]`` (packed tokens),
+    ``cu_q``/``cu_k``: ``batch + 1`` non-decreasing offsets; sequence ``b`` owns
+    query tokens ``[cu_q[b], cu_q[b+1])`` and key tokens ``[cu_k[b], cu_k[b+1])``
+    (the ragged batches of continuous batching, "Fused Multi-Head Attention",
+    section on continuous batching).  Each sequence is exact attention on its
+    own tokens; causal masking is top-left within the sequence (query i of the
+    sequence sees keys j <= i).
+
+    Returns ``(O [total_q, H, Dv], LSE [H, total_q])`` in float64."""
+    q = _as_f64(q)
+    k = _as_f64(k)
+    v = _as_f64(v)
+    total_q, H, _ = q.shape
+    Dv = v.shape[2]
+    out = np.zeros((total_q, H, Dv), dtype=np.float64)
+    lse = np.full((H, total_q), -np.inf, dtype=np.float64)
+    cu_q = [int(x) for x in np.asarray(cu_q).reshape(-1)]
+    cu_k = [int(x) for x in np.asarray(cu_k).reshape(-1)]
+    for b in range(len(cu_q) - 1):
+        qs, qe = cu_q[b], cu_q[b + 1]
+        ks, ke = cu_k[b], cu_k[b + 1]
+        if qe <= qs:
+            continue
+        rows = np.arange(qe - qs)
+        for h in range(H):
+            o_b, l_b = _head_rows(q[qs:qe, h], rows, k[ks:ke, h], v[ks:ke, h], scale, causal, ke - ks)
+            out[qs:qe, h] = o_b
+            lse[h, qs:qe] = l_b
+    return out, lse

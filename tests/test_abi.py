@@ -161,3 +161,24 @@ def test_merge_argument_checks(lib, args, code):
     a = dict(op=A, lp=A, n=3, o=A, lse=A, rows=100, D=128)
     a.update(args)
     assert attn.attn_lse_merge(a["op"], a["lp"], a["n"], a["o"], a["lse"], a["rows"], a["D"], None) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(D=100), attn.ATTN_ERR_UNSUPPORTED_D),
+    (dict(batch=-1), attn.ATTN_ERR_SHAPE),
+    (dict(tq=-1), attn.ATTN_ERR_SHAPE),
+    (dict(cq=0), attn.ATTN_ERR_NULLPTR),
+    (dict(ck=0), attn.ATTN_ERR_NULLPTR),
+    (dict(cq=A + 2), attn.ATTN_ERR_ALIGN),
+    (dict(q=A + 8), attn.ATTN_ERR_ALIGN),
+    (dict(scale=float("nan")), attn.ATTN_ERR_SCALE),
+    (dict(batch=0), attn.ATTN_OK),
+    (dict(tq=0), attn.ATTN_OK),
+    (dict(maxq=0), attn.ATTN_OK),
+])
+def test_varlen_argument_checks(lib, args, code):
+    a = dict(q=A, k=A, v=A, o=A, lse=A, cq=A, ck=A, batch=3, maxq=300, tq=600, tk=700, H=4, D=128, scale=0.1)
+    a.update(args)
+    st = attn.attn_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"], a["batch"], a["maxq"],
+                              a["tq"], a["tk"], a["H"], a["D"], a["scale"], 0, None)
+    assert st == code

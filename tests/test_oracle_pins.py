@@ -379,3 +379,49 @@ def test_merge_of_empty_sets():
     Om, Lm = lse_merge(o, l2)       # one empty set: the other passes through unchanged
     np.testing.assert_array_equal(Om, o[1])
     assert Lm[0] == 0.3
+
+
+# --------------------------------------------------------------------------
+# Packed variable-length batches
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_equal_lengths_is_padded_batch(causal):
+    from oracle import attention_varlen_ref
+    B, H, S, D = 3, 2, 11, 5
+    q = _rand((B, H, S, D), 141)
+    k = _rand((B, H, S, D), 142)
+    v = _rand((B, H, S, D), 143)
+    O, L = attention_ref(q, k, v, 0.6, causal=causal)
+    pack = lambda t: t.transpose(0, 2, 1, 3).reshape(B * S, H, D)  # noqa: E731  [B,H,S,D] -> [B*S,H,D]
+    cu = np.arange(0, (B + 1) * S, S)
+    Ov, Lv = attention_varlen_ref(pack(q), pack(k), pack(v), cu, cu, 0.6, causal=causal)
+    np.testing.assert_array_equal(Ov, pack(O))
+    np.testing.assert_array_equal(Lv, L.transpose(1, 0, 2).reshape(H, B * S))
+
+
+def test_varlen_sequences_are_independent_and_match_brute_force():
+    from oracle import attention_varlen_ref
+    H, D = 2, 4
+    lens_q = [3, 0, 5, 1]
+    lens_k = [4, 2, 5, 0]
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)])
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)])
+    q = _rand((cu_q[-1], H, D), 151)
+    k = _rand((cu_k[-1], H, D), 152)
+    v = _rand((cu_k[-1], H, D), 153)
+    for causal in (False, True):
+        O, L = attention_varlen_ref(q, k, v, cu_q, cu_k, 0.5, causal=causal)
+        for b in range(4):
+            for i in range(lens_q[b]):
+                t = cu_q[b] + i
+                for h in range(H):
+                    keys = [j for j in range(lens_k[b]) if (not causal or j <= i)]
+                    if not keys:
+                        assert np.all(O[t, h] == 0) and L[h, t] == -np.inf
+                        continue
+                    e = [math.exp(0.5 * math.fsum(q[t, h] * k[cu_k[b] + j, h])) for j in keys]
+                    den = math.fsum(e)
+                    want = sum(w * v[cu_k[b] + j, h] for w, j in zip(e, keys)) / den
+                    np.testing.assert_allclose(O[t, h], want, rtol=1e-12, atol=1e-13)
+                    assert abs(L[h, t] - math.log(den)) < 1e-12

@@ -1,0 +1,110 @@
+"""GPU parity of the packed variable-length forward against the fp64 oracle."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_86_gb300 import attn
+from exact_attention_86_gb300.build import build
+from oracle import attention_varlen_ref
+
+from parity import check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build()
+    attn.lib()
+
+
+def _packed(lens_q, lens_k, H, D, seed, std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    tq, tk = int(sum(lens_q)), int(sum(lens_k))
+    q = (torch.randn(tq, H, D, generator=g) * std).to(torch.bfloat16)
+    k = (torch.randn(tk, H, D, generator=g) * std).to(torch.bfloat16)
+    v = (torch.randn(tk, H, D, generator=g) * std).to(torch.bfloat16)
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lens_q)]), dtype=torch.int32)
+    cu_k = torch.tensor(np.concatenate([[0], np.cumsum(lens_k)]), dtype=torch.int32)
+    return q, k, v, cu_q, cu_k
+
+
+def _np(t):
+    return t.float().numpy().astype(np.float64)
+
+
+def _run(q, k, v, cu_q, cu_k, max_q, scale, causal):
+    dev = torch.device("cuda:0")
+    o, lse = attn.forward_varlen(q.to(dev), k.to(dev), v.to(dev), cu_q.to(dev), cu_k.to(dev), max_q,
+                                 scale=scale, causal=causal)
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, (st, site)
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+CASES = [
+    # lens_q, lens_k
+    ([300, 1, 128, 129, 0, 500], [300, 1, 128, 129, 7, 500]),   # self-attention lengths (one empty query set)
+    ([127, 64, 260], [400, 0, 200]),                            # Sq != Sk per sequence, one sequence without keys
+    ([1, 1, 1, 1], [1000, 5, 130, 256]),                        # decode-like: one query per sequence
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_varlen_matches_oracle(case, causal, D):
+    lens_q, lens_k = CASES[case]
+    H = 3
+    q, k, v, cu_q, cu_k = _packed(lens_q, lens_k, H, D, seed=case * 7 + D + int(causal))
+    scale = 1.0 / math.sqrt(D)
+    o, lse = _run(q, k, v, cu_q, cu_k, max(lens_q), scale, causal)
+    o_ref, l_ref = attention_varlen_ref(_np(q), _np(k), _np(v), cu_q.numpy(), cu_k.numpy(), scale, causal=causal)
+    # O [total_q, H, D] against LSE [H, total_q]: compare head-major
+    check(o.transpose(1, 0, 2), lse, o_ref.transpose(1, 0, 2), l_ref, f"varlen case {case} causal={causal} D={D}")
+
+
+def test_varlen_guard_rows_untouched():
+    # query tiles that run past a sequence end must not write the next sequence's rows,
+    # and nothing past total_q may be written
+    lens = [130, 3, 250]
+    H, D = 2, 128
+    q, k, v, cu_q, cu_k = _packed(lens, lens, H, D, seed=3)
+    dev = torch.device("cuda:0")
+    tq = sum(lens)
+    pad = 4 * H * D
+    o_buf = torch.full((tq * H * D + pad,), 777, dtype=torch.int16, device=dev)
+    l_buf = torch.full((H * tq + 64,), 5.5, dtype=torch.float32, device=dev)
+    o_view = o_buf[:tq * H * D].view(torch.bfloat16).view(tq, H, D)
+    l_view = l_buf[:H * tq].view(H, tq)
+    qd, kd, vd, cqd, ckd = (t.to(dev) for t in (q, k, v, cu_q, cu_k))  # keep alive across the async call
+    st = attn.attn_fwd_varlen(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o_view.data_ptr(), l_view.data_ptr(),
+                              cqd.data_ptr(), ckd.data_ptr(), 3, 250, tq, tq, H, D, 1 / math.sqrt(D), 1,
+                              torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK
+    torch.cuda.synchronize()
+    assert torch.all(o_buf[tq * H * D:] == 777) and torch.all(l_buf[H * tq:] == 5.5)
+    o_ref, l_ref = attention_varlen_ref(_np(q), _np(k), _np(v), cu_q.numpy(), cu_k.numpy(), 1 / math.sqrt(D),
+                                        causal=True)
+    check(o_view.float().cpu().numpy().transpose(1, 0, 2), l_view.cpu().numpy(), o_ref.transpose(1, 0, 2), l_ref,
+          "varlen guard")
+
+
+def test_varlen_equals_padded_forward_for_equal_lengths():
+    B, H, S, D = 2, 4, 384, 128
+    g = torch.Generator().manual_seed(11)
+    q = torch.randn(B, H, S, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, H, S, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, H, S, D, generator=g).to(torch.bfloat16)
+    dev = torch.device("cuda:0")
+    o_pad, l_pad = attn.forward(q.to(dev), k.to(dev), v.to(dev), causal=True)
+    pack = lambda t: t.permute(0, 2, 1, 3).reshape(B * S, H, D).contiguous().to(dev)  # noqa: E731
+    cu = torch.arange(0, (B + 1) * S, S, dtype=torch.int32, device=dev)
+    o_var, l_var = attn.forward_varlen(pack(q), pack(k), pack(v), cu, cu, S, causal=True)
+    torch.cuda.synchronize()
+    # same kernel, same arithmetic order per row: identical bits
+    assert torch.equal(o_var.view(torch.int16), pack(o_pad).view(torch.int16))
+    assert torch.equal(l_var, l_pad.permute(1, 0, 2).reshape(H, B * S))
