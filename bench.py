@@ -8,7 +8,10 @@ A step is one ``attn_fwd`` call over the whole workload (default: B=2, H=16,
 Sq=Sk=8192, D=128, non-causal, bf16 N(0,1) inputs from seed 3).  ``value`` is
 whole-job TFLOP/s (4*B*H*Sq*Sk*D per step, halved when causal) with inputs
 resident in HBM; every step re-reads 192 MiB of Q/K/V (plus 64 MiB of O
-written), more than the 129 MB L2, so no explicit flush is needed.
+written), more than the 129 MB L2, so no explicit flush is needed.  Smaller
+workloads (``--workload``) get a 256 MiB L2 flush before every timed launch and
+report the launch time alone.  The ``varlen_*`` workloads time
+``attn_fwd_varlen`` on a packed batch of variable-length sequences.
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (weak
 scaling: the attention units shard with no exchange step); the barrier and the
@@ -39,6 +42,7 @@ METRIC = "fused attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor pe
 FALLBACK_PEAK_TFLOPS = 1900.0
 KERNEL_SOURCES = ["exact_attention_86_gb300/csrc/attn_fwd.cu", "exact_attention_86_gb300/csrc/sm103_ptx.cuh"]
 TRAFFIC_FILE = "profiles/attn_fwd_kernel_s8192_d128_traffic.md"
+L2_BYTES = 129 * 10**6
 
 
 def kernel_source_hash() -> str:
@@ -139,25 +143,37 @@ class ClockSampler:
                 "power_w_max": max((num(p[3]) or 0.0) for _, p in window)}
 
 
-def cpu_oracle_steps(w, q, k, v, kv, n_steps: int, budget_s: float | None):
-    """Runs the fp64 oracle on successive 256-row query blocks of head (0, 0).
-    Returns (flops, seconds, blocks)."""
+def oracle_heads(w, q, k, v, kv):
+    """The (q_head, k_head, v_head, kv_len) slices the CPU oracle walks: head 0
+    of batch entry 0 for a padded workload; head 0 of every sequence for a
+    packed variable-length one (``kv`` is then the offsets array)."""
     import numpy as np
+
+    from exact_attention_86_gb300 import workloads
+
+    f64 = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    if isinstance(w, workloads.VarlenWorkload):
+        cu = [int(x) for x in kv]
+        return [(f64(q[a:b, 0]), f64(k[a:b, 0]), f64(v[a:b, 0]), None)
+                for a, b in zip(cu[:-1], cu[1:]) if b > a]
+    return [(f64(q[0, 0]), f64(k[0, 0]), f64(v[0, 0]), None if kv is None else int(kv[0]))]
+
+
+def cpu_oracle_steps(w, q, k, v, kv, n_steps: int, budget_s: float | None):
+    """Runs the fp64 oracle on successive 256-row query blocks of the heads
+    ``oracle_heads`` lists.  Returns (flops, seconds, blocks)."""
     from oracle import attention_rows
 
-    qh = q[0, 0].float().numpy().astype(np.float64)
-    kh = k[0, 0].float().numpy().astype(np.float64)
-    vh = v[0, 0].float().numpy().astype(np.float64)
-    kvb = None if kv is None else int(kv[0])
-    n_blocks = (w.Sq + 255) // 256
+    blocks = [(h, r0) for h in oracle_heads(w, q, k, v, kv) for r0 in range(0, h[0].shape[0], 256)]
     flops = 0.0
     t0 = time.perf_counter()
     i = 0
     while True:
-        blk = i % n_blocks
-        rows = list(range(blk * 256, min(w.Sq, blk * 256 + 256)))
+        (qh, kh, vh, kvb), r0 = blocks[i % len(blocks)]
+        sq, sk = qh.shape[0], kh.shape[0]
+        rows = list(range(r0, min(sq, r0 + 256)))
         attention_rows(qh, kh, vh, rows, w.scale, causal=w.causal, kv_len=kvb)
-        keys = w.Sk if kvb is None else min(max(kvb, 0), w.Sk)
+        keys = sk if kvb is None else min(max(kvb, 0), sk)
         for r in rows:
             n = min(keys, r + 1) if w.causal else keys
             flops += 4.0 * n * w.D
@@ -182,18 +198,42 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+def lookup(name):
+    from exact_attention_86_gb300 import workloads
+    if name in workloads.WORKLOADS:
+        return workloads.WORKLOADS[name]
+    if name in workloads.VARLEN_WORKLOADS:
+        return workloads.VARLEN_WORKLOADS[name]
+    raise SystemExit(f"unknown workload {name}; known: "
+                     f"{sorted(workloads.WORKLOADS) + sorted(workloads.VARLEN_WORKLOADS)}")
+
+
+def is_varlen(w) -> bool:
+    from exact_attention_86_gb300 import workloads
+    return isinstance(w, workloads.VarlenWorkload)
+
+
+def generate(w, draw: int):
+    """(q, k, v, extra): extra is kv_lens (padded) or the offsets (varlen)."""
+    from exact_attention_86_gb300 import workloads
+    if is_varlen(w):
+        if draw != 0:
+            raise SystemExit(f"workload {w.name} has a single draw")
+        return workloads.generate_varlen(w)
+    return workloads.generate(w, draw)
+
+
 def run_reference(args, w):
     """The CPU oracle as the reference arm."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    from exact_attention_86_gb300 import workloads
-    q, k, v, kv = workloads.generate(w)
+    q, k, v, kv = generate(w, 0)
     cpu_oracle_steps(w, q, k, v, kv, n_steps=args.warmup, budget_s=None) if args.warmup > 0 else None
     flops, secs, blocks = cpu_oracle_steps(w, q, k, v, kv, n_steps=args.steps, budget_s=None)
     tflops = flops / secs / 1e12
-    sample = (f"{blocks} steps; each one 256-row query block of head (0,0) against all "
-              f"{w.Sk} keys, fp64 NumPy/BLAS")
+    sample = (f"{blocks} steps; each one 256-row query block of head 0 of "
+              f"{'a sequence' if is_varlen(w) else 'batch entry 0'} against all its keys, fp64 NumPy/BLAS")
     line = {
         "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / max(blocks, 1) * 1e3,
@@ -223,7 +263,8 @@ def main():
     args = ap.parse_args()
 
     from exact_attention_86_gb300 import workloads
-    w = workloads.WORKLOADS[args.workload or workloads.HEADLINE]
+    w = lookup(args.workload or workloads.HEADLINE)
+    varlen = is_varlen(w)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
 
@@ -249,22 +290,33 @@ def main():
         dist.barrier()
     attn.lib()
 
-    q, k, v, kv = workloads.generate(w, args.draw)
+    q, k, v, kv = generate(w, args.draw)
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     kvd = kv.to(dev) if kv is not None else None
     o = torch.empty_like(qd)
-    lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev)
+    if varlen:
+        lse = torch.empty(w.H, q.shape[0], dtype=torch.float32, device=dev)
+    else:
+        lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     kv_ptr = kvd.data_ptr() if kvd is not None else None
+    if varlen and args.splits > 0:
+        raise SystemExit("--splits applies to padded workloads only")
 
     ws = None
     if args.splits > 0:
         ws_bytes = attn.attn_fwd_splitkv_workspace_size(w.B, w.H, w.Sq, w.D, args.splits)
         ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    max_len = w.max_len if varlen else 0
 
     def step():
-        if ws is None:
+        if varlen:
+            total = q.shape[0]
+            st = attn.attn_fwd_varlen(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                      kv_ptr, kv_ptr, w.batch, max_len, total, total, w.H, w.D, w.scale,
+                                      int(w.causal), sptr)
+        elif ws is None:
             st = attn.attn_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
                                w.B, w.H, w.Sq, w.Sk, w.D, w.scale, int(w.causal), kv_ptr, sptr)
         else:
@@ -273,6 +325,12 @@ def main():
                                        ws.data_ptr(), ws.numel(), sptr)
         if st != attn.ATTN_OK:
             raise attn.AttnError(st, "attn_fwd")
+
+    # Workloads whose bytes fit in L2 get an L2 flush (a 256 MiB write) before
+    # every timed launch; the launch events bracket the kernel alone.
+    flush = None
+    if w.min_bytes < 2 * L2_BYTES:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def barrier():
         torch.cuda.synchronize(dev)
@@ -298,6 +356,8 @@ def main():
     wall0 = time.time()
     t_all0.record(stream)
     for i in range(args.steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -314,7 +374,8 @@ def main():
         t = torch.tensor([elapsed_ms, launch_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms, launch_ms = float(t[0]), float(t[1])
-    ms_per_step = elapsed_ms / args.steps
+    # with an L2 flush between launches the step time is the launch alone
+    ms_per_step = launch_ms if flush is not None else elapsed_ms / args.steps
     value = w.flops * world / (ms_per_step * 1e-3) / 1e12
     clocks = sampler.summary(wall0, wall1)
 
@@ -324,11 +385,14 @@ def main():
     vh = v.pin_memory()
     oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
     lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    cuh = kv.pin_memory() if varlen else None
 
     def e2e_step():
         qd.copy_(qh, non_blocking=True)
         kd.copy_(kh, non_blocking=True)
         vd.copy_(vh, non_blocking=True)
+        if varlen:
+            kvd.copy_(cuh, non_blocking=True)
         step()
         oh.copy_(o, non_blocking=True)
         lh.copy_(lse, non_blocking=True)
@@ -348,7 +412,7 @@ def main():
         t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t[0])
-    h2d = (q.numel() + k.numel() + v.numel()) * 2
+    h2d = (q.numel() + k.numel() + v.numel()) * 2 + (kv.numel() * 4 if varlen else 0)
     d2h = o.numel() * 2 + lse.numel() * 4
 
     # -------------------------------------------------------------- roofline
@@ -370,7 +434,8 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         flops, secs, blocks = cpu_oracle_steps(w, q, k, v, kv, n_steps=None, budget_s=args.cpu_budget_s)
         cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
-               "sample": f"{blocks} query blocks of 256 rows of head (0,0) against all {w.Sk} keys "
+               "sample": f"{blocks} query blocks of 256 rows of head 0 of "
+                         f"{'the sequences' if varlen else 'batch entry 0'} against all their keys "
                          f"({secs:.1f} s of fp64 NumPy/BLAS)"}
 
     if rank == 0:
@@ -380,8 +445,10 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "shape": w.label(), "draw": args.draw,
                        "inputs": f"bf16 N(0,{(w.std if args.draw == 0 else w.second_std) ** 2:g}) seed {w.seed}",
-                       "l2": "no flush: each step reads 192 MiB of Q/K/V and writes 64 MiB of O, more than the "
-                             "129 MB L2",
+                       "l2": (f"flushed: a 256 MiB write before every timed launch (the workload moves "
+                              f"{w.min_bytes / 2**20:.1f} MiB)") if flush is not None else
+                             (f"no flush: each step moves {w.min_bytes / 2**20:.0f} MiB of Q/K/V/O/LSE, more "
+                              f"than the 129 MB L2"),
                        "parallelism": f"weak: {world} replica(s) of the workload, one per GPU",
                        "splits": args.splits},
             "roofline": roofline,

@@ -40,6 +40,11 @@ SIGNATURES = {
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                        ctypes.c_int, ctypes.c_void_p]),
+    "attn_fwd_paged": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                      ctypes.c_void_p]),
     "attn_fwd_splitkv_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                           ctypes.c_int]),
     "attn_fwd_splitkv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -94,6 +99,13 @@ def attn_fwd_varlen(q: int, k: int, v: int, o: int, lse: int, cu_q: int, cu_k: i
                     stream: Optional[int]) -> int:
     return lib().attn_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, batch, max_seqlen_q, total_q, total_k, H, D, scale,
                                  int(causal), stream)
+
+
+def attn_fwd_paged(q: int, k_cache: int, v_cache: int, o: int, lse: int, cu_q: int, seqlens_k: int,
+                   block_table: int, batch: int, max_seqlen_q: int, total_q: int, num_pages: int, page_size: int,
+                   max_pages_per_seq: int, H: int, D: int, scale: float, causal: int, stream: Optional[int]) -> int:
+    return lib().attn_fwd_paged(q, k_cache, v_cache, o, lse, cu_q, seqlens_k, block_table, batch, max_seqlen_q,
+                                total_q, num_pages, page_size, max_pages_per_seq, H, D, scale, int(causal), stream)
 
 
 def attn_fwd_splitkv_workspace_size(B: int, H: int, Sq: int, D: int, num_splits: int) -> int:
@@ -209,6 +221,46 @@ def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, scale
                              total_k, H, D, float(scale), int(bool(causal)), stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_varlen")
+    return out, lse
+
+
+def forward_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, max_seqlen_q: int,
+                  scale: Optional[float] = None, causal: bool = False):
+    """Packed queries ``q [total_q, H, D]`` against a paged KV cache
+    ``k_cache``/``v_cache [num_pages, page_size, H, D]`` (bf16 CUDA tensors);
+    ``cu_seqlens_q`` int32 ``[batch + 1]``, ``seqlens_k`` int32 ``[batch]``,
+    ``block_table`` int32 ``[batch, max_pages_per_seq]`` on the same device.
+    Returns ``(o [total_q, H, D], lse [H, total_q])``."""
+    import torch
+
+    if q.dtype != torch.bfloat16 or not q.is_cuda or not q.is_contiguous() or q.dim() != 3:
+        raise ValueError("q must be a contiguous 3-d bf16 CUDA tensor")
+    total_q, H, D = q.shape
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if t.dtype != torch.bfloat16 or t.device != q.device or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-d bf16 tensor on q's device")
+    num_pages, page_size = k_cache.shape[0], k_cache.shape[1]
+    if tuple(k_cache.shape) != (num_pages, page_size, H, D) or tuple(v_cache.shape) != tuple(k_cache.shape):
+        raise ValueError("k_cache and v_cache must be [num_pages, page_size, H, D] with q's H, D")
+    for name, t, dim in (("cu_seqlens_q", cu_seqlens_q, 1), ("seqlens_k", seqlens_k, 1),
+                         ("block_table", block_table, 2)):
+        if t.dtype != torch.int32 or t.device != q.device or not t.is_contiguous() or t.dim() != dim:
+            raise ValueError(f"{name} must be a contiguous {dim}-d int32 tensor on q's device")
+    batch = cu_seqlens_q.numel() - 1
+    if seqlens_k.numel() != batch or block_table.shape[0] != batch:
+        raise ValueError("seqlens_k and block_table must have one entry (row) per sequence")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = torch.empty((total_q, H, D), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = attn_fwd_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                            cu_seqlens_q.data_ptr(), seqlens_k.data_ptr(), block_table.data_ptr(), batch,
+                            int(max_seqlen_q), total_q, num_pages, page_size, block_table.shape[1], H, D,
+                            float(scale), int(bool(causal)), stream)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_paged")
     return out, lse
 
 

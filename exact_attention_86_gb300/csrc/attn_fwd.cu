@@ -91,6 +91,15 @@ struct Geo {
   static constexpr int kChunkBytes = 128 * 128;      // 128 rows x 64 bf16 (one 128-B swizzle column)
   static constexpr int kChunks = D / 64;
   static constexpr int kSlots = (D == 128) ? 5 : 12; // K/V ring depth (tiles)
+  // Ring position pos holds K (pos even) or V (pos odd) in slot pos % kSlots.
+  // With an odd depth a slot alternates between K and V fills, so each slot
+  // has one "full" barrier per kind: every barrier is then waited on, phase
+  // after phase, by the one issuer that consumes that kind, and a parity wait
+  // can never match a phase two fills old.  This is the use index of the
+  // fill at pos among the fills of its kind in its slot.
+  static __device__ __forceinline__ uint32_t kind_use(uint32_t pos) {
+    return (kSlots & 1) ? (pos / kSlots) >> 1 : pos / kSlots;
+  }
   static constexpr uint32_t kTmemS = 0;              // + 128 * buffer
   static constexpr uint32_t kTmemP = 256;            // + 64 * buffer
   static constexpr uint32_t kTmemO = 384;
@@ -102,7 +111,7 @@ struct Geo {
 
 struct Ctrl {
   uint64_t q_full, q_empty;
-  uint64_t kv_full[12], kv_empty[12];
+  uint64_t k_full[12], v_full[12], kv_empty[12];  // full: per kind (see Geo::kind_use)
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t o_full;
   uint64_t drain[2];
@@ -136,6 +145,13 @@ struct Params {
   const int32_t* cu_q;
   const int32_t* cu_k;
   int total_q, total_k;
+  // paged-KV mode (block_table != nullptr, with packed queries): k/v caches
+  // [num_pages, page_size, H, D]; key j of sequence b is slot j % page_size of
+  // page block_table[b * max_pages + j / page_size]; seqlens_k[b] keys
+  const int32_t* block_table;
+  const int32_t* seqlens_k;
+  int page_size, max_pages, num_pages;
+  int cache_tokens;        // num_pages * page_size: a key coordinate that reads zeros
   float c;                 // |scale| * log2(e)
   uint32_t idesc_qk;       // negate-A set when scale < 0
   uint32_t idesc_pv;
@@ -176,12 +192,17 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int t_in) {
     // packed sequences: offsets clamped so that any content stays in bounds
     const int qs = min(max(__ldg(p.cu_q + u.b), 0), p.total_q);
     const int qe = min(max(__ldg(p.cu_q + u.b + 1), qs), p.total_q);
-    const int ks = min(max(__ldg(p.cu_k + u.b), 0), p.total_k);
-    const int ke = min(max(__ldg(p.cu_k + u.b + 1), ks), p.total_k);
     q_len = qe - qs;
-    kv = ke - ks;
     u.q_tok0 = qs + u.q0;
-    u.k_tok0 = ks;
+    if (p.block_table != nullptr) {
+      kv = min(max(__ldg(p.seqlens_k + u.b), 0), p.max_pages * p.page_size);
+      u.k_tok0 = 0;
+    } else {
+      const int ks = min(max(__ldg(p.cu_k + u.b), 0), p.total_k);
+      const int ke = min(max(__ldg(p.cu_k + u.b + 1), ks), p.total_k);
+      kv = ke - ks;
+      u.k_tok0 = ks;
+    }
   } else {
     q_len = p.Sq;
     kv = p.Sk;
@@ -356,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t bar_q_full = smem_addr(&ctl.q_full);
   const uint32_t bar_q_empty = smem_addr(&ctl.q_empty);
-  const uint32_t bar_kv_full0 = smem_addr(&ctl.kv_full[0]);
+  const uint32_t bar_k_full0 = smem_addr(&ctl.k_full[0]);
+  const uint32_t bar_v_full0 = smem_addr(&ctl.v_full[0]);
   const uint32_t bar_kv_empty0 = smem_addr(&ctl.kv_empty[0]);
   // barrier of buffer b = barrier of buffer 0 + 8 * b (consecutive uint64_t)
   const uint32_t bar_s_full0 = smem_addr(&ctl.s_full[0]);
@@ -369,7 +391,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_q_full, 1);
     mbar_init(bar_q_empty, 1);
     for (int s = 0; s < G::kSlots; ++s) {
-      mbar_init(bar_kv_full0 + 8 * s, 1);
+      mbar_init(bar_k_full0 + 8 * s, 1);
+      mbar_init(bar_v_full0 + 8 * s, 1);
       mbar_init(bar_kv_empty0 + 8 * s, 1);  // K slots: QK issuer; V slots: PV issuer
     }
     for (int b = 0; b < 2; ++b) {
@@ -428,13 +451,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t slot = ring % G::kSlots;
             const uint32_t ph = (ring / G::kSlots) & 1u;
             if (!wait_phase(bar_kv_empty0 + 8 * slot, ph ^ 1u, abort_flag, kSiteKvEmpty, limit)) { ok = false; break; }
-            const uint32_t full = bar_kv_full0 + 8 * slot;
+            const uint32_t full = (sel ? bar_v_full0 : bar_k_full0) + 8 * slot;
             mbar_arrive_expect_tx(full, G::kTileBytes);
             const CUtensorMap* m = sel ? &map_v : &map_k;
             const int key0 = (u.j0 + j) * kBK;
-            for (int c = 0; c < G::kChunks; ++c)
-              tma_load_4d_hint(base + G::kOffRing + slot * G::kTileBytes + c * G::kChunkBytes, m, full, c * 64,
-                               packed ? u.h : key0, packed ? u.k_tok0 + key0 : u.h, packed ? 0 : u.b, pol_keep);
+            const uint32_t dst = base + G::kOffRing + slot * G::kTileBytes;
+            if (p.block_table == nullptr) {
+              for (int c = 0; c < G::kChunks; ++c)
+                tma_load_4d_hint(dst + c * G::kChunkBytes, m, full, c * 64, packed ? u.h : key0,
+                                 packed ? u.k_tok0 + key0 : u.h, packed ? 0 : u.b, pol_keep);
+            } else {
+              // paged: two 64-key boxes, each inside one page (page_size is a
+              // multiple of 64); a box past the sequence's keys reads zeros
+              for (int hf = 0; hf < 2; ++hf) {
+                const int pos = key0 + 64 * hf;
+                int tok = p.cache_tokens;
+                if (pos < u.kv) {
+                  const int pg = __ldg(p.block_table + static_cast<size_t>(u.b) * p.max_pages + pos / p.page_size);
+                  tok = min(max(pg, 0), p.num_pages - 1) * p.page_size + pos % p.page_size;
+                }
+                for (int c = 0; c < G::kChunks; ++c)
+                  tma_load_4d_hint(dst + c * G::kChunkBytes + hf * (G::kChunkBytes / 2), m, full, c * 64, u.h, tok,
+                                   0, pol_keep);
+              }
+            }
             ++ring;
           }
         }
@@ -444,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (qcount > 0) wait_phase_drain(bar_q_full, (qcount - 1) & 1u);
         for (uint32_t s = 0; s < (uint32_t)G::kSlots && s < ring; ++s) {
           const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);  // last load issued into slot s
-          wait_phase_drain(bar_kv_full0 + 8 * s, (last / G::kSlots) & 1u);
+          wait_phase_drain(((last & 1u) ? bar_v_full0 : bar_k_full0) + 8 * s, G::kind_use(last) & 1u);
         }
       }
       // The issuers release slots and the Q buffer with tcgen05.commit, whose
@@ -481,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t pos = ring + 2 * j;
         const uint32_t slot = pos % G::kSlots;
-        if (!wait_warp(bar_kv_full0 + 8 * slot, (pos / G::kSlots) & 1u, abort_flag, kSiteKvFull, limit)) {
+        if (!wait_warp(bar_k_full0 + 8 * slot, G::kind_use(pos) & 1u, abort_flag, kSiteKvFull, limit)) {
           ok = false;
           break;
         }
@@ -521,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t pos = ring + 2 * j + 1;
         const uint32_t slot = pos % G::kSlots;
-        if (!wait_warp(bar_kv_full0 + 8 * slot, (pos / G::kSlots) & 1u, abort_flag, kSiteKvFull, limit)) {
+        if (!wait_warp(bar_v_full0 + 8 * slot, G::kind_use(pos) & 1u, abort_flag, kSiteKvFull, limit)) {
           ok = false;
           break;
         }
@@ -861,18 +901,28 @@ bool make_map(CUtensorMap* m, const void* ptr, int B, int H, int S, int D) {
 }
 
 // Rank-4 map over a packed [tokens, H, D] tensor as (D, H, tokens, 1) with a
-// 64 x 1 x 128 box: the box lands in shared memory as the same 128 rows x 128 B
-// tile as the padded map's.  Token rows past the end read as zeros.
-bool make_map_packed(CUtensorMap* m, const void* ptr, int H, int total, int D) {
+// 64 x 1 x box_rows box: a 128-row box lands in shared memory as the same
+// 128 rows x 128 B tile as the padded map's, a 64-row box as its upper or lower
+// half.  Token rows past the end read as zeros.
+bool make_map_packed(CUtensorMap* m, const void* ptr, int H, int total, int D, int box_rows = 128) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
   if (encode == nullptr) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)total, 1};
   const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)total * H * D * 2};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+void clear_paged(Params& p) {
+  p.block_table = nullptr;
+  p.seqlens_k = nullptr;
+  p.page_size = 0;
+  p.max_pages = 0;
+  p.num_pages = 0;
+  p.cache_tokens = 0;
 }
 
 template <int D, bool CAUSAL>
@@ -996,6 +1046,41 @@ attn_status check_args(const void* q, const void* k, const void* v, const void* 
 
 // Launches the attention kernel.  o_part == nullptr: final bf16 O and LSE;
 // otherwise num_splits key ranges write fp32 partials to o_part / lse_part.
+// Parameters of a packed-query launch (variable-length or paged); the caller
+// fills in the key side.
+Params packed_params(void* o, float* lse, const int32_t* cu_q, int batch, int max_seqlen_q, int total_q, int H,
+                     int D, float scale) {
+  Params p;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.kv_lens = nullptr;
+  p.B = batch;
+  p.H = H;
+  p.Sq = max_seqlen_q;
+  p.Sk = 0;
+  p.n_qtiles = static_cast<int>((static_cast<int64_t>(max_seqlen_q) + kBQ - 1) / kBQ);
+  p.num_splits = 1;
+  p.total_units = static_cast<int>(static_cast<int64_t>(batch) * H * p.n_qtiles);  // checked by the caller
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
+  p.cu_q = cu_q;
+  p.cu_k = nullptr;
+  p.total_q = total_q;
+  p.total_k = 0;
+  clear_paged(p);
+  p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634);
+  p.idesc_qk = idesc_bf16_f32(kBQ, kBK, scale < 0.0f, false);
+  p.idesc_pv = idesc_bf16_f32(kBQ, D, false, true);
+  p.wait_limit_ns = kWaitLimitNs;
+  return p;
+}
+
+attn_status launch_any(DeviceInfo& dev, int D, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
+                       const CUtensorMap& mv, const Params& p, cudaStream_t s) {
+  if (D == 64) return causal ? launch<64, true>(dev, 0, mq, mk, mv, p, s) : launch<64, false>(dev, 1, mq, mk, mv, p, s);
+  return causal ? launch<128, true>(dev, 2, mq, mk, mv, p, s) : launch<128, false>(dev, 3, mq, mk, mv, p, s);
+}
+
 attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int H, int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens, int num_splits,
                         float* o_part, float* lse_part, cudaStream_t s) {
@@ -1025,6 +1110,7 @@ attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const voi
   p.cu_k = nullptr;
   p.total_q = 0;
   p.total_k = 0;
+  clear_paged(p);
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634);
   p.idesc_qk = idesc_bf16_f32(kBQ, kBK, scale < 0.0f, false);
   p.idesc_pv = idesc_bf16_f32(kBQ, D, false, true);
@@ -1080,32 +1166,51 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
     mk = mq;
     mv = mq;
   }
-  Params p;
-  p.o = static_cast<uint16_t*>(o);
-  p.lse = lse;
-  p.kv_lens = nullptr;
-  p.B = batch;
-  p.H = H;
-  p.Sq = max_seqlen_q;
-  p.Sk = 0;
-  p.n_qtiles = static_cast<int>(n_qtiles);
-  p.num_splits = 1;
-  p.total_units = static_cast<int>(static_cast<uint64_t>(batch) * H * n_qtiles);
-  p.o_part = nullptr;
-  p.lse_part = nullptr;
-  p.cu_q = cu_seqlens_q;
+  Params p = packed_params(o, lse, cu_seqlens_q, batch, max_seqlen_q, total_q, H, D, scale);
   p.cu_k = cu_seqlens_k;
-  p.total_q = total_q;
   p.total_k = total_k;
-  p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634);
-  p.idesc_qk = idesc_bf16_f32(kBQ, kBK, scale < 0.0f, false);
-  p.idesc_pv = idesc_bf16_f32(kBQ, D, false, true);
-  p.wait_limit_ns = kWaitLimitNs;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (D == 64) {
-    return causal ? launch<64, true>(*dev, 0, mq, mk, mv, p, s) : launch<64, false>(*dev, 1, mq, mk, mv, p, s);
-  }
-  return causal ? launch<128, true>(*dev, 2, mq, mk, mv, p, s) : launch<128, false>(*dev, 3, mq, mk, mv, p, s);
+  return launch_any(*dev, D, causal != 0, mq, mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                           const int32_t* cu_seqlens_q, const int32_t* seqlens_k, const int32_t* block_table,
+                           int batch, int max_seqlen_q, int total_q, int num_pages, int page_size,
+                           int max_pages_per_seq, int H, int D, float scale, int causal, attn_stream_t stream) {
+  if (batch < 0 || max_seqlen_q < 0 || total_q < 0 || H < 0) return ATTN_ERR_SHAPE;
+  if (num_pages < 1 || max_pages_per_seq < 1 || page_size < 64 || page_size % 64 != 0) return ATTN_ERR_SHAPE;
+  if (static_cast<uint64_t>(num_pages) * page_size + 64 > 0x7fffffffull ||
+      static_cast<uint64_t>(max_pages_per_seq) * page_size > 0x7fffffffull)
+    return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED_D;
+  if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
+  if (batch == 0 || H == 0 || total_q == 0 || max_seqlen_q == 0) return ATTN_OK;
+  if (q == nullptr || k_cache == nullptr || v_cache == nullptr || o == nullptr || lse == nullptr ||
+      cu_seqlens_q == nullptr || seqlens_k == nullptr || block_table == nullptr)
+    return ATTN_ERR_NULLPTR;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(seqlens_k, 4) || !aligned(block_table, 4))
+    return ATTN_ERR_ALIGN;
+  const uint64_t cache_tokens = static_cast<uint64_t>(num_pages) * page_size;
+  const uint64_t max_t = cache_tokens > static_cast<uint64_t>(total_q) ? cache_tokens : total_q;
+  if (max_t * H * D * 2 >= (1ull << 40)) return ATTN_ERR_SHAPE;
+  const uint64_t n_qtiles = (static_cast<uint64_t>(max_seqlen_q) + kBQ - 1) / kBQ;
+  if (static_cast<uint64_t>(batch) * H * n_qtiles > 0x7fff0000ull) return ATTN_ERR_SHAPE;
+  DeviceInfo* dev = nullptr;
+  attn_status st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  CUtensorMap mq, mk, mv;
+  if (!make_map_packed(&mq, q, H, total_q, D) ||
+      !make_map_packed(&mk, k_cache, H, static_cast<int>(cache_tokens), D, 64) ||
+      !make_map_packed(&mv, v_cache, H, static_cast<int>(cache_tokens), D, 64))
+    return ATTN_ERR_CUDA;
+  Params p = packed_params(o, lse, cu_seqlens_q, batch, max_seqlen_q, total_q, H, D, scale);
+  p.block_table = block_table;
+  p.seqlens_k = seqlens_k;
+  p.page_size = page_size;
+  p.max_pages = max_pages_per_seq;
+  p.num_pages = num_pages;
+  p.cache_tokens = static_cast<int>(cache_tokens);
+  return launch_any(*dev, D, causal != 0, mq, mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t attn_fwd_splitkv_workspace_size(int B, int H, int Sq, int D, int num_splits) {

@@ -117,3 +117,74 @@ def small(name: str, B: int, H: int, Sq: int, Sk: int, D: int, causal: bool, see
 
 def shrink(w: Workload, **kw) -> Workload:
     return replace(w, **kw)
+
+
+@dataclass(frozen=True)
+class VarlenWorkload:
+    """A packed batch of variable-length sequences (self-attention: each
+    sequence's query and key lengths are equal).
+
+    Recipe: a CPU ``torch.Generator`` seeded with ``seed`` first draws the
+    ``batch`` lengths with ``torch.randint(len_lo, len_hi + 1, (batch,))``,
+    then ``q`` ``[total, H, D]``, ``k``, ``v`` as in the padded recipe
+    (``torch.randn`` float32 times ``std``, rounded to bfloat16)."""
+    name: str
+    batch: int
+    H: int
+    D: int
+    len_lo: int
+    len_hi: int
+    causal: bool
+    seed: int
+    std: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    def lengths(self):
+        g = torch.Generator(device="cpu")
+        g.manual_seed(self.seed)
+        return torch.randint(self.len_lo, self.len_hi + 1, (self.batch,), generator=g, dtype=torch.int64)
+
+    @property
+    def flops(self) -> float:
+        """Sum over sequences of 4*H*n*n*D, halved when causal."""
+        n = self.lengths().double()
+        f = 4.0 * self.H * self.D * float((n * n).sum())
+        return f / 2 if self.causal else f
+
+    @property
+    def min_bytes(self) -> int:
+        t = int(self.lengths().sum())
+        return 2 * self.H * self.D * 4 * t + 4 * self.H * t
+
+    @property
+    def max_len(self) -> int:
+        return int(self.lengths().max())
+
+    def label(self) -> str:
+        return (f"packed batch of {self.batch} sequences, lengths U[{self.len_lo},{self.len_hi}], H{self.H} "
+                f"D{self.D} {'causal' if self.causal else 'non-causal'}")
+
+
+VARLEN_WORKLOADS = {
+    "varlen_b32_d128_causal": VarlenWorkload("varlen_b32_d128_causal", 32, 16, 128, 1, 4096, True, seed=6),
+    "varlen_b32_d128": VarlenWorkload("varlen_b32_d128", 32, 16, 128, 1, 4096, False, seed=6),
+}
+
+
+def generate_varlen(w: VarlenWorkload):
+    """Return ``(q, k, v, cu_seqlens)`` on the CPU: bf16 ``[total, H, D]``
+    tensors and the int32 ``[batch + 1]`` offsets (shared by queries and keys)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    lens = torch.randint(w.len_lo, w.len_hi + 1, (w.batch,), generator=g, dtype=torch.int64)
+    total = int(lens.sum())
+    shape = (total, w.H, w.D)
+    q = (torch.randn(shape, generator=g, dtype=torch.float32) * w.std).to(torch.bfloat16)
+    k = (torch.randn(shape, generator=g, dtype=torch.float32) * w.std).to(torch.bfloat16)
+    v = (torch.randn(shape, generator=g, dtype=torch.float32) * w.std).to(torch.bfloat16)
+    cu = torch.zeros(w.batch + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lens, 0).to(torch.int32)
+    return q, k, v, cu

@@ -109,6 +109,36 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
                             int total_q, int total_k, int H, int D, float scale, int causal, attn_stream_t stream);
 
 /*
+ * attn_fwd_paged — the packed-query forward with keys and values read through
+ * a page table from a paged KV cache (the PagedAttention layout named in
+ * "Fused Multi-Head Attention", section on continuous batching): a sequence's
+ * keys need not be contiguous in memory.
+ *
+ * q, o         bf16 [total_q, H, D] packed queries, as in attn_fwd_varlen.
+ * lse          fp32 [H, total_q].
+ * cu_seqlens_q device int32 [batch + 1] query offsets, as in attn_fwd_varlen.
+ * k_cache,     bf16 [num_pages, page_size, H, D], contiguous, device, 16-byte
+ * v_cache      aligned.
+ * seqlens_k    device int32 [batch]: keys of sequence b, clamped to
+ *              [0, max_pages_per_seq * page_size].
+ * block_table  device int32 [batch, max_pages_per_seq]: key j of sequence b is
+ *              slot j % page_size of page block_table[b][j / page_size]
+ *              (entries clamped to [0, num_pages - 1]; entries past the
+ *              sequence's last key are never read).
+ * page_size    a multiple of 64 (each 64-key half of a 128-key tile is one copy).
+ * Per sequence the operation is attn_fwd's on its gathered keys (causal:
+ * query i of the sequence sees keys j <= i).  Slots of the last used page past
+ * seqlens_k[b] that share a 64-key half with a valid key are read with weight
+ * zero and must hold finite values; whole halves past it read zeros.
+ * Asynchronous on `stream`; argument errors return before any launch
+ * (page_size, num_pages or max_pages_per_seq out of range: ATTN_ERR_SHAPE).
+ */
+attn_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                           const int32_t* cu_seqlens_q, const int32_t* seqlens_k, const int32_t* block_table,
+                           int batch, int max_seqlen_q, int total_q, int num_pages, int page_size,
+                           int max_pages_per_seq, int H, int D, float scale, int causal, attn_stream_t stream);
+
+/*
  * attn_fwd_splitkv — the same forward with the keys of every (b, h, 128-row
  * query block) cut into `num_splits` contiguous ranges of 128-key tiles that
  * run as separate units of work, then merged (split-KV).  It raises the
@@ -180,7 +210,7 @@ attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream);
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 3
+#define ATTN_ABI_VERSION 4
 
 #ifdef __cplusplus
 }

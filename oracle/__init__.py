@@ -16,6 +16,9 @@ Contents:
   rows of one head, used for sampled parity at full size.
 * ``attention.attention_varlen_ref`` — the same definition for a packed batch
   of variable-length sequences (each sequence on its own tokens).
+* ``attention.attention_paged_ref`` — packed queries against a paged key/value
+  cache: each sequence's keys gathered through its page table, then the same
+  definition.
 * ``online.online_softmax_attention`` — the tiled online-softmax recurrence
   (running max, normaliser, numerator, each corrected by exp(m_old - m_new))
   from "Attention softmax fusion", section "The tile loop", and "Kernel Fusion
@@ -28,6 +31,7 @@ The oracle shares no code with the CUDA path: it reads float64 NumPy arrays
 and nothing else.
 """
 
-from .attention import attention_ref, attention_rows, attention_varlen_ref, valid_key_count  # noqa: F401
+from .attention import (attention_paged_ref, attention_ref, attention_rows, attention_varlen_ref,  # noqa: F401
+                        valid_key_count)
 from .online import online_softmax_attention  # noqa: F401
 from .merge import lse_merge  # noqa: F401

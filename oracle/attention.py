@@ -181,3 +181,44 @@ def attention_varlen_ref(q, k, v, cu_q, cu_k, scale: float, causal: bool = False
             out[qs:qe, h] = o_b
             lse[h, qs:qe] = l_b
     return out, lse
+
+
+def attention_paged_ref(q, k_cache, v_cache, cu_q, seqlens_k, block_table, scale: float, causal: bool = False):
+    """Exact attention of packed queries against a paged key/value cache.
+
+    ``q [total_q, H, D]`` with offsets ``cu_q`` (``batch + 1``);
+    ``k_cache``/``v_cache [num_pages, page_size, H, D]``; ``seqlens_k [batch]``;
+    ``block_table [batch, max_pages]``: key ``j`` of sequence ``b`` is slot
+    ``j % page_size`` of page ``block_table[b][j // page_size]`` (the paged
+    KV cache that "Fused Multi-Head Attention", section on continuous batching,
+    names as PagedAttention).  Each sequence is exact attention of its queries
+    on its gathered keys, as ``attention_varlen_ref``; ``seqlens_k`` is
+    clamped to ``[0, max_pages * page_size]``.
+
+    Returns ``(O [total_q, H, Dv], LSE [H, total_q])`` in float64."""
+    q = _as_f64(q)
+    k_cache = _as_f64(k_cache)
+    v_cache = _as_f64(v_cache)
+    total_q, H, _ = q.shape
+    page_size = k_cache.shape[1]
+    Dv = v_cache.shape[3]
+    table = np.asarray(block_table).reshape(len(seqlens_k), -1)
+    out = np.zeros((total_q, H, Dv), dtype=np.float64)
+    lse = np.full((H, total_q), -np.inf, dtype=np.float64)
+    cu_q = [int(x) for x in np.asarray(cu_q).reshape(-1)]
+    for b in range(len(cu_q) - 1):
+        qs, qe = cu_q[b], cu_q[b + 1]
+        if qe <= qs:
+            continue
+        n = min(max(int(seqlens_k[b]), 0), table.shape[1] * page_size)
+        # gather the sequence's keys in logical order
+        pages = [int(table[b, j // page_size]) for j in range(n)]
+        slots = [j % page_size for j in range(n)]
+        k_seq = k_cache[pages, slots] if n else np.zeros((0, H, k_cache.shape[3]))
+        v_seq = v_cache[pages, slots] if n else np.zeros((0, H, Dv))
+        rows = np.arange(qe - qs)
+        for h in range(H):
+            o_b, l_b = _head_rows(q[qs:qe, h], rows, k_seq[:, h], v_seq[:, h], scale, causal, n)
+            out[qs:qe, h] = o_b
+            lse[h, qs:qe] = l_b
+    return out, lse

@@ -90,3 +90,53 @@ def test_real_oracle_passes_reduced_pins():
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_pins_catch_planted_mistake(name):
     assert not _pins_pass(_mutant(name)), f"planted mistake {name} went unnoticed"
+
+
+PAGED_MUTATIONS = {
+    "page_and_slot_swapped": ("slots = [j % page_size for j in range(n)]", "slots = [j // page_size for j in range(n)]"),
+    "table_row_of_next_sequence": ("pages = [int(table[b, j // page_size]) for j in range(n)]",
+                                   "pages = [int(table[(b + 1) % table.shape[0], j // page_size]) for j in range(n)]"),
+    "seqlen_off_by_one": ("n = min(max(int(seqlens_k[b]), 0), table.shape[1] * page_size)",
+                          "n = min(max(int(seqlens_k[b]) - 1, 0), table.shape[1] * page_size)"),
+}
+
+
+def _paged_pins_pass(mod) -> bool:
+    """Shuffled page table against a per-key brute force (both masks)."""
+    rng = np.random.default_rng(9)
+    H, D, ps = 2, 3, 2
+    lens_q, lens_k = [3, 2], [5, 3]
+    table = rng.permutation(8)[:6].reshape(2, 3)
+    kc, vc = rng.normal(size=(8, ps, H, D)), rng.normal(size=(8, ps, H, D))
+    cu_q = np.array([0, 3, 5])
+    q = rng.normal(size=(5, H, D))
+    try:
+        for causal in (False, True):
+            O, L = mod.attention_paged_ref(q, kc, vc, cu_q, lens_k, table, 0.8, causal=causal)
+            for b in range(2):
+                for i in range(lens_q[b]):
+                    t = cu_q[b] + i
+                    for h in range(H):
+                        keys = [j for j in range(lens_k[b]) if not causal or j <= i]
+                        e = [math.exp(0.8 * math.fsum(q[t, h] * kc[table[b][j // ps], j % ps, h])) for j in keys]
+                        want = sum(w * vc[table[b][j // ps], j % ps, h] for w, j in zip(e, keys)) / math.fsum(e)
+                        if not np.allclose(O[t, h], want, rtol=1e-12, atol=1e-13):
+                            return False
+                        if abs(L[h, t] - math.log(math.fsum(e))) > 1e-12:
+                            return False
+    except Exception:
+        return False
+    return True
+
+
+def test_real_paged_oracle_passes_pins():
+    assert _paged_pins_pass(real)
+
+
+@pytest.mark.parametrize("name", sorted(PAGED_MUTATIONS))
+def test_paged_pins_catch_planted_mistake(name):
+    old, new = PAGED_MUTATIONS[name]
+    assert SRC.count(old) == 1, name
+    mod = types.ModuleType("oracle_paged_mutant_" + name)
+    exec(compile(SRC.replace(old, new), "<mutant " + name + ">", "exec"), mod.__dict__)
+    assert not _paged_pins_pass(mod), f"planted mistake {name} went unnoticed"

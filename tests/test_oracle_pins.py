@@ -425,3 +425,91 @@ def test_varlen_sequences_are_independent_and_match_brute_force():
                     want = sum(w * v[cu_k[b] + j, h] for w, j in zip(e, keys)) / den
                     np.testing.assert_allclose(O[t, h], want, rtol=1e-12, atol=1e-13)
                     assert abs(L[h, t] - math.log(den)) < 1e-12
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_paged_with_pages_in_order_is_varlen(causal):
+    """Pages laid out back to back in sequence order make the paged cache the
+    packed key tensor itself: the paged oracle must then equal the pinned
+    variable-length oracle exactly."""
+    from oracle import attention_paged_ref, attention_varlen_ref
+    H, D, ps = 2, 4, 3
+    lens_q = [4, 0, 6, 2]
+    lens_k = [6, 3, 5, 0]           # ragged last pages
+    pages_per = [(n + ps - 1) // ps for n in lens_k]
+    max_pages = max(pages_per)
+    num_pages = sum(pages_per)
+    # sequence b's keys occupy pages first_page[b] .. first_page[b] + pages_per[b] - 1
+    first = np.concatenate([[0], np.cumsum(pages_per)])[:-1]
+    table = np.full((4, max_pages), -7, dtype=np.int64)  # unused entries: never read
+    for b in range(4):
+        table[b, :pages_per[b]] = first[b] + np.arange(pages_per[b])
+    k_cache = _rand((num_pages, ps, H, D), 161)
+    v_cache = _rand((num_pages, ps, H, D), 162)
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)])
+    q = _rand((cu_q[-1], H, D), 163)
+    # the packed keys of the same sequences, taken from the page rows
+    flat_k = k_cache.reshape(num_pages * ps, H, D)
+    flat_v = v_cache.reshape(num_pages * ps, H, D)
+    idx = np.concatenate([first[b] * ps + np.arange(lens_k[b]) for b in range(4)]).astype(np.int64)
+    cu_k = np.concatenate([[0], np.cumsum(lens_k)])
+    O, L = attention_paged_ref(q, k_cache, v_cache, cu_q, lens_k, table, 0.7, causal=causal)
+    Ov, Lv = attention_varlen_ref(q, flat_k[idx], flat_v[idx], cu_q, cu_k, 0.7, causal=causal)
+    np.testing.assert_array_equal(O, Ov)
+    np.testing.assert_array_equal(L, Lv)
+
+
+def test_paged_scattered_pages_match_brute_force():
+    """A shuffled page table: every output checked by a loop that looks each
+    key up through the table on its own."""
+    from oracle import attention_paged_ref
+    rng = np.random.default_rng(171)
+    H, D, ps = 2, 3, 2
+    lens_q = [3, 2, 1]
+    lens_k = [5, 0, 3]
+    num_pages, max_pages = 9, 3
+    perm = rng.permutation(num_pages)
+    table = perm[:3 * max_pages].reshape(3, max_pages)
+    k_cache = _rand((num_pages, ps, H, D), 172)
+    v_cache = _rand((num_pages, ps, H, D), 173)
+    cu_q = np.concatenate([[0], np.cumsum(lens_q)])
+    q = _rand((cu_q[-1], H, D), 174)
+    for causal in (False, True):
+        O, L = attention_paged_ref(q, k_cache, v_cache, cu_q, lens_k, table, 0.9, causal=causal)
+        for b in range(3):
+            for i in range(lens_q[b]):
+                t = cu_q[b] + i
+                for h in range(H):
+                    keys = [j for j in range(lens_k[b]) if (not causal or j <= i)]
+                    if not keys:
+                        assert np.all(O[t, h] == 0) and L[h, t] == -np.inf
+                        continue
+                    kv = [(k_cache[table[b][j // ps], j % ps, h], v_cache[table[b][j // ps], j % ps, h])
+                          for j in keys]
+                    e = [math.exp(0.9 * math.fsum(q[t, h] * kk)) for kk, _ in kv]
+                    den = math.fsum(e)
+                    want = sum(w * vv for w, (_, vv) in zip(e, kv)) / den
+                    np.testing.assert_allclose(O[t, h], want, rtol=1e-12, atol=1e-13)
+                    assert abs(L[h, t] - math.log(den)) < 1e-12
+
+
+def test_paged_result_is_invariant_to_physical_page_order():
+    from oracle import attention_paged_ref
+    rng = np.random.default_rng(181)
+    H, D, ps = 1, 4, 4
+    num_pages = 6
+    table = np.array([[4, 1, 5], [0, 2, 3]])
+    lens_k = [10, 7]
+    cu_q = np.array([0, 5, 9])
+    k_cache = _rand((num_pages, ps, H, D), 182)
+    v_cache = _rand((num_pages, ps, H, D), 183)
+    q = _rand((9, H, D), 184)
+    O, L = attention_paged_ref(q, k_cache, v_cache, cu_q, lens_k, table, 0.5, causal=True)
+    perm = rng.permutation(num_pages)        # physical page p moves to slot perm[p]
+    k2 = np.empty_like(k_cache)
+    v2 = np.empty_like(v_cache)
+    k2[perm] = k_cache
+    v2[perm] = v_cache
+    O2, L2 = attention_paged_ref(q, k2, v2, cu_q, lens_k, perm[table], 0.5, causal=True)
+    np.testing.assert_array_equal(O, O2)
+    np.testing.assert_array_equal(L, L2)

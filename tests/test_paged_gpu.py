@@ -1,0 +1,113 @@
+"""GPU parity of the paged-KV forward against the fp64 oracle."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_86_gb300 import attn
+from exact_attention_86_gb300.build import build
+from oracle import attention_paged_ref
+
+from parity import check
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    build()
+    attn.lib()
+
+
+def _paged_case(lens_q, lens_k, H, D, page_size, seed, spare_pages=3):
+    """Random cache with shuffled pages.  Pages no sequence uses, and every
+    64-key half of a last page that lies wholly past the sequence's keys, hold
+    NaN: the kernel must never read them."""
+    g = torch.Generator().manual_seed(seed)
+    rng = np.random.default_rng(seed)
+    pages_per = [(n + page_size - 1) // page_size for n in lens_k]
+    used = int(sum(pages_per))
+    num_pages = used + spare_pages
+    max_pages = max(max(pages_per), 1) + 1
+    perm = rng.permutation(num_pages)
+    table = np.full((len(lens_k), max_pages), -1, dtype=np.int32)
+    at = 0
+    for b, n in enumerate(pages_per):
+        table[b, :n] = perm[at:at + n]
+        at += n
+    kc = torch.randn(num_pages, page_size, H, D, generator=g)
+    vc = torch.randn(num_pages, page_size, H, D, generator=g)
+    nan_mask = torch.ones(num_pages, page_size, dtype=torch.bool)
+    for b, n in enumerate(lens_k):
+        for j in range(0, n, 64):                      # halves that hold a valid key
+            pg = table[b, j // page_size]
+            nan_mask[pg, j % page_size:j % page_size + 64] = False
+    kc[nan_mask] = float("nan")
+    vc[nan_mask] = float("nan")
+    kc, vc = kc.to(torch.bfloat16), vc.to(torch.bfloat16)
+    tq = int(sum(lens_q))
+    q = torch.randn(tq, H, D, generator=g).to(torch.bfloat16)
+    cu_q = torch.tensor(np.concatenate([[0], np.cumsum(lens_q)]), dtype=torch.int32)
+    seqlens_k = torch.tensor(lens_k, dtype=torch.int32)
+    return q, kc, vc, cu_q, seqlens_k, torch.from_numpy(table)
+
+
+def _np(t):
+    return t.float().numpy().astype(np.float64)
+
+
+def _run(q, kc, vc, cu_q, sk, table, max_q, scale, causal):
+    dev = torch.device("cuda:0")
+    o, lse = attn.forward_paged(q.to(dev), kc.to(dev), vc.to(dev), cu_q.to(dev), sk.to(dev), table.to(dev), max_q,
+                                scale=scale, causal=causal)
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, (st, site)
+    return o.float().cpu().numpy(), lse.cpu().numpy()
+
+
+CASES = [
+    # lens_q, lens_k
+    ([300, 1, 128, 129, 0, 64], [300, 1, 128, 129, 7, 65]),    # prefill-like, one empty query set
+    ([1, 1, 1, 1, 1], [1000, 0, 63, 64, 257]),                  # decode: one query per sequence
+    ([200, 70], [450, 130]),                                    # Sq != Sk per sequence
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+@pytest.mark.parametrize("page_size", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_paged_matches_oracle(case, page_size, causal, D):
+    lens_q, lens_k = CASES[case]
+    H = 2
+    q, kc, vc, cu_q, sk, table = _paged_case(lens_q, lens_k, H, D, page_size, seed=case * 13 + page_size + D)
+    scale = 1.0 / math.sqrt(D)
+    o, lse = _run(q, kc, vc, cu_q, sk, table, max(lens_q), scale, causal)
+    o_ref, l_ref = attention_paged_ref(_np(q), _np(kc), _np(vc), cu_q.numpy(), sk.numpy(), table.numpy(), scale,
+                                       causal=causal)
+    check(o.transpose(1, 0, 2), lse, o_ref.transpose(1, 0, 2), l_ref,
+          f"paged case {case} page {page_size} causal={causal} D={D}")
+
+
+def test_paged_in_order_pages_equal_varlen_bitwise():
+    """Pages laid out in sequence order turn the cache into the packed keys:
+    the paged and variable-length forwards then compute identical bits."""
+    H, D, ps = 4, 128, 128
+    lens = [384, 256, 512]
+    g = torch.Generator().manual_seed(21)
+    dev = torch.device("cuda:0")
+    total = sum(lens)
+    q = torch.randn(total, H, D, generator=g).to(torch.bfloat16).to(dev)
+    k = torch.randn(total, H, D, generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn(total, H, D, generator=g).to(torch.bfloat16).to(dev)
+    cu = torch.tensor([0, 384, 640, 1152], dtype=torch.int32, device=dev)
+    table = torch.tensor([[0, 1, 2, 0], [3, 4, 0, 0], [5, 6, 7, 8]], dtype=torch.int32, device=dev)
+    sk = torch.tensor(lens, dtype=torch.int32, device=dev)
+    o_v, l_v = attn.forward_varlen(q, k, v, cu, cu, max(lens), causal=True)
+    o_p, l_p = attn.forward_paged(q, k.view(total // ps, ps, H, D), v.view(total // ps, ps, H, D), cu, sk, table,
+                                  max(lens), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o_v.view(torch.int16), o_p.view(torch.int16))
+    assert torch.equal(l_v, l_p)

@@ -108,3 +108,45 @@ def test_varlen_equals_padded_forward_for_equal_lengths():
     # same kernel, same arithmetic order per row: identical bits
     assert torch.equal(o_var.view(torch.int16), pack(o_pad).view(torch.int16))
     assert torch.equal(l_var, l_pad.permute(1, 0, 2).reshape(H, B * S))
+
+
+@pytest.mark.parametrize("name", ["varlen_b32_d128_causal", "varlen_b32_d128"])
+def test_varlen_benchmark_workload_sampled(name):
+    """The benchmarked packed batch at full size, in the benchmark's launch
+    configuration; sampled rows of the shortest, the longest and two other
+    sequences on the first and last head against the oracle."""
+    from exact_attention_86_gb300 import workloads
+    from oracle import attention_rows
+
+    w = workloads.VARLEN_WORKLOADS[name]
+    q, k, v, cu = workloads.generate_varlen(w)
+    o, lse = _run(q, k, v, cu, cu, w.max_len, w.scale, w.causal)
+    lens = (cu[1:] - cu[:-1]).numpy()
+    picks = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 3, 17})
+    rng = np.random.default_rng(5)
+    for b in picks:
+        a, e = int(cu[b]), int(cu[b + 1])
+        n = e - a
+        rows = sorted(set(rng.integers(0, n, size=min(n, 24)).tolist()) | {0, n - 1})
+        for h in (0, w.H - 1):
+            o_ref, l_ref = attention_rows(_np(q[a:e, h]), _np(k[a:e, h]), _np(v[a:e, h]), rows, w.scale,
+                                          causal=w.causal)
+            check(o[a:e, h][rows], lse[h, a:e][rows], o_ref, l_ref, f"{name} seq {b} head {h}")
+
+
+def test_varlen_repeated_launches_are_bitwise_identical():
+    """50 back-to-back launches of the benchmarked causal packed batch: every
+    launch must give the same bits and no wait may give up."""
+    from exact_attention_86_gb300 import workloads
+
+    w = workloads.VARLEN_WORKLOADS["varlen_b32_d128_causal"]
+    q, k, v, cu = workloads.generate_varlen(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, cud = q.to(dev), k.to(dev), v.to(dev), cu.to(dev)
+    o0, l0 = attn.forward_varlen(qd, kd, vd, cud, cud, w.max_len, causal=True)
+    outs = [attn.forward_varlen(qd, kd, vd, cud, cud, w.max_len, causal=True) for _ in range(49)]
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, (st, site)
+    for i, (o, lse) in enumerate(outs, 1):
+        assert torch.equal(o.view(torch.int16), o0.view(torch.int16)), f"launch {i} differs"
+        assert torch.equal(lse, l0), f"launch {i} LSE differs"
