@@ -11,7 +11,9 @@ resident in HBM; every step re-reads 192 MiB of Q/K/V (plus 64 MiB of O
 written), more than the 129 MB L2, so no explicit flush is needed.  Smaller
 workloads (``--workload``) get a 256 MiB L2 flush before every timed launch and
 report the launch time alone.  The ``varlen_*`` workloads time
-``attn_fwd_varlen`` on a packed batch of variable-length sequences.
+``attn_fwd_varlen`` on a packed batch of variable-length sequences, the
+``paged_*`` ones ``attn_fwd_paged`` on the same batch with its keys and values
+in a paged cache.
 
 Under torchrun (N > 1) every rank runs the same workload on its own GPU (weak
 scaling: the attention units shard with no exchange step); the barrier and the
@@ -200,27 +202,100 @@ def blas_threads() -> int:
 
 def lookup(name):
     from exact_attention_86_gb300 import workloads
-    if name in workloads.WORKLOADS:
-        return workloads.WORKLOADS[name]
-    if name in workloads.VARLEN_WORKLOADS:
-        return workloads.VARLEN_WORKLOADS[name]
-    raise SystemExit(f"unknown workload {name}; known: "
-                     f"{sorted(workloads.WORKLOADS) + sorted(workloads.VARLEN_WORKLOADS)}")
+    for table in (workloads.WORKLOADS, workloads.VARLEN_WORKLOADS, workloads.PAGED_WORKLOADS):
+        if name in table:
+            return table[name]
+    known = sorted(workloads.WORKLOADS) + sorted(workloads.VARLEN_WORKLOADS) + sorted(workloads.PAGED_WORKLOADS)
+    raise SystemExit(f"unknown workload {name}; known: {known}")
 
 
 def is_varlen(w) -> bool:
+    """Packed variable-length workloads (paged ones included)."""
     from exact_attention_86_gb300 import workloads
     return isinstance(w, workloads.VarlenWorkload)
 
 
+def is_paged(w) -> bool:
+    from exact_attention_86_gb300 import workloads
+    return isinstance(w, workloads.PagedWorkload)
+
+
 def generate(w, draw: int):
-    """(q, k, v, extra): extra is kv_lens (padded) or the offsets (varlen)."""
+    """(q, k, v, extra) with packed or padded keys: extra is kv_lens (padded)
+    or the offsets (varlen; for a paged workload these are the same tokens
+    its cache holds)."""
     from exact_attention_86_gb300 import workloads
     if is_varlen(w):
         if draw != 0:
             raise SystemExit(f"workload {w.name} has a single draw")
         return workloads.generate_varlen(w)
     return workloads.generate(w, draw)
+
+
+class Job:
+    """Device buffers and the step of one workload.  ``inputs`` are (host,
+    device) pairs the end-to-end step copies in; ``outputs`` the device
+    tensors it copies back."""
+
+    def __init__(self, w, args, dev, attn, torch):
+        from exact_attention_86_gb300 import workloads
+        self.stream = torch.cuda.current_stream(dev)
+        sptr = self.stream.cuda_stream
+        if args.splits > 0 and is_varlen(w):
+            raise SystemExit("--splits applies to padded workloads only")
+        if is_paged(w):
+            q, kc, vc, cu, sk, table = workloads.generate_paged(w)
+            host = [q, kc, vc, cu, sk, table]
+        else:
+            q, k, v, kv = generate(w, args.draw)
+            host = [q, k, v] + ([kv] if kv is not None else [])
+        dev_t = [t.to(dev) for t in host]
+        self.inputs = list(zip(host, dev_t))
+        o = torch.empty_like(dev_t[0])
+        if is_varlen(w):
+            lse = torch.empty(w.H, q.shape[0], dtype=torch.float32, device=dev)
+        else:
+            lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev)
+        self.outputs = [o, lse]
+        ptr = [t.data_ptr() for t in dev_t]
+        total = q.shape[0]
+        ws = None
+        if args.splits > 0:
+            ws_bytes = attn.attn_fwd_splitkv_workspace_size(w.B, w.H, w.Sq, w.D, args.splits)
+            ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+        self.launches_per_step = 2 if ws is not None else 1
+
+        if is_paged(w):
+            num_pages, page_size, max_pages = kc.shape[0], kc.shape[1], table.shape[1]
+
+            def call():
+                return attn.attn_fwd_paged(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), ptr[3], ptr[4],
+                                           ptr[5], w.batch, w.max_len, total, num_pages, page_size, max_pages, w.H,
+                                           w.D, w.scale, int(w.causal), sptr)
+        elif is_varlen(w):
+            def call():
+                return attn.attn_fwd_varlen(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), ptr[3], ptr[3],
+                                            w.batch, w.max_len, total, total, w.H, w.D, w.scale, int(w.causal), sptr)
+        elif ws is None:
+            kv_ptr = ptr[3] if len(ptr) > 3 else None
+
+            def call():
+                return attn.attn_fwd(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), w.B, w.H, w.Sq, w.Sk,
+                                     w.D, w.scale, int(w.causal), kv_ptr, sptr)
+        else:
+            kv_ptr = ptr[3] if len(ptr) > 3 else None
+
+            def call():
+                return attn.attn_fwd_splitkv(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), w.B, w.H, w.Sq,
+                                             w.Sk, w.D, w.scale, int(w.causal), kv_ptr, args.splits, ws.data_ptr(),
+                                             ws.numel(), sptr)
+        self._call = call
+        self._attn = attn
+
+    def step(self):
+        st = self._call()
+        if st != self._attn.ATTN_OK:
+            raise self._attn.AttnError(st, "forward")
 
 
 def run_reference(args, w):
@@ -290,41 +365,11 @@ def main():
         dist.barrier()
     attn.lib()
 
-    q, k, v, kv = generate(w, args.draw)
-    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
-    kvd = kv.to(dev) if kv is not None else None
-    o = torch.empty_like(qd)
-    if varlen:
-        lse = torch.empty(w.H, q.shape[0], dtype=torch.float32, device=dev)
-    else:
-        lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    job = Job(w, args, dev, attn, torch)
+    stream = job.stream
     sptr = stream.cuda_stream
-    kv_ptr = kvd.data_ptr() if kvd is not None else None
-    if varlen and args.splits > 0:
-        raise SystemExit("--splits applies to padded workloads only")
-
-    ws = None
-    if args.splits > 0:
-        ws_bytes = attn.attn_fwd_splitkv_workspace_size(w.B, w.H, w.Sq, w.D, args.splits)
-        ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-    max_len = w.max_len if varlen else 0
-
-    def step():
-        if varlen:
-            total = q.shape[0]
-            st = attn.attn_fwd_varlen(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                      kv_ptr, kv_ptr, w.batch, max_len, total, total, w.H, w.D, w.scale,
-                                      int(w.causal), sptr)
-        elif ws is None:
-            st = attn.attn_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                               w.B, w.H, w.Sq, w.Sk, w.D, w.scale, int(w.causal), kv_ptr, sptr)
-        else:
-            st = attn.attn_fwd_splitkv(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                       w.B, w.H, w.Sq, w.Sk, w.D, w.scale, int(w.causal), kv_ptr, args.splits,
-                                       ws.data_ptr(), ws.numel(), sptr)
-        if st != attn.ATTN_OK:
-            raise attn.AttnError(st, "attn_fwd")
+    step = job.step
+    o, lse = job.outputs
 
     # Workloads whose bytes fit in L2 get an L2 flush (a 256 MiB write) before
     # every timed launch; the launch events bracket the kernel alone.
@@ -380,22 +425,15 @@ def main():
     clocks = sampler.summary(wall0, wall1)
 
     # ------------------------------------------------------------ end to end
-    qh = q.pin_memory()
-    kh = k.pin_memory()
-    vh = v.pin_memory()
-    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    cuh = kv.pin_memory() if varlen else None
+    pinned = [(h.pin_memory(), d) for h, d in job.inputs]
+    outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in job.outputs]
 
     def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        if varlen:
-            kvd.copy_(cuh, non_blocking=True)
+        for h, d in pinned:
+            d.copy_(h, non_blocking=True)
         step()
-        oh.copy_(o, non_blocking=True)
-        lh.copy_(lse, non_blocking=True)
+        for h, d in zip(outs_h, job.outputs):
+            h.copy_(d, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -412,8 +450,8 @@ def main():
         t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t[0])
-    h2d = (q.numel() + k.numel() + v.numel()) * 2 + (kv.numel() * 4 if varlen else 0)
-    d2h = o.numel() * 2 + lse.numel() * 4
+    h2d = sum(h.numel() * h.element_size() for h, _ in pinned)
+    d2h = sum(t.numel() * t.element_size() for t in job.outputs)
 
     # -------------------------------------------------------------- roofline
     peaks = measured_peaks()
@@ -432,6 +470,7 @@ def main():
     # ----------------------------------------------------------- CPU oracle
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
+        q, k, v, kv = generate(w, args.draw)
         flops, secs, blocks = cpu_oracle_steps(w, q, k, v, kv, n_steps=None, budget_s=args.cpu_budget_s)
         cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                "sample": f"{blocks} query blocks of 256 rows of head 0 of "
@@ -456,7 +495,7 @@ def main():
             "e2e": {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "clocks": clocks,
-            "gpu_launches": args.steps * (2 if args.splits > 0 else 1),
+            "gpu_launches": args.steps * job.launches_per_step,
             "pct_of_peak": 100.0 * value / world / peak,
         }
         print(json.dumps(line), flush=True)

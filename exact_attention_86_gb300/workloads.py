@@ -188,3 +188,55 @@ def generate_varlen(w: VarlenWorkload):
     cu = torch.zeros(w.batch + 1, dtype=torch.int32)
     cu[1:] = torch.cumsum(lens, 0).to(torch.int32)
     return q, k, v, cu
+
+
+@dataclass(frozen=True)
+class PagedWorkload(VarlenWorkload):
+    """The packed batch of a ``VarlenWorkload`` with its keys and values in a
+    paged cache: after the packed q, k, v the same generator draws
+    ``torch.randperm(num_pages)``, which places the sequences' pages (filled
+    in order, ``page_size`` tokens each) at shuffled physical pages."""
+    page_size: int = 256
+
+    def label(self) -> str:
+        return super().label() + f", paged KV cache ({self.page_size}-token pages, shuffled)"
+
+
+PAGED_WORKLOADS = {
+    "paged_b32_d128_causal": PagedWorkload("paged_b32_d128_causal", 32, 16, 128, 1, 4096, True, seed=6,
+                                           page_size=256),
+}
+
+
+def generate_paged(w: PagedWorkload):
+    """Return ``(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table)``
+    on the CPU; the queries and the per-sequence keys are those of
+    ``generate_varlen`` for the same workload."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    lens = torch.randint(w.len_lo, w.len_hi + 1, (w.batch,), generator=g, dtype=torch.int64)
+    total = int(lens.sum())
+    shape = (total, w.H, w.D)
+    q = (torch.randn(shape, generator=g, dtype=torch.float32) * w.std).to(torch.bfloat16)
+    k = (torch.randn(shape, generator=g, dtype=torch.float32) * w.std).to(torch.bfloat16)
+    v = (torch.randn(shape, generator=g, dtype=torch.float32) * w.std).to(torch.bfloat16)
+    ps = w.page_size
+    pages_per = [(int(n) + ps - 1) // ps for n in lens]
+    num_pages = sum(pages_per)
+    perm = torch.randperm(num_pages, generator=g)
+    k_cache = torch.zeros((num_pages, ps, w.H, w.D), dtype=torch.bfloat16)
+    v_cache = torch.zeros((num_pages, ps, w.H, w.D), dtype=torch.bfloat16)
+    table = torch.zeros((w.batch, max(pages_per)), dtype=torch.int32)
+    cu = torch.zeros(w.batch + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(lens, 0).to(torch.int32)
+    at = 0
+    for b, n_pages in enumerate(pages_per):
+        for i in range(n_pages):
+            pg = int(perm[at + i])
+            table[b, i] = pg
+            t0 = int(cu[b]) + i * ps
+            t1 = min(int(cu[b + 1]), t0 + ps)
+            k_cache[pg, :t1 - t0] = k[t0:t1]
+            v_cache[pg, :t1 - t0] = v[t0:t1]
+        at += n_pages
+    return q, k_cache, v_cache, cu, lens.to(torch.int32), table

@@ -111,3 +111,25 @@ def test_paged_in_order_pages_equal_varlen_bitwise():
     torch.cuda.synchronize()
     assert torch.equal(o_v.view(torch.int16), o_p.view(torch.int16))
     assert torch.equal(l_v, l_p)
+
+
+def test_paged_benchmark_workload_equals_varlen_bitwise():
+    """The benchmarked paged batch at full size, in the benchmark's launch
+    configuration: the shuffled pages hold the same tokens as the packed batch
+    (whose parity against the oracle is tested at full size), and the kernel
+    stages the same tiles either way, so the bits must agree."""
+    from exact_attention_86_gb300 import workloads
+
+    w = workloads.PAGED_WORKLOADS["paged_b32_d128_causal"]
+    q, kc, vc, cu, sk, table = workloads.generate_paged(w)
+    _, k, v, cu2 = workloads.generate_varlen(w)
+    assert torch.equal(cu, cu2)
+    dev = torch.device("cuda:0")
+    qd, cud = q.to(dev), cu.to(dev)
+    o_p, l_p = attn.forward_paged(qd, kc.to(dev), vc.to(dev), cud, sk.to(dev), table.to(dev), w.max_len,
+                                  causal=w.causal)
+    o_v, l_v = attn.forward_varlen(qd, k.to(dev), v.to(dev), cud, cud, w.max_len, causal=w.causal)
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, (st, site)
+    assert torch.equal(o_p.view(torch.int16), o_v.view(torch.int16))
+    assert torch.equal(l_p, l_v)
