@@ -182,3 +182,28 @@ def test_varlen_argument_checks(lib, args, code):
     st = attn.attn_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"], a["batch"], a["maxq"],
                               a["tq"], a["tk"], a["H"], a["D"], a["scale"], 0, None)
     assert st == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(D=100), attn.ATTN_ERR_UNSUPPORTED_D),
+    (dict(ps=96), attn.ATTN_ERR_SHAPE),
+    (dict(ps=32), attn.ATTN_ERR_SHAPE),
+    (dict(npg=0), attn.ATTN_ERR_SHAPE),
+    (dict(mp=0), attn.ATTN_ERR_SHAPE),
+    (dict(npg=1 << 30), attn.ATTN_ERR_SHAPE),
+    (dict(bt=0), attn.ATTN_ERR_NULLPTR),
+    (dict(sk=0), attn.ATTN_ERR_NULLPTR),
+    (dict(kc=A + 8), attn.ATTN_ERR_ALIGN),
+    (dict(bt=A + 2), attn.ATTN_ERR_ALIGN),
+    (dict(scale=float("inf")), attn.ATTN_ERR_SCALE),
+    (dict(batch=0), attn.ATTN_OK),
+    (dict(tq=0), attn.ATTN_OK),
+])
+def test_paged_argument_checks(lib, args, code):
+    # every case ends in a host-side check (no launch, with or without a GPU)
+    a = dict(q=A, kc=A, vc=A, o=A, lse=A, cq=A, sk=A, bt=A, batch=3, maxq=300, tq=600, npg=40, ps=128, mp=8, H=4,
+             D=128, scale=0.1)
+    a.update(args)
+    st = attn.attn_fwd_paged(a["q"], a["kc"], a["vc"], a["o"], a["lse"], a["cq"], a["sk"], a["bt"], a["batch"],
+                             a["maxq"], a["tq"], a["npg"], a["ps"], a["mp"], a["H"], a["D"], a["scale"], 0, None)
+    assert st == code
