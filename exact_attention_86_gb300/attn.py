@@ -51,6 +51,10 @@ SIGNATURES = {
                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                         ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "attn_fwd_splitkv_noalloc": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p,
+                                                ctypes.c_int, ctypes.c_void_p]),
     "attn_lse_merge": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_void_p]),
     "attn_get_error_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -117,6 +121,13 @@ def attn_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, S
                      workspace_bytes: int, stream: Optional[int]) -> int:
     return lib().attn_fwd_splitkv(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, num_splits,
                                   workspace, workspace_bytes, stream)
+
+
+def attn_fwd_splitkv_noalloc(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
+                             scale: float, causal: int, kv_lens: Optional[int], num_splits: int,
+                             stream: Optional[int]) -> int:
+    return lib().attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, num_splits,
+                                          stream)
 
 
 def attn_lse_merge(o_parts: int, lse_parts: int, num_parts: int, o: int, lse: int, rows: int, D: int,

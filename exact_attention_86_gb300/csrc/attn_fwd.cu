@@ -84,6 +84,11 @@ enum WaitSite : uint32_t {
 // [0]: 1 once any wait gave up; [1]: site of the first one; [2]: its block.
 __device__ uint32_t g_attn_status[3];
 
+// Fixed split-KV scratch of attn_fwd_splitkv_noalloc: a static device array,
+// instantiated once in every device context that loads the library, so that
+// entry point needs neither an allocation nor a caller workspace.
+__device__ __align__(256) uint8_t g_splitkv_scratch[ATTN_SPLITKV_SCRATCH_BYTES];
+
 template <int D>
 struct Geo {
   static_assert(D == 64 || D == 128, "head dim");
@@ -840,6 +845,7 @@ struct DeviceInfo {
   int supported = 0;
   int num_sms = 0;
   bool smem_set[4] = {false, false, false, false};
+  void* scratch = nullptr;  // this device's address of g_splitkv_scratch
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -1237,6 +1243,29 @@ attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* 
   st = run_forward(*dev, q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, num_splits, o_part, lse_part, s);
   if (st != ATTN_OK) return st;
   return launch_merge(*dev, o_part, lse_part, num_splits, static_cast<long long>(B) * H * Sq, D, o, lse, s);
+}
+
+attn_status attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                     int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens,
+                                     int num_splits, attn_stream_t stream) {
+  attn_status st = check_args(q, k, v, o, lse, B, H, Sq, Sk, D, scale, kv_lens, num_splits);
+  if (st != ATTN_OK || B == 0 || H == 0 || Sq == 0) return st;
+  if (splitkv_bytes(B, H, Sq, D, num_splits, nullptr) > static_cast<size_t>(ATTN_SPLITKV_SCRATCH_BYTES))
+    return ATTN_ERR_WORKSPACE;
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (dev->scratch == nullptr && cudaGetSymbolAddress(&dev->scratch, g_splitkv_scratch) != cudaSuccess) {
+      dev->scratch = nullptr;
+      return ATTN_ERR_CUDA;
+    }
+    scratch = dev->scratch;
+  }
+  return attn_fwd_splitkv(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, num_splits, scratch,
+                          static_cast<size_t>(ATTN_SPLITKV_SCRATCH_BYTES), stream);
 }
 
 attn_status attn_lse_merge(const float* o_parts, const float* lse_parts, int num_parts, void* o, float* lse,

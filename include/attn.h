@@ -25,8 +25,9 @@
  * All entry points are host functions; device pointers are plain CUDA device
  * (or managed) addresses on the CURRENT device.  The caller allocates and owns
  * every buffer (including the split-KV workspace).  The library allocates no
- * device memory: its only device state is one status word per device, a
- * static __device__ variable in the library.
+ * device memory: its only device state is one status word per device and the
+ * fixed scratch of attn_fwd_splitkv_noalloc, static __device__ variables in
+ * the library.
  */
 #ifndef EXACT_ATTENTION_86_GB300_ATTN_H
 #define EXACT_ATTENTION_86_GB300_ATTN_H
@@ -167,6 +168,23 @@ attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* 
                              void* workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_fwd_splitkv_noalloc — attn_fwd_splitkv without a caller workspace and
+ * without any allocation: the partial results go to a fixed scratch array of
+ * ATTN_SPLITKV_SCRATCH_BYTES bytes that the library holds in device memory
+ * (a static __device__ array, one per device; its address is looked up for
+ * the current device).  Arguments as attn_fwd_splitkv minus the workspace.
+ * A call whose attn_fwd_splitkv_workspace_size(B, H, Sq, D, num_splits)
+ * exceeds the scratch returns ATTN_ERR_WORKSPACE before any CUDA call.
+ * All calls of this entry point on one device share the scratch, so they
+ * must not overlap on the GPU (issue them on one stream, or order them).
+ */
+#define ATTN_SPLITKV_SCRATCH_BYTES (32u << 20)
+
+attn_status attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                     int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens,
+                                     int num_splits, attn_stream_t stream);
+
+/*
  * attn_lse_merge — combine attention results computed over disjoint key sets
  * into the result over their union ("Kernel Fusion and the Memory Wall",
  * section "FlashAttention: avoid the full score matrix": rescale each part by
@@ -210,7 +228,7 @@ attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream);
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 4
+#define ATTN_ABI_VERSION 5
 
 #ifdef __cplusplus
 }
