@@ -19,6 +19,9 @@ Contents:
 * ``attention.attention_paged_ref`` — packed queries against a paged key/value
   cache: each sequence's keys gathered through its page table, then the same
   definition.
+* ``fp8.decode_e4m3`` / ``fp8.attention_fp8_ref`` — E4M3 codes decoded from
+  the format definition, and exact attention of FP8 inputs with per-tensor
+  descales.
 * ``online.online_softmax_attention`` — the tiled online-softmax recurrence
   (running max, normaliser, numerator, each corrected by exp(m_old - m_new))
   from "Attention softmax fusion", section "The tile loop", and "Kernel Fusion
@@ -35,3 +38,4 @@ from .attention import (attention_paged_ref, attention_ref, attention_rows, atte
                         valid_key_count)
 from .online import online_softmax_attention  # noqa: F401
 from .merge import lse_merge  # noqa: F401
+from .fp8 import attention_fp8_ref, decode_e4m3  # noqa: F401
