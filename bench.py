@@ -154,6 +154,9 @@ def oracle_heads(w, q, k, v, kv):
     from exact_attention_86_gb300 import workloads
 
     f64 = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    if isinstance(w, workloads.Fp8Workload):
+        from oracle import decode_e4m3
+        f64 = lambda t: decode_e4m3(t.numpy()) * w.descale  # noqa: E731
     if isinstance(w, workloads.VarlenWorkload):
         cu = [int(x) for x in kv]
         return [(f64(q[a:b, 0]), f64(k[a:b, 0]), f64(v[a:b, 0]), None)
@@ -202,10 +205,11 @@ def blas_threads() -> int:
 
 def lookup(name):
     from exact_attention_86_gb300 import workloads
-    for table in (workloads.WORKLOADS, workloads.VARLEN_WORKLOADS, workloads.PAGED_WORKLOADS):
+    tables = (workloads.WORKLOADS, workloads.VARLEN_WORKLOADS, workloads.PAGED_WORKLOADS, workloads.FP8_WORKLOADS)
+    for table in tables:
         if name in table:
             return table[name]
-    known = sorted(workloads.WORKLOADS) + sorted(workloads.VARLEN_WORKLOADS) + sorted(workloads.PAGED_WORKLOADS)
+    known = sorted(n for table in tables for n in table)
     raise SystemExit(f"unknown workload {name}; known: {known}")
 
 
@@ -220,15 +224,24 @@ def is_paged(w) -> bool:
     return isinstance(w, workloads.PagedWorkload)
 
 
+def is_fp8(w) -> bool:
+    from exact_attention_86_gb300 import workloads
+    return isinstance(w, workloads.Fp8Workload)
+
+
 def generate(w, draw: int):
     """(q, k, v, extra) with packed or padded keys: extra is kv_lens (padded)
     or the offsets (varlen; for a paged workload these are the same tokens
     its cache holds)."""
     from exact_attention_86_gb300 import workloads
-    if is_varlen(w):
+    if is_varlen(w) or is_fp8(w):
         if draw != 0:
             raise SystemExit(f"workload {w.name} has a single draw")
+    if is_varlen(w):
         return workloads.generate_varlen(w)
+    if is_fp8(w):
+        q8, k8, v8, _, kv = workloads.generate_fp8(w)
+        return q8, k8, v8, kv
     return workloads.generate(w, draw)
 
 
@@ -246,12 +259,15 @@ class Job:
         if is_paged(w):
             q, kc, vc, cu, sk, table = workloads.generate_paged(w)
             host = [q, kc, vc, cu, sk, table]
+        elif is_fp8(w):
+            q, k8, _, vt8, kv = workloads.generate_fp8(w)
+            host = [q, k8, vt8] + ([kv] if kv is not None else [])
         else:
             q, k, v, kv = generate(w, args.draw)
             host = [q, k, v] + ([kv] if kv is not None else [])
         dev_t = [t.to(dev) for t in host]
         self.inputs = list(zip(host, dev_t))
-        o = torch.empty_like(dev_t[0])
+        o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
         if is_varlen(w):
             lse = torch.empty(w.H, q.shape[0], dtype=torch.float32, device=dev)
         else:
@@ -272,6 +288,12 @@ class Job:
                 return attn.attn_fwd_paged(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), ptr[3], ptr[4],
                                            ptr[5], w.batch, w.max_len, total, num_pages, page_size, max_pages, w.H,
                                            w.D, w.scale, int(w.causal), sptr)
+        elif is_fp8(w):
+            kv_ptr = ptr[3] if len(ptr) > 3 else None
+
+            def call():
+                return attn.attn_fwd_fp8(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), w.B, w.H, w.Sq, w.Sk,
+                                         w.D, w.scale, int(w.causal), kv_ptr, w.descale, w.descale, w.descale, sptr)
         elif is_varlen(w):
             def call():
                 return attn.attn_fwd_varlen(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), ptr[3], ptr[3],
@@ -461,6 +483,11 @@ def main():
     else:
         peak = FALLBACK_PEAK_TFLOPS
         peak_src = "fallback (1.9 PFLOP/s bf16 burst)"
+    if is_fp8(w):
+        # the E4M3 contraction's own peak: the bf16 figure times the nominal
+        # dense fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
+        peak *= 2.0
+        peak_src += " x 2 (nominal dense fp8 / bf16 ratio)"
     achieved = w.flops / (launch_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": recorded_traffic(w.name), "kernel": "attn_fwd_kernel", "peak_source": peak_src,
@@ -481,9 +508,10 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "e4m3" if is_fp8(w) else "bf16", "data": "synthetic",
             "config": {"workload": w.name, "shape": w.label(), "draw": args.draw,
-                       "inputs": f"bf16 N(0,{(w.std if args.draw == 0 else w.second_std) ** 2:g}) seed {w.seed}",
+                       "inputs": f"{'e4m3' if is_fp8(w) else 'bf16'} "
+                                 f"N(0,{(w.std if args.draw == 0 else w.second_std) ** 2:g}) seed {w.seed}",
                        "l2": (f"flushed: a 256 MiB write before every timed launch (the workload moves "
                               f"{w.min_bytes / 2**20:.1f} MiB)") if flush is not None else
                              (f"no flush: each step moves {w.min_bytes / 2**20:.0f} MiB of Q/K/V/O/LSE, more "

@@ -36,6 +36,10 @@ SIGNATURES = {
     "attn_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "attn_fwd_fp8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                    ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
+                                    ctypes.c_float, ctypes.c_float, ctypes.c_void_p]),
     "attn_fwd_varlen": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
@@ -96,6 +100,13 @@ def lib():
 def attn_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
              scale: float, causal: int, kv_lens: Optional[int], stream: Optional[int]) -> int:
     return lib().attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, stream)
+
+
+def attn_fwd_fp8(q: int, k: int, v_t: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
+                 scale: float, causal: int, kv_lens: Optional[int], q_descale: float, k_descale: float,
+                 v_descale: float, stream: Optional[int]) -> int:
+    return lib().attn_fwd_fp8(q, k, v_t, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, q_descale, k_descale,
+                              v_descale, stream)
 
 
 def attn_fwd_varlen(q: int, k: int, v: int, o: int, lse: int, cu_q: int, cu_k: int, batch: int,
@@ -198,6 +209,37 @@ def forward_splitkv(q, k, v, num_splits: int, scale: Optional[float] = None, cau
                               workspace.data_ptr(), workspace.numel() * workspace.element_size(), stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_splitkv")
+    return out, lse
+
+
+def forward_fp8(q8, k8, v8_t, q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0,
+                scale: Optional[float] = None, causal: bool = False, kv_lens=None):
+    """FP8 forward on torch CUDA tensors of E4M3 codes (``torch.uint8`` or
+    ``torch.float8_e4m3fn``): ``q8 [B,H,Sq,D]``, ``k8 [B,H,Sk,D]`` and
+    ``v8_t [B,H,D,Sk]`` (V transposed).  Returns ``(o bf16 [B,H,Sq,D],
+    lse fp32 [B,H,Sq])``."""
+    import torch
+
+    for name, t in (("q8", q8), ("k8", k8), ("v8_t", v8_t)):
+        if t.element_size() != 1 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
+            raise ValueError(f"{name} must be a contiguous 4-d CUDA tensor of 1-byte E4M3 codes")
+    B, H, Sq, D = q8.shape
+    Sk = k8.shape[2]
+    if tuple(k8.shape) != (B, H, Sk, D) or tuple(v8_t.shape) != (B, H, D, Sk):
+        raise ValueError("k8 must be [B,H,Sk,D] and v8_t [B,H,D,Sk]")
+    if kv_lens is not None and (kv_lens.dtype != torch.int32 or kv_lens.device != q8.device):
+        raise ValueError("kv_lens must be int32 on q's device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=q8.device)
+    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q8.device)
+    with torch.cuda.device(q8.device):
+        stream = torch.cuda.current_stream(q8.device).cuda_stream
+        st = attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8_t.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Sq,
+                          Sk, D, float(scale), int(bool(causal)), None if kv_lens is None else kv_lens.data_ptr(),
+                          float(q_descale), float(k_descale), float(v_descale), stream)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_fp8")
     return out, lse
 
 

@@ -62,8 +62,16 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpQK = 9;
 constexpr int kWarpPV = 10;
-constexpr float kTau = 16.0f;     // lazy rescale threshold (log2 units): terms stay <= 2^16
-constexpr float kTauPow2 = 65536.0f;  // 2^kTau
+// Lazy rescale threshold (log2 units) and the shift of P (log2 units): each P
+// term is 2^(x - m + shift) <= 2^(tau + shift).  bf16 P: tau 16, shift 0.
+// E4M3 P (largest finite value 448): tau 4.5, shift 4, so terms stay <= 2^8.5
+// and terms down to 2^-13 of the reference keep a nonzero code.
+template <bool FP8>
+struct Prec {
+  static constexpr float kTau = FP8 ? 4.5f : 16.0f;
+  static constexpr float kShift = FP8 ? 4.0f : 0.0f;
+  static constexpr float kSumLimit = FP8 ? 362.03867196751236f : 65536.0f;  // 2^(kTau + kShift)
+};
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s: far above any legitimate wait
 constexpr uint64_t kDrainLimitNs = 100000000ull;   // 0.1 s for draining after an abort
@@ -89,13 +97,17 @@ __device__ uint32_t g_attn_status[3];
 // entry point needs neither an allocation nor a caller workspace.
 __device__ __align__(256) uint8_t g_splitkv_scratch[ATTN_SPLITKV_SCRATCH_BYTES];
 
-template <int D>
+template <int D, bool FP8 = false>
 struct Geo {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int kTileBytes = 128 * D * 2;     // one Q, K or V tile (128 rows)
-  static constexpr int kChunkBytes = 128 * 128;      // 128 rows x 64 bf16 (one 128-B swizzle column)
-  static constexpr int kChunks = D / 64;
-  static constexpr int kSlots = (D == 128) ? 5 : 12; // K/V ring depth (tiles)
+  static_assert(!FP8 || D == 128, "E4M3 path: D = 128");
+  static constexpr int kElem = FP8 ? 1 : 2;            // bytes per element of Q, K, V
+  static constexpr int kTileBytes = 128 * D * kElem;   // one Q, K or V tile (128 rows)
+  static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 128 B (one 128-B swizzle column)
+  static constexpr int kChunks = D * kElem / 128;
+  static constexpr int kChunkElems = 128 / kElem;      // elements per 128-B row of a chunk
+  static constexpr int kKSteps = D * kElem / 32;       // QK^T instructions: 32 B of D each
+  static constexpr int kSlots = (D == 128 && !FP8) ? 5 : 12;  // K/V ring depth (tiles)
   // Ring position pos holds K (pos even) or V (pos odd) in slot pos % kSlots.
   // With an odd depth a slot alternates between K and V fills, so each slot
   // has one "full" barrier per kind: every barrier is then waited on, phase
@@ -157,7 +169,8 @@ struct Params {
   const int32_t* seqlens_k;
   int page_size, max_pages, num_pages;
   int cache_tokens;        // num_pages * page_size: a key coordinate that reads zeros
-  float c;                 // |scale| * log2(e)
+  float c;                 // |scale| * log2(e) (E4M3: |scale * q_descale * k_descale| * log2(e))
+  float v_scale;           // 1, or the E4M3 V descale (multiplies O)
   uint32_t idesc_qk;       // negate-A set when scale < 0
   uint32_t idesc_pv;
   uint64_t wait_limit_ns;
@@ -306,15 +319,17 @@ __device__ __forceinline__ float half_row_max(const uint32_t (&s)[2][32], int cl
 }
 
 // p = 2^(s*c - mb) for a thread's 64 scores (one packed FMA per pair; masked
-// columns give 0) into 32 bf16 pairs; returns the fp32 sum.  With WITH_MAX it
-// also returns the maximum of the raw valid scores, found in the same pass.
-template <bool MASKED, bool WITH_MAX>
+// columns give 0) into 32 bf16 pairs (FP8: 16 words of four E4M3 values, in
+// pk[0..15]); returns the fp32 sum.  With WITH_MAX it also returns the maximum
+// of the raw valid scores, found in the same pass.
+template <bool MASKED, bool WITH_MAX, bool FP8 = false>
 __device__ __forceinline__ float half_row_exp(const uint32_t (&s)[2][32], float c, float mb, int climit,
                                               uint32_t (&pk)[32], float& mx) {
   const uint64_t c2 = f2_pack(c, c);
   const uint64_t nmb2 = f2_pack(-mb, -mb);
   uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
   float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  float pprev0 = 0.0f, pprev1 = 0.0f;  // FP8: the previous pair, packed with the next
 #pragma unroll
   for (int e = 0; e < 32; ++e) {
     const int col = 2 * e;
@@ -334,7 +349,13 @@ __device__ __forceinline__ float half_row_exp(const uint32_t (&s)[2][32], float 
       m4[e & 3] = max3(m4[e & 3], s0, s1);
     }
     acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
-    pk[e] = pack_bf16x2(p0, p1);
+    if constexpr (FP8) {
+      if (e & 1) pk[e >> 1] = pack_e4m3x4(pprev0, pprev1, p0, p1);
+      pprev0 = p0;
+      pprev1 = p1;
+    } else {
+      pk[e] = pack_bf16x2(p0, p1);
+    }
   }
   if (WITH_MAX) mx = fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
   const uint64_t a01 = f2_add(acc[0], acc[1]);
@@ -364,11 +385,12 @@ __device__ __forceinline__ void rescale_o_half(uint32_t tO, float alpha) {
   }
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const Params p) {
-  using G = Geo<D>;
+  using G = Geo<D, FP8>;
+  using PR = Prec<FP8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -448,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // padded maps are (D, S, H, B); packed maps are (D, H, tokens, 1)
         const bool packed = p.cu_q != nullptr;
         for (int c = 0; c < G::kChunks; ++c)
-          tma_load_4d_hint(base + G::kOffQ + c * G::kChunkBytes, &map_q, bar_q_full, c * 64,
+          tma_load_4d_hint(base + G::kOffQ + c * G::kChunkBytes, &map_q, bar_q_full, c * G::kChunkElems,
                            packed ? u.h : u.q0, packed ? u.q_tok0 : u.h, packed ? 0 : u.b, pol_once);
         ++qcount;
         for (int j = 0; ok && j < u.n; ++j) {
@@ -461,9 +483,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const CUtensorMap* m = sel ? &map_v : &map_k;
             const int key0 = (u.j0 + j) * kBK;
             const uint32_t dst = base + G::kOffRing + slot * G::kTileBytes;
-            if (p.block_table == nullptr) {
+            if (FP8 && sel) {
+              // E4M3 V is stored transposed, (Sk, D, H, B): the tile is 128
+              // rows of D, each 128 keys long (K-major for the P V product)
+              tma_load_4d_hint(dst, m, full, key0, 0, u.h, u.b, pol_keep);
+            } else if (p.block_table == nullptr) {
               for (int c = 0; c < G::kChunks; ++c)
-                tma_load_4d_hint(dst + c * G::kChunkBytes, m, full, c * 64, packed ? u.h : key0,
+                tma_load_4d_hint(dst + c * G::kChunkBytes, m, full, c * G::kChunkElems, packed ? u.h : key0,
                                  packed ? u.k_tok0 + key0 : u.h, packed ? 0 : u.b, pol_keep);
             } else {
               // paged: two 64-key boxes, each inside one page (page_size is a
@@ -533,10 +559,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S_b = Q K_j^T: both operands K-major, 128-B swizzled; one MMA per 16 columns of D.
         const uint32_t ka = base + G::kOffRing + slot * G::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < G::kKSteps; ++kk) {
           const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-          mma_ss_elect(tmem + G::kTmemS + 128u * b, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                       p.idesc_qk, kk > 0 ? 1u : 0u);
+          if constexpr (FP8)
+            mma_ss_f8_elect(tmem + G::kTmemS + 128u * b, sdesc_sw128(qa + off, 16, 1024),
+                            sdesc_sw128(ka + off, 16, 1024), p.idesc_qk, kk > 0 ? 1u : 0u);
+          else
+            mma_ss_elect(tmem + G::kTmemS + 128u * b, sdesc_sw128(qa + off, 16, 1024),
+                         sdesc_sw128(ka + off, 16, 1024), p.idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit_elect(bar_s_full0 + 8 * b);
         mma_commit_elect(bar_kv_empty0 + 8 * slot);
@@ -570,14 +600,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        // O += P_b V_j: P from TMEM (16 keys = 8 columns per MMA), V MN-major in
-        // smem (LBO = distance between 64-column chunks of D, SBO = 8 keys x 128 B).
         const uint32_t va = base + G::kOffRing + slot * G::kTileBytes;
+        if constexpr (FP8) {
+          // O += P_b V_j with E4M3 P (32 keys = 8 columns per MMA, four per
+          // column) and V^T K-major in shared memory (rows of D, keys contiguous).
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          mma_ts_elect(tmem + G::kTmemO, tmem + G::kTmemP + 64u * b + kk * 8,
-                       sdesc_sw128(va + kk * 16 * 128, G::kChunkBytes, 1024), p.idesc_pv,
-                       (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            mma_ts_f8_elect(tmem + G::kTmemO, tmem + G::kTmemP + 64u * b + kk * 8,
+                            sdesc_sw128(va + kk * 32, 16, 1024), p.idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        } else {
+          // O += P_b V_j: P from TMEM (16 keys = 8 columns per MMA), V MN-major in
+          // smem (LBO = distance between 64-column chunks of D, SBO = 8 keys x 128 B).
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            mma_ts_elect(tmem + G::kTmemO, tmem + G::kTmemP + 64u * b + kk * 8,
+                         sdesc_sw128(va + kk * 16 * 128, G::kChunkBytes, 1024), p.idesc_pv,
+                         (j > 0 || kk > 0) ? 1u : 0u);
+          }
         }
         mma_commit_elect(bar_p_free0 + 8 * b);
         mma_commit_elect(bar_kv_empty0 + 8 * slot);
@@ -684,13 +723,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tcount >= 2) pf_ready = mbar_test_wait(bar_pf, (use - 1) & 1u);
           if (j > 0) {
             // Exponentiate against the current reference right away.  Each term
-            // is 2^(x - m_used); if they all stay <= 2^kTau no score of this part
-            // of the row grew past the reference by more than kTau, and a part
-            // sum <= 2^kTau proves it (the test is also false for NaN / inf).
+            // is 2^(x - m_used + shift); if they all stay <= 2^(tau + shift) no
+            // score of this part of the row grew past the reference by more than
+            // tau, and a part sum <= 2^(tau + shift) proves it (the test is also
+            // false for NaN / inf).
             float unused;
-            sum = masked ? half_row_exp<true, false>(s, c, m_used, climit, pk, unused)
-                         : half_row_exp<false, false>(s, c, m_used, climit, pk, unused);
-            suspect = !(sum <= kTauPow2);
+            sum = masked ? half_row_exp<true, false, FP8>(s, c, m_used - PR::kShift, climit, pk, unused)
+                         : half_row_exp<false, false, FP8>(s, c, m_used - PR::kShift, climit, pk, unused);
+            suspect = !(sum <= PR::kSumLimit);
           } else {
             suspect = true;  // first tile: the reference is this tile's row max
           }
@@ -716,17 +756,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // First tile: its row max is the reference (every row of a unit with
             // n > 0 has key 0 valid, so the reference is finite afterwards).
             m_used = m_tile;
-            const float mb = (m_used == -INFINITY) ? 0.0f : m_used;
+            const float mb = (m_used == -INFINITY) ? 0.0f : m_used - PR::kShift;
             float unused;
-            sum = masked ? half_row_exp<true, false>(s, c, mb, climit, pk, unused)
-                         : half_row_exp<false, false>(s, c, mb, climit, pk, unused);
+            sum = masked ? half_row_exp<true, false, FP8>(s, c, mb, climit, pk, unused)
+                         : half_row_exp<false, false, FP8>(s, c, mb, climit, pk, unused);
           } else {
-            // Lazy correction: only when the max grew by more than kTau is the
+            // Lazy correction: only when the max grew by more than tau is the
             // reference moved, this tile recomputed, and l and O rescaled by
-            // alpha = 2^(m_old - m_new); every term stays <= 2^kTau and O and l
+            // alpha = 2^(m_old - m_new); every term stays <= 2^(tau + shift) and O and l
             // always share one reference.  Both halves see the same row max, so
             // they take the same decision.
-            const bool grow = m_tile > m_used + kTau;
+            const bool grow = m_tile > m_used + PR::kTau;
             if (__any_sync(0xffffffffu, grow)) {
               rescale = true;
               if (grow) {
@@ -734,8 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_used = m_tile;
               }
               float unused;
-              sum = masked ? half_row_exp<true, false>(s, c, m_used, climit, pk, unused)
-                           : half_row_exp<false, false>(s, c, m_used, climit, pk, unused);
+              sum = masked ? half_row_exp<true, false, FP8>(s, c, m_used - PR::kShift, climit, pk, unused)
+                           : half_row_exp<false, false, FP8>(s, c, m_used - PR::kShift, climit, pk, unused);
             }
           }
         }
@@ -753,9 +793,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!failed) {
           tc_fence_after_sync();
-          const uint32_t tP = tmem + lane_off + G::kTmemP + 64u * b + 32u * half;
-          tmem_st_32x32b_x16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
-          tmem_st_32x32b_x16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+          if constexpr (FP8) {  // 64 keys x 1 B = 16 columns per half
+            const uint32_t tP = tmem + lane_off + G::kTmemP + 64u * b + 16u * half;
+            tmem_st_32x32b_x16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+          } else {              // 64 keys x 2 B = 32 columns per half
+            const uint32_t tP = tmem + lane_off + G::kTmemP + 64u * b + 32u * half;
+            tmem_st_32x32b_x16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+            tmem_st_32x32b_x16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+          }
           tmem_st_wait();
           warp_arrive_after_tc(bar_p_full0 + 8 * b, lane);
           l += sum;
@@ -772,8 +817,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const float l_row = l + xch.xsum[half ^ 1][r];
       const bool has_key = l_row > 0.0f;
-      const float inv_l = has_key ? 1.0f / l_row : 0.0f;
-      const float lse_row = has_key ? (m_used + log2f(l_row)) * kLn2 : -INFINITY;
+      const float inv_l = has_key ? p.v_scale / l_row : 0.0f;
+      const float lse_row = has_key ? (m_used - PR::kShift + log2f(l_row)) * kLn2 : -INFINITY;
 #pragma unroll
       for (int q = 0; q < D / 64; ++q) {
         uint32_t o[32];
@@ -844,7 +889,7 @@ struct DeviceInfo {
   int initialised = 0;
   int supported = 0;
   int num_sms = 0;
-  bool smem_set[4] = {false, false, false, false};
+  bool smem_set[6] = {false, false, false, false, false, false};
   void* scratch = nullptr;  // this device's address of g_splitkv_scratch
 };
 constexpr int kMaxDevices = 64;
@@ -906,6 +951,22 @@ bool make_map(CUtensorMap* m, const void* ptr, int B, int H, int S, int D) {
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Rank-4 maps over E4M3 tensors (one byte per element), 128-B swizzled boxes
+// of 128 x 128 bytes.  Q and K [B,H,S,D] as (D, S, H, B); V^T [B,H,D,Sk] as
+// (Sk, D, H, B), so that a box is 128 rows of D, each 128 keys long.  Bytes
+// past an edge read as zeros.
+bool make_map_e4m3(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, int H, int B) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
+  if (encode == nullptr) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)inner, (cuuint64_t)(inner * rows), (cuuint64_t)(inner * rows * H)};
+  const cuuint32_t box[4] = {128, 128, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Rank-4 map over a packed [tokens, H, D] tensor as (D, H, tokens, 1) with a
 // 64 x 1 x box_rows box: a 128-row box lands in shared memory as the same
 // 128 rows x 128 B tile as the padded map's, a 64-row box as its upper or lower
@@ -931,11 +992,11 @@ void clear_paged(Params& p) {
   p.cache_tokens = 0;
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool FP8 = false>
 attn_status launch(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                    const Params& p, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<D, CAUSAL>;
-  constexpr int smem = Geo<D>::kSmemBytes;
+  auto kern = attn_fwd_kernel<D, CAUSAL, FP8>;
+  constexpr int smem = Geo<D, FP8>::kSmemBytes;
   if (!dev.smem_set[idx]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return ATTN_ERR_CUDA;
@@ -1075,6 +1136,7 @@ Params packed_params(void* o, float* lse, const int32_t* cu_q, int batch, int ma
   p.total_k = 0;
   clear_paged(p);
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634);
+  p.v_scale = 1.0f;
   p.idesc_qk = idesc_bf16_f32(kBQ, kBK, scale < 0.0f, false);
   p.idesc_pv = idesc_bf16_f32(kBQ, D, false, true);
   p.wait_limit_ns = kWaitLimitNs;
@@ -1118,6 +1180,7 @@ attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const voi
   p.total_k = 0;
   clear_paged(p);
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634);
+  p.v_scale = 1.0f;
   p.idesc_qk = idesc_bf16_f32(kBQ, kBK, scale < 0.0f, false);
   p.idesc_pv = idesc_bf16_f32(kBQ, D, false, true);
   p.wait_limit_ns = kWaitLimitNs;
@@ -1140,6 +1203,64 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   if (st != ATTN_OK) return st;
   return run_forward(*dev, q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, 1, nullptr, nullptr,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o, float* lse, int B, int H, int Sq,
+                         int Sk, int D, float scale, int causal, const int32_t* kv_lens, float q_descale,
+                         float k_descale, float v_descale, attn_stream_t stream) {
+  if (B < 0 || H < 0 || Sq < 0 || Sk < 0) return ATTN_ERR_SHAPE;
+  if (D != 128) return ATTN_ERR_UNSUPPORTED_D;
+  if (!std::isfinite(scale) || !std::isfinite(q_descale) || !std::isfinite(k_descale) || !std::isfinite(v_descale))
+    return ATTN_ERR_SCALE;
+  const double qk_scale = static_cast<double>(scale) * q_descale * k_descale;
+  if (!std::isfinite(static_cast<float>(qk_scale))) return ATTN_ERR_SCALE;
+  if (Sk % 16 != 0) return ATTN_ERR_SHAPE;  // V^T rows are Sk bytes: a TMA stride must be a multiple of 16
+  if (B == 0 || H == 0 || Sq == 0) return ATTN_OK;
+  if (q == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_NULLPTR;
+  if (Sk > 0 && (k == nullptr || v_t == nullptr)) return ATTN_ERR_NULLPTR;
+  if (!aligned(q, 16) || !aligned(o, 16) || !aligned(lse, 4)) return ATTN_ERR_ALIGN;
+  if (Sk > 0 && (!aligned(k, 16) || !aligned(v_t, 16))) return ATTN_ERR_ALIGN;
+  if (kv_lens != nullptr && !aligned(kv_lens, 4)) return ATTN_ERR_ALIGN;
+  const uint64_t max_s = static_cast<uint64_t>(Sq > Sk ? Sq : Sk);
+  if (static_cast<uint64_t>(H) * max_s * D * 2 >= (1ull << 40)) return ATTN_ERR_SHAPE;
+  const uint64_t n_qtiles = (static_cast<uint64_t>(Sq) + kBQ - 1) / kBQ;
+  if (static_cast<uint64_t>(B) * H * n_qtiles > 0x7fff0000ull) return ATTN_ERR_SHAPE;
+  DeviceInfo* dev = nullptr;
+  attn_status st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  CUtensorMap mq, mk, mv;
+  if (!make_map_e4m3(&mq, q, D, Sq, H, B)) return ATTN_ERR_CUDA;
+  if (Sk > 0) {
+    if (!make_map_e4m3(&mk, k, D, Sk, H, B) || !make_map_e4m3(&mv, v_t, Sk, D, H, B)) return ATTN_ERR_CUDA;
+  } else {  // never dereferenced: with no keys every unit has zero K tiles
+    mk = mq;
+    mv = mq;
+  }
+  Params p;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.kv_lens = kv_lens;
+  p.B = B;
+  p.H = H;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.n_qtiles = static_cast<int>(n_qtiles);
+  p.num_splits = 1;
+  p.total_units = static_cast<int>(static_cast<uint64_t>(B) * H * n_qtiles);
+  p.o_part = nullptr;
+  p.lse_part = nullptr;
+  p.cu_q = nullptr;
+  p.cu_k = nullptr;
+  p.total_q = 0;
+  p.total_k = 0;
+  clear_paged(p);
+  p.c = static_cast<float>(std::fabs(qk_scale) * 1.4426950408889634);
+  p.v_scale = v_descale;
+  p.idesc_qk = idesc_e4m3_f32(kBQ, kBK, qk_scale < 0.0);
+  p.idesc_pv = idesc_e4m3_f32(kBQ, D, false);
+  p.wait_limit_ns = kWaitLimitNs;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return causal ? launch<128, true, true>(*dev, 4, mq, mk, mv, p, s) : launch<128, false, true>(*dev, 5, mq, mk, mv, p, s);
 }
 
 attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -240,3 +240,48 @@ def generate_paged(w: PagedWorkload):
             v_cache[pg, :t1 - t0] = v[t0:t1]
         at += n_pages
     return q, k_cache, v_cache, cu, lens.to(torch.int32), table
+
+
+@dataclass(frozen=True)
+class Fp8Workload(Workload):
+    """A padded workload with FP8 (E4M3) inputs: the bf16 recipe's float32
+    draws (times std) are rounded to E4M3 codes with torch's float8_e4m3fn
+    conversion instead of to bf16; every descale is ``descale``.  V is also
+    given transposed (``[B, H, D, Sk]``), the layout the FP8 kernel reads."""
+    descale: float = 1.0
+
+    @property
+    def min_bytes(self) -> int:
+        """Read Q, K, V once (1 byte each), write O (bf16) and LSE (fp32) once."""
+        return (self.B * self.H * self.D * (self.Sq + 2 * self.Sk) + 2 * self.B * self.H * self.Sq * self.D
+                + 4 * self.B * self.H * self.Sq)
+
+    def label(self) -> str:
+        return super().label() + ", E4M3 inputs"
+
+
+FP8_WORKLOADS = {
+    "s8192_d128_fp8": Fp8Workload("s8192_d128_fp8", 2, 16, 8192, 8192, 128, False, seed=3),
+    "s8192_d128_causal_fp8": Fp8Workload("s8192_d128_causal_fp8", 2, 16, 8192, 8192, 128, True, seed=3),
+}
+
+
+def to_e4m3_codes(x: torch.Tensor) -> torch.Tensor:
+    """Round float32 values to E4M3 codes (uint8), via torch's float8_e4m3fn."""
+    return x.to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def generate_fp8(w: Fp8Workload):
+    """Return ``(q8, k8, v8, v8_t, kv_lens)`` on the CPU: uint8 E4M3 codes
+    ``[B,H,S,D]`` (``v8_t`` is ``v8`` transposed to ``[B,H,D,Sk]``, contiguous)
+    and the int32 ``kv_lens`` or ``None``."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    q = to_e4m3_codes(torch.randn((w.B, w.H, w.Sq, w.D), generator=g, dtype=torch.float32) * w.std)
+    k = to_e4m3_codes(torch.randn((w.B, w.H, w.Sk, w.D), generator=g, dtype=torch.float32) * w.std)
+    v = to_e4m3_codes(torch.randn((w.B, w.H, w.Sk, w.D), generator=g, dtype=torch.float32) * w.std)
+    kv = None
+    if w.padded:
+        kv = torch.randint(0, w.Sk + 1, (w.B,), generator=g, dtype=torch.int64).to(torch.int32)
+        kv[w.kv_zero_index] = 0
+    return q, k, v, v.transpose(-1, -2).contiguous(), kv

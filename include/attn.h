@@ -86,6 +86,31 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      int Sk, int D, float scale, int causal, const int32_t* kv_lens, attn_stream_t stream);
 
 /*
+ * attn_fwd_fp8 — the forward with FP8 (E4M3) inputs and both products on the
+ * tensor cores' 8-bit path ("Fused Multi-Head Attention", the "Quantization"
+ * item of the techniques fused attention combines with: FP8 data for the
+ * GEMMs; "Kernel Fusion and the Memory Wall", the paragraph after "A small
+ * executable reference", on FlashAttention-3's low-precision facilities).
+ *
+ * q       E4M3 codes [B, H, Sq, D], contiguous, device, 16-byte aligned.
+ * k       E4M3 codes [B, H, Sk, D], contiguous, device, 16-byte aligned.
+ * v_t     E4M3 codes of V TRANSPOSED, [B, H, D, Sk] (keys innermost), so that
+ *         both operands of both products are K-major; 16-byte aligned.
+ * q_descale, k_descale, v_descale: the value of a code is descale * E4M3(code)
+ *         (OCP E4M3: bias 7, subnormals, no infinities, 0x7F/0xFF NaN).
+ * o, lse  as attn_fwd (bf16 O, fp32 natural-log LSE over the scaled scores).
+ * D must be 128 (else ATTN_ERR_UNSUPPORTED_D); Sk a multiple of 16 (the
+ * V^T rows are Sk bytes long; else ATTN_ERR_SHAPE); scale and the descales
+ * finite (else ATTN_ERR_SCALE).  Other arguments and all mask semantics as
+ * attn_fwd.  The probabilities are rounded to E4M3 (scaled by 2^4, never
+ * above 2^8.5) before the P V product; O and the row sums are accumulated in
+ * fp32.
+ */
+attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o, float* lse, int B, int H, int Sq,
+                         int Sk, int D, float scale, int causal, const int32_t* kv_lens, float q_descale,
+                         float k_descale, float v_descale, attn_stream_t stream);
+
+/*
  * attn_fwd_varlen — the same forward over a packed batch of variable-length
  * sequences (the ragged tensors of continuous batching, "Fused Multi-Head
  * Attention", section on continuous batching): no padding is stored or read.
@@ -228,7 +253,7 @@ attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream);
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 5
+#define ATTN_ABI_VERSION 6
 
 #ifdef __cplusplus
 }

@@ -207,3 +207,28 @@ def test_paged_argument_checks(lib, args, code):
     st = attn.attn_fwd_paged(a["q"], a["kc"], a["vc"], a["o"], a["lse"], a["cq"], a["sk"], a["bt"], a["batch"],
                              a["maxq"], a["tq"], a["npg"], a["ps"], a["mp"], a["H"], a["D"], a["scale"], 0, None)
     assert st == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(D=64), attn.ATTN_ERR_UNSUPPORTED_D),
+    (dict(Sk=200), attn.ATTN_ERR_SHAPE),
+    (dict(B=-1), attn.ATTN_ERR_SHAPE),
+    (dict(scale=float("nan")), attn.ATTN_ERR_SCALE),
+    (dict(qd=float("inf")), attn.ATTN_ERR_SCALE),
+    (dict(vd=float("nan")), attn.ATTN_ERR_SCALE),
+    (dict(qd=3e38, kd=3e38), attn.ATTN_ERR_SCALE),
+    (dict(q=0), attn.ATTN_ERR_NULLPTR),
+    (dict(v=0), attn.ATTN_ERR_NULLPTR),
+    (dict(v=A + 8), attn.ATTN_ERR_ALIGN),
+    (dict(kv=A + 2), attn.ATTN_ERR_ALIGN),
+    (dict(B=0), attn.ATTN_OK),
+    (dict(Sq=0), attn.ATTN_OK),
+])
+def test_fp8_argument_checks(lib, args, code):
+    # every case ends in a host-side check (no launch, with or without a GPU)
+    a = dict(q=A, k=A, v=A, o=A, lse=A, B=2, H=2, Sq=256, Sk=256, D=128, scale=0.088, kv=None, qd=1.0, kd=1.0,
+             vd=1.0)
+    a.update(args)
+    st = attn.attn_fwd_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Sq"], a["Sk"], a["D"],
+                           a["scale"], 0, a["kv"], a["qd"], a["kd"], a["vd"], None)
+    assert st == code
