@@ -22,6 +22,9 @@ Contents:
 * ``fp8.decode_e4m3`` / ``fp8.attention_fp8_ref`` — E4M3 codes decoded from
   the format definition, and exact attention of FP8 inputs with per-tensor
   descales.
+* ``backward.attention_bwd_ref`` (and ``attention_bwd_head``,
+  ``attention_bwd_sampled``) — gradients of the forward with respect to Q, K
+  and V for an upstream dO, from the chain rule on the materialised softmax.
 * ``online.online_softmax_attention`` — the tiled online-softmax recurrence
   (running max, normaliser, numerator, each corrected by exp(m_old - m_new))
   from "Attention softmax fusion", section "The tile loop", and "Kernel Fusion
@@ -39,3 +42,4 @@ from .attention import (attention_paged_ref, attention_ref, attention_rows, atte
 from .online import online_softmax_attention  # noqa: F401
 from .merge import lse_merge  # noqa: F401
 from .fp8 import attention_fp8_ref, decode_e4m3  # noqa: F401
+from .backward import attention_bwd_head, attention_bwd_ref, attention_bwd_sampled  # noqa: F401
