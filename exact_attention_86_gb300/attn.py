@@ -61,6 +61,10 @@ SIGNATURES = {
                                                 ctypes.c_int, ctypes.c_void_p]),
     "attn_lse_merge": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int, ctypes.c_void_p]),
+    "attn_bwd_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "attn_bwd": (ctypes.c_int, [ctypes.c_void_p] * 9 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int,
+                                                                          ctypes.c_void_p, ctypes.c_void_p,
+                                                                          ctypes.c_size_t, ctypes.c_void_p]),
     "attn_get_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_check_device_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
     "attn_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
@@ -144,6 +148,17 @@ def attn_fwd_splitkv_noalloc(q: int, k: int, v: int, o: int, lse: int, B: int, H
 def attn_lse_merge(o_parts: int, lse_parts: int, num_parts: int, o: int, lse: int, rows: int, D: int,
                    stream: Optional[int]) -> int:
     return lib().attn_lse_merge(o_parts, lse_parts, num_parts, o, lse, rows, D, stream)
+
+
+def attn_bwd_workspace_size(B: int, H: int, Sq: int) -> int:
+    return lib().attn_bwd_workspace_size(B, H, Sq)
+
+
+def attn_bwd(q: int, k: int, v: int, o: int, dout: int, lse: int, dq: int, dk: int, dv: int, B: int, H: int, Sq: int,
+             Sk: int, D: int, scale: float, causal: int, kv_lens: Optional[int], workspace: Optional[int],
+             workspace_bytes: int, stream: Optional[int]) -> int:
+    return lib().attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, Sq, Sk, D, scale, int(causal), kv_lens, workspace,
+                          workspace_bytes, stream)
 
 
 def attn_get_error_string(status: int) -> str:
@@ -315,6 +330,37 @@ def forward_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, max
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_paged")
     return out, lse
+
+
+def backward(q, k, v, o, lse, dout, scale: Optional[float] = None, causal: bool = False, kv_lens=None):
+    """Gradients ``(dq, dk, dv)`` (bf16, shaped like q, k, v) of the forward's
+    ``o`` for the upstream gradient ``dout``; ``o`` and ``lse`` are the
+    forward's outputs for the same arguments."""
+    import torch
+
+    _check_qkv(q, k, v, kv_lens)
+    B, H, Sq, D = q.shape
+    Sk = k.shape[2]
+    for name, t in (("o", o), ("dout", dout)):
+        if t.dtype != torch.bfloat16 or t.device != q.device or not t.is_contiguous() or tuple(t.shape) != tuple(q.shape):
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    if lse.dtype != torch.float32 or lse.device != q.device or tuple(lse.shape) != (B, H, Sq):
+        raise ValueError("lse must be fp32 [B, H, Sq] on q's device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    ws_bytes = attn_bwd_workspace_size(B, H, Sq)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    with torch.cuda.device(q.device):
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+        st = attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                      dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, Sq, Sk, D, float(scale), int(bool(causal)),
+                      None if kv_lens is None else kv_lens.data_ptr(), ws.data_ptr(), ws.numel(), stream)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def lse_merge(o_parts, lse_parts):

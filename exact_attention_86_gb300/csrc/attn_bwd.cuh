@@ -1,0 +1,906 @@
+// attn_bwd.cuh — backward pass of the exact attention on GB300 (sm_103a).
+//
+// Included by attn_fwd.cu inside its anonymous namespace: the backward shares
+// the forward's status word, bounded waits, unit decoding and tensor maps.
+//
+// With P_ij = exp(s_ij - LSE_i) (s = scale * Q K^T, masked entries 0), the
+// gradients of O = P V for an upstream dO are
+//   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - Delta),   Delta_i = <dO_i, O_i>,
+//   dQ = scale * dS K,   dK = scale * dS^T Q
+// (the chain rule on the softmax; the pages give the forward only).  Three
+// kernels:
+//   bwd_delta_kernel  Delta_i in fp32, one warp per row;
+//   bwd_dq_kernel     one unit = 128 query rows of one (b, h): S and dP on
+//                     the tensor cores, P and dS in the elementwise warps,
+//                     dQ accumulated in TMEM over the key tiles;
+//   bwd_dkdv_kernel   one unit = 128 keys of one (b, h): S^T = K Q^T and
+//                     dP^T = V dO^T, P^T and dS^T, then dV and dK accumulated
+//                     in TMEM over the query tiles.
+// Both main kernels use only the operand forms of the forward: A and B
+// K-major from shared memory (S, dP, S^T, dP^T) and A from TMEM with B
+// MN-major from shared memory (dQ, dV, dK, like the forward's P V).
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum BwdSite : uint32_t {
+  kSiteBwdQFull = 33,
+  kSiteBwdQEmpty = 34,
+  kSiteBwdKvFull = 35,
+  kSiteBwdKvEmpty = 36,
+  kSiteBwdSFull = 37,
+  kSiteBwdSFree = 38,
+  kSiteBwdDsFull = 39,
+  kSiteBwdDsFree = 40,
+  kSiteBwdOutFull = 41,
+};
+
+struct BwdParams {
+  Params f;              // shapes, kv_lens, n_qtiles, total_units (query or key tiles)
+  const float* lse;      // [B,H,Sq] from the forward (natural log)
+  const float* delta;    // [B,H,Sq] <dO_i, O_i>
+  uint16_t* dq;          // [B,H,Sq,D]
+  uint16_t* dk;          // [B,H,Sk,D]
+  uint16_t* dv;          // [B,H,Sk,D]
+  float c2;              // scale * log2(e) (signed)
+  float scale;
+  int n_ktiles;
+};
+
+// ---------------------------------------------------------------- Delta
+template <int D>
+__global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restrict__ o,
+                                                        const uint16_t* __restrict__ dout, float* __restrict__ delta,
+                                                        long long rows) {
+  constexpr int C = D / 32;  // elements per lane (2 or 4)
+  const int lane = threadIdx.x & 31;
+  const long long warp_id = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const long long n_warps = (static_cast<long long>(gridDim.x) * blockDim.x) >> 5;
+  for (long long r = warp_id; r < rows; r += n_warps) {
+    const uint16_t* po = o + r * D + lane * C;
+    const uint16_t* pd = dout + r * D + lane * C;
+    float acc = 0.0f;
+    if constexpr (C == 4) {
+      const uint2 a = __ldg(reinterpret_cast<const uint2*>(po));
+      const uint2 b = __ldg(reinterpret_cast<const uint2*>(pd));
+      const uint32_t av[2] = {a.x, a.y}, bv[2] = {b.x, b.y};
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        acc = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(bv[e] << 16), acc);
+        acc = fmaf(__uint_as_float(av[e] & 0xffff0000u), __uint_as_float(bv[e] & 0xffff0000u), acc);
+      }
+    } else {
+      const uint32_t a = __ldg(reinterpret_cast<const uint32_t*>(po));
+      const uint32_t b = __ldg(reinterpret_cast<const uint32_t*>(pd));
+      acc = fmaf(__uint_as_float(a << 16), __uint_as_float(b << 16), acc);
+      acc = fmaf(__uint_as_float(a & 0xffff0000u), __uint_as_float(b & 0xffff0000u), acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) delta[r] = acc;
+  }
+}
+
+// Two fp32 scores of a thread's 64 (from two 32-column TMEM loads).
+__device__ __forceinline__ void pair_at(const uint32_t (&s)[2][32], int e, float& a, float& b) {
+  const int col = 2 * e;
+  a = __uint_as_float(s[col >> 5][col & 31]);
+  b = __uint_as_float(s[col >> 5][(col + 1) & 31]);
+}
+
+// ------------------------------------------------------------------ dQ
+template <int D>
+struct GeoDq {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kChunkBytes = 128 * 128;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kSlots = (D == 128) ? 5 : 12;  // K/V ring (per-kind full barriers, as the forward)
+  static __device__ __forceinline__ uint32_t kind_use(uint32_t pos) {
+    return (kSlots & 1) ? (pos / kSlots) >> 1 : pos / kSlots;
+  }
+  static constexpr int kOffQ = 1024;
+  static constexpr int kOffDo = kOffQ + kTileBytes;
+  static constexpr int kOffRing = kOffDo + kTileBytes;
+  static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes + 1024;
+  static constexpr uint32_t kTmemS = 0, kTmemDp = 128, kTmemDs = 256, kTmemDq = 384;
+};
+
+struct CtrlDq {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[12], v_full[12], kv_empty[12];
+  uint64_t sp_full, sp_free, ds_full, ds_free, dq_full;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(CtrlDq) <= 1024, "control block");
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+                  const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                  const BwdParams bp) {
+  using G = GeoDq<D>;
+  const Params& p = bp.f;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  CtrlDq& ctl = *reinterpret_cast<CtrlDq*>(smem_raw + (base - raw));
+  volatile int* abort_flag = &ctl.abort_flag;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar_q_full = smem_addr(&ctl.q_full), bar_q_empty = smem_addr(&ctl.q_empty);
+  const uint32_t bar_k_full0 = smem_addr(&ctl.k_full[0]), bar_v_full0 = smem_addr(&ctl.v_full[0]);
+  const uint32_t bar_kv_empty0 = smem_addr(&ctl.kv_empty[0]);
+  const uint32_t bar_sp_full = smem_addr(&ctl.sp_full), bar_sp_free = smem_addr(&ctl.sp_free);
+  const uint32_t bar_ds_full = smem_addr(&ctl.ds_full), bar_ds_free = smem_addr(&ctl.ds_free);
+  const uint32_t bar_dq_full = smem_addr(&ctl.dq_full);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q_full, 1);
+    mbar_init(bar_q_empty, 1);
+    for (int s = 0; s < G::kSlots; ++s) {
+      mbar_init(bar_k_full0 + 8 * s, 1);
+      mbar_init(bar_v_full0 + 8 * s, 1);
+      mbar_init(bar_kv_empty0 + 8 * s, 1);
+    }
+    mbar_init(bar_sp_full, 1);
+    mbar_init(bar_sp_free, kSoftmaxWarps);
+    mbar_init(bar_ds_full, kSoftmaxWarps);
+    mbar_init(bar_ds_free, 1);
+    mbar_init(bar_dq_full, 1);
+    mbar_init(smem_addr(&ctl.drain), 1);
+    ctl.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpQK) {
+    tmem_alloc(smem_addr(&ctl.tmem_base), 512);
+    tmem_relinquish_alloc_permit();
+  }
+  if (warp == kWarpLoad && lane == 0) {
+    prefetch_tensor_map(&map_q);
+    prefetch_tensor_map(&map_do);
+    prefetch_tensor_map(&map_k);
+    prefetch_tensor_map(&map_v);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl.tmem_base;
+  const uint64_t limit = p.wait_limit_ns;
+  const int t_end = (p.total_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) *
+                    static_cast<int>(gridDim.x);
+
+  if (warp >= kSoftmaxWarps) {
+    regs_decrease<kRegsOther>();
+    if (warp == kWarpLoad) {
+      // -------------------------------------------------------------- TMA
+      if (lane == 0) {
+        const uint64_t pol_keep = l2_policy_evict_last();
+        const uint64_t pol_once = l2_policy_evict_first();
+        uint32_t ring = 0, qcount = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
+          const int unit = unit_at<CAUSAL>(t);
+          if (unit >= p.total_units) continue;
+          const Unit u = decode_unit<CAUSAL>(p, unit);
+          if (u.n == 0) continue;
+          if (!wait_phase(bar_q_empty, (qcount & 1u) ^ 1u, abort_flag, kSiteBwdQEmpty, limit)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar_q_full, 2 * G::kTileBytes);
+          for (int c = 0; c < G::kChunks; ++c) {
+            tma_load_4d_hint(base + G::kOffQ + c * G::kChunkBytes, &map_q, bar_q_full, c * 64, u.q0, u.h, u.b,
+                             pol_once);
+            tma_load_4d_hint(base + G::kOffDo + c * G::kChunkBytes, &map_do, bar_q_full, c * 64, u.q0, u.h, u.b,
+                             pol_once);
+          }
+          ++qcount;
+          for (int j = 0; ok && j < u.n; ++j) {
+            for (int sel = 0; sel < 2; ++sel) {  // K_j, then V_j
+              const uint32_t slot = ring % G::kSlots;
+              const uint32_t ph = (ring / G::kSlots) & 1u;
+              if (!wait_phase(bar_kv_empty0 + 8 * slot, ph ^ 1u, abort_flag, kSiteBwdKvEmpty, limit)) {
+                ok = false;
+                break;
+              }
+              const uint32_t full = (sel ? bar_v_full0 : bar_k_full0) + 8 * slot;
+              mbar_arrive_expect_tx(full, G::kTileBytes);
+              const int key0 = (u.j0 + j) * kBK;
+              for (int c = 0; c < G::kChunks; ++c)
+                tma_load_4d_hint(base + G::kOffRing + slot * G::kTileBytes + c * G::kChunkBytes,
+                                 sel ? &map_v : &map_k, full, c * 64, key0, u.h, u.b, pol_keep);
+              ++ring;
+            }
+          }
+        }
+        if (!ok) {
+          if (qcount > 0) wait_phase_drain(bar_q_full, (qcount - 1) & 1u);
+          for (uint32_t s = 0; s < (uint32_t)G::kSlots && s < ring; ++s) {
+            const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);
+            wait_phase_drain(((last & 1u) ? bar_v_full0 : bar_k_full0) + 8 * s, G::kind_use(last) & 1u);
+          }
+        }
+        // the issuer's last commit arrivals land asynchronously: wait for them
+        if (qcount > 0) wait_phase_drain(bar_q_empty, (qcount - 1) & 1u);
+        for (uint32_t s = 0; s < (uint32_t)G::kSlots && s < ring; ++s) {
+          const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);
+          wait_phase_drain(bar_kv_empty0 + 8 * s, (last / G::kSlots) & 1u);
+        }
+      }
+      __syncwarp();
+    } else if (warp == kWarpQK) {
+      // ---------------------------------------------------------- issuer
+      // Per tile t: S = Q K_t^T and dP = dO V_t^T (once the elementwise warps
+      // have read the previous S and dP), then dQ += dS_{t-1} K_{t-1}.
+      const uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK, false, false);
+      const uint32_t idesc_q = idesc_bf16_f32(kBQ, D, false, true);
+      const uint32_t qa = base + G::kOffQ, da = base + G::kOffDo;
+      uint32_t ring = 0, qcount = 0, tcount = 0;
+      bool ok = true;
+      // dQ += dS K for tile tt whose K sits in ring slot ks
+      auto issue_dq = [&](uint32_t tt, uint32_t ks, bool first) -> bool {
+        if (!wait_warp(bar_ds_full, tt & 1u, abort_flag, kSiteBwdDsFull, limit)) return false;
+        tc_fence_after_sync();
+        const uint32_t ka = base + G::kOffRing + ks * G::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          mma_ts_elect(tmem + G::kTmemDq, tmem + G::kTmemDs + kk * 8,
+                       sdesc_sw128(ka + kk * 16 * 128, G::kChunkBytes, 1024), idesc_q,
+                       (first && kk == 0) ? 0u : 1u);
+        mma_commit_elect(bar_ds_free);
+        mma_commit_elect(bar_kv_empty0 + 8 * ks);
+        return true;
+      };
+      for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
+        const int unit = unit_at<CAUSAL>(t);
+        if (unit >= p.total_units) continue;
+        const Unit u = decode_unit<CAUSAL>(p, unit);
+        if (u.n == 0) continue;
+        if (!wait_warp(bar_q_full, qcount & 1u, abort_flag, kSiteBwdQFull, limit)) { ok = false; break; }
+        ++qcount;
+        uint32_t prev_ks = 0;
+        for (int j = 0; j < u.n; ++j) {
+          const uint32_t tt = tcount + j;
+          if (tt >= 1 && !wait_warp(bar_sp_free, (tt - 1) & 1u, abort_flag, kSiteBwdSFree, limit)) { ok = false; break; }
+          const uint32_t posk = ring + 2 * j, posv = posk + 1;
+          const uint32_t ks = posk % G::kSlots, vs = posv % G::kSlots;
+          if (!wait_warp(bar_k_full0 + 8 * ks, G::kind_use(posk) & 1u, abort_flag, kSiteBwdKvFull, limit) ||
+              !wait_warp(bar_v_full0 + 8 * vs, G::kind_use(posv) & 1u, abort_flag, kSiteBwdKvFull, limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t ka = base + G::kOffRing + ks * G::kTileBytes;
+          const uint32_t va = base + G::kOffRing + vs * G::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
+            mma_ss_elect(tmem + G::kTmemS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s,
+                         kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
+            mma_ss_elect(tmem + G::kTmemDp, sdesc_sw128(da + off, 16, 1024), sdesc_sw128(va + off, 16, 1024),
+                         idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_elect(bar_sp_full);
+          mma_commit_elect(bar_kv_empty0 + 8 * vs);  // V_j is done once dP is
+          if (j == u.n - 1) mma_commit_elect(bar_q_empty);  // Q and dO are done after the unit's last S, dP
+          if (j >= 1 && !issue_dq(tt - 1, prev_ks, j == 1)) { ok = false; break; }
+          prev_ks = ks;
+        }
+        if (!ok) break;
+        if (!issue_dq(tcount + u.n - 1, prev_ks, u.n == 1)) { ok = false; break; }
+        mma_commit_elect(bar_dq_full);
+        ring += 2 * u.n;
+        tcount += u.n;
+      }
+      if (!ok) {
+        const uint32_t bar_d = smem_addr(&ctl.drain);
+        mma_commit_elect(bar_d);
+        wait_phase_drain(bar_d, 0);
+      }
+    }
+  } else {
+    regs_increase<kRegsSoftmax>();
+    // ------------------------------------------------------- elementwise
+    // Two threads per query row: warps 0-3 own key columns 0-63 of each tile
+    // and dQ columns [0, D/2), warps 4-7 the rest.
+    const int half = warp >> 2;
+    const int r = threadIdx.x & (kBQ - 1);
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    uint32_t tcount = 0, ucount = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
+      const int unit = unit_at<CAUSAL>(t);
+      if (unit >= p.total_units) continue;
+      const Unit u = decode_unit<CAUSAL>(p, unit);
+      const int row = u.q0 + r;
+      const bool row_ok = row < p.Sq;
+      const size_t row_index = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq) + row;
+      uint16_t* dq_dst = bp.dq + row_index * D + (D / 2) * half;
+      if (u.n == 0) {  // no valid key for any row: dQ = 0
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(dq_dst);
+#pragma unroll
+          for (int q = 0; q < D / 16; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
+      const float lse_i = row_ok ? __ldg(bp.lse + row_index) : -INFINITY;
+      const bool live = row_ok && lse_i != -INFINITY;
+      const float lse2 = live ? lse_i * kLog2e : 0.0f;
+      const float delta_i = row_ok ? __ldg(bp.delta + row_index) : 0.0f;
+      const bool rows_tail = u.q0 + kBQ > p.Sq;
+      for (int j = 0; j < u.n; ++j) {
+        const uint32_t tt = tcount + j;
+        const int k0 = (u.j0 + j) * kBK;
+        const bool masked = !live || rows_tail || (k0 + kBK > u.kv) || (CAUSAL && k0 + kBK - 1 > u.q0);
+        int climit = u.kv - k0;
+        if (CAUSAL) climit = min(climit, row - k0 + 1);
+        climit = live ? climit - 64 * half : 0;
+        if (!wait_warp(bar_sp_full, tt & 1u, abort_flag, kSiteBwdSFull, limit)) { ok = false; break; }
+        tc_fence_after_sync();
+        uint32_t s[2][32], dp[2][32];
+        const uint32_t tS = tmem + lane_off + G::kTmemS + 64u * half;
+        const uint32_t tD = tmem + lane_off + G::kTmemDp + 64u * half;
+        tmem_ld_32x32b_x32(tS, s[0]);
+        tmem_ld_32x32b_x32(tS + 32, s[1]);
+        tmem_ld_32x32b_x32(tD, dp[0]);
+        tmem_ld_32x32b_x32(tD + 32, dp[1]);
+        tmem_ld_wait_x32(s[0]);
+        tmem_ld_wait_x32(s[1]);
+        tmem_ld_wait_x32(dp[0]);
+        tmem_ld_wait_x32(dp[1]);
+        warp_arrive_after_tc(bar_sp_free, lane);  // the issuer may compute the next S and dP
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float s0, s1, d0, d1;
+          pair_at(s, e, s0, s1);
+          pair_at(dp, e, d0, d1);
+          float p0 = ex2_approx(fmaf(s0, bp.c2, -lse2));
+          float p1 = ex2_approx(fmaf(s1, bp.c2, -lse2));
+          if (masked) {
+            p0 = (2 * e < climit) ? p0 : 0.0f;
+            p1 = (2 * e + 1 < climit) ? p1 : 0.0f;
+          }
+          pk[e] = pack_bf16x2(p0 * (d0 - delta_i), p1 * (d1 - delta_i));
+        }
+        // dS buffer is free once the previous tile's dQ product has completed
+        if (tt >= 1 && !wait_warp(bar_ds_free, (tt - 1) & 1u, abort_flag, kSiteBwdDsFree, limit)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t tP = tmem + lane_off + G::kTmemDs + 32u * half;
+        tmem_st_32x32b_x16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+        tmem_st_32x32b_x16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+        tmem_st_wait();
+        warp_arrive_after_tc(bar_ds_full, lane);
+      }
+      if (!ok) break;
+      tcount += u.n;
+      if (!wait_warp(bar_dq_full, ucount & 1u, abort_flag, kSiteBwdOutFull, limit)) { ok = false; break; }
+      ++ucount;
+      tc_fence_after_sync();
+      const uint32_t tQ = tmem + lane_off + G::kTmemDq + (D / 2) * half;
+#pragma unroll
+      for (int q = 0; q < D / 64; ++q) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tQ + q * 32, o);
+        tmem_ld_wait_x32(o);
+        if (row_ok) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(o[2 * e]) * bp.scale, __uint_as_float(o[2 * e + 1]) * bp.scale);
+          uint4* dst = reinterpret_cast<uint4*>(dq_dst + q * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+      }
+      // the next unit's first dQ product overwrites the accumulator only after
+      // every elementwise warp has arrived on ds_full for it, which comes after this
+      tc_fence_before_sync();
+    }
+    // the last ds_free arrival lands asynchronously: wait before exiting
+    if (tcount > 0) wait_phase_drain(bar_ds_free, (tcount - 1) & 1u);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kWarpQK) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// --------------------------------------------------------------- dK, dV
+template <int D>
+struct GeoKv {
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kChunkBytes = 128 * 128;
+  static constexpr int kChunks = D / 64;
+  static constexpr int kSlots = (D == 128) ? 2 : 4;   // ring of (Q_i, dO_i) pairs
+  static constexpr int kOffStat = 1024;               // LSE*log2e and Delta, two tiles each (2 KB)
+  static constexpr int kOffK = 4096;
+  static constexpr int kOffV = kOffK + kTileBytes;
+  static constexpr int kOffRing = kOffV + kTileBytes;
+  static constexpr int kSmemBytes = kOffRing + kSlots * 2 * kTileBytes + 1024;
+  static constexpr uint32_t kTmemSt = 0, kTmemDpt = 128, kTmemDv = 256, kTmemDk = 256 + D;
+};
+
+struct CtrlKv {
+  uint64_t kv_full, kv_empty;
+  uint64_t qd_full[4], qd_empty[4];
+  uint64_t st_full, pd_full, pd_free, out_full;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(CtrlKv) <= 1024, "control block");
+
+struct KvUnit {
+  int b, h, key0, rows_k;  // rows_k: keys of the tile that exist (< Sk)
+  int kv;                  // valid keys of the batch entry
+  int i0, n;               // first query tile and number of query tiles (0: no gradient)
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams& bp, int t) {
+  const Params& p = bp.f;
+  KvUnit u;
+  const int bh_count = p.B * p.H;
+  int kt, bh;
+  if (CAUSAL) {  // longest first: key tiles from the start of the sequence
+    kt = t / bh_count;
+    bh = t % bh_count;
+  } else {       // consecutive units share a head, so its Q and dO stay hot in L2
+    kt = t % bp.n_ktiles;
+    bh = t / bp.n_ktiles;
+  }
+  u.b = bh / p.H;
+  u.h = bh % p.H;
+  u.key0 = kt * kBK;
+  u.rows_k = max(min(kBK, p.Sk - u.key0), 0);
+  int kv = p.Sk;
+  if (p.kv_lens != nullptr) kv = min(max(__ldg(p.kv_lens + u.b), 0), p.Sk);
+  u.kv = kv;
+  u.i0 = CAUSAL ? u.key0 / kBQ : 0;  // query rows below key0 see none of these keys
+  u.n = (u.key0 < kv && u.rows_k > 0) ? max(p.n_qtiles - u.i0, 0) : 0;
+  return u;
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+                    const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                    const BwdParams bp) {
+  using G = GeoKv<D>;
+  const Params& p = bp.f;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* base_ptr = smem_raw + (base - raw);
+  CtrlKv& ctl = *reinterpret_cast<CtrlKv*>(base_ptr);
+  float* stat = reinterpret_cast<float*>(base_ptr + G::kOffStat);  // [2 tiles][LSE*log2e 128 | Delta 128]
+  volatile int* abort_flag = &ctl.abort_flag;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar_kv_full = smem_addr(&ctl.kv_full), bar_kv_empty = smem_addr(&ctl.kv_empty);
+  const uint32_t bar_qd_full0 = smem_addr(&ctl.qd_full[0]), bar_qd_empty0 = smem_addr(&ctl.qd_empty[0]);
+  const uint32_t bar_st_full = smem_addr(&ctl.st_full), bar_pd_full = smem_addr(&ctl.pd_full);
+  const uint32_t bar_pd_free = smem_addr(&ctl.pd_free), bar_out_full = smem_addr(&ctl.out_full);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv_full, 1);
+    mbar_init(bar_kv_empty, 1);
+    for (int s = 0; s < G::kSlots; ++s) {
+      mbar_init(bar_qd_full0 + 8 * s, 1);
+      mbar_init(bar_qd_empty0 + 8 * s, 1);
+    }
+    mbar_init(bar_st_full, 1);
+    mbar_init(bar_pd_full, kSoftmaxWarps);
+    mbar_init(bar_pd_free, 1);
+    mbar_init(bar_out_full, 1);
+    mbar_init(smem_addr(&ctl.drain), 1);
+    ctl.abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kWarpQK) {
+    tmem_alloc(smem_addr(&ctl.tmem_base), 512);
+    tmem_relinquish_alloc_permit();
+  }
+  if (warp == kWarpLoad && lane == 0) {
+    prefetch_tensor_map(&map_q);
+    prefetch_tensor_map(&map_do);
+    prefetch_tensor_map(&map_k);
+    prefetch_tensor_map(&map_v);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl.tmem_base;
+  const uint64_t limit = p.wait_limit_ns;
+  const int t_end = (p.total_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) *
+                    static_cast<int>(gridDim.x);
+
+  if (warp >= kSoftmaxWarps) {
+    regs_decrease<kRegsOther>();
+    if (warp == kWarpLoad) {
+      // -------------------------------------------------------------- TMA
+      if (lane == 0) {
+        const uint64_t pol_keep = l2_policy_evict_last();   // Q, dO: re-read by every key tile of the head
+        const uint64_t pol_once = l2_policy_evict_first();  // K, V: read once
+        uint32_t ring = 0, ucount = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
+          const int unit = unit_at<CAUSAL>(t);
+          if (unit >= p.total_units) continue;
+          const KvUnit u = decode_kv_unit<CAUSAL>(bp, unit);
+          if (u.n == 0) continue;
+          if (!wait_phase(bar_kv_empty, (ucount & 1u) ^ 1u, abort_flag, kSiteBwdKvEmpty, limit)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar_kv_full, 2 * G::kTileBytes);
+          for (int c = 0; c < G::kChunks; ++c) {
+            tma_load_4d_hint(base + G::kOffK + c * G::kChunkBytes, &map_k, bar_kv_full, c * 64, u.key0, u.h, u.b,
+                             pol_once);
+            tma_load_4d_hint(base + G::kOffV + c * G::kChunkBytes, &map_v, bar_kv_full, c * 64, u.key0, u.h, u.b,
+                             pol_once);
+          }
+          ++ucount;
+          for (int i = 0; ok && i < u.n; ++i) {
+            const uint32_t slot = ring % G::kSlots;
+            const uint32_t ph = (ring / G::kSlots) & 1u;
+            if (!wait_phase(bar_qd_empty0 + 8 * slot, ph ^ 1u, abort_flag, kSiteBwdQEmpty, limit)) {
+              ok = false;
+              break;
+            }
+            const uint32_t full = bar_qd_full0 + 8 * slot;
+            mbar_arrive_expect_tx(full, 2 * G::kTileBytes);
+            const uint32_t dst = base + G::kOffRing + slot * 2 * G::kTileBytes;
+            const int q0 = (u.i0 + i) * kBQ;
+            for (int c = 0; c < G::kChunks; ++c) {
+              tma_load_4d_hint(dst + c * G::kChunkBytes, &map_q, full, c * 64, q0, u.h, u.b, pol_keep);
+              tma_load_4d_hint(dst + G::kTileBytes + c * G::kChunkBytes, &map_do, full, c * 64, q0, u.h, u.b,
+                               pol_keep);
+            }
+            ++ring;
+          }
+        }
+        if (!ok) {
+          if (ucount > 0) wait_phase_drain(bar_kv_full, (ucount - 1) & 1u);
+          for (uint32_t s = 0; s < (uint32_t)G::kSlots && s < ring; ++s) {
+            const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);
+            wait_phase_drain(bar_qd_full0 + 8 * s, (last / G::kSlots) & 1u);
+          }
+        }
+        if (ucount > 0) wait_phase_drain(bar_kv_empty, (ucount - 1) & 1u);
+        for (uint32_t s = 0; s < (uint32_t)G::kSlots && s < ring; ++s) {
+          const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);
+          wait_phase_drain(bar_qd_empty0 + 8 * s, (last / G::kSlots) & 1u);
+        }
+      }
+      __syncwarp();
+    } else if (warp == kWarpQK) {
+      // ---------------------------------------------------------- issuer
+      // Per query tile: S^T = K Q_i^T and dP^T = V dO_i^T; once the
+      // elementwise warps have written P^T over S^T and dS^T over dP^T:
+      // dV += P^T dO_i and dK += dS^T Q_i.  The next S^T waits for those.
+      const uint32_t idesc_s = idesc_bf16_f32(kBK, kBQ, false, false);
+      const uint32_t idesc_o = idesc_bf16_f32(kBK, D, false, true);
+      const uint32_t ka = base + G::kOffK, va = base + G::kOffV;
+      uint32_t ring = 0, ucount = 0, tcount = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
+        const int unit = unit_at<CAUSAL>(t);
+        if (unit >= p.total_units) continue;
+        const KvUnit u = decode_kv_unit<CAUSAL>(bp, unit);
+        if (u.n == 0) continue;
+        if (!wait_warp(bar_kv_full, ucount & 1u, abort_flag, kSiteBwdKvFull, limit)) { ok = false; break; }
+        ++ucount;
+        for (int i = 0; i < u.n; ++i) {
+          const uint32_t tt = tcount + i;
+          const uint32_t slot = ring % G::kSlots;
+          if (!wait_warp(bar_qd_full0 + 8 * slot, (ring / G::kSlots) & 1u, abort_flag, kSiteBwdQFull, limit)) {
+            ok = false;
+            break;
+          }
+          if (tt >= 1 && !wait_warp(bar_pd_free, (tt - 1) & 1u, abort_flag, kSiteBwdDsFree, limit)) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint32_t qa = base + G::kOffRing + slot * 2 * G::kTileBytes;
+          const uint32_t da = qa + G::kTileBytes;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
+            mma_ss_elect(tmem + G::kTmemSt, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
+                         idesc_s, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
+            mma_ss_elect(tmem + G::kTmemDpt, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024),
+                         idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_elect(bar_st_full);
+          if (!wait_warp(bar_pd_full, tt & 1u, abort_flag, kSiteBwdDsFull, limit)) { ok = false; break; }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < kBQ / 16; ++kk) {
+            const uint32_t acc = (i == 0 && kk == 0) ? 0u : 1u;
+            mma_ts_elect(tmem + G::kTmemDv, tmem + G::kTmemSt + kk * 8,
+                         sdesc_sw128(da + kk * 16 * 128, G::kChunkBytes, 1024), idesc_o, acc);
+            mma_ts_elect(tmem + G::kTmemDk, tmem + G::kTmemDpt + kk * 8,
+                         sdesc_sw128(qa + kk * 16 * 128, G::kChunkBytes, 1024), idesc_o, acc);
+          }
+          mma_commit_elect(bar_qd_empty0 + 8 * slot);
+          mma_commit_elect(bar_pd_free);
+          ++ring;
+        }
+        if (!ok) break;
+        mma_commit_elect(bar_out_full);
+        mma_commit_elect(bar_kv_empty);
+        tcount += u.n;
+      }
+      if (!ok) {
+        const uint32_t bar_d = smem_addr(&ctl.drain);
+        mma_commit_elect(bar_d);
+        wait_phase_drain(bar_d, 0);
+      }
+    }
+  } else {
+    regs_increase<kRegsSoftmax>();
+    // ------------------------------------------------------- elementwise
+    // Two threads per key row: warps 0-3 own query columns 0-63 of each tile
+    // and dK/dV columns [0, D/2), warps 4-7 the rest.  P^T is written over the
+    // S^T columns and dS^T over the dP^T columns, so the eight warps meet at a
+    // named barrier between reading and writing; as in the forward, a failed
+    // wait only marks the warp, every warp executes every named barrier, and
+    // all test the abort flag right after it.
+    const int half = warp >> 2;
+    const int r = threadIdx.x & (kBK - 1);
+    const int tid = threadIdx.x;  // 0..255
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    constexpr uint32_t kBarEw = 1;
+    constexpr uint32_t kEwThreads = kSoftmaxWarps * 32;
+    uint32_t tcount = 0, ucount = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
+      const int unit = unit_at<CAUSAL>(t);
+      if (unit >= p.total_units) continue;
+      const KvUnit u = decode_kv_unit<CAUSAL>(bp, unit);
+      const int key = u.key0 + r;
+      const bool key_exists = r < u.rows_k;
+      const bool key_ok = key < u.kv;
+      const size_t key_index = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sk) + key;
+      uint16_t* dk_dst = bp.dk + key_index * D + (D / 2) * half;
+      uint16_t* dv_dst = bp.dv + key_index * D + (D / 2) * half;
+      if (u.n == 0) {  // no query sees these keys (or none is valid): dK = dV = 0
+        if (key_exists) {
+#pragma unroll
+          for (int q = 0; q < D / 16; ++q) {
+            reinterpret_cast<uint4*>(dk_dst)[q] = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4*>(dv_dst)[q] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+        continue;
+      }
+      const size_t head_row0 = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq);
+      bool failed = false;
+      for (int i = 0; i < u.n; ++i) {
+        const uint32_t tt = tcount + i;
+        const int q0 = (u.i0 + i) * kBQ;
+        // LSE (base 2) and Delta of the tile's 128 queries, shared through
+        // shared memory by tile parity; a query past Sq or without a valid
+        // key gets LSE = +inf, so its P is 0
+        float* st = stat + (tt & 1u) * 2 * kBQ;
+        {
+          const int c = tid & (kBQ - 1);
+          const int q = q0 + c;
+          if (tid < kBQ) {
+            float v = INFINITY;
+            if (q < p.Sq) {
+              const float l = __ldg(bp.lse + head_row0 + q);
+              if (l != -INFINITY) v = l * kLog2e;
+            }
+            st[c] = v;
+          } else {
+            st[kBQ + c] = (q < p.Sq) ? __ldg(bp.delta + head_row0 + q) : 0.0f;
+          }
+        }
+        named_bar_sync(kBarEw, kEwThreads);
+        if (*abort_flag) { ok = false; break; }
+        // query column c of this half is q0 + 64*half + c; key <= query for causal
+        const bool masked = !key_ok || (CAUSAL && q0 < u.key0 + kBK - 1);
+        const int cstart = key_ok ? (CAUSAL ? key - q0 - 64 * half : 0) : 64;  // first valid column
+        uint32_t s[2][32], dp[2][32];
+        if (!failed && !wait_warp(bar_st_full, tt & 1u, abort_flag, kSiteBwdSFull, limit)) failed = true;
+        if (!failed) {
+          tc_fence_after_sync();
+          const uint32_t tS = tmem + lane_off + G::kTmemSt + 64u * half;
+          const uint32_t tD = tmem + lane_off + G::kTmemDpt + 64u * half;
+          tmem_ld_32x32b_x32(tS, s[0]);
+          tmem_ld_32x32b_x32(tS + 32, s[1]);
+          tmem_ld_32x32b_x32(tD, dp[0]);
+          tmem_ld_32x32b_x32(tD + 32, dp[1]);
+          tmem_ld_wait_x32(s[0]);
+          tmem_ld_wait_x32(s[1]);
+          tmem_ld_wait_x32(dp[0]);
+          tmem_ld_wait_x32(dp[1]);
+        }
+        uint32_t pk[32], dk_pk[32];
+        if (!failed) {
+          const float* lse_c = st + 64 * half;
+          const float* del_c = st + kBQ + 64 * half;
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            float s0, s1, d0, d1;
+            pair_at(s, e, s0, s1);
+            pair_at(dp, e, d0, d1);
+            float p0 = ex2_approx(fmaf(s0, bp.c2, -lse_c[2 * e]));
+            float p1 = ex2_approx(fmaf(s1, bp.c2, -lse_c[2 * e + 1]));
+            if (masked) {
+              p0 = (2 * e >= cstart) ? p0 : 0.0f;
+              p1 = (2 * e + 1 >= cstart) ? p1 : 0.0f;
+            }
+            pk[e] = pack_bf16x2(p0, p1);
+            dk_pk[e] = pack_bf16x2(p0 * (d0 - del_c[2 * e]), p1 * (d1 - del_c[2 * e + 1]));
+          }
+        }
+        // every half has read its S^T and dP^T columns before any is overwritten
+        tc_fence_before_sync();
+        named_bar_sync(kBarEw, kEwThreads);
+        if (*abort_flag) { ok = false; break; }
+        if (!failed) {
+          tc_fence_after_sync();
+          const uint32_t tP = tmem + lane_off + G::kTmemSt + 32u * half;
+          const uint32_t tQ = tmem + lane_off + G::kTmemDpt + 32u * half;
+          tmem_st_32x32b_x16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
+          tmem_st_32x32b_x16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+          tmem_st_32x32b_x16(tQ, *reinterpret_cast<const uint32_t(*)[16]>(&dk_pk[0]));
+          tmem_st_32x32b_x16(tQ + 16, *reinterpret_cast<const uint32_t(*)[16]>(&dk_pk[16]));
+          tmem_st_wait();
+          warp_arrive_after_tc(bar_pd_full, lane);
+        }
+      }
+      if (!ok) break;
+      tcount += u.n;
+      if (!failed && !wait_warp(bar_out_full, ucount & 1u, abort_flag, kSiteBwdOutFull, limit)) failed = true;
+      ++ucount;
+      named_bar_sync(kBarEw, kEwThreads);
+      if (*abort_flag || failed) { ok = false; break; }
+      tc_fence_after_sync();
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {  // dV, then dK (times scale)
+        const uint32_t tA = tmem + lane_off + (which ? G::kTmemDk : G::kTmemDv) + (D / 2) * half;
+        const float mul = which ? bp.scale : 1.0f;
+        uint16_t* dst16 = which ? dk_dst : dv_dst;
+#pragma unroll
+        for (int q = 0; q < D / 64; ++q) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tA + q * 32, o);
+          tmem_ld_wait_x32(o);
+          if (key_exists) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = key_ok ? pack_bf16x2(__uint_as_float(o[2 * e]) * mul, __uint_as_float(o[2 * e + 1]) * mul) : 0u;
+            uint4* dst = reinterpret_cast<uint4*>(dst16 + q * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
+        }
+      }
+      // the next unit's first dV/dK product overwrites the accumulators only
+      // after every elementwise warp has arrived on pd_full for it
+      tc_fence_before_sync();
+    }
+    // the last pd_free arrival lands asynchronously: wait before exiting
+    if (tcount > 0) wait_phase_drain(bar_pd_free, (tcount - 1) & 1u);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kWarpQK) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ------------------------------------------------------------------ host
+size_t bwd_delta_bytes(int B, int H, int Sq) {
+  return round_up_256(static_cast<size_t>(B) * H * Sq * sizeof(float));
+}
+
+template <int D, bool CAUSAL>
+attn_status launch_bwd(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CUtensorMap& mdo,
+                       const CUtensorMap& mk, const CUtensorMap& mv, const BwdParams& bq, const BwdParams& bk,
+                       cudaStream_t stream) {
+  auto kq = bwd_dq_kernel<D, CAUSAL>;
+  auto kk = bwd_dkdv_kernel<D, CAUSAL>;
+  constexpr int smem_q = GeoDq<D>::kSmemBytes;
+  constexpr int smem_k = GeoKv<D>::kSmemBytes;
+  if (!dev.bwd_smem_set[idx]) {
+    if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q) != cudaSuccess ||
+        cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_k) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    dev.bwd_smem_set[idx] = true;
+  }
+  if (bq.f.total_units > 0) {
+    const int grid = bq.f.total_units < dev.num_sms ? bq.f.total_units : dev.num_sms;
+    kq<<<grid, kThreads, smem_q, stream>>>(mq, mdo, mk, mv, bq);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  if (bk.f.total_units > 0) {
+    const int grid = bk.f.total_units < dev.num_sms ? bk.f.total_units : dev.num_sms;
+    kk<<<grid, kThreads, smem_k, stream>>>(mq, mdo, mk, mv, bk);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  }
+  return ATTN_OK;
+}
+
+attn_status run_backward(DeviceInfo& dev, const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H, int Sq,
+                         int Sk, int D, float scale, int causal, const int32_t* kv_lens, float* delta,
+                         cudaStream_t s) {
+  if (Sq == 0) {  // no query: dK = dV = 0
+    const size_t bytes = static_cast<size_t>(B) * H * Sk * D * 2;
+    if (cudaMemsetAsync(dk, 0, bytes, s) != cudaSuccess || cudaMemsetAsync(dv, 0, bytes, s) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  if (Sk == 0) {  // no key: dQ = 0
+    if (cudaMemsetAsync(dq, 0, static_cast<size_t>(B) * H * Sq * D * 2, s) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+  }
+  // Delta_i = <dO_i, O_i>
+  const long long rows = static_cast<long long>(B) * H * Sq;
+  long long blocks = (rows + 7) / 8;
+  const long long max_blocks = static_cast<long long>(dev.num_sms) * 8;
+  if (blocks > max_blocks) blocks = max_blocks;
+  if (D == 64)
+    bwd_delta_kernel<64><<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const uint16_t*>(o),
+                                                                   static_cast<const uint16_t*>(dout), delta, rows);
+  else
+    bwd_delta_kernel<128><<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<const uint16_t*>(o),
+                                                                    static_cast<const uint16_t*>(dout), delta, rows);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+
+  CUtensorMap mq, mdo, mk, mv;
+  if (!make_map(&mq, q, B, H, Sq, D) || !make_map(&mdo, dout, B, H, Sq, D) || !make_map(&mk, k, B, H, Sk, D) ||
+      !make_map(&mv, v, B, H, Sk, D))
+    return ATTN_ERR_CUDA;
+  BwdParams bq;
+  Params& f = bq.f;
+  f.o = nullptr;
+  f.lse = nullptr;
+  f.kv_lens = kv_lens;
+  f.B = B;
+  f.H = H;
+  f.Sq = Sq;
+  f.Sk = Sk;
+  f.n_qtiles = (Sq + kBQ - 1) / kBQ;
+  f.num_splits = 1;
+  f.total_units = static_cast<int>(static_cast<int64_t>(B) * H * f.n_qtiles);
+  f.o_part = nullptr;
+  f.lse_part = nullptr;
+  f.cu_q = nullptr;
+  f.cu_k = nullptr;
+  f.total_q = 0;
+  f.total_k = 0;
+  clear_paged(f);
+  f.c = 0.0f;
+  f.v_scale = 1.0f;
+  f.idesc_qk = 0;
+  f.idesc_pv = 0;
+  f.wait_limit_ns = kWaitLimitNs;
+  bq.lse = lse;
+  bq.delta = delta;
+  bq.dq = static_cast<uint16_t*>(dq);
+  bq.dk = static_cast<uint16_t*>(dk);
+  bq.dv = static_cast<uint16_t*>(dv);
+  bq.c2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  bq.scale = scale;
+  bq.n_ktiles = (Sk + kBK - 1) / kBK;
+  BwdParams bk = bq;
+  bk.f.total_units = static_cast<int>(static_cast<int64_t>(B) * H * bq.n_ktiles);
+  if (D == 64)
+    return causal ? launch_bwd<64, true>(dev, 0, mq, mdo, mk, mv, bq, bk, s)
+                  : launch_bwd<64, false>(dev, 1, mq, mdo, mk, mv, bq, bk, s);
+  return causal ? launch_bwd<128, true>(dev, 2, mq, mdo, mk, mv, bq, bk, s)
+                : launch_bwd<128, false>(dev, 3, mq, mdo, mk, mv, bq, bk, s);
+}

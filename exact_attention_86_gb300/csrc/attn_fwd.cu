@@ -890,6 +890,7 @@ struct DeviceInfo {
   int supported = 0;
   int num_sms = 0;
   bool smem_set[6] = {false, false, false, false, false, false};
+  bool bwd_smem_set[4] = {false, false, false, false};
   void* scratch = nullptr;  // this device's address of g_splitkv_scratch
 };
 constexpr int kMaxDevices = 64;
@@ -1190,6 +1191,8 @@ attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const voi
   return causal ? launch<128, true>(dev, 2, mq, mk, mv, p, s) : launch<128, false>(dev, 3, mq, mk, mv, p, s);
 }
 
+#include "attn_bwd.cuh"
+
 }  // namespace
 
 extern "C" {
@@ -1400,6 +1403,33 @@ attn_status attn_lse_merge(const float* o_parts, const float* lse_parts, int num
   attn_status st = device_info(&dev);
   if (st != ATTN_OK) return st;
   return launch_merge(*dev, o_parts, lse_parts, num_parts, rows, D, o, lse, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int Sq) {
+  if (B < 0 || H < 0 || Sq < 0) return 0;
+  return bwd_delta_bytes(B, H, Sq);
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, float scale, int causal,
+                     const int32_t* kv_lens, void* workspace, size_t workspace_bytes, attn_stream_t stream) {
+  attn_status st = check_args(q, k, v, o, lse, B, H, Sq, Sk, D, scale, kv_lens, 1);
+  if (st != ATTN_OK) return st;
+  if (B == 0 || H == 0 || (Sq == 0 && Sk == 0)) return ATTN_OK;
+  if (Sq > 0 && (dout == nullptr || dq == nullptr)) return ATTN_ERR_NULLPTR;
+  if (Sk > 0 && (dk == nullptr || dv == nullptr)) return ATTN_ERR_NULLPTR;
+  if (Sq > 0 && (!aligned(dout, 16) || !aligned(dq, 16))) return ATTN_ERR_ALIGN;
+  if (Sk > 0 && (!aligned(dk, 16) || !aligned(dv, 16))) return ATTN_ERR_ALIGN;
+  if (Sq > 0 && Sk > 0) {
+    if (workspace == nullptr) return ATTN_ERR_NULLPTR;
+    if (!aligned(workspace, 256)) return ATTN_ERR_ALIGN;
+    if (workspace_bytes < bwd_delta_bytes(B, H, Sq)) return ATTN_ERR_WORKSPACE;
+  }
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  return run_backward(*dev, q, k, v, o, dout, lse, dq, dk, dv, B, H, Sq, Sk, D, scale, causal, kv_lens,
+                      static_cast<float*>(workspace), reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* attn_get_error_string(attn_status status) {

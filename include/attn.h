@@ -227,6 +227,31 @@ attn_status attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v
 attn_status attn_lse_merge(const float* o_parts, const float* lse_parts, int num_parts, void* o, float* lse,
                            long long rows, int D, attn_stream_t stream);
 
+/*
+ * attn_bwd — gradients of attn_fwd's O with respect to Q, K and V for an
+ * upstream gradient dO (the LSE output is not differentiated).  The pages
+ * give the forward only ("Fused Multi-Head Attention" notes that fused
+ * kernels also make training with long sequences efficient); the gradients
+ * are the chain rule on the softmax: with P = exp(scale QK^T + mask - LSE),
+ *   dV = P^T dO,  dP = dO V^T,  dS = P * (dP - Delta),  Delta_i = <dO_i, O_i>,
+ *   dQ = scale dS K,  dK = scale dS^T Q.
+ *
+ * q, k, v, o, lse  the forward's inputs and outputs (layouts as attn_fwd).
+ * dout             bf16 [B, H, Sq, D], contiguous, device, 16-byte aligned.
+ * dq               bf16 [B, H, Sq, D] output; dk, dv: bf16 [B, H, Sk, D].
+ * workspace        device, 256-byte aligned, caller-owned, at least
+ *                  attn_bwd_workspace_size(B, H, Sq) bytes (fp32 Delta).
+ * Other arguments, masks and the D restriction as attn_fwd.  Rows without a
+ * valid key get dQ = 0; keys no query sees (past kv_lens, or masked for
+ * every query) get dK = dV = 0.  Sq == 0: dK = dV = 0; Sk == 0: dQ = 0.
+ * Three kernels on `stream` (Delta, dQ, dK/dV); the call never synchronises.
+ */
+size_t attn_bwd_workspace_size(int B, int H, int Sq);
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                     void* dq, void* dk, void* dv, int B, int H, int Sq, int Sk, int D, float scale, int causal,
+                     const int32_t* kv_lens, void* workspace, size_t workspace_bytes, attn_stream_t stream);
+
 /* Static, human-readable description of a status code. */
 const char* attn_get_error_string(attn_status status);
 
@@ -253,7 +278,7 @@ attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream);
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 6
+#define ATTN_ABI_VERSION 7
 
 #ifdef __cplusplus
 }

@@ -232,3 +232,31 @@ def test_fp8_argument_checks(lib, args, code):
     st = attn.attn_fwd_fp8(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Sq"], a["Sk"], a["D"],
                            a["scale"], 0, a["kv"], a["qd"], a["kd"], a["vd"], None)
     assert st == code
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(D=96), attn.ATTN_ERR_UNSUPPORTED_D),
+    (dict(Sk=-1), attn.ATTN_ERR_SHAPE),
+    (dict(scale=float("nan")), attn.ATTN_ERR_SCALE),
+    (dict(dout=0), attn.ATTN_ERR_NULLPTR),
+    (dict(dq=0), attn.ATTN_ERR_NULLPTR),
+    (dict(dk=0), attn.ATTN_ERR_NULLPTR),
+    (dict(ws=0), attn.ATTN_ERR_NULLPTR),
+    (dict(dv=A + 8), attn.ATTN_ERR_ALIGN),
+    (dict(ws=A + 64), attn.ATTN_ERR_ALIGN),
+    (dict(wsb=16), attn.ATTN_ERR_WORKSPACE),
+    (dict(B=0), attn.ATTN_OK),
+    (dict(Sq=0, Sk=0), attn.ATTN_OK),
+])
+def test_bwd_argument_checks(lib, args, code):
+    # every case ends in a host-side check (no launch, with or without a GPU)
+    a = dict(dout=A, dq=A, dk=A, dv=A, ws=A, wsb=1 << 20, B=2, H=2, Sq=256, Sk=256, D=128, scale=0.1)
+    a.update(args)
+    st = attn.attn_bwd(A, A, A, A, a["dout"], A, a["dq"], a["dk"], a["dv"], a["B"], a["H"], a["Sq"], a["Sk"], a["D"],
+                       a["scale"], 0, None, a["ws"], a["wsb"], None)
+    assert st == code
+
+
+def test_bwd_workspace_size(lib):
+    assert attn.attn_bwd_workspace_size(2, 3, 300) == -(-(2 * 3 * 300 * 4) // 256) * 256
+    assert attn.attn_bwd_workspace_size(-1, 3, 300) == 0
