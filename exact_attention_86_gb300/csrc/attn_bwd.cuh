@@ -649,9 +649,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Two threads per key row: warps 0-3 own query columns 0-63 of each tile
     // and dK/dV columns [0, D/2), warps 4-7 the rest.  P^T is written over the
     // S^T columns and dS^T over the dP^T columns, so the eight warps meet at a
-    // named barrier between reading and writing; as in the forward, a failed
-    // wait only marks the warp, every warp executes every named barrier, and
-    // all test the abort flag right after it.
+    // named barrier between reading and writing.  A failed wait only marks the
+    // warp, every warp executes every named barrier, and every decision to
+    // leave is the OR of the abort flag reduced by the barrier itself, so all
+    // eight take it together.
     const int half = warp >> 2;
     const int r = threadIdx.x & (kBK - 1);
     const int tid = threadIdx.x;  // 0..255
@@ -703,8 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             st[kBQ + c] = (q < p.Sq) ? __ldg(bp.delta + head_row0 + q) : 0.0f;
           }
         }
-        named_bar_sync(kBarEw, kEwThreads);
-        if (*abort_flag) { ok = false; break; }
+        if (named_bar_red_or(kBarEw, kEwThreads, *abort_flag != 0)) { ok = false; break; }
         // query column c of this half is q0 + 64*half + c; key <= query for causal
         const bool masked = !key_ok || (CAUSAL && q0 < u.key0 + kBK - 1);
         const int cstart = key_ok ? (CAUSAL ? key - q0 - 64 * half : 0) : 64;  // first valid column
@@ -744,8 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // every half has read its S^T and dP^T columns before any is overwritten
         tc_fence_before_sync();
-        named_bar_sync(kBarEw, kEwThreads);
-        if (*abort_flag) { ok = false; break; }
+        if (named_bar_red_or(kBarEw, kEwThreads, *abort_flag != 0)) { ok = false; break; }
         if (!failed) {
           tc_fence_after_sync();
           const uint32_t tP = tmem + lane_off + G::kTmemSt + 32u * half;
@@ -762,8 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tcount += u.n;
       if (!failed && !wait_warp(bar_out_full, ucount & 1u, abort_flag, kSiteBwdOutFull, limit)) failed = true;
       ++ucount;
-      named_bar_sync(kBarEw, kEwThreads);
-      if (*abort_flag || failed) { ok = false; break; }
+      if (named_bar_red_or(kBarEw, kEwThreads, *abort_flag != 0 || failed)) { ok = false; break; }
       tc_fence_after_sync();
 #pragma unroll
       for (int which = 0; which < 2; ++which) {  // dV, then dK (times scale)

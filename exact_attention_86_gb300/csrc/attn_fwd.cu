@@ -636,22 +636,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------------- softmax
     // Two threads per query row: half 0 (warps 0-3) owns columns 0-63 of each
     // score tile, half 1 (warps 4-7) columns 64-127.  Both keep the same
-    // reference max (they exchange their partial maxima every tile through
-    // shared memory and named barrier 1) and their own partial row sums, added
-    // in the epilogue.
+    // reference max (when a row may have grown they exchange their partial
+    // maxima through shared memory and the pair's named barrier) and their
+    // own partial row sums, added in the epilogue.
     //
-    // Named barriers cannot time out, so the eight warps keep one discipline:
-    // a wait that fails only marks the warp as failed and skips work; every
-    // warp still executes every named barrier, and right after each one all of
-    // them test the CTA abort flag (raised before the barrier by whoever gave
-    // up) and leave together.
+    // The two halves of a row are warps w and w + 4; each such pair has its own
+    // named barrier (id 1 + w, 64 threads), so pairs never wait on each other.
+    // Named barriers cannot time out, so the pair keeps one discipline: a wait
+    // that fails only marks the warp as failed and skips work; both warps
+    // execute every barrier of the pair; and every decision to leave is the OR
+    // of the abort flag over the pair, reduced by the barrier itself, so both
+    // warps take it together.
     const int half = warp >> 2;
     const int r = threadIdx.x & (kBQ - 1);         // row within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tO = tmem + lane_off + G::kTmemO + (D / 2) * half;
     const float c = p.c;
-    constexpr uint32_t kBarSoftmax = 1;
-    constexpr uint32_t kSoftmaxThreads = kSoftmaxWarps * 32;
+    const uint32_t bar_pair = 1u + static_cast<uint32_t>(warp & 3);
+    constexpr uint32_t kPairThreads = 64;
     uint32_t tcount = 0, ocount = 0;
     bool ok = true;
 
@@ -735,21 +737,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             suspect = true;  // first tile: the reference is this tile's row max
           }
         }
-        // One barrier per tile for the eight softmax warps; it also tells every
-        // thread whether any row of the tile needs its exact maximum.
-        const bool any_suspect = named_bar_red_or(kBarSoftmax, kSoftmaxThreads, suspect);
-        if (*abort_flag) { ok = false; break; }
+        // One barrier per tile for the pair; it also tells both warps whether
+        // any of their rows needs its exact maximum (or the CTA is aborting).
+        const bool any_suspect = named_bar_red_or(bar_pair, kPairThreads, suspect || *abort_flag != 0);
         bool rescale = false;
         float alpha = 1.0f;
         if (any_suspect) {
           // Exact row max: partial maxima of both halves through shared memory
           // (by tile parity, so a slow partner still reads the previous value
-          // undisturbed).  Taken by all eight warps together.
+          // undisturbed).  The second barrier publishes them and settles abort.
           if (!failed) {
             xch.xmax[b][half][r] = masked ? half_row_max<true>(s, climit) : half_row_max<false>(s, climit);
           }
-          named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-          if (*abort_flag) { ok = false; break; }
+          if (named_bar_red_or(bar_pair, kPairThreads, *abort_flag != 0)) { ok = false; break; }
           const float mx = fmaxf(xch.xmax[b][0][r], xch.xmax[b][1][r]);
           const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
           if (j == 0) {
@@ -812,8 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!failed && !wait_warp(bar_o_full, ocount & 1u, abort_flag, kSiteOFull, limit)) failed = true;
       ++ocount;
       if (!failed) xch.xsum[half][r] = l;
-      named_bar_sync(kBarSoftmax, kSoftmaxThreads);
-      if (*abort_flag) { ok = false; break; }
+      if (named_bar_red_or(bar_pair, kPairThreads, *abort_flag != 0)) { ok = false; break; }
       tc_fence_after_sync();
       const float l_row = l + xch.xsum[half ^ 1][r];
       const bool has_key = l_row > 0.0f;
