@@ -41,6 +41,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor peak"
+METRIC_BWD = "fused attention bwd TFLOP/s (bf16, 2.5x the forward FLOPs) and % of GB300 dense BF16 tensor peak"
 FALLBACK_PEAK_TFLOPS = 1900.0
 KERNEL_SOURCES = ["exact_attention_86_gb300/csrc/attn_fwd.cu", "exact_attention_86_gb300/csrc/sm103_ptx.cuh"]
 TRAFFIC_FILE = "profiles/attn_fwd_kernel_s8192_d128_traffic.md"
@@ -245,6 +246,47 @@ def generate(w, draw: int):
     return workloads.generate(w, draw)
 
 
+class BwdJob:
+    """The backward pass of a padded bf16 workload: the forward's O and LSE are
+    computed once before timing; a step is one ``attn_bwd`` call (three
+    kernels) for a fixed upstream gradient dO ~ N(0, 1) drawn after the
+    workload's inputs."""
+
+    def __init__(self, w, args, dev, attn, torch):
+        from exact_attention_86_gb300 import workloads
+        if is_varlen(w) or is_fp8(w) or args.splits > 0:
+            raise SystemExit("--backward applies to padded bf16 workloads")
+        self.stream = torch.cuda.current_stream(dev)
+        sptr = self.stream.cuda_stream
+        q, k, v, kv = workloads.generate(w, args.draw)
+        g = torch.Generator().manual_seed(w.seed + 1000)
+        dout = torch.randn(q.shape, generator=g).to(torch.bfloat16)
+        qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), dout.to(dev)
+        kvd = kv.to(dev) if kv is not None else None
+        o, lse = attn.forward(qd, kd, vd, scale=w.scale, causal=w.causal, kv_lens=kvd)
+        torch.cuda.synchronize(dev)
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        ws = torch.empty(max(attn.attn_bwd_workspace_size(w.B, w.H, w.Sq), 256), dtype=torch.uint8, device=dev)
+        host = [q, k, v, o.cpu(), lse.cpu(), dout] + ([kv] if kv is not None else [])
+        dev_t = [qd, kd, vd, o, lse, dod] + ([kvd] if kvd is not None else [])
+        self.inputs = list(zip(host, dev_t))
+        self.outputs = [dq, dk, dv]
+        self.launches_per_step = 3
+        kv_ptr = kvd.data_ptr() if kvd is not None else None
+
+        def call():
+            return attn.attn_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), dod.data_ptr(),
+                                 lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.Sq, w.Sk,
+                                 w.D, w.scale, int(w.causal), kv_ptr, ws.data_ptr(), ws.numel(), sptr)
+        self._call = call
+        self._attn = attn
+
+    def step(self):
+        st = self._call()
+        if st != self._attn.ATTN_OK:
+            raise self._attn.AttnError(st, "backward")
+
+
 class Job:
     """Device buffers and the step of one workload.  ``inputs`` are (host,
     device) pairs the end-to-end step copies in; ``outputs`` the device
@@ -355,6 +397,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (dQ, dK, dV) of the workload instead of the forward")
     ap.add_argument("--splits", type=int, default=0,
                     help="use the split-KV forward with this many key ranges (0: the plain forward)")
     args = ap.parse_args()
@@ -387,11 +431,13 @@ def main():
         dist.barrier()
     attn.lib()
 
-    job = Job(w, args, dev, attn, torch)
+    job = (BwdJob if args.backward else Job)(w, args, dev, attn, torch)
+    # FLOPs of a step: the forward's; the backward counts 2.5 times that (its
+    # five products against the forward's two, the usual count)
+    step_flops = w.flops * (2.5 if args.backward else 1.0)
     stream = job.stream
     sptr = stream.cuda_stream
     step = job.step
-    o, lse = job.outputs
 
     # Workloads whose bytes fit in L2 get an L2 flush (a 256 MiB write) before
     # every timed launch; the launch events bracket the kernel alone.
@@ -443,7 +489,7 @@ def main():
         elapsed_ms, launch_ms = float(t[0]), float(t[1])
     # with an L2 flush between launches the step time is the launch alone
     ms_per_step = launch_ms if flush is not None else elapsed_ms / args.steps
-    value = w.flops * world / (ms_per_step * 1e-3) / 1e12
+    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
     clocks = sampler.summary(wall0, wall1)
 
     # ------------------------------------------------------------ end to end
@@ -488,15 +534,17 @@ def main():
         # dense fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
         peak *= 2.0
         peak_src += " x 2 (nominal dense fp8 / bf16 ratio)"
-    achieved = w.flops / (launch_ms * 1e-3) / 1e12
+    achieved = step_flops / (launch_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": recorded_traffic(w.name), "kernel": "attn_fwd_kernel", "peak_source": peak_src,
-                "launch_ms": launch_ms, "algorithmic_flops_per_launch": w.flops,
+                "traffic": None if args.backward else recorded_traffic(w.name),
+                "kernel": "attn_bwd (delta, dq, dkdv kernels)" if args.backward else "attn_fwd_kernel",
+                "peak_source": peak_src,
+                "launch_ms": launch_ms, "algorithmic_flops_per_launch": step_flops,
                 "algorithmic_bytes_per_launch": w.min_bytes}
 
     # ----------------------------------------------------------- CPU oracle
     cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
+    if rank == 0 and not args.no_cpu_baseline and not args.backward:
         q, k, v, kv = generate(w, args.draw)
         flops, secs, blocks = cpu_oracle_steps(w, q, k, v, kv, n_steps=None, budget_s=args.cpu_budget_s)
         cpu = {"value": flops / secs / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
@@ -506,7 +554,8 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "metric": METRIC_BWD if args.backward else METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "e4m3" if is_fp8(w) else "bf16", "data": "synthetic",
             "config": {"workload": w.name, "shape": w.label(), "draw": args.draw,
@@ -520,7 +569,7 @@ def main():
                        "splits": args.splits},
             "roofline": roofline,
             "cpu_baseline": cpu,
-            "e2e": {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "e2e": {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "clocks": clocks,
             "gpu_launches": args.steps * job.launches_per_step,

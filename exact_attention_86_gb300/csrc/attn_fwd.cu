@@ -117,10 +117,29 @@ struct Geo {
   static __device__ __forceinline__ uint32_t kind_use(uint32_t pos) {
     return (kSlots & 1) ? (pos / kSlots) >> 1 : pos / kSlots;
   }
-  static constexpr uint32_t kTmemS = 0;              // + 128 * buffer
-  static constexpr uint32_t kTmemP = 256;            // + 64 * buffer
-  static constexpr uint32_t kTmemO = 384;
+  // Two TMEM protocols (both modelled by the protocol tests):
+  //  bf16: S buffers 0/1 at [0,128) and [128,256), released by the softmax
+  //        once read; P buffers 0/1 at [256,320) and [320,384); one O buffer
+  //        at [384, 384 + D).
+  //  E4M3 (kPInS): S buffers as above, P_b written over the S_b columns each
+  //        half has read (half h: from column 64 h), so S_b is released by
+  //        the P V commit; O buffers 0/1 at [256, 256 + D) and [256 + D,
+  //        256 + 2 D), alternating between consecutive units.  With half-time
+  //        products the shorter QK^T lead costs nothing and the P buffer wait
+  //        disappears (measured faster for E4M3, slower for bf16).
+  static constexpr bool kPInS = FP8;
+  static constexpr int kOBufs = kPInS ? 2 : 1;
+  static constexpr uint32_t kTmemS = 0;                  // + 128 * buffer
+  static constexpr uint32_t kTmemP = 256;                // + 64 * buffer (bf16 protocol)
+  static constexpr uint32_t kTmemO = kPInS ? 256 : 384;  // + D * buffer
   static constexpr int kTmemCols = 512;
+  // TMEM column of the P operand of the kk-th P V instruction, relative to the
+  // tile's S buffer (P over S) or P buffer (16 bf16 keys or 32 E4M3 keys = 8
+  // columns per instruction)
+  static __device__ __forceinline__ uint32_t p_col(int kk) {
+    if constexpr (kPInS) return 64u * static_cast<uint32_t>(kk / 2) + 8u * static_cast<uint32_t>(kk % 2);
+    return 8u * static_cast<uint32_t>(kk);
+  }
   static constexpr int kOffQ = 4096;                 // after control block and exchange buffers
   static constexpr int kOffRing = kOffQ + kTileBytes;
   static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes + 1024;  // + alignment slack
@@ -130,7 +149,7 @@ struct Ctrl {
   uint64_t q_full, q_empty;
   uint64_t k_full[12], v_full[12], kv_empty[12];  // full: per kind (see Geo::kind_use)
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
-  uint64_t o_full;
+  uint64_t o_full[2], o_free[2];
   uint64_t drain[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -409,10 +428,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_kv_empty0 = smem_addr(&ctl.kv_empty[0]);
   // barrier of buffer b = barrier of buffer 0 + 8 * b (consecutive uint64_t)
   const uint32_t bar_s_full0 = smem_addr(&ctl.s_full[0]);
-  const uint32_t bar_s_free0 = smem_addr(&ctl.s_free[0]);
+  const uint32_t bar_s_free0 = smem_addr(&ctl.s_free[0]);  // bf16 protocol: the softmax has read S_b
   const uint32_t bar_p_full0 = smem_addr(&ctl.p_full[0]);
-  const uint32_t bar_p_free0 = smem_addr(&ctl.p_free[0]);
-  const uint32_t bar_o_full = smem_addr(&ctl.o_full);
+  const uint32_t bar_p_free0 = smem_addr(&ctl.p_free[0]);  // P V of the buffer's tile done: P_b (and S_b) free
+  const uint32_t bar_o_full0 = smem_addr(&ctl.o_full[0]);
+  const uint32_t bar_o_free0 = smem_addr(&ctl.o_free[0]);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
@@ -427,9 +447,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_s_free0 + 8 * b, kSoftmaxWarps);
       mbar_init(bar_p_full0 + 8 * b, kSoftmaxWarps);
       mbar_init(bar_p_free0 + 8 * b, 1);
+      mbar_init(bar_o_full0 + 8 * b, 1);
+      mbar_init(bar_o_free0 + 8 * b, kSoftmaxWarps);
       mbar_init(smem_addr(&ctl.drain[b]), 1);
     }
-    mbar_init(bar_o_full, 1);
     ctl.abort_flag = 0;
     fence_barrier_init();
   }
@@ -546,8 +567,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < u.n; ++j, ++tcount) {
         const uint32_t b = tcount & 1u;
         const uint32_t use = tcount >> 1;
-        if (tcount >= 2) {  // the softmax has read S of tile tcount-2 out of buffer b
-          if (!wait_warp(bar_s_free0 + 8 * b, (use - 1) & 1u, abort_flag, kSiteSFree, limit)) { ok = false; break; }
+        if (tcount >= 2) {
+          // S_b is free once the softmax has read S of tile tcount-2 (bf16), or
+          // once the P V of tile tcount-2 has consumed the P written over it
+          const uint32_t bar_sb = (G::kPInS ? bar_p_free0 : bar_s_free0) + 8 * b;
+          if (!wait_warp(bar_sb, (use - 1) & 1u, abort_flag, kSiteSFree, limit)) { ok = false; break; }
           tc_fence_after_sync();
         }
         const uint32_t pos = ring + 2 * j;
@@ -582,7 +606,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpPV) {
     // ---------------------------------------------------- O += P V issuer
-    uint32_t ring = 0, tcount = 0;
+    // Consecutive units alternate between the two O buffers, so a unit's
+    // products never wait for the epilogue of the unit before.
+    uint32_t ring = 0, tcount = 0, ucount = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
       const int unit = unit_at<CAUSAL>(t);
@@ -593,7 +619,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t b = tcount & 1u;
         const uint32_t use = tcount >> 1;
         if (!wait_warp(bar_p_full0 + 8 * b, use & 1u, abort_flag, kSitePFull, limit)) { ok = false; break; }
+        const uint32_t ob = ucount % G::kOBufs;
+        if (G::kPInS && j == 0 && ucount >= 2 &&  // the epilogue two units back has read O buffer ob
+            !wait_warp(bar_o_free0 + 8 * ob, ((ucount >> 1) - 1) & 1u, abort_flag, kSiteOFull, limit)) {
+          ok = false;
+          break;
+        }
         tc_fence_after_sync();
+        const uint32_t tOb = tmem + G::kTmemO + static_cast<uint32_t>(D) * ob;
+        // the tile's P: over its S buffer, or in its own P buffer
+        const uint32_t tSb = tmem + (G::kPInS ? G::kTmemS + 128u * b : G::kTmemP + 64u * b);
         const uint32_t pos = ring + 2 * j + 1;
         const uint32_t slot = pos % G::kSlots;
         if (!wait_warp(bar_v_full0 + 8 * slot, G::kind_use(pos) & 1u, abort_flag, kSiteKvFull, limit)) {
@@ -606,24 +641,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           // column) and V^T K-major in shared memory (rows of D, keys contiguous).
 #pragma unroll
           for (int kk = 0; kk < kBK / 32; ++kk)
-            mma_ts_f8_elect(tmem + G::kTmemO, tmem + G::kTmemP + 64u * b + kk * 8,
-                            sdesc_sw128(va + kk * 32, 16, 1024), p.idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_f8_elect(tOb, tSb + G::p_col(kk), sdesc_sw128(va + kk * 32, 16, 1024), p.idesc_pv,
+                            (j > 0 || kk > 0) ? 1u : 0u);
         } else {
           // O += P_b V_j: P from TMEM (16 keys = 8 columns per MMA), V MN-major in
           // smem (LBO = distance between 64-column chunks of D, SBO = 8 keys x 128 B).
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            mma_ts_elect(tmem + G::kTmemO, tmem + G::kTmemP + 64u * b + kk * 8,
-                         sdesc_sw128(va + kk * 16 * 128, G::kChunkBytes, 1024), p.idesc_pv,
-                         (j > 0 || kk > 0) ? 1u : 0u);
+            mma_ts_elect(tOb, tSb + G::p_col(kk), sdesc_sw128(va + kk * 16 * 128, G::kChunkBytes, 1024),
+                         p.idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
           }
         }
         mma_commit_elect(bar_p_free0 + 8 * b);
         mma_commit_elect(bar_kv_empty0 + 8 * slot);
-        if (j == u.n - 1) mma_commit_elect(bar_o_full);
+        if (j == u.n - 1) mma_commit_elect(bar_o_full0 + 8 * ob);
       }
       if (!ok) break;
       ring += 2 * u.n;
+      ++ucount;
     }
     if (!ok) {
       const uint32_t bar_d = smem_addr(&ctl.drain[1]);
@@ -650,7 +685,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = warp >> 2;
     const int r = threadIdx.x & (kBQ - 1);         // row within the tile == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tO = tmem + lane_off + G::kTmemO + (D / 2) * half;
     const float c = p.c;
     const uint32_t bar_pair = 1u + static_cast<uint32_t>(warp & 3);
     constexpr uint32_t kPairThreads = 64;
@@ -693,13 +727,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
 
+      // this unit's O buffer (units with keys alternate, as in the P V issuer)
+      const uint32_t ob = ocount % G::kOBufs;
+      const uint32_t tO = tmem + lane_off + G::kTmemO + static_cast<uint32_t>(D) * ob + (D / 2) * half;
       float m_used = -INFINITY;  // reference max (log2 units, scale folded in), shared by both halves
       float l = 0.0f;            // this half's sum of 2^(x - m_used)
       bool failed = false;
       for (int j = 0; j < u.n; ++j, ++tcount) {
         const uint32_t b = tcount & 1u;
         const uint32_t use = tcount >> 1;
-        const uint32_t bar_pf = bar_p_free0 + 8 * b;
         const int k0 = (u.j0 + j) * kBK;
         const bool masked = (k0 + kBK > u.kv) || (CAUSAL && k0 + kBK - 1 > u.q0);
         int climit = u.kv - k0;  // columns >= climit of the tile are masked for this row
@@ -719,10 +755,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_32x32b_x32(tS + 32, s[1]);
           tmem_ld_wait_x32(s[0]);
           tmem_ld_wait_x32(s[1]);
-          warp_arrive_after_tc(bar_s_free0 + 8 * b, lane);  // the QK issuer may refill buffer b
-          // P buffer b is free once the PV of tile tcount-2 has completed: ask
-          // now, use the answer after the exponentials.
-          if (tcount >= 2) pf_ready = mbar_test_wait(bar_pf, (use - 1) & 1u);
+          if constexpr (!G::kPInS) {
+            warp_arrive_after_tc(bar_s_free0 + 8 * b, lane);  // the QK issuer may refill S_b
+            // P buffer b is free once the P V of tile tcount-2 has completed:
+            // ask now, use the answer after the exponentials.
+            if (tcount >= 2) pf_ready = mbar_test_wait(bar_p_free0 + 8 * b, (use - 1) & 1u);
+          }
+          // (P over S: P_b goes over the columns just read; S_b was written
+          // after the P V of tile tcount-2 had consumed the previous P_b.)
           if (j > 0) {
             // Exponentiate against the current reference right away.  Each term
             // is 2^(x - m_used + shift); if they all stay <= 2^(tau + shift) no
@@ -779,7 +819,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (!pf_ready && !wait_warp(bar_pf, (use - 1) & 1u, abort_flag, kSitePFree, limit)) failed = true;
+        if (!G::kPInS && !pf_ready &&
+            !wait_warp(bar_p_free0 + 8 * b, (use - 1) & 1u, abort_flag, kSitePFree, limit))
+          failed = true;
         if (rescale && !failed) {
           // O is stable once the PV of the previous tile (buffer b^1) completed.
           const uint32_t tp = tcount - 1;
@@ -793,11 +835,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!failed) {
           tc_fence_after_sync();
-          if constexpr (FP8) {  // 64 keys x 1 B = 16 columns per half
-            const uint32_t tP = tmem + lane_off + G::kTmemP + 64u * b + 16u * half;
+          const uint32_t tP = tmem + lane_off +
+                              (G::kPInS ? G::kTmemS + 128u * b + 64u * half    // over this half's S
+                                        : G::kTmemP + 64u * b + 32u * half);   // own P buffer
+          if constexpr (FP8) {  // 64 keys x 1 B = 16 columns
             tmem_st_32x32b_x16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
-          } else {              // 64 keys x 2 B = 32 columns per half
-            const uint32_t tP = tmem + lane_off + G::kTmemP + 64u * b + 32u * half;
+          } else {              // 64 keys x 2 B = 32 columns
             tmem_st_32x32b_x16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
             tmem_st_32x32b_x16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
           }
@@ -809,7 +852,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
 
       // ------------------------------------------------------------ epilogue
-      if (!failed && !wait_warp(bar_o_full, ocount & 1u, abort_flag, kSiteOFull, limit)) failed = true;
+      if (!failed &&
+          !wait_warp(bar_o_full0 + 8 * ob, (ocount / G::kOBufs) & 1u, abort_flag, kSiteOFull, limit))
+        failed = true;
       ++ocount;
       if (!failed) xch.xsum[half][r] = l;
       if (named_bar_red_or(bar_pair, kPairThreads, *abort_flag != 0)) { ok = false; break; }
@@ -842,13 +887,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if constexpr (G::kPInS) {
+        // O buffer ob has been read: the unit two units later may use it
+        warp_arrive_after_tc(bar_o_free0 + 8 * ob, lane);
+      } else {
+        // one O buffer: the next unit's first P V overwrites it only after every
+        // softmax warp has arrived on p_full for it, which comes after this
+        tc_fence_before_sync();
+      }
       if (row_ok && half == 0) {
         if (op_dst == nullptr) p.lse[lse_index] = lse_row;
         else p.lse_part[prow] = lse_row;
       }
-      // The next unit's first PV overwrites O only after every softmax warp has
-      // arrived on p_full for it, which each warp does after this epilogue.
-      tc_fence_before_sync();
     }
     // The last p_free arrivals (commits of the last two PVs) land
     // asynchronously and nothing else waits for them: wait before exiting.

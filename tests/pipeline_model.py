@@ -2,7 +2,14 @@
 logic only; no attention arithmetic).
 
 Roles, as in the kernel: the TMA producer, the QK^T issuer, the softmax warps
-(one actor) and the P.V issuer.  TMA loads land after random delays, in any
+(one actor) and the P.V issuer.  Tensor memory as in the kernel, in both of
+its protocols: (bf16) two S buffers released by the softmax once read, two
+P buffers, one O buffer; (E4M3) two S buffers with P_b written over S_b and
+released by the P V commit, and two O buffers that consecutive units
+alternate between.  The model checks that no S or P buffer is overwritten
+before it has been consumed, that P V reads the P of its own tile, that a
+rescale or an epilogue sees O holding exactly the products issued so far,
+and that an O buffer is reused only after its epilogue.  TMA loads land after random delays, in any
 order; the MMAs of one issuer complete in order after random delays, and a
 tcgen05.commit arrival fires when every earlier MMA of its issuer completed.
 A wait follows the hardware rule for a parity wait, passing iff the parity
@@ -53,7 +60,13 @@ class Bar:
         return ok
 
 
-def run(units, slots, per_kind, seed, rescale_p=0.3):
+def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False):
+    """``p_in_s`` selects the E4M3 kernel's protocol (P written over S, two O
+    buffers, S released by the P V commit) instead of the bf16 kernel's
+    (separate P buffers, S released by the softmax, one O buffer).
+    ``mistake`` plants one protocol error, for the tests that show the model
+    catches it: "qk_skips_buffer_wait", "pv_skips_o_free",
+    "rescale_skips_p_free", "p_store_skips_p_free"."""
     rng = random.Random(seed)
     B = {}
 
@@ -63,8 +76,9 @@ def run(units, slots, per_kind, seed, rescale_p=0.3):
         return B[name]
 
     for b in (0, 1):
-        bar(f"s_full{b}"); bar(f"s_free{b}"); bar(f"p_full{b}"); bar(f"p_free{b}")
-    bar("q_full"); bar("q_empty"); bar("o_full")
+        bar(f"s_full{b}"); bar(f"s_free{b}"); bar(f"p_full{b}"); bar(f"p_free{b}"); bar(f"o_full{b}")
+        bar(f"o_free{b}")
+    bar("q_full"); bar("q_empty")
 
     def full_bar(pos):
         slot = pos % slots
@@ -121,6 +135,16 @@ def run(units, slots, per_kind, seed, rescale_p=0.3):
                     later(rng.expovariate(0.5) if rng.random() < 0.9 else rng.uniform(5, 30), land)
                     ring += 1
 
+    # TMEM state.  S_b: ("S", t) after QK_t, then ("S", t, "read") once the
+    # softmax has read it (separate-P protocol) or ("P", t) once P_t is written
+    # over it (P-over-S protocol), ("P", t, "done") after P V_t.  P_b (separate
+    # P buffers): ("P", t), then ("P", t, "done").  O buffers: ("busy", unit,
+    # last tile issued) or ("free", unit whose epilogue read it).
+    tmem_s = {0: None, 1: None}
+    tmem_p = {0: None, 1: None}
+    n_obuf = 2 if p_in_s else 1
+    o_state = {0: ("free", -2 if p_in_s else -1), 1: ("free", -1)}
+
     def qk():
         ring = qcount = tcount = 0
         for n in units:
@@ -128,15 +152,22 @@ def run(units, slots, per_kind, seed, rescale_p=0.3):
             qcount += 1
             for j in range(n):
                 b, use = tcount & 1, tcount >> 1
-                if tcount >= 2:
-                    yield lambda: bar(f"s_free{b}").try_wait((use - 1) & 1, use - 1)
+                if tcount >= 2 and mistake != "qk_skips_buffer_wait":
+                    if p_in_s:   # the P V of tile tcount-2 has consumed P_b, which overlays S_b
+                        yield lambda: bar(f"p_free{b}").try_wait((use - 1) & 1, use - 1)
+                    else:        # the softmax has read S of tile tcount-2
+                        yield lambda: bar(f"s_free{b}").try_wait((use - 1) & 1, use - 1)
                 pos = ring + 2 * j
                 slot = pos % slots
                 yield lambda: full_bar(pos).try_wait(full_use(pos) & 1, full_use(pos))
                 assert slot_data.get(slot) == pos, f"QK read slot {slot}: has {slot_data.get(slot)}, wants {pos}"
+                st = tmem_s[b]
+                ok_prev = ("P", tcount - 2, "done") if p_in_s else ("S", tcount - 2, "read")
+                assert st is None or st == ok_prev, f"S{b} overwritten while holding {st}"
 
-                def chk(slot=slot, pos=pos):
+                def chk(slot=slot, pos=pos, b=b, t=tcount):
                     assert slot_data.get(slot) == pos, f"K slot {slot} overwritten under the MMA"
+                    tmem_s[b] = ("S", t)
                 mma("qk", chk, [bar(f"s_full{b}"), bar(f"kv_empty{slot}")])
                 tcount += 1
             ring += 2 * n
@@ -145,39 +176,66 @@ def run(units, slots, per_kind, seed, rescale_p=0.3):
     def softmax():
         tcount = ocount = 0
         for n in units:
+            ob = ocount % n_obuf
             for j in range(n):
                 b, use = tcount & 1, tcount >> 1
                 yield lambda: bar(f"s_full{b}").try_wait(use & 1, use)
-                bar(f"s_free{b}").arrive()
-                if tcount >= 2:
-                    yield lambda: bar(f"p_free{b}").try_wait((use - 1) & 1, use - 1)
-                if j > 0 and rng.random() < rescale_p:
+                assert tmem_s[b] == ("S", tcount), f"softmax read S{b} holding {tmem_s[b]}, wants tile {tcount}"
+                if not p_in_s:
+                    tmem_s[b] = ("S", tcount, "read")
+                    bar(f"s_free{b}").arrive()
+                    if tcount >= 2 and mistake != "p_store_skips_p_free":   # P_b consumed by P V tcount-2
+                        yield lambda: bar(f"p_free{b}").try_wait((use - 1) & 1, use - 1)
+                if j > 0 and rng.random() < rescale_p:   # O (this unit's buffer) is rescaled in place
                     tp = tcount - 1
-                    yield lambda: bar(f"p_free{tp & 1}").try_wait((tp >> 1) & 1, tp >> 1)
+                    if mistake != "rescale_skips_p_free":
+                        yield lambda: bar(f"p_free{tp & 1}").try_wait((tp >> 1) & 1, tp >> 1)
+                    assert o_state[ob] == ("busy", ocount, tp), f"rescale of O{ob} while {o_state[ob]}"
+                if p_in_s:
+                    tmem_s[b] = ("P", tcount)
+                else:
+                    pb = tmem_p[b]
+                    assert pb is None or pb == ("P", tcount - 2, "done"), f"P{b} overwritten while holding {pb}"
+                    tmem_p[b] = ("P", tcount)
                 bar(f"p_full{b}").arrive()
                 tcount += 1
-            yield lambda: bar("o_full").try_wait(ocount & 1, ocount)
+            phase = ocount // n_obuf
+            yield lambda: bar(f"o_full{ob}").try_wait(phase & 1, phase)
+            assert o_state[ob] == ("busy", ocount, tcount - 1), f"epilogue read O{ob} while {o_state[ob]}"
+            o_state[ob] = ("free", ocount)
+            if p_in_s:
+                bar(f"o_free{ob}").arrive()
             ocount += 1
 
     def pv():
-        ring = tcount = 0
+        ring = tcount = ucount = 0
         for n in units:
+            ob = ucount % n_obuf
             for j in range(n):
                 b, use = tcount & 1, tcount >> 1
                 yield lambda: bar(f"p_full{b}").try_wait(use & 1, use)
+                if p_in_s and j == 0 and ucount >= 2 and mistake != "pv_skips_o_free":
+                    yield lambda: bar(f"o_free{ob}").try_wait(((ucount >> 1) - 1) & 1, (ucount >> 1) - 1)
+                if j == 0:
+                    assert o_state[ob] == ("free", ucount - n_obuf), f"O{ob} reused while {o_state[ob]}"
                 pos = ring + 2 * j + 1
                 slot = pos % slots
                 yield lambda: full_bar(pos).try_wait(full_use(pos) & 1, full_use(pos))
                 assert slot_data.get(slot) == pos, f"PV read slot {slot}: has {slot_data.get(slot)}, wants {pos}"
 
-                def chk(slot=slot, pos=pos):
+                def chk(slot=slot, pos=pos, b=b, t=tcount, u=ucount, ob=ob):
                     assert slot_data.get(slot) == pos, f"V slot {slot} overwritten under the MMA"
+                    buf = tmem_s if p_in_s else tmem_p
+                    assert buf[b] == ("P", t), f"PV read P{b} holding {buf[b]}, wants tile {t}"
+                    buf[b] = ("P", t, "done")
+                    o_state[ob] = ("busy", u, t)
                 commits = [bar(f"p_free{b}"), bar(f"kv_empty{slot}")]
                 if j == n - 1:
-                    commits.append(bar("o_full"))
+                    commits.append(bar(f"o_full{ob}"))
                 mma("pv", chk, commits)
                 tcount += 1
             ring += 2 * n
+            ucount += 1
 
     for s in range(slots):
         bar(f"kv_empty{s}")

@@ -13,15 +13,34 @@ def _units(seed):
     return [rng.choice([1, 2, 3, 5, 8, 16, 64]) for _ in range(rng.randint(1, 6))]
 
 
-@pytest.mark.parametrize("slots", [5, 12])   # the ring depths of D = 128 and D = 64
-def test_per_kind_full_barriers_never_alias_or_deadlock(slots):
+@pytest.mark.parametrize("p_in_s,slots", [(False, 5), (False, 12), (True, 12)])  # bf16 D=128, D=64; E4M3
+def test_kernel_protocol_never_aliases_or_deadlocks(p_in_s, slots):
     for seed in range(400):
-        run(_units(seed), slots, per_kind=True, seed=seed)
+        run(_units(seed), slots, per_kind=True, seed=seed, p_in_s=p_in_s)
 
 
-def test_shared_full_barrier_with_odd_depth_aliases():
-    """The model has teeth: one full barrier per slot with an odd ring depth
-    lets the QK issuer pass a K wait on the phase of an older fill."""
+@pytest.mark.parametrize("p_in_s,mistake", [
+    (False, "qk_skips_buffer_wait"), (False, "p_store_skips_p_free"), (False, "rescale_skips_p_free"),
+    (True, "qk_skips_buffer_wait"), (True, "rescale_skips_p_free"),
+])
+def test_model_catches_a_skipped_wait(p_in_s, mistake):
+    """The model has teeth: leaving out any one of the waits that guard the
+    TMEM buffers shows up as a hazard in some random schedule.  (The E4M3
+    protocol's o_free wait is implied by the softmax's own order, which the
+    model confirms by never needing it; the kernel keeps it.)"""
+    failures = 0
+    for seed in range(300):
+        try:
+            run(_units(seed), 5, per_kind=True, seed=seed, rescale_p=0.6, mistake=mistake, p_in_s=p_in_s)
+        except AssertionError:
+            failures += 1
+    assert failures > 0, mistake
+
+
+def test_odd_depth_with_one_full_barrier_per_slot_aliases_in_the_bf16_protocol():
+    """With S released by the softmax, the QK^T issuer can run ahead of the
+    V fills; one full barrier per slot with an odd depth then aliases (the
+    fault the per-kind barriers fixed)."""
     failures = 0
     for seed in range(200):
         try:
@@ -32,6 +51,11 @@ def test_shared_full_barrier_with_odd_depth_aliases():
     assert failures > 0
 
 
-def test_shared_full_barrier_with_even_depth_is_safe():
+@pytest.mark.parametrize("p_in_s,slots", [(False, 12), (True, 5), (True, 12)])
+def test_one_full_barrier_per_slot_holds_with_even_depth_or_p_over_s(p_in_s, slots):
+    """An even depth keeps each slot to one kind; and with the P V commit
+    releasing the S buffers (E4M3 protocol) the QK^T issuer reaches K_j only
+    after the V fills before it have landed.  The kernel keeps one full
+    barrier per kind all the same."""
     for seed in range(200):
-        run(_units(seed), 12, per_kind=False, seed=seed)
+        run(_units(seed), slots, per_kind=False, seed=seed, p_in_s=p_in_s)
