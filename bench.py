@@ -317,6 +317,12 @@ class Job:
         self.outputs = [o, lse]
         ptr = [t.data_ptr() for t in dev_t]
         total = q.shape[0]
+        # packed and paged batches: dynamic scheduling through a persistent
+        # counter (each launch leaves it zero); --static-schedule turns it off
+        counter_ptr = None
+        if is_varlen(w) and not args.static_schedule:
+            self.counter = torch.zeros(2, dtype=torch.int32, device=dev)
+            counter_ptr = self.counter.data_ptr()
         ws = None
         if args.splits > 0:
             ws_bytes = attn.attn_fwd_splitkv_workspace_size(w.B, w.H, w.Sq, w.D, args.splits)
@@ -329,7 +335,7 @@ class Job:
             def call():
                 return attn.attn_fwd_paged(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), ptr[3], ptr[4],
                                            ptr[5], w.batch, w.max_len, total, num_pages, page_size, max_pages, w.H,
-                                           w.D, w.scale, int(w.causal), sptr)
+                                           w.D, w.scale, int(w.causal), counter_ptr, sptr)
         elif is_fp8(w):
             kv_ptr = ptr[3] if len(ptr) > 3 else None
 
@@ -339,7 +345,8 @@ class Job:
         elif is_varlen(w):
             def call():
                 return attn.attn_fwd_varlen(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), ptr[3], ptr[3],
-                                            w.batch, w.max_len, total, total, w.H, w.D, w.scale, int(w.causal), sptr)
+                                            w.batch, w.max_len, total, total, w.H, w.D, w.scale, int(w.causal),
+                                            counter_ptr, sptr)
         elif ws is None:
             kv_ptr = ptr[3] if len(ptr) > 3 else None
 
@@ -397,6 +404,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--static-schedule", action="store_true",
+                    help="packed/paged workloads: deal the units round-robin instead of claiming them")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (dQ, dK, dV) of the workload instead of the forward")
     ap.add_argument("--splits", type=int, default=0,
@@ -566,7 +575,9 @@ def main():
                              (f"no flush: each step moves {w.min_bytes / 2**20:.0f} MiB of Q/K/V/O/LSE, more "
                               f"than the 129 MB L2"),
                        "parallelism": f"weak: {world} replica(s) of the workload, one per GPU",
-                       "splits": args.splits},
+                       "splits": args.splits,
+                       "schedule": ("static" if args.static_schedule or w.causal else "dynamic") if varlen
+                                   else "static"},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",

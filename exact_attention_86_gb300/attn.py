@@ -43,12 +43,12 @@ SIGNATURES = {
     "attn_fwd_varlen": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
-                                       ctypes.c_int, ctypes.c_void_p]),
+                                       ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "attn_fwd_paged": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
-                                      ctypes.c_void_p]),
+                                      ctypes.c_void_p, ctypes.c_void_p]),
     "attn_fwd_splitkv_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                           ctypes.c_int]),
     "attn_fwd_splitkv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -115,16 +115,18 @@ def attn_fwd_fp8(q: int, k: int, v_t: int, o: int, lse: int, B: int, H: int, Sq:
 
 def attn_fwd_varlen(q: int, k: int, v: int, o: int, lse: int, cu_q: int, cu_k: int, batch: int,
                     max_seqlen_q: int, total_q: int, total_k: int, H: int, D: int, scale: float, causal: int,
-                    stream: Optional[int]) -> int:
+                    tile_counter: Optional[int], stream: Optional[int]) -> int:
     return lib().attn_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, batch, max_seqlen_q, total_q, total_k, H, D, scale,
-                                 int(causal), stream)
+                                 int(causal), tile_counter, stream)
 
 
 def attn_fwd_paged(q: int, k_cache: int, v_cache: int, o: int, lse: int, cu_q: int, seqlens_k: int,
                    block_table: int, batch: int, max_seqlen_q: int, total_q: int, num_pages: int, page_size: int,
-                   max_pages_per_seq: int, H: int, D: int, scale: float, causal: int, stream: Optional[int]) -> int:
+                   max_pages_per_seq: int, H: int, D: int, scale: float, causal: int, tile_counter: Optional[int],
+                   stream: Optional[int]) -> int:
     return lib().attn_fwd_paged(q, k_cache, v_cache, o, lse, cu_q, seqlens_k, block_table, batch, max_seqlen_q,
-                                total_q, num_pages, page_size, max_pages_per_seq, H, D, scale, int(causal), stream)
+                                total_q, num_pages, page_size, max_pages_per_seq, H, D, scale, int(causal),
+                                tile_counter, stream)
 
 
 def attn_fwd_splitkv_workspace_size(B: int, H: int, Sq: int, D: int, num_splits: int) -> int:
@@ -258,8 +260,25 @@ def forward_fp8(q8, k8, v8_t, q_descale: float = 1.0, k_descale: float = 1.0, v_
     return out, lse
 
 
+_counters = {}
+
+
+def tile_counter(device, stream: int):
+    """A zeroed device uint32[2] for dynamic scheduling, one per (device,
+    stream); every launch leaves it zero again, so calls on one stream can
+    share it."""
+    import torch
+
+    key = (str(device), int(stream or 0))
+    t = _counters.get(key)
+    if t is None:
+        t = torch.zeros(2, dtype=torch.int32, device=device)
+        _counters[key] = t
+    return t
+
+
 def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, scale: Optional[float] = None,
-                   causal: bool = False):
+                   causal: bool = False, dynamic: bool = True):
     """Packed variable-length forward on torch CUDA tensors: ``q [total_q, H, D]``,
     ``k``/``v [total_k, H, D]`` bf16, ``cu_seqlens_q``/``cu_seqlens_k`` int32
     ``[batch + 1]`` on the same device.  Returns ``(o [total_q, H, D], lse [H, total_q])``."""
@@ -284,16 +303,17 @@ def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, scale
     lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
+        counter = tile_counter(q.device, stream).data_ptr() if dynamic else None
         st = attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
                              cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), batch, int(max_seqlen_q), total_q,
-                             total_k, H, D, float(scale), int(bool(causal)), stream)
+                             total_k, H, D, float(scale), int(bool(causal)), counter, stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_varlen")
     return out, lse
 
 
 def forward_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, max_seqlen_q: int,
-                  scale: Optional[float] = None, causal: bool = False):
+                  scale: Optional[float] = None, causal: bool = False, dynamic: bool = True):
     """Packed queries ``q [total_q, H, D]`` against a paged KV cache
     ``k_cache``/``v_cache [num_pages, page_size, H, D]`` (bf16 CUDA tensors);
     ``cu_seqlens_q`` int32 ``[batch + 1]``, ``seqlens_k`` int32 ``[batch]``,
@@ -323,10 +343,11 @@ def forward_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, max
     lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
+        counter = tile_counter(q.device, stream).data_ptr() if dynamic else None
         st = attn_fwd_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), lse.data_ptr(),
                             cu_seqlens_q.data_ptr(), seqlens_k.data_ptr(), block_table.data_ptr(), batch,
                             int(max_seqlen_q), total_q, num_pages, page_size, block_table.shape[1], H, D,
-                            float(scale), int(bool(causal)), stream)
+                            float(scale), int(bool(causal)), counter, stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_paged")
     return out, lse

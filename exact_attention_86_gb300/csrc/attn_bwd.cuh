@@ -881,6 +881,7 @@ attn_status run_backward(DeviceInfo& dev, const void* q, const void* k, const vo
   f.total_q = 0;
   f.total_k = 0;
   clear_paged(f);
+  f.sched = nullptr;
   f.c = 0.0f;
   f.v_scale = 1.0f;
   f.idesc_qk = 0;

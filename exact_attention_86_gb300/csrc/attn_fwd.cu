@@ -62,6 +62,8 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpQK = 9;
 constexpr int kWarpPV = 10;
+constexpr int kUnitQ = 4;           // depth of a CTA's unit queue
+constexpr int kUnitQReaders = 10;   // warps that read it: QK^T issuer, P V issuer, 8 softmax warps
 // Lazy rescale threshold (log2 units) and the shift of P (log2 units): each P
 // term is 2^(x - m + shift) <= 2^(tau + shift).  bf16 P: tau 16, shift 0.
 // E4M3 P (largest finite value 448): tau 4.5, shift 4, so terms stay <= 2^8.5
@@ -87,6 +89,7 @@ enum WaitSite : uint32_t {
   kSiteSelftest = 8,
   kSiteSFree = 9,
   kSitePFree = 10,
+  kSiteUnitQ = 11,
 };
 
 // [0]: 1 once any wait gave up; [1]: site of the first one; [2]: its block.
@@ -150,6 +153,8 @@ struct Ctrl {
   uint64_t k_full[12], v_full[12], kv_empty[12];  // full: per kind (see Geo::kind_use)
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t o_full[2], o_free[2];
+  uint64_t uq_full[4], uq_empty[4];  // the CTA's unit queue (filled by the producer lane)
+  int unit_q[4];
   uint64_t drain[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -188,6 +193,8 @@ struct Params {
   const int32_t* seqlens_k;
   int page_size, max_pages, num_pages;
   int cache_tokens;        // num_pages * page_size: a key coordinate that reads zeros
+  uint32_t* sched;         // dynamic scheduling: [0] next unit to claim, [1] CTAs done (both 0 on entry
+                           // and on exit); nullptr: static round-robin
   float c;                 // |scale| * log2(e) (E4M3: |scale * q_descale * k_descale| * log2(e))
   float v_scale;           // 1, or the E4M3 V descale (multiplies O)
   uint32_t idesc_qk;       // negate-A set when scale < 0
@@ -299,6 +306,20 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t site,
                                           uint64_t limit_ns) {
   return __all_sync(0xffffffffu, wait_phase(bar, parity, abort_flag, site, limit_ns));
+}
+
+// Next unit of this CTA from its unit queue, which the producer lane fills:
+// every reading warp takes each entry once, in order.  Returns the unit, -1
+// at the end of the CTA's work, or -2 when the wait gave up.
+__device__ __forceinline__ int take_unit(uint32_t& k, volatile int* unit_q, uint32_t full0, uint32_t empty0,
+                                         volatile int* abort_flag, uint64_t limit, int lane) {
+  const uint32_t slot = k % kUnitQ;
+  if (!wait_warp(full0 + 8 * slot, (k / kUnitQ) & 1u, abort_flag, kSiteUnitQ, limit)) return -2;
+  const int unit = unit_q[slot];
+  __syncwarp();
+  if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+  ++k;
+  return unit;
 }
 
 // Wait used only while draining after an abort: ignores the abort flag.
@@ -433,6 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_p_free0 = smem_addr(&ctl.p_free[0]);  // P V of the buffer's tile done: P_b (and S_b) free
   const uint32_t bar_o_full0 = smem_addr(&ctl.o_full[0]);
   const uint32_t bar_o_free0 = smem_addr(&ctl.o_free[0]);
+  const uint32_t bar_uq_full0 = smem_addr(&ctl.uq_full[0]);
+  const uint32_t bar_uq_empty0 = smem_addr(&ctl.uq_empty[0]);
+  volatile int* unit_q = ctl.unit_q;
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
@@ -450,6 +474,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_o_full0 + 8 * b, 1);
       mbar_init(bar_o_free0 + 8 * b, kSoftmaxWarps);
       mbar_init(smem_addr(&ctl.drain[b]), 1);
+    }
+    for (int k = 0; k < kUnitQ; ++k) {
+      mbar_init(bar_uq_full0 + 8 * k, 1);
+      mbar_init(bar_uq_empty0 + 8 * k, kUnitQReaders);
     }
     ctl.abort_flag = 0;
     fence_barrier_init();
@@ -479,11 +507,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_keep = l2_policy_evict_last();   // K/V: re-read by every query block of the head
       const uint64_t pol_once = l2_policy_evict_first();  // Q: read once
-      uint32_t ring = 0, qcount = 0;
+      uint32_t ring = 0, qcount = 0, kq = 0;
+      int t_static = blockIdx.x;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
-        const int unit = unit_at<CAUSAL>(t);
-        if (unit >= p.total_units) continue;
+      while (ok) {
+        // The next unit with rows: claimed from the launch's counter (dynamic:
+        // any CTA takes the next unit in the units' own order, longest first
+        // when causal) or dealt round-robin; pushed to the CTA's unit queue.
+        int unit = -1;
+        for (;;) {
+          int cand;
+          if (p.sched != nullptr) {
+            cand = static_cast<int>(atomicAdd(p.sched, 1u));
+            if (cand >= p.total_units) break;
+          } else {
+            if (t_static >= t_end) break;
+            cand = unit_at<CAUSAL>(t_static);
+            t_static += gridDim.x;
+            if (cand >= p.total_units) continue;
+          }
+          if (decode_unit<CAUSAL>(p, cand).rows > 0) {
+            unit = cand;
+            break;
+          }
+        }
+        {
+          const uint32_t slot = kq % kUnitQ;
+          if (!wait_phase(bar_uq_empty0 + 8 * slot, ((kq / kUnitQ) & 1u) ^ 1u, abort_flag, kSiteUnitQ, limit)) {
+            ok = false;
+            break;
+          }
+          unit_q[slot] = unit;
+          mbar_arrive(bar_uq_full0 + 8 * slot);
+          ++kq;
+        }
+        if (unit < 0) break;
         const Unit u = decode_unit<CAUSAL>(p, unit);
         if (u.n == 0) continue;
         if (!wait_phase(bar_q_empty, (qcount & 1u) ^ 1u, abort_flag, kSiteQEmpty, limit)) { ok = false; break; }
@@ -548,19 +606,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);
         wait_phase_drain(bar_kv_empty0 + 8 * s, (last / G::kSlots) & 1u);
       }
+      // Dynamic scheduling: this CTA makes no more claims.  The last CTA to get
+      // here (every CTA does, aborting or not) puts the counter back to 0 for
+      // the next launch that uses it.
+      if (p.sched != nullptr) {
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+          atomicExch(p.sched, 0u);
+          atomicExch(p.sched + 1, 0u);
+        }
+      }
     }
     __syncwarp();
   } else if (warp == kWarpQK) {
     // ---------------------------------------------------- S = Q K^T issuer
     // Runs up to two tiles ahead of the softmax (two S buffers).  Releases
     // each K slot once its MMAs complete.
-    uint32_t ring = 0, qcount = 0, tcount = 0;
+    uint32_t ring = 0, qcount = 0, tcount = 0, kq = 0;
     bool ok = true;
     const uint32_t qa = base + G::kOffQ;
-    for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
-      const int unit = unit_at<CAUSAL>(t);
-        if (unit >= p.total_units) continue;
-        const Unit u = decode_unit<CAUSAL>(p, unit);
+    while (ok) {
+      const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
+      if (unit == -2) { ok = false; break; }
+      if (unit < 0) break;
+      const Unit u = decode_unit<CAUSAL>(p, unit);
       if (u.n == 0) continue;
       if (!wait_warp(bar_q_full, qcount & 1u, abort_flag, kSiteQFull, limit)) { ok = false; break; }
       ++qcount;
@@ -608,12 +677,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------- O += P V issuer
     // Consecutive units alternate between the two O buffers, so a unit's
     // products never wait for the epilogue of the unit before.
-    uint32_t ring = 0, tcount = 0, ucount = 0;
+    uint32_t ring = 0, tcount = 0, ucount = 0, kq = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
-      const int unit = unit_at<CAUSAL>(t);
-        if (unit >= p.total_units) continue;
-        const Unit u = decode_unit<CAUSAL>(p, unit);
+    while (ok) {
+      const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
+      if (unit == -2) { ok = false; break; }
+      if (unit < 0) break;
+      const Unit u = decode_unit<CAUSAL>(p, unit);
       if (u.n == 0) continue;
       for (int j = 0; j < u.n; ++j, ++tcount) {
         const uint32_t b = tcount & 1u;
@@ -688,13 +758,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c = p.c;
     const uint32_t bar_pair = 1u + static_cast<uint32_t>(warp & 3);
     constexpr uint32_t kPairThreads = 64;
-    uint32_t tcount = 0, ocount = 0;
+    uint32_t tcount = 0, ocount = 0, kq = 0;
     bool ok = true;
 
-    for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
-      const int unit = unit_at<CAUSAL>(t);
-        if (unit >= p.total_units) continue;
-        const Unit u = decode_unit<CAUSAL>(p, unit);
+    while (ok) {
+      const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
+      // both warps of the pair read the same entry; they leave together if
+      // either gave up or the CTA aborts
+      if (named_bar_red_or(bar_pair, kPairThreads, unit == -2 || *abort_flag != 0)) { ok = false; break; }
+      if (unit < 0) break;
+      const Unit u = decode_unit<CAUSAL>(p, unit);
       const int row = u.q0 + r;     // position of this thread's query row within its sequence
       const bool row_ok = r < u.rows;
       size_t row_index, lse_index;  // row of O (in units of D elements) and index into lse
@@ -1185,6 +1258,7 @@ Params packed_params(void* o, float* lse, const int32_t* cu_q, int batch, int ma
   p.total_q = total_q;
   p.total_k = 0;
   clear_paged(p);
+  p.sched = nullptr;
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634);
   p.v_scale = 1.0f;
   p.idesc_qk = idesc_bf16_f32(kBQ, kBK, scale < 0.0f, false);
@@ -1229,6 +1303,7 @@ attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const voi
   p.total_q = 0;
   p.total_k = 0;
   clear_paged(p);
+  p.sched = nullptr;
   p.c = static_cast<float>(std::fabs(static_cast<double>(scale)) * 1.4426950408889634);
   p.v_scale = 1.0f;
   p.idesc_qk = idesc_bf16_f32(kBQ, kBK, scale < 0.0f, false);
@@ -1306,6 +1381,7 @@ attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o,
   p.total_q = 0;
   p.total_k = 0;
   clear_paged(p);
+  p.sched = nullptr;
   p.c = static_cast<float>(std::fabs(qk_scale) * 1.4426950408889634);
   p.v_scale = v_descale;
   p.idesc_qk = idesc_e4m3_f32(kBQ, kBK, qk_scale < 0.0);
@@ -1317,7 +1393,7 @@ attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o,
 
 attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int max_seqlen_q,
-                            int total_q, int total_k, int H, int D, float scale, int causal,
+                            int total_q, int total_k, int H, int D, float scale, int causal, uint32_t* tile_counter,
                             attn_stream_t stream) {
   if (batch < 0 || max_seqlen_q < 0 || total_q < 0 || total_k < 0 || H < 0) return ATTN_ERR_SHAPE;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED_D;
@@ -1330,6 +1406,7 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
       !aligned(cu_seqlens_k, 4))
     return ATTN_ERR_ALIGN;
   if (total_k > 0 && (!aligned(k, 16) || !aligned(v, 16))) return ATTN_ERR_ALIGN;
+  if (tile_counter != nullptr && !aligned(tile_counter, 8)) return ATTN_ERR_ALIGN;
   const uint64_t max_t = static_cast<uint64_t>(total_q > total_k ? total_q : total_k);
   if (max_t * H * D * 2 >= (1ull << 40)) return ATTN_ERR_SHAPE;
   const uint64_t n_qtiles = (static_cast<uint64_t>(max_seqlen_q) + kBQ - 1) / kBQ;
@@ -1348,13 +1425,19 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   Params p = packed_params(o, lse, cu_seqlens_q, batch, max_seqlen_q, total_q, H, D, scale);
   p.cu_k = cu_seqlens_k;
   p.total_k = total_k;
+  // claimed units balance ragged non-causal batches (measured +18 %); causal
+  // batches keep the longest-first snake deal, since claiming them in
+  // longest-first order walks through the empty high query tiles of the short
+  // sequences one atomic at a time (measured 8 % slower)
+  p.sched = causal ? nullptr : tile_counter;
   return launch_any(*dev, D, causal != 0, mq, mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
 }
 
 attn_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
                            const int32_t* cu_seqlens_q, const int32_t* seqlens_k, const int32_t* block_table,
                            int batch, int max_seqlen_q, int total_q, int num_pages, int page_size,
-                           int max_pages_per_seq, int H, int D, float scale, int causal, attn_stream_t stream) {
+                           int max_pages_per_seq, int H, int D, float scale, int causal, uint32_t* tile_counter,
+                           attn_stream_t stream) {
   if (batch < 0 || max_seqlen_q < 0 || total_q < 0 || H < 0) return ATTN_ERR_SHAPE;
   if (num_pages < 1 || max_pages_per_seq < 1 || page_size < 64 || page_size % 64 != 0) return ATTN_ERR_SHAPE;
   if (static_cast<uint64_t>(num_pages) * page_size + 64 > 0x7fffffffull ||
@@ -1367,7 +1450,8 @@ attn_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cac
       cu_seqlens_q == nullptr || seqlens_k == nullptr || block_table == nullptr)
     return ATTN_ERR_NULLPTR;
   if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
-      !aligned(cu_seqlens_q, 4) || !aligned(seqlens_k, 4) || !aligned(block_table, 4))
+      !aligned(cu_seqlens_q, 4) || !aligned(seqlens_k, 4) || !aligned(block_table, 4) ||
+      (tile_counter != nullptr && !aligned(tile_counter, 8)))
     return ATTN_ERR_ALIGN;
   const uint64_t cache_tokens = static_cast<uint64_t>(num_pages) * page_size;
   const uint64_t max_t = cache_tokens > static_cast<uint64_t>(total_q) ? cache_tokens : total_q;
@@ -1389,6 +1473,7 @@ attn_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cac
   p.max_pages = max_pages_per_seq;
   p.num_pages = num_pages;
   p.cache_tokens = static_cast<int>(cache_tokens);
+  p.sched = causal ? nullptr : tile_counter;  // as attn_fwd_varlen
   return launch_any(*dev, D, causal != 0, mq, mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -128,11 +128,20 @@ attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o,
  * within the sequence; a sequence with no key gives O = 0, LSE = -inf).  The
  * last 128-key tile of a sequence also reads the next sequence's first keys
  * with weight zero (they must be finite); past total_k the tile reads zeros.
+ * tile_counter NULL (work is dealt round-robin to the SMs) or device uint32
+ *              [2], 8-byte aligned, both zero on entry: for a non-causal call
+ *              the SMs then claim the units of work (128 query rows of one
+ *              sequence and head) one by one, which balances ragged batches;
+ *              causal calls keep the longest-first round-robin deal and do
+ *              not touch it.  A launch leaves both words zero when it ends,
+ *              so one counter serves consecutive calls on a stream; calls that
+ *              share a counter must not overlap on the GPU.
  * Asynchronous on `stream`; argument errors return before any launch.
  */
 attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int max_seqlen_q,
-                            int total_q, int total_k, int H, int D, float scale, int causal, attn_stream_t stream);
+                            int total_q, int total_k, int H, int D, float scale, int causal, uint32_t* tile_counter,
+                            attn_stream_t stream);
 
 /*
  * attn_fwd_paged — the packed-query forward with keys and values read through
@@ -156,13 +165,15 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
  * query i of the sequence sees keys j <= i).  Slots of the last used page past
  * seqlens_k[b] that share a 64-key half with a valid key are read with weight
  * zero and must hold finite values; whole halves past it read zeros.
- * Asynchronous on `stream`; argument errors return before any launch
- * (page_size, num_pages or max_pages_per_seq out of range: ATTN_ERR_SHAPE).
+ * tile_counter as attn_fwd_varlen.  Asynchronous on `stream`; argument errors
+ * return before any launch (page_size, num_pages or max_pages_per_seq out of
+ * range: ATTN_ERR_SHAPE).
  */
 attn_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
                            const int32_t* cu_seqlens_q, const int32_t* seqlens_k, const int32_t* block_table,
                            int batch, int max_seqlen_q, int total_q, int num_pages, int page_size,
-                           int max_pages_per_seq, int H, int D, float scale, int causal, attn_stream_t stream);
+                           int max_pages_per_seq, int H, int D, float scale, int causal, uint32_t* tile_counter,
+                           attn_stream_t stream);
 
 /*
  * attn_fwd_splitkv — the same forward with the keys of every (b, h, 128-row
@@ -278,7 +289,7 @@ attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream);
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 7
+#define ATTN_ABI_VERSION 8
 
 #ifdef __cplusplus
 }

@@ -175,12 +175,14 @@ def test_merge_argument_checks(lib, args, code):
     (dict(batch=0), attn.ATTN_OK),
     (dict(tq=0), attn.ATTN_OK),
     (dict(maxq=0), attn.ATTN_OK),
+    (dict(tc=A + 4), attn.ATTN_ERR_ALIGN),
 ])
 def test_varlen_argument_checks(lib, args, code):
-    a = dict(q=A, k=A, v=A, o=A, lse=A, cq=A, ck=A, batch=3, maxq=300, tq=600, tk=700, H=4, D=128, scale=0.1)
+    a = dict(q=A, k=A, v=A, o=A, lse=A, cq=A, ck=A, batch=3, maxq=300, tq=600, tk=700, H=4, D=128, scale=0.1,
+             tc=None)
     a.update(args)
     st = attn.attn_fwd_varlen(a["q"], a["k"], a["v"], a["o"], a["lse"], a["cq"], a["ck"], a["batch"], a["maxq"],
-                              a["tq"], a["tk"], a["H"], a["D"], a["scale"], 0, None)
+                              a["tq"], a["tk"], a["H"], a["D"], a["scale"], 0, a["tc"], None)
     assert st == code
 
 
@@ -198,14 +200,16 @@ def test_varlen_argument_checks(lib, args, code):
     (dict(scale=float("inf")), attn.ATTN_ERR_SCALE),
     (dict(batch=0), attn.ATTN_OK),
     (dict(tq=0), attn.ATTN_OK),
+    (dict(tc=A + 4), attn.ATTN_ERR_ALIGN),
 ])
 def test_paged_argument_checks(lib, args, code):
     # every case ends in a host-side check (no launch, with or without a GPU)
     a = dict(q=A, kc=A, vc=A, o=A, lse=A, cq=A, sk=A, bt=A, batch=3, maxq=300, tq=600, npg=40, ps=128, mp=8, H=4,
-             D=128, scale=0.1)
+             D=128, scale=0.1, tc=None)
     a.update(args)
     st = attn.attn_fwd_paged(a["q"], a["kc"], a["vc"], a["o"], a["lse"], a["cq"], a["sk"], a["bt"], a["batch"],
-                             a["maxq"], a["tq"], a["npg"], a["ps"], a["mp"], a["H"], a["D"], a["scale"], 0, None)
+                             a["maxq"], a["tq"], a["npg"], a["ps"], a["mp"], a["H"], a["D"], a["scale"], 0, a["tc"],
+                             None)
     assert st == code
 
 

@@ -133,3 +133,18 @@ def test_paged_benchmark_workload_equals_varlen_bitwise():
     assert st == attn.ATTN_OK, (st, site)
     assert torch.equal(o_p.view(torch.int16), o_v.view(torch.int16))
     assert torch.equal(l_p, l_v)
+
+
+def test_paged_dynamic_and_static_scheduling_agree_bitwise():
+    from exact_attention_86_gb300 import workloads
+
+    w = workloads.PAGED_WORKLOADS["paged_b32_d128_causal"]
+    q, kc, vc, cu, sk, table = workloads.generate_paged(w)
+    dev = torch.device("cuda:0")
+    args = [t.to(dev) for t in (q, kc, vc, cu, sk, table)]
+    o_s, l_s = attn.forward_paged(*args, w.max_len, causal=w.causal, dynamic=False)
+    o_d, l_d = attn.forward_paged(*args, w.max_len, causal=w.causal, dynamic=True)
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, (st, site)
+    assert torch.equal(o_d.view(torch.int16), o_s.view(torch.int16))
+    assert torch.equal(l_d, l_s)

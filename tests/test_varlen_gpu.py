@@ -82,7 +82,7 @@ def test_varlen_guard_rows_untouched():
     l_view = l_buf[:H * tq].view(H, tq)
     qd, kd, vd, cqd, ckd = (t.to(dev) for t in (q, k, v, cu_q, cu_k))  # keep alive across the async call
     st = attn.attn_fwd_varlen(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o_view.data_ptr(), l_view.data_ptr(),
-                              cqd.data_ptr(), ckd.data_ptr(), 3, 250, tq, tq, H, D, 1 / math.sqrt(D), 1,
+                              cqd.data_ptr(), ckd.data_ptr(), 3, 250, tq, tq, H, D, 1 / math.sqrt(D), 1, None,
                               torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK
     torch.cuda.synchronize()
@@ -150,3 +150,24 @@ def test_varlen_repeated_launches_are_bitwise_identical():
     for i, (o, lse) in enumerate(outs, 1):
         assert torch.equal(o.view(torch.int16), o0.view(torch.int16)), f"launch {i} differs"
         assert torch.equal(lse, l0), f"launch {i} LSE differs"
+
+
+@pytest.mark.parametrize("name", ["varlen_b32_d128_causal", "varlen_b32_d128"])
+def test_varlen_dynamic_and_static_scheduling_agree_bitwise(name):
+    """The claimed (dynamic) and dealt (static) schedules run the same units
+    with the same arithmetic: identical bits; the counter is zero afterwards."""
+    from exact_attention_86_gb300 import workloads
+
+    w = workloads.VARLEN_WORKLOADS[name]
+    q, k, v, cu = workloads.generate_varlen(w)
+    dev = torch.device("cuda:0")
+    qd, kd, vd, cud = q.to(dev), k.to(dev), v.to(dev), cu.to(dev)
+    o_s, l_s = attn.forward_varlen(qd, kd, vd, cud, cud, w.max_len, causal=w.causal, dynamic=False)
+    runs = [attn.forward_varlen(qd, kd, vd, cud, cud, w.max_len, causal=w.causal, dynamic=True) for _ in range(5)]
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, (st, site)
+    for o_d, l_d in runs:
+        assert torch.equal(o_d.view(torch.int16), o_s.view(torch.int16))
+        assert torch.equal(l_d, l_s)
+    counter = attn.tile_counter(dev, torch.cuda.current_stream().cuda_stream)
+    assert counter.tolist() == [0, 0]
