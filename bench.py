@@ -204,6 +204,25 @@ def blas_threads() -> int:
     return os.cpu_count() or 1
 
 
+def max_over_ranks(values, device, world: int):
+    """Element-wise maximum of a list of floats over all ranks (the job's time
+    is its slowest rank's); a no-op for one rank.  torch.distributed carries
+    only these timings, never attention data."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Weak scaling: every rank processes its own copy of the workload, so the
+    job's rate is all ranks' units over the slowest rank's time (units/s)."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 def lookup(name):
     from exact_attention_86_gb300 import workloads
     tables = (workloads.WORKLOADS, workloads.VARLEN_WORKLOADS, workloads.PAGED_WORKLOADS, workloads.FP8_WORKLOADS)
@@ -492,13 +511,10 @@ def main():
         raise attn.AttnError(st, f"timed region (site {site})")
     elapsed_ms = t_all0.elapsed_time(t_all1)
     launch_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([elapsed_ms, launch_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, launch_ms = float(t[0]), float(t[1])
+    elapsed_ms, launch_ms = max_over_ranks([elapsed_ms, launch_ms], dev, world)
     # with an L2 flush between launches the step time is the launch alone
     ms_per_step = launch_ms if flush is not None else elapsed_ms / args.steps
-    value = step_flops * world / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_rate(step_flops, world, ms_per_step) / 1e12
     clocks = sampler.summary(wall0, wall1)
 
     # ------------------------------------------------------------ end to end
@@ -523,10 +539,7 @@ def main():
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    (e2e_ms,) = max_over_ranks([e2e_ms], dev, world)
     h2d = sum(h.numel() * h.element_size() for h, _ in pinned)
     d2h = sum(t.numel() * t.element_size() for t in job.outputs)
 
@@ -580,7 +593,7 @@ def main():
                                    else "static"},
             "roofline": roofline,
             "cpu_baseline": cpu,
-            "e2e": {"value": step_flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "e2e": {"value": whole_job_rate(step_flops, world, e2e_ms) / 1e12, "unit": "TFLOP/s",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
             "clocks": clocks,
             "gpu_launches": args.steps * job.launches_per_step,
