@@ -1,7 +1,9 @@
 """Builds the C-ABI library ``libattn.so`` in-tree with nvcc for sm_103a.
 
 ``python -m exact_attention_86_gb300.build`` (or ``build()``) compiles
-``csrc/attn_fwd.cu`` into ``exact_attention_86_gb300/libattn.so``.  The library
+``csrc/attn_fwd.cu`` (which includes the backward kernels of
+``csrc/attn_bwd.cuh`` and the PTX wrappers of ``csrc/sm103_ptx.cuh``) into
+``exact_attention_86_gb300/libattn.so``.  The library
 links only the CUDA runtime (statically); the driver's tensor-map encoder is
 looked up at run time, so the library also loads on a machine without a GPU.
 """
@@ -15,7 +17,8 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 SOURCES = [os.path.join(PKG, "csrc", "attn_fwd.cu")]
-DEPS = SOURCES + [os.path.join(PKG, "csrc", "sm103_ptx.cuh"), os.path.join(ROOT, "include", "attn.h")]
+DEPS = SOURCES + [os.path.join(PKG, "csrc", "sm103_ptx.cuh"), os.path.join(PKG, "csrc", "attn_bwd.cuh"),
+                  os.path.join(ROOT, "include", "attn.h")]
 LIB = os.path.join(PKG, "libattn.so")
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
               "-Xcompiler", "-fPIC", "-shared"]
