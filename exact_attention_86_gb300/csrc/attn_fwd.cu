@@ -140,7 +140,9 @@ struct Geo {
   // tile's S buffer (P over S) or P buffer (16 bf16 keys or 32 E4M3 keys = 8
   // columns per instruction)
   static __device__ __forceinline__ uint32_t p_col(int kk) {
-    if constexpr (kPInS) return 64u * static_cast<uint32_t>(kk / 2) + 8u * static_cast<uint32_t>(kk % 2);
+    constexpr int per_half = FP8 ? 2 : 4;  // instructions per half's 64 keys
+    if constexpr (kPInS)
+      return 64u * static_cast<uint32_t>(kk / per_half) + 8u * static_cast<uint32_t>(kk % per_half);
     return 8u * static_cast<uint32_t>(kk);
   }
   static constexpr int kOffQ = 4096;                 // after control block and exchange buffers
