@@ -555,6 +555,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                            packed ? u.h : u.q0, packed ? u.q_tok0 : u.h, packed ? 0 : u.b, pol_once);
         ++qcount;
         for (int j = 0; ok && j < u.n; ++j) {
+          // paged: the tile's two 64-key halves are looked up once (both loads
+          // in flight together) and serve both K_j and V_j; a half past the
+          // sequence's keys is copied from one row past the cache: zeros
+          int page_tok[2] = {p.cache_tokens, p.cache_tokens};
+          if (p.block_table != nullptr) {
+            const int key0 = (u.j0 + j) * kBK;
+            int pg[2] = {0, 0};
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int pos = key0 + 64 * hf;
+              if (pos < u.kv) pg[hf] = __ldg(p.block_table + static_cast<size_t>(u.b) * p.max_pages + pos / p.page_size);
+            }
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              const int pos = key0 + 64 * hf;
+              if (pos < u.kv) page_tok[hf] = min(max(pg[hf], 0), p.num_pages - 1) * p.page_size + pos % p.page_size;
+            }
+          }
           for (int sel = 0; sel < 2; ++sel) {  // K_j, then V_j
             const uint32_t slot = ring % G::kSlots;
             const uint32_t ph = (ring / G::kSlots) & 1u;
@@ -574,18 +592,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  packed ? u.k_tok0 + key0 : u.h, packed ? 0 : u.b, pol_keep);
             } else {
               // paged: two 64-key boxes, each inside one page (page_size is a
-              // multiple of 64); a box past the sequence's keys reads zeros
-              for (int hf = 0; hf < 2; ++hf) {
-                const int pos = key0 + 64 * hf;
-                int tok = p.cache_tokens;
-                if (pos < u.kv) {
-                  const int pg = __ldg(p.block_table + static_cast<size_t>(u.b) * p.max_pages + pos / p.page_size);
-                  tok = min(max(pg, 0), p.num_pages - 1) * p.page_size + pos % p.page_size;
-                }
+              // multiple of 64)
+              for (int hf = 0; hf < 2; ++hf)
                 for (int c = 0; c < G::kChunks; ++c)
-                  tma_load_4d_hint(dst + c * G::kChunkBytes + hf * (G::kChunkBytes / 2), m, full, c * 64, u.h, tok,
-                                   0, pol_keep);
-              }
+                  tma_load_4d_hint(dst + c * G::kChunkBytes + hf * (G::kChunkBytes / 2), m, full, c * 64, u.h,
+                                   page_tok[hf], 0, pol_keep);
             }
             ++ring;
           }
