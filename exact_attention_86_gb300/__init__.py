@@ -1,4 +1,4 @@
-"""GB300-native exact fused attention forward (sm_103a).
+"""GB300-native exact fused attention, forward and backward (sm_103a).
 
 The compute path is the C-ABI library ``libattn.so`` built from ``csrc/``;
 ``exact_attention_86_gb300.attn`` is its thin Python binding.  Importing the

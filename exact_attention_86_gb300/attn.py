@@ -1,11 +1,14 @@
 """Python binding of the C-ABI attention library (argument marshalling only).
 
-The functions with the C names (``attn_fwd``, ``attn_get_error_string``,
-``attn_check_device_status``, ``attn_selftest_wait_timeout``,
-``attn_abi_version``) take raw device addresses and sizes exactly like
-``include/attn.h``.  ``forward`` is the torch-facing convenience: it checks
-dtypes / devices / contiguity, allocates ``o`` and ``lse`` with torch, and calls
-``attn_fwd`` on the current CUDA stream.  Every step of the computation runs in
+The functions with the C names (``attn_fwd``, ``attn_fwd_varlen``,
+``attn_fwd_paged``, ``attn_fwd_fp8``, ``attn_fwd_splitkv``,
+``attn_fwd_splitkv_noalloc``, ``attn_lse_merge``, ``attn_bwd``, the status and
+self-test calls) take raw device addresses and sizes exactly like
+``include/attn.h``.  ``forward``, ``forward_varlen``, ``forward_paged``,
+``forward_fp8``, ``forward_splitkv``, ``lse_merge`` and ``backward`` are the
+torch-facing conveniences: they check dtypes / devices / contiguity, allocate
+the outputs (and any workspace) with torch, and call the library on the
+current CUDA stream.  Every step of the computation runs in
 the library's CUDA kernel; there is no CPU fallback, and a missing library is
 an error.
 """
