@@ -872,6 +872,7 @@ attn_status run_backward(DeviceInfo& dev, const void* q, const void* k, const vo
   f.Sq = Sq;
   f.Sk = Sk;
   f.n_qtiles = (Sq + kBQ - 1) / kBQ;
+  f.head_group = head_group_for(B * H, Sk, D, 2);
   f.num_splits = 1;
   f.total_units = static_cast<int>(static_cast<int64_t>(B) * H * f.n_qtiles);
   f.o_part = nullptr;

@@ -177,6 +177,7 @@ struct Params {
   const int32_t* kv_lens;
   int B, H, Sq, Sk;
   int n_qtiles;
+  int head_group;          // causal order: heads per group (their K/V fit in a share of L2)
   int num_splits;          // key ranges per (b, h, query tile); 1 = whole rows
   int total_units;
   float* o_part;           // split mode: fp32 [num_splits][B*H*Sq][D] normalised partial outputs
@@ -223,9 +224,17 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int t_in) {
   const int t = t_in / p.num_splits;
   const int bh_count = p.B * p.H;
   int qt, bh;
-  if (CAUSAL) {  // longest units first: query blocks from the end of the sequence
-    qt = p.n_qtiles - 1 - t / bh_count;
-    bh = t % bh_count;
+  if (CAUSAL) {
+    // Heads in groups whose K/V fit in a share of L2, one group after the
+    // other; within a group the longest units first (query blocks from the
+    // end of the sequence), the group's heads fastest.  The CTAs working at
+    // the same time then read the K/V of one group only.
+    const int units_per_group = p.head_group * p.n_qtiles;
+    const int grp = t / units_per_group;
+    const int w = t - grp * units_per_group;
+    const int heads = min(p.head_group, bh_count - grp * p.head_group);
+    qt = p.n_qtiles - 1 - w / heads;
+    bh = grp * p.head_group + w % heads;
   } else {       // consecutive units share a head, so its K/V stay hot in L2
     qt = t % p.n_qtiles;
     bh = t / p.n_qtiles;
@@ -1119,6 +1128,16 @@ bool make_map_packed(CUtensorMap* m, const void* ptr, int H, int total, int D, i
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Heads per causal group: as many as keep their K and V within 48 MB of L2
+// (K/V bytes of one head = 2 * keys * D * element size).
+int head_group_for(int bh_count, int keys, int D, int elem_bytes) {
+  const uint64_t per_head = 2ull * static_cast<uint64_t>(keys > 0 ? keys : 1) * D * elem_bytes;
+  uint64_t g = (48ull << 20) / per_head;
+  if (g < 1) g = 1;
+  if (g > static_cast<uint64_t>(bh_count > 0 ? bh_count : 1)) g = bh_count > 0 ? bh_count : 1;
+  return static_cast<int>(g);
+}
+
 void clear_paged(Params& p) {
   p.block_table = nullptr;
   p.seqlens_k = nullptr;
@@ -1262,6 +1281,7 @@ Params packed_params(void* o, float* lse, const int32_t* cu_q, int batch, int ma
   p.Sq = max_seqlen_q;
   p.Sk = 0;
   p.n_qtiles = static_cast<int>((static_cast<int64_t>(max_seqlen_q) + kBQ - 1) / kBQ);
+  p.head_group = head_group_for(batch * H, max_seqlen_q, D, 2);  // sequence lengths are not known here
   p.num_splits = 1;
   p.total_units = static_cast<int>(static_cast<int64_t>(batch) * H * p.n_qtiles);  // checked by the caller
   p.o_part = nullptr;
@@ -1307,6 +1327,7 @@ attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const voi
   p.Sq = Sq;
   p.Sk = Sk;
   p.n_qtiles = static_cast<int>(n_qtiles);
+  p.head_group = head_group_for(B * H, Sk, D, 2);
   p.num_splits = num_splits;
   p.total_units = static_cast<int>(static_cast<uint64_t>(B) * H * n_qtiles * num_splits);
   p.o_part = o_part;
@@ -1385,6 +1406,7 @@ attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o,
   p.Sq = Sq;
   p.Sk = Sk;
   p.n_qtiles = static_cast<int>(n_qtiles);
+  p.head_group = head_group_for(B * H, Sk, D, 1);
   p.num_splits = 1;
   p.total_units = static_cast<int>(static_cast<uint64_t>(B) * H * n_qtiles);
   p.o_part = nullptr;
