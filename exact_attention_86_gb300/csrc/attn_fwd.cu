@@ -1509,6 +1509,9 @@ attn_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cac
   p.num_pages = num_pages;
   p.cache_tokens = static_cast<int>(cache_tokens);
   p.sched = causal ? nullptr : tile_counter;  // as attn_fwd_varlen
+  // causal paged batches keep the longest-first order over all heads: the
+  // head groups that help the packed batch (+9 %) cost this one 5 % (measured)
+  p.head_group = batch * H;
   return launch_any(*dev, D, causal != 0, mq, mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
 }
 
