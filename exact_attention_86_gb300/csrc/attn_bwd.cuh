@@ -14,8 +14,9 @@
 //                     the tensor cores, P and dS in the elementwise warps,
 //                     dQ accumulated in TMEM over the key tiles;
 //   bwd_dkdv_kernel   one unit = 128 keys of one (b, h): S^T = K Q^T and
-//                     dP^T = V dO^T, P^T and dS^T, then dV and dK accumulated
-//                     in TMEM over the query tiles.
+//                     dP^T = V dO^T for 64 queries at a time (two steps in
+//                     flight), P^T and dS^T, then dV and dK accumulated in
+//                     TMEM over the query steps.
 // Both main kernels use only the operand forms of the forward: A and B
 // K-major from shared memory (S, dP, S^T, dP^T) and A from TMEM with B
 // MN-major from shared memory (dQ, dV, dK, like the forward's P V).
@@ -412,25 +413,50 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // --------------------------------------------------------------- dK, dV
+// A unit is 128 keys of one (b, h); the query rows stream past it in steps of
+// 64, so that the two products of a step (S^T, dP^T: 64 columns each) fit
+// twice in Tensor Memory beside the dV and dK accumulators, and the tensor
+// cores compute the next step's products while the elementwise warps turn the
+// current ones into P^T and dS^T.
+constexpr int kBQKv = 64;  // query rows per step
+
 template <int D>
 struct GeoKv {
-  static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kChunkBytes = 128 * 128;
+  static constexpr int kTileK = 128 * D * 2;     // K or V: 128 keys
+  static constexpr int kTileQ = kBQKv * D * 2;   // Q_i or dO_i: 64 queries
+  static constexpr int kChunkK = 128 * 128;      // one 128-B swizzle column of a K/V tile
+  static constexpr int kChunkQ = kBQKv * 128;    // one 128-B swizzle column of a Q/dO tile
   static constexpr int kChunks = D / 64;
-  static constexpr int kSlots = (D == 128) ? 2 : 4;   // ring of (Q_i, dO_i) pairs
-  static constexpr int kOffStat = 1024;               // LSE*log2e and Delta, two tiles each (2 KB)
-  static constexpr int kOffK = 4096;
-  static constexpr int kOffV = kOffK + kTileBytes;
-  static constexpr int kOffRing = kOffV + kTileBytes;
-  static constexpr int kSmemBytes = kOffRing + kSlots * 2 * kTileBytes + 1024;
-  static constexpr uint32_t kTmemSt = 0, kTmemDpt = 128, kTmemDv = 256, kTmemDk = 256 + D;
+  static constexpr int kSlots = (D == 128) ? 4 : 8;  // ring of (Q_i, dO_i) pairs
+  static constexpr int kOffStat = 1024;  // per warp and step parity: LSE*log2e[32], Delta[32] (4 KB)
+  static constexpr int kOffK = 5120;
+  static constexpr int kOffV = kOffK + kTileK;
+  static constexpr int kOffRing = kOffV + kTileK;
+  static constexpr int kSmemBytes = kOffRing + kSlots * 2 * kTileQ + 1024;
+  // TMEM: step parity b holds S^T at [128 b, 128 b + 64) and dP^T at
+  // [128 b + 64, 128 b + 128).  Each half of the elementwise warps reads its 32
+  // columns of both and writes P^T and dS^T (bf16 pairs) over the first 16 of
+  // them, so no half writes where the other reads.  dV at 256, dK at 256 + D.
+  static constexpr uint32_t kTmemDv = 256, kTmemDk = 256 + D;
+  static __device__ __forceinline__ uint32_t st_col(uint32_t b) { return 128u * b; }
+  // column of the A operand (P^T or dS^T) of the kk-th product instruction
+  // (16 queries = 8 columns), relative to st_col: 2 instructions per half
+  static __device__ __forceinline__ uint32_t a_col(int kk) {
+    return 32u * static_cast<uint32_t>(kk >> 1) + 8u * static_cast<uint32_t>(kk & 1);
+  }
 };
+static_assert(GeoKv<128>::kSmemBytes <= 232448 && GeoKv<64>::kSmemBytes <= 232448, "shared memory");
+static_assert(8 * 2 * 64 * 4 <= GeoKv<128>::kOffK - GeoKv<128>::kOffStat, "staging area");
 
 struct CtrlKv {
   uint64_t kv_full, kv_empty;
-  uint64_t qd_full[4], qd_empty[4];
-  uint64_t st_full, pd_full, pd_free, out_full;
-  uint64_t drain;
+  uint64_t qd_full[8], qd_empty[8];
+  uint64_t st_full[2];  // S^T and dP^T of the step complete
+  uint64_t pd_full[2];  // P^T and dS^T written (8 warp arrivals)
+  uint64_t s_free[2];   // the dV product of the step completed (its S^T columns are free)
+  uint64_t d_free[2];   // the dK product completed (dP^T columns and the ring slot are free)
+  uint64_t out_full;
+  uint64_t drain[2];  // one per issuing warp
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -439,7 +465,7 @@ static_assert(sizeof(CtrlKv) <= 1024, "control block");
 struct KvUnit {
   int b, h, key0, rows_k;  // rows_k: keys of the tile that exist (< Sk)
   int kv;                  // valid keys of the batch entry
-  int i0, n;               // first query tile and number of query tiles (0: no gradient)
+  int i0, n;               // first query step and number of steps (0: no gradient)
 };
 
 template <bool CAUSAL>
@@ -462,8 +488,8 @@ __device__ __forceinline__ KvUnit decode_kv_unit(const BwdParams& bp, int t) {
   int kv = p.Sk;
   if (p.kv_lens != nullptr) kv = min(max(__ldg(p.kv_lens + u.b), 0), p.Sk);
   u.kv = kv;
-  u.i0 = CAUSAL ? u.key0 / kBQ : 0;  // query rows below key0 see none of these keys
-  u.n = (u.key0 < kv && u.rows_k > 0) ? max(p.n_qtiles - u.i0, 0) : 0;
+  u.i0 = CAUSAL ? u.key0 / kBQKv : 0;  // query rows below key0 see none of these keys
+  u.n = (u.key0 < kv && u.rows_k > 0) ? max(p.n_qtiles - u.i0, 0) : 0;  // n_qtiles counts 64-row steps here
   return u;
 }
 
@@ -479,14 +505,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
   CtrlKv& ctl = *reinterpret_cast<CtrlKv*>(base_ptr);
-  float* stat = reinterpret_cast<float*>(base_ptr + G::kOffStat);  // [2 tiles][LSE*log2e 128 | Delta 128]
   volatile int* abort_flag = &ctl.abort_flag;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t bar_kv_full = smem_addr(&ctl.kv_full), bar_kv_empty = smem_addr(&ctl.kv_empty);
   const uint32_t bar_qd_full0 = smem_addr(&ctl.qd_full[0]), bar_qd_empty0 = smem_addr(&ctl.qd_empty[0]);
-  const uint32_t bar_st_full = smem_addr(&ctl.st_full), bar_pd_full = smem_addr(&ctl.pd_full);
-  const uint32_t bar_pd_free = smem_addr(&ctl.pd_free), bar_out_full = smem_addr(&ctl.out_full);
+  const uint32_t bar_st_full0 = smem_addr(&ctl.st_full[0]), bar_pd_full0 = smem_addr(&ctl.pd_full[0]);
+  const uint32_t bar_s_free0 = smem_addr(&ctl.s_free[0]), bar_d_free0 = smem_addr(&ctl.d_free[0]);
+  const uint32_t bar_out_full = smem_addr(&ctl.out_full);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv_full, 1);
@@ -495,11 +521,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_qd_full0 + 8 * s, 1);
       mbar_init(bar_qd_empty0 + 8 * s, 1);
     }
-    mbar_init(bar_st_full, 1);
-    mbar_init(bar_pd_full, kSoftmaxWarps);
-    mbar_init(bar_pd_free, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_st_full0 + 8 * b, 1);
+      mbar_init(bar_pd_full0 + 8 * b, kSoftmaxWarps);
+      mbar_init(bar_s_free0 + 8 * b, 1);
+      mbar_init(bar_d_free0 + 8 * b, 1);
+    }
     mbar_init(bar_out_full, 1);
-    mbar_init(smem_addr(&ctl.drain), 1);
+    mbar_init(smem_addr(&ctl.drain[0]), 1);
+    mbar_init(smem_addr(&ctl.drain[1]), 1);
     ctl.abort_flag = 0;
     fence_barrier_init();
   }
@@ -536,11 +566,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const KvUnit u = decode_kv_unit<CAUSAL>(bp, unit);
           if (u.n == 0) continue;
           if (!wait_phase(bar_kv_empty, (ucount & 1u) ^ 1u, abort_flag, kSiteBwdKvEmpty, limit)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar_kv_full, 2 * G::kTileBytes);
+          mbar_arrive_expect_tx(bar_kv_full, 2 * G::kTileK);
           for (int c = 0; c < G::kChunks; ++c) {
-            tma_load_4d_hint(base + G::kOffK + c * G::kChunkBytes, &map_k, bar_kv_full, c * 64, u.key0, u.h, u.b,
+            tma_load_4d_hint(base + G::kOffK + c * G::kChunkK, &map_k, bar_kv_full, c * 64, u.key0, u.h, u.b,
                              pol_once);
-            tma_load_4d_hint(base + G::kOffV + c * G::kChunkBytes, &map_v, bar_kv_full, c * 64, u.key0, u.h, u.b,
+            tma_load_4d_hint(base + G::kOffV + c * G::kChunkK, &map_v, bar_kv_full, c * 64, u.key0, u.h, u.b,
                              pol_once);
           }
           ++ucount;
@@ -552,13 +582,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             const uint32_t full = bar_qd_full0 + 8 * slot;
-            mbar_arrive_expect_tx(full, 2 * G::kTileBytes);
-            const uint32_t dst = base + G::kOffRing + slot * 2 * G::kTileBytes;
-            const int q0 = (u.i0 + i) * kBQ;
+            mbar_arrive_expect_tx(full, 2 * G::kTileQ);
+            const uint32_t dst = base + G::kOffRing + slot * 2 * G::kTileQ;
+            const int q0 = (u.i0 + i) * kBQKv;
             for (int c = 0; c < G::kChunks; ++c) {
-              tma_load_4d_hint(dst + c * G::kChunkBytes, &map_q, full, c * 64, q0, u.h, u.b, pol_keep);
-              tma_load_4d_hint(dst + G::kTileBytes + c * G::kChunkBytes, &map_do, full, c * 64, q0, u.h, u.b,
-                               pol_keep);
+              tma_load_4d_hint(dst + c * G::kChunkQ, &map_q, full, c * 64, q0, u.h, u.b, pol_keep);
+              tma_load_4d_hint(dst + G::kTileQ + c * G::kChunkQ, &map_do, full, c * 64, q0, u.h, u.b, pol_keep);
             }
             ++ring;
           }
@@ -578,14 +607,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     } else if (warp == kWarpQK) {
-      // ---------------------------------------------------------- issuer
-      // Per query tile: S^T = K Q_i^T and dP^T = V dO_i^T; once the
-      // elementwise warps have written P^T over S^T and dS^T over dP^T:
-      // dV += P^T dO_i and dK += dS^T Q_i.  The next S^T waits for those.
-      const uint32_t idesc_s = idesc_bf16_f32(kBK, kBQ, false, false);
-      const uint32_t idesc_o = idesc_bf16_f32(kBK, D, false, true);
+      // ------------------------------------------------- S^T, dP^T issuer
+      // Per step t: S^T_t once the dV product of step t-2 has released its
+      // columns, dP^T_t once the dK product of t-2 has, one commit for both.
+      // The products have their own issuing warp, so this one runs ahead
+      // while they wait for the elementwise warps.
+      const uint32_t idesc_s = idesc_bf16_f32(kBK, kBQKv, false, false);
       const uint32_t ka = base + G::kOffK, va = base + G::kOffV;
-      uint32_t ring = 0, ucount = 0, tcount = 0;
+      uint32_t tcount = 0, ucount = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
         const int unit = unit_at<CAUSAL>(t);
@@ -596,69 +625,117 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++ucount;
         for (int i = 0; i < u.n; ++i) {
           const uint32_t tt = tcount + i;
-          const uint32_t slot = ring % G::kSlots;
-          if (!wait_warp(bar_qd_full0 + 8 * slot, (ring / G::kSlots) & 1u, abort_flag, kSiteBwdQFull, limit)) {
+          const uint32_t b = tt & 1u;
+          const uint32_t slot = tt % G::kSlots;
+          if (!wait_warp(bar_qd_full0 + 8 * slot, (tt / G::kSlots) & 1u, abort_flag, kSiteBwdQFull, limit)) {
             ok = false;
             break;
           }
-          if (tt >= 1 && !wait_warp(bar_pd_free, (tt - 1) & 1u, abort_flag, kSiteBwdDsFree, limit)) { ok = false; break; }
+          const uint32_t prev_use = ((tt >> 1) - 1) & 1u;  // parity of step tt-2's release
+          if (tt >= 2 && !wait_warp(bar_s_free0 + 8 * b, prev_use, abort_flag, kSiteBwdSFree, limit)) {
+            ok = false;
+            break;
+          }
           tc_fence_after_sync();
-          const uint32_t qa = base + G::kOffRing + slot * 2 * G::kTileBytes;
-          const uint32_t da = qa + G::kTileBytes;
+          const uint32_t qa = base + G::kOffRing + slot * 2 * G::kTileQ;
+          const uint32_t da = qa + G::kTileQ;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-            mma_ss_elect(tmem + G::kTmemSt, sdesc_sw128(ka + off, 16, 1024), sdesc_sw128(qa + off, 16, 1024),
+            const uint32_t off_k = (kk >> 2) * G::kChunkK + (kk & 3) * 32;
+            const uint32_t off_q = (kk >> 2) * G::kChunkQ + (kk & 3) * 32;
+            mma_ss_elect(tmem + G::st_col(b), sdesc_sw128(ka + off_k, 16, 1024), sdesc_sw128(qa + off_q, 16, 1024),
                          idesc_s, kk > 0 ? 1u : 0u);
           }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-            mma_ss_elect(tmem + G::kTmemDpt, sdesc_sw128(va + off, 16, 1024), sdesc_sw128(da + off, 16, 1024),
-                         idesc_s, kk > 0 ? 1u : 0u);
+          if (tt >= 2 && !wait_warp(bar_d_free0 + 8 * b, prev_use, abort_flag, kSiteBwdDsFree, limit)) {
+            ok = false;
+            break;
           }
-          mma_commit_elect(bar_st_full);
-          if (!wait_warp(bar_pd_full, tt & 1u, abort_flag, kSiteBwdDsFull, limit)) { ok = false; break; }
           tc_fence_after_sync();
 #pragma unroll
-          for (int kk = 0; kk < kBQ / 16; ++kk) {
-            const uint32_t acc = (i == 0 && kk == 0) ? 0u : 1u;
-            mma_ts_elect(tmem + G::kTmemDv, tmem + G::kTmemSt + kk * 8,
-                         sdesc_sw128(da + kk * 16 * 128, G::kChunkBytes, 1024), idesc_o, acc);
-            mma_ts_elect(tmem + G::kTmemDk, tmem + G::kTmemDpt + kk * 8,
-                         sdesc_sw128(qa + kk * 16 * 128, G::kChunkBytes, 1024), idesc_o, acc);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off_k = (kk >> 2) * G::kChunkK + (kk & 3) * 32;
+            const uint32_t off_q = (kk >> 2) * G::kChunkQ + (kk & 3) * 32;
+            mma_ss_elect(tmem + G::st_col(b) + 64, sdesc_sw128(va + off_k, 16, 1024),
+                         sdesc_sw128(da + off_q, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
           }
+          mma_commit_elect(bar_st_full0 + 8 * b);
+        }
+        if (!ok) break;
+        tcount += u.n;
+      }
+      // every MMA of this warp has completed before TMEM is released
+      const uint32_t bar_d = smem_addr(&ctl.drain[0]);
+      mma_commit_elect(bar_d);
+      wait_phase_drain(bar_d, 0);
+    } else if (warp == kWarpPV) {
+      // ------------------------------------------------ dV, dK issuer
+      // Per step t, once the elementwise warps have written P^T and dS^T:
+      // dV += P^T dO_t (its commit releases the S^T columns), dK += dS^T Q_t
+      // (releases the dP^T columns and the ring slot).  After a unit's last
+      // step: the accumulators are complete, and K/V may be replaced (the
+      // S^T and dP^T products that read them completed before the elementwise
+      // warps could finish that step).
+      const uint32_t idesc_o = idesc_bf16_f32(kBK, D, false, true);
+      uint32_t tcount = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
+        const int unit = unit_at<CAUSAL>(t);
+        if (unit >= p.total_units) continue;
+        const KvUnit u = decode_kv_unit<CAUSAL>(bp, unit);
+        if (u.n == 0) continue;
+        for (int i = 0; i < u.n; ++i) {
+          const uint32_t tt = tcount + i;
+          const uint32_t b = tt & 1u;
+          const uint32_t slot = tt % G::kSlots;
+          if (!wait_warp(bar_pd_full0 + 8 * b, (tt >> 1) & 1u, abort_flag, kSiteBwdDsFull, limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t qa = base + G::kOffRing + slot * 2 * G::kTileQ;
+          const uint32_t da = qa + G::kTileQ;
+#pragma unroll
+          for (int kk = 0; kk < kBQKv / 16; ++kk)
+            mma_ts_elect(tmem + G::kTmemDv, tmem + G::st_col(b) + G::a_col(kk),
+                         sdesc_sw128(da + kk * 16 * 128, G::kChunkQ, 1024), idesc_o, (i == 0 && kk == 0) ? 0u : 1u);
+          mma_commit_elect(bar_s_free0 + 8 * b);
+#pragma unroll
+          for (int kk = 0; kk < kBQKv / 16; ++kk)
+            mma_ts_elect(tmem + G::kTmemDk, tmem + G::st_col(b) + 64 + G::a_col(kk),
+                         sdesc_sw128(qa + kk * 16 * 128, G::kChunkQ, 1024), idesc_o, (i == 0 && kk == 0) ? 0u : 1u);
+          mma_commit_elect(bar_d_free0 + 8 * b);
           mma_commit_elect(bar_qd_empty0 + 8 * slot);
-          mma_commit_elect(bar_pd_free);
-          ++ring;
         }
         if (!ok) break;
         mma_commit_elect(bar_out_full);
         mma_commit_elect(bar_kv_empty);
         tcount += u.n;
       }
-      if (!ok) {
-        const uint32_t bar_d = smem_addr(&ctl.drain);
-        mma_commit_elect(bar_d);
-        wait_phase_drain(bar_d, 0);
+      // every product has completed (and its commits have landed) before
+      // TMEM is released and the CTA exits
+      const uint32_t bar_d = smem_addr(&ctl.drain[1]);
+      mma_commit_elect(bar_d);
+      wait_phase_drain(bar_d, 0);
+      if (ok) {
+        for (uint32_t back = 1; back <= 2 && back <= tcount; ++back) {
+          const uint32_t t = tcount - back;
+          wait_phase_drain(bar_s_free0 + 8 * (t & 1u), (t >> 1) & 1u);
+          wait_phase_drain(bar_d_free0 + 8 * (t & 1u), (t >> 1) & 1u);
+        }
       }
     }
   } else {
     regs_increase<kRegsSoftmax>();
     // ------------------------------------------------------- elementwise
-    // Two threads per key row: warps 0-3 own query columns 0-63 of each tile
-    // and dK/dV columns [0, D/2), warps 4-7 the rest.  P^T is written over the
-    // S^T columns and dS^T over the dP^T columns, so the eight warps meet at a
-    // named barrier between reading and writing.  A failed wait only marks the
-    // warp, every warp executes every named barrier, and every decision to
-    // leave is the OR of the abort flag reduced by the barrier itself, so all
-    // eight take it together.
+    // Two threads per key row: warps 0-3 own query columns 0-31 of each step
+    // and dK/dV columns [0, D/2), warps 4-7 the rest.  The warps never wait
+    // for one another: each reads and writes only its own TMEM columns and
+    // stages its own LSE and Delta values, so a failed wait lets a warp leave
+    // on its own.
     const int half = warp >> 2;
     const int r = threadIdx.x & (kBK - 1);
-    const int tid = threadIdx.x;  // 0..255
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    constexpr uint32_t kBarEw = 1;
-    constexpr uint32_t kEwThreads = kSoftmaxWarps * 32;
+    float* stage = reinterpret_cast<float*>(base_ptr + G::kOffStat) + warp * 2 * 64;
     uint32_t tcount = 0, ucount = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
@@ -682,86 +759,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const size_t head_row0 = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq);
-      bool failed = false;
+      // LSE (base 2) and Delta of this half's 32 queries of a step, one per
+      // lane, fetched a step ahead; a query past Sq or without a valid key
+      // gets LSE = +inf, so its P is 0
+      float lse_raw = -INFINITY, del_raw = 0.0f;
+      auto fetch = [&](int step) {
+        const int q = (u.i0 + step) * kBQKv + 32 * half + lane;
+        lse_raw = -INFINITY;
+        del_raw = 0.0f;
+        if (q < p.Sq) {
+          lse_raw = __ldg(bp.lse + head_row0 + q);
+          del_raw = __ldg(bp.delta + head_row0 + q);
+        }
+      };
+      fetch(0);
       for (int i = 0; i < u.n; ++i) {
         const uint32_t tt = tcount + i;
-        const int q0 = (u.i0 + i) * kBQ;
-        // LSE (base 2) and Delta of the tile's 128 queries, shared through
-        // shared memory by tile parity; a query past Sq or without a valid
-        // key gets LSE = +inf, so its P is 0
-        float* st = stat + (tt & 1u) * 2 * kBQ;
-        {
-          const int c = tid & (kBQ - 1);
-          const int q = q0 + c;
-          if (tid < kBQ) {
-            float v = INFINITY;
-            if (q < p.Sq) {
-              const float l = __ldg(bp.lse + head_row0 + q);
-              if (l != -INFINITY) v = l * kLog2e;
-            }
-            st[c] = v;
-          } else {
-            st[kBQ + c] = (q < p.Sq) ? __ldg(bp.delta + head_row0 + q) : 0.0f;
-          }
-        }
-        if (named_bar_red_or(kBarEw, kEwThreads, *abort_flag != 0)) { ok = false; break; }
-        // query column c of this half is q0 + 64*half + c; key <= query for causal
+        const uint32_t b = tt & 1u;
+        const int q0 = (u.i0 + i) * kBQKv;
+        // into the warp's staging slot of this step's parity
+        stage[b * 64 + lane] = (lse_raw == -INFINITY) ? INFINITY : lse_raw * kLog2e;
+        stage[b * 64 + 32 + lane] = del_raw;
+        __syncwarp();
+        if (i + 1 < u.n) fetch(i + 1);
+        // query column c of this half is q0 + 32*half + c; key <= query for causal
         const bool masked = !key_ok || (CAUSAL && q0 < u.key0 + kBK - 1);
-        const int cstart = key_ok ? (CAUSAL ? key - q0 - 64 * half : 0) : 64;  // first valid column
-        uint32_t s[2][32], dp[2][32];
-        if (!failed && !wait_warp(bar_st_full, tt & 1u, abort_flag, kSiteBwdSFull, limit)) failed = true;
-        if (!failed) {
-          tc_fence_after_sync();
-          const uint32_t tS = tmem + lane_off + G::kTmemSt + 64u * half;
-          const uint32_t tD = tmem + lane_off + G::kTmemDpt + 64u * half;
-          tmem_ld_32x32b_x32(tS, s[0]);
-          tmem_ld_32x32b_x32(tS + 32, s[1]);
-          tmem_ld_32x32b_x32(tD, dp[0]);
-          tmem_ld_32x32b_x32(tD + 32, dp[1]);
-          tmem_ld_wait_x32(s[0]);
-          tmem_ld_wait_x32(s[1]);
-          tmem_ld_wait_x32(dp[0]);
-          tmem_ld_wait_x32(dp[1]);
-        }
-        uint32_t pk[32], dk_pk[32];
-        if (!failed) {
-          const float* lse_c = st + 64 * half;
-          const float* del_c = st + kBQ + 64 * half;
+        const int cstart = key_ok ? (CAUSAL ? key - q0 - 32 * half : 0) : 32;  // first valid column
+        if (!wait_warp(bar_st_full0 + 8 * b, (tt >> 1) & 1u, abort_flag, kSiteBwdSFull, limit)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t tS = tmem + lane_off + G::st_col(b) + 32u * half;
+        const uint32_t tD = tS + 64u;
+        uint32_t s[32], dp[32];
+        tmem_ld_32x32b_x32(tS, s);
+        tmem_ld_32x32b_x32(tD, dp);
+        tmem_ld_wait_x32(s);
+        tmem_ld_wait_x32(dp);
+        const float* lse_c = stage + b * 64;
+        const float* del_c = lse_c + 32;
+        uint32_t pk[16], ds_pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            float s0, s1, d0, d1;
-            pair_at(s, e, s0, s1);
-            pair_at(dp, e, d0, d1);
-            float p0 = ex2_approx(fmaf(s0, bp.c2, -lse_c[2 * e]));
-            float p1 = ex2_approx(fmaf(s1, bp.c2, -lse_c[2 * e + 1]));
-            if (masked) {
-              p0 = (2 * e >= cstart) ? p0 : 0.0f;
-              p1 = (2 * e + 1 >= cstart) ? p1 : 0.0f;
-            }
-            pk[e] = pack_bf16x2(p0, p1);
-            dk_pk[e] = pack_bf16x2(p0 * (d0 - del_c[2 * e]), p1 * (d1 - del_c[2 * e + 1]));
+        for (int e = 0; e < 16; ++e) {
+          const float s0 = __uint_as_float(s[2 * e]), s1 = __uint_as_float(s[2 * e + 1]);
+          const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
+          float p0 = ex2_approx(fmaf(s0, bp.c2, -lse_c[2 * e]));
+          float p1 = ex2_approx(fmaf(s1, bp.c2, -lse_c[2 * e + 1]));
+          if (masked) {
+            p0 = (2 * e >= cstart) ? p0 : 0.0f;
+            p1 = (2 * e + 1 >= cstart) ? p1 : 0.0f;
           }
+          pk[e] = pack_bf16x2(p0, p1);
+          ds_pk[e] = pack_bf16x2(p0 * (d0 - del_c[2 * e]), p1 * (d1 - del_c[2 * e + 1]));
         }
-        // every half has read its S^T and dP^T columns before any is overwritten
-        tc_fence_before_sync();
-        if (named_bar_red_or(kBarEw, kEwThreads, *abort_flag != 0)) { ok = false; break; }
-        if (!failed) {
-          tc_fence_after_sync();
-          const uint32_t tP = tmem + lane_off + G::kTmemSt + 32u * half;
-          const uint32_t tQ = tmem + lane_off + G::kTmemDpt + 32u * half;
-          tmem_st_32x32b_x16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
-          tmem_st_32x32b_x16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
-          tmem_st_32x32b_x16(tQ, *reinterpret_cast<const uint32_t(*)[16]>(&dk_pk[0]));
-          tmem_st_32x32b_x16(tQ + 16, *reinterpret_cast<const uint32_t(*)[16]>(&dk_pk[16]));
-          tmem_st_wait();
-          warp_arrive_after_tc(bar_pd_full, lane);
-        }
+        tmem_st_32x32b_x16(tS, pk);
+        tmem_st_32x32b_x16(tD, ds_pk);
+        tmem_st_wait();
+        warp_arrive_after_tc(bar_pd_full0 + 8 * b, lane);
       }
       if (!ok) break;
       tcount += u.n;
-      if (!failed && !wait_warp(bar_out_full, ucount & 1u, abort_flag, kSiteBwdOutFull, limit)) failed = true;
+      if (!wait_warp(bar_out_full, ucount & 1u, abort_flag, kSiteBwdOutFull, limit)) { ok = false; break; }
       ++ucount;
-      if (named_bar_red_or(kBarEw, kEwThreads, *abort_flag != 0 || failed)) { ok = false; break; }
       tc_fence_after_sync();
 #pragma unroll
       for (int which = 0; which < 2; ++which) {  // dV, then dK (times scale)
@@ -785,11 +842,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // the next unit's first dV/dK product overwrites the accumulators only
-      // after every elementwise warp has arrived on pd_full for it
+      // after every elementwise warp has arrived on pd_full for it, which
+      // comes after this
       tc_fence_before_sync();
     }
-    // the last pd_free arrival lands asynchronously: wait before exiting
-    if (tcount > 0) wait_phase_drain(bar_pd_free, (tcount - 1) & 1u);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -806,8 +862,8 @@ size_t bwd_delta_bytes(int B, int H, int Sq) {
 
 template <int D, bool CAUSAL>
 attn_status launch_bwd(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CUtensorMap& mdo,
-                       const CUtensorMap& mk, const CUtensorMap& mv, const BwdParams& bq, const BwdParams& bk,
-                       cudaStream_t stream) {
+                       const CUtensorMap& mq64, const CUtensorMap& mdo64, const CUtensorMap& mk,
+                       const CUtensorMap& mv, const BwdParams& bq, const BwdParams& bk, cudaStream_t stream) {
   auto kq = bwd_dq_kernel<D, CAUSAL>;
   auto kk = bwd_dkdv_kernel<D, CAUSAL>;
   constexpr int smem_q = GeoDq<D>::kSmemBytes;
@@ -825,7 +881,7 @@ attn_status launch_bwd(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CU
   }
   if (bk.f.total_units > 0) {
     const int grid = bk.f.total_units < dev.num_sms ? bk.f.total_units : dev.num_sms;
-    kk<<<grid, kThreads, smem_k, stream>>>(mq, mdo, mk, mv, bk);
+    kk<<<grid, kThreads, smem_k, stream>>>(mq64, mdo64, mk, mv, bk);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   }
   return ATTN_OK;
@@ -858,9 +914,10 @@ attn_status run_backward(DeviceInfo& dev, const void* q, const void* k, const vo
                                                                     static_cast<const uint16_t*>(dout), delta, rows);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
 
-  CUtensorMap mq, mdo, mk, mv;
-  if (!make_map(&mq, q, B, H, Sq, D) || !make_map(&mdo, dout, B, H, Sq, D) || !make_map(&mk, k, B, H, Sk, D) ||
-      !make_map(&mv, v, B, H, Sk, D))
+  CUtensorMap mq, mdo, mq64, mdo64, mk, mv;
+  if (!make_map(&mq, q, B, H, Sq, D) || !make_map(&mdo, dout, B, H, Sq, D) ||
+      !make_map(&mq64, q, B, H, Sq, D, kBQKv) || !make_map(&mdo64, dout, B, H, Sq, D, kBQKv) ||
+      !make_map(&mk, k, B, H, Sk, D) || !make_map(&mv, v, B, H, Sk, D))
     return ATTN_ERR_CUDA;
   BwdParams bq;
   Params& f = bq.f;
@@ -898,9 +955,10 @@ attn_status run_backward(DeviceInfo& dev, const void* q, const void* k, const vo
   bq.n_ktiles = (Sk + kBK - 1) / kBK;
   BwdParams bk = bq;
   bk.f.total_units = static_cast<int>(static_cast<int64_t>(B) * H * bq.n_ktiles);
+  bk.f.n_qtiles = (Sq + kBQKv - 1) / kBQKv;  // the dK/dV kernel steps through the queries 64 at a time
   if (D == 64)
-    return causal ? launch_bwd<64, true>(dev, 0, mq, mdo, mk, mv, bq, bk, s)
-                  : launch_bwd<64, false>(dev, 1, mq, mdo, mk, mv, bq, bk, s);
-  return causal ? launch_bwd<128, true>(dev, 2, mq, mdo, mk, mv, bq, bk, s)
-                : launch_bwd<128, false>(dev, 3, mq, mdo, mk, mv, bq, bk, s);
+    return causal ? launch_bwd<64, true>(dev, 0, mq, mdo, mq64, mdo64, mk, mv, bq, bk, s)
+                  : launch_bwd<64, false>(dev, 1, mq, mdo, mq64, mdo64, mk, mv, bq, bk, s);
+  return causal ? launch_bwd<128, true>(dev, 2, mq, mdo, mq64, mdo64, mk, mv, bq, bk, s)
+                : launch_bwd<128, false>(dev, 3, mq, mdo, mq64, mdo64, mk, mv, bq, bk, s);
 }

@@ -1080,15 +1080,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-// Rank-4 map over [B, H, S, D] (D innermost) with a 64 x 128 box (one 128-B
-// swizzle column of a tile).  Rows past S read as zeros and never spill into the
-// next head.
-bool make_map(CUtensorMap* m, const void* ptr, int B, int H, int S, int D) {
+// Rank-4 map over [B, H, S, D] (D innermost) with a 64 x box_rows box (one
+// 128-B swizzle column of a tile).  Rows past S read as zeros and never spill
+// into the next head.
+bool make_map(CUtensorMap* m, const void* ptr, int B, int H, int S, int D, int box_rows = 128) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
   if (encode == nullptr) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2, (cuuint64_t)H * S * D * 2};
-  const cuuint32_t box[4] = {64, 128, 1, 1};
+  const cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides, box,
                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -59,3 +59,31 @@ def test_one_full_barrier_per_slot_holds_with_even_depth_or_p_over_s(p_in_s, slo
     barrier per kind all the same."""
     for seed in range(200):
         run(_units(seed), slots, per_kind=False, seed=seed, p_in_s=p_in_s)
+
+
+# ------------------------------------------------------------ dK/dV backward
+from bwd_pipeline_model import run as run_bwd  # noqa: E402
+
+
+def _bwd_units(seed):
+    rng = random.Random(seed)
+    return [rng.choice([0, 1, 2, 3, 5, 8, 40]) for _ in range(rng.randint(1, 6))]
+
+
+@pytest.mark.parametrize("slots", [4, 8])  # D = 128, D = 64
+def test_dkdv_protocol_never_aliases_or_deadlocks(slots):
+    for seed in range(400):
+        run_bwd(_bwd_units(seed), slots, seed=seed)
+
+
+@pytest.mark.parametrize("mistake", ["s_skips_s_free", "dp_skips_d_free", "products_skip_pd_full",
+                                     "producer_skips_qd_empty", "epilogue_skips_out_full",
+                                     "kv_load_skips_kv_empty"])
+def test_dkdv_model_catches_a_skipped_wait(mistake):
+    failures = 0
+    for seed in range(300):
+        try:
+            run_bwd(_bwd_units(seed), 4, seed=seed, mistake=mistake)
+        except AssertionError:
+            failures += 1
+    assert failures > 0, mistake
