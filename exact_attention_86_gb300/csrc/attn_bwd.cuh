@@ -11,8 +11,9 @@
 // kernels:
 //   bwd_delta_kernel  Delta_i in fp32, one warp per row;
 //   bwd_dq_kernel     one unit = 128 query rows of one (b, h): S and dP on
-//                     the tensor cores, P and dS in the elementwise warps,
-//                     dQ accumulated in TMEM over the key tiles;
+//                     the tensor cores for 64 keys at a time (two steps in
+//                     flight), P and dS in the elementwise warps, dQ
+//                     accumulated in TMEM over the key steps;
 //   bwd_dkdv_kernel   one unit = 128 keys of one (b, h): S^T = K Q^T and
 //                     dP^T = V dO^T for 64 queries at a time (two steps in
 //                     flight), P^T and dS^T, then dV and dK accumulated in
@@ -81,39 +82,62 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restri
   }
 }
 
-// Two fp32 scores of a thread's 64 (from two 32-column TMEM loads).
-__device__ __forceinline__ void pair_at(const uint32_t (&s)[2][32], int e, float& a, float& b) {
-  const int col = 2 * e;
-  a = __uint_as_float(s[col >> 5][col & 31]);
-  b = __uint_as_float(s[col >> 5][(col + 1) & 31]);
-}
-
 // ------------------------------------------------------------------ dQ
+// A unit is 128 query rows of one (b, h); the keys stream past in steps of 64,
+// so that the S and dP of two steps fit in Tensor Memory beside the dQ
+// accumulator and the tensor cores compute the next step's products while the
+// elementwise warps form dS.
+constexpr int kBKDq = 64;  // keys per step
+
 template <int D>
 struct GeoDq {
-  static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kChunkBytes = 128 * 128;
+  static constexpr int kTileQ = 128 * D * 2;    // Q or dO: 128 queries
+  static constexpr int kTileK = kBKDq * D * 2;  // K_j or V_j: 64 keys
+  static constexpr int kChunkQ = 128 * 128;     // one 128-B swizzle column of a Q/dO tile
+  static constexpr int kChunkK = kBKDq * 128;   // one 128-B swizzle column of a K/V tile
   static constexpr int kChunks = D / 64;
-  static constexpr int kSlots = (D == 128) ? 5 : 12;  // K/V ring (per-kind full barriers, as the forward)
-  static __device__ __forceinline__ uint32_t kind_use(uint32_t pos) {
-    return (kSlots & 1) ? (pos / kSlots) >> 1 : pos / kSlots;
-  }
+  static constexpr int kSlots = (D == 128) ? 4 : 8;  // ring of (K_j, V_j) pairs
   static constexpr int kOffQ = 1024;
-  static constexpr int kOffDo = kOffQ + kTileBytes;
-  static constexpr int kOffRing = kOffDo + kTileBytes;
-  static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes + 1024;
-  static constexpr uint32_t kTmemS = 0, kTmemDp = 128, kTmemDs = 256, kTmemDq = 384;
+  static constexpr int kOffDo = kOffQ + kTileQ;
+  static constexpr int kOffRing = kOffDo + kTileQ;
+  static constexpr int kSmemBytes = kOffRing + kSlots * 2 * kTileK + 1024;
+  // TMEM: step parity b holds S at [128 b, 128 b + 64) and dP at
+  // [128 b + 64, 128 b + 128); each half of the elementwise warps writes dS
+  // (bf16 pairs) over the first 16 of the 32 S columns it has read.  dQ at 256.
+  static constexpr uint32_t kTmemDq = 256;
+  static __device__ __forceinline__ uint32_t st_col(uint32_t b) { return 128u * b; }
+  // column of the dS operand of the kk-th dQ instruction (16 keys = 8
+  // columns), relative to st_col: 2 instructions per half
+  static __device__ __forceinline__ uint32_t a_col(int kk) {
+    return 32u * static_cast<uint32_t>(kk >> 1) + 8u * static_cast<uint32_t>(kk & 1);
+  }
 };
+static_assert(GeoDq<128>::kSmemBytes <= 232448 && GeoDq<64>::kSmemBytes <= 232448, "shared memory");
 
 struct CtrlDq {
   uint64_t q_full, q_empty;
-  uint64_t k_full[12], v_full[12], kv_empty[12];
-  uint64_t sp_full, sp_free, ds_full, ds_free, dq_full;
-  uint64_t drain;
+  uint64_t kv_full[8], kv_empty[8];
+  uint64_t st_full[2];   // S and dP of the step complete
+  uint64_t ds_full[2];   // dS written (8 warp arrivals)
+  uint64_t buf_free[2];  // the dQ product of the step completed: its TMEM buffer is free
+  uint64_t dq_full;
+  uint64_t drain[2];     // one per issuing warp
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(CtrlDq) <= 1024, "control block");
+
+// The forward's unit (head, query block, valid keys), with the keys counted in
+// steps of 64: n = steps that hold a key some row of the unit may see.
+template <bool CAUSAL>
+__device__ __forceinline__ Unit decode_dq_unit(const Params& p, int t) {
+  Unit u = decode_unit<CAUSAL>(p, t);
+  int lim = u.kv;
+  if (CAUSAL) lim = min(lim, u.q0 + u.rows);
+  u.j0 = 0;
+  u.n = u.rows > 0 ? (lim + kBKDq - 1) / kBKDq : 0;
+  return u;
+}
 
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -130,26 +154,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t bar_q_full = smem_addr(&ctl.q_full), bar_q_empty = smem_addr(&ctl.q_empty);
-  const uint32_t bar_k_full0 = smem_addr(&ctl.k_full[0]), bar_v_full0 = smem_addr(&ctl.v_full[0]);
-  const uint32_t bar_kv_empty0 = smem_addr(&ctl.kv_empty[0]);
-  const uint32_t bar_sp_full = smem_addr(&ctl.sp_full), bar_sp_free = smem_addr(&ctl.sp_free);
-  const uint32_t bar_ds_full = smem_addr(&ctl.ds_full), bar_ds_free = smem_addr(&ctl.ds_free);
+  const uint32_t bar_kv_full0 = smem_addr(&ctl.kv_full[0]), bar_kv_empty0 = smem_addr(&ctl.kv_empty[0]);
+  const uint32_t bar_st_full0 = smem_addr(&ctl.st_full[0]), bar_ds_full0 = smem_addr(&ctl.ds_full[0]);
+  const uint32_t bar_buf_free0 = smem_addr(&ctl.buf_free[0]);
   const uint32_t bar_dq_full = smem_addr(&ctl.dq_full);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
     mbar_init(bar_q_empty, 1);
     for (int s = 0; s < G::kSlots; ++s) {
-      mbar_init(bar_k_full0 + 8 * s, 1);
-      mbar_init(bar_v_full0 + 8 * s, 1);
+      mbar_init(bar_kv_full0 + 8 * s, 1);
       mbar_init(bar_kv_empty0 + 8 * s, 1);
     }
-    mbar_init(bar_sp_full, 1);
-    mbar_init(bar_sp_free, kSoftmaxWarps);
-    mbar_init(bar_ds_full, kSoftmaxWarps);
-    mbar_init(bar_ds_free, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_st_full0 + 8 * b, 1);
+      mbar_init(bar_ds_full0 + 8 * b, kSoftmaxWarps);
+      mbar_init(bar_buf_free0 + 8 * b, 1);
+    }
     mbar_init(bar_dq_full, 1);
-    mbar_init(smem_addr(&ctl.drain), 1);
+    mbar_init(smem_addr(&ctl.drain[0]), 1);
+    mbar_init(smem_addr(&ctl.drain[1]), 1);
     ctl.abort_flag = 0;
     fence_barrier_init();
   }
@@ -176,50 +200,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kWarpLoad) {
       // -------------------------------------------------------------- TMA
       if (lane == 0) {
-        const uint64_t pol_keep = l2_policy_evict_last();
-        const uint64_t pol_once = l2_policy_evict_first();
+        const uint64_t pol_keep = l2_policy_evict_last();   // K, V: re-read by every query block of the head
+        const uint64_t pol_once = l2_policy_evict_first();  // Q, dO: read once
         uint32_t ring = 0, qcount = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
           const int unit = unit_at<CAUSAL>(t);
           if (unit >= p.total_units) continue;
-          const Unit u = decode_unit<CAUSAL>(p, unit);
+          const Unit u = decode_dq_unit<CAUSAL>(p, unit);
           if (u.n == 0) continue;
           if (!wait_phase(bar_q_empty, (qcount & 1u) ^ 1u, abort_flag, kSiteBwdQEmpty, limit)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar_q_full, 2 * G::kTileBytes);
+          mbar_arrive_expect_tx(bar_q_full, 2 * G::kTileQ);
           for (int c = 0; c < G::kChunks; ++c) {
-            tma_load_4d_hint(base + G::kOffQ + c * G::kChunkBytes, &map_q, bar_q_full, c * 64, u.q0, u.h, u.b,
+            tma_load_4d_hint(base + G::kOffQ + c * G::kChunkQ, &map_q, bar_q_full, c * 64, u.q0, u.h, u.b,
                              pol_once);
-            tma_load_4d_hint(base + G::kOffDo + c * G::kChunkBytes, &map_do, bar_q_full, c * 64, u.q0, u.h, u.b,
+            tma_load_4d_hint(base + G::kOffDo + c * G::kChunkQ, &map_do, bar_q_full, c * 64, u.q0, u.h, u.b,
                              pol_once);
           }
           ++qcount;
           for (int j = 0; ok && j < u.n; ++j) {
-            for (int sel = 0; sel < 2; ++sel) {  // K_j, then V_j
-              const uint32_t slot = ring % G::kSlots;
-              const uint32_t ph = (ring / G::kSlots) & 1u;
-              if (!wait_phase(bar_kv_empty0 + 8 * slot, ph ^ 1u, abort_flag, kSiteBwdKvEmpty, limit)) {
-                ok = false;
-                break;
-              }
-              const uint32_t full = (sel ? bar_v_full0 : bar_k_full0) + 8 * slot;
-              mbar_arrive_expect_tx(full, G::kTileBytes);
-              const int key0 = (u.j0 + j) * kBK;
-              for (int c = 0; c < G::kChunks; ++c)
-                tma_load_4d_hint(base + G::kOffRing + slot * G::kTileBytes + c * G::kChunkBytes,
-                                 sel ? &map_v : &map_k, full, c * 64, key0, u.h, u.b, pol_keep);
-              ++ring;
+            const uint32_t slot = ring % G::kSlots;
+            const uint32_t ph = (ring / G::kSlots) & 1u;
+            if (!wait_phase(bar_kv_empty0 + 8 * slot, ph ^ 1u, abort_flag, kSiteBwdKvEmpty, limit)) {
+              ok = false;
+              break;
             }
+            const uint32_t full = bar_kv_full0 + 8 * slot;
+            mbar_arrive_expect_tx(full, 2 * G::kTileK);
+            const uint32_t dst = base + G::kOffRing + slot * 2 * G::kTileK;
+            const int key0 = (u.j0 + j) * kBKDq;
+            for (int c = 0; c < G::kChunks; ++c) {
+              tma_load_4d_hint(dst + c * G::kChunkK, &map_k, full, c * 64, key0, u.h, u.b, pol_keep);
+              tma_load_4d_hint(dst + G::kTileK + c * G::kChunkK, &map_v, full, c * 64, key0, u.h, u.b, pol_keep);
+            }
+            ++ring;
           }
         }
         if (!ok) {
           if (qcount > 0) wait_phase_drain(bar_q_full, (qcount - 1) & 1u);
           for (uint32_t s = 0; s < (uint32_t)G::kSlots && s < ring; ++s) {
             const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);
-            wait_phase_drain(((last & 1u) ? bar_v_full0 : bar_k_full0) + 8 * s, G::kind_use(last) & 1u);
+            wait_phase_drain(bar_kv_full0 + 8 * s, (last / G::kSlots) & 1u);
           }
         }
-        // the issuer's last commit arrivals land asynchronously: wait for them
+        // the issuers' last commit arrivals land asynchronously: wait for them
         if (qcount > 0) wait_phase_drain(bar_q_empty, (qcount - 1) & 1u);
         for (uint32_t s = 0; s < (uint32_t)G::kSlots && s < ring; ++s) {
           const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);
@@ -228,84 +252,110 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
     } else if (warp == kWarpQK) {
-      // ---------------------------------------------------------- issuer
-      // Per tile t: S = Q K_t^T and dP = dO V_t^T (once the elementwise warps
-      // have read the previous S and dP), then dQ += dS_{t-1} K_{t-1}.
-      const uint32_t idesc_s = idesc_bf16_f32(kBQ, kBK, false, false);
-      const uint32_t idesc_q = idesc_bf16_f32(kBQ, D, false, true);
+      // ---------------------------------------------------- S, dP issuer
+      // Per step t: S = Q K_t^T and dP = dO V_t^T into the buffer of its
+      // parity, once the dQ product of step t-2 has released it.
+      const uint32_t idesc_s = idesc_bf16_f32(kBQ, kBKDq, false, false);
       const uint32_t qa = base + G::kOffQ, da = base + G::kOffDo;
-      uint32_t ring = 0, qcount = 0, tcount = 0;
+      uint32_t tcount = 0, qcount = 0;
       bool ok = true;
-      // dQ += dS K for tile tt whose K sits in ring slot ks
-      auto issue_dq = [&](uint32_t tt, uint32_t ks, bool first) -> bool {
-        if (!wait_warp(bar_ds_full, tt & 1u, abort_flag, kSiteBwdDsFull, limit)) return false;
-        tc_fence_after_sync();
-        const uint32_t ka = base + G::kOffRing + ks * G::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          mma_ts_elect(tmem + G::kTmemDq, tmem + G::kTmemDs + kk * 8,
-                       sdesc_sw128(ka + kk * 16 * 128, G::kChunkBytes, 1024), idesc_q,
-                       (first && kk == 0) ? 0u : 1u);
-        mma_commit_elect(bar_ds_free);
-        mma_commit_elect(bar_kv_empty0 + 8 * ks);
-        return true;
-      };
       for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
         const int unit = unit_at<CAUSAL>(t);
         if (unit >= p.total_units) continue;
-        const Unit u = decode_unit<CAUSAL>(p, unit);
+        const Unit u = decode_dq_unit<CAUSAL>(p, unit);
         if (u.n == 0) continue;
         if (!wait_warp(bar_q_full, qcount & 1u, abort_flag, kSiteBwdQFull, limit)) { ok = false; break; }
         ++qcount;
-        uint32_t prev_ks = 0;
         for (int j = 0; j < u.n; ++j) {
           const uint32_t tt = tcount + j;
-          if (tt >= 1 && !wait_warp(bar_sp_free, (tt - 1) & 1u, abort_flag, kSiteBwdSFree, limit)) { ok = false; break; }
-          const uint32_t posk = ring + 2 * j, posv = posk + 1;
-          const uint32_t ks = posk % G::kSlots, vs = posv % G::kSlots;
-          if (!wait_warp(bar_k_full0 + 8 * ks, G::kind_use(posk) & 1u, abort_flag, kSiteBwdKvFull, limit) ||
-              !wait_warp(bar_v_full0 + 8 * vs, G::kind_use(posv) & 1u, abort_flag, kSiteBwdKvFull, limit)) {
+          const uint32_t b = tt & 1u;
+          const uint32_t slot = tt % G::kSlots;
+          if (!wait_warp(bar_kv_full0 + 8 * slot, (tt / G::kSlots) & 1u, abort_flag, kSiteBwdKvFull, limit)) {
+            ok = false;
+            break;
+          }
+          if (tt >= 2 &&
+              !wait_warp(bar_buf_free0 + 8 * b, ((tt >> 1) - 1) & 1u, abort_flag, kSiteBwdSFree, limit)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const uint32_t ka = base + G::kOffRing + ks * G::kTileBytes;
-          const uint32_t va = base + G::kOffRing + vs * G::kTileBytes;
+          const uint32_t ka = base + G::kOffRing + slot * 2 * G::kTileK;
+          const uint32_t va = ka + G::kTileK;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-            mma_ss_elect(tmem + G::kTmemS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idesc_s,
-                         kk > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-            mma_ss_elect(tmem + G::kTmemDp, sdesc_sw128(da + off, 16, 1024), sdesc_sw128(va + off, 16, 1024),
+            const uint32_t off_q = (kk >> 2) * G::kChunkQ + (kk & 3) * 32;
+            const uint32_t off_k = (kk >> 2) * G::kChunkK + (kk & 3) * 32;
+            mma_ss_elect(tmem + G::st_col(b), sdesc_sw128(qa + off_q, 16, 1024), sdesc_sw128(ka + off_k, 16, 1024),
                          idesc_s, kk > 0 ? 1u : 0u);
           }
-          mma_commit_elect(bar_sp_full);
-          mma_commit_elect(bar_kv_empty0 + 8 * vs);  // V_j is done once dP is
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off_q = (kk >> 2) * G::kChunkQ + (kk & 3) * 32;
+            const uint32_t off_k = (kk >> 2) * G::kChunkK + (kk & 3) * 32;
+            mma_ss_elect(tmem + G::st_col(b) + 64, sdesc_sw128(da + off_q, 16, 1024),
+                         sdesc_sw128(va + off_k, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          mma_commit_elect(bar_st_full0 + 8 * b);
           if (j == u.n - 1) mma_commit_elect(bar_q_empty);  // Q and dO are done after the unit's last S, dP
-          if (j >= 1 && !issue_dq(tt - 1, prev_ks, j == 1)) { ok = false; break; }
-          prev_ks = ks;
         }
         if (!ok) break;
-        if (!issue_dq(tcount + u.n - 1, prev_ks, u.n == 1)) { ok = false; break; }
-        mma_commit_elect(bar_dq_full);
-        ring += 2 * u.n;
         tcount += u.n;
       }
-      if (!ok) {
-        const uint32_t bar_d = smem_addr(&ctl.drain);
-        mma_commit_elect(bar_d);
-        wait_phase_drain(bar_d, 0);
+      const uint32_t bar_d = smem_addr(&ctl.drain[0]);
+      mma_commit_elect(bar_d);
+      wait_phase_drain(bar_d, 0);
+    } else if (warp == kWarpPV) {
+      // --------------------------------------------------------- dQ issuer
+      // Per step t, once the elementwise warps have written dS_t: dQ +=
+      // dS_t K_t; its commit frees the step's TMEM buffer and ring slot (V_t
+      // was read by dP_t, which completed before the elementwise warps began).
+      const uint32_t idesc_q = idesc_bf16_f32(kBQ, D, false, true);
+      uint32_t tcount = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
+        const int unit = unit_at<CAUSAL>(t);
+        if (unit >= p.total_units) continue;
+        const Unit u = decode_dq_unit<CAUSAL>(p, unit);
+        if (u.n == 0) continue;
+        for (int j = 0; j < u.n; ++j) {
+          const uint32_t tt = tcount + j;
+          const uint32_t b = tt & 1u;
+          const uint32_t slot = tt % G::kSlots;
+          if (!wait_warp(bar_ds_full0 + 8 * b, (tt >> 1) & 1u, abort_flag, kSiteBwdDsFull, limit)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t ka = base + G::kOffRing + slot * 2 * G::kTileK;
+#pragma unroll
+          for (int kk = 0; kk < kBKDq / 16; ++kk)
+            mma_ts_elect(tmem + G::kTmemDq, tmem + G::st_col(b) + G::a_col(kk),
+                         sdesc_sw128(ka + kk * 16 * 128, G::kChunkK, 1024), idesc_q, (j == 0 && kk == 0) ? 0u : 1u);
+          mma_commit_elect(bar_buf_free0 + 8 * b);
+          mma_commit_elect(bar_kv_empty0 + 8 * slot);
+        }
+        if (!ok) break;
+        mma_commit_elect(bar_dq_full);
+        tcount += u.n;
+      }
+      const uint32_t bar_d = smem_addr(&ctl.drain[1]);
+      mma_commit_elect(bar_d);
+      wait_phase_drain(bar_d, 0);
+      if (ok) {
+        for (uint32_t back = 1; back <= 2 && back <= tcount; ++back) {
+          const uint32_t t = tcount - back;
+          wait_phase_drain(bar_buf_free0 + 8 * (t & 1u), (t >> 1) & 1u);
+        }
       }
     }
   } else {
     regs_increase<kRegsSoftmax>();
     // ------------------------------------------------------- elementwise
-    // Two threads per query row: warps 0-3 own key columns 0-63 of each tile
-    // and dQ columns [0, D/2), warps 4-7 the rest.
+    // Two threads per query row: warps 0-3 own key columns 0-31 of each step
+    // and dQ columns [0, D/2), warps 4-7 the rest.  Each warp reads and
+    // writes only its own TMEM columns, so the warps never wait for one
+    // another and a failed wait lets a warp leave on its own.
     const int half = warp >> 2;
     const int r = threadIdx.x & (kBQ - 1);
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -314,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
       const int unit = unit_at<CAUSAL>(t);
       if (unit >= p.total_units) continue;
-      const Unit u = decode_unit<CAUSAL>(p, unit);
+      const Unit u = decode_dq_unit<CAUSAL>(p, unit);
       const int row = u.q0 + r;
       const bool row_ok = row < p.Sq;
       const size_t row_index = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq) + row;
@@ -334,31 +384,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool rows_tail = u.q0 + kBQ > p.Sq;
       for (int j = 0; j < u.n; ++j) {
         const uint32_t tt = tcount + j;
-        const int k0 = (u.j0 + j) * kBK;
-        const bool masked = !live || rows_tail || (k0 + kBK > u.kv) || (CAUSAL && k0 + kBK - 1 > u.q0);
+        const uint32_t b = tt & 1u;
+        const int k0 = (u.j0 + j) * kBKDq;
+        // key column c of this half is k0 + 32*half + c: valid below kv and,
+        // causal, up to the row
+        const bool masked = !live || rows_tail || (k0 + kBKDq > u.kv) || (CAUSAL && k0 + kBKDq - 1 > u.q0);
         int climit = u.kv - k0;
         if (CAUSAL) climit = min(climit, row - k0 + 1);
-        climit = live ? climit - 64 * half : 0;
-        if (!wait_warp(bar_sp_full, tt & 1u, abort_flag, kSiteBwdSFull, limit)) { ok = false; break; }
+        climit = live ? climit - 32 * half : 0;
+        if (!wait_warp(bar_st_full0 + 8 * b, (tt >> 1) & 1u, abort_flag, kSiteBwdSFull, limit)) { ok = false; break; }
         tc_fence_after_sync();
-        uint32_t s[2][32], dp[2][32];
-        const uint32_t tS = tmem + lane_off + G::kTmemS + 64u * half;
-        const uint32_t tD = tmem + lane_off + G::kTmemDp + 64u * half;
-        tmem_ld_32x32b_x32(tS, s[0]);
-        tmem_ld_32x32b_x32(tS + 32, s[1]);
-        tmem_ld_32x32b_x32(tD, dp[0]);
-        tmem_ld_32x32b_x32(tD + 32, dp[1]);
-        tmem_ld_wait_x32(s[0]);
-        tmem_ld_wait_x32(s[1]);
-        tmem_ld_wait_x32(dp[0]);
-        tmem_ld_wait_x32(dp[1]);
-        warp_arrive_after_tc(bar_sp_free, lane);  // the issuer may compute the next S and dP
-        uint32_t pk[32];
+        const uint32_t tS = tmem + lane_off + G::st_col(b) + 32u * half;
+        uint32_t s[32], dp[32];
+        tmem_ld_32x32b_x32(tS, s);
+        tmem_ld_32x32b_x32(tS + 64, dp);
+        tmem_ld_wait_x32(s);
+        tmem_ld_wait_x32(dp);
+        uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float s0, s1, d0, d1;
-          pair_at(s, e, s0, s1);
-          pair_at(dp, e, d0, d1);
+        for (int e = 0; e < 16; ++e) {
+          const float s0 = __uint_as_float(s[2 * e]), s1 = __uint_as_float(s[2 * e + 1]);
+          const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
           float p0 = ex2_approx(fmaf(s0, bp.c2, -lse2));
           float p1 = ex2_approx(fmaf(s1, bp.c2, -lse2));
           if (masked) {
@@ -367,14 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           pk[e] = pack_bf16x2(p0 * (d0 - delta_i), p1 * (d1 - delta_i));
         }
-        // dS buffer is free once the previous tile's dQ product has completed
-        if (tt >= 1 && !wait_warp(bar_ds_free, (tt - 1) & 1u, abort_flag, kSiteBwdDsFree, limit)) { ok = false; break; }
-        tc_fence_after_sync();
-        const uint32_t tP = tmem + lane_off + G::kTmemDs + 32u * half;
-        tmem_st_32x32b_x16(tP, *reinterpret_cast<const uint32_t(*)[16]>(&pk[0]));
-        tmem_st_32x32b_x16(tP + 16, *reinterpret_cast<const uint32_t(*)[16]>(&pk[16]));
+        tmem_st_32x32b_x16(tS, pk);  // dS over the S columns just read
         tmem_st_wait();
-        warp_arrive_after_tc(bar_ds_full, lane);
+        warp_arrive_after_tc(bar_ds_full0 + 8 * b, lane);
       }
       if (!ok) break;
       tcount += u.n;
@@ -401,8 +442,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // every elementwise warp has arrived on ds_full for it, which comes after this
       tc_fence_before_sync();
     }
-    // the last ds_free arrival lands asynchronously: wait before exiting
-    if (tcount > 0) wait_phase_drain(bar_ds_free, (tcount - 1) & 1u);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -777,9 +816,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tt = tcount + i;
         const uint32_t b = tt & 1u;
         const int q0 = (u.i0 + i) * kBQKv;
-        // into the warp's staging slot of this step's parity
-        stage[b * 64 + lane] = (lse_raw == -INFINITY) ? INFINITY : lse_raw * kLog2e;
-        stage[b * 64 + 32 + lane] = del_raw;
+        // into the warp's staging slot of this step's parity, negated:
+        // -LSE*log2e (-inf for no key: P = 0) and -Delta
+        stage[b * 64 + lane] = (lse_raw == -INFINITY) ? -INFINITY : -lse_raw * kLog2e;
+        stage[b * 64 + 32 + lane] = -del_raw;
         __syncwarp();
         if (i + 1 < u.n) fetch(i + 1);
         // query column c of this half is q0 + 32*half + c; key <= query for causal
@@ -794,21 +834,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_32x32b_x32(tD, dp);
         tmem_ld_wait_x32(s);
         tmem_ld_wait_x32(dp);
-        const float* lse_c = stage + b * 64;
-        const float* del_c = lse_c + 32;
+        // pairs of columns: -LSE*log2e and -Delta come as packed pairs
+        const uint64_t* nlse2 = reinterpret_cast<const uint64_t*>(stage + b * 64);
+        const uint64_t* ndel2 = nlse2 + 16;
+        const uint64_t c2x2 = f2_pack(bp.c2, bp.c2);
         uint32_t pk[16], ds_pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float s0 = __uint_as_float(s[2 * e]), s1 = __uint_as_float(s[2 * e + 1]);
-          const float d0 = __uint_as_float(dp[2 * e]), d1 = __uint_as_float(dp[2 * e + 1]);
-          float p0 = ex2_approx(fmaf(s0, bp.c2, -lse_c[2 * e]));
-          float p1 = ex2_approx(fmaf(s1, bp.c2, -lse_c[2 * e + 1]));
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])), c2x2, nlse2[e]), x0,
+                    x1);
+          float p0 = ex2_approx(x0);
+          float p1 = ex2_approx(x1);
           if (masked) {
             p0 = (2 * e >= cstart) ? p0 : 0.0f;
             p1 = (2 * e + 1 >= cstart) ? p1 : 0.0f;
           }
           pk[e] = pack_bf16x2(p0, p1);
-          ds_pk[e] = pack_bf16x2(p0 * (d0 - del_c[2 * e]), p1 * (d1 - del_c[2 * e + 1]));
+          const uint64_t diff = f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])), ndel2[e]);
+          float g0, g1;
+          f2_unpack(f2_mul(f2_pack(p0, p1), diff), g0, g1);
+          ds_pk[e] = pack_bf16x2(g0, g1);
         }
         tmem_st_32x32b_x16(tS, pk);
         tmem_st_32x32b_x16(tD, ds_pk);
@@ -863,7 +909,8 @@ size_t bwd_delta_bytes(int B, int H, int Sq) {
 template <int D, bool CAUSAL>
 attn_status launch_bwd(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CUtensorMap& mdo,
                        const CUtensorMap& mq64, const CUtensorMap& mdo64, const CUtensorMap& mk,
-                       const CUtensorMap& mv, const BwdParams& bq, const BwdParams& bk, cudaStream_t stream) {
+                       const CUtensorMap& mv, const CUtensorMap& mk64, const CUtensorMap& mv64, const BwdParams& bq,
+                       const BwdParams& bk, cudaStream_t stream) {
   auto kq = bwd_dq_kernel<D, CAUSAL>;
   auto kk = bwd_dkdv_kernel<D, CAUSAL>;
   constexpr int smem_q = GeoDq<D>::kSmemBytes;
@@ -876,7 +923,7 @@ attn_status launch_bwd(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CU
   }
   if (bq.f.total_units > 0) {
     const int grid = bq.f.total_units < dev.num_sms ? bq.f.total_units : dev.num_sms;
-    kq<<<grid, kThreads, smem_q, stream>>>(mq, mdo, mk, mv, bq);
+    kq<<<grid, kThreads, smem_q, stream>>>(mq, mdo, mk64, mv64, bq);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   }
   if (bk.f.total_units > 0) {
@@ -914,10 +961,13 @@ attn_status run_backward(DeviceInfo& dev, const void* q, const void* k, const vo
                                                                     static_cast<const uint16_t*>(dout), delta, rows);
   if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
 
-  CUtensorMap mq, mdo, mq64, mdo64, mk, mv;
+  // 128-row boxes for what a kernel holds for a whole unit, 64-row boxes for
+  // what streams past it in steps
+  CUtensorMap mq, mdo, mq64, mdo64, mk, mv, mk64, mv64;
   if (!make_map(&mq, q, B, H, Sq, D) || !make_map(&mdo, dout, B, H, Sq, D) ||
       !make_map(&mq64, q, B, H, Sq, D, kBQKv) || !make_map(&mdo64, dout, B, H, Sq, D, kBQKv) ||
-      !make_map(&mk, k, B, H, Sk, D) || !make_map(&mv, v, B, H, Sk, D))
+      !make_map(&mk, k, B, H, Sk, D) || !make_map(&mv, v, B, H, Sk, D) ||
+      !make_map(&mk64, k, B, H, Sk, D, kBKDq) || !make_map(&mv64, v, B, H, Sk, D, kBKDq))
     return ATTN_ERR_CUDA;
   BwdParams bq;
   Params& f = bq.f;
@@ -957,8 +1007,8 @@ attn_status run_backward(DeviceInfo& dev, const void* q, const void* k, const vo
   bk.f.total_units = static_cast<int>(static_cast<int64_t>(B) * H * bq.n_ktiles);
   bk.f.n_qtiles = (Sq + kBQKv - 1) / kBQKv;  // the dK/dV kernel steps through the queries 64 at a time
   if (D == 64)
-    return causal ? launch_bwd<64, true>(dev, 0, mq, mdo, mq64, mdo64, mk, mv, bq, bk, s)
-                  : launch_bwd<64, false>(dev, 1, mq, mdo, mq64, mdo64, mk, mv, bq, bk, s);
-  return causal ? launch_bwd<128, true>(dev, 2, mq, mdo, mq64, mdo64, mk, mv, bq, bk, s)
-                : launch_bwd<128, false>(dev, 3, mq, mdo, mq64, mdo64, mk, mv, bq, bk, s);
+    return causal ? launch_bwd<64, true>(dev, 0, mq, mdo, mq64, mdo64, mk, mv, mk64, mv64, bq, bk, s)
+                  : launch_bwd<64, false>(dev, 1, mq, mdo, mq64, mdo64, mk, mv, mk64, mv64, bq, bk, s);
+  return causal ? launch_bwd<128, true>(dev, 2, mq, mdo, mq64, mdo64, mk, mv, mk64, mv64, bq, bk, s)
+                : launch_bwd<128, false>(dev, 3, mq, mdo, mq64, mdo64, mk, mv, mk64, mv64, bq, bk, s);
 }

@@ -32,11 +32,18 @@ import random
 from pipeline_model import Bar
 
 
-def run(units, slots, seed, mistake=None):
+def run(units, slots, seed, mistake=None, kernel="dkdv"):
     """``units``: steps per unit (0 = a unit without gradient work).
+    ``kernel`` "dkdv" models the dK/dV kernel as described above; "dq" the
+    dQ kernel, which differs in three ways: one product per step (dQ += dS
+    K_t) reads only the S half, where dS was written, and its commit frees the
+    whole step buffer and the ring slot; S and dP both wait for that one
+    release; and the unit-resident operands (Q and dO there) are freed by the
+    score issuer's commit after the unit's last S and dP.
     ``mistake`` plants one protocol error: "s_skips_s_free",
     "dp_skips_d_free", "products_skip_pd_full", "producer_skips_qd_empty",
     "epilogue_skips_out_full", "kv_load_skips_kv_empty"."""
+    dq = kernel == "dq"
     rng = random.Random(seed)
     B = {}
 
@@ -149,13 +156,25 @@ def run(units, slots, seed, mistake=None):
                 assert acc["dk"][0] != "reading", f"dK of step {t} lands while the epilogue reads"
                 half_d[b] = ("dS", t, "done")
                 acc["dk"] = ("busy", u, t)
-            mma(dv_start, dv_end, [bar(f"s_free{b}")], "pd")
-            mma(dk_start, dk_end, [bar(f"d_free{b}"), bar(f"qd_empty{slot}")], "pd")
+            def dq_end(t=t, b=b, slot=slot, u=u):
+                assert half_s[b] == ("P", t) and slot_data.get(slot) == t, f"operands of dQ {t} changed"
+                assert acc["dv"][0] != "reading", f"dQ of step {t} lands while the epilogue reads"
+                half_s[b] = ("P", t, "done")
+                half_d[b] = ("dS", t, "done")   # the dP half was only read
+                acc["dv"] = acc["dk"] = ("busy", u, t)
+            if dq:
+                mma(dv_start, dq_end, [bar(f"s_free{b}"), bar(f"qd_empty{slot}")], "pd")
+            else:
+                mma(dv_start, dv_end, [bar(f"s_free{b}")], "pd")
+                mma(dk_start, dk_end, [bar(f"d_free{b}"), bar(f"qd_empty{slot}")], "pd")
 
         for u, n in enumerate(work):
             for i in range(n):
                 yield from products(tcount + i, u, i == 0)
-            commit(bar("out_full"), bar("kv_empty"), issuer="pd")
+            if dq:
+                commit(bar("out_full"), issuer="pd")
+            else:
+                commit(bar("out_full"), bar("kv_empty"), issuer="pd")
             tcount += n
 
     def scores_issuer():
@@ -179,7 +198,7 @@ def run(units, slots, seed, mistake=None):
                     assert half_s[b] in (None, ("P", tt - 2, "done")), f"S^T {tt} lands on {half_s[b]}"
                     half_s[b] = ("S", tt)
                 mma(s_start, s_end)
-                if tt >= 2 and mistake != "dp_skips_d_free":
+                if tt >= 2 and mistake != "dp_skips_d_free" and not dq:
                     yield lambda: bar(f"d_free{b}").try_wait((use - 1) & 1, use - 1)
 
                 def d_start(tt=tt, b=b, slot=slot, u=u):
@@ -191,6 +210,8 @@ def run(units, slots, seed, mistake=None):
                     assert half_d[b] in (None, ("dS", tt - 2, "done")), f"dP^T {tt} lands on {half_d[b]}"
                     half_d[b] = ("dP", tt)
                 mma(d_start, d_end, [bar(f"st_full{b}")])
+            if dq:   # Q and dO are done after the unit's last S and dP
+                commit(bar("kv_empty"))
             tcount += n
 
     def elementwise():

@@ -70,20 +70,24 @@ def _bwd_units(seed):
     return [rng.choice([0, 1, 2, 3, 5, 8, 40]) for _ in range(rng.randint(1, 6))]
 
 
+@pytest.mark.parametrize("kernel", ["dkdv", "dq"])
 @pytest.mark.parametrize("slots", [4, 8])  # D = 128, D = 64
-def test_dkdv_protocol_never_aliases_or_deadlocks(slots):
+def test_backward_protocols_never_alias_or_deadlock(kernel, slots):
     for seed in range(400):
-        run_bwd(_bwd_units(seed), slots, seed=seed)
+        run_bwd(_bwd_units(seed), slots, seed=seed, kernel=kernel)
 
 
-@pytest.mark.parametrize("mistake", ["s_skips_s_free", "dp_skips_d_free", "products_skip_pd_full",
-                                     "producer_skips_qd_empty", "epilogue_skips_out_full",
-                                     "kv_load_skips_kv_empty"])
-def test_dkdv_model_catches_a_skipped_wait(mistake):
+@pytest.mark.parametrize("kernel,mistake", [
+    ("dkdv", "s_skips_s_free"), ("dkdv", "dp_skips_d_free"), ("dkdv", "products_skip_pd_full"),
+    ("dkdv", "producer_skips_qd_empty"), ("dkdv", "epilogue_skips_out_full"), ("dkdv", "kv_load_skips_kv_empty"),
+    ("dq", "s_skips_s_free"), ("dq", "products_skip_pd_full"), ("dq", "producer_skips_qd_empty"),
+    ("dq", "epilogue_skips_out_full"), ("dq", "kv_load_skips_kv_empty"),
+])
+def test_backward_models_catch_a_skipped_wait(kernel, mistake):
     failures = 0
     for seed in range(300):
         try:
-            run_bwd(_bwd_units(seed), 4, seed=seed, mistake=mistake)
+            run_bwd(_bwd_units(seed), 4, seed=seed, mistake=mistake, kernel=kernel)
         except AssertionError:
             failures += 1
-    assert failures > 0, mistake
+    assert failures > 0, (kernel, mistake)
