@@ -13,10 +13,10 @@
 // CTA layout (384 threads, persistent over work units):
 //   warps 0-3  softmax, columns 0-63 of every score tile (one thread per row)
 //   warps 4-7  softmax, columns 64-127 (the partner thread of the same row)
-//   warp 8     TMA producer (one lane)
+//   warp 8     TMA producer of the units, Q and the K ring (one lane)
 //   warp 9     TMEM owner; issues S = Q K^T (whole warp, one elected lane)
 //   warp 10    issues O += P V (whole warp, one elected lane)
-//   warp 11    idle
+//   warp 11    TMA producer of the V ring (one lane; split rings only, else idle)
 //
 // Tensor Memory (512 columns x 128 lanes, lane = query row):
 //   [  0,128)  S buffer 0      [128,256)  S buffer 1     (fp32 scores)
@@ -62,8 +62,9 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kWarpLoad = 8;
 constexpr int kWarpQK = 9;
 constexpr int kWarpPV = 10;
+constexpr int kWarpLoadV = 11;   // forward: the V producer
 constexpr int kUnitQ = 4;           // depth of a CTA's unit queue
-constexpr int kUnitQReaders = 10;   // warps that read it: QK^T issuer, P V issuer, 8 softmax warps
+constexpr int kUnitQReaders = 10;   // warps that read it: QK^T and P V issuers, 8 softmax warps (+ the V producer with split rings)
 // Lazy rescale threshold (log2 units) and the shift of P (log2 units): each P
 // term is 2^(x - m + shift) <= 2^(tau + shift).  bf16 P: tau 16, shift 0.
 // E4M3 P (largest finite value 448): tau 4.5, shift 4, so terms stay <= 2^8.5
@@ -110,15 +111,45 @@ struct Geo {
   static constexpr int kChunks = D * kElem / 128;
   static constexpr int kChunkElems = 128 / kElem;      // elements per 128-B row of a chunk
   static constexpr int kKSteps = D * kElem / 32;       // QK^T instructions: 32 B of D each
-  static constexpr int kSlots = (D == 128 && !FP8) ? 5 : 12;  // K/V ring depth (tiles)
-  // Ring position pos holds K (pos even) or V (pos odd) in slot pos % kSlots.
-  // With an odd depth a slot alternates between K and V fills, so each slot
-  // has one "full" barrier per kind: every barrier is then waited on, phase
-  // after phase, by the one issuer that consumes that kind, and a parity wait
-  // can never match a phase two fills old.  This is the use index of the
-  // fill at pos among the fills of its kind in its slot.
-  static __device__ __forceinline__ uint32_t kind_use(uint32_t pos) {
-    return (kSlots & 1) ? (pos / kSlots) >> 1 : pos / kSlots;
+  static constexpr int kSlots = (D == 128 && !FP8) ? 5 : 12;  // K and V tiles in shared memory
+  // Two layouts of the K/V tiles over those slots (both modelled by the
+  // protocol tests):
+  //  single ring (padded batches): the producer fills K_0 V_0 K_1 V_1 ... in
+  //    order, position pos = 2 t (+1 for V) in slot pos % kSlots.  With an odd
+  //    depth a slot alternates between K and V fills, so each slot has one
+  //    "full" barrier per kind (waited on, phase after phase, by the one issuer
+  //    that consumes that kind: a parity wait can never match a phase two
+  //    fills old) and one "empty" barrier counting all its fills.  A K fill
+  //    then waits for the P V of an earlier tile, which paces the QK^T issuer
+  //    (measured faster here than the split layout, 3 %).
+  //  split rings (packed and paged batches): K_t in slot t % kSlotsK, V_t in
+  //    slot kSlotsK + t % kSlotsV, each ring filled by its own producer warp,
+  //    so a K fill never waits behind a V fill or its page lookups (measured
+  //    faster there: paged 6 %, packed 2 %).
+  static constexpr int kSlotsK = (kSlots == 5) ? 3 : kSlots / 2;
+  static constexpr int kSlotsV = kSlots - kSlotsK;
+  struct Fill {
+    uint32_t slot;       // shared-memory slot of the tile
+    uint32_t full_use;   // phase index on the slot's full barrier of its kind
+    uint32_t empty_use;  // phase index on the slot's empty barrier (fills of the slot before it)
+  };
+  // where K_t (is_v false) or V_t goes
+  static __device__ __forceinline__ Fill fill_of(uint32_t t, bool is_v, bool split) {
+    if (split) {
+      const uint32_t n = is_v ? kSlotsV : kSlotsK;
+      return {(is_v ? static_cast<uint32_t>(kSlotsK) : 0u) + t % n, t / n, t / n};
+    }
+    const uint32_t pos = 2 * t + (is_v ? 1u : 0u);
+    return {pos % kSlots, (kSlots & 1) ? (pos / kSlots) >> 1 : pos / kSlots, pos / kSlots};
+  }
+  // The last of the first `issued` fills of kind is_v that went to slot s
+  // (false if none did).
+  static __device__ __forceinline__ bool last_fill(uint32_t s, bool is_v, bool split, uint32_t issued, Fill& f) {
+    for (uint32_t back = 1; back <= static_cast<uint32_t>(kSlots) && back <= issued; ++back) {
+      f = fill_of(issued - back, is_v, split);
+      if (f.slot == s) return true;
+    }
+    return false;
   }
   // Two TMEM protocols (both modelled by the protocol tests):
   //  bf16: S buffers 0/1 at [0,128) and [128,256), released by the softmax
@@ -152,7 +183,7 @@ struct Geo {
 
 struct Ctrl {
   uint64_t q_full, q_empty;
-  uint64_t k_full[12], v_full[12], kv_empty[12];  // full: per kind (see Geo::kind_use)
+  uint64_t k_full[12], v_full[12], kv_empty[12];  // per slot; full: one per kind (Geo::fill_of)
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t o_full[2], o_free[2];
   uint64_t uq_full[4], uq_empty[4];  // the CTA's unit queue (filled by the producer lane)
@@ -436,7 +467,10 @@ __device__ __forceinline__ void rescale_o_half(uint32_t tO, float alpha) {
   }
 }
 
-template <int D, bool CAUSAL, bool FP8>
+// SPLIT: K and V in rings of their own, each with its own producer warp
+// (packed and paged batches); otherwise one ring of alternating K and V tiles
+// (see Geo).
+template <int D, bool CAUSAL, bool FP8, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const Params p) {
@@ -488,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int k = 0; k < kUnitQ; ++k) {
       mbar_init(bar_uq_full0 + 8 * k, 1);
-      mbar_init(bar_uq_empty0 + 8 * k, kUnitQReaders);
+      mbar_init(bar_uq_empty0 + 8 * k, kUnitQReaders + (SPLIT ? 1 : 0));
     }
     ctl.abort_flag = 0;
     fence_barrier_init();
@@ -511,14 +545,80 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t_end = (p.total_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) *
                     static_cast<int>(gridDim.x);
 
+  // K/V tile layout (Geo): split rings (packed and paged batches) or one ring
+  constexpr bool split = SPLIT;
+
   if (warp >= kSoftmaxWarps) {
     regs_decrease<kRegsOther>();
+  // The two 64-key halves of tile j of unit u in a paged cache, as token rows
+  // of the cache; a half past the sequence's keys is read from one row past
+  // the cache: zeros.  (Both lookups are in flight together.)
+  auto lookup_pages = [&](const Unit& u, int j, int (&page_tok)[2]) {
+    page_tok[0] = page_tok[1] = p.cache_tokens;
+    if (p.block_table == nullptr) return;
+    const int key0 = (u.j0 + j) * kBK;
+    int pg[2] = {0, 0};
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int pos = key0 + 64 * hf;
+      if (pos < u.kv) pg[hf] = __ldg(p.block_table + static_cast<size_t>(u.b) * p.max_pages + pos / p.page_size);
+    }
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int pos = key0 + 64 * hf;
+      if (pos < u.kv) page_tok[hf] = min(max(pg[hf], 0), p.num_pages - 1) * p.page_size + pos % p.page_size;
+    }
+  };
+  // K_j (is_v false) or V_j of unit u into ring slot `slot`, completing on `full`
+  auto load_tile = [&](bool is_v, uint32_t slot, uint32_t full, const Unit& u, int j, const int (&page_tok)[2],
+                       uint64_t pol) {
+    mbar_arrive_expect_tx(full, G::kTileBytes);
+    const CUtensorMap* m = is_v ? &map_v : &map_k;
+    const int key0 = (u.j0 + j) * kBK;
+    const uint32_t dst = base + G::kOffRing + slot * G::kTileBytes;
+    const bool packed = p.cu_q != nullptr;  // padded maps are (D, S, H, B); packed maps are (D, H, tokens, 1)
+    if (FP8 && is_v) {
+      // E4M3 V is stored transposed, (Sk, D, H, B): the tile is 128 rows of
+      // D, each 128 keys long (K-major for the P V product)
+      tma_load_4d_hint(dst, m, full, key0, 0, u.h, u.b, pol);
+    } else if (p.block_table == nullptr) {
+      for (int c = 0; c < G::kChunks; ++c)
+        tma_load_4d_hint(dst + c * G::kChunkBytes, m, full, c * G::kChunkElems, packed ? u.h : key0,
+                         packed ? u.k_tok0 + key0 : u.h, packed ? 0 : u.b, pol);
+    } else {
+      // paged: two 64-key boxes, each inside one page (page_size is a
+      // multiple of 64)
+      for (int hf = 0; hf < 2; ++hf)
+        for (int c = 0; c < G::kChunks; ++c)
+          tma_load_4d_hint(dst + c * G::kChunkBytes + hf * (G::kChunkBytes / 2), m, full, c * 64, u.h,
+                           page_tok[hf], 0, pol);
+    }
+  };
+  // Drains of a producer lane before the CTA exits: after a failure, every
+  // copy it started must land; in any case the issuers' last commit arrivals
+  // on the empty barriers of its slots (nothing else waits for them) must
+  // have landed before this CTA's shared memory is gone.
+  auto drain_slots = [&](bool with_k, bool with_v, uint32_t k_issued, uint32_t v_issued, bool failed) {
+    for (uint32_t s = 0; s < static_cast<uint32_t>(G::kSlots); ++s) {
+      typename G::Fill fk, fv;
+      const bool hk = with_k && G::last_fill(s, false, split, k_issued, fk);
+      const bool hv = with_v && G::last_fill(s, true, split, v_issued, fv);
+      if (failed) {
+        if (hk) wait_phase_drain(bar_k_full0 + 8 * s, fk.full_use & 1u);
+        if (hv) wait_phase_drain(bar_v_full0 + 8 * s, fv.full_use & 1u);
+      }
+      if (hk || hv) {
+        const uint32_t e = (hk && hv) ? max(fk.empty_use, fv.empty_use) : (hk ? fk.empty_use : fv.empty_use);
+        wait_phase_drain(bar_kv_empty0 + 8 * s, e & 1u);
+      }
+    }
+  };
   if (warp == kWarpLoad) {
-    // ------------------------------------------------------------------ TMA
+    // ------------------------------------------- TMA: units, Q, K (and V)
     if (lane == 0) {
       const uint64_t pol_keep = l2_policy_evict_last();   // K/V: re-read by every query block of the head
       const uint64_t pol_once = l2_policy_evict_first();  // Q: read once
-      uint32_t ring = 0, qcount = 0, kq = 0;
+      uint32_t k_issued = 0, v_issued = 0, qcount = 0, kq = 0;
       int t_static = blockIdx.x;
       bool ok = true;
       while (ok) {
@@ -557,77 +657,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u.n == 0) continue;
         if (!wait_phase(bar_q_empty, (qcount & 1u) ^ 1u, abort_flag, kSiteQEmpty, limit)) { ok = false; break; }
         mbar_arrive_expect_tx(bar_q_full, G::kTileBytes);
-        // padded maps are (D, S, H, B); packed maps are (D, H, tokens, 1)
         const bool packed = p.cu_q != nullptr;
         for (int c = 0; c < G::kChunks; ++c)
           tma_load_4d_hint(base + G::kOffQ + c * G::kChunkBytes, &map_q, bar_q_full, c * G::kChunkElems,
                            packed ? u.h : u.q0, packed ? u.q_tok0 : u.h, packed ? 0 : u.b, pol_once);
         ++qcount;
         for (int j = 0; ok && j < u.n; ++j) {
-          // paged: the tile's two 64-key halves are looked up once (both loads
-          // in flight together) and serve both K_j and V_j; a half past the
-          // sequence's keys is copied from one row past the cache: zeros
-          int page_tok[2] = {p.cache_tokens, p.cache_tokens};
-          if (p.block_table != nullptr) {
-            const int key0 = (u.j0 + j) * kBK;
-            int pg[2] = {0, 0};
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              const int pos = key0 + 64 * hf;
-              if (pos < u.kv) pg[hf] = __ldg(p.block_table + static_cast<size_t>(u.b) * p.max_pages + pos / p.page_size);
+          int page_tok[2];
+          lookup_pages(u, j, page_tok);
+          for (int sel = 0; sel < (split ? 1 : 2); ++sel) {  // K_j, then (single ring) V_j
+            const typename G::Fill f = G::fill_of(sel ? v_issued : k_issued, sel != 0, split);
+            if (!wait_phase(bar_kv_empty0 + 8 * f.slot, (f.empty_use & 1u) ^ 1u, abort_flag, kSiteKvEmpty, limit)) {
+              ok = false;
+              break;
             }
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-              const int pos = key0 + 64 * hf;
-              if (pos < u.kv) page_tok[hf] = min(max(pg[hf], 0), p.num_pages - 1) * p.page_size + pos % p.page_size;
-            }
-          }
-          for (int sel = 0; sel < 2; ++sel) {  // K_j, then V_j
-            const uint32_t slot = ring % G::kSlots;
-            const uint32_t ph = (ring / G::kSlots) & 1u;
-            if (!wait_phase(bar_kv_empty0 + 8 * slot, ph ^ 1u, abort_flag, kSiteKvEmpty, limit)) { ok = false; break; }
-            const uint32_t full = (sel ? bar_v_full0 : bar_k_full0) + 8 * slot;
-            mbar_arrive_expect_tx(full, G::kTileBytes);
-            const CUtensorMap* m = sel ? &map_v : &map_k;
-            const int key0 = (u.j0 + j) * kBK;
-            const uint32_t dst = base + G::kOffRing + slot * G::kTileBytes;
-            if (FP8 && sel) {
-              // E4M3 V is stored transposed, (Sk, D, H, B): the tile is 128
-              // rows of D, each 128 keys long (K-major for the P V product)
-              tma_load_4d_hint(dst, m, full, key0, 0, u.h, u.b, pol_keep);
-            } else if (p.block_table == nullptr) {
-              for (int c = 0; c < G::kChunks; ++c)
-                tma_load_4d_hint(dst + c * G::kChunkBytes, m, full, c * G::kChunkElems, packed ? u.h : key0,
-                                 packed ? u.k_tok0 + key0 : u.h, packed ? 0 : u.b, pol_keep);
-            } else {
-              // paged: two 64-key boxes, each inside one page (page_size is a
-              // multiple of 64)
-              for (int hf = 0; hf < 2; ++hf)
-                for (int c = 0; c < G::kChunks; ++c)
-                  tma_load_4d_hint(dst + c * G::kChunkBytes + hf * (G::kChunkBytes / 2), m, full, c * 64, u.h,
-                                   page_tok[hf], 0, pol_keep);
-            }
-            ++ring;
+            load_tile(sel != 0, f.slot, (sel ? bar_v_full0 : bar_k_full0) + 8 * f.slot, u, j, page_tok, pol_keep);
+            if (sel) ++v_issued; else ++k_issued;
           }
         }
       }
-      if (!ok) {
-        // Let every copy this lane started land before the CTA exits.
-        if (qcount > 0) wait_phase_drain(bar_q_full, (qcount - 1) & 1u);
-        for (uint32_t s = 0; s < (uint32_t)G::kSlots && s < ring; ++s) {
-          const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);  // last load issued into slot s
-          wait_phase_drain(((last & 1u) ? bar_v_full0 : bar_k_full0) + 8 * s, G::kind_use(last) & 1u);
-        }
-      }
-      // The issuers release slots and the Q buffer with tcgen05.commit, whose
-      // mbarrier arrivals land asynchronously; nothing else waits for the last
-      // ones.  Wait for them here so that none can land after this CTA's shared
-      // memory is gone.
+      if (!ok && qcount > 0) wait_phase_drain(bar_q_full, (qcount - 1) & 1u);
       if (qcount > 0) wait_phase_drain(bar_q_empty, (qcount - 1) & 1u);
-      for (uint32_t s = 0; s < (uint32_t)G::kSlots && s < ring; ++s) {
-        const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);
-        wait_phase_drain(bar_kv_empty0 + 8 * s, (last / G::kSlots) & 1u);
-      }
+      drain_slots(true, !split, k_issued, v_issued, !ok);
       // Dynamic scheduling: this CTA makes no more claims.  The last CTA to get
       // here (every CTA does, aborting or not) puts the counter back to 0 for
       // the next launch that uses it.
@@ -640,11 +691,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
+  } else if (SPLIT && warp == kWarpLoadV) {
+    // ----------------------------------------------------------- TMA: V
+    // Split rings only: V tiles have a producer of their own, so that a V
+    // fill waiting for its slot (free once that tile's P V completes) or for
+    // its page lookup never holds up the K fills.  Units come from the CTA's
+    // unit queue, of which this warp is then a reader.
+    const uint64_t pol_keep = l2_policy_evict_last();
+    uint32_t v_issued = 0, kq = 0;  // (lane 0)
+    bool ok = true;
+    while (ok) {
+      const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
+      if (unit == -2) { ok = false; break; }
+      if (unit < 0) break;
+      const Unit u = decode_unit<CAUSAL>(p, unit);
+      if (u.n == 0) continue;
+      if (lane == 0) {
+        for (int j = 0; j < u.n; ++j) {
+          int page_tok[2];
+          lookup_pages(u, j, page_tok);
+          const typename G::Fill f = G::fill_of(v_issued, true, true);
+          if (!wait_phase(bar_kv_empty0 + 8 * f.slot, (f.empty_use & 1u) ^ 1u, abort_flag, kSiteKvEmpty, limit)) {
+            ok = false;
+            break;
+          }
+          load_tile(true, f.slot, bar_v_full0 + 8 * f.slot, u, j, page_tok, pol_keep);
+          ++v_issued;
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    }
+    if (lane == 0) drain_slots(false, true, 0, v_issued, !ok);
+    __syncwarp();
   } else if (warp == kWarpQK) {
     // ---------------------------------------------------- S = Q K^T issuer
     // Runs up to two tiles ahead of the softmax (two S buffers).  Releases
     // each K slot once its MMAs complete.
-    uint32_t ring = 0, qcount = 0, tcount = 0, kq = 0;
+    uint32_t qcount = 0, tcount = 0, kq = 0;
     bool ok = true;
     const uint32_t qa = base + G::kOffQ;
     while (ok) {
@@ -665,9 +748,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_warp(bar_sb, (use - 1) & 1u, abort_flag, kSiteSFree, limit)) { ok = false; break; }
           tc_fence_after_sync();
         }
-        const uint32_t pos = ring + 2 * j;
-        const uint32_t slot = pos % G::kSlots;
-        if (!wait_warp(bar_k_full0 + 8 * slot, G::kind_use(pos) & 1u, abort_flag, kSiteKvFull, limit)) {
+        const typename G::Fill f = G::fill_of(tcount, false, split);
+        const uint32_t slot = f.slot;
+        if (!wait_warp(bar_k_full0 + 8 * slot, f.full_use & 1u, abort_flag, kSiteKvFull, limit)) {
           ok = false;
           break;
         }
@@ -687,7 +770,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_elect(bar_kv_empty0 + 8 * slot);
       }
       if (!ok) break;
-      ring += 2 * u.n;
       mma_commit_elect(bar_q_empty);
     }
     if (!ok) {
@@ -699,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------- O += P V issuer
     // Consecutive units alternate between the two O buffers, so a unit's
     // products never wait for the epilogue of the unit before.
-    uint32_t ring = 0, tcount = 0, ucount = 0, kq = 0;
+    uint32_t tcount = 0, ucount = 0, kq = 0;
     bool ok = true;
     while (ok) {
       const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
@@ -721,9 +803,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tOb = tmem + G::kTmemO + static_cast<uint32_t>(D) * ob;
         // the tile's P: over its S buffer, or in its own P buffer
         const uint32_t tSb = tmem + (G::kPInS ? G::kTmemS + 128u * b : G::kTmemP + 64u * b);
-        const uint32_t pos = ring + 2 * j + 1;
-        const uint32_t slot = pos % G::kSlots;
-        if (!wait_warp(bar_v_full0 + 8 * slot, G::kind_use(pos) & 1u, abort_flag, kSiteKvFull, limit)) {
+        const typename G::Fill f = G::fill_of(tcount, true, split);
+        const uint32_t slot = f.slot;
+        if (!wait_warp(bar_v_full0 + 8 * slot, f.full_use & 1u, abort_flag, kSiteKvFull, limit)) {
           ok = false;
           break;
         }
@@ -749,7 +831,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j == u.n - 1) mma_commit_elect(bar_o_full0 + 8 * ob);
       }
       if (!ok) break;
-      ring += 2 * u.n;
       ++ucount;
     }
     if (!ok) {
@@ -1033,7 +1114,7 @@ struct DeviceInfo {
   int initialised = 0;
   int supported = 0;
   int num_sms = 0;
-  bool smem_set[6] = {false, false, false, false, false, false};
+  bool smem_set[10] = {};
   bool bwd_smem_set[4] = {false, false, false, false};
   void* scratch = nullptr;  // this device's address of g_splitkv_scratch
 };
@@ -1147,10 +1228,10 @@ void clear_paged(Params& p) {
   p.cache_tokens = 0;
 }
 
-template <int D, bool CAUSAL, bool FP8 = false>
+template <int D, bool CAUSAL, bool FP8 = false, bool SPLIT = false>
 attn_status launch(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                    const Params& p, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<D, CAUSAL, FP8>;
+  auto kern = attn_fwd_kernel<D, CAUSAL, FP8, SPLIT>;
   constexpr int smem = Geo<D, FP8>::kSmemBytes;
   if (!dev.smem_set[idx]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -1300,10 +1381,14 @@ Params packed_params(void* o, float* lse, const int32_t* cu_q, int batch, int ma
   return p;
 }
 
+// Packed and paged batches: the kernels with split K/V rings.
 attn_status launch_any(DeviceInfo& dev, int D, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
                        const CUtensorMap& mv, const Params& p, cudaStream_t s) {
-  if (D == 64) return causal ? launch<64, true>(dev, 0, mq, mk, mv, p, s) : launch<64, false>(dev, 1, mq, mk, mv, p, s);
-  return causal ? launch<128, true>(dev, 2, mq, mk, mv, p, s) : launch<128, false>(dev, 3, mq, mk, mv, p, s);
+  if (D == 64)
+    return causal ? launch<64, true, false, true>(dev, 6, mq, mk, mv, p, s)
+                  : launch<64, false, false, true>(dev, 7, mq, mk, mv, p, s);
+  return causal ? launch<128, true, false, true>(dev, 8, mq, mk, mv, p, s)
+                : launch<128, false, false, true>(dev, 9, mq, mk, mv, p, s);
 }
 
 attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const void* v, void* o, float* lse, int B,

@@ -60,10 +60,15 @@ class Bar:
         return ok
 
 
-def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False):
+def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False, rings=None):
     """``p_in_s`` selects the E4M3 kernel's protocol (P written over S, two O
     buffers, S released by the P V commit) instead of the bf16 kernel's
     (separate P buffers, S released by the softmax, one O buffer).
+    ``rings`` = (slots_k, slots_v) selects the kernel's ring layout: K_t in
+    slot t % slots_k, V_t in slot slots_k + t % slots_v, one full and one empty
+    barrier per slot, and two producers (Q and K; V), each filling its ring in
+    order (``slots`` and ``per_kind`` are then unused); without it the single
+    ring of positions described above, filled by one producer.
     ``mistake`` plants one protocol error, for the tests that show the model
     catches it: "qk_skips_buffer_wait", "pv_skips_o_free",
     "rescale_skips_p_free", "p_store_skips_p_free"."""
@@ -80,13 +85,27 @@ def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False)
         bar(f"o_free{b}")
     bar("q_full"); bar("q_empty")
 
+    def slot_of(pos):
+        if rings:
+            t, sel = pos >> 1, pos & 1
+            return rings[0] + t % rings[1] if sel else t % rings[0]
+        return pos % slots
+
+    def empty_use(pos):   # fills of the slot before this one
+        if rings:
+            t, sel = pos >> 1, pos & 1
+            return t // rings[sel]
+        return pos // slots
+
     def full_bar(pos):
-        slot = pos % slots
-        if per_kind:
+        slot = slot_of(pos)
+        if per_kind and not rings:
             return bar(f"{'v' if pos & 1 else 'k'}_full{slot}")
         return bar(f"kv_full{slot}")
 
     def full_use(pos):
+        if rings:
+            return empty_use(pos)
         if per_kind:
             return ((pos // slots) >> 1) if (slots & 1) else pos // slots
         return pos // slots
@@ -113,16 +132,22 @@ def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False)
         seq[0] += 1
         events.append((t, seq[0], done))
 
-    def producer():
+    def producer(kinds=(0, 1)):
+        # kinds: (0, 1) one producer for Q, K and V in order; (0,) the split
+        # layout's producer of Q and the K ring; (1,) its producer of the V ring
         ring = qcount = 0
         for n in units:
-            yield lambda: bar("q_empty").try_wait((qcount & 1) ^ 1, qcount - 1)
-            bar("q_full").arrive(tx=1)
-            later(rng.expovariate(1.0), lambda: bar("q_full").complete_tx(1))
-            qcount += 1
+            if 0 in kinds:
+                yield lambda: bar("q_empty").try_wait((qcount & 1) ^ 1, qcount - 1)
+                bar("q_full").arrive(tx=1)
+                later(rng.expovariate(1.0), lambda: bar("q_full").complete_tx(1))
+                qcount += 1
             for j in range(n):
                 for sel in (0, 1):
-                    slot, use = ring % slots, ring // slots
+                    if sel not in kinds:
+                        ring += 1
+                        continue
+                    slot, use = slot_of(ring), empty_use(ring)
                     yield lambda: bar(f"kv_empty{slot}").try_wait((use & 1) ^ 1, use - 1)
                     f = full_bar(ring)
                     f.arrive(tx=1)
@@ -158,7 +183,7 @@ def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False)
                     else:        # the softmax has read S of tile tcount-2
                         yield lambda: bar(f"s_free{b}").try_wait((use - 1) & 1, use - 1)
                 pos = ring + 2 * j
-                slot = pos % slots
+                slot = slot_of(pos)
                 yield lambda: full_bar(pos).try_wait(full_use(pos) & 1, full_use(pos))
                 assert slot_data.get(slot) == pos, f"QK read slot {slot}: has {slot_data.get(slot)}, wants {pos}"
                 st = tmem_s[b]
@@ -219,7 +244,7 @@ def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False)
                 if j == 0:
                     assert o_state[ob] == ("free", ucount - n_obuf), f"O{ob} reused while {o_state[ob]}"
                 pos = ring + 2 * j + 1
-                slot = pos % slots
+                slot = slot_of(pos)
                 yield lambda: full_bar(pos).try_wait(full_use(pos) & 1, full_use(pos))
                 assert slot_data.get(slot) == pos, f"PV read slot {slot}: has {slot_data.get(slot)}, wants {pos}"
 
@@ -237,13 +262,19 @@ def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False)
             ring += 2 * n
             ucount += 1
 
-    for s in range(slots):
+    for s in range(sum(rings) if rings else slots):
         bar(f"kv_empty{s}")
-        if per_kind:
+        if rings:
+            bar(f"kv_full{s}")
+        elif per_kind:
             bar(f"k_full{s}"); bar(f"v_full{s}")
         else:
             bar(f"kv_full{s}")
-    actors = {"prod": producer(), "qk": qk(), "sm": softmax(), "pv": pv()}
+    actors = {"qk": qk(), "sm": softmax(), "pv": pv()}
+    if rings:
+        actors["prod_k"], actors["prod_v"] = producer((0,)), producer((1,))
+    else:
+        actors["prod"] = producer()
     waiting = {k: next(g, None) for k, g in actors.items()}
     while True:
         ready = [k for k, w in waiting.items() if w is not None and w()]

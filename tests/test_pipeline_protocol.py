@@ -13,8 +13,33 @@ def _units(seed):
     return [rng.choice([1, 2, 3, 5, 8, 16, 64]) for _ in range(rng.randint(1, 6))]
 
 
-@pytest.mark.parametrize("p_in_s,slots", [(False, 5), (False, 12), (True, 12)])  # bf16 D=128, D=64; E4M3
-def test_kernel_protocol_never_aliases_or_deadlocks(p_in_s, slots):
+# packed and paged batches: K and V in rings of their own, each with its own
+# producer (bf16 D=128: 3 + 2 slots; bf16 D=64: 6 + 6)
+@pytest.mark.parametrize("p_in_s,rings", [(False, (3, 2)), (False, (6, 6)), (True, (6, 6))])
+def test_split_ring_protocol_never_aliases_or_deadlocks(p_in_s, rings):
+    for seed in range(400):
+        run(_units(seed), 0, per_kind=False, seed=seed, p_in_s=p_in_s, rings=rings)
+
+
+@pytest.mark.parametrize("p_in_s,mistake", [
+    (False, "qk_skips_buffer_wait"), (False, "p_store_skips_p_free"), (False, "rescale_skips_p_free"),
+    (True, "qk_skips_buffer_wait"), (True, "rescale_skips_p_free"),
+])
+def test_model_with_split_rings_catches_a_skipped_wait(p_in_s, mistake):
+    failures = 0
+    for seed in range(300):
+        try:
+            run(_units(seed), 0, per_kind=False, seed=seed, rescale_p=0.6, mistake=mistake, p_in_s=p_in_s,
+                rings=(3, 2))
+        except AssertionError:
+            failures += 1
+    assert failures > 0, mistake
+
+
+# padded batches: one ring of alternating K and V positions, one producer
+# (bf16 D=128: 5 slots; bf16 D=64 and E4M3: 12)
+@pytest.mark.parametrize("p_in_s,slots", [(False, 5), (False, 12), (True, 12)])
+def test_single_ring_protocol_never_aliases_or_deadlocks(p_in_s, slots):
     for seed in range(400):
         run(_units(seed), slots, per_kind=True, seed=seed, p_in_s=p_in_s)
 
