@@ -142,15 +142,6 @@ struct Geo {
     const uint32_t pos = 2 * t + (is_v ? 1u : 0u);
     return {pos % kSlots, (kSlots & 1) ? (pos / kSlots) >> 1 : pos / kSlots, pos / kSlots};
   }
-  // The last of the first `issued` fills of kind is_v that went to slot s
-  // (false if none did).
-  static __device__ __forceinline__ bool last_fill(uint32_t s, bool is_v, bool split, uint32_t issued, Fill& f) {
-    for (uint32_t back = 1; back <= static_cast<uint32_t>(kSlots) && back <= issued; ++back) {
-      f = fill_of(issued - back, is_v, split);
-      if (f.slot == s) return true;
-    }
-    return false;
-  }
   // Two TMEM protocols (both modelled by the protocol tests):
   //  bf16: S buffers 0/1 at [0,128) and [128,256), released by the softmax
   //        once read; P buffers 0/1 at [256,320) and [320,384); one O buffer
@@ -599,18 +590,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   // on the empty barriers of its slots (nothing else waits for them) must
   // have landed before this CTA's shared memory is gone.
   auto drain_slots = [&](bool with_k, bool with_v, uint32_t k_issued, uint32_t v_issued, bool failed) {
-    for (uint32_t s = 0; s < static_cast<uint32_t>(G::kSlots); ++s) {
-      typename G::Fill fk, fv;
-      const bool hk = with_k && G::last_fill(s, false, split, k_issued, fk);
-      const bool hv = with_v && G::last_fill(s, true, split, v_issued, fv);
+    // per slot, 1 + the phase index of its last fill (0: none), found in one
+    // pass over the last kSlots fills of each kind (every slot that was ever
+    // filled appears among them)
+    uint32_t full_k[G::kSlots], full_v[G::kSlots], empty[G::kSlots];
+    for (int s = 0; s < G::kSlots; ++s) full_k[s] = full_v[s] = empty[s] = 0;
+    for (int kind = 0; kind < 2; ++kind) {
+      const bool is_v = kind == 1;
+      if (is_v ? !with_v : !with_k) continue;
+      const uint32_t issued = is_v ? v_issued : k_issued;
+      const uint32_t first = issued > static_cast<uint32_t>(G::kSlots) ? issued - G::kSlots : 0u;
+      for (uint32_t t = first; t < issued; ++t) {  // oldest first: later fills overwrite
+        const typename G::Fill f = G::fill_of(t, is_v, split);
+        (is_v ? full_v : full_k)[f.slot] = f.full_use + 1;
+        empty[f.slot] = max(empty[f.slot], f.empty_use + 1);
+      }
+    }
+    for (int s = 0; s < G::kSlots; ++s) {
       if (failed) {
-        if (hk) wait_phase_drain(bar_k_full0 + 8 * s, fk.full_use & 1u);
-        if (hv) wait_phase_drain(bar_v_full0 + 8 * s, fv.full_use & 1u);
+        if (full_k[s]) wait_phase_drain(bar_k_full0 + 8 * s, (full_k[s] - 1) & 1u);
+        if (full_v[s]) wait_phase_drain(bar_v_full0 + 8 * s, (full_v[s] - 1) & 1u);
       }
-      if (hk || hv) {
-        const uint32_t e = (hk && hv) ? max(fk.empty_use, fv.empty_use) : (hk ? fk.empty_use : fv.empty_use);
-        wait_phase_drain(bar_kv_empty0 + 8 * s, e & 1u);
-      }
+      if (empty[s]) wait_phase_drain(bar_kv_empty0 + 8 * s, (empty[s] - 1) & 1u);
     }
   };
   if (warp == kWarpLoad) {
