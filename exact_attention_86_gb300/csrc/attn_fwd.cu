@@ -590,28 +590,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   // on the empty barriers of its slots (nothing else waits for them) must
   // have landed before this CTA's shared memory is gone.
   auto drain_slots = [&](bool with_k, bool with_v, uint32_t k_issued, uint32_t v_issued, bool failed) {
-    // per slot, 1 + the phase index of its last fill (0: none), found in one
-    // pass over the last kSlots fills of each kind (every slot that was ever
-    // filled appears among them)
-    uint32_t full_k[G::kSlots], full_v[G::kSlots], empty[G::kSlots];
-    for (int s = 0; s < G::kSlots; ++s) full_k[s] = full_v[s] = empty[s] = 0;
-    for (int kind = 0; kind < 2; ++kind) {
-      const bool is_v = kind == 1;
-      if (is_v ? !with_v : !with_k) continue;
-      const uint32_t issued = is_v ? v_issued : k_issued;
-      const uint32_t first = issued > static_cast<uint32_t>(G::kSlots) ? issued - G::kSlots : 0u;
-      for (uint32_t t = first; t < issued; ++t) {  // oldest first: later fills overwrite
-        const typename G::Fill f = G::fill_of(t, is_v, split);
-        (is_v ? full_v : full_k)[f.slot] = f.full_use + 1;
-        empty[f.slot] = max(empty[f.slot], f.empty_use + 1);
+    if constexpr (!SPLIT) {
+      // one ring: positions 0 .. ring-1 were issued (K_t at 2t, V_t at 2t+1)
+      const uint32_t ring = k_issued + v_issued;
+      for (uint32_t s = 0; s < static_cast<uint32_t>(G::kSlots) && s < ring; ++s) {
+        const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);  // last position issued into slot s
+        const typename G::Fill f = G::fill_of(last >> 1, (last & 1u) != 0, false);
+        if (failed) wait_phase_drain(((last & 1u) ? bar_v_full0 : bar_k_full0) + 8 * s, f.full_use & 1u);
+        wait_phase_drain(bar_kv_empty0 + 8 * s, f.empty_use & 1u);
       }
-    }
-    for (int s = 0; s < G::kSlots; ++s) {
-      if (failed) {
-        if (full_k[s]) wait_phase_drain(bar_k_full0 + 8 * s, (full_k[s] - 1) & 1u);
-        if (full_v[s]) wait_phase_drain(bar_v_full0 + 8 * s, (full_v[s] - 1) & 1u);
+    } else {
+      // split rings: ring r of n slots from slot `first` got `issued` fills in order
+      for (int kind = 0; kind < 2; ++kind) {
+        const bool is_v = kind == 1;
+        if (is_v ? !with_v : !with_k) continue;
+        const uint32_t issued = is_v ? v_issued : k_issued;
+        const uint32_t first = is_v ? static_cast<uint32_t>(G::kSlotsK) : 0u;
+        const uint32_t n = is_v ? static_cast<uint32_t>(G::kSlotsV) : static_cast<uint32_t>(G::kSlotsK);
+        for (uint32_t i = 0; i < n && i < issued; ++i) {
+          const uint32_t use = (issued - 1 - i) / n;  // phase index of the last fill of slot first + i
+          if (failed) wait_phase_drain((is_v ? bar_v_full0 : bar_k_full0) + 8 * (first + i), use & 1u);
+          wait_phase_drain(bar_kv_empty0 + 8 * (first + i), use & 1u);
+        }
       }
-      if (empty[s]) wait_phase_drain(bar_kv_empty0 + 8 * s, (empty[s] - 1) & 1u);
     }
   };
   if (warp == kWarpLoad) {
