@@ -43,6 +43,7 @@ sys.path.insert(0, ROOT)
 METRIC = "fused attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor peak"
 METRIC_BWD = "fused attention bwd TFLOP/s (bf16, 2.5x the forward FLOPs) and % of GB300 dense BF16 tensor peak"
 FALLBACK_PEAK_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["exact_attention_86_gb300/csrc/attn_fwd.cu", "exact_attention_86_gb300/csrc/sm103_ptx.cuh"]
 TRAFFIC_FILE = "profiles/attn_fwd_kernel_s8192_d128_traffic.md"
 L2_BYTES = 129 * 10**6
@@ -69,6 +70,27 @@ def recorded_traffic(workload: str):
     if not (src and wl and val) or src.group(1) != kernel_source_hash() or wl.group(1) != workload:
         return None
     return float(val.group(1))
+
+
+def roofline_bound(flops: float, min_bytes: int, launch_ms: float, peak_tflops: float, hbm_gbs: float,
+                   backward: bool = False) -> dict:
+    """The launch against its ceiling: the tensor cores when the arithmetic
+    intensity (FLOPs per algorithmic byte) is at or above the ridge of the two
+    peaks, HBM below it (a query block against long keys, the small shapes).
+    The backward reads and writes about twice the forward's bytes for 2.5 x
+    its FLOPs and is taken as tensor-bound."""
+    intensity = flops / min_bytes
+    ridge = peak_tflops * 1e12 / (hbm_gbs * 1e9)
+    if backward or intensity >= ridge:
+        achieved = flops / (launch_ms * 1e-3) / 1e12
+        out = {"bound": "tensor", "achieved": achieved, "peak": peak_tflops, "unit": "TFLOP/s"}
+    else:
+        achieved = min_bytes / (launch_ms * 1e-3) / 1e9
+        out = {"bound": "hbm", "achieved": achieved, "peak": hbm_gbs, "unit": "GB/s"}
+    out["frac"] = achieved / out["peak"]
+    out["intensity_flop_per_byte"] = intensity
+    out["ridge_flop_per_byte"] = ridge
+    return out
 
 
 def measured_peaks():
@@ -428,7 +450,8 @@ def main():
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (dQ, dK, dV) of the workload instead of the forward")
     ap.add_argument("--splits", type=int, default=0,
-                    help="use the split-KV forward with this many key ranges (0: the plain forward)")
+                    help="use the split-KV forward with this many key ranges (0: the plain forward; "
+                         "-1: attn.suggest_num_splits for the device)")
     args = ap.parse_args()
 
     from exact_attention_86_gb300 import workloads
@@ -452,6 +475,11 @@ def main():
         torch.cuda.set_device(local)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    if args.splits < 0:
+        if varlen:
+            raise SystemExit("--splits applies to padded workloads only")
+        args.splits = attn.suggest_num_splits(w.B, w.H, w.Sq, w.Sk,
+                                              torch.cuda.get_device_properties(dev).multi_processor_count)
 
     if rank == 0:
         build()
@@ -556,13 +584,18 @@ def main():
         # dense fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
         peak *= 2.0
         peak_src += " x 2 (nominal dense fp8 / bf16 ratio)"
-    achieved = step_flops / (launch_ms * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None if args.backward else recorded_traffic(w.name),
-                "kernel": "attn_bwd (delta, dq, dkdv kernels)" if args.backward else "attn_fwd_kernel",
-                "peak_source": peak_src,
-                "launch_ms": launch_ms, "algorithmic_flops_per_launch": step_flops,
-                "algorithmic_bytes_per_launch": w.min_bytes}
+    if peaks and peaks.get("hbm_gbs"):
+        hbm = float(peaks["hbm_gbs"])
+        hbm_src = "measured (MEASURED_PEAKS.json hbm_gbs, copy)"
+    else:
+        hbm = FALLBACK_HBM_GBS
+        hbm_src = "fallback (6.8 TB/s copy)"
+    roofline = roofline_bound(step_flops, w.min_bytes, launch_ms, peak, hbm, args.backward)
+    roofline["peak_source"] = peak_src if roofline["bound"] == "tensor" else hbm_src
+    roofline.update({"traffic": None if args.backward else recorded_traffic(w.name),
+                     "kernel": "attn_bwd (delta, dq, dkdv kernels)" if args.backward else "attn_fwd_kernel",
+                     "launch_ms": launch_ms, "algorithmic_flops_per_launch": step_flops,
+                     "algorithmic_bytes_per_launch": w.min_bytes})
 
     # ----------------------------------------------------------- CPU oracle
     cpu = None

@@ -207,14 +207,33 @@ def _check_qkv(q, k, v, kv_lens):
     return B, H, Sq, Sk, D, kv_ptr
 
 
-def forward_splitkv(q, k, v, num_splits: int, scale: Optional[float] = None, causal: bool = False,
-                    kv_lens=None, workspace=None):
-    """Split-KV forward on torch CUDA tensors (see ``forward``).  ``workspace``
-    (a CUDA tensor of at least ``attn_fwd_splitkv_workspace_size`` bytes) is
-    allocated with torch when not given."""
+MAX_SPLITS = 128  # attn_fwd_splitkv accepts 1 .. 128 key ranges
+
+
+def suggest_num_splits(B: int, H: int, Sq: int, Sk: int, num_sms: int) -> int:
+    """Key ranges for attn_fwd_splitkv that fill one wave of the GPU: with U
+    work units of 128 query rows, the largest S with U * S <= num_sms (at
+    least 1, at most one range per 128-key tile and MAX_SPLITS).  Shapes with
+    U >= num_sms gain nothing from splitting and get 1."""
+    units = B * H * ((Sq + 127) // 128)
+    if units <= 0 or units >= num_sms:
+        return 1
+    tiles = max((Sk + 127) // 128, 1)
+    return max(1, min(num_sms // units, tiles, MAX_SPLITS))
+
+
+def forward_splitkv(q, k, v, num_splits: Optional[int] = None, scale: Optional[float] = None,
+                    causal: bool = False, kv_lens=None, workspace=None):
+    """Split-KV forward on torch CUDA tensors (see ``forward``).
+    ``num_splits`` None picks ``suggest_num_splits`` for the device's SM
+    count.  ``workspace`` (a CUDA tensor of at least
+    ``attn_fwd_splitkv_workspace_size`` bytes) is allocated with torch when not
+    given."""
     import torch
 
     B, H, Sq, Sk, D, kv_ptr = _check_qkv(q, k, v, kv_lens)
+    if num_splits is None:
+        num_splits = suggest_num_splits(B, H, Sq, Sk, torch.cuda.get_device_properties(q.device).multi_processor_count)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     out = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=q.device)

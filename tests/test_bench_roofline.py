@@ -1,0 +1,57 @@
+"""The benchmark's roofline bound (host logic only)."""
+
+import os
+import sys
+
+import pytest
+
+sys.path.insert(0, os.path.join(os.path.dirname(__file__), ".."))
+import bench  # noqa: E402
+from exact_attention_86_gb300 import workloads  # noqa: E402
+
+PEAK, HBM = 1860.3, 6782.4   # TFLOP/s, GB/s
+
+
+@pytest.mark.parametrize("name,bound", [
+    ("s8192_d128", "tensor"), ("s8192_d128_causal", "tensor"), ("s32768_d128_causal", "tensor"),
+    ("s2048_d128_padded", "tensor"), ("q128_k32768_d128", "hbm"), ("s1024_d64_causal", "hbm"),
+    ("s128_d64", "hbm"),
+])
+def test_bound_follows_the_ridge(name, bound):
+    w = workloads.WORKLOADS[name]
+    r = bench.roofline_bound(w.flops, w.min_bytes, 1.0, PEAK, HBM)
+    assert r["bound"] == bound
+    assert (r["intensity_flop_per_byte"] >= r["ridge_flop_per_byte"]) == (bound == "tensor")
+
+
+def test_achieved_and_fraction_in_each_unit():
+    # 1 TFLOP and 1 GB in 1 ms: 1000 TFLOP/s, or 1000 GB/s
+    t = bench.roofline_bound(1e12, 10**8, 1.0, PEAK, HBM)        # 10^4 FLOP/B: tensor
+    assert t["unit"] == "TFLOP/s" and t["achieved"] == pytest.approx(1000.0)
+    assert t["frac"] == pytest.approx(1000.0 / PEAK)
+    h = bench.roofline_bound(1e9, 10**9, 1.0, PEAK, HBM)         # 1 FLOP/B: HBM
+    assert h["unit"] == "GB/s" and h["achieved"] == pytest.approx(1000.0)
+    assert h["frac"] == pytest.approx(1000.0 / HBM)
+
+
+def test_backward_is_taken_as_tensor_bound():
+    assert bench.roofline_bound(1e9, 10**9, 1.0, PEAK, HBM, backward=True)["bound"] == "tensor"
+
+
+# ---------------------------------------------------------- split-KV count
+from exact_attention_86_gb300 import attn  # noqa: E402
+
+
+@pytest.mark.parametrize("B,H,Sq,Sk,sms,expect", [
+    (1, 8, 128, 32768, 152, 19),     # 8 units: 19 ranges fill the 152 SMs once
+    (1, 8, 128, 1024, 152, 8),       # capped at one range per 128-key tile
+    (2, 16, 8192, 8192, 152, 1),     # 2048 units: no split
+    (1, 1, 1, 10**6, 152, 128),      # capped at the entry point's limit
+    (1, 152, 128, 4096, 152, 1),     # exactly one wave already
+    (0, 8, 128, 4096, 152, 1),       # empty batch
+])
+def test_suggested_splits(B, H, Sq, Sk, sms, expect):
+    s = attn.suggest_num_splits(B, H, Sq, Sk, sms)
+    assert s == expect
+    units = B * H * ((Sq + 127) // 128)
+    assert 1 <= s <= attn.MAX_SPLITS and (units == 0 or units * s <= max(sms, units))

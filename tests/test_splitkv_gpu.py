@@ -78,12 +78,17 @@ def test_splitkv_decode_like_long_context():
     B, H, Sq, Sk, D = 1, 8, 128, 32768, 128
     q, k, v, _ = _inputs(B, H, Sq, Sk, D, seed=17)
     scale = 1.0 / math.sqrt(D)
-    o, lse = _run_split(q, k, v, 16, scale, False, None)
-    rng = np.random.default_rng(17)
-    for h in (0, 5):
-        rows = sorted(set([0, 1, 64, 127] + [int(x) for x in rng.integers(0, Sq, 8)]))
-        o_ref, l_ref = attention_rows(_np(q[0, h]), _np(k[0, h]), _np(v[0, h]), rows, scale)
-        check(o[0, h, rows], lse[0, h, rows], o_ref, l_ref, f"decode-like h{h}")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # 16 ranges, and the suggested count (None: one wave of the SMs, 19 on 152)
+    for ns in (16, None):
+        o, lse = _run_split(q, k, v, ns, scale, False, None)
+        if ns is None:
+            assert attn.suggest_num_splits(B, H, Sq, Sk, sms) * H <= sms
+        rng = np.random.default_rng(17)
+        for h in (0, 5):
+            rows = sorted(set([0, 1, 64, 127] + [int(x) for x in rng.integers(0, Sq, 8)]))
+            o_ref, l_ref = attention_rows(_np(q[0, h]), _np(k[0, h]), _np(v[0, h]), rows, scale)
+            check(o[0, h, rows], lse[0, h, rows], o_ref, l_ref, f"decode-like h{h} splits {ns}")
 
 
 @pytest.mark.parametrize("D", [64, 128])
