@@ -43,7 +43,9 @@ from exact_attention_86_gb300 import attn  # noqa: E402
 
 
 @pytest.mark.parametrize("B,H,Sq,Sk,sms,expect", [
-    (1, 8, 128, 32768, 152, 19),     # 8 units: 19 ranges fill the 152 SMs once
+    (1, 8, 128, 32768, 152, 16),     # 8 units: at most 19 ranges; 16 cut the 256 tiles evenly
+    (1, 8, 128, 128 * 19 * 3, 152, 19),  # 57 tiles: 19 even ranges
+    (1, 8, 128, 128 * 37, 152, 19),  # 37 tiles (prime): no even cut near 19, so 19
     (1, 8, 128, 1024, 152, 8),       # capped at one range per 128-key tile
     (2, 16, 8192, 8192, 152, 1),     # 2048 units: no split
     (1, 1, 1, 10**6, 152, 128),      # capped at the entry point's limit

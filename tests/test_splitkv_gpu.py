@@ -79,7 +79,7 @@ def test_splitkv_decode_like_long_context():
     q, k, v, _ = _inputs(B, H, Sq, Sk, D, seed=17)
     scale = 1.0 / math.sqrt(D)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    # 16 ranges, and the suggested count (None: one wave of the SMs, 19 on 152)
+    # 16 ranges, and the suggested count (None: within one wave of the SMs)
     for ns in (16, None):
         o, lse = _run_split(q, k, v, ns, scale, False, None)
         if ns is None:
