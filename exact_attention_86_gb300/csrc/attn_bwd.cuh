@@ -84,8 +84,8 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restri
 
 // ------------------------------------------------------------------ dQ
 // A unit is 128 query rows of one (b, h); the keys stream past in steps of 64,
-// so that the S and dP of two steps fit in Tensor Memory beside the dQ
-// accumulator and the tensor cores compute the next step's products while the
+// so that the S and dP of three steps fit in Tensor Memory beside the dQ
+// accumulator and the tensor cores compute the next steps' products while the
 // elementwise warps form dS.
 constexpr int kBKDq = 64;  // keys per step
 
@@ -101,10 +101,12 @@ struct GeoDq {
   static constexpr int kOffDo = kOffQ + kTileQ;
   static constexpr int kOffRing = kOffDo + kTileQ;
   static constexpr int kSmemBytes = kOffRing + kSlots * 2 * kTileK + 1024;
-  // TMEM: step parity b holds S at [128 b, 128 b + 64) and dP at
-  // [128 b + 64, 128 b + 128); each half of the elementwise warps writes dS
-  // (bf16 pairs) over the first 16 of the 32 S columns it has read.  dQ at 256.
-  static constexpr uint32_t kTmemDq = 256;
+  // TMEM: step buffer b = step % kBufs holds S at [128 b, 128 b + 64) and dP
+  // at [128 b + 64, 128 b + 128); each half of the elementwise warps writes dS
+  // (bf16 pairs) over the first 16 of the 32 S columns it has read.  dQ at
+  // 128 kBufs.
+  static constexpr int kBufs = 3;
+  static constexpr uint32_t kTmemDq = 128 * kBufs;
   static __device__ __forceinline__ uint32_t st_col(uint32_t b) { return 128u * b; }
   // column of the dS operand of the kk-th dQ instruction (16 keys = 8
   // columns), relative to st_col: 2 instructions per half
@@ -117,9 +119,9 @@ static_assert(GeoDq<128>::kSmemBytes <= 232448 && GeoDq<64>::kSmemBytes <= 23244
 struct CtrlDq {
   uint64_t q_full, q_empty;
   uint64_t kv_full[8], kv_empty[8];
-  uint64_t st_full[2];   // S and dP of the step complete
-  uint64_t ds_full[2];   // dS written (8 warp arrivals)
-  uint64_t buf_free[2];  // the dQ product of the step completed: its TMEM buffer is free
+  uint64_t st_full[3];   // S and dP of the step complete (per step buffer)
+  uint64_t ds_full[3];   // dS written (8 warp arrivals)
+  uint64_t buf_free[3];  // the dQ product of the step completed: its TMEM buffer is free
   uint64_t dq_full;
   uint64_t drain[2];     // one per issuing warp
   uint32_t tmem_base;
@@ -166,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_kv_full0 + 8 * s, 1);
       mbar_init(bar_kv_empty0 + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < G::kBufs; ++b) {
       mbar_init(bar_st_full0 + 8 * b, 1);
       mbar_init(bar_ds_full0 + 8 * b, kSoftmaxWarps);
       mbar_init(bar_buf_free0 + 8 * b, 1);
@@ -253,8 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     } else if (warp == kWarpQK) {
       // ---------------------------------------------------- S, dP issuer
-      // Per step t: S = Q K_t^T and dP = dO V_t^T into the buffer of its
-      // parity, once the dQ product of step t-2 has released it.
+      // Per step t: S = Q K_t^T and dP = dO V_t^T into step buffer t % kBufs,
+      // once the dQ product of step t - kBufs has released it.
       const uint32_t idesc_s = idesc_bf16_f32(kBQ, kBKDq, false, false);
       const uint32_t qa = base + G::kOffQ, da = base + G::kOffDo;
       uint32_t tcount = 0, qcount = 0;
@@ -268,14 +270,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++qcount;
         for (int j = 0; j < u.n; ++j) {
           const uint32_t tt = tcount + j;
-          const uint32_t b = tt & 1u;
+          const uint32_t b = tt % G::kBufs;
           const uint32_t slot = tt % G::kSlots;
           if (!wait_warp(bar_kv_full0 + 8 * slot, (tt / G::kSlots) & 1u, abort_flag, kSiteBwdKvFull, limit)) {
             ok = false;
             break;
           }
-          if (tt >= 2 &&
-              !wait_warp(bar_buf_free0 + 8 * b, ((tt >> 1) - 1) & 1u, abort_flag, kSiteBwdSFree, limit)) {
+          if (tt >= static_cast<uint32_t>(G::kBufs) &&
+              !wait_warp(bar_buf_free0 + 8 * b, (tt / G::kBufs - 1) & 1u, abort_flag, kSiteBwdSFree, limit)) {
             ok = false;
             break;
           }
@@ -320,9 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (u.n == 0) continue;
         for (int j = 0; j < u.n; ++j) {
           const uint32_t tt = tcount + j;
-          const uint32_t b = tt & 1u;
+          const uint32_t b = tt % G::kBufs;
           const uint32_t slot = tt % G::kSlots;
-          if (!wait_warp(bar_ds_full0 + 8 * b, (tt >> 1) & 1u, abort_flag, kSiteBwdDsFull, limit)) {
+          if (!wait_warp(bar_ds_full0 + 8 * b, (tt / G::kBufs) & 1u, abort_flag, kSiteBwdDsFull, limit)) {
             ok = false;
             break;
           }
@@ -343,9 +345,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit_elect(bar_d);
       wait_phase_drain(bar_d, 0);
       if (ok) {
-        for (uint32_t back = 1; back <= 2 && back <= tcount; ++back) {
+        for (uint32_t back = 1; back <= static_cast<uint32_t>(G::kBufs) && back <= tcount; ++back) {
           const uint32_t t = tcount - back;
-          wait_phase_drain(bar_buf_free0 + 8 * (t & 1u), (t >> 1) & 1u);
+          wait_phase_drain(bar_buf_free0 + 8 * (t % G::kBufs), (t / G::kBufs) & 1u);
         }
       }
     }
@@ -384,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool rows_tail = u.q0 + kBQ > p.Sq;
       for (int j = 0; j < u.n; ++j) {
         const uint32_t tt = tcount + j;
-        const uint32_t b = tt & 1u;
+        const uint32_t b = tt % G::kBufs;
         const int k0 = (u.j0 + j) * kBKDq;
         // key column c of this half is k0 + 32*half + c: valid below kv and,
         // causal, up to the row
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int climit = u.kv - k0;
         if (CAUSAL) climit = min(climit, row - k0 + 1);
         climit = live ? climit - 32 * half : 0;
-        if (!wait_warp(bar_st_full0 + 8 * b, (tt >> 1) & 1u, abort_flag, kSiteBwdSFull, limit)) { ok = false; break; }
+        if (!wait_warp(bar_st_full0 + 8 * b, (tt / G::kBufs) & 1u, abort_flag, kSiteBwdSFull, limit)) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t tS = tmem + lane_off + G::st_col(b) + 32u * half;
         uint32_t s[32], dp[32];

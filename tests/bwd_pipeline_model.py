@@ -5,7 +5,7 @@ Roles, as in the kernel: the TMA producer (K and V once per unit, then a ring
 of (Q_t, dO_t) pairs, one per 64-query step), the warp that issues S^T and
 dP^T, the warp that issues the dV and dK products, and the elementwise warps
 (one actor).  Tensor memory as in the kernel: two step
-buffers b = t & 1, each with an S^T half and a dP^T half; the elementwise
+buffers b = t % 2 (the dQ kernel: three, b = t % 3), each with an S^T half and a dP^T half; the elementwise
 warps read both and write P^T and dS^T over them; the dV product reads P^T
 (its commit releases the S^T half) and the dK product reads dS^T (its commit
 releases the dP^T half and the ring slot).  Per step t the first issuer
@@ -52,7 +52,8 @@ def run(units, slots, seed, mistake=None, kernel="dkdv"):
             B[name] = Bar(name, count)
         return B[name]
 
-    for b in (0, 1):
+    nbuf = 3 if dq else 2
+    for b in range(nbuf):
         for n in ("st_full", "pd_full", "s_free", "d_free"):
             bar(f"{n}{b}")
     for s in range(slots):
@@ -95,8 +96,8 @@ def run(units, slots, seed, mistake=None, kernel="dkdv"):
     work = [u for u in units if u > 0]
     slot_data = {}                    # ring slot -> step whose Q/dO it holds
     kv_data = [None]                  # unit whose K/V is resident
-    half_s = {0: None, 1: None}       # ("S", t) -> ("P", t) -> ("P", t, "done")
-    half_d = {0: None, 1: None}       # ("dP", t) -> ("dS", t) -> ("dS", t, "done")
+    half_s = {b: None for b in range(nbuf)}   # ("S", t) -> ("P", t) -> ("P", t, "done")
+    half_d = {b: None for b in range(nbuf)}   # ("dP", t) -> ("dS", t) -> ("dS", t, "done")
     acc = {"dv": ("free", -1), "dk": ("free", -1)}   # ("busy", unit, last step) / ("free", unit)
 
     def producer():
@@ -129,9 +130,9 @@ def run(units, slots, seed, mistake=None, kernel="dkdv"):
         tcount = 0
 
         def products(t, u, first):
-            b, slot = t & 1, t % slots
+            b, slot = t % nbuf, t % slots
             if mistake != "products_skip_pd_full":
-                yield lambda: bar(f"pd_full{b}").try_wait((t >> 1) & 1, t >> 1)
+                yield lambda: bar(f"pd_full{b}").try_wait((t // nbuf) & 1, t // nbuf)
 
             def dv_start(t=t, b=b, slot=slot, u=u, first=first):
                 assert half_s[b] == ("P", t), f"dV of step {t} reads S half {b} holding {half_s[b]}"
@@ -184,30 +185,30 @@ def run(units, slots, seed, mistake=None, kernel="dkdv"):
             yield lambda: bar("kv_full").try_wait(u & 1, u)
             for i in range(n):
                 tt = tcount + i
-                b, slot, use = tt & 1, tt % slots, tt >> 1
+                b, slot, use = tt % nbuf, tt % slots, tt // nbuf
                 yield lambda: bar(f"qd_full{slot}").try_wait((tt // slots) & 1, tt // slots)
-                if tt >= 2 and mistake != "s_skips_s_free":
+                if tt >= nbuf and mistake != "s_skips_s_free":
                     yield lambda: bar(f"s_free{b}").try_wait((use - 1) & 1, use - 1)
 
                 def s_start(tt=tt, b=b, slot=slot, u=u):
-                    assert half_s[b] in (None, ("P", tt - 2, "done")), f"S^T {tt} overwrites {half_s[b]}"
+                    assert half_s[b] in (None, ("P", tt - nbuf, "done")), f"S^T {tt} overwrites {half_s[b]}"
                     assert slot_data.get(slot) == tt and kv_data[0] == u, f"S^T {tt} reads the wrong Q or K"
 
                 def s_end(tt=tt, b=b, slot=slot, u=u):
                     assert slot_data.get(slot) == tt and kv_data[0] == u, f"Q or K changed under S^T {tt}"
-                    assert half_s[b] in (None, ("P", tt - 2, "done")), f"S^T {tt} lands on {half_s[b]}"
+                    assert half_s[b] in (None, ("P", tt - nbuf, "done")), f"S^T {tt} lands on {half_s[b]}"
                     half_s[b] = ("S", tt)
                 mma(s_start, s_end)
-                if tt >= 2 and mistake != "dp_skips_d_free" and not dq:
+                if tt >= nbuf and mistake != "dp_skips_d_free" and not dq:
                     yield lambda: bar(f"d_free{b}").try_wait((use - 1) & 1, use - 1)
 
                 def d_start(tt=tt, b=b, slot=slot, u=u):
-                    assert half_d[b] in (None, ("dS", tt - 2, "done")), f"dP^T {tt} overwrites {half_d[b]}"
+                    assert half_d[b] in (None, ("dS", tt - nbuf, "done")), f"dP^T {tt} overwrites {half_d[b]}"
                     assert slot_data.get(slot) == tt and kv_data[0] == u, f"dP^T {tt} reads the wrong dO or V"
 
                 def d_end(tt=tt, b=b, slot=slot, u=u):
                     assert slot_data.get(slot) == tt and kv_data[0] == u, f"dO or V changed under dP^T {tt}"
-                    assert half_d[b] in (None, ("dS", tt - 2, "done")), f"dP^T {tt} lands on {half_d[b]}"
+                    assert half_d[b] in (None, ("dS", tt - nbuf, "done")), f"dP^T {tt} lands on {half_d[b]}"
                     half_d[b] = ("dP", tt)
                 mma(d_start, d_end, [bar(f"st_full{b}")])
             if dq:   # Q and dO are done after the unit's last S and dP
@@ -220,8 +221,8 @@ def run(units, slots, seed, mistake=None, kernel="dkdv"):
         for u, n in enumerate(work):
             for i in range(n):
                 tt = tcount + i
-                b = tt & 1
-                yield lambda: bar(f"st_full{b}").try_wait((tt >> 1) & 1, tt >> 1)
+                b = tt % nbuf
+                yield lambda: bar(f"st_full{b}").try_wait((tt // nbuf) & 1, tt // nbuf)
                 assert half_s[b] == ("S", tt) and half_d[b] == ("dP", tt), \
                     f"step {tt} reads {half_s[b]}, {half_d[b]}"
                 half_s[b] = ("reading", tt)
