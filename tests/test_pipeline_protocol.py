@@ -15,7 +15,7 @@ def _units(seed):
 
 # packed and paged batches: K and V in rings of their own, each with its own
 # producer (bf16 D=128: 3 + 2 slots; bf16 D=64: 6 + 6)
-@pytest.mark.parametrize("p_in_s,rings", [(False, (3, 2)), (False, (6, 6)), (True, (6, 6))])
+@pytest.mark.parametrize("p_in_s,rings", [(False, (3, 2)), (False, (6, 6)), (True, (3, 2)), (True, (6, 6))])
 def test_split_ring_protocol_never_aliases_or_deadlocks(p_in_s, rings):
     for seed in range(400):
         run(_units(seed), 0, per_kind=False, seed=seed, p_in_s=p_in_s, rings=rings)
