@@ -71,7 +71,7 @@ def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False,
     ring of positions described above, filled by one producer.
     ``mistake`` plants one protocol error, for the tests that show the model
     catches it: "qk_skips_buffer_wait", "pv_skips_o_free",
-    "rescale_skips_p_free", "p_store_skips_p_free"."""
+    "rescale_skips_p_free", "p_store_skips_p_free", "producer_skips_kv_empty"."""
     rng = random.Random(seed)
     B = {}
 
@@ -148,7 +148,8 @@ def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False,
                         ring += 1
                         continue
                     slot, use = slot_of(ring), empty_use(ring)
-                    yield lambda: bar(f"kv_empty{slot}").try_wait((use & 1) ^ 1, use - 1)
+                    if mistake != "producer_skips_kv_empty":
+                        yield lambda: bar(f"kv_empty{slot}").try_wait((use & 1) ^ 1, use - 1)
                     f = full_bar(ring)
                     f.arrive(tx=1)
                     slot_data[slot] = None

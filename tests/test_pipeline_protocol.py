@@ -23,7 +23,7 @@ def test_split_ring_protocol_never_aliases_or_deadlocks(p_in_s, rings):
 
 @pytest.mark.parametrize("p_in_s,mistake", [
     (False, "qk_skips_buffer_wait"), (False, "p_store_skips_p_free"), (False, "rescale_skips_p_free"),
-    (True, "qk_skips_buffer_wait"), (True, "rescale_skips_p_free"),
+    (True, "qk_skips_buffer_wait"), (True, "rescale_skips_p_free"), (False, "producer_skips_kv_empty"),
 ])
 def test_model_with_split_rings_catches_a_skipped_wait(p_in_s, mistake):
     failures = 0
@@ -46,7 +46,7 @@ def test_single_ring_protocol_never_aliases_or_deadlocks(p_in_s, slots):
 
 @pytest.mark.parametrize("p_in_s,mistake", [
     (False, "qk_skips_buffer_wait"), (False, "p_store_skips_p_free"), (False, "rescale_skips_p_free"),
-    (True, "qk_skips_buffer_wait"), (True, "rescale_skips_p_free"),
+    (True, "qk_skips_buffer_wait"), (True, "rescale_skips_p_free"), (False, "producer_skips_kv_empty"),
 ])
 def test_model_catches_a_skipped_wait(p_in_s, mistake):
     """The model has teeth: leaving out any one of the waits that guard the
