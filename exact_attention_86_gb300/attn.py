@@ -54,6 +54,7 @@ SIGNATURES = {
                                       ctypes.c_void_p, ctypes.c_void_p]),
     "attn_fwd_splitkv_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                           ctypes.c_int]),
+    "attn_fwd_splitkv_suggest_splits": (ctypes.c_int, [ctypes.c_int] * 5),
     "attn_fwd_splitkv": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                         ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
@@ -136,6 +137,10 @@ def attn_fwd_splitkv_workspace_size(B: int, H: int, Sq: int, D: int, num_splits:
     return lib().attn_fwd_splitkv_workspace_size(B, H, Sq, D, num_splits)
 
 
+def attn_fwd_splitkv_suggest_splits(B: int, H: int, Sq: int, Sk: int, num_sms: int) -> int:
+    return lib().attn_fwd_splitkv_suggest_splits(B, H, Sq, Sk, num_sms)
+
+
 def attn_fwd_splitkv(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
                      scale: float, causal: int, kv_lens: Optional[int], num_splits: int, workspace: int,
                      workspace_bytes: int, stream: Optional[int]) -> int:
@@ -211,21 +216,10 @@ MAX_SPLITS = 128  # attn_fwd_splitkv accepts 1 .. 128 key ranges
 
 
 def suggest_num_splits(B: int, H: int, Sq: int, Sk: int, num_sms: int) -> int:
-    """Key ranges for attn_fwd_splitkv within one wave of the GPU.  With U work
-    units of 128 query rows, at most S_max = num_sms // U ranges (and at most
-    one per 128-key tile, and MAX_SPLITS) fit one wave; of those the largest S
-    that cuts the tiles into equal ranges, unless that is below S_max / 2 (the
-    tile count has no divisor near S_max), in which case S_max.  Shapes with
-    U >= num_sms gain nothing from splitting and get 1.  (Measured on 8 query
-    blocks against 32768 keys: 16 equal ranges 45.3 us, 19 ranges of 13-14
-    tiles 46.4 us.)"""
-    units = B * H * ((Sq + 127) // 128)
-    if units <= 0 or units >= num_sms:
-        return 1
-    tiles = max((Sk + 127) // 128, 1)
-    s_max = max(1, min(num_sms // units, tiles, MAX_SPLITS))
-    even = max(s for s in range(1, s_max + 1) if tiles % s == 0)
-    return even if 2 * even >= s_max else s_max
+    """Key ranges for attn_fwd_splitkv on a GPU with num_sms SMs (the
+    library's attn_fwd_splitkv_suggest_splits: within one wave of SMs, equal
+    ranges preferred)."""
+    return attn_fwd_splitkv_suggest_splits(B, H, Sq, Sk, num_sms)
 
 
 def forward_splitkv(q, k, v, num_splits: Optional[int] = None, scale: Optional[float] = None,

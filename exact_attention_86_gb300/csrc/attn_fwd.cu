@@ -1607,6 +1607,27 @@ size_t attn_fwd_splitkv_workspace_size(int B, int H, int Sq, int D, int num_spli
   return splitkv_bytes(B, H, Sq, D, num_splits, nullptr);
 }
 
+// Equal ranges matter because the slowest range sets the time: on 8 query
+// blocks against 32768 keys (256 tiles) on 152 SMs, 16 equal ranges took
+// 45.3 us and 19 ranges of 13-14 tiles 46.4 us (merge included).
+int attn_fwd_splitkv_suggest_splits(int B, int H, int Sq, int Sk, int num_sms) {
+  if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || num_sms < 1) return 0;
+  const int64_t units = static_cast<int64_t>(B) * H * ((static_cast<int64_t>(Sq) + kBQ - 1) / kBQ);
+  if (units == 0 || units >= num_sms) return 1;
+  const int64_t tiles = Sk > 0 ? (static_cast<int64_t>(Sk) + kBK - 1) / kBK : 1;
+  int64_t s_max = num_sms / units;
+  if (s_max > tiles) s_max = tiles;
+  if (s_max > kMaxSplits) s_max = kMaxSplits;
+  if (s_max < 1) s_max = 1;
+  int64_t even = 1;
+  for (int64_t s = s_max; s >= 1; --s)
+    if (tiles % s == 0) {
+      even = s;
+      break;
+    }
+  return static_cast<int>(2 * even >= s_max ? even : s_max);
+}
+
 attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
                              int Sk, int D, float scale, int causal, const int32_t* kv_lens, int num_splits,
                              void* workspace, size_t workspace_bytes, attn_stream_t stream) {

@@ -199,6 +199,18 @@ attn_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cac
  */
 size_t attn_fwd_splitkv_workspace_size(int B, int H, int Sq, int D, int num_splits);
 
+/*
+ * attn_fwd_splitkv_suggest_splits — a key-range count for attn_fwd_splitkv on
+ * a GPU with `num_sms` SMs.  With U = B * H * ceil(Sq / 128) units of work, at
+ * most S_max = num_sms / U ranges (capped by the number of 128-key tiles and
+ * by 128) keep the units within one wave of SMs; the result is the largest
+ * S <= S_max that cuts the tiles into equal ranges, unless that is below
+ * S_max / 2 (then S_max).  Returns 1 when U >= num_sms (splitting gains
+ * nothing) or when a size is 0, and 0 for a negative size or num_sms < 1.
+ * Host arithmetic only: no CUDA call, no device needed.
+ */
+int attn_fwd_splitkv_suggest_splits(int B, int H, int Sq, int Sk, int num_sms);
+
 attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
                              int Sk, int D, float scale, int causal, const int32_t* kv_lens, int num_splits,
                              void* workspace, size_t workspace_bytes, attn_stream_t stream);
@@ -289,7 +301,7 @@ attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream);
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 8
+#define ATTN_ABI_VERSION 9
 
 #ifdef __cplusplus
 }

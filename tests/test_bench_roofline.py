@@ -40,6 +40,13 @@ def test_backward_is_taken_as_tensor_bound():
 
 # ---------------------------------------------------------- split-KV count
 from exact_attention_86_gb300 import attn  # noqa: E402
+from exact_attention_86_gb300.build import build  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def _lib():
+    build()   # host-only entry point: the library loads and runs without a GPU
+    attn.lib()
 
 
 @pytest.mark.parametrize("B,H,Sq,Sk,sms,expect", [
@@ -52,8 +59,32 @@ from exact_attention_86_gb300 import attn  # noqa: E402
     (1, 152, 128, 4096, 152, 1),     # exactly one wave already
     (0, 8, 128, 4096, 152, 1),       # empty batch
 ])
-def test_suggested_splits(B, H, Sq, Sk, sms, expect):
+def test_suggested_splits(_lib, B, H, Sq, Sk, sms, expect):
     s = attn.suggest_num_splits(B, H, Sq, Sk, sms)
     assert s == expect
     units = B * H * ((Sq + 127) // 128)
     assert 1 <= s <= attn.MAX_SPLITS and (units == 0 or units * s <= max(sms, units))
+
+
+def test_suggested_splits_rejects_negative_sizes(_lib):
+    for args in [(-1, 8, 128, 4096, 152), (1, 8, -1, 4096, 152), (1, 8, 128, -5, 152), (1, 8, 128, 4096, 0)]:
+        assert attn.attn_fwd_splitkv_suggest_splits(*args) == 0
+
+
+def test_suggested_splits_against_a_direct_search(_lib):
+    # the rule written as a search: among S <= S_max, the largest even cut
+    # unless it is below S_max / 2
+    import random
+    rng = random.Random(3)
+    for _ in range(300):
+        B, H, Sq, Sk, sms = rng.randint(1, 3), rng.randint(1, 16), rng.randint(1, 600), rng.randint(1, 70000), \
+            rng.choice([132, 148, 152, 160])
+        units = B * H * -(-Sq // 128)
+        tiles = -(-Sk // 128)
+        if units >= sms:
+            want = 1
+        else:
+            s_max = max(1, min(sms // units, tiles, 128))
+            even = max(s for s in range(1, s_max + 1) if tiles % s == 0)
+            want = even if 2 * even >= s_max else s_max
+        assert attn.suggest_num_splits(B, H, Sq, Sk, sms) == want, (B, H, Sq, Sk, sms)
