@@ -212,6 +212,23 @@ def _check_qkv(q, k, v, kv_lens):
     return B, H, Sq, Sk, D, kv_ptr
 
 
+def _outputs(out, lse, o_shape, lse_shape, device):
+    """The caller's output tensors (checked) or new ones."""
+    import torch
+
+    if out is None:
+        out = torch.empty(o_shape, dtype=torch.bfloat16, device=device)
+    elif out.dtype != torch.bfloat16 or out.device != device or not out.is_contiguous() \
+            or tuple(out.shape) != tuple(o_shape):
+        raise ValueError(f"out must be a contiguous bf16 tensor {tuple(o_shape)} on the inputs' device")
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=device)
+    elif lse.dtype != torch.float32 or lse.device != device or not lse.is_contiguous() \
+            or tuple(lse.shape) != tuple(lse_shape):
+        raise ValueError(f"lse must be a contiguous fp32 tensor {tuple(lse_shape)} on the inputs' device")
+    return out, lse
+
+
 MAX_SPLITS = 128  # attn_fwd_splitkv accepts 1 .. 128 key ranges
 
 
@@ -252,11 +269,11 @@ def forward_splitkv(q, k, v, num_splits: Optional[int] = None, scale: Optional[f
 
 
 def forward_fp8(q8, k8, v8_t, q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0,
-                scale: Optional[float] = None, causal: bool = False, kv_lens=None):
+                scale: Optional[float] = None, causal: bool = False, kv_lens=None, out=None, lse=None):
     """FP8 forward on torch CUDA tensors of E4M3 codes (``torch.uint8`` or
     ``torch.float8_e4m3fn``): ``q8 [B,H,Sq,D]``, ``k8 [B,H,Sk,D]`` and
     ``v8_t [B,H,D,Sk]`` (V transposed).  Returns ``(o bf16 [B,H,Sq,D],
-    lse fp32 [B,H,Sq])``."""
+    lse fp32 [B,H,Sq])``, written into ``out`` / ``lse`` when given."""
     import torch
 
     for name, t in (("q8", q8), ("k8", k8), ("v8_t", v8_t)):
@@ -270,8 +287,7 @@ def forward_fp8(q8, k8, v8_t, q_descale: float = 1.0, k_descale: float = 1.0, v_
         raise ValueError("kv_lens must be int32 on q's device")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    out = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=q8.device)
-    lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q8.device)
+    out, lse = _outputs(out, lse, (B, H, Sq, D), (B, H, Sq), q8.device)
     with torch.cuda.device(q8.device):
         stream = torch.cuda.current_stream(q8.device).cuda_stream
         st = attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8_t.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Sq,
@@ -300,10 +316,11 @@ def tile_counter(device, stream: int):
 
 
 def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, scale: Optional[float] = None,
-                   causal: bool = False, dynamic: bool = True):
+                   causal: bool = False, dynamic: bool = True, out=None, lse=None):
     """Packed variable-length forward on torch CUDA tensors: ``q [total_q, H, D]``,
     ``k``/``v [total_k, H, D]`` bf16, ``cu_seqlens_q``/``cu_seqlens_k`` int32
-    ``[batch + 1]`` on the same device.  Returns ``(o [total_q, H, D], lse [H, total_q])``."""
+    ``[batch + 1]`` on the same device.  Returns ``(o [total_q, H, D], lse [H, total_q])``,
+    written into ``out`` / ``lse`` when given."""
     import torch
 
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -321,8 +338,7 @@ def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, scale
         raise ValueError("cu_seqlens_q and cu_seqlens_k must have the same length")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    out = torch.empty((total_q, H, D), dtype=torch.bfloat16, device=q.device)
-    lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    out, lse = _outputs(out, lse, (total_q, H, D), (H, total_q), q.device)
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         counter = tile_counter(q.device, stream).data_ptr() if dynamic else None
@@ -335,12 +351,13 @@ def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, scale
 
 
 def forward_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, max_seqlen_q: int,
-                  scale: Optional[float] = None, causal: bool = False, dynamic: bool = True):
+                  scale: Optional[float] = None, causal: bool = False, dynamic: bool = True, out=None, lse=None):
     """Packed queries ``q [total_q, H, D]`` against a paged KV cache
     ``k_cache``/``v_cache [num_pages, page_size, H, D]`` (bf16 CUDA tensors);
     ``cu_seqlens_q`` int32 ``[batch + 1]``, ``seqlens_k`` int32 ``[batch]``,
     ``block_table`` int32 ``[batch, max_pages_per_seq]`` on the same device.
-    Returns ``(o [total_q, H, D], lse [H, total_q])``."""
+    Returns ``(o [total_q, H, D], lse [H, total_q])``, written into ``out`` /
+    ``lse`` when given."""
     import torch
 
     if q.dtype != torch.bfloat16 or not q.is_cuda or not q.is_contiguous() or q.dim() != 3:
@@ -361,8 +378,7 @@ def forward_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, max
         raise ValueError("seqlens_k and block_table must have one entry (row) per sequence")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    out = torch.empty((total_q, H, D), dtype=torch.bfloat16, device=q.device)
-    lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    out, lse = _outputs(out, lse, (total_q, H, D), (H, total_q), q.device)
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         counter = tile_counter(q.device, stream).data_ptr() if dynamic else None
@@ -450,10 +466,7 @@ def forward(q, k, v, scale: Optional[float] = None, causal: bool = False, kv_len
                 or not kv_lens.is_contiguous():
             raise ValueError("kv_lens must be a contiguous int32 tensor [B] on q's device")
         kv_ptr = kv_lens.data_ptr()
-    if out is None:
-        out = torch.empty((B, H, Sq, D), dtype=torch.bfloat16, device=q.device)
-    if lse is None:
-        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    out, lse = _outputs(out, lse, (B, H, Sq, D), (B, H, Sq), q.device)
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),

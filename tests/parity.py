@@ -32,3 +32,30 @@ def check(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     lerr = np.abs(lse_gpu[~empty] - lse_ref[~empty])
     assert lerr.size == 0 or lerr.max() <= LSE_ATOL, f"{what}: LSE max abs err {lerr.max():.3e}"
     return float(err.max()) if err.size else 0.0, float(lerr.max()) if lerr.size else 0.0
+
+
+def tile_rows(n_rows, rng, tile=128):
+    """Query rows to compare in a full-size output: the first and the last row
+    of EVERY 128-row query tile (the kernel's work unit) plus one random row
+    inside each tile, so that a unit the schedule skips or runs twice shows up
+    in the comparison, not only in a whole-output NaN check."""
+    rows = []
+    for t0 in range(0, n_rows, tile):
+        t1 = min(t0 + tile, n_rows)
+        rows.extend({t0, t1 - 1, int(rng.integers(t0, t1))})
+    return sorted(rows)
+
+
+def nan_filled(shape, dtype, device):
+    """An output buffer whose every element is NaN before the call: any element
+    that the kernel leaves unwritten stays NaN and fails the checks."""
+    import torch
+    return torch.full(shape, float("nan"), dtype=dtype, device=device)
+
+
+def assert_no_nan(*tensors, what=""):
+    """Every element was written: none of the NaN fill survives."""
+    import torch
+    for t in tensors:
+        n = int(torch.isnan(t.float()).sum())
+        assert n == 0, f"{what}: {n} elements still hold the NaN fill (a work unit was not written)"

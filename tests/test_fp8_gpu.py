@@ -29,6 +29,8 @@ from exact_attention_86_gb300 import attn, workloads
 from exact_attention_86_gb300.build import build
 from oracle import attention_fp8_ref, attention_rows, decode_e4m3
 
+from parity import assert_no_nan, nan_filled, tile_rows
+
 pytestmark = pytest.mark.gpu
 
 
@@ -144,26 +146,32 @@ def test_fp8_negative_scale():
 
 
 @pytest.mark.parametrize("name", sorted(workloads.FP8_WORKLOADS))
-def test_fp8_workload_sampled(name):
+def test_fp8_workload_every_tile(name):
     """The benchmarked FP8 workload at full size, in the benchmark's launch
-    configuration: sampled rows of two heads against the oracle."""
+    configuration, into NaN-filled outputs: no NaN may survive, and the first,
+    last and one random row of every (batch entry, head, 128-row query tile)
+    must match the oracle."""
     w = workloads.FP8_WORKLOADS[name]
     q, k, v, vt, kv = workloads.generate_fp8(w)
     dev = torch.device("cuda:0")
-    o, lse = attn.forward_fp8(q.to(dev), k.to(dev), vt.to(dev), w.descale, w.descale, w.descale, scale=w.scale,
-                              causal=w.causal)
+    o = nan_filled((w.B, w.H, w.Sq, w.D), torch.bfloat16, dev)
+    lse = nan_filled((w.B, w.H, w.Sq), torch.float32, dev)
+    attn.forward_fp8(q.to(dev), k.to(dev), vt.to(dev), w.descale, w.descale, w.descale, scale=w.scale,
+                     causal=w.causal, out=o, lse=lse)
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
+    assert_no_nan(o, lse, what=name)
     o = o.float().cpu().numpy()
     lse = lse.cpu().numpy()
     rng = np.random.default_rng(7)
-    for b, h in ((0, 0), (w.B - 1, w.H - 1)):
-        rows = sorted(set([0, 1, 127, 128, w.Sq - 1] + [int(x) for x in rng.integers(0, w.Sq, 27)]))
-        qh, kh, vh = (decode_e4m3(t[b, h].numpy()) * w.descale for t in (q, k, v))
-        o_ref, l_ref = attention_rows(qh, kh, vh, rows, w.scale, causal=w.causal)
-        a_ref, _ = attention_rows(qh, kh, np.abs(vh), rows, w.scale, causal=w.causal)
-        check_fp8(o[b, h, rows], lse[b, h, rows], o_ref, l_ref, a_ref, float(np.abs(vh).max()),
-                  f"{name} b{b} h{h}")
+    for b in range(w.B):
+        for h in range(w.H):
+            rows = tile_rows(w.Sq, rng)
+            qh, kh, vh = (decode_e4m3(t[b, h].numpy()) * w.descale for t in (q, k, v))
+            o_ref, l_ref = attention_rows(qh, kh, vh, rows, w.scale, causal=w.causal)
+            a_ref, _ = attention_rows(qh, kh, np.abs(vh), rows, w.scale, causal=w.causal)
+            check_fp8(o[b, h, rows], lse[b, h, rows], o_ref, l_ref, a_ref, float(np.abs(vh).max()),
+                      f"{name} b{b} h{h}")
 
 
 def test_fp8_repeated_launches_are_bitwise_identical():

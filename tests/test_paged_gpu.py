@@ -10,7 +10,7 @@ from exact_attention_86_gb300 import attn
 from exact_attention_86_gb300.build import build
 from oracle import attention_paged_ref
 
-from parity import check
+from parity import assert_no_nan, check, nan_filled
 
 pytestmark = pytest.mark.gpu
 
@@ -117,7 +117,8 @@ def test_paged_benchmark_workload_equals_varlen_bitwise():
     """The benchmarked paged batch at full size, in the benchmark's launch
     configuration: the shuffled pages hold the same tokens as the packed batch
     (whose parity against the oracle is tested at full size), and the kernel
-    stages the same tiles either way, so the bits must agree."""
+    stages the same tiles either way, so the bits must agree.  Both outputs
+    are NaN-filled before the calls."""
     from exact_attention_86_gb300 import workloads
 
     w = workloads.PAGED_WORKLOADS["paged_b32_d128_causal"]
@@ -126,11 +127,18 @@ def test_paged_benchmark_workload_equals_varlen_bitwise():
     assert torch.equal(cu, cu2)
     dev = torch.device("cuda:0")
     qd, cud = q.to(dev), cu.to(dev)
-    o_p, l_p = attn.forward_paged(qd, kc.to(dev), vc.to(dev), cud, sk.to(dev), table.to(dev), w.max_len,
-                                  causal=w.causal)
-    o_v, l_v = attn.forward_varlen(qd, k.to(dev), v.to(dev), cud, cud, w.max_len, causal=w.causal)
+    total = q.shape[0]
+    # both outputs start as NaN, so an element that either schedule leaves
+    # unwritten cannot compare equal to a stale value
+    o_p, o_v = (nan_filled((total, w.H, w.D), torch.bfloat16, dev) for _ in range(2))
+    l_p, l_v = (nan_filled((w.H, total), torch.float32, dev) for _ in range(2))
+    attn.forward_paged(qd, kc.to(dev), vc.to(dev), cud, sk.to(dev), table.to(dev), w.max_len, causal=w.causal,
+                       out=o_p, lse=l_p)
+    attn.forward_varlen(qd, k.to(dev), v.to(dev), cud, cud, w.max_len, causal=w.causal, out=o_v, lse=l_v)
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
+    assert_no_nan(o_p, l_p, what="paged")
+    assert_no_nan(o_v, l_v, what="packed")
     assert torch.equal(o_p.view(torch.int16), o_v.view(torch.int16))
     assert torch.equal(l_p, l_v)
 

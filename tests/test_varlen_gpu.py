@@ -10,7 +10,7 @@ from exact_attention_86_gb300 import attn
 from exact_attention_86_gb300.build import build
 from oracle import attention_varlen_ref
 
-from parity import check
+from parity import assert_no_nan, check, nan_filled, tile_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -111,24 +111,35 @@ def test_varlen_equals_padded_forward_for_equal_lengths():
 
 
 @pytest.mark.parametrize("name", ["varlen_b32_d128_causal", "varlen_b32_d128"])
-def test_varlen_benchmark_workload_sampled(name):
+def test_varlen_benchmark_workload_every_tile(name):
     """The benchmarked packed batch at full size, in the benchmark's launch
-    configuration; sampled rows of the shortest, the longest and two other
-    sequences on the first and last head against the oracle."""
+    configuration (dynamic schedule for the non-causal batch), into NaN-filled
+    outputs: no NaN may survive, and the first, last and one random row of
+    every (sequence, head, 128-row query tile) must match the oracle."""
     from exact_attention_86_gb300 import workloads
     from oracle import attention_rows
 
     w = workloads.VARLEN_WORKLOADS[name]
     q, k, v, cu = workloads.generate_varlen(w)
-    o, lse = _run(q, k, v, cu, cu, w.max_len, w.scale, w.causal)
-    lens = (cu[1:] - cu[:-1]).numpy()
-    picks = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 3, 17})
+    dev = torch.device("cuda:0")
+    total = q.shape[0]
+    o = nan_filled((total, w.H, w.D), torch.bfloat16, dev)
+    lse = nan_filled((w.H, total), torch.float32, dev)
+    cud = cu.to(dev)
+    attn.forward_varlen(q.to(dev), k.to(dev), v.to(dev), cud, cud, w.max_len, scale=w.scale, causal=w.causal,
+                        out=o, lse=lse)
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, (st, site)
+    assert_no_nan(o, lse, what=name)
+    o = o.float().cpu().numpy()
+    lse = lse.cpu().numpy()
     rng = np.random.default_rng(5)
-    for b in picks:
+    for b in range(w.batch):
         a, e = int(cu[b]), int(cu[b + 1])
-        n = e - a
-        rows = sorted(set(rng.integers(0, n, size=min(n, 24)).tolist()) | {0, n - 1})
-        for h in (0, w.H - 1):
+        if e == a:
+            continue
+        for h in range(w.H):
+            rows = tile_rows(e - a, rng)
             o_ref, l_ref = attention_rows(_np(q[a:e, h]), _np(k[a:e, h]), _np(v[a:e, h]), rows, w.scale,
                                           causal=w.causal)
             check(o[a:e, h][rows], lse[h, a:e][rows], o_ref, l_ref, f"{name} seq {b} head {h}")
