@@ -44,7 +44,10 @@ METRIC = "fused attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor pe
 METRIC_BWD = "fused attention bwd TFLOP/s (bf16, 2.5x the forward FLOPs) and % of GB300 dense BF16 tensor peak"
 FALLBACK_PEAK_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["exact_attention_86_gb300/csrc/attn_fwd.cu", "exact_attention_86_gb300/csrc/sm103_ptx.cuh"]
+# every source file of the translation unit that holds the forward kernel
+# (attn_fwd.cu includes the PTX wrappers and the backward kernels)
+KERNEL_SOURCES = ["exact_attention_86_gb300/csrc/attn_fwd.cu", "exact_attention_86_gb300/csrc/sm103_ptx.cuh",
+                  "exact_attention_86_gb300/csrc/attn_bwd.cuh", "include/attn.h"]
 TRAFFIC_FILE = "profiles/attn_fwd_kernel_s8192_d128_traffic.md"
 L2_BYTES = 129 * 10**6
 

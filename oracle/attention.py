@@ -23,7 +23,7 @@ What it computes (one head ``(b, h)``, one query row ``i``):
   break": a fully masked tile must not poison the result with NaN) has
   ``O_i = +0.0`` in every column and ``LSE_i = -inf``.
 
-Readings where the pages are silent (each one is listed in the design doc):
+Readings where the pages are silent:
 
 * causal alignment is top-left: key ``j`` is masked for query ``i`` when
   ``j > i``, for any ``Sq`` and ``Sk``;

@@ -5,6 +5,8 @@ documented codes before touching CUDA."""
 import ctypes
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -87,12 +89,24 @@ def test_argument_checks(lib, args, code):
 
 
 def test_no_silent_success_without_gpu(lib):
-    import torch
-    if torch.cuda.is_available():
-        pytest.skip("a GPU is present")
-    st = attn.attn_fwd(A, A, A, A, A, 1, 1, 128, 128, 64, 0.125, 0, None, None)
+    # The calls run in a child process that sees no device at all
+    # (CUDA_VISIBLE_DEVICES empty), so whatever machine runs this test, the
+    # shapes below, which pass every host-side check, can never reach a launch
+    # with the dummy addresses: the library must report an error instead of
+    # success.
+    code = (
+        "import sys; sys.path.insert(0, %r)\n"
+        "from exact_attention_86_gb300 import attn\n"
+        "A = 1 << 20\n"
+        "st = attn.attn_fwd(A, A, A, A, A, 1, 1, 128, 128, 64, 0.125, 0, None, None)\n"
+        "sf = attn.attn_selftest_wait_timeout(1000, None)\n"
+        "print(st, sf)\n" % ROOT)
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr
+    st, sf = (int(x) for x in out.stdout.split())
     assert st in (attn.ATTN_ERR_CUDA, attn.ATTN_ERR_UNSUPPORTED_DEVICE)
-    assert attn.attn_selftest_wait_timeout(1000, None) in (attn.ATTN_ERR_CUDA, attn.ATTN_ERR_UNSUPPORTED_DEVICE)
+    assert sf in (attn.ATTN_ERR_CUDA, attn.ATTN_ERR_UNSUPPORTED_DEVICE)
 
 
 def test_selftest_limit_checked(lib):
