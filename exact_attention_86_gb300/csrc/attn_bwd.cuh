@@ -917,11 +917,11 @@ attn_status launch_bwd(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CU
   auto kk = bwd_dkdv_kernel<D, CAUSAL>;
   constexpr int smem_q = GeoDq<D>::kSmemBytes;
   constexpr int smem_k = GeoKv<D>::kSmemBytes;
-  if (!dev.bwd_smem_set[idx]) {
+  if (!dev.bwd_smem_set[idx].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q) != cudaSuccess ||
         cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_k) != cudaSuccess)
       return ATTN_ERR_CUDA;
-    dev.bwd_smem_set[idx] = true;
+    dev.bwd_smem_set[idx].store(true, std::memory_order_release);
   }
   if (bq.f.total_units > 0) {
     const int grid = bq.f.total_units < dev.num_sms ? bq.f.total_units : dev.num_sms;

@@ -40,6 +40,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "attn.h"
@@ -1116,9 +1117,10 @@ struct DeviceInfo {
   int initialised = 0;
   int supported = 0;
   int num_sms = 0;
-  bool smem_set[10] = {};
-  bool bwd_smem_set[4] = {false, false, false, false};
-  void* scratch = nullptr;  // this device's address of g_splitkv_scratch
+  // dynamic shared memory attribute set for kernel instantiation i (set at
+  // most once; two host threads may both set it, which is harmless)
+  std::atomic<bool> smem_set[12] = {};
+  std::atomic<bool> bwd_smem_set[4] = {};
 };
 constexpr int kMaxDevices = 64;
 DeviceInfo g_dev[kMaxDevices];
@@ -1235,10 +1237,10 @@ attn_status launch(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CUtens
                    const Params& p, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D, CAUSAL, FP8, SPLIT>;
   constexpr int smem = Geo<D, FP8>::kSmemBytes;
-  if (!dev.smem_set[idx]) {
+  if (!dev.smem_set[idx].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return ATTN_ERR_CUDA;
-    dev.smem_set[idx] = true;
+    dev.smem_set[idx].store(true, std::memory_order_release);
   }
   const int grid = p.total_units < dev.num_sms ? p.total_units : dev.num_sms;
   kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
@@ -1659,15 +1661,13 @@ attn_status attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v
   DeviceInfo* dev = nullptr;
   st = device_info(&dev);
   if (st != ATTN_OK) return st;
+  // The array exists once per CUDA context, and in host code its name is
+  // only a stand-in: the device address is looked up in the current context
+  // on every call (a host-side query that allocates nothing), so a context
+  // made current after a reset or by the caller is never given another
+  // context's address.
   void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lock(g_dev_mutex);
-    if (dev->scratch == nullptr && cudaGetSymbolAddress(&dev->scratch, g_splitkv_scratch) != cudaSuccess) {
-      dev->scratch = nullptr;
-      return ATTN_ERR_CUDA;
-    }
-    scratch = dev->scratch;
-  }
+  if (cudaGetSymbolAddress(&scratch, g_splitkv_scratch) != cudaSuccess || scratch == nullptr) return ATTN_ERR_CUDA;
   return attn_fwd_splitkv(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, num_splits, scratch,
                           static_cast<size_t>(ATTN_SPLITKV_SCRATCH_BYTES), stream);
 }

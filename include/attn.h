@@ -25,9 +25,9 @@
  * All entry points are host functions; device pointers are plain CUDA device
  * (or managed) addresses on the CURRENT device.  The caller allocates and owns
  * every buffer (including the split-KV workspace).  The library allocates no
- * device memory: its only device state is one status word per device and the
- * fixed scratch of attn_fwd_splitkv_noalloc, static __device__ variables in
- * the library.
+ * device memory: its only device state is one status word and the fixed
+ * scratch of attn_fwd_splitkv_noalloc, static __device__ variables that exist
+ * once in every CUDA context that loads the library.
  */
 #ifndef EXACT_ATTENTION_86_GB300_ATTN_H
 #define EXACT_ATTENTION_86_GB300_ATTN_H
@@ -216,15 +216,30 @@ attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* 
                              void* workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
- * attn_fwd_splitkv_noalloc — attn_fwd_splitkv without a caller workspace and
- * without any allocation: the partial results go to a fixed scratch array of
- * ATTN_SPLITKV_SCRATCH_BYTES bytes that the library holds in device memory
- * (a static __device__ array, one per device; its address is looked up for
- * the current device).  Arguments as attn_fwd_splitkv minus the workspace.
- * A call whose attn_fwd_splitkv_workspace_size(B, H, Sq, D, num_splits)
- * exceeds the scratch returns ATTN_ERR_WORKSPACE before any CUDA call.
- * All calls of this entry point on one device share the scratch, so they
- * must not overlap on the GPU (issue them on one stream, or order them).
+ * attn_fwd_splitkv_noalloc — attn_fwd_splitkv for callers that cannot
+ * allocate device memory and have no workspace to hand over: a plugin inside
+ * a host framework that owns every byte of device memory and gives its
+ * plugins none, a serving loop that runs under a fixed memory budget, or code
+ * that must never call cudaMalloc / cudaFree because those calls may
+ * synchronise the device.  The partial results go to a fixed scratch array of
+ * ATTN_SPLITKV_SCRATCH_BYTES bytes inside the library (a static __device__
+ * array).  That array is part of the library's device image: every CUDA
+ * context that loads the library reserves ATTN_SPLITKV_SCRATCH_BYTES of
+ * device memory for it until the context ends, whether or not this entry
+ * point is ever called.  In host code the array's name is not a device
+ * address; each call looks the address up in the current context
+ * (cudaGetSymbolAddress, which allocates nothing).  The first call in a
+ * context may be the one that loads the library's module there, so make it
+ * before any stream capture.
+ *
+ * Arguments as attn_fwd_splitkv minus the workspace.  A call whose
+ * attn_fwd_splitkv_workspace_size(B, H, Sq, D, num_splits) exceeds the
+ * scratch returns ATTN_ERR_WORKSPACE before any CUDA call.  The call makes no
+ * cudaMalloc, cudaFree or other allocating call.  Every call in one context
+ * shares the scratch, and the scratch keeps what the last call wrote (every
+ * element a call reads back was written by that same call, so no clearing is
+ * needed): calls that overlap on the GPU race on it, so issue them on one
+ * stream or order them with events.
  */
 #define ATTN_SPLITKV_SCRATCH_BYTES (32u << 20)
 

@@ -1,5 +1,13 @@
 """attn_fwd_splitkv_noalloc: the split-KV forward on the library's fixed
-device scratch (no allocation, no caller workspace)."""
+device scratch, for callers that cannot allocate device memory (a plugin in
+a framework that owns all device memory, a serving loop under a fixed
+budget, code that must not risk the synchronisation of cudaMalloc/cudaFree)
+and so cannot hand over a workspace either.
+
+This file is named to be collected last: if the entry point fails, a run that
+stops at the first failure has already run every other test.  Its GPU tests
+pass in a fresh process too: the first call in the process loads the module
+and with it the static scratch."""
 
 import math
 import os
@@ -53,35 +61,75 @@ def test_argument_checks(lib):
     assert _call(0, 8, 128, 4096, 128, 4) == attn.ATTN_OK
 
 
+def _noalloc(q, k, v, o, lse, ns, causal, kv):
+    B, H, Sq, D = q.shape
+    st = attn.attn_fwd_splitkv_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                       B, H, Sq, k.shape[2], D, 1.0 / math.sqrt(D), int(causal),
+                                       None if kv is None else kv.data_ptr(), ns,
+                                       torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, st
+
+
+# (B, H, Sq, Sk, D, num_splits, causal, kv_lens): the decode-like shape the
+# split path is for, causal, a padded batch with an empty sequence, D = 64
+CASES = [
+    (1, 8, 128, 32768, 128, 16, False, None),
+    (2, 4, 300, 2000, 128, 7, True, None),
+    (3, 2, 256, 1500, 128, 5, False, [1500, 0, 777]),
+    (2, 3, 200, 3000, 64, 9, True, [0, 2900]),
+]
+
+
 @pytest.mark.gpu
-def test_noalloc_equals_workspace_split_and_allocates_nothing(lib):
-    B, H, Sq, Sk, D, ns = 1, 8, 128, 32768, 128, 16
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_noalloc_equals_workspace_split_and_allocates_nothing(lib, case):
+    """Two calls in a row of the no-allocation entry point give exactly the
+    bits of attn_fwd_splitkv with a caller workspace, and device memory stays
+    as it was."""
+    B, H, Sq, Sk, D, ns, causal, kvl = CASES[case]
     assert attn.attn_fwd_splitkv_workspace_size(B, H, Sq, D, ns) <= SCRATCH
-    g = torch.Generator().manual_seed(31)
+    g = torch.Generator().manual_seed(31 + case)
     dev = torch.device("cuda:0")
     q, k, v = (torch.randn(B, H, n, D, generator=g).to(torch.bfloat16).to(dev) for n in (Sq, Sk, Sk))
-    o_ws, l_ws = attn.forward_splitkv(q, k, v, ns)
-    o = torch.empty_like(q)
-    lse = torch.empty(B, H, Sq, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream().cuda_stream
-    scale = 1.0 / math.sqrt(D)
-
-    def run():
-        st = attn.attn_fwd_splitkv_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                           B, H, Sq, Sk, D, scale, 0, None, ns, stream)
-        assert st == attn.ATTN_OK
-    run()  # the first call loads the module (and with it the static scratch)
+    kv = None if kvl is None else torch.tensor(kvl, dtype=torch.int32, device=dev)
+    o_ws, l_ws = attn.forward_splitkv(q, k, v, ns, causal=causal, kv_lens=kv)
+    outs = [(torch.full_like(q, float("nan")), torch.full((B, H, Sq), float("nan"), device=dev)) for _ in range(2)]
+    _noalloc(q, k, v, *outs[0], ns, causal, kv)  # the first call may load the module (and the scratch)
     torch.cuda.synchronize()
     free0, _ = torch.cuda.mem_get_info()
     alloc0 = torch.cuda.memory_allocated()
-    for _ in range(20):
-        run()
-    st, site = attn.attn_check_device_status(stream)
+    _noalloc(q, k, v, *outs[1], ns, causal, kv)
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0 and torch.cuda.memory_allocated() == alloc0
-    assert torch.equal(o.view(torch.int16), o_ws.view(torch.int16))
-    assert torch.equal(lse, l_ws)
+    for o, lse in outs:
+        assert torch.equal(o.view(torch.int16), o_ws.view(torch.int16))
+        assert torch.equal(lse.view(torch.int32), l_ws.view(torch.int32))
+
+
+@pytest.mark.gpu
+def test_noalloc_larger_then_smaller_call_leaves_nothing_stale(lib):
+    """A call that fills much of the scratch, then a smaller one of another
+    shape: the second result must not pick up anything the first left in the
+    shared scratch."""
+    dev = torch.device("cuda:0")
+    g = torch.Generator().manual_seed(77)
+    qb = torch.randn(2, 8, 512, 128, generator=g).to(torch.bfloat16).to(dev)
+    kb, vb = (torch.randn(2, 8, 4096, 128, generator=g).to(torch.bfloat16).to(dev) for _ in range(2))
+    qs = torch.randn(1, 3, 130, 64, generator=g).to(torch.bfloat16).to(dev)
+    ks, vs = (torch.randn(1, 3, 900, 64, generator=g).to(torch.bfloat16).to(dev) for _ in range(2))
+    assert attn.attn_fwd_splitkv_workspace_size(2, 8, 512, 128, 12) <= SCRATCH
+    ob, lb = torch.empty_like(qb), torch.empty(2, 8, 512, device=dev)
+    os_, ls = torch.full_like(qs, float("nan")), torch.full((1, 3, 130), float("nan"), device=dev)
+    _noalloc(qb, kb, vb, ob, lb, 12, False, None)
+    _noalloc(qs, ks, vs, os_, ls, 5, True, None)
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, (st, site)
+    o_ref, l_ref = attn.forward_splitkv(qs, ks, vs, 5, causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(os_.view(torch.int16), o_ref.view(torch.int16))
+    assert torch.equal(ls.view(torch.int32), l_ref.view(torch.int32))
 
 
 @pytest.mark.gpu
