@@ -290,7 +290,34 @@ def generate(w, draw: int):
     return workloads.generate(w, draw)
 
 
-class BwdJob:
+class BufferSet:
+    """One set of device buffers for a job: the inputs (device copies of the
+    job's host tensors), the outputs, and the library call that reads and
+    writes them on the compute stream."""
+
+    def __init__(self, dev_inputs, outputs, call, keep=()):
+        self.inputs = dev_inputs
+        self.outputs = outputs
+        self.call = call
+        self.keep = list(keep)  # other device buffers the call uses (scheduling counter, workspace)
+
+
+class _JobBase:
+    """A workload's host inputs and one or more device buffer sets.  Set 0 is
+    what the device-timed loop launches; the end-to-end loop alternates two
+    sets so that one step's copies run under another step's kernel."""
+
+    def add_set(self):
+        self.sets.append(self._make_set())
+        return self.sets[-1]
+
+    def step(self, k: int = 0):
+        st = self.sets[k].call()
+        if st != self._attn.ATTN_OK:
+            raise self._attn.AttnError(st, self._what)
+
+
+class BwdJob(_JobBase):
     """The backward pass of a padded bf16 workload: the forward's O and LSE are
     computed once before timing; a step is one ``attn_bwd`` call (three
     kernels) for a fixed upstream gradient dO ~ N(0, 1) drawn after the
@@ -300,88 +327,91 @@ class BwdJob:
         from exact_attention_86_gb300 import workloads
         if is_varlen(w) or is_fp8(w) or args.splits > 0:
             raise SystemExit("--backward applies to padded bf16 workloads")
+        self._attn, self._what, self.w, self.dev, self.torch = attn, "backward", w, dev, torch
         self.stream = torch.cuda.current_stream(dev)
-        sptr = self.stream.cuda_stream
         q, k, v, kv = workloads.generate(w, args.draw)
         g = torch.Generator().manual_seed(w.seed + 1000)
         dout = torch.randn(q.shape, generator=g).to(torch.bfloat16)
-        qd, kd, vd, dod = q.to(dev), k.to(dev), v.to(dev), dout.to(dev)
         kvd = kv.to(dev) if kv is not None else None
-        o, lse = attn.forward(qd, kd, vd, scale=w.scale, causal=w.causal, kv_lens=kvd)
+        o, lse = attn.forward(q.to(dev), k.to(dev), v.to(dev), scale=w.scale, causal=w.causal, kv_lens=kvd)
         torch.cuda.synchronize(dev)
-        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-        ws = torch.empty(max(attn.attn_bwd_workspace_size(w.B, w.H, w.Sq), 256), dtype=torch.uint8, device=dev)
-        host = [q, k, v, o.cpu(), lse.cpu(), dout] + ([kv] if kv is not None else [])
-        dev_t = [qd, kd, vd, o, lse, dod] + ([kvd] if kvd is not None else [])
-        self.inputs = list(zip(host, dev_t))
-        self.outputs = [dq, dk, dv]
+        self.host = [q, k, v, o.cpu(), lse.cpu(), dout] + ([kv] if kv is not None else [])
         self.launches_per_step = 3
-        kv_ptr = kvd.data_ptr() if kvd is not None else None
+        self.sets = [self._make_set()]
+
+    def _make_set(self):
+        w, torch, attn = self.w, self.torch, self._attn
+        d = [t.to(self.dev) for t in self.host]
+        qd, kd, vd, o, lse, dod = d[:6]
+        kv_ptr = d[6].data_ptr() if len(d) > 6 else None
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        ws = torch.empty(max(attn.attn_bwd_workspace_size(w.B, w.H, w.Sq), 256), dtype=torch.uint8, device=self.dev)
+        sptr = self.stream.cuda_stream
 
         def call():
             return attn.attn_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), dod.data_ptr(),
                                  lse.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.Sq, w.Sk,
                                  w.D, w.scale, int(w.causal), kv_ptr, ws.data_ptr(), ws.numel(), sptr)
-        self._call = call
-        self._attn = attn
-
-    def step(self):
-        st = self._call()
-        if st != self._attn.ATTN_OK:
-            raise self._attn.AttnError(st, "backward")
+        return BufferSet(d, [dq, dk, dv], call)
 
 
-class Job:
-    """Device buffers and the step of one workload.  ``inputs`` are (host,
-    device) pairs the end-to-end step copies in; ``outputs`` the device
-    tensors it copies back."""
+class Job(_JobBase):
+    """The forward of one workload.  The host inputs are what the end-to-end
+    step copies in; the outputs what it copies back."""
 
     def __init__(self, w, args, dev, attn, torch):
-        from exact_attention_86_gb300 import workloads
+        self._attn, self._what, self.w, self.dev, self.torch, self.args = attn, "forward", w, dev, torch, args
         self.stream = torch.cuda.current_stream(dev)
-        sptr = self.stream.cuda_stream
         if args.splits > 0 and is_varlen(w):
             raise SystemExit("--splits applies to padded workloads only")
         if is_paged(w):
-            q, kc, vc, cu, sk, table = workloads.generate_paged(w)
-            host = [q, kc, vc, cu, sk, table]
+            q, kc, vc, cu, sk, table = workloads_mod().generate_paged(w)
+            self.host = [q, kc, vc, cu, sk, table]
+            self.paged_dims = (kc.shape[0], kc.shape[1], table.shape[1])
         elif is_fp8(w):
-            q, k8, _, vt8, kv = workloads.generate_fp8(w)
-            host = [q, k8, vt8] + ([kv] if kv is not None else [])
+            q, k8, _, vt8, kv = workloads_mod().generate_fp8(w)
+            self.host = [q, k8, vt8] + ([kv] if kv is not None else [])
         else:
             q, k, v, kv = generate(w, args.draw)
-            host = [q, k, v] + ([kv] if kv is not None else [])
-        dev_t = [t.to(dev) for t in host]
-        self.inputs = list(zip(host, dev_t))
+            self.host = [q, k, v] + ([kv] if kv is not None else [])
+        self.launches_per_step = 2 if args.splits > 0 else 1
+        self.sets = [self._make_set()]
+
+    def _make_set(self):
+        w, torch, attn, args, dev = self.w, self.torch, self._attn, self.args, self.dev
+        sptr = self.stream.cuda_stream
+        dev_t = [t.to(dev) for t in self.host]
+        q = self.host[0]
         o = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
         if is_varlen(w):
             lse = torch.empty(w.H, q.shape[0], dtype=torch.float32, device=dev)
         else:
             lse = torch.empty(w.B, w.H, w.Sq, dtype=torch.float32, device=dev)
-        self.outputs = [o, lse]
         ptr = [t.data_ptr() for t in dev_t]
         total = q.shape[0]
         # packed and paged batches: dynamic scheduling through a persistent
         # counter (each launch leaves it zero); --static-schedule turns it off
         counter_ptr = None
+        keep = []
         if is_varlen(w) and not args.static_schedule:
-            self.counter = torch.zeros(2, dtype=torch.int32, device=dev)
-            counter_ptr = self.counter.data_ptr()
+            counter = torch.zeros(2, dtype=torch.int32, device=dev)
+            keep.append(counter)
+            counter_ptr = counter.data_ptr()
         ws = None
         if args.splits > 0:
             ws_bytes = attn.attn_fwd_splitkv_workspace_size(w.B, w.H, w.Sq, w.D, args.splits)
             ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
-        self.launches_per_step = 2 if ws is not None else 1
+            keep.append(ws)
 
         if is_paged(w):
-            num_pages, page_size, max_pages = kc.shape[0], kc.shape[1], table.shape[1]
+            num_pages, page_size, max_pages = self.paged_dims
 
             def call():
                 return attn.attn_fwd_paged(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), ptr[3], ptr[4],
                                            ptr[5], w.batch, w.max_len, total, num_pages, page_size, max_pages, w.H,
                                            w.D, w.scale, int(w.causal), counter_ptr, sptr)
         elif is_fp8(w):
-            kv_ptr = ptr[3] if len(ptr) > 3 else None
+            kv_ptr = ptr[3] if len(self.host) > 3 else None
 
             def call():
                 return attn.attn_fwd_fp8(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), w.B, w.H, w.Sq, w.Sk,
@@ -392,25 +422,24 @@ class Job:
                                             w.batch, w.max_len, total, total, w.H, w.D, w.scale, int(w.causal),
                                             counter_ptr, sptr)
         elif ws is None:
-            kv_ptr = ptr[3] if len(ptr) > 3 else None
+            kv_ptr = ptr[3] if len(self.host) > 3 else None
 
             def call():
                 return attn.attn_fwd(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), w.B, w.H, w.Sq, w.Sk,
                                      w.D, w.scale, int(w.causal), kv_ptr, sptr)
         else:
-            kv_ptr = ptr[3] if len(ptr) > 3 else None
+            kv_ptr = ptr[3] if len(self.host) > 3 else None
 
             def call():
                 return attn.attn_fwd_splitkv(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), w.B, w.H, w.Sq,
                                              w.Sk, w.D, w.scale, int(w.causal), kv_ptr, args.splits, ws.data_ptr(),
                                              ws.numel(), sptr)
-        self._call = call
-        self._attn = attn
+        return BufferSet(dev_t, [o, lse], call, keep)
 
-    def step(self):
-        st = self._call()
-        if st != self._attn.ATTN_OK:
-            raise self._attn.AttnError(st, "forward")
+
+def workloads_mod():
+    from exact_attention_86_gb300 import workloads
+    return workloads
 
 
 def run_reference(args, w):
@@ -548,31 +577,112 @@ def main():
     value = whole_job_rate(step_flops, world, ms_per_step) / 1e12
     clocks = sampler.summary(wall0, wall1)
 
+    # ---------------------------------------------------------- launch floor
+    # Small workloads: the same launch shape with no work (mode 0) and with
+    # only the kernel's fixed set-up / tear-down (mode 1), each timed like the
+    # workload (an L2 flush before every launch), so that the line separates
+    # the floor from the work.
+    floor = None
+    if flush is not None and not args.backward and not is_varlen(w) and args.splits == 0:
+        n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        units = w.B * w.H * ((w.Sq + 127) // 128)
+        grid = max(1, min(units, n_sms))
+        floor = {"grid": grid}
+        for mode, name in ((0, "empty_us"), (1, "setup_teardown_us")):
+            n = min(args.steps, 200)
+            fe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            for i in range(n + 3):
+                flush.fill_(i & 0xFF)
+                if i >= 3:
+                    fe[i - 3][0].record(stream)
+                st = attn.attn_selftest_launch_floor(grid, w.D, mode, sptr)
+                if st != attn.ATTN_OK:
+                    raise attn.AttnError(st, "launch floor")
+                if i >= 3:
+                    fe[i - 3][1].record(stream)
+            torch.cuda.synchronize(dev)
+            floor[name] = 1e3 * statistics.mean(a.elapsed_time(b) for a, b in fe)
+        floor["workload_us"] = 1e3 * launch_ms
+
     # ------------------------------------------------------------ end to end
-    pinned = [(h.pin_memory(), d) for h, d in job.inputs]
-    outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in job.outputs]
+    # Every step copies its own inputs in from pinned host memory, runs the
+    # library call and copies its own outputs back, all inside the timed
+    # region.  Two device buffer sets alternate: the host-to-device copy of
+    # step i+1 (copy-in stream) and the device-to-host copy of step i-1
+    # (copy-out stream) run under the kernel of step i; events order each
+    # copy after the last kernel that used its buffers.
+    job.add_set()
+    pinned_in = [t.pin_memory() for t in job.host]
+    outs_h = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in job.sets[0].outputs] for _ in range(2)]
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
 
-    def e2e_step():
-        for h, d in pinned:
-            d.copy_(h, non_blocking=True)
-        step()
-        for h, d in zip(outs_h, job.outputs):
-            h.copy_(d, non_blocking=True)
+    def new_event():
+        return torch.cuda.Event()
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_run(n: int):
+        computed = [None, None]    # kernel of the last step on set k done
+        copied_out = [None, None]  # device-to-host copy of the last step on set k done
+        start = new_event()
+        start.record(stream)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        for i in range(n):
+            kset = i % 2
+            bs = job.sets[kset]
+            with torch.cuda.stream(s_in):
+                if computed[kset] is not None:
+                    s_in.wait_event(computed[kset])
+                for h, d in zip(pinned_in, bs.inputs):
+                    d.copy_(h, non_blocking=True)
+                copied_in = new_event()
+                copied_in.record(s_in)
+            stream.wait_event(copied_in)
+            if copied_out[kset] is not None:
+                stream.wait_event(copied_out[kset])
+            job.step(kset)
+            done = new_event()
+            done.record(stream)
+            computed[kset] = done
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                for h, d in zip(outs_h[kset], bs.outputs):
+                    h.copy_(d, non_blocking=True)
+                out_done = new_event()
+                out_done.record(s_out)
+                copied_out[kset] = out_done
+        for e in copied_out:
+            if e is not None:
+                stream.wait_event(e)
+
+    e2e_run(3)
     barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
+    e2e_run(args.e2e_steps)
     e1.record(stream)
     barrier()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
     (e2e_ms,) = max_over_ranks([e2e_ms], dev, world)
-    h2d = sum(h.numel() * h.element_size() for h, _ in pinned)
-    d2h = sum(t.numel() * t.element_size() for t in job.outputs)
+    h2d = sum(h.numel() * h.element_size() for h in pinned_in)
+    d2h = sum(t.numel() * t.element_size() for t in job.sets[0].outputs)
+
+    # the box's pinned copy rates for these buffers, each direction alone
+    def copy_ms(fn, reps=5):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        fn()
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / reps
+
+    h2d_ms = copy_ms(lambda: [d.copy_(h, non_blocking=True) for h, d in zip(pinned_in, job.sets[0].inputs)])
+    d2h_ms = copy_ms(lambda: [h.copy_(d, non_blocking=True) for h, d in zip(outs_h[0], job.sets[0].outputs)])
+    e2e_bound_ms = max(h2d_ms, d2h_ms, ms_per_step)
 
     # -------------------------------------------------------------- roofline
     peaks = measured_peaks()
@@ -630,8 +740,14 @@ def main():
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": whole_job_rate(step_flops, world, e2e_ms) / 1e12, "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "pipeline": "two device buffer sets; copy-in and copy-out streams overlap the next and "
+                                "previous steps' copies with each kernel",
+                    "h2d_gbs": h2d / (h2d_ms * 1e-3) / 1e9, "d2h_gbs": d2h / (d2h_ms * 1e-3) / 1e9,
+                    "bound_ms_per_step": e2e_bound_ms,
+                    "bound_value": whole_job_rate(step_flops, world, e2e_bound_ms) / 1e12},
             "clocks": clocks,
+            "launch_floor": floor,
             "gpu_launches": args.steps * job.launches_per_step,
             "pct_of_peak": 100.0 * value / world / peak,
         }
