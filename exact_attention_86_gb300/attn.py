@@ -72,6 +72,11 @@ SIGNATURES = {
     "attn_get_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "attn_check_device_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.POINTER(ctypes.c_uint32)]),
     "attn_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_int64, ctypes.c_void_p]),
+    "attn_selftest_launch_floor": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "attn_selftest_fwd_abort": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int,
+                                                                                          ctypes.c_void_p, ctypes.c_int,
+                                                                                          ctypes.c_int64,
+                                                                                          ctypes.c_void_p]),
     "attn_abi_version": (ctypes.c_int, []),
 }
 
@@ -183,6 +188,17 @@ def attn_check_device_status(stream: Optional[int] = None) -> Tuple[int, int]:
 
 def attn_selftest_wait_timeout(limit_ns: int, stream: Optional[int] = None) -> int:
     return lib().attn_selftest_wait_timeout(limit_ns, stream)
+
+
+def attn_selftest_fwd_abort(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
+                            scale: float, causal: int, kv_lens: Optional[int], skip_fill: int, limit_ns: int,
+                            stream: Optional[int] = None) -> int:
+    return lib().attn_selftest_fwd_abort(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, skip_fill,
+                                         limit_ns, stream)
+
+
+def attn_selftest_launch_floor(grid: int, D: int, mode: int, stream: Optional[int] = None) -> int:
+    return lib().attn_selftest_launch_floor(grid, D, mode, stream)
 
 
 def attn_abi_version() -> int:

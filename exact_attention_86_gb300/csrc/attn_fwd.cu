@@ -226,6 +226,10 @@ struct Params {
   uint32_t idesc_qk;       // negate-A set when scale < 0
   uint32_t idesc_pv;
   uint64_t wait_limit_ns;
+  // Self test of the give-up path only (attn_selftest_fwd_abort): block 0's
+  // producer leaves out its K fill with this index, so the bounded wait of the
+  // fill's consumer must give up and every role must drain; -1 otherwise.
+  int selftest_skip_fill = -1;
 };
 
 struct Unit {
@@ -674,7 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            load_tile(sel != 0, f.slot, (sel ? bar_v_full0 : bar_k_full0) + 8 * f.slot, u, j, page_tok, pol_keep);
+            if (!(sel == 0 && blockIdx.x == 0 && static_cast<int>(k_issued) == p.selftest_skip_fill))
+              load_tile(sel != 0, f.slot, (sel ? bar_v_full0 : bar_k_full0) + 8 * f.slot, u, j, page_tok, pol_keep);
             if (sel) ++v_issued; else ++k_issued;
           }
         }
@@ -1111,6 +1116,38 @@ __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
   __syncthreads();
 }
 
+// The forward kernel's launch shape with none of its work (mode 0), or with
+// only its fixed per-block set-up and tear-down (mode 1): mbarrier
+// initialisation, the 512-column Tensor Memory allocation, the block-wide
+// synchronisations and the release.  The host requires one block per SM
+// (the forward's shared memory), so allocations never wait on each other.
+__global__ void __launch_bounds__(kThreads, 1) launch_floor_kernel(int mode) {
+  if (mode == 0) return;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  Ctrl& ctl = *reinterpret_cast<Ctrl*>(smem_raw + (base - raw));
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 12; ++s) mbar_init(smem_addr(&ctl.k_full[s]), 1);
+    fence_barrier_init();
+  }
+  if (warp == kWarpQK) {
+    tmem_alloc(smem_addr(&ctl.tmem_base), 512);
+    tmem_relinquish_alloc_permit();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl.tmem_base;
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kWarpQK) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ------------------------------------------------------------------- host side
 
 struct DeviceInfo {
@@ -1397,7 +1434,8 @@ attn_status launch_any(DeviceInfo& dev, int D, bool causal, const CUtensorMap& m
 
 attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int H, int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens, int num_splits,
-                        float* o_part, float* lse_part, cudaStream_t s) {
+                        float* o_part, float* lse_part, cudaStream_t s, uint64_t wait_limit_ns = kWaitLimitNs,
+                        int selftest_skip_fill = -1) {
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, B, H, Sq, D)) return ATTN_ERR_CUDA;
   if (Sk > 0) {
@@ -1431,7 +1469,8 @@ attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const voi
   p.v_scale = 1.0f;
   p.idesc_qk = idesc_bf16_f32(kBQ, kBK, scale < 0.0f, false);
   p.idesc_pv = idesc_bf16_f32(kBQ, D, false, true);
-  p.wait_limit_ns = kWaitLimitNs;
+  p.wait_limit_ns = wait_limit_ns;
+  p.selftest_skip_fill = selftest_skip_fill;
   if (D == 64) {
     return causal ? launch<64, true>(dev, 0, mq, mk, mv, p, s) : launch<64, false>(dev, 1, mq, mk, mv, p, s);
   }
@@ -1748,6 +1787,42 @@ attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream) {
   if (st != ATTN_OK) return st;
   wait_timeout_selftest_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
       static_cast<uint64_t>(limit_ns));
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_selftest_fwd_abort(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                    int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens,
+                                    int skip_fill, int64_t limit_ns, attn_stream_t stream) {
+  attn_status st = check_args(q, k, v, o, lse, B, H, Sq, Sk, D, scale, kv_lens, 1);
+  if (st != ATTN_OK) return st;
+  if (limit_ns < 1000 || limit_ns > 2000000000LL || skip_fill < 0) return ATTN_ERR_SHAPE;
+  // block 0 must have a K fill with that index: its first unit's tiles
+  if (B == 0 || H == 0 || Sq == 0 || Sk == 0) return ATTN_ERR_SHAPE;
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  return run_forward(*dev, q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, 1, nullptr, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream), static_cast<uint64_t>(limit_ns), skip_fill);
+}
+
+attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t stream) {
+  if (grid < 1 || grid > 65535 || mode < 0 || mode > 1) return ATTN_ERR_SHAPE;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED_D;
+  DeviceInfo* dev = nullptr;
+  attn_status st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  const int smem = D == 64 ? Geo<64>::kSmemBytes : Geo<128>::kSmemBytes;
+  // both sizes exceed half of an SM's shared memory: one block per SM
+  static_assert(2 * Geo<128>::kSmemBytes > 233472 && 2 * Geo<64>::kSmemBytes > 233472, "one block per SM");
+  const int idx = D == 64 ? 10 : 11;
+  if (!dev->smem_set[idx].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(launch_floor_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Geo<64>::kSmemBytes > Geo<128>::kSmemBytes ? Geo<64>::kSmemBytes : Geo<128>::kSmemBytes) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
+    dev->smem_set[idx].store(true, std::memory_order_release);
+  }
+  launch_floor_kernel<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(mode);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

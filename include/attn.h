@@ -313,10 +313,49 @@ attn_status attn_check_device_status(attn_stream_t stream, uint32_t* site);
  */
 attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream);
 
+/*
+ * attn_selftest_fwd_abort — failure-detection self test of the attention
+ * kernel itself ("Attention softmax fusion", section "Things that break": a
+ * fused kernel must fail without corrupting what it shares).  Runs attn_fwd
+ * (same arguments, same checks; Sk >= 1 required) with every bounded wait
+ * limited to `limit_ns` nanoseconds (1000 .. 2e9) instead of 2 s, and with
+ * block 0's producer leaving out its K fill number `skip_fill` (>= 0,
+ * counted over that block's K tiles in its order of work).  Nothing ever
+ * arrives for that fill, so a wait in block 0 gives up: the block records the
+ * site, raises its abort flag, every role drains its copies and products,
+ * frees Tensor Memory and returns; attn_check_device_status then reports
+ * ATTN_ERR_DEVICE_TIMEOUT.  The other blocks finish their units normally
+ * (unless `limit_ns` is shorter than their own legitimate waits).  If block 0
+ * has fewer K fills than skip_fill + 1 nothing is left out.  The rows of
+ * block 0's units are left undefined.  No fault, trap or unbounded spin is
+ * involved.
+ */
+attn_status attn_selftest_fwd_abort(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                    int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens,
+                                    int skip_fill, int64_t limit_ns, attn_stream_t stream);
+
+/*
+ * attn_selftest_launch_floor — measurement aid, no attention arithmetic.
+ * Launches `grid` blocks (1 .. 65535) of a kernel with the attention
+ * forward's launch shape for head dimension D (64 or 128): 384 threads and the
+ * same dynamic shared memory, so one block per SM.  mode 0: the kernel returns
+ * at once (the cost of the launch itself); mode 1: it does only the forward
+ * kernel's fixed per-block set-up and tear-down (mbarrier initialisation,
+ * Tensor Memory allocation of 512 columns, the block-wide synchronisations,
+ * Tensor Memory release) with no loads and no products.  Timing it against
+ * the forward on a small workload separates the launch and set-up floor from
+ * the work ("Attention softmax fusion", section "Things that break", warns
+ * against judging a fused kernel by one short sequence length).
+ * Errors: ATTN_ERR_SHAPE for a grid or mode out of range,
+ * ATTN_ERR_UNSUPPORTED_D, ATTN_ERR_CUDA / ATTN_ERR_UNSUPPORTED_DEVICE as for
+ * the other calls.  Asynchronous on `stream`.
+ */
+attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t stream);
+
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 9
+#define ATTN_ABI_VERSION 10
 
 #ifdef __cplusplus
 }

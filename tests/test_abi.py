@@ -278,3 +278,22 @@ def test_bwd_argument_checks(lib, args, code):
 def test_bwd_workspace_size(lib):
     assert attn.attn_bwd_workspace_size(2, 3, 300) == -(-(2 * 3 * 300 * 4) // 256) * 256
     assert attn.attn_bwd_workspace_size(-1, 3, 300) == 0
+
+
+def test_launch_floor_argument_checks(lib):
+    # each call ends at a host-side check (no device query, no launch)
+    assert attn.attn_selftest_launch_floor(0, 64, 0, None) == attn.ATTN_ERR_SHAPE
+    assert attn.attn_selftest_launch_floor(70000, 64, 0, None) == attn.ATTN_ERR_SHAPE
+    assert attn.attn_selftest_launch_floor(1, 64, 2, None) == attn.ATTN_ERR_SHAPE
+    assert attn.attn_selftest_launch_floor(1, 96, 0, None) == attn.ATTN_ERR_UNSUPPORTED_D
+
+
+def test_fwd_abort_selftest_argument_checks(lib):
+    # each call ends at a host-side check (no device query, no launch)
+    f = attn.attn_selftest_fwd_abort
+    assert f(A, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, 0, 999, None) == attn.ATTN_ERR_SHAPE
+    assert f(A, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, 0, 3_000_000_000, None) == attn.ATTN_ERR_SHAPE
+    assert f(A, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, -1, 10_000, None) == attn.ATTN_ERR_SHAPE
+    assert f(A, A, A, A, A, 1, 2, 256, 0, 128, 0.1, 0, None, 0, 10_000, None) == attn.ATTN_ERR_SHAPE
+    assert f(A, A, A, A, A, 1, 2, 256, 256, 96, 0.1, 0, None, 0, 10_000, None) == attn.ATTN_ERR_UNSUPPORTED_D
+    assert f(A + 8, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, 0, 10_000, None) == attn.ATTN_ERR_ALIGN

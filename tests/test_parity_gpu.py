@@ -200,6 +200,62 @@ def test_wait_timeout_selftest_reports_and_recovers():
     _full_check(q, k, v, 0.125, False, None, "after selftest")
 
 
+# every site a bounded wait of the forward kernel can report
+WAIT_SITES = set(range(1, 12)) - {8}
+
+
+@pytest.mark.parametrize("D,causal,skip", [(128, False, 5), (128, True, 0), (64, False, 3), (64, True, 10)])
+def test_forward_kernel_gives_up_drains_and_recovers(D, causal, skip):
+    """The attention kernel's own give-up path: block 0's producer leaves out
+    one K fill, so a bounded wait (1 ms) in block 0 runs out; every role of
+    that block must drain its copies and products, free Tensor Memory and
+    return.  The status reports the timeout and its site, every other block's
+    rows are exact, and the context then computes correct results."""
+    B, H, S = 1, 2, 2048
+    q, k, v, _ = _inputs(B, H, S, S, D, seed=61 + D + int(causal))
+    dev = torch.device("cuda:0")
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o = nan_filled((B, H, S, D), torch.bfloat16, dev)
+    lse = nan_filled((B, H, S), torch.float32, dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    assert attn.attn_check_device_status(stream)[0] == attn.ATTN_OK
+    scale = 1.0 / math.sqrt(D)
+    st = attn.attn_selftest_fwd_abort(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                      B, H, S, S, D, scale, int(causal), None, skip, 1_000_000, stream)
+    assert st == attn.ATTN_OK
+    st, site = attn.attn_check_device_status(stream)
+    assert st == attn.ATTN_ERR_DEVICE_TIMEOUT and site in WAIT_SITES, (st, site)
+    assert attn.attn_check_device_status(stream)[0] == attn.ATTN_OK  # cleared
+    # block 0 handles one unit (32 units on the SMs): only its 128 rows may differ
+    o_ref, l_ref = attention_ref(_np(q), _np(k), _np(v), scale, causal=causal)
+    on, ln = o.float().cpu().numpy(), lse.cpu().numpy()
+    bad = []
+    for h in range(H):
+        for t0 in range(0, S, 128):
+            sl = (0, h, slice(t0, t0 + 128))
+            try:
+                check(on[sl], ln[sl], o_ref[sl], l_ref[sl], "")
+            except AssertionError:
+                bad.append((h, t0))
+    assert len(bad) <= 1, bad
+    # the context is healthy: a normal call matches the oracle
+    _full_check(q, k, v, scale, causal, None, "after the aborted launch")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("mode", [0, 1])
+def test_launch_floor_kernel_runs_clean(D, mode):
+    # the measurement aid: a full wave of blocks with the forward's launch
+    # shape, empty or with the fixed set-up / tear-down only
+    stream = torch.cuda.current_stream().cuda_stream
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for grid in (1, n_sms, 2 * n_sms):
+        assert attn.attn_selftest_launch_floor(grid, D, mode, stream) == attn.ATTN_OK
+    assert attn.attn_check_device_status(stream)[0] == attn.ATTN_OK
+    q, k, v, _ = _inputs(1, 1, 130, 130, D, seed=4)
+    _full_check(q, k, v, 0.125, True, None, "after launch floor")
+
+
 # ------------------------------------------------------ the five workloads
 
 def _device_inputs(w, draw=0):
