@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ring = 0, qcount = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
-          const int unit = unit_at<CAUSAL>(t);
+          const int unit = unit_at<CAUSAL>(p, t);
           if (unit >= p.total_units) continue;
           const Unit u = decode_dq_unit<CAUSAL>(p, unit);
           if (u.n == 0) continue;
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t tcount = 0, qcount = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
-        const int unit = unit_at<CAUSAL>(t);
+        const int unit = unit_at<CAUSAL>(p, t);
         if (unit >= p.total_units) continue;
         const Unit u = decode_dq_unit<CAUSAL>(p, unit);
         if (u.n == 0) continue;
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t tcount = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
-        const int unit = unit_at<CAUSAL>(t);
+        const int unit = unit_at<CAUSAL>(p, t);
         if (unit >= p.total_units) continue;
         const Unit u = decode_dq_unit<CAUSAL>(p, unit);
         if (u.n == 0) continue;
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tcount = 0, ucount = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
-      const int unit = unit_at<CAUSAL>(t);
+      const int unit = unit_at<CAUSAL>(p, t);
       if (unit >= p.total_units) continue;
       const Unit u = decode_dq_unit<CAUSAL>(p, unit);
       const int row = u.q0 + r;
@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t ring = 0, ucount = 0;
         bool ok = true;
         for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
-          const int unit = unit_at<CAUSAL>(t);
+          const int unit = unit_at<CAUSAL>(p, t);
           if (unit >= p.total_units) continue;
           const KvUnit u = decode_kv_unit<CAUSAL>(bp, unit);
           if (u.n == 0) continue;
@@ -658,7 +658,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t tcount = 0, ucount = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
-        const int unit = unit_at<CAUSAL>(t);
+        const int unit = unit_at<CAUSAL>(p, t);
         if (unit >= p.total_units) continue;
         const KvUnit u = decode_kv_unit<CAUSAL>(bp, unit);
         if (u.n == 0) continue;
@@ -720,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t tcount = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
-        const int unit = unit_at<CAUSAL>(t);
+        const int unit = unit_at<CAUSAL>(p, t);
         if (unit >= p.total_units) continue;
         const KvUnit u = decode_kv_unit<CAUSAL>(bp, unit);
         if (u.n == 0) continue;
@@ -780,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tcount = 0, ucount = 0;
     bool ok = true;
     for (int t = blockIdx.x; ok && t < t_end; t += gridDim.x) {
-      const int unit = unit_at<CAUSAL>(t);
+      const int unit = unit_at<CAUSAL>(p, t);
       if (unit >= p.total_units) continue;
       const KvUnit u = decode_kv_unit<CAUSAL>(bp, unit);
       const int key = u.key0 + r;
@@ -925,12 +925,16 @@ attn_status launch_bwd(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CU
   }
   if (bq.f.total_units > 0) {
     const int grid = bq.f.total_units < dev.num_sms ? bq.f.total_units : dev.num_sms;
-    kq<<<grid, kThreads, smem_q, stream>>>(mq, mdo, mk64, mv64, bq);
+    BwdParams bqd = bq;
+    bqd.f = with_divisors(bq.f, grid);
+    kq<<<grid, kThreads, smem_q, stream>>>(mq, mdo, mk64, mv64, bqd);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   }
   if (bk.f.total_units > 0) {
     const int grid = bk.f.total_units < dev.num_sms ? bk.f.total_units : dev.num_sms;
-    kk<<<grid, kThreads, smem_k, stream>>>(mq64, mdo64, mk, mv, bk);
+    BwdParams bkd = bk;
+    bkd.f = with_divisors(bk.f, grid);
+    kk<<<grid, kThreads, smem_k, stream>>>(mq64, mdo64, mk, mv, bkd);
     if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
   }
   return ATTN_OK;

@@ -92,6 +92,8 @@ enum WaitSite : uint32_t {
   kSiteSFree = 9,
   kSitePFree = 10,
   kSiteUnitQ = 11,
+  kSiteAlign = 12,   // not a wait: the block's shared memory was not 1024-byte aligned
+  kSitePvIssued = 13,
 };
 
 // [0]: 1 once any wait gave up; [1]: site of the first one; [2]: its block.
@@ -102,7 +104,14 @@ __device__ uint32_t g_attn_status[3];
 // entry point needs neither an allocation nor a caller workspace.
 __device__ __align__(256) uint8_t g_splitkv_scratch[ATTN_SPLITKV_SCRATCH_BYTES];
 
-template <int D, bool FP8 = false>
+#ifndef ATTN_SPLIT_SLOTS_K
+#define ATTN_SPLIT_SLOTS_K 3   // K slots of the split rings at D = 128 (bf16)
+#endif
+#ifndef ATTN_SPLIT_SLOTS_V
+#define ATTN_SPLIT_SLOTS_V 2   // V slots of the split rings at D = 128 (bf16)
+#endif
+
+template <int D, bool FP8 = false, bool SPLIT = false>
 struct Geo {
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(!FP8 || D == 128, "E4M3 path: D = 128");
@@ -112,7 +121,11 @@ struct Geo {
   static constexpr int kChunks = D * kElem / 128;
   static constexpr int kChunkElems = 128 / kElem;      // elements per 128-B row of a chunk
   static constexpr int kKSteps = D * kElem / 32;       // QK^T instructions: 32 B of D each
-  static constexpr int kSlots = (D == 128 && !FP8) ? 5 : 12;  // K and V tiles in shared memory
+  // K and V tiles in shared memory.  Padded batches (one ring): as many as
+  // the 227 KB a block may use leave after the control block, the exchange
+  // buffers and Q.  Packed and paged batches (split rings) at D = 128: 3 K
+  // and 2 V slots (measured faster than 3 + 3 there).
+  static constexpr int kSlots = (D == 128 && !FP8) ? (SPLIT ? ATTN_SPLIT_SLOTS_K + ATTN_SPLIT_SLOTS_V : 6) : 12;
   // Two layouts of the K/V tiles over those slots (both modelled by the
   // protocol tests):
   //  single ring (padded batches): the producer fills K_0 V_0 K_1 V_1 ... in
@@ -127,7 +140,7 @@ struct Geo {
   //    slot kSlotsK + t % kSlotsV, each ring filled by its own producer warp,
   //    so a K fill never waits behind a V fill or its page lookups (measured
   //    faster there: paged 6 %, packed 2 %).
-  static constexpr int kSlotsK = (kSlots == 5) ? 3 : kSlots / 2;
+  static constexpr int kSlotsK = (D == 128 && !FP8 && SPLIT) ? ATTN_SPLIT_SLOTS_K : kSlots / 2;
   static constexpr int kSlotsV = kSlots - kSlotsK;
   struct Fill {
     uint32_t slot;       // shared-memory slot of the tile
@@ -168,9 +181,25 @@ struct Geo {
       return 64u * static_cast<uint32_t>(kk / per_half) + 8u * static_cast<uint32_t>(kk % per_half);
     return 8u * static_cast<uint32_t>(kk);
   }
-  static constexpr int kOffQ = 4096;                 // after control block and exchange buffers
+  // Control block [0, 1024), exchange buffers [1024, 3072), Q, the ring.  The
+  // dynamic shared memory of a block starts 1024-byte aligned (checked at
+  // kernel entry), as the 128-byte swizzle atoms need, so no slack is added.
+  static constexpr int kOffQ = 3072;
   static constexpr int kOffRing = kOffQ + kTileBytes;
-  static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes;
+  static_assert(kOffQ % 1024 == 0 || kTileBytes % 1024 == 0, "swizzle atoms 1024-byte aligned");
+  static_assert(kSmemBytes <= 232448, "shared memory per block");
+  static_assert(kSlots <= 16, "barrier initialisation: one lane per slot among lanes 0-15");
+};
+
+struct Unit {
+  int b, h, q0;            // q0: position of the unit's first query row within its sequence
+  int rows;                // query rows of the unit that exist (<= 128; 0: nothing to do)
+  int q_tok0, k_tok0;      // packed mode: token index of the first query row / first key
+  int kv;                  // valid keys of this batch entry (kv_lens clamped to [0, Sk])
+  int j0;                  // first K tile of the unit
+  int n;                   // K tiles the unit processes (0: no valid key for any row)
+  int split;               // key range index (split mode)
 };
 
 struct Ctrl {
@@ -178,6 +207,7 @@ struct Ctrl {
   uint64_t k_full[12], v_full[12], kv_empty[12];  // per slot; full: one per kind (Geo::fill_of)
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t o_full[2], o_free[2];
+  uint64_t pv_issued;  // the P V issuer has issued the last product of a unit
   uint64_t uq_full[4], uq_empty[4];  // the CTA's unit queue (filled by the producer lane)
   int unit_q[4];
   uint64_t drain[2];
@@ -187,12 +217,28 @@ struct Ctrl {
 static_assert(sizeof(Ctrl) <= 1024, "control block");
 
 // Exchange buffers (shared memory, after the control block at +1024):
-//   xmax[2][2][128] fp32 (tile parity, half, row), then xsum[2][128].
+// xmax[2][2][128] fp32 (tile parity, half, row).  The partial row sums of a
+// unit's epilogue go through xmax[b ^ 1], b the parity of the unit's last tile:
+// both halves of a row passed that tile's barrier after their last read of
+// xmax[b ^ 1] (the tile before), and the next write to it is the next unit's
+// first tile, after two more barriers of the pair.
 struct Xchg {
   float xmax[2][2][kBQ];
-  float xsum[2][kBQ];
 };
-static_assert(sizeof(Xchg) <= 3072, "exchange buffers");
+static_assert(sizeof(Xchg) <= 2048, "exchange buffers");
+
+// Division by a divisor fixed for a launch, with one multiply-high, an add
+// and a shift (the method of Granlund and Montgomery, "Division by invariant
+// integers using multiplication", 1994): for d >= 1 let s = ceil(log2 d) and
+// m = floor(2^32 (2^s - d) / d) + 1; then floor(n / d) = (mulhi(n, m) + n) >> s
+// for every 0 <= n < 2^31 (the sum stays below 2^32).  The work-unit decode of
+// every role used to spend most of its time in general integer divisions.
+struct FastDiv {
+  uint32_t d, m, s;
+  __device__ __forceinline__ int div(int n) const {
+    return static_cast<int>((__umulhi(static_cast<uint32_t>(n), m) + static_cast<uint32_t>(n)) >> s);
+  }
+};
 
 struct Params {
   uint16_t* o;
@@ -226,48 +272,43 @@ struct Params {
   uint32_t idesc_qk;       // negate-A set when scale < 0
   uint32_t idesc_pv;
   uint64_t wait_limit_ns;
+  // divisors of the unit decode, set at launch (with_divisors)
+  FastDiv fd_splits, fd_qtiles, fd_group_units, fd_group_heads, fd_last_heads, fd_H, fd_grid;
+  int last_group;          // causal order: index of the last head group (it may hold fewer heads)
   // Self test of the give-up path only (attn_selftest_fwd_abort): block 0's
   // producer leaves out its K fill with this index, so the bounded wait of the
   // fill's consumer must give up and every role must drain; -1 otherwise.
   int selftest_skip_fill = -1;
+  int o_align32 = 0;       // o is 32-byte aligned: the epilogue writes 32-byte pieces
 };
 
-struct Unit {
-  int b, h, q0;            // q0: position of the unit's first query row within its sequence
-  int rows;                // query rows of the unit that exist (<= 128; 0: nothing to do)
-  int q_tok0, k_tok0;      // packed mode: token index of the first query row / first key
-  int kv;                  // valid keys of this batch entry (kv_lens clamped to [0, Sk])
-  int j0;                  // first K tile of the unit
-  int n;                   // K tiles the unit processes (0: no valid key for any row)
-  int split;               // key range index (split mode)
-};
 
 template <bool CAUSAL>
 __device__ __forceinline__ Unit decode_unit(const Params& p, int t_in) {
   Unit u;
   // split mode: the key tiles of a (b, h, query tile) are cut into num_splits
   // contiguous ranges, consecutive units
-  u.split = t_in % p.num_splits;
-  const int t = t_in / p.num_splits;
-  const int bh_count = p.B * p.H;
+  const int t = p.fd_splits.div(t_in);
+  u.split = t_in - t * p.num_splits;
   int qt, bh;
   if (CAUSAL) {
     // Heads in groups whose K/V fit in a share of L2, one group after the
     // other; within a group the longest units first (query blocks from the
     // end of the sequence), the group's heads fastest.  The CTAs working at
-    // the same time then read the K/V of one group only.
-    const int units_per_group = p.head_group * p.n_qtiles;
-    const int grp = t / units_per_group;
-    const int w = t - grp * units_per_group;
-    const int heads = min(p.head_group, bh_count - grp * p.head_group);
-    qt = p.n_qtiles - 1 - w / heads;
-    bh = grp * p.head_group + w % heads;
+    // the same time then read the K/V of one group only.  (The last group
+    // may hold fewer heads.)
+    const int grp = p.fd_group_units.div(t);
+    const int w = t - grp * p.head_group * p.n_qtiles;
+    const FastDiv& fh = grp == p.last_group ? p.fd_last_heads : p.fd_group_heads;
+    const int wq = fh.div(w);
+    qt = p.n_qtiles - 1 - wq;
+    bh = grp * p.head_group + (w - wq * static_cast<int>(fh.d));
   } else {       // consecutive units share a head, so its K/V stay hot in L2
-    qt = t % p.n_qtiles;
-    bh = t / p.n_qtiles;
+    bh = p.fd_qtiles.div(t);
+    qt = t - bh * p.n_qtiles;
   }
-  u.b = bh / p.H;
-  u.h = bh % p.H;
+  u.b = p.fd_H.div(bh);
+  u.h = bh - u.b * p.H;
   u.q0 = qt * kBQ;
   int kv, q_len;
   if (p.cu_q != nullptr) {
@@ -297,8 +338,8 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int t_in) {
   int lim = kv;
   if (CAUSAL) lim = min(lim, u.q0 + u.rows);  // last row of the tile + 1
   const int n_all = u.rows > 0 ? (lim + kBK - 1) / kBK : 0;
-  u.j0 = u.split * n_all / p.num_splits;
-  u.n = (u.split + 1) * n_all / p.num_splits - u.j0;
+  u.j0 = p.fd_splits.div(u.split * n_all);
+  u.n = p.fd_splits.div((u.split + 1) * n_all) - u.j0;
   return u;
 }
 
@@ -307,9 +348,9 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int t_in) {
 // in alternating direction each round ("snake" order), which evens out the
 // per-CTA sums of their lengths.  Values >= total_units are skipped.
 template <bool CAUSAL>
-__device__ __forceinline__ int unit_at(int t) {
+__device__ __forceinline__ int unit_at(const Params& p, int t) {
   if (!CAUSAL) return t;
-  const int round = t / static_cast<int>(gridDim.x);
+  const int round = p.fd_grid.div(t);
   const int pos = t - round * static_cast<int>(gridDim.x);
   return (round & 1) ? round * static_cast<int>(gridDim.x) + (static_cast<int>(gridDim.x) - 1 - pos) : t;
 }
@@ -470,18 +511,24 @@ template <int D, bool CAUSAL, bool FP8, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                     const __grid_constant__ CUtensorMap map_v, const Params p) {
-  using G = Geo<D, FP8>;
+  using G = Geo<D, FP8, SPLIT>;
   using PR = Prec<FP8>;
   extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_addr(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* base_ptr = smem_raw + (base - raw);
+  const uint32_t base = smem_addr(smem_raw);
+  uint8_t* base_ptr = smem_raw;
   Ctrl& ctl = *reinterpret_cast<Ctrl*>(base_ptr);
   Xchg& xch = *reinterpret_cast<Xchg*>(base_ptr + 1024);
   volatile int* abort_flag = &ctl.abort_flag;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // The layout leaves no slack for aligning the 128-byte swizzle atoms: a
+  // block whose dynamic shared memory does not start 1024-byte aligned
+  // (never seen) reports it and does nothing, before touching anything.
+  if ((base & 1023u) != 0u) {
+    if (threadIdx.x == 0) record_give_up(kSiteAlign);
+    return;
+  }
 
   const uint32_t bar_q_full = smem_addr(&ctl.q_full);
   const uint32_t bar_q_empty = smem_addr(&ctl.q_empty);
@@ -499,28 +546,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_uq_empty0 = smem_addr(&ctl.uq_empty[0]);
   volatile int* unit_q = ctl.unit_q;
 
-  if (threadIdx.x == 0) {
-    mbar_init(bar_q_full, 1);
-    mbar_init(bar_q_empty, 1);
-    for (int s = 0; s < G::kSlots; ++s) {
-      mbar_init(bar_k_full0 + 8 * s, 1);
-      mbar_init(bar_v_full0 + 8 * s, 1);
-      mbar_init(bar_kv_empty0 + 8 * s, 1);  // K slots: QK issuer; V slots: PV issuer
-    }
-    for (int b = 0; b < 2; ++b) {
+  if (warp == 0) {
+    // the barriers are initialised by the 32 lanes of warp 0, a few each
+    // (one thread initialising all of them serially took ~1500 cycles)
+    if (lane < G::kSlots) {
+      mbar_init(bar_k_full0 + 8 * lane, 1);
+      mbar_init(bar_v_full0 + 8 * lane, 1);
+      mbar_init(bar_kv_empty0 + 8 * lane, 1);  // K slots: QK issuer; V slots: PV issuer
+    } else if (lane >= 16 && lane < 18) {
+      const int b = lane - 16;
       mbar_init(bar_s_full0 + 8 * b, 1);
       mbar_init(bar_s_free0 + 8 * b, kSoftmaxWarps);
       mbar_init(bar_p_full0 + 8 * b, kSoftmaxWarps);
       mbar_init(bar_p_free0 + 8 * b, 1);
+    } else if (lane >= 18 && lane < 20) {
+      const int b = lane - 18;
       mbar_init(bar_o_full0 + 8 * b, 1);
       mbar_init(bar_o_free0 + 8 * b, kSoftmaxWarps);
       mbar_init(smem_addr(&ctl.drain[b]), 1);
-    }
-    for (int k = 0; k < kUnitQ; ++k) {
+    } else if (lane >= 20 && lane < 20 + kUnitQ) {
+      const int k = lane - 20;
       mbar_init(bar_uq_full0 + 8 * k, 1);
       mbar_init(bar_uq_empty0 + 8 * k, kUnitQReaders + (SPLIT ? 1 : 0));
+    } else if (lane == 31) {
+      mbar_init(bar_q_full, 1);
+      mbar_init(bar_q_empty, 1);
+      mbar_init(smem_addr(&ctl.pv_issued), 1);
+      ctl.abort_flag = 0;
     }
-    ctl.abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == kWarpQK) {
@@ -633,6 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // any CTA takes the next unit in the units' own order, longest first
         // when causal) or dealt round-robin; pushed to the CTA's unit queue.
         int unit = -1;
+        Unit u;
         for (;;) {
           int cand;
           if (p.sched != nullptr) {
@@ -640,11 +694,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (cand >= p.total_units) break;
           } else {
             if (t_static >= t_end) break;
-            cand = unit_at<CAUSAL>(t_static);
+            cand = unit_at<CAUSAL>(p, t_static);
             t_static += gridDim.x;
             if (cand >= p.total_units) continue;
           }
-          if (decode_unit<CAUSAL>(p, cand).rows > 0) {
+          u = decode_unit<CAUSAL>(p, cand);
+          if (u.rows > 0) {
             unit = cand;
             break;
           }
@@ -660,7 +715,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++kq;
         }
         if (unit < 0) break;
-        const Unit u = decode_unit<CAUSAL>(p, unit);
         if (u.n == 0) continue;
         if (!wait_phase(bar_q_empty, (qcount & 1u) ^ 1u, abort_flag, kSiteQEmpty, limit)) { ok = false; break; }
         mbar_arrive_expect_tx(bar_q_full, G::kTileBytes);
@@ -738,6 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t qcount = 0, tcount = 0, kq = 0;
     bool ok = true;
     const uint32_t qa = base + G::kOffQ;
+    const uint32_t bar_pv_issued = smem_addr(&ctl.pv_issued);
     while (ok) {
       const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
       if (unit == -2) { ok = false; break; }
@@ -745,6 +800,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit u = decode_unit<CAUSAL>(p, unit);
       if (u.n == 0) continue;
       if (!wait_warp(bar_q_full, qcount & 1u, abort_flag, kSiteQFull, limit)) { ok = false; break; }
+      // The unit's first S = Q K^T goes into the tensor pipe after the last
+      // P V of the unit before: queued ahead of it, the products of this unit
+      // would delay that unit's O (and the epilogue of the softmax warps, who
+      // need this S only after it) by two QK^T products.
+      if (qcount > 0 && !wait_warp(bar_pv_issued, (qcount - 1) & 1u, abort_flag, kSitePvIssued, limit)) {
+        ok = false;
+        break;
+      }
       ++qcount;
       for (int j = 0; j < u.n; ++j, ++tcount) {
         const uint32_t b = tcount & 1u;
@@ -836,7 +899,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit_elect(bar_p_free0 + 8 * b);
         mma_commit_elect(bar_kv_empty0 + 8 * slot);
-        if (j == u.n - 1) mma_commit_elect(bar_o_full0 + 8 * ob);
+        if (j == u.n - 1) {
+          mma_commit_elect(bar_o_full0 + 8 * ob);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&ctl.pv_issued));  // the next unit's first QK^T may follow
+        }
       }
       if (!ok) break;
       ++ucount;
@@ -1040,13 +1107,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           !wait_warp(bar_o_full0 + 8 * ob, (ocount / G::kOBufs) & 1u, abort_flag, kSiteOFull, limit))
         failed = true;
       ++ocount;
-      if (!failed) xch.xsum[half][r] = l;
+      const uint32_t bsum = ((tcount - 1u) & 1u) ^ 1u;  // the parity the unit's last tile did not use
+      if (!failed) xch.xmax[bsum][half][r] = l;
       if (named_bar_red_or(bar_pair, kPairThreads, *abort_flag != 0)) { ok = false; break; }
       tc_fence_after_sync();
-      const float l_row = l + xch.xsum[half ^ 1][r];
+      const float l_row = l + xch.xmax[bsum][half ^ 1][r];
       const bool has_key = l_row > 0.0f;
-      const float inv_l = has_key ? p.v_scale / l_row : 0.0f;
-      const float lse_row = has_key ? (m_used - PR::kShift + log2f(l_row)) * kLn2 : -INFINITY;
+      // hardware reciprocal and log2 (relative errors near 2^-23; O is
+      // rounded to bf16, LSE is compared at 1e-3)
+      const float inv_l = has_key ? p.v_scale * rcp_approx(l_row) : 0.0f;
+      const float lse_row = has_key ? (m_used - PR::kShift + lg2_approx(l_row)) * kLn2 : -INFINITY;
 #pragma unroll
       for (int q = 0; q < D / 64; ++q) {
         uint32_t o[32];
@@ -1058,16 +1128,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               w[e] = has_key ? pack_bf16x2(u2f(o[2 * e]) * inv_l, u2f(o[2 * e + 1]) * inv_l) : 0u;
-            uint4* dst = reinterpret_cast<uint4*>(o_dst + q * 32);
+            // The warp's 32 threads write 32 different rows, so each store
+            // instruction touches 32 lines: 32-byte stores (when O is 32-byte
+            // aligned, as every row half then is) halve the instructions and
+            // write whole sectors.
+            if (p.o_align32) {
+              st_global_v8(o_dst + q * 32, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
+              st_global_v8(o_dst + q * 32 + 16, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(o_dst + q * 32);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-          } else {  // normalised fp32 partial output
-            float4* dst = reinterpret_cast<float4*>(op_dst + q * 32);
+              for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            }
+          } else {  // normalised fp32 partial output (the workspace is 256-byte aligned)
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[e] = has_key ? make_float4(u2f(o[4 * e]) * inv_l, u2f(o[4 * e + 1]) * inv_l,
-                                             u2f(o[4 * e + 2]) * inv_l, u2f(o[4 * e + 3]) * inv_l)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int e = 0; e < 32; ++e) o[e] = has_key ? __float_as_uint(u2f(o[e]) * inv_l) : 0u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              st_global_v8(op_dst + q * 32 + 8 * e, *reinterpret_cast<const uint32_t(*)[8]>(&o[8 * e]));
           }
         }
       }
@@ -1260,6 +1338,35 @@ int head_group_for(int bh_count, int keys, int D, int elem_bytes) {
   return static_cast<int>(g);
 }
 
+FastDiv make_fastdiv(int divisor) {
+  FastDiv f;
+  f.d = static_cast<uint32_t>(divisor < 1 ? 1 : divisor);
+  uint32_t sh = 0;
+  while ((1ull << sh) < f.d) ++sh;
+  f.s = sh;
+  f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << sh) - f.d)) / f.d + 1);
+  return f;
+}
+
+// The launch's Params with the divisors of the unit decode filled in (grid:
+// the number of blocks the kernel is launched with).
+Params with_divisors(const Params& p0, int grid) {
+  Params p = p0;
+  const int bh = p.B * p.H;
+  const int hg = p.head_group < 1 ? 1 : p.head_group;
+  const int groups = bh > 0 ? (bh + hg - 1) / hg : 1;
+  p.fd_splits = make_fastdiv(p.num_splits);
+  p.fd_qtiles = make_fastdiv(p.n_qtiles);
+  p.fd_group_units = make_fastdiv(hg * p.n_qtiles);
+  p.fd_group_heads = make_fastdiv(hg);
+  p.last_group = groups - 1;
+  p.fd_last_heads = make_fastdiv(bh - (groups - 1) * hg);
+  p.fd_H = make_fastdiv(p.H);
+  p.fd_grid = make_fastdiv(grid);
+  p.o_align32 = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0 ? 1 : 0;
+  return p;
+}
+
 void clear_paged(Params& p) {
   p.block_table = nullptr;
   p.seqlens_k = nullptr;
@@ -1273,14 +1380,14 @@ template <int D, bool CAUSAL, bool FP8 = false, bool SPLIT = false>
 attn_status launch(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                    const Params& p, cudaStream_t stream) {
   auto kern = attn_fwd_kernel<D, CAUSAL, FP8, SPLIT>;
-  constexpr int smem = Geo<D, FP8>::kSmemBytes;
+  constexpr int smem = Geo<D, FP8, SPLIT>::kSmemBytes;
   if (!dev.smem_set[idx].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return ATTN_ERR_CUDA;
     dev.smem_set[idx].store(true, std::memory_order_release);
   }
   const int grid = p.total_units < dev.num_sms ? p.total_units : dev.num_sms;
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, p);
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, with_divisors(p, grid));
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

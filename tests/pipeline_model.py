@@ -2,7 +2,8 @@
 logic only; no attention arithmetic).
 
 Roles, as in the kernel: the TMA producer, the QK^T issuer, the softmax warps
-(one actor) and the P.V issuer.  Tensor memory as in the kernel, in both of
+(one actor) and the P.V issuer; the QK^T issuer starts a unit's products only
+once the P.V issuer has issued the last product of the unit before.  Tensor memory as in the kernel, in both of
 its protocols: (bf16) two S buffers released by the softmax once read, two
 P buffers, one O buffer; (E4M3) two S buffers with P_b written over S_b and
 released by the P V commit, and two O buffers that consecutive units
@@ -83,7 +84,7 @@ def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False,
     for b in (0, 1):
         bar(f"s_full{b}"); bar(f"s_free{b}"); bar(f"p_full{b}"); bar(f"p_free{b}"); bar(f"o_full{b}")
         bar(f"o_free{b}")
-    bar("q_full"); bar("q_empty")
+    bar("q_full"); bar("q_empty"); bar("pv_issued")
 
     def slot_of(pos):
         if rings:
@@ -175,6 +176,8 @@ def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False,
         ring = qcount = tcount = 0
         for n in units:
             yield lambda: bar("q_full").try_wait(qcount & 1, qcount)
+            if qcount > 0:   # the unit before has issued its last P V
+                yield lambda: bar("pv_issued").try_wait((qcount - 1) & 1, qcount - 1)
             qcount += 1
             for j in range(n):
                 b, use = tcount & 1, tcount >> 1
@@ -259,6 +262,8 @@ def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False,
                 if j == n - 1:
                     commits.append(bar(f"o_full{ob}"))
                 mma("pv", chk, commits)
+                if j == n - 1:
+                    bar("pv_issued").arrive()   # a plain arrive right after the issue
                 tcount += 1
             ring += 2 * n
             ucount += 1

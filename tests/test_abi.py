@@ -297,3 +297,4 @@ def test_fwd_abort_selftest_argument_checks(lib):
     assert f(A, A, A, A, A, 1, 2, 256, 0, 128, 0.1, 0, None, 0, 10_000, None) == attn.ATTN_ERR_SHAPE
     assert f(A, A, A, A, A, 1, 2, 256, 256, 96, 0.1, 0, None, 0, 10_000, None) == attn.ATTN_ERR_UNSUPPORTED_D
     assert f(A + 8, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, 0, 10_000, None) == attn.ATTN_ERR_ALIGN
+
