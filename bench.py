@@ -369,8 +369,8 @@ class Job(_JobBase):
             self.host = [q, kc, vc, cu, sk, table]
             self.paged_dims = (kc.shape[0], kc.shape[1], table.shape[1])
         elif is_fp8(w):
-            q, k8, _, vt8, kv = workloads_mod().generate_fp8(w)
-            self.host = [q, k8, vt8] + ([kv] if kv is not None else [])
+            q, k8, v8, vt8, kv = workloads_mod().generate_fp8(w)
+            self.host = [q, k8, v8 if w.v_layout == "rows" else vt8] + ([kv] if kv is not None else [])
         else:
             q, k, v, kv = generate(w, args.draw)
             self.host = [q, k, v] + ([kv] if kv is not None else [])
@@ -413,9 +413,12 @@ class Job(_JobBase):
         elif is_fp8(w):
             kv_ptr = ptr[3] if len(self.host) > 3 else None
 
+            layout = attn.ATTN_V_ROWS if w.v_layout == "rows" else attn.ATTN_V_TRANSPOSED
+
             def call():
-                return attn.attn_fwd_fp8(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), w.B, w.H, w.Sq, w.Sk,
-                                         w.D, w.scale, int(w.causal), kv_ptr, w.descale, w.descale, w.descale, sptr)
+                return attn.attn_fwd_fp8_ex(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), w.B, w.H, w.Sq,
+                                            w.Sk, w.D, w.scale, int(w.causal), kv_ptr, w.descale, w.descale,
+                                            w.descale, layout, sptr)
         elif is_varlen(w):
             def call():
                 return attn.attn_fwd_varlen(ptr[0], ptr[1], ptr[2], o.data_ptr(), lse.data_ptr(), ptr[3], ptr[3],
@@ -735,6 +738,7 @@ def main():
                               f"than the 129 MB L2"),
                        "parallelism": f"weak: {world} replica(s) of the workload, one per GPU",
                        "splits": args.splits,
+                       "v_layout": (w.v_layout if is_fp8(w) else "rows"),
                        "schedule": ("static" if args.static_schedule or w.causal else "dynamic") if varlen
                                    else "static"},
             "roofline": roofline,

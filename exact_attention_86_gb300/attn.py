@@ -34,6 +34,9 @@ ATTN_ERR_DEVICE_TIMEOUT = 7
 ATTN_ERR_UNSUPPORTED_DEVICE = 8
 ATTN_ERR_WORKSPACE = 9
 
+ATTN_V_ROWS = 0        # E4M3 V as [B, H, Sk, D]
+ATTN_V_TRANSPOSED = 1  # E4M3 V as [B, H, D, Sk]
+
 #: Functions declared in include/attn.h, with their ctypes signatures.
 SIGNATURES = {
     "attn_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
@@ -43,6 +46,10 @@ SIGNATURES = {
                                     ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
                                     ctypes.c_float, ctypes.c_float, ctypes.c_void_p]),
+    "attn_fwd_fp8_ex": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
+                                       ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
     "attn_fwd_varlen": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
@@ -120,6 +127,13 @@ def attn_fwd_fp8(q: int, k: int, v_t: int, o: int, lse: int, B: int, H: int, Sq:
                  v_descale: float, stream: Optional[int]) -> int:
     return lib().attn_fwd_fp8(q, k, v_t, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, q_descale, k_descale,
                               v_descale, stream)
+
+
+def attn_fwd_fp8_ex(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
+                    scale: float, causal: int, kv_lens: Optional[int], q_descale: float, k_descale: float,
+                    v_descale: float, v_layout: int, stream: Optional[int]) -> int:
+    return lib().attn_fwd_fp8_ex(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, q_descale,
+                                 k_descale, v_descale, v_layout, stream)
 
 
 def attn_fwd_varlen(q: int, k: int, v: int, o: int, lse: int, cu_q: int, cu_k: int, batch: int,
@@ -284,21 +298,25 @@ def forward_splitkv(q, k, v, num_splits: Optional[int] = None, scale: Optional[f
     return out, lse
 
 
-def forward_fp8(q8, k8, v8_t, q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0,
-                scale: Optional[float] = None, causal: bool = False, kv_lens=None, out=None, lse=None):
+def forward_fp8(q8, k8, v8, q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0,
+                scale: Optional[float] = None, causal: bool = False, kv_lens=None, out=None, lse=None,
+                v_layout: int = ATTN_V_TRANSPOSED):
     """FP8 forward on torch CUDA tensors of E4M3 codes (``torch.uint8`` or
-    ``torch.float8_e4m3fn``): ``q8 [B,H,Sq,D]``, ``k8 [B,H,Sk,D]`` and
-    ``v8_t [B,H,D,Sk]`` (V transposed).  Returns ``(o bf16 [B,H,Sq,D],
-    lse fp32 [B,H,Sq])``, written into ``out`` / ``lse`` when given."""
+    ``torch.float8_e4m3fn``): ``q8 [B,H,Sq,D]``, ``k8 [B,H,Sk,D]`` and ``v8``,
+    which is ``[B,H,D,Sk]`` (V transposed) with ``v_layout=ATTN_V_TRANSPOSED``
+    (the default) or ``[B,H,Sk,D]`` with ``v_layout=ATTN_V_ROWS``.  Returns
+    ``(o bf16 [B,H,Sq,D], lse fp32 [B,H,Sq])``, written into ``out`` / ``lse``
+    when given."""
     import torch
 
-    for name, t in (("q8", q8), ("k8", k8), ("v8_t", v8_t)):
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
         if t.element_size() != 1 or not t.is_cuda or not t.is_contiguous() or t.dim() != 4:
             raise ValueError(f"{name} must be a contiguous 4-d CUDA tensor of 1-byte E4M3 codes")
     B, H, Sq, D = q8.shape
     Sk = k8.shape[2]
-    if tuple(k8.shape) != (B, H, Sk, D) or tuple(v8_t.shape) != (B, H, D, Sk):
-        raise ValueError("k8 must be [B,H,Sk,D] and v8_t [B,H,D,Sk]")
+    v_shape = (B, H, Sk, D) if v_layout == ATTN_V_ROWS else (B, H, D, Sk)
+    if tuple(k8.shape) != (B, H, Sk, D) or tuple(v8.shape) != v_shape:
+        raise ValueError(f"k8 must be [B,H,Sk,D] and v8 {list(v_shape)}")
     if kv_lens is not None and (kv_lens.dtype != torch.int32 or kv_lens.device != q8.device):
         raise ValueError("kv_lens must be int32 on q's device")
     if scale is None:
@@ -306,9 +324,10 @@ def forward_fp8(q8, k8, v8_t, q_descale: float = 1.0, k_descale: float = 1.0, v_
     out, lse = _outputs(out, lse, (B, H, Sq, D), (B, H, Sq), q8.device)
     with torch.cuda.device(q8.device):
         stream = torch.cuda.current_stream(q8.device).cuda_stream
-        st = attn_fwd_fp8(q8.data_ptr(), k8.data_ptr(), v8_t.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, Sq,
-                          Sk, D, float(scale), int(bool(causal)), None if kv_lens is None else kv_lens.data_ptr(),
-                          float(q_descale), float(k_descale), float(v_descale), stream)
+        st = attn_fwd_fp8_ex(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H,
+                             Sq, Sk, D, float(scale), int(bool(causal)),
+                             None if kv_lens is None else kv_lens.data_ptr(), float(q_descale), float(k_descale),
+                             float(v_descale), int(v_layout), stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_fp8")
     return out, lse

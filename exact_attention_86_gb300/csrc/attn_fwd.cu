@@ -279,6 +279,9 @@ struct Params {
   // producer leaves out its K fill with this index, so the bounded wait of the
   // fill's consumer must give up and every role must drain; -1 otherwise.
   int selftest_skip_fill = -1;
+  // E4M3 only: V given in rows, [B, H, Sk, D] (the P V product then reads it
+  // MN-major, like bf16 V); 0: V given transposed, [B, H, D, Sk] (K-major)
+  int v_rows = 0;
   int o_align32 = 0;       // o is 32-byte aligned: the epilogue writes 32-byte pieces
 };
 
@@ -626,9 +629,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key0 = (u.j0 + j) * kBK;
     const uint32_t dst = base + G::kOffRing + slot * G::kTileBytes;
     const bool packed = p.cu_q != nullptr;  // padded maps are (D, S, H, B); packed maps are (D, H, tokens, 1)
-    if (FP8 && is_v) {
-      // E4M3 V is stored transposed, (Sk, D, H, B): the tile is 128 rows of
-      // D, each 128 keys long (K-major for the P V product)
+    if (FP8 && is_v && !p.v_rows) {
+      // E4M3 V given transposed, (Sk, D, H, B): the tile is 128 rows of D,
+      // each 128 keys long (K-major for the P V product)
       tma_load_4d_hint(dst, m, full, key0, 0, u.h, u.b, pol);
     } else if (p.block_table == nullptr) {
       for (int c = 0; c < G::kChunks; ++c)
@@ -883,10 +886,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t va = base + G::kOffRing + slot * G::kTileBytes;
         if constexpr (FP8) {
           // O += P_b V_j with E4M3 P (32 keys = 8 columns per MMA, four per
-          // column) and V^T K-major in shared memory (rows of D, keys contiguous).
+          // column).  V given transposed: K-major in shared memory (rows of D,
+          // keys contiguous), 32 keys = 32 bytes along each row per MMA.  V in
+          // rows: MN-major (rows of keys, D contiguous: one 128-byte swizzle
+          // atom wide), 32 keys = 32 rows of 128 bytes per MMA, 8-key groups
+          // 1024 bytes apart.
+          const uint32_t vstep = p.v_rows ? 32u * 128u : 32u;
 #pragma unroll
           for (int kk = 0; kk < kBK / 32; ++kk)
-            mma_ts_f8_elect(tOb, tSb + G::p_col(kk), sdesc_sw128(va + kk * 32, 16, 1024), p.idesc_pv,
+            mma_ts_f8_elect(tOb, tSb + G::p_col(kk), sdesc_sw128(va + kk * vstep, 16, 1024), p.idesc_pv,
                             (j > 0 || kk > 0) ? 1u : 0u);
         } else {
           // O += P_b V_j: P from TMEM (16 keys = 8 columns per MMA), V MN-major in
@@ -1601,16 +1609,19 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      reinterpret_cast<cudaStream_t>(stream));
 }
 
-attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o, float* lse, int B, int H, int Sq,
-                         int Sk, int D, float scale, int causal, const int32_t* kv_lens, float q_descale,
-                         float k_descale, float v_descale, attn_stream_t stream) {
+attn_status attn_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
+                            int Sk, int D, float scale, int causal, const int32_t* kv_lens, float q_descale,
+                            float k_descale, float v_descale, int v_layout, attn_stream_t stream) {
+  if (v_layout != ATTN_V_ROWS && v_layout != ATTN_V_TRANSPOSED) return ATTN_ERR_SHAPE;
+  const bool v_rows = v_layout == ATTN_V_ROWS;
+  const void* v_t = v;
   if (B < 0 || H < 0 || Sq < 0 || Sk < 0) return ATTN_ERR_SHAPE;
   if (D != 128) return ATTN_ERR_UNSUPPORTED_D;
   if (!std::isfinite(scale) || !std::isfinite(q_descale) || !std::isfinite(k_descale) || !std::isfinite(v_descale))
     return ATTN_ERR_SCALE;
   const double qk_scale = static_cast<double>(scale) * q_descale * k_descale;
   if (!std::isfinite(static_cast<float>(qk_scale))) return ATTN_ERR_SCALE;
-  if (Sk % 16 != 0) return ATTN_ERR_SHAPE;  // V^T rows are Sk bytes: a TMA stride must be a multiple of 16
+  if (!v_rows && Sk % 16 != 0) return ATTN_ERR_SHAPE;  // V^T rows are Sk bytes: a TMA stride must be a multiple of 16
   if (B == 0 || H == 0 || Sq == 0) return ATTN_OK;
   if (q == nullptr || o == nullptr || lse == nullptr) return ATTN_ERR_NULLPTR;
   if (Sk > 0 && (k == nullptr || v_t == nullptr)) return ATTN_ERR_NULLPTR;
@@ -1627,7 +1638,8 @@ attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o,
   CUtensorMap mq, mk, mv;
   if (!make_map_e4m3(&mq, q, D, Sq, H, B)) return ATTN_ERR_CUDA;
   if (Sk > 0) {
-    if (!make_map_e4m3(&mk, k, D, Sk, H, B) || !make_map_e4m3(&mv, v_t, Sk, D, H, B)) return ATTN_ERR_CUDA;
+    if (!make_map_e4m3(&mk, k, D, Sk, H, B)) return ATTN_ERR_CUDA;
+    if (v_rows ? !make_map_e4m3(&mv, v, D, Sk, H, B) : !make_map_e4m3(&mv, v_t, Sk, D, H, B)) return ATTN_ERR_CUDA;
   } else {  // never dereferenced: with no keys every unit has zero K tiles
     mk = mq;
     mv = mq;
@@ -1655,10 +1667,18 @@ attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o,
   p.c = static_cast<float>(std::fabs(qk_scale) * 1.4426950408889634);
   p.v_scale = v_descale;
   p.idesc_qk = idesc_e4m3_f32(kBQ, kBK, qk_scale < 0.0);
-  p.idesc_pv = idesc_e4m3_f32(kBQ, D, false);
+  p.idesc_pv = idesc_e4m3_f32(kBQ, D, false, v_rows);
+  p.v_rows = v_rows ? 1 : 0;
   p.wait_limit_ns = kWaitLimitNs;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return causal ? launch<128, true, true>(*dev, 4, mq, mk, mv, p, s) : launch<128, false, true>(*dev, 5, mq, mk, mv, p, s);
+}
+
+attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o, float* lse, int B, int H, int Sq,
+                         int Sk, int D, float scale, int causal, const int32_t* kv_lens, float q_descale,
+                         float k_descale, float v_descale, attn_stream_t stream) {
+  return attn_fwd_fp8_ex(q, k, v_t, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, q_descale, k_descale, v_descale,
+                         ATTN_V_TRANSPOSED, stream);
 }
 
 attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -207,11 +207,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool negate_
 }
 
 // Instruction descriptor, kind::f8f6f4 with E4M3 A and B (format code 0 in
-// bits 7-9 and 10-12), f32 D; every other field as for kind::f16.  Both
-// operands K-major.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool negate_a) {
-  return (1u << 4) | ((negate_a ? 1u : 0u) << 13) | (static_cast<uint32_t>(N >> 3) << 17) |
-         (static_cast<uint32_t>(M >> 4) << 24);
+// bits 7-9 and 10-12), f32 D; every other field as for kind::f16.  A is
+// K-major; B K-major, or MN-major when b_mn_major (8-bit operands may be
+// MN-major; the 6- and 4-bit ones may not).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool negate_a, bool b_mn_major = false) {
+  return (1u << 4) | ((negate_a ? 1u : 0u) << 13) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor with 128-byte swizzling: bits 0-13 start

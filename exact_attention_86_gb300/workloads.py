@@ -247,8 +247,10 @@ class Fp8Workload(Workload):
     """A padded workload with FP8 (E4M3) inputs: the bf16 recipe's float32
     draws (times std) are rounded to E4M3 codes with torch's float8_e4m3fn
     conversion instead of to bf16; every descale is ``descale``.  V is also
-    given transposed (``[B, H, D, Sk]``), the layout the FP8 kernel reads."""
+    given transposed (``[B, H, D, Sk]``); ``v_layout`` names the layout the
+    benchmark passes ("rows": ``[B, H, Sk, D]``, "transposed")."""
     descale: float = 1.0
+    v_layout: str = "rows"
 
     @property
     def min_bytes(self) -> int:
@@ -257,12 +259,14 @@ class Fp8Workload(Workload):
                 + 4 * self.B * self.H * self.Sq)
 
     def label(self) -> str:
-        return super().label() + ", E4M3 inputs"
+        return super().label() + f", E4M3 inputs, V {'[B,H,Sk,D]' if self.v_layout == 'rows' else '[B,H,D,Sk]'}"
 
 
 FP8_WORKLOADS = {
     "s8192_d128_fp8": Fp8Workload("s8192_d128_fp8", 2, 16, 8192, 8192, 128, False, seed=3),
     "s8192_d128_causal_fp8": Fp8Workload("s8192_d128_causal_fp8", 2, 16, 8192, 8192, 128, True, seed=3),
+    "s8192_d128_fp8_vt": Fp8Workload("s8192_d128_fp8_vt", 2, 16, 8192, 8192, 128, False, seed=3,
+                                     v_layout="transposed"),
 }
 
 

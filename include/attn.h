@@ -110,6 +110,26 @@ attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o,
                          int Sk, int D, float scale, int causal, const int32_t* kv_lens, float q_descale,
                          float k_descale, float v_descale, attn_stream_t stream);
 
+/* Layout of the E4M3 V operand of attn_fwd_fp8_ex. */
+typedef enum attn_v_layout {
+  ATTN_V_ROWS = 0,       /* [B, H, Sk, D], like q and k (D innermost)          */
+  ATTN_V_TRANSPOSED = 1  /* [B, H, D, Sk] (keys innermost), as attn_fwd_fp8    */
+} attn_v_layout;
+
+/*
+ * attn_fwd_fp8_ex — attn_fwd_fp8 with the layout of V chosen by `v_layout`.
+ * With ATTN_V_ROWS, v holds E4M3 codes [B, H, Sk, D] (contiguous, 16-byte
+ * aligned), the layout q and k have, and the P V product reads each V tile
+ * MN-major straight from the tile the copy engine loaded; no transposition
+ * is needed anywhere and Sk may have any value.  With ATTN_V_TRANSPOSED the
+ * call is exactly attn_fwd_fp8 (v = V^T, Sk a multiple of 16).  Both layouts
+ * give bit-identical results: the products see the same values in the same
+ * order.  Any other v_layout: ATTN_ERR_SHAPE.
+ */
+attn_status attn_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
+                            int Sk, int D, float scale, int causal, const int32_t* kv_lens, float q_descale,
+                            float k_descale, float v_descale, int v_layout, attn_stream_t stream);
+
 /*
  * attn_fwd_varlen — the same forward over a packed batch of variable-length
  * sequences (the ragged tensors of continuous batching, "Fused Multi-Head
@@ -355,7 +375,7 @@ attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t 
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 10
+#define ATTN_ABI_VERSION 11
 
 #ifdef __cplusplus
 }

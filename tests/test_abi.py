@@ -298,3 +298,14 @@ def test_fwd_abort_selftest_argument_checks(lib):
     assert f(A, A, A, A, A, 1, 2, 256, 256, 96, 0.1, 0, None, 0, 10_000, None) == attn.ATTN_ERR_UNSUPPORTED_D
     assert f(A + 8, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, 0, 10_000, None) == attn.ATTN_ERR_ALIGN
 
+
+def test_fp8_ex_argument_checks(lib):
+    # each call ends at a host-side check (no device query, no launch)
+    f = attn.attn_fwd_fp8_ex
+    args = (A, A, A, A, A, 1, 2, 256, 256)
+    assert f(*args, 128, 0.1, 0, None, 1.0, 1.0, 1.0, 2, None) == attn.ATTN_ERR_SHAPE      # unknown layout
+    assert f(*args, 128, 0.1, 0, None, 1.0, 1.0, 1.0, -1, None) == attn.ATTN_ERR_SHAPE
+    assert f(*args, 64, 0.1, 0, None, 1.0, 1.0, 1.0, 0, None) == attn.ATTN_ERR_UNSUPPORTED_D
+    assert f(A, A, A, A, A, 1, 2, 256, 100, 128, 0.1, 0, None, 1.0, 1.0, 1.0, 1, None) == attn.ATTN_ERR_SHAPE
+    assert f(*args, 128, float("nan"), 0, None, 1.0, 1.0, 1.0, 0, None) == attn.ATTN_ERR_SCALE
+    assert f(A + 8, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, 1.0, 1.0, 1.0, 0, None) == attn.ATTN_ERR_ALIGN

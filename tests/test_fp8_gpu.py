@@ -48,13 +48,23 @@ def _inputs(B, H, Sq, Sk, seed, std=1.0, D=128):
     return q, k, v
 
 
-def _run(q, k, v, scale, causal=False, kv=None, qd=1.0, kd=1.0, vd=1.0):
+ROWS, TRANSPOSED = attn.ATTN_V_ROWS, attn.ATTN_V_TRANSPOSED
+LAYOUTS = pytest.mark.parametrize("layout", [ROWS, TRANSPOSED], ids=["v_rows", "v_transposed"])
+
+
+def _run(q, k, v, scale, causal=False, kv=None, qd=1.0, kd=1.0, vd=1.0, layout=TRANSPOSED):
+    """The E4M3 forward with V in the given layout, into NaN-filled outputs."""
     dev = torch.device("cuda:0")
-    vt = v.transpose(-1, -2).contiguous()
-    o, lse = attn.forward_fp8(q.to(dev), k.to(dev), vt.to(dev), qd, kd, vd, scale=scale, causal=causal,
-                              kv_lens=None if kv is None else torch.tensor(kv, dtype=torch.int32, device=dev))
+    vl = v if layout == ROWS else v.transpose(-1, -2).contiguous()
+    B, H, Sq, D = q.shape
+    o = nan_filled((B, H, Sq, D), torch.bfloat16, dev)
+    lse = nan_filled((B, H, Sq), torch.float32, dev)
+    attn.forward_fp8(q.to(dev), k.to(dev), vl.to(dev), qd, kd, vd, scale=scale, causal=causal,
+                     kv_lens=None if kv is None else torch.tensor(kv, dtype=torch.int32, device=dev), out=o, lse=lse,
+                     v_layout=layout)
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
+    assert_no_nan(o, lse, what="fp8")
     return o, lse
 
 
@@ -98,31 +108,61 @@ SHAPES = [
 ]
 
 
+@LAYOUTS
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_matches_oracle(shape, causal):
+def test_fp8_matches_oracle(shape, causal, layout):
     B, H, Sq, Sk = shape
     q, k, v = _inputs(B, H, Sq, Sk, seed=Sq + Sk + int(causal))
     scale = 1.0 / math.sqrt(128)
-    o, lse = _run(q, k, v, scale, causal)
+    o, lse = _run(q, k, v, scale, causal, layout=layout)
     o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, scale, causal)
-    check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax, f"fp8 {shape} causal={causal}")
+    check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax,
+              f"fp8 {shape} causal={causal} layout={layout}")
 
 
+@LAYOUTS
 @pytest.mark.parametrize("kv", [[0, 1], [16, 143], [128, 129], [255, 256]])
-def test_fp8_key_lengths(kv):
+def test_fp8_key_lengths(kv, layout):
     q, k, v = _inputs(2, 2, 200, 256, seed=sum(kv))
-    o, lse = _run(q, k, v, 0.09, kv=kv)
+    o, lse = _run(q, k, v, 0.09, kv=kv, layout=layout)
     o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, 0.09, kv=kv)
-    check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax, f"fp8 kv={kv}")
+    check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax, f"fp8 kv={kv} layout={layout}")
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 1), (1, 2, 100, 100), (2, 1, 300, 333), (1, 2, 129, 1000)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_v_rows_any_key_count(shape, causal):
+    """V in rows has no key-count restriction (the transposed layout needs a
+    multiple of 16): ragged key counts against the oracle."""
+    B, H, Sq, Sk = shape
+    q, k, v = _inputs(B, H, Sq, Sk, seed=Sq * 3 + Sk + int(causal))
+    scale = 1.0 / math.sqrt(128)
+    o, lse = _run(q, k, v, scale, causal, layout=ROWS)
+    o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, scale, causal)
+    check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax, f"fp8 rows {shape}")
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 100, 144), (2, 2, 300, 1024), (1, 4, 1000, 2048)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_v_layouts_bitwise_identical(shape, causal):
+    """The two V layouts feed the products the same values in the same order:
+    identical bits."""
+    B, H, Sq, Sk = shape
+    q, k, v = _inputs(B, H, Sq, Sk, seed=Sq + 7 * Sk + int(causal), std=2.0)
+    o_r, l_r = _run(q, k, v, 0.07, causal, layout=ROWS)
+    o_t, l_t = _run(q, k, v, 0.07, causal, layout=TRANSPOSED)
+    assert torch.equal(o_r.view(torch.int16), o_t.view(torch.int16))
+    assert torch.equal(l_r.view(torch.int32), l_t.view(torch.int32))
 
 
 def test_fp8_descales_and_large_scores():
     # std 4 inputs (scores std about 16 after scaling by q and k descales) move the max often
     q, k, v = _inputs(1, 2, 256, 512, seed=41, std=4.0)
-    o, lse = _run(q, k, v, 0.05, qd=0.5, kd=2.0, vd=0.25)
-    o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, 0.05, qd=0.5, kd=2.0, vd=0.25)
-    check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax, "fp8 descales")
+    for layout in (ROWS, TRANSPOSED):
+        o, lse = _run(q, k, v, 0.05, qd=0.5, kd=2.0, vd=0.25, layout=layout)
+        o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, 0.05, qd=0.5, kd=2.0, vd=0.25)
+        check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax, f"fp8 descales {layout}")
 
 
 def test_fp8_descale_laws_bitwise():
@@ -156,8 +196,9 @@ def test_fp8_workload_every_tile(name):
     dev = torch.device("cuda:0")
     o = nan_filled((w.B, w.H, w.Sq, w.D), torch.bfloat16, dev)
     lse = nan_filled((w.B, w.H, w.Sq), torch.float32, dev)
-    attn.forward_fp8(q.to(dev), k.to(dev), vt.to(dev), w.descale, w.descale, w.descale, scale=w.scale,
-                     causal=w.causal, out=o, lse=lse)
+    layout = ROWS if w.v_layout == "rows" else TRANSPOSED
+    attn.forward_fp8(q.to(dev), k.to(dev), (v if layout == ROWS else vt).to(dev), w.descale, w.descale, w.descale,
+                     scale=w.scale, causal=w.causal, out=o, lse=lse, v_layout=layout)
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
     assert_no_nan(o, lse, what=name)
@@ -174,11 +215,13 @@ def test_fp8_workload_every_tile(name):
                       f"{name} b{b} h{h}")
 
 
-def test_fp8_repeated_launches_are_bitwise_identical():
+@LAYOUTS
+def test_fp8_repeated_launches_are_bitwise_identical(layout):
     q, k, v = _inputs(2, 8, 1024, 4096, seed=53)
     dev = torch.device("cuda:0")
-    qd, kd, vtd = q.to(dev), k.to(dev), v.transpose(-1, -2).contiguous().to(dev)
-    outs = [attn.forward_fp8(qd, kd, vtd, causal=True) for _ in range(30)]
+    qd, kd = q.to(dev), k.to(dev)
+    vd = (v if layout == ROWS else v.transpose(-1, -2).contiguous()).to(dev)
+    outs = [attn.forward_fp8(qd, kd, vd, causal=True, v_layout=layout) for _ in range(30)]
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
     for o, lse in outs[1:]:
