@@ -114,18 +114,25 @@ __device__ __align__(256) uint8_t g_splitkv_scratch[ATTN_SPLITKV_SCRATCH_BYTES];
 template <int D, bool FP8 = false, bool SPLIT = false>
 struct Geo {
   static_assert(D == 64 || D == 128, "head dim");
-  static_assert(!FP8 || D == 128, "E4M3 path: D = 128");
   static constexpr int kElem = FP8 ? 1 : 2;            // bytes per element of Q, K, V
+  static constexpr int kRowBytes = D * kElem;          // one row of a Q or K tile (and of V in rows)
   static constexpr int kTileBytes = 128 * D * kElem;   // one Q, K or V tile (128 rows)
-  static constexpr int kChunkBytes = 128 * 128;        // 128 rows x 128 B (one 128-B swizzle column)
-  static constexpr int kChunks = D * kElem / 128;
-  static constexpr int kChunkElems = 128 / kElem;      // elements per 128-B row of a chunk
+  // Rows of 128 bytes (bf16 D = 64, E4M3 D = 128) or 256 bytes (bf16 D = 128,
+  // two 64-column chunks) use the 128-byte swizzle; the 64-byte rows of E4M3
+  // at D = 64 the 64-byte swizzle (8-row atoms of 64 bytes, 512 bytes apart).
+  static constexpr bool kSw64 = kRowBytes == 64;
+  static constexpr int kChunkBytes = kSw64 ? 128 * 64 : 128 * 128;  // 128 rows of one swizzle column
+  static constexpr int kChunks = kSw64 ? 1 : kRowBytes / 128;
+  static constexpr int kChunkElems = kSw64 ? 64 : 128 / kElem;      // elements per row of a chunk
+  static constexpr uint32_t kSwMode = kSw64 ? kSmemSwizzle64B : kSmemSwizzle128B;
+  static constexpr uint32_t kSbo = kSw64 ? 512 : 1024;               // 8-row groups of a chunk
   static constexpr int kKSteps = D * kElem / 32;       // QK^T instructions: 32 B of D each
   // K and V tiles in shared memory.  Padded batches (one ring): as many as
   // the 227 KB a block may use leave after the control block, the exchange
   // buffers and Q.  Packed and paged batches (split rings) at D = 128: 3 K
   // and 2 V slots (measured faster than 3 + 3 there).
-  static constexpr int kSlots = (D == 128 && !FP8) ? (SPLIT ? ATTN_SPLIT_SLOTS_K + ATTN_SPLIT_SLOTS_V : 6) : 12;
+  static constexpr int kSlots =
+      (D == 128 && !FP8) ? (SPLIT ? ATTN_SPLIT_SLOTS_K + ATTN_SPLIT_SLOTS_V : 6) : (kSw64 ? 16 : 12);
   // Two layouts of the K/V tiles over those slots (both modelled by the
   // protocol tests):
   //  single ring (padded batches): the producer fills K_0 V_0 K_1 V_1 ... in
@@ -186,7 +193,10 @@ struct Geo {
   // kernel entry), as the 128-byte swizzle atoms need, so no slack is added.
   static constexpr int kOffQ = 3072;
   static constexpr int kOffRing = kOffQ + kTileBytes;
-  static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes;
+  // E4M3 at D = 64 leaves room to spare: an unused tile-sized pad after the
+  // ring keeps any read of the last slot inside the allocation
+  static constexpr int kPadBytes = kSw64 ? kTileBytes : 0;
+  static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes + kPadBytes;
   static_assert(kOffQ % 1024 == 0 || kTileBytes % 1024 == 0, "swizzle atoms 1024-byte aligned");
   static_assert(kSmemBytes <= 232448, "shared memory per block");
   static_assert(kSlots <= 16, "barrier initialisation: one lane per slot among lanes 0-15");
@@ -204,7 +214,7 @@ struct Unit {
 
 struct Ctrl {
   uint64_t q_full, q_empty;
-  uint64_t k_full[12], v_full[12], kv_empty[12];  // per slot; full: one per kind (Geo::fill_of)
+  uint64_t k_full[16], v_full[16], kv_empty[16];  // per slot; full: one per kind (Geo::fill_of)
   uint64_t s_full[2], s_free[2], p_full[2], p_free[2];
   uint64_t o_full[2], o_free[2];
   uint64_t pv_issued;  // the P V issuer has issued the last product of a unit
@@ -630,8 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t dst = base + G::kOffRing + slot * G::kTileBytes;
     const bool packed = p.cu_q != nullptr;  // padded maps are (D, S, H, B); packed maps are (D, H, tokens, 1)
     if (FP8 && is_v && !p.v_rows) {
-      // E4M3 V given transposed, (Sk, D, H, B): the tile is 128 rows of D,
-      // each 128 keys long (K-major for the P V product)
+      // E4M3 V given transposed, (Sk, D, H, B): the tile is D rows, each 128
+      // keys long (K-major for the P V product)
       tma_load_4d_hint(dst, m, full, key0, 0, u.h, u.b, pol);
     } else if (p.block_table == nullptr) {
       for (int c = 0; c < G::kChunks; ++c)
@@ -834,11 +844,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < G::kKSteps; ++kk) {
           const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
           if constexpr (FP8)
-            mma_ss_f8_elect(tmem + G::kTmemS + 128u * b, sdesc_sw128(qa + off, 16, 1024),
-                            sdesc_sw128(ka + off, 16, 1024), p.idesc_qk, kk > 0 ? 1u : 0u);
+            mma_ss_f8_elect(tmem + G::kTmemS + 128u * b, sdesc_sw(qa + off, 16, G::kSbo, G::kSwMode),
+                            sdesc_sw(ka + off, 16, G::kSbo, G::kSwMode), p.idesc_qk, kk > 0 ? 1u : 0u);
           else
-            mma_ss_elect(tmem + G::kTmemS + 128u * b, sdesc_sw128(qa + off, 16, 1024),
-                         sdesc_sw128(ka + off, 16, 1024), p.idesc_qk, kk > 0 ? 1u : 0u);
+            mma_ss_elect(tmem + G::kTmemS + 128u * b, sdesc_sw(qa + off, 16, G::kSbo, G::kSwMode),
+                         sdesc_sw(ka + off, 16, G::kSbo, G::kSwMode), p.idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit_elect(bar_s_full0 + 8 * b);
         mma_commit_elect(bar_kv_empty0 + 8 * slot);
@@ -886,16 +896,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t va = base + G::kOffRing + slot * G::kTileBytes;
         if constexpr (FP8) {
           // O += P_b V_j with E4M3 P (32 keys = 8 columns per MMA, four per
-          // column).  V given transposed: K-major in shared memory (rows of D,
-          // keys contiguous), 32 keys = 32 bytes along each row per MMA.  V in
-          // rows: MN-major (rows of keys, D contiguous: one 128-byte swizzle
-          // atom wide), 32 keys = 32 rows of 128 bytes per MMA, 8-key groups
-          // 1024 bytes apart.
-          const uint32_t vstep = p.v_rows ? 32u * 128u : 32u;
+          // column).  V given transposed: K-major in shared memory (D rows of
+          // 128 keys, 128-byte swizzle), 32 keys = 32 bytes along each row per
+          // MMA.  V in rows: MN-major (rows of keys, D contiguous: one swizzle
+          // atom wide, 128 or 64 bytes), 32 keys = 32 rows per MMA.
 #pragma unroll
-          for (int kk = 0; kk < kBK / 32; ++kk)
-            mma_ts_f8_elect(tOb, tSb + G::p_col(kk), sdesc_sw128(va + kk * vstep, 16, 1024), p.idesc_pv,
-                            (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBK / 32; ++kk) {
+            const uint64_t vdesc =
+                p.v_rows ? sdesc_sw(va + kk * 32 * G::kRowBytes, 16, G::kSbo, G::kSwMode)
+                         : sdesc_sw(va + kk * 32, 16, 1024, kSmemSwizzle128B);
+            mma_ts_f8_elect(tOb, tSb + G::p_col(kk), vdesc, p.idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+          }
         } else {
           // O += P_b V_j: P from TMEM (16 keys = 8 columns per MMA), V MN-major in
           // smem (LBO = distance between 64-column chunks of D, SBO = 8 keys x 128 B).
@@ -1242,7 +1253,7 @@ struct DeviceInfo {
   int num_sms = 0;
   // dynamic shared memory attribute set for kernel instantiation i (set at
   // most once; two host threads may both set it, which is harmless)
-  std::atomic<bool> smem_set[12] = {};
+  std::atomic<bool> smem_set[14] = {};
   std::atomic<bool> bwd_smem_set[4] = {};
 };
 constexpr int kMaxDevices = 64;
@@ -1304,19 +1315,22 @@ bool make_map(CUtensorMap* m, const void* ptr, int B, int H, int S, int D, int b
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Rank-4 maps over E4M3 tensors (one byte per element), 128-B swizzled boxes
-// of 128 x 128 bytes.  Q and K [B,H,S,D] as (D, S, H, B); V^T [B,H,D,Sk] as
-// (Sk, D, H, B), so that a box is 128 rows of D, each 128 keys long.  Bytes
-// past an edge read as zeros.
-bool make_map_e4m3(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, int H, int B) {
+// Rank-4 maps over E4M3 tensors (one byte per element), (inner, rows, H, B)
+// with a box of box_inner bytes x box_rows rows, swizzled to the box's row
+// length (128 or 64 bytes).  Q, K and V in rows [B,H,S,D] as (D, S, H, B),
+// boxes of 128 rows of D bytes; V^T [B,H,D,Sk] as (Sk, D, H, B), boxes of D
+// rows, each 128 keys long.  Bytes past an edge read as zeros.
+bool make_map_e4m3(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t rows, int H, int B, uint32_t box_inner,
+                   uint32_t box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = encoder();
   if (encode == nullptr) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)H, (cuuint64_t)B};
   const cuuint64_t strides[3] = {(cuuint64_t)inner, (cuuint64_t)(inner * rows), (cuuint64_t)(inner * rows * H)};
-  const cuuint32_t box[4] = {128, 128, 1, 1};
+  const cuuint32_t box[4] = {box_inner, box_rows, 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapSwizzle sw = box_inner == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   return encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1616,7 +1630,7 @@ attn_status attn_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o
   const bool v_rows = v_layout == ATTN_V_ROWS;
   const void* v_t = v;
   if (B < 0 || H < 0 || Sq < 0 || Sk < 0) return ATTN_ERR_SHAPE;
-  if (D != 128) return ATTN_ERR_UNSUPPORTED_D;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED_D;
   if (!std::isfinite(scale) || !std::isfinite(q_descale) || !std::isfinite(k_descale) || !std::isfinite(v_descale))
     return ATTN_ERR_SCALE;
   const double qk_scale = static_cast<double>(scale) * q_descale * k_descale;
@@ -1636,10 +1650,12 @@ attn_status attn_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o
   attn_status st = device_info(&dev);
   if (st != ATTN_OK) return st;
   CUtensorMap mq, mk, mv;
-  if (!make_map_e4m3(&mq, q, D, Sq, H, B)) return ATTN_ERR_CUDA;
+  const uint32_t dbox = static_cast<uint32_t>(D);  // bytes of a row of D
+  if (!make_map_e4m3(&mq, q, D, Sq, H, B, dbox, 128)) return ATTN_ERR_CUDA;
   if (Sk > 0) {
-    if (!make_map_e4m3(&mk, k, D, Sk, H, B)) return ATTN_ERR_CUDA;
-    if (v_rows ? !make_map_e4m3(&mv, v, D, Sk, H, B) : !make_map_e4m3(&mv, v_t, Sk, D, H, B)) return ATTN_ERR_CUDA;
+    if (!make_map_e4m3(&mk, k, D, Sk, H, B, dbox, 128)) return ATTN_ERR_CUDA;
+    if (v_rows ? !make_map_e4m3(&mv, v, D, Sk, H, B, dbox, 128) : !make_map_e4m3(&mv, v_t, Sk, D, H, B, 128, dbox))
+      return ATTN_ERR_CUDA;
   } else {  // never dereferenced: with no keys every unit has zero K tiles
     mk = mq;
     mv = mq;
@@ -1671,6 +1687,8 @@ attn_status attn_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o
   p.v_rows = v_rows ? 1 : 0;
   p.wait_limit_ns = kWaitLimitNs;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (D == 64)
+    return causal ? launch<64, true, true>(*dev, 12, mq, mk, mv, p, s) : launch<64, false, true>(*dev, 13, mq, mk, mv, p, s);
   return causal ? launch<128, true, true>(*dev, 4, mq, mk, mv, p, s) : launch<128, false, true>(*dev, 5, mq, mk, mv, p, s);
 }
 

@@ -219,13 +219,23 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool negate_
 // address >> 4, 16-29 leading-dimension byte offset >> 4, 32-45 stride-dimension
 // byte offset >> 4, 46-48 fixed 0b001, 49-51 base offset (0: atoms 1024-B aligned),
 // 61-63 swizzle mode (2 = 128B).
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+// Layout-type field values (bits 61-63) of the descriptor.
+constexpr uint32_t kSmemSwizzle128B = 2;
+constexpr uint32_t kSmemSwizzle64B = 4;
+
+// The same descriptor for a given swizzle (kSmemSwizzle128B: 8-row atoms of
+// 128 bytes; kSmemSwizzle64B: 8-row atoms of 64 bytes).
+__device__ __forceinline__ uint64_t sdesc_sw(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes, uint32_t mode) {
   uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
   d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
+  d |= static_cast<uint64_t>(mode & 7u) << 61;
   return d;
+}
+
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  return sdesc_sw(saddr, lbo_bytes, sbo_bytes, kSmemSwizzle128B);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]

@@ -267,6 +267,7 @@ FP8_WORKLOADS = {
     "s8192_d128_causal_fp8": Fp8Workload("s8192_d128_causal_fp8", 2, 16, 8192, 8192, 128, True, seed=3),
     "s8192_d128_fp8_vt": Fp8Workload("s8192_d128_fp8_vt", 2, 16, 8192, 8192, 128, False, seed=3,
                                      v_layout="transposed"),
+    "s8192_d64_fp8": Fp8Workload("s8192_d64_fp8", 2, 16, 8192, 8192, 64, False, seed=3),
 }
 
 

@@ -99,7 +99,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
  * q_descale, k_descale, v_descale: the value of a code is descale * E4M3(code)
  *         (OCP E4M3: bias 7, subnormals, no infinities, 0x7F/0xFF NaN).
  * o, lse  as attn_fwd (bf16 O, fp32 natural-log LSE over the scaled scores).
- * D must be 128 (else ATTN_ERR_UNSUPPORTED_D); Sk a multiple of 16 (the
+ * D 64 or 128 (else ATTN_ERR_UNSUPPORTED_D); Sk a multiple of 16 (the
  * V^T rows are Sk bytes long; else ATTN_ERR_SHAPE); scale and the descales
  * finite (else ATTN_ERR_SCALE).  Other arguments and all mask semantics as
  * attn_fwd.  The probabilities are rounded to E4M3 (scaled by 2^4, never

@@ -228,7 +228,8 @@ def test_paged_argument_checks(lib, args, code):
 
 
 @pytest.mark.parametrize("args,code", [
-    (dict(D=64), attn.ATTN_ERR_UNSUPPORTED_D),
+    (dict(D=96), attn.ATTN_ERR_UNSUPPORTED_D),
+    (dict(D=32), attn.ATTN_ERR_UNSUPPORTED_D),
     (dict(Sk=200), attn.ATTN_ERR_SHAPE),
     (dict(B=-1), attn.ATTN_ERR_SHAPE),
     (dict(scale=float("nan")), attn.ATTN_ERR_SCALE),
@@ -305,7 +306,8 @@ def test_fp8_ex_argument_checks(lib):
     args = (A, A, A, A, A, 1, 2, 256, 256)
     assert f(*args, 128, 0.1, 0, None, 1.0, 1.0, 1.0, 2, None) == attn.ATTN_ERR_SHAPE      # unknown layout
     assert f(*args, 128, 0.1, 0, None, 1.0, 1.0, 1.0, -1, None) == attn.ATTN_ERR_SHAPE
-    assert f(*args, 64, 0.1, 0, None, 1.0, 1.0, 1.0, 0, None) == attn.ATTN_ERR_UNSUPPORTED_D
+    assert f(*args, 96, 0.1, 0, None, 1.0, 1.0, 1.0, 0, None) == attn.ATTN_ERR_UNSUPPORTED_D
+    assert f(*args, 32, 0.1, 0, None, 1.0, 1.0, 1.0, 1, None) == attn.ATTN_ERR_UNSUPPORTED_D
     assert f(A, A, A, A, A, 1, 2, 256, 100, 128, 0.1, 0, None, 1.0, 1.0, 1.0, 1, None) == attn.ATTN_ERR_SHAPE
     assert f(*args, 128, float("nan"), 0, None, 1.0, 1.0, 1.0, 0, None) == attn.ATTN_ERR_SCALE
     assert f(A + 8, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, 1.0, 1.0, 1.0, 0, None) == attn.ATTN_ERR_ALIGN

@@ -109,12 +109,13 @@ SHAPES = [
 
 
 @LAYOUTS
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_matches_oracle(shape, causal, layout):
+def test_fp8_matches_oracle(shape, causal, layout, D):
     B, H, Sq, Sk = shape
-    q, k, v = _inputs(B, H, Sq, Sk, seed=Sq + Sk + int(causal))
-    scale = 1.0 / math.sqrt(128)
+    q, k, v = _inputs(B, H, Sq, Sk, seed=Sq + Sk + int(causal) + D, D=D)
+    scale = 1.0 / math.sqrt(D)
     o, lse = _run(q, k, v, scale, causal, layout=layout)
     o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, scale, causal)
     check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax,
@@ -122,34 +123,37 @@ def test_fp8_matches_oracle(shape, causal, layout):
 
 
 @LAYOUTS
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("kv", [[0, 1], [16, 143], [128, 129], [255, 256]])
-def test_fp8_key_lengths(kv, layout):
-    q, k, v = _inputs(2, 2, 200, 256, seed=sum(kv))
+def test_fp8_key_lengths(kv, layout, D):
+    q, k, v = _inputs(2, 2, 200, 256, seed=sum(kv) + D, D=D)
     o, lse = _run(q, k, v, 0.09, kv=kv, layout=layout)
     o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, 0.09, kv=kv)
     check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax, f"fp8 kv={kv} layout={layout}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("shape", [(1, 1, 1, 1), (1, 2, 100, 100), (2, 1, 300, 333), (1, 2, 129, 1000)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_v_rows_any_key_count(shape, causal):
+def test_fp8_v_rows_any_key_count(shape, causal, D):
     """V in rows has no key-count restriction (the transposed layout needs a
     multiple of 16): ragged key counts against the oracle."""
     B, H, Sq, Sk = shape
-    q, k, v = _inputs(B, H, Sq, Sk, seed=Sq * 3 + Sk + int(causal))
-    scale = 1.0 / math.sqrt(128)
+    q, k, v = _inputs(B, H, Sq, Sk, seed=Sq * 3 + Sk + int(causal) + D, D=D)
+    scale = 1.0 / math.sqrt(D)
     o, lse = _run(q, k, v, scale, causal, layout=ROWS)
     o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, scale, causal)
     check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax, f"fp8 rows {shape}")
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("shape", [(1, 2, 100, 144), (2, 2, 300, 1024), (1, 4, 1000, 2048)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_v_layouts_bitwise_identical(shape, causal):
+def test_fp8_v_layouts_bitwise_identical(shape, causal, D):
     """The two V layouts feed the products the same values in the same order:
     identical bits."""
     B, H, Sq, Sk = shape
-    q, k, v = _inputs(B, H, Sq, Sk, seed=Sq + 7 * Sk + int(causal), std=2.0)
+    q, k, v = _inputs(B, H, Sq, Sk, seed=Sq + 7 * Sk + int(causal), std=2.0, D=D)
     o_r, l_r = _run(q, k, v, 0.07, causal, layout=ROWS)
     o_t, l_t = _run(q, k, v, 0.07, causal, layout=TRANSPOSED)
     assert torch.equal(o_r.view(torch.int16), o_t.view(torch.int16))
