@@ -958,11 +958,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tcount = 0, ocount = 0, kq = 0;
     bool ok = true;
 
+    // The next unit is taken from the queue before a unit's epilogue, under
+    // the wait for the unit's last P V (pend != -3).
+    int pend = -3;
     while (ok) {
-      const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
-      // both warps of the pair read the same entry; they leave together if
-      // either gave up or the CTA aborts
-      if (named_bar_red_or(bar_pair, kPairThreads, unit == -2 || *abort_flag != 0)) { ok = false; break; }
+      int unit = pend;
+      if (pend != -3) {
+        pend = -3;
+      } else {
+        unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
+        // both warps of the pair read the same entry; they leave together if
+        // either gave up or the CTA aborts
+        if (named_bar_red_or(bar_pair, kPairThreads, unit == -2 || *abort_flag != 0)) { ok = false; break; }
+      }
       if (unit < 0) break;
       const Unit u = decode_unit<CAUSAL>(p, unit);
       const int row = u.q0 + r;     // position of this thread's query row within its sequence
@@ -1120,6 +1128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
+
+      // the next unit (see above); the pair leaves together on a failure
+      pend = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
+      if (named_bar_red_or(bar_pair, kPairThreads, pend == -2 || *abort_flag != 0)) { ok = false; break; }
 
       // ------------------------------------------------------------ epilogue
       if (!failed &&
