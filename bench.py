@@ -46,9 +46,9 @@ FALLBACK_PEAK_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 # every source file of the translation unit that holds the forward kernel
 # (attn_fwd.cu includes the PTX wrappers and the backward kernels)
-KERNEL_SOURCES = ["exact_attention_86_gb300/csrc/attn_fwd.cu", "exact_attention_86_gb300/csrc/sm103_ptx.cuh",
+KERNEL_SOURCES = ["exact_attention_86_gb300/csrc/attn_fwd.cu", "exact_attention_86_gb300/csrc/attn_fwd_pair.cu",
+                  "exact_attention_86_gb300/csrc/attn_common.cuh", "exact_attention_86_gb300/csrc/sm103_ptx.cuh",
                   "exact_attention_86_gb300/csrc/attn_bwd.cuh", "include/attn.h"]
-TRAFFIC_FILE = "profiles/attn_fwd_kernel_s8192_d128_traffic.md"
 L2_BYTES = 129 * 10**6
 
 
@@ -60,10 +60,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source and this workload; else None."""
-    path = os.path.join(ROOT, TRAFFIC_FILE)
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary
+    ``profiles/<kernel>_<workload>_traffic.md``, if it was taken on the current
+    kernel source and this workload; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}_traffic.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -272,6 +273,15 @@ def is_paged(w) -> bool:
 def is_fp8(w) -> bool:
     from exact_attention_86_gb300 import workloads
     return isinstance(w, workloads.Fp8Workload)
+
+
+def forward_kernel(w, splits: int) -> str:
+    """The kernel that does the forward's work for this workload: padded bf16
+    batches without causal masking or key ranges run the two-query-tile kernel,
+    every other mode the one-tile kernel."""
+    if not is_varlen(w) and not is_fp8(w) and not w.causal and splits == 0:
+        return "attn_fwd_pair_kernel"
+    return "attn_fwd_kernel"
 
 
 def generate(w, draw: int):
@@ -708,8 +718,9 @@ def main():
         hbm_src = "fallback (6.8 TB/s copy)"
     roofline = roofline_bound(step_flops, w.min_bytes, launch_ms, peak, hbm, args.backward)
     roofline["peak_source"] = peak_src if roofline["bound"] == "tensor" else hbm_src
-    roofline.update({"traffic": None if args.backward else recorded_traffic(w.name),
-                     "kernel": "attn_bwd (delta, dq, dkdv kernels)" if args.backward else "attn_fwd_kernel",
+    kernel = "attn_bwd (delta, dq, dkdv kernels)" if args.backward else forward_kernel(w, args.splits)
+    roofline.update({"traffic": None if args.backward else recorded_traffic(kernel, w.name),
+                     "kernel": kernel,
                      "launch_ms": launch_ms, "algorithmic_flops_per_launch": step_flops,
                      "algorithmic_bytes_per_launch": w.min_bytes})
 

@@ -1,0 +1,665 @@
+// The padded-batch bf16 forward with two query tiles per work unit.
+//
+// Same operation as attn_fwd_kernel (softmax(scale * Q K^T + mask) V and the
+// row LSE; "Kernel Fusion and the Memory Wall", section "FlashAttention: avoid
+// the full score matrix", and the tile loop of "Attention softmax fusion"), for
+// padded [B, H, S, D] batches without key ranges.  A translation unit of its
+// own (with the shared parameters, waits and unit order of attn_common.cuh),
+// so that its code leaves the register allocation of attn_fwd.cu's kernels
+// untouched: compiled into one file with them, it cost two of those kernels a
+// register spill.
+//
+// A work unit is 256 query rows of one (b, h): tiles A (rows q0 .. q0 + 127)
+// and B (q0 + 128 .. q0 + 255), which share every K/V tile the producer loads.
+// Each tile has one softmax warpgroup with ONE thread per row (warps 0-3: A,
+// warps 4-7: B), so a row's max and sum never leave its thread: no barrier,
+// no exchange.  The two tiles' work interleaves on the tensor pipe: while
+// the softmax of A works on S_A, the pipe computes S_B = Q_B K^T and the
+// previous P_B V, and the other way round.
+//
+//   warps 0-3  softmax of tile A (thread = row)
+//   warps 4-7  softmax of tile B
+//   warp 8     TMA producer of the unit queue, the Q pair and the K/V ring (one lane)
+//   warp 9     TMEM owner; issues S_x = Q_x K^T for x = A, B
+//   warp 10    issues O_x += P_x V for x = A, B
+//   warp 11    idle
+//
+// Tensor Memory (512 columns): S_A [0,128), S_B [128,256), O_A [256, 256+D),
+// O_B [256+D, 256+2D).  P_x (bf16 pairs, 64 columns) is written over the first
+// 64 columns of S_x once the softmax has read S_x; S_x is written again only
+// after the P V of its previous tile has consumed P_x (the QK^T issuer waits
+// for that product's commit).  So when the softmax of x sees a new S_x, the
+// P V of the previous tile has completed and O_x is stable: a rescale of O_x
+// never waits.
+//
+// Every wait is bounded, as in attn_fwd_kernel; a wait that gives up records
+// its site and raises the block's abort flag, and every role drains what it
+// has in flight, frees TMEM and returns.  The softmax threads never use a
+// named barrier, so no role can be left waiting for another that has left.
+
+#include <atomic>
+
+#include "attn_common.cuh"
+#include "attn_pair_host.h"
+
+using namespace attn_sm103;
+
+namespace {
+
+template <int D>
+struct GeoPair {
+  static_assert(D == 64 || D == 128, "head dim");
+  static constexpr int kTileBytes = 128 * D * 2;      // one Q, K or V tile (128 rows of bf16)
+  static constexpr int kChunkBytes = 128 * 128;       // 128 rows x 128 B (one 128-B swizzle column)
+  static constexpr int kChunks = D / 64;
+  static constexpr int kKSteps = D / 16;              // QK^T instructions (16 columns of D each)
+  static constexpr int kOffQ = 1024;                  // after the control block
+  static constexpr int kOffRing = kOffQ + 2 * kTileBytes;
+  // as many K/V slots as the 227 KB a block may use leave (D = 128: 5, D = 64: 12)
+  static constexpr int kSlots = (232448 - kOffRing) / kTileBytes;
+  static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes;
+  static_assert(kSlots >= 2 && kSlots <= 16, "ring depth");
+  static_assert(2 * kSmemBytes > 233472, "one block per SM (the TMEM allocation is the whole of it)");
+  static constexpr uint32_t kTmemS = 0;               // + 128 * x
+  static constexpr uint32_t kTmemO = 256;             // + D * x
+  // One ring of alternating K and V tiles, as attn_fwd_kernel's padded layout
+  // (position p = 2 t (+1 for V) in slot p % kSlots; one full barrier per
+  // slot and kind; an odd depth alternates kinds within a slot).
+  struct Fill {
+    uint32_t slot, full_use, empty_use;
+  };
+  static __device__ __forceinline__ Fill fill_of(uint32_t t, bool is_v) {
+    const uint32_t pos = 2 * t + (is_v ? 1u : 0u);
+    return {pos % kSlots, (kSlots & 1) ? (pos / kSlots) >> 1 : pos / kSlots, pos / kSlots};
+  }
+};
+
+struct CtrlPair {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[16], v_full[16], kv_empty[16];
+  uint64_t s_full[2], p_full[2], p_free[2], o_full[2];  // per query tile
+  uint64_t qk_issued_a;  // one phase per S_A = Q_A K^T issued (orders the tensor pipe's queue)
+  uint64_t uq_full[kUnitQ], uq_empty[kUnitQ];
+  int unit_q[kUnitQ];
+  uint64_t drain[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(CtrlPair) <= 1024, "control block");
+
+struct UnitPair {
+  int b, h;
+  int q0;       // first row of tile A
+  int rows[2];  // rows of tiles A and B that exist (0 .. 128)
+  int kv;       // valid keys of the batch entry
+  int n[2];     // K tiles tile A / B processes
+  int n_max;
+};
+
+// Unit t: (b, h, pair of query tiles), ordered as attn_fwd_kernel's units
+// (Params::n_qtiles counts tile pairs per head here).
+template <bool CAUSAL>
+__device__ __forceinline__ UnitPair decode_pair(const Params& p, int t) {
+  UnitPair u;
+  int pr, bh;
+  if (CAUSAL) {  // head groups, longest units first within a group (see decode_unit)
+    const int grp = p.fd_group_units.div(t);
+    const int w = t - grp * p.head_group * p.n_qtiles;
+    const FastDiv& fh = grp == p.last_group ? p.fd_last_heads : p.fd_group_heads;
+    const int wq = fh.div(w);
+    pr = p.n_qtiles - 1 - wq;
+    bh = grp * p.head_group + (w - wq * static_cast<int>(fh.d));
+  } else {
+    bh = p.fd_qtiles.div(t);
+    pr = t - bh * p.n_qtiles;
+  }
+  u.b = p.fd_H.div(bh);
+  u.h = bh - u.b * p.H;
+  u.q0 = pr * (2 * kBQ);
+  int kv = p.Sk;
+  if (p.kv_lens != nullptr) kv = min(max(__ldg(p.kv_lens + u.b), 0), p.Sk);
+  u.kv = kv;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const int q0x = u.q0 + kBQ * x;
+    u.rows[x] = max(min(kBQ, p.Sq - q0x), 0);
+    int lim = kv;
+    if (CAUSAL) lim = min(lim, q0x + u.rows[x]);  // last row of the tile + 1
+    u.n[x] = u.rows[x] > 0 ? (lim + kBK - 1) / kBK : 0;
+  }
+  u.n_max = max(u.n[0], u.n[1]);
+  return u;
+}
+
+// p = 2^(s*c - mb) for a thread's 128 scores, packed to bf16 pairs IN PLACE
+// (pair e goes to sp[e], whose score was read at pair e / 2 <= e); masked
+// columns (>= climit) give 0.  Returns the fp32 sum of the unrounded terms.
+template <bool MASKED>
+__device__ __forceinline__ float row_exp128(uint32_t (&sp)[128], float c, float mb, int climit) {
+  const uint64_t c2 = f2_pack(c, c);
+  const uint64_t nmb2 = f2_pack(-mb, -mb);
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int e = 0; e < 64; ++e) {
+    const int col = 2 * e;
+    float x0, x1;
+    f2_unpack(f2_fma(f2_pack(u2f(sp[col]), u2f(sp[col + 1])), c2, nmb2), x0, x1);
+    float p0 = ex2_approx(x0);
+    float p1 = ex2_approx(x1);
+    if (MASKED) {
+      p0 = (col < climit) ? p0 : 0.0f;
+      p1 = (col + 1 < climit) ? p1 : 0.0f;
+    }
+    acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
+    sp[e] = pack_bf16x2(p0, p1);
+  }
+  const uint64_t a01 = f2_add(acc[0], acc[1]);
+  const uint64_t a23 = f2_add(acc[2], acc[3]);
+  float lo, hi;
+  f2_unpack(f2_add(a01, a23), lo, hi);
+  return lo + hi;
+}
+
+// Maximum of a thread's 128 raw scores (columns >= climit excluded when MASKED).
+template <bool MASKED>
+__device__ __forceinline__ float row_max128(const uint32_t (&sp)[128], int climit) {
+  float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int col = 0; col < 128; col += 2) {
+    float x0 = u2f(sp[col]);
+    float x1 = u2f(sp[col + 1]);
+    if (MASKED) {
+      x0 = (col < climit) ? x0 : -INFINITY;
+      x1 = (col + 1 < climit) ? x1 : -INFINITY;
+    }
+    m4[(col >> 1) & 3] = max3(m4[(col >> 1) & 3], x0, x1);
+  }
+  return fmaxf(max3(m4[0], m4[1], m4[2]), m4[3]);
+}
+
+// A thread's 128 scores of S at TMEM address tS (4 loads of 32 columns).
+__device__ __forceinline__ void load_s128(uint32_t tS, uint32_t (&sp)[128]) {
+  uint32_t(&a)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sp[0]);
+  uint32_t(&b)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sp[32]);
+  uint32_t(&c)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sp[64]);
+  uint32_t(&d)[32] = *reinterpret_cast<uint32_t(*)[32]>(&sp[96]);
+  tmem_ld_32x32b_x32(tS, a);
+  tmem_ld_32x32b_x32(tS + 32, b);
+  tmem_ld_32x32b_x32(tS + 64, c);
+  tmem_ld_32x32b_x32(tS + 96, d);
+  tmem_ld_wait_x32(a);
+  tmem_ld_wait_x32(b);
+  tmem_ld_wait_x32(c);
+  tmem_ld_wait_x32(d);
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+                         const __grid_constant__ CUtensorMap map_v, const Params p) {
+  using G = GeoPair<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t base = smem_addr(smem_raw);
+  CtrlPair& ctl = *reinterpret_cast<CtrlPair*>(smem_raw);
+  volatile int* abort_flag = &ctl.abort_flag;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // the swizzle atoms need 1024-byte aligned tiles and the layout has no slack
+  if ((base & 1023u) != 0u) {
+    if (threadIdx.x == 0) record_give_up(kSiteAlign);
+    return;
+  }
+  const uint32_t bar_q_full = smem_addr(&ctl.q_full);
+  const uint32_t bar_q_empty = smem_addr(&ctl.q_empty);
+  const uint32_t bar_k_full0 = smem_addr(&ctl.k_full[0]);
+  const uint32_t bar_v_full0 = smem_addr(&ctl.v_full[0]);
+  const uint32_t bar_kv_empty0 = smem_addr(&ctl.kv_empty[0]);
+  const uint32_t bar_s_full0 = smem_addr(&ctl.s_full[0]);   // + 8 * x
+  const uint32_t bar_p_full0 = smem_addr(&ctl.p_full[0]);
+  const uint32_t bar_p_free0 = smem_addr(&ctl.p_free[0]);
+  const uint32_t bar_o_full0 = smem_addr(&ctl.o_full[0]);
+  const uint32_t bar_uq_full0 = smem_addr(&ctl.uq_full[0]);
+  const uint32_t bar_uq_empty0 = smem_addr(&ctl.uq_empty[0]);
+  volatile int* unit_q = ctl.unit_q;
+
+  if (warp == 0) {
+    if (lane < G::kSlots) {
+      mbar_init(bar_k_full0 + 8 * lane, 1);
+      mbar_init(bar_v_full0 + 8 * lane, 1);
+      mbar_init(bar_kv_empty0 + 8 * lane, 1);
+    } else if (lane >= 16 && lane < 18) {
+      const int x = lane - 16;
+      mbar_init(bar_s_full0 + 8 * x, 1);
+      mbar_init(bar_p_full0 + 8 * x, 4);  // the 4 softmax warps of tile x
+      mbar_init(bar_p_free0 + 8 * x, 1);
+      mbar_init(bar_o_full0 + 8 * x, 1);
+    } else if (lane >= 20 && lane < 20 + kUnitQ) {
+      const int k = lane - 20;
+      mbar_init(bar_uq_full0 + 8 * k, 1);
+      mbar_init(bar_uq_empty0 + 8 * k, kUnitQReaders);
+    } else if (lane == 30) {
+      mbar_init(smem_addr(&ctl.drain[0]), 1);
+      mbar_init(smem_addr(&ctl.drain[1]), 1);
+      mbar_init(smem_addr(&ctl.qk_issued_a), 1);
+    } else if (lane == 31) {
+      mbar_init(bar_q_full, 1);
+      mbar_init(bar_q_empty, 1);
+      ctl.abort_flag = 0;
+    }
+    fence_barrier_init();
+  }
+  if (warp == kWarpQK) {
+    tmem_alloc(smem_addr(&ctl.tmem_base), 512);
+    tmem_relinquish_alloc_permit();
+  }
+  if (warp == kWarpLoad && lane == 0) {
+    prefetch_tensor_map(&map_q);
+    prefetch_tensor_map(&map_k);
+    prefetch_tensor_map(&map_v);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = ctl.tmem_base;
+  const uint64_t limit = p.wait_limit_ns;
+  const int t_end = (p.total_units + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x) *
+                    static_cast<int>(gridDim.x);
+
+  if (warp >= kSoftmaxWarps) {
+    regs_decrease<kRegsOther>();
+    if (warp == kWarpLoad) {
+      // ------------------------------------------ TMA: units, Q pairs, K/V
+      if (lane == 0) {
+        const uint64_t pol_keep = l2_policy_evict_last();   // K/V: re-read by the head's other units
+        const uint64_t pol_once = l2_policy_evict_first();  // Q: read once
+        uint32_t pos = 0, qcount = 0, kq = 0;               // pos: ring positions filled (K_t at 2t, V_t at 2t+1)
+        int t_static = blockIdx.x;
+        bool ok = true;
+        while (ok) {
+          int unit = -1;
+          UnitPair u;
+          while (t_static < t_end) {
+            const int cand = unit_at<CAUSAL>(p, t_static);
+            t_static += gridDim.x;
+            if (cand >= p.total_units) continue;
+            u = decode_pair<CAUSAL>(p, cand);
+            if (u.rows[0] > 0) {
+              unit = cand;
+              break;
+            }
+          }
+          {
+            const uint32_t slot = kq % kUnitQ;
+            if (!wait_phase(bar_uq_empty0 + 8 * slot, ((kq / kUnitQ) & 1u) ^ 1u, abort_flag, kSiteUnitQ, limit)) {
+              ok = false;
+              break;
+            }
+            unit_q[slot] = unit;
+            mbar_arrive(bar_uq_full0 + 8 * slot);
+            ++kq;
+          }
+          if (unit < 0) break;
+          if (u.n_max == 0) continue;
+          if (!wait_phase(bar_q_empty, (qcount & 1u) ^ 1u, abort_flag, kSiteQEmpty, limit)) { ok = false; break; }
+          // both Q tiles (rows past Sq read as zeros and count as loaded)
+          mbar_arrive_expect_tx(bar_q_full, 2 * G::kTileBytes);
+          for (int x = 0; x < 2; ++x)
+            for (int c = 0; c < G::kChunks; ++c)
+              tma_load_4d_hint(base + G::kOffQ + x * G::kTileBytes + c * G::kChunkBytes, &map_q, bar_q_full, c * 64,
+                               u.q0 + kBQ * x, u.h, u.b, pol_once);
+          ++qcount;
+          for (int j = 0; ok && j < u.n_max; ++j) {
+            for (int sel = 0; sel < 2; ++sel) {  // K_j, then V_j
+              const typename G::Fill f = G::fill_of(pos >> 1, sel != 0);
+              if (!wait_phase(bar_kv_empty0 + 8 * f.slot, (f.empty_use & 1u) ^ 1u, abort_flag, kSiteKvEmpty,
+                              limit)) {
+                ok = false;
+                break;
+              }
+              // (self test only: block 0 leaves out one K fill; the position
+              // still counts, so its consumer waits for it in vain)
+              if (!(sel == 0 && blockIdx.x == 0 && static_cast<int>(pos >> 1) == p.selftest_skip_fill)) {
+                const uint32_t full = (sel ? bar_v_full0 : bar_k_full0) + 8 * f.slot;
+                mbar_arrive_expect_tx(full, G::kTileBytes);
+                const CUtensorMap* m = sel ? &map_v : &map_k;
+                const uint32_t dst = base + G::kOffRing + f.slot * G::kTileBytes;
+                for (int c = 0; c < G::kChunks; ++c)
+                  tma_load_4d_hint(dst + c * G::kChunkBytes, m, full, c * 64, j * kBK, u.h, u.b, pol_keep);
+              }
+              ++pos;
+            }
+          }
+        }
+        // Drains: after a failure every issued copy must land; in any case the
+        // issuers' last commit arrivals on the empty barriers must have landed
+        // before the block's shared memory is gone.
+        if (!ok && qcount > 0) wait_phase_drain(bar_q_full, (qcount - 1) & 1u);
+        if (qcount > 0) wait_phase_drain(bar_q_empty, (qcount - 1) & 1u);
+        const uint32_t ring = pos;  // positions 0 .. pos - 1 were filled, in order
+        for (uint32_t s = 0; s < static_cast<uint32_t>(G::kSlots) && s < ring; ++s) {
+          const uint32_t last = ring - 1 - ((ring - 1 - s) % G::kSlots);
+          const typename G::Fill f = G::fill_of(last >> 1, (last & 1u) != 0);
+          if (!ok) wait_phase_drain(((last & 1u) ? bar_v_full0 : bar_k_full0) + 8 * s, f.full_use & 1u);
+          wait_phase_drain(bar_kv_empty0 + 8 * s, f.empty_use & 1u);
+        }
+      }
+      __syncwarp();
+    } else if (warp == kWarpQK) {
+      // ---------------------------------------------- S_x = Q_x K^T issuer
+      uint32_t qcount = 0, tiles = 0, kq = 0;
+      uint32_t sc[2] = {0u, 0u};  // S_x products issued
+      bool ok = true;
+      while (ok) {
+        const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
+        if (unit == -2) { ok = false; break; }
+        if (unit < 0) break;
+        const UnitPair u = decode_pair<CAUSAL>(p, unit);
+        if (u.n_max == 0) continue;
+        if (!wait_warp(bar_q_full, qcount & 1u, abort_flag, kSiteQFull, limit)) { ok = false; break; }
+        ++qcount;
+        for (int j = 0; ok && j < u.n_max; ++j, ++tiles) {
+          const typename G::Fill f = G::fill_of(tiles, false);
+          if (!wait_warp(bar_k_full0 + 8 * f.slot, f.full_use & 1u, abort_flag, kSiteKvFull, limit)) {
+            ok = false;
+            break;
+          }
+          const uint32_t ka = base + G::kOffRing + f.slot * G::kTileBytes;
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (j >= u.n[x]) continue;
+            // S_x (and the P_x over it) is free once the P V of its previous
+            // tile has completed
+            if (sc[x] > 0 &&
+                !wait_warp(bar_p_free0 + 8 * x, (sc[x] - 1) & 1u, abort_flag, kSitePFree, limit)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t qa = base + G::kOffQ + x * G::kTileBytes;
+#pragma unroll
+            for (int kk = 0; kk < G::kKSteps; ++kk) {
+              const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
+              mma_ss_elect(tmem + G::kTmemS + 128u * x, sdesc_sw128(qa + off, 16, 1024),
+                           sdesc_sw128(ka + off, 16, 1024), p.idesc_qk, kk > 0 ? 1u : 0u);
+            }
+            mma_commit_elect(bar_s_full0 + 8 * x);
+            if (x == 0) {  // a plain arrive right after the issue
+              __syncwarp();
+              if (lane == 0) mbar_arrive(smem_addr(&ctl.qk_issued_a));
+            }
+            ++sc[x];
+          }
+          if (!ok) break;
+          mma_commit_elect(bar_kv_empty0 + 8 * f.slot);
+        }
+        if (!ok) break;
+        mma_commit_elect(bar_q_empty);
+      }
+      if (!ok) {
+        const uint32_t bar_d = smem_addr(&ctl.drain[0]);
+        mma_commit_elect(bar_d);
+        wait_phase_drain(bar_d, 0);
+      }
+    } else if (warp == kWarpPV) {
+      // ---------------------------------------------- O_x += P_x V issuer
+      uint32_t tiles = 0, kq = 0;
+      uint32_t pc[2] = {0u, 0u};  // P_x V products issued
+      bool ok = true;
+      while (ok) {
+        const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
+        if (unit == -2) { ok = false; break; }
+        if (unit < 0) break;
+        const UnitPair u = decode_pair<CAUSAL>(p, unit);
+        if (u.n_max == 0) continue;
+        for (int j = 0; ok && j < u.n_max; ++j, ++tiles) {
+          const typename G::Fill f = G::fill_of(tiles, true);
+          bool v_ready = false;
+          const uint32_t va = base + G::kOffRing + f.slot * G::kTileBytes;
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (j >= u.n[x]) continue;
+            if (!wait_warp(bar_p_full0 + 8 * x, pc[x] & 1u, abort_flag, kSitePFull, limit)) {
+              ok = false;
+              break;
+            }
+            // P_B V_j goes into the tensor pipe's (in-order) queue after
+            // S_A = Q_A K_{j+1}^T, which waits for P_A V_j to complete: queued
+            // the other way round, every tile of A would wait for both P V
+            // products before its next S.  (pc[0] = index of that S_A product.)
+            if (x == 1 && j + 1 < u.n[0] &&
+                !wait_warp(smem_addr(&ctl.qk_issued_a), pc[0] & 1u, abort_flag, kSitePvIssued, limit)) {
+              ok = false;
+              break;
+            }
+            if (!v_ready) {
+              if (!wait_warp(bar_v_full0 + 8 * f.slot, f.full_use & 1u, abort_flag, kSiteKvFull, limit)) {
+                ok = false;
+                break;
+              }
+              v_ready = true;
+            }
+            tc_fence_after_sync();
+            // O_x += P_x V_j: P from TMEM (16 keys = 8 columns per MMA), V
+            // MN-major in shared memory (LBO = distance between 64-column
+            // chunks of D, SBO = 8 keys x 128 B)
+            const uint32_t tO = tmem + G::kTmemO + static_cast<uint32_t>(D) * x;
+            const uint32_t tP = tmem + G::kTmemS + 128u * x;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_ts_elect(tO, tP + 8u * kk, sdesc_sw128(va + kk * 16 * 128, G::kChunkBytes, 1024), p.idesc_pv,
+                           (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_elect(bar_p_free0 + 8 * x);
+            ++pc[x];
+            if (j == u.n[x] - 1) mma_commit_elect(bar_o_full0 + 8 * x);
+          }
+          if (!ok) break;
+          mma_commit_elect(bar_kv_empty0 + 8 * f.slot);
+        }
+      }
+      if (!ok) {
+        const uint32_t bar_d = smem_addr(&ctl.drain[1]);
+        mma_commit_elect(bar_d);
+        wait_phase_drain(bar_d, 0);
+      }
+    }
+  } else {
+    regs_increase<kRegsSoftmax>();
+    // ---------------------------------------------------------- softmax
+    // Thread = one row of tile x; its reference max and sum stay in the
+    // thread.  A tile is first exponentiated against the current reference;
+    // a row sum above 2^16 (or not a number) shows that some score grew past
+    // the reference by more than 16 (log2 units): only then is the exact max
+    // taken (the scores reloaded), and if it grew by more than 16 the
+    // reference moves and O and the sum are rescaled by 2^(m_old - m_new)
+    // (lazy correction, as attn_fwd_kernel's).
+    const int x = warp >> 2;
+    const int r = threadIdx.x & (kBQ - 1);
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float c = p.c;
+    const uint32_t tS = tmem + lane_off + G::kTmemS + 128u * x;
+    const uint32_t tO = tmem + lane_off + G::kTmemO + static_cast<uint32_t>(D) * x;
+    const uint32_t bar_s_full = bar_s_full0 + 8 * x;
+    const uint32_t bar_p_full = bar_p_full0 + 8 * x;
+    const uint32_t bar_o_full = bar_o_full0 + 8 * x;
+    uint32_t sc = 0, oc = 0, kq = 0;
+    bool ok = true;
+    while (ok) {
+      const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
+      if (unit == -2) { ok = false; break; }
+      if (unit < 0) break;
+      const UnitPair u = decode_pair<CAUSAL>(p, unit);
+      const int rows = x ? u.rows[1] : u.rows[0];  // (constant indices keep the unit in registers)
+      const int nx = x ? u.n[1] : u.n[0];
+      if (rows == 0) continue;  // tile B past the end of the sequence
+      const int q0x = u.q0 + kBQ * x;
+      const int row = q0x + r;
+      const bool row_ok = r < rows;
+      const size_t row_index = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq) + row;
+      uint16_t* o_dst = p.o + row_index * D;
+      if (nx == 0) {  // no valid key for any row of this tile: O = 0, LSE = -inf
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(o_dst);
+#pragma unroll
+          for (int q = 0; q < D / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+          p.lse[row_index] = -INFINITY;
+        }
+        continue;
+      }
+      float m_used = -INFINITY;  // reference max (log2 units, scale folded in)
+      float l = 0.0f;            // sum of 2^(x - m_used) over the row
+      bool failed = false;
+      for (int j = 0; j < nx; ++j, ++sc) {
+        const int k0 = j * kBK;
+        const bool masked = (k0 + kBK > u.kv) || (CAUSAL && k0 + kBK - 1 > q0x);
+        int climit = u.kv - k0;  // columns >= climit are masked for this row
+        if (CAUSAL) climit = min(climit, row - k0 + 1);
+        // (a failed wait is warp-uniform and means the block is aborting)
+        if (!wait_warp(bar_s_full, sc & 1u, abort_flag, kSiteSFull, limit)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after_sync();
+        uint32_t sp[128];
+        load_s128(tS, sp);
+        float sum = 0.0f;
+        bool suspect = true;  // the first tile always takes its exact max
+        if (j > 0) {
+          sum = masked ? row_exp128<true>(sp, c, m_used, climit) : row_exp128<false>(sp, c, m_used, climit);
+          suspect = !(sum <= 65536.0f);
+        }
+        // (warp-uniform decisions: the TMEM loads and stores below are
+        // warp-wide instructions)
+        if (__any_sync(0xffffffffu, suspect)) {
+          if (j > 0) load_s128(tS, sp);  // the raw scores again (P is not stored yet)
+          const float mx = masked ? row_max128<true>(sp, climit) : row_max128<false>(sp, climit);
+          const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
+          bool grow = (j == 0) || m_tile > m_used + 16.0f;
+          float alpha = 1.0f;
+          if (grow && j > 0) alpha = ex2_approx(m_used - m_tile);
+          if (grow) m_used = m_tile;
+          const float mb = (m_used == -INFINITY) ? 0.0f : m_used;
+          sum = masked ? row_exp128<true>(sp, c, mb, climit) : row_exp128<false>(sp, c, mb, climit);
+          if (j > 0 && __any_sync(0xffffffffu, grow)) {
+            // O_x holds the products of the tiles before (all completed: this
+            // S_x was written after the last of them): rescale this row
+            l *= alpha;
+            const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+              uint32_t o[32];
+              tmem_ld_32x32b_x32(tO + q * 32, o);
+              tmem_ld_wait_x32(o);
+#pragma unroll
+              for (int e = 0; e < 16; ++e) {
+                float lo, hi;
+                f2_unpack(f2_mul(f2_pack(u2f(o[2 * e]), u2f(o[2 * e + 1])), a2), lo, hi);
+                o[2 * e] = __float_as_uint(lo);
+                o[2 * e + 1] = __float_as_uint(hi);
+              }
+              tmem_st_32x32b_x32(tO + q * 32, o);
+            }
+          }
+        }
+        // P over the first 64 columns of S_x (their scores are in registers)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          tmem_st_32x32b_x16(tS + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(&sp[16 * q]));
+        tmem_st_wait();
+        warp_arrive_after_tc(bar_p_full, lane);
+        l += sum;
+      }
+      if (failed) { ok = false; break; }
+      // ------------------------------------------------------------ epilogue
+      if (!wait_warp(bar_o_full, oc & 1u, abort_flag, kSiteOFull, limit)) { ok = false; break; }
+      ++oc;
+      tc_fence_after_sync();
+      const bool has_key = l > 0.0f;
+      const float inv_l = has_key ? rcp_approx(l) : 0.0f;
+      const float lse_row = has_key ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
+#pragma unroll
+      for (int q = 0; q < D / 32; ++q) {
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tO + q * 32, o);
+        tmem_ld_wait_x32(o);
+        if (row_ok) {
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = has_key ? pack_bf16x2(u2f(o[2 * e]) * inv_l, u2f(o[2 * e + 1]) * inv_l) : 0u;
+          if (p.o_align32) {
+            st_global_v8(o_dst + q * 32, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
+            st_global_v8(o_dst + q * 32 + 16, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(o_dst + q * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
+        }
+      }
+      // the next unit's first P V overwrites O_x only after this warpgroup's
+      // p_full for it, which comes after these loads
+      tc_fence_before_sync();
+      if (row_ok) p.lse[row_index] = lse_row;
+    }
+    // The commit of the last P_x V lands asynchronously and nothing else
+    // waits for it: wait before exiting.
+    if (sc > 0) wait_phase_drain(bar_p_free0 + 8 * x, (sc - 1) & 1u);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kWarpQK) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// dynamic shared memory attribute set, per device and instantiation
+constexpr int kMaxDevicesPair = 64;
+std::atomic<bool> g_pair_smem_set[kMaxDevicesPair][4];
+
+template <int D, bool CAUSAL>
+attn_status launch_pair(int dev, int idx, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk,
+                        const CUtensorMap& mv, const Params& p0, cudaStream_t stream) {
+  auto kern = attn_fwd_pair_kernel<D, CAUSAL>;
+  constexpr int smem = GeoPair<D>::kSmemBytes;
+  if (dev < 0 || dev >= kMaxDevicesPair) return ATTN_ERR_UNSUPPORTED_DEVICE;
+  if (!g_pair_smem_set[dev][idx].load(std::memory_order_acquire)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    g_pair_smem_set[dev][idx].store(true, std::memory_order_release);
+  }
+  const int grid = p0.total_units < num_sms ? p0.total_units : num_sms;
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, with_divisors(p0, grid));
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+namespace attn_pair_host {
+
+attn_status launch(int D, bool causal, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk,
+                   const CUtensorMap& mv, const attn_detail::Params& p, cudaStream_t s) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+#if ATTN_PAIR_CAUSAL
+  if (causal)
+    return D == 64 ? launch_pair<64, true>(dev, 0, num_sms, mq, mk, mv, p, s)
+                   : launch_pair<128, true>(dev, 2, num_sms, mq, mk, mv, p, s);
+#else
+  if (causal) return ATTN_ERR_SHAPE;  // not reached: causal batches take attn_fwd_kernel then
+#endif
+  return D == 64 ? launch_pair<64, false>(dev, 1, num_sms, mq, mk, mv, p, s)
+                 : launch_pair<128, false>(dev, 3, num_sms, mq, mk, mv, p, s);
+}
+
+attn_status status_read_clear(uint32_t host[3]) {
+  host[0] = host[1] = host[2] = 0;
+  if (cudaMemcpyFromSymbol(host, g_attn_status, 3 * sizeof(uint32_t)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (host[0] == 0) return ATTN_OK;
+  const uint32_t zero[3] = {0, 0, 0};
+  if (cudaMemcpyToSymbol(g_attn_status, zero, sizeof(zero)) != cudaSuccess) return ATTN_ERR_CUDA;
+  return ATTN_OK;
+}
+
+}  // namespace attn_pair_host

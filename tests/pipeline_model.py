@@ -298,3 +298,204 @@ def run(units, slots, per_kind, seed, rescale_p=0.3, mistake=None, p_in_s=False,
         fn()
 
 
+
+
+def run_pair(units, slots, seed, mistake=None):
+    """The barrier protocol of the padded forward with two query tiles per
+    unit (attn_fwd_pair_kernel).  ``units`` is a list of (n_A, n_B): the K
+    tiles each query tile processes (a unit loads max(n_A, n_B) K/V tiles;
+    tile x takes part in K tile j iff j < n_x).  One ring of alternating K
+    and V positions with one full barrier per (slot, kind); S_x written by
+    the QK^T issuer after the P V of the previous S_x completed (P_x is
+    written over S_x); the softmax of x reads S_x, writes P_x and, after the
+    unit's last tile, reads O_x, which the next unit's first P V of x
+    overwrites only after the softmax's p_full for it.  The P V issuer issues
+    P_B V_j only after S_A of tile j + 1 has been issued (when tile A has
+    one).  ``mistake``:
+    "qk_skips_p_free", "producer_skips_kv_empty", "pv_skips_p_full"."""
+    rng = random.Random(seed)
+    B = {}
+
+    def bar(name, count=1):
+        if name not in B:
+            B[name] = Bar(name, count)
+        return B[name]
+
+    for x in (0, 1):
+        bar(f"s_full{x}"); bar(f"p_free{x}"); bar(f"o_full{x}"); bar(f"p_full{x}")
+    bar("q_full"); bar("q_empty"); bar("qk_issued_a")
+    for s in range(slots):
+        bar(f"k_full{s}"); bar(f"v_full{s}"); bar(f"kv_empty{s}")
+
+    def fill(pos):   # slot, full-barrier use, empty-barrier use of ring position pos
+        return pos % slots, ((pos // slots) >> 1) if (slots & 1) else pos // slots, pos // slots
+
+    slot_data = {}
+    events = []
+    now = [0.0]
+    seq = [0]
+
+    def later(delay, fn):
+        seq[0] += 1
+        events.append((now[0] + delay, seq[0], fn))
+
+    mma_tail = {"qk": 0.0, "pv": 0.0}
+
+    def mma(issuer, check, commits):
+        t = max(now[0], mma_tail[issuer]) + rng.uniform(0.1, 2.0)
+        mma_tail[issuer] = t
+
+        def done():
+            check()
+            for c in commits:
+                c.arrive()
+        seq[0] += 1
+        events.append((t, seq[0], done))
+
+    # TMEM: s[x] = ("S", x, k) after QK_x #k, ("P", x, k) once the softmax
+    # wrote P over it, ("P", x, k, "done") after its P V; o[x] = (unit, products)
+    s_state = {0: None, 1: None}
+    o_state = {0: None, 1: None}
+
+    def producer():
+        pos = qcount = 0
+        for nA, nB in units:
+            n = max(nA, nB)
+            if n == 0:
+                continue
+            yield lambda: bar("q_empty").try_wait((qcount & 1) ^ 1, qcount - 1)
+            bar("q_full").arrive(tx=1)
+            later(rng.expovariate(1.0), lambda: bar("q_full").complete_tx(1))
+            qcount += 1
+            for j in range(n):
+                for sel in (0, 1):
+                    slot, fuse, euse = fill(pos)
+                    if mistake != "producer_skips_kv_empty":
+                        yield lambda: bar(f"kv_empty{slot}").try_wait((euse & 1) ^ 1, euse - 1)
+                    f = bar(f"{'v' if sel else 'k'}_full{slot}")
+                    f.arrive(tx=1)
+                    slot_data[slot] = None
+
+                    def land(slot=slot, p=pos, f=f):
+                        slot_data[slot] = p
+                        f.complete_tx(1)
+                    later(rng.expovariate(0.5) if rng.random() < 0.9 else rng.uniform(5, 30), land)
+                    pos += 1
+
+    def qk():
+        pos = qcount = 0
+        sc = [0, 0]
+        for nA, nB in units:
+            n, nx = max(nA, nB), (nA, nB)
+            if n == 0:
+                continue
+            yield lambda: bar("q_full").try_wait(qcount & 1, qcount)
+            qcount += 1
+            for j in range(n):
+                slot, fuse, _ = fill(pos)
+                yield lambda: bar(f"k_full{slot}").try_wait(fuse & 1, fuse)
+                assert slot_data.get(slot) == pos, f"QK read slot {slot}: has {slot_data.get(slot)}, wants {pos}"
+                for x in (0, 1):
+                    if j >= nx[x]:
+                        continue
+                    k = sc[x]
+                    if k > 0 and mistake != "qk_skips_p_free":
+                        yield lambda: bar(f"p_free{x}").try_wait((k - 1) & 1, k - 1)
+                    st = s_state[x]
+                    assert st is None or st == ("P", x, k - 1, "done"), f"S{x} overwritten while holding {st}"
+
+                    def chk(x=x, k=k, slot=slot, p=pos):
+                        assert slot_data.get(slot) == p, f"K slot {slot} overwritten under the MMA"
+                        s_state[x] = ("S", x, k)
+                    mma("qk", chk, [bar(f"s_full{x}")])
+                    if x == 0:
+                        bar("qk_issued_a").arrive()   # a plain arrive right after the issue
+                    sc[x] += 1
+                mma("qk", lambda: None, [bar(f"kv_empty{slot}")])
+                pos += 2
+            mma("qk", lambda: None, [bar("q_empty")])
+
+    def pv():
+        pos = 0
+        pc = [0, 0]
+        unit_no = 0
+        for nA, nB in units:
+            n, nx = max(nA, nB), (nA, nB)
+            if n == 0:
+                continue
+            for j in range(n):
+                slot, fuse, _ = fill(pos + 1)
+                v_ready = False
+                for x in (0, 1):
+                    if j >= nx[x]:
+                        continue
+                    k = pc[x]
+                    if mistake != "pv_skips_p_full":
+                        yield lambda: bar(f"p_full{x}").try_wait(k & 1, k)
+                    if x == 1 and j + 1 < nA:   # P_B V_j queued after S_A of tile j + 1
+                        ka = pc[0]
+                        yield lambda: bar("qk_issued_a").try_wait(ka & 1, ka)
+                    if not v_ready:
+                        yield lambda: bar(f"v_full{slot}").try_wait(fuse & 1, fuse)
+                        v_ready = True
+                    assert slot_data.get(slot) == pos + 1, f"PV read slot {slot}: has {slot_data.get(slot)}"
+
+                    def chk(x=x, k=k, j=j, u=unit_no, slot=slot, p=pos + 1):
+                        assert slot_data.get(slot) == p, f"V slot {slot} overwritten under the MMA"
+                        assert s_state[x] == ("P", x, k), f"PV read P{x} holding {s_state[x]}, wants {k}"
+                        s_state[x] = ("P", x, k, "done")
+                        if j == 0:
+                            assert o_state[x] in (None, ("read",)), f"O{x} overwritten while {o_state[x]}"
+                            o_state[x] = (u, 1)
+                        else:
+                            assert o_state[x] == (u, j), f"O{x} holds {o_state[x]}, wants ({u}, {j})"
+                            o_state[x] = (u, j + 1)
+                    commits = [bar(f"p_free{x}")]
+                    if j == nx[x] - 1:
+                        commits.append(bar(f"o_full{x}"))
+                    mma("pv", chk, commits)
+                    pc[x] += 1
+                mma("pv", lambda: None, [bar(f"kv_empty{slot}")])
+                pos += 2
+            unit_no += 1
+
+    def softmax(x):
+        sc = oc = 0
+        unit_no = 0
+        for nA, nB in units:
+            n, nx = max(nA, nB), (nA, nB)
+            if n == 0:
+                continue
+            for j in range(nx[x]):
+                k = sc
+                yield lambda: bar(f"s_full{x}").try_wait(k & 1, k)
+                assert s_state[x] == ("S", x, k), f"softmax read S{x} holding {s_state[x]}, wants {k}"
+                if j > 0 and rng.random() < 0.3:   # a rescale reads and writes O_x in place
+                    assert o_state[x] == (unit_no, j), f"rescale of O{x} while {o_state[x]}"
+                s_state[x] = ("P", x, k)
+                bar(f"p_full{x}").arrive()
+                sc += 1
+            if nx[x] > 0:
+                o = oc
+                yield lambda: bar(f"o_full{x}").try_wait(o & 1, o)
+                assert o_state[x] == (unit_no, nx[x]), f"epilogue read O{x} while {o_state[x]}"
+                o_state[x] = ("read",)
+                oc += 1
+            unit_no += 1
+
+    actors = {"prod": producer(), "qk": qk(), "pv": pv(), "smA": softmax(0), "smB": softmax(1)}
+    waiting = {k: next(g, None) for k, g in actors.items()}
+    while True:
+        ready = [k for k, w in waiting.items() if w is not None and w()]
+        if ready:
+            k = rng.choice(ready)
+            waiting[k] = next(actors[k], None)
+            continue
+        if all(w is None for w in waiting.values()) and not events:
+            return
+        if not events:
+            raise AssertionError(f"deadlock: {[k for k, w in waiting.items() if w is not None]}")
+        events.sort()
+        t, _, fn = events.pop(0)
+        now[0] = t
+        fn()

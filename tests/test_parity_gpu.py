@@ -226,7 +226,9 @@ def test_forward_kernel_gives_up_drains_and_recovers(D, causal, skip):
     st, site = attn.attn_check_device_status(stream)
     assert st == attn.ATTN_ERR_DEVICE_TIMEOUT and site in WAIT_SITES, (st, site)
     assert attn.attn_check_device_status(stream)[0] == attn.ATTN_OK  # cleared
-    # block 0 handles one unit (32 units on the SMs): only its 128 rows may differ
+    # block 0 handles one unit (fewer units than SMs): only its rows may
+    # differ, one 128-row query tile or two adjacent ones of one head (the
+    # padded forward's units are pairs of query tiles)
     o_ref, l_ref = attention_ref(_np(q), _np(k), _np(v), scale, causal=causal)
     on, ln = o.float().cpu().numpy(), lse.cpu().numpy()
     bad = []
@@ -237,7 +239,9 @@ def test_forward_kernel_gives_up_drains_and_recovers(D, causal, skip):
                 check(on[sl], ln[sl], o_ref[sl], l_ref[sl], "")
             except AssertionError:
                 bad.append((h, t0))
-    assert len(bad) <= 1, bad
+    assert len(bad) <= 2, bad
+    if len(bad) == 2:
+        assert bad[0][0] == bad[1][0] and bad[1][1] - bad[0][1] == 128, bad
     # the context is healthy: a normal call matches the oracle
     _full_check(q, k, v, scale, causal, None, "after the aborted launch")
 

@@ -5,7 +5,7 @@ import random
 
 import pytest
 
-from pipeline_model import run
+from pipeline_model import run, run_pair
 
 
 def _units(seed):
@@ -119,3 +119,32 @@ def test_backward_models_catch_a_skipped_wait(kernel, mistake):
         except AssertionError:
             failures += 1
     assert failures > 0, (kernel, mistake)
+
+
+# the padded forward with two query tiles per unit (5 slots at D = 128, 12 at
+# D = 64): unit lists of (K tiles of tile A, of tile B) as causal and
+# non-causal batches give them (n_A = n_B, or n_A = n_B - 1, or tile B absent)
+def _pair_units(seed):
+    rng = random.Random(seed)
+    out = []
+    for _ in range(rng.randint(1, 6)):
+        n = rng.choice([1, 2, 3, 5, 8, 16])
+        out.append(rng.choice([(n, n), (n - 1, n), (n, 0), (0, 0)]))
+    return out
+
+
+@pytest.mark.parametrize("slots", [5, 12])
+def test_pair_protocol_never_aliases_or_deadlocks(slots):
+    for seed in range(400):
+        run_pair(_pair_units(seed), slots, seed=seed)
+
+
+@pytest.mark.parametrize("mistake", ["qk_skips_p_free", "producer_skips_kv_empty", "pv_skips_p_full"])
+def test_pair_model_catches_a_skipped_wait(mistake):
+    failures = 0
+    for seed in range(300):
+        try:
+            run_pair(_pair_units(seed), 5, seed=seed, mistake=mistake)
+        except AssertionError:
+            failures += 1
+    assert failures > 0, mistake

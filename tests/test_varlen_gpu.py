@@ -8,7 +8,7 @@ import torch
 
 from exact_attention_86_gb300 import attn
 from exact_attention_86_gb300.build import build
-from oracle import attention_varlen_ref
+from oracle import attention_ref, attention_varlen_ref
 
 from parity import assert_no_nan, check, nan_filled, tile_rows
 
@@ -105,9 +105,16 @@ def test_varlen_equals_padded_forward_for_equal_lengths():
     cu = torch.arange(0, (B + 1) * S, S, dtype=torch.int32, device=dev)
     o_var, l_var = attn.forward_varlen(pack(q), pack(k), pack(v), cu, cu, S, causal=True)
     torch.cuda.synchronize()
-    # same kernel, same arithmetic order per row: identical bits
-    assert torch.equal(o_var.view(torch.int16), pack(o_pad).view(torch.int16))
-    assert torch.equal(l_var, l_pad.permute(1, 0, 2).reshape(H, B * S))
+    # Different kernels (the padded forward runs two query tiles per unit and
+    # sums a row in one thread, the packed one in two halves): both against
+    # the oracle, and against each other within a rounding of the row sum.
+    o_ref, l_ref = attention_ref(_np(q), _np(k), _np(v), 1 / math.sqrt(D), causal=True)
+    check(o_pad.float().cpu().numpy(), l_pad.cpu().numpy(), o_ref, l_ref, "padded")
+    o_var_p = o_var.view(B, S, H, D).permute(0, 2, 1, 3).float().cpu().numpy()
+    l_var_p = l_var.view(H, B, S).permute(1, 0, 2).cpu().numpy()
+    check(o_var_p, l_var_p, o_ref, l_ref, "packed")
+    assert float((o_var.float() - pack(o_pad).float()).abs().max()) <= 1e-2
+    assert float((l_var - l_pad.permute(1, 0, 2).reshape(H, B * S)).abs().max()) <= 1e-5
 
 
 @pytest.mark.parametrize("name", ["varlen_b32_d128_causal", "varlen_b32_d128"])
