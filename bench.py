@@ -275,12 +275,15 @@ def is_fp8(w) -> bool:
     return isinstance(w, workloads.Fp8Workload)
 
 
-def forward_kernel(w, splits: int) -> str:
-    """The kernel that does the forward's work for this workload: padded bf16
-    batches without causal masking or key ranges run the two-query-tile kernel,
-    every other mode the one-tile kernel."""
-    if not is_varlen(w) and not is_fp8(w) and not w.causal and splits == 0:
-        return "attn_fwd_pair_kernel"
+def forward_kernel(w, splits: int, num_sms: int) -> str:
+    """The kernel that does the forward's work for this workload, as the
+    library chooses it: padded bf16 batches without key ranges may run the
+    two-query-tile kernel (attn_fwd_kernel_choice), every other mode the
+    one-tile kernel."""
+    from exact_attention_86_gb300 import attn
+    if not is_varlen(w) and not is_fp8(w) and splits == 0:
+        if attn.attn_fwd_kernel_choice(w.B, w.H, w.Sq, int(w.causal), num_sms) == 1:
+            return "attn_fwd_pair_kernel"
     return "attn_fwd_kernel"
 
 
@@ -718,7 +721,8 @@ def main():
         hbm_src = "fallback (6.8 TB/s copy)"
     roofline = roofline_bound(step_flops, w.min_bytes, launch_ms, peak, hbm, args.backward)
     roofline["peak_source"] = peak_src if roofline["bound"] == "tensor" else hbm_src
-    kernel = "attn_bwd (delta, dq, dkdv kernels)" if args.backward else forward_kernel(w, args.splits)
+    kernel = "attn_bwd (delta, dq, dkdv kernels)" if args.backward else forward_kernel(
+        w, args.splits, torch.cuda.get_device_properties(dev).multi_processor_count)
     roofline.update({"traffic": None if args.backward else recorded_traffic(kernel, w.name),
                      "kernel": kernel,
                      "launch_ms": launch_ms, "algorithmic_flops_per_launch": step_flops,

@@ -34,6 +34,9 @@ ATTN_ERR_DEVICE_TIMEOUT = 7
 ATTN_ERR_UNSUPPORTED_DEVICE = 8
 ATTN_ERR_WORKSPACE = 9
 
+ATTN_KERNEL_AUTO = -1      # attn_fwd_variant: the kernel attn_fwd would run
+ATTN_KERNEL_ONE_TILE = 0   # units of 128 query rows
+ATTN_KERNEL_TWO_TILE = 1   # units of two 128-row query tiles (non-causal)
 ATTN_V_ROWS = 0        # E4M3 V as [B, H, Sk, D]
 ATTN_V_TRANSPOSED = 1  # E4M3 V as [B, H, D, Sk]
 
@@ -42,6 +45,10 @@ SIGNATURES = {
     "attn_fwd": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                 ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "attn_fwd_variant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                        ctypes.c_void_p]),
     "attn_fwd_fp8": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                     ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
@@ -82,8 +89,9 @@ SIGNATURES = {
     "attn_selftest_launch_floor": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
     "attn_selftest_fwd_abort": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 5 + [ctypes.c_float, ctypes.c_int,
                                                                                           ctypes.c_void_p, ctypes.c_int,
-                                                                                          ctypes.c_int64,
+                                                                                          ctypes.c_int, ctypes.c_int64,
                                                                                           ctypes.c_void_p]),
+    "attn_fwd_kernel_choice": (ctypes.c_int, [ctypes.c_int] * 5),
     "attn_abi_version": (ctypes.c_int, []),
 }
 
@@ -120,6 +128,11 @@ def lib():
 def attn_fwd(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
              scale: float, causal: int, kv_lens: Optional[int], stream: Optional[int]) -> int:
     return lib().attn_fwd(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, stream)
+
+
+def attn_fwd_variant(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
+                     scale: float, causal: int, kv_lens: Optional[int], kernel: int, stream: Optional[int]) -> int:
+    return lib().attn_fwd_variant(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, kernel, stream)
 
 
 def attn_fwd_fp8(q: int, k: int, v_t: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
@@ -205,14 +218,18 @@ def attn_selftest_wait_timeout(limit_ns: int, stream: Optional[int] = None) -> i
 
 
 def attn_selftest_fwd_abort(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
-                            scale: float, causal: int, kv_lens: Optional[int], skip_fill: int, limit_ns: int,
-                            stream: Optional[int] = None) -> int:
-    return lib().attn_selftest_fwd_abort(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, skip_fill,
-                                         limit_ns, stream)
+                            scale: float, causal: int, kv_lens: Optional[int], kernel: int, skip_fill: int,
+                            limit_ns: int, stream: Optional[int] = None) -> int:
+    return lib().attn_selftest_fwd_abort(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, kernel,
+                                         skip_fill, limit_ns, stream)
 
 
 def attn_selftest_launch_floor(grid: int, D: int, mode: int, stream: Optional[int] = None) -> int:
     return lib().attn_selftest_launch_floor(grid, D, mode, stream)
+
+
+def attn_fwd_kernel_choice(B: int, H: int, Sq: int, causal: int, num_sms: int) -> int:
+    return lib().attn_fwd_kernel_choice(B, H, Sq, int(causal), num_sms)
 
 
 def attn_abi_version() -> int:
@@ -475,13 +492,14 @@ def lse_merge(o_parts, lse_parts):
 
 
 def forward(q, k, v, scale: Optional[float] = None, causal: bool = False, kv_lens=None,
-            out=None, lse=None):
+            out=None, lse=None, kernel: int = ATTN_KERNEL_AUTO):
     """Fused attention forward on torch CUDA tensors.
 
     ``q [B,H,Sq,D]``, ``k``/``v [B,H,Sk,D]``: bf16, contiguous, same device.
     ``kv_lens``: ``None`` or an int32 CUDA tensor ``[B]``.  ``scale`` defaults to
-    ``1/sqrt(D)``.  Returns ``(o bf16 [B,H,Sq,D], lse fp32 [B,H,Sq])``.  The call
-    is asynchronous on the current stream."""
+    ``1/sqrt(D)``.  ``kernel``: ``ATTN_KERNEL_AUTO`` (``attn_fwd``) or a kernel
+    forced through ``attn_fwd_variant``.  Returns ``(o bf16 [B,H,Sq,D], lse
+    fp32 [B,H,Sq])``.  The call is asynchronous on the current stream."""
     import torch
 
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -504,8 +522,12 @@ def forward(q, k, v, scale: Optional[float] = None, causal: bool = False, kv_len
     out, lse = _outputs(out, lse, (B, H, Sq, D), (B, H, Sq), q.device)
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
-        st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                      B, H, Sq, Sk, D, float(scale), int(bool(causal)), kv_ptr, stream)
+        if kernel == ATTN_KERNEL_AUTO:
+            st = attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                          B, H, Sq, Sk, D, float(scale), int(bool(causal)), kv_ptr, stream)
+        else:
+            st = attn_fwd_variant(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                  B, H, Sq, Sk, D, float(scale), int(bool(causal)), kv_ptr, int(kernel), stream)
     if st != ATTN_OK:
-        raise AttnError(st, "attn_fwd")
+        raise AttnError(st, "attn_fwd" if kernel == ATTN_KERNEL_AUTO else "attn_fwd_variant")
     return out, lse

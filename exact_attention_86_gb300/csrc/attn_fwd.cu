@@ -1224,6 +1224,23 @@ attn_status launch(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CUtens
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// Whether attn_fwd runs the two-tile kernel: it must finish a batch of
+// equal-length units sooner than the one-tile kernel, counted in waves of
+// units over the SMs, a two-tile unit costing about 1.84 one-tile units (both
+// measured on the S = 8192 and 2048 workloads: 1527 against 1390 TFLOP/s at 7
+// against 14 waves).  A single query tile per head (Sq <= 128) leaves every
+// pair half empty; a small batch whose single tiles fit one wave runs them
+// all at once on the one-tile kernel (e.g. 8 heads of 128 queries).  Causal batches take the one-tile kernel (their
+// pair units measured 3-12 % slower) unless built with ATTN_PAIR_CAUSAL.
+bool use_pair_kernel(int B, int H, int Sq, bool causal, int num_sms) {
+  if ((causal && !ATTN_PAIR_CAUSAL) || B <= 0 || H <= 0 || Sq <= kBQ || num_sms < 1) return false;
+  const uint64_t bh = static_cast<uint64_t>(B) * static_cast<uint64_t>(H);
+  const uint64_t pair_units = bh * ((static_cast<uint64_t>(Sq) + 2 * kBQ - 1) / (2 * kBQ));
+  const uint64_t tile_units = bh * ((static_cast<uint64_t>(Sq) + kBQ - 1) / kBQ);
+  const uint64_t g = static_cast<uint64_t>(num_sms);
+  return 184 * ((pair_units + g - 1) / g) < 100 * ((tile_units + g - 1) / g);
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // LSE merge of key-range partial results: one warp per row, each lane owns
@@ -1374,8 +1391,8 @@ attn_status launch_any(DeviceInfo& dev, int D, bool causal, const CUtensorMap& m
 
 attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const void* v, void* o, float* lse, int B,
                         int H, int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens, int num_splits,
-                        float* o_part, float* lse_part, cudaStream_t s, uint64_t wait_limit_ns = kWaitLimitNs,
-                        int selftest_skip_fill = -1) {
+                        float* o_part, float* lse_part, cudaStream_t s, int kernel = ATTN_KERNEL_AUTO,
+                        uint64_t wait_limit_ns = kWaitLimitNs, int selftest_skip_fill = -1) {
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, B, H, Sq, D)) return ATTN_ERR_CUDA;
   if (Sk > 0) {
@@ -1412,11 +1429,10 @@ attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const voi
   p.wait_limit_ns = wait_limit_ns;
   p.selftest_skip_fill = selftest_skip_fill;
 #ifndef ATTN_NO_PAIR
-  if (o_part == nullptr && (!causal || ATTN_PAIR_CAUSAL)) {
-    // Whole rows without a causal mask: units of two query tiles
-    // (attn_fwd_pair_kernel), measured 8-10 % faster on the non-causal
-    // workloads.  Causal batches stay on attn_fwd_kernel: their pair units
-    // measured 3-12 % slower (coarser units balance worse).
+  const bool pair = kernel == ATTN_KERNEL_TWO_TILE ||
+                    (kernel == ATTN_KERNEL_AUTO && use_pair_kernel(B, H, Sq, causal != 0, dev.num_sms));
+  if (o_part == nullptr && pair) {
+    // whole rows: units of two query tiles (attn_fwd_pair_kernel)
     Params pp = p;
     const uint64_t n_pairs = (static_cast<uint64_t>(Sq) + 2 * kBQ - 1) / (2 * kBQ);
     pp.n_qtiles = static_cast<int>(n_pairs);
@@ -1445,6 +1461,20 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
   if (st != ATTN_OK) return st;
   return run_forward(*dev, q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, 1, nullptr, nullptr,
                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_fwd_variant(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
+                             int Sk, int D, float scale, int causal, const int32_t* kv_lens, int kernel,
+                             attn_stream_t stream) {
+  if (kernel < ATTN_KERNEL_AUTO || kernel > ATTN_KERNEL_TWO_TILE) return ATTN_ERR_SHAPE;
+  if (kernel == ATTN_KERNEL_TWO_TILE && causal && !ATTN_PAIR_CAUSAL) return ATTN_ERR_SHAPE;
+  attn_status st = check_args(q, k, v, o, lse, B, H, Sq, Sk, D, scale, kv_lens, 1);
+  if (st != ATTN_OK || B == 0 || H == 0 || Sq == 0) return st;
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != ATTN_OK) return st;
+  return run_forward(*dev, q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, 1, nullptr, nullptr,
+                     reinterpret_cast<cudaStream_t>(stream), kernel);
 }
 
 attn_status attn_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
@@ -1766,7 +1796,9 @@ attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream) {
 
 attn_status attn_selftest_fwd_abort(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                     int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens,
-                                    int skip_fill, int64_t limit_ns, attn_stream_t stream) {
+                                    int kernel, int skip_fill, int64_t limit_ns, attn_stream_t stream) {
+  if (kernel < ATTN_KERNEL_AUTO || kernel > ATTN_KERNEL_TWO_TILE) return ATTN_ERR_SHAPE;
+  if (kernel == ATTN_KERNEL_TWO_TILE && causal && !ATTN_PAIR_CAUSAL) return ATTN_ERR_SHAPE;
   attn_status st = check_args(q, k, v, o, lse, B, H, Sq, Sk, D, scale, kv_lens, 1);
   if (st != ATTN_OK) return st;
   if (limit_ns < 1000 || limit_ns > 2000000000LL || skip_fill < 0) return ATTN_ERR_SHAPE;
@@ -1776,7 +1808,7 @@ attn_status attn_selftest_fwd_abort(const void* q, const void* k, const void* v,
   st = device_info(&dev);
   if (st != ATTN_OK) return st;
   return run_forward(*dev, q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, 1, nullptr, nullptr,
-                     reinterpret_cast<cudaStream_t>(stream), static_cast<uint64_t>(limit_ns), skip_fill);
+                     reinterpret_cast<cudaStream_t>(stream), kernel, static_cast<uint64_t>(limit_ns), skip_fill);
 }
 
 attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t stream) {
@@ -1798,6 +1830,11 @@ attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t 
   }
   launch_floor_kernel<<<grid, kThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(mode);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_fwd_kernel_choice(int B, int H, int Sq, int causal, int num_sms) {
+  if (B < 0 || H < 0 || Sq < 0 || num_sms < 0) return -1;
+  return use_pair_kernel(B, H, Sq, causal != 0, num_sms) ? 1 : 0;
 }
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }

@@ -86,6 +86,25 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
                      int Sk, int D, float scale, int causal, const int32_t* kv_lens, attn_stream_t stream);
 
 /*
+ * attn_fwd_variant — attn_fwd with the kernel chosen by the caller instead of
+ * by attn_fwd_kernel_choice.  Same arguments, checks, results and errors as
+ * attn_fwd, plus `kernel`:
+ *   ATTN_KERNEL_AUTO (-1)     the kernel attn_fwd would run;
+ *   ATTN_KERNEL_ONE_TILE (0)  work units of 128 query rows;
+ *   ATTN_KERNEL_TWO_TILE (1)  work units of two 128-row query tiles that share
+ *                             every K/V tile (non-causal batches only: with
+ *                             causal != 0 it returns ATTN_ERR_SHAPE).
+ * Both kernels compute the same function within the forward's tolerance;
+ * they split a row's sums differently over threads, so their results are not
+ * bit-identical to each other.
+ * Any other `kernel` value: ATTN_ERR_SHAPE.
+ */
+enum { ATTN_KERNEL_AUTO = -1, ATTN_KERNEL_ONE_TILE = 0, ATTN_KERNEL_TWO_TILE = 1 };
+attn_status attn_fwd_variant(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
+                             int Sk, int D, float scale, int causal, const int32_t* kv_lens, int kernel,
+                             attn_stream_t stream);
+
+/*
  * attn_fwd_fp8 — the forward with FP8 (E4M3) inputs and both products on the
  * tensor cores' 8-bit path ("Fused Multi-Head Attention", the "Quantization"
  * item of the techniques fused attention combines with: FP8 data for the
@@ -336,8 +355,9 @@ attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream);
 /*
  * attn_selftest_fwd_abort — failure-detection self test of the attention
  * kernel itself ("Attention softmax fusion", section "Things that break": a
- * fused kernel must fail without corrupting what it shares).  Runs attn_fwd
- * (same arguments, same checks; Sk >= 1 required) with every bounded wait
+ * fused kernel must fail without corrupting what it shares).  Runs
+ * attn_fwd_variant (same arguments, same checks, `kernel` as there; Sk >= 1
+ * required) with every bounded wait
  * limited to `limit_ns` nanoseconds (1000 .. 2e9) instead of 2 s, and with
  * block 0's producer leaving out its K fill number `skip_fill` (>= 0,
  * counted over that block's K tiles in its order of work).  Nothing ever
@@ -352,7 +372,7 @@ attn_status attn_selftest_wait_timeout(int64_t limit_ns, attn_stream_t stream);
  */
 attn_status attn_selftest_fwd_abort(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                                     int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens,
-                                    int skip_fill, int64_t limit_ns, attn_stream_t stream);
+                                    int kernel, int skip_fill, int64_t limit_ns, attn_stream_t stream);
 
 /*
  * attn_selftest_launch_floor — measurement aid, no attention arithmetic.
@@ -372,10 +392,20 @@ attn_status attn_selftest_fwd_abort(const void* q, const void* k, const void* v,
  */
 attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t stream);
 
+/*
+ * attn_fwd_kernel_choice — which kernel attn_fwd runs for a padded batch of
+ * B x H heads of Sq queries, causal or not, on a device with `num_sms` SMs.
+ * Returns 1 for the two-query-tile kernel (units of 256 query rows), 0 for
+ * the one-tile kernel (units of 128 rows), -1 for a negative argument.  The
+ * two compute the same function; the choice is a performance model (waves of
+ * units over the SMs) and never depends on the data.  Host only: no CUDA call.
+ */
+int attn_fwd_kernel_choice(int B, int H, int Sq, int causal, int num_sms);
+
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 11
+#define ATTN_ABI_VERSION 12
 
 #ifdef __cplusplus
 }

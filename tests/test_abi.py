@@ -289,15 +289,50 @@ def test_launch_floor_argument_checks(lib):
     assert attn.attn_selftest_launch_floor(1, 96, 0, None) == attn.ATTN_ERR_UNSUPPORTED_D
 
 
+def test_kernel_choice(lib):
+    # host-only model of which padded-forward kernel runs (no device call)
+    f = attn.attn_fwd_kernel_choice
+    assert f(2, 16, 8192, 0, 152) == 1      # 1024 pairs: 7 waves against 14 of single tiles
+    assert f(8, 16, 2048, 0, 152) == 1
+    assert f(2, 16, 8192, 1, 152) == 0      # causal: one-tile kernel
+    assert f(1, 8, 128, 0, 152) == 0        # one query tile per head: pairs half empty
+    assert f(1, 1, 128, 0, 152) == 0
+    assert f(1, 1, 8192, 0, 152) == 0       # 64 single tiles fit one wave
+    assert f(0, 16, 8192, 0, 152) == 0
+    assert f(-1, 16, 8192, 0, 152) == -1
+    assert f(2, 16, 8192, 0, -1) == -1
+    # never for a single query tile, whatever the batch
+    for bh in (1, 7, 152, 153, 10_000):
+        assert f(1, bh, 100, 0, 152) == 0
+        assert f(1, bh, 128, 0, 152) == 0
+
+
 def test_fwd_abort_selftest_argument_checks(lib):
     # each call ends at a host-side check (no device query, no launch)
     f = attn.attn_selftest_fwd_abort
-    assert f(A, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, 0, 999, None) == attn.ATTN_ERR_SHAPE
-    assert f(A, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, 0, 3_000_000_000, None) == attn.ATTN_ERR_SHAPE
-    assert f(A, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, -1, 10_000, None) == attn.ATTN_ERR_SHAPE
-    assert f(A, A, A, A, A, 1, 2, 256, 0, 128, 0.1, 0, None, 0, 10_000, None) == attn.ATTN_ERR_SHAPE
-    assert f(A, A, A, A, A, 1, 2, 256, 256, 96, 0.1, 0, None, 0, 10_000, None) == attn.ATTN_ERR_UNSUPPORTED_D
-    assert f(A + 8, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, 0, 10_000, None) == attn.ATTN_ERR_ALIGN
+    a = (A, A, A, A, A, 1, 2, 256)
+    assert f(*a, 256, 128, 0.1, 0, None, -1, 0, 999, None) == attn.ATTN_ERR_SHAPE
+    assert f(*a, 256, 128, 0.1, 0, None, -1, 0, 3_000_000_000, None) == attn.ATTN_ERR_SHAPE
+    assert f(*a, 256, 128, 0.1, 0, None, -1, -1, 10_000, None) == attn.ATTN_ERR_SHAPE
+    assert f(*a, 0, 128, 0.1, 0, None, -1, 0, 10_000, None) == attn.ATTN_ERR_SHAPE
+    assert f(*a, 256, 96, 0.1, 0, None, -1, 0, 10_000, None) == attn.ATTN_ERR_UNSUPPORTED_D
+    assert f(A + 8, *a[1:], 256, 128, 0.1, 0, None, -1, 0, 10_000, None) == attn.ATTN_ERR_ALIGN
+    assert f(*a, 256, 128, 0.1, 0, None, 2, 0, 10_000, None) == attn.ATTN_ERR_SHAPE    # unknown kernel
+    assert f(*a, 256, 128, 0.1, 1, None, 1, 0, 10_000, None) == attn.ATTN_ERR_SHAPE    # two-tile, causal
+
+
+def test_variant_argument_checks(lib):
+    # each call ends at a host-side check (no device query, no launch)
+    f = attn.attn_fwd_variant
+    a = (A, A, A, A, A, 1, 2, 256, 256)
+    assert f(*a, 128, 0.1, 0, None, 2, None) == attn.ATTN_ERR_SHAPE
+    assert f(*a, 128, 0.1, 0, None, -2, None) == attn.ATTN_ERR_SHAPE
+    assert f(*a, 128, 0.1, 1, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_SHAPE
+    assert f(*a, 96, 0.1, 0, None, attn.ATTN_KERNEL_ONE_TILE, None) == attn.ATTN_ERR_UNSUPPORTED_D
+    assert f(*a, 128, float("inf"), 0, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_SCALE
+    assert f(A, None, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, -1, None) == attn.ATTN_ERR_NULLPTR
+    # nothing to compute: OK without a device query or a launch
+    assert f(*a[:5], 0, 2, 256, 256, 128, 0.1, 0, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_OK
 
 
 def test_fp8_ex_argument_checks(lib):

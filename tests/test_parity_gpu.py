@@ -33,7 +33,7 @@ def _lib():
     torch.cuda.init()
 
 
-def _run(q, k, v, scale, causal, kv_lens):
+def _run(q, k, v, scale, causal, kv_lens, kernel=attn.ATTN_KERNEL_AUTO):
     dev = torch.device("cuda:0")
     qd, kd, vd = (t.to(dev).contiguous() for t in (q, k, v))
     kvd = kv_lens.to(dev) if kv_lens is not None else None
@@ -41,7 +41,7 @@ def _run(q, k, v, scale, causal, kv_lens):
     # result of an earlier call in reused memory
     o = nan_filled(tuple(q.shape), torch.bfloat16, dev)
     lse = nan_filled(tuple(q.shape[:3]), torch.float32, dev)
-    attn.forward(qd, kd, vd, scale=scale, causal=causal, kv_lens=kvd, out=o, lse=lse)
+    attn.forward(qd, kd, vd, scale=scale, causal=causal, kv_lens=kvd, out=o, lse=lse, kernel=kernel)
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
     assert_no_nan(o, lse, what="forward")
@@ -61,8 +61,8 @@ def _inputs(B, H, Sq, Sk, D, seed, std=1.0, kv=None):
     return q, k, v, kvt
 
 
-def _full_check(q, k, v, scale, causal, kv_lens, what):
-    o, lse = _run(q, k, v, scale, causal, kv_lens)
+def _full_check(q, k, v, scale, causal, kv_lens, what, kernel=attn.ATTN_KERNEL_AUTO):
+    o, lse = _run(q, k, v, scale, causal, kv_lens, kernel)
     o_ref, lse_ref = attention_ref(_np(q), _np(k), _np(v), scale, causal=causal,
                                    kv_lens=None if kv_lens is None else kv_lens.numpy())
     return check(o, lse, o_ref, lse_ref, what)
@@ -89,20 +89,34 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "B{}H{}q{}k{}d{}{}".format(*s[:5], "c" if s[5] else ""))
-def test_small_shapes(shape):
+# both padded-forward kernels on every non-causal case (the automatic choice
+# takes the one-tile kernel for most small batches); causal: one-tile only
+KERNELS = [attn.ATTN_KERNEL_ONE_TILE, attn.ATTN_KERNEL_TWO_TILE]
+
+
+def _kernels(causal):
+    return [attn.ATTN_KERNEL_ONE_TILE] if causal else KERNELS
+
+
+SMALL_CASES = [(s, kern) for s in SMALL for kern in _kernels(s[5])]
+
+
+@pytest.mark.parametrize("shape,kernel", SMALL_CASES,
+                         ids=lambda x: ("B{}H{}q{}k{}d{}{}".format(*x[:5], "c" if x[5] else "")
+                                        if isinstance(x, tuple) else ("two" if x else "one")))
+def test_small_shapes(shape, kernel):
     B, H, Sq, Sk, D, causal = shape
     q, k, v, _ = _inputs(B, H, Sq, Sk, D, seed=(B * 131 + H * 71 + Sq * 7 + Sk * 13 + D + int(causal)) % 997)
-    _full_check(q, k, v, 1.0 / math.sqrt(D), causal, None, str(shape))
+    _full_check(q, k, v, 1.0 / math.sqrt(D), causal, None, f"{shape} kernel {kernel}", kernel)
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("causal", [False, True])
-def test_kv_lens_edges(D, causal):
+@pytest.mark.parametrize("causal,kernel", [(False, 0), (False, 1), (True, 0)])
+def test_kv_lens_edges(D, causal, kernel):
     Sk = 400
     kv = [0, 1, 127, 128, 129, Sk, 255, 257]
     q, k, v, kvt = _inputs(len(kv), 2, 384, Sk, D, seed=7 + D, kv=kv)
-    _full_check(q, k, v, 1.0 / math.sqrt(D), causal, kvt, f"kv edges D{D} causal{causal}")
+    _full_check(q, k, v, 1.0 / math.sqrt(D), causal, kvt, f"kv edges D{D} causal{causal} kernel {kernel}", kernel)
 
 
 def test_kv_lens_out_of_range_are_clamped():
@@ -113,11 +127,11 @@ def test_kv_lens_out_of_range_are_clamped():
 
 
 @pytest.mark.parametrize("std", [2.0, 4.0])
-@pytest.mark.parametrize("causal", [False, True])
-def test_large_scores_stress_rescale(std, causal):
+@pytest.mark.parametrize("causal,kernel", [(False, 0), (False, 1), (True, 0)])
+def test_large_scores_stress_rescale(std, causal, kernel):
     # Scores with std ~ std^2 * sqrt(D) * scale: the running max moves often.
     q, k, v, _ = _inputs(1, 2, 512, 1024, 128, seed=11, std=std)
-    _full_check(q, k, v, 1.0 / math.sqrt(128), causal, None, f"std {std}")
+    _full_check(q, k, v, 1.0 / math.sqrt(128), causal, None, f"std {std} kernel {kernel}", kernel)
 
 
 def test_increasing_scores_force_rescale_every_tile():
@@ -129,23 +143,26 @@ def test_increasing_scores_force_rescale_every_tile():
     k = torch.linspace(0, 1, S).view(1, 1, S, 1).expand(B, H, S, D) * 0.5 + torch.randn(B, H, S, D, generator=g) * 0.01
     v = torch.randn(B, H, S, D, generator=g)
     q, k, v = (t.to(torch.bfloat16).contiguous() for t in (q, k, v))
-    _full_check(q, k, v, 2.0, False, None, "rescale every tile")
+    for kernel in KERNELS:
+        _full_check(q, k, v, 2.0, False, None, f"rescale every tile, kernel {kernel}", kernel)
     _full_check(q, k, v, 2.0, True, None, "rescale every tile, causal")
 
 
 @pytest.mark.parametrize("scale", [-0.125, 0.0, 1e-3, 0.5])
-def test_scale_values(scale):
+@pytest.mark.parametrize("causal,kernel", [(False, 1), (True, 0)])
+def test_scale_values(scale, causal, kernel):
     q, k, v, _ = _inputs(1, 2, 300, 300, 64, seed=21)
-    _full_check(q, k, v, scale, True, None, f"scale {scale}")
+    _full_check(q, k, v, scale, causal, None, f"scale {scale}", kernel)
 
 
-def test_no_keys_at_all():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_no_keys_at_all(kernel):
     q, k, v, _ = _inputs(2, 2, 200, 1, 128, seed=1)
     k = k[:, :, :0].contiguous()
     v = v[:, :, :0].contiguous()
     dev = torch.device("cuda:0")
     o, lse = attn.forward(q.to(dev), torch.empty(2, 2, 0, 128, dtype=torch.bfloat16, device=dev),
-                          torch.empty(2, 2, 0, 128, dtype=torch.bfloat16, device=dev))
+                          torch.empty(2, 2, 0, 128, dtype=torch.bfloat16, device=dev), kernel=kernel)
     torch.cuda.synchronize()
     assert torch.all(o == 0) and not torch.any(torch.signbit(o.float()))
     assert torch.all(lse == float("-inf"))
@@ -160,7 +177,8 @@ def test_empty_query_is_a_no_op():
     assert o.numel() == 0 and lse.numel() == 0
 
 
-def test_output_guard_bands_untouched():
+@pytest.mark.parametrize("causal,kernel", [(False, 1), (True, 0)])
+def test_output_guard_bands_untouched(causal, kernel):
     # Canary words around O and LSE catch out-of-bounds writes.
     B, H, Sq, Sk, D = 2, 3, 300, 333, 128
     q, k, v, kvt = _inputs(B, H, Sq, Sk, D, seed=9, kv=[333, 100])
@@ -170,19 +188,21 @@ def test_output_guard_bands_untouched():
     l_buf = torch.full((2 * pad + B * H * Sq,), 7.25, dtype=torch.float32, device=dev)
     o_view = o_buf[pad:pad + B * H * Sq * D].view(torch.bfloat16).view(B, H, Sq, D)
     l_view = l_buf[pad:pad + B * H * Sq].view(B, H, Sq)
-    attn.forward(q.to(dev), k.to(dev), v.to(dev), causal=True, kv_lens=kvt.to(dev), out=o_view, lse=l_view)
+    attn.forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, kv_lens=kvt.to(dev), out=o_view, lse=l_view,
+                 kernel=kernel)
     torch.cuda.synchronize()
     assert torch.all(o_buf[:pad] == 12345) and torch.all(o_buf[-pad:] == 12345)
     assert torch.all(l_buf[:pad] == 7.25) and torch.all(l_buf[-pad:] == 7.25)
-    o_ref, lse_ref = attention_ref(_np(q), _np(k), _np(v), 1 / math.sqrt(D), causal=True, kv_lens=[333, 100])
+    o_ref, lse_ref = attention_ref(_np(q), _np(k), _np(v), 1 / math.sqrt(D), causal=causal, kv_lens=[333, 100])
     check(o_view.float().cpu().numpy(), l_view.cpu().numpy(), o_ref, lse_ref, "guard bands")
 
 
-def test_deterministic():
+@pytest.mark.parametrize("causal,kernel", [(False, 1), (True, 0)])
+def test_deterministic(causal, kernel):
     q, k, v, _ = _inputs(2, 4, 1000, 1000, 128, seed=13)
     dev = torch.device("cuda:0")
-    a = attn.forward(q.to(dev), k.to(dev), v.to(dev), causal=True)
-    b = attn.forward(q.to(dev), k.to(dev), v.to(dev), causal=True)
+    a = attn.forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, kernel=kernel)
+    b = attn.forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, kernel=kernel)
     torch.cuda.synchronize()
     assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
     assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
@@ -204,8 +224,9 @@ def test_wait_timeout_selftest_reports_and_recovers():
 WAIT_SITES = set(range(1, 14)) - {8, 12}
 
 
-@pytest.mark.parametrize("D,causal,skip", [(128, False, 5), (128, True, 0), (64, False, 3), (64, True, 10)])
-def test_forward_kernel_gives_up_drains_and_recovers(D, causal, skip):
+@pytest.mark.parametrize("D,causal,kernel,skip", [(128, False, 1, 5), (128, False, 0, 5), (128, True, 0, 0),
+                                                  (64, False, 1, 3), (64, False, 0, 2), (64, True, 0, 10)])
+def test_forward_kernel_gives_up_drains_and_recovers(D, causal, kernel, skip):
     """The attention kernel's own give-up path: block 0's producer leaves out
     one K fill, so a bounded wait (1 ms) in block 0 runs out; every role of
     that block must drain its copies and products, free Tensor Memory and
@@ -221,14 +242,14 @@ def test_forward_kernel_gives_up_drains_and_recovers(D, causal, skip):
     assert attn.attn_check_device_status(stream)[0] == attn.ATTN_OK
     scale = 1.0 / math.sqrt(D)
     st = attn.attn_selftest_fwd_abort(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
-                                      B, H, S, S, D, scale, int(causal), None, skip, 1_000_000, stream)
+                                      B, H, S, S, D, scale, int(causal), None, kernel, skip, 1_000_000, stream)
     assert st == attn.ATTN_OK
     st, site = attn.attn_check_device_status(stream)
     assert st == attn.ATTN_ERR_DEVICE_TIMEOUT and site in WAIT_SITES, (st, site)
     assert attn.attn_check_device_status(stream)[0] == attn.ATTN_OK  # cleared
     # block 0 handles one unit (fewer units than SMs): only its rows may
-    # differ, one 128-row query tile or two adjacent ones of one head (the
-    # padded forward's units are pairs of query tiles)
+    # differ, one 128-row query tile (one-tile kernel) or two adjacent ones of
+    # one head (two-tile kernel)
     o_ref, l_ref = attention_ref(_np(q), _np(k), _np(v), scale, causal=causal)
     on, ln = o.float().cpu().numpy(), lse.cpu().numpy()
     bad = []
@@ -239,11 +260,11 @@ def test_forward_kernel_gives_up_drains_and_recovers(D, causal, skip):
                 check(on[sl], ln[sl], o_ref[sl], l_ref[sl], "")
             except AssertionError:
                 bad.append((h, t0))
-    assert len(bad) <= 2, bad
+    assert len(bad) <= (2 if kernel == attn.ATTN_KERNEL_TWO_TILE else 1), bad
     if len(bad) == 2:
         assert bad[0][0] == bad[1][0] and bad[1][1] - bad[0][1] == 128, bad
     # the context is healthy: a normal call matches the oracle
-    _full_check(q, k, v, scale, causal, None, "after the aborted launch")
+    _full_check(q, k, v, scale, causal, None, "after the aborted launch", kernel)
 
 
 @pytest.mark.parametrize("D", [64, 128])
