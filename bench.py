@@ -44,17 +44,21 @@ METRIC = "fused attention fwd TFLOP/s (bf16) and % of GB300 dense BF16 tensor pe
 METRIC_BWD = "fused attention bwd TFLOP/s (bf16, 2.5x the forward FLOPs) and % of GB300 dense BF16 tensor peak"
 FALLBACK_PEAK_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
-# every source file of the translation unit that holds the forward kernel
-# (attn_fwd.cu includes the PTX wrappers and the backward kernels)
-KERNEL_SOURCES = ["exact_attention_86_gb300/csrc/attn_fwd.cu", "exact_attention_86_gb300/csrc/attn_fwd_pair.cu",
-                  "exact_attention_86_gb300/csrc/attn_common.cuh", "exact_attention_86_gb300/csrc/sm103_ptx.cuh",
-                  "exact_attention_86_gb300/csrc/attn_bwd.cuh", "include/attn.h"]
+# The sources each forward kernel's translation unit compiles from: a traffic
+# record under profiles/ counts only while their hash is the one it names.
+_CSRC = "exact_attention_86_gb300/csrc/"
+KERNEL_SOURCES = {
+    "attn_fwd_kernel": [_CSRC + n for n in ("attn_fwd.cu", "attn_common.cuh", "sm103_ptx.cuh", "attn_bwd.cuh",
+                                            "attn_pair_host.h")] + ["include/attn.h"],
+    "attn_fwd_pair_kernel": [_CSRC + n for n in ("attn_fwd_pair.cu", "attn_common.cuh", "sm103_ptx.cuh",
+                                                 "attn_pair_host.h")],
+}
 L2_BYTES = 129 * 10**6
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -71,7 +75,7 @@ def recorded_traffic(kernel: str, workload: str):
     src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
     wl = re.search(r"workload:\s*(\S+)", text)
     val = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if not (src and wl and val) or src.group(1) != kernel_source_hash() or wl.group(1) != workload:
+    if not (src and wl and val) or src.group(1) != kernel_source_hash(kernel) or wl.group(1) != workload:
         return None
     return float(val.group(1))
 
@@ -282,7 +286,7 @@ def forward_kernel(w, splits: int, num_sms: int) -> str:
     one-tile kernel."""
     from exact_attention_86_gb300 import attn
     if not is_varlen(w) and not is_fp8(w) and splits == 0:
-        if attn.attn_fwd_kernel_choice(w.B, w.H, w.Sq, int(w.causal), num_sms) == 1:
+        if attn.attn_fwd_kernel_choice(w.B, w.H, w.Sq, w.Sk, int(w.causal), num_sms) == 1:
             return "attn_fwd_pair_kernel"
     return "attn_fwd_kernel"
 

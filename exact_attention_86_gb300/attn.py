@@ -36,7 +36,7 @@ ATTN_ERR_WORKSPACE = 9
 
 ATTN_KERNEL_AUTO = -1      # attn_fwd_variant: the kernel attn_fwd would run
 ATTN_KERNEL_ONE_TILE = 0   # units of 128 query rows
-ATTN_KERNEL_TWO_TILE = 1   # units of two 128-row query tiles (non-causal)
+ATTN_KERNEL_TWO_TILE = 1   # units of two 128-row query tiles
 ATTN_V_ROWS = 0        # E4M3 V as [B, H, Sk, D]
 ATTN_V_TRANSPOSED = 1  # E4M3 V as [B, H, D, Sk]
 
@@ -91,7 +91,8 @@ SIGNATURES = {
                                                                                           ctypes.c_void_p, ctypes.c_int,
                                                                                           ctypes.c_int, ctypes.c_int64,
                                                                                           ctypes.c_void_p]),
-    "attn_fwd_kernel_choice": (ctypes.c_int, [ctypes.c_int] * 5),
+    "attn_fwd_kernel_choice": (ctypes.c_int, [ctypes.c_int] * 6),
+    "attn_fwd_pair_schedule": (ctypes.c_int64, [ctypes.c_int] * 6 + [ctypes.c_void_p, ctypes.c_int64]),
     "attn_abi_version": (ctypes.c_int, []),
 }
 
@@ -228,8 +229,17 @@ def attn_selftest_launch_floor(grid: int, D: int, mode: int, stream: Optional[in
     return lib().attn_selftest_launch_floor(grid, D, mode, stream)
 
 
-def attn_fwd_kernel_choice(B: int, H: int, Sq: int, causal: int, num_sms: int) -> int:
-    return lib().attn_fwd_kernel_choice(B, H, Sq, int(causal), num_sms)
+def attn_fwd_kernel_choice(B: int, H: int, Sq: int, Sk: int, causal: int, num_sms: int) -> int:
+    return lib().attn_fwd_kernel_choice(B, H, Sq, Sk, int(causal), num_sms)
+
+
+def attn_fwd_pair_schedule(B: int, H: int, Sq: int, Sk: int, head_group: int, grid: int, max_units: int = 4096):
+    """The static deal of a causal batch's two-tile units: a bytes object whose
+    entry t is the block that runs unit t, or None when the library declines
+    (too many units or an argument out of range)."""
+    buf = (ctypes.c_uint8 * max(max_units, 1))()
+    n = lib().attn_fwd_pair_schedule(B, H, Sq, Sk, head_group, grid, buf, max_units)
+    return None if n < 0 else bytes(buf[:n])
 
 
 def attn_abi_version() -> int:

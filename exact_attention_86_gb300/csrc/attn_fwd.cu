@@ -1224,23 +1224,6 @@ attn_status launch(DeviceInfo& dev, int idx, const CUtensorMap& mq, const CUtens
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-// Whether attn_fwd runs the two-tile kernel: it must finish a batch of
-// equal-length units sooner than the one-tile kernel, counted in waves of
-// units over the SMs, a two-tile unit costing about 1.84 one-tile units (both
-// measured on the S = 8192 and 2048 workloads: 1527 against 1390 TFLOP/s at 7
-// against 14 waves).  A single query tile per head (Sq <= 128) leaves every
-// pair half empty; a small batch whose single tiles fit one wave runs them
-// all at once on the one-tile kernel (e.g. 8 heads of 128 queries).  Causal batches take the one-tile kernel (their
-// pair units measured 3-12 % slower) unless built with ATTN_PAIR_CAUSAL.
-bool use_pair_kernel(int B, int H, int Sq, bool causal, int num_sms) {
-  if ((causal && !ATTN_PAIR_CAUSAL) || B <= 0 || H <= 0 || Sq <= kBQ || num_sms < 1) return false;
-  const uint64_t bh = static_cast<uint64_t>(B) * static_cast<uint64_t>(H);
-  const uint64_t pair_units = bh * ((static_cast<uint64_t>(Sq) + 2 * kBQ - 1) / (2 * kBQ));
-  const uint64_t tile_units = bh * ((static_cast<uint64_t>(Sq) + kBQ - 1) / kBQ);
-  const uint64_t g = static_cast<uint64_t>(num_sms);
-  return 184 * ((pair_units + g - 1) / g) < 100 * ((tile_units + g - 1) / g);
-}
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // LSE merge of key-range partial results: one warp per row, each lane owns
@@ -1430,7 +1413,7 @@ attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const voi
   p.selftest_skip_fill = selftest_skip_fill;
 #ifndef ATTN_NO_PAIR
   const bool pair = kernel == ATTN_KERNEL_TWO_TILE ||
-                    (kernel == ATTN_KERNEL_AUTO && use_pair_kernel(B, H, Sq, causal != 0, dev.num_sms));
+                    (kernel == ATTN_KERNEL_AUTO && attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, dev.num_sms));
   if (o_part == nullptr && pair) {
     // whole rows: units of two query tiles (attn_fwd_pair_kernel)
     Params pp = p;
@@ -1467,7 +1450,6 @@ attn_status attn_fwd_variant(const void* q, const void* k, const void* v, void* 
                              int Sk, int D, float scale, int causal, const int32_t* kv_lens, int kernel,
                              attn_stream_t stream) {
   if (kernel < ATTN_KERNEL_AUTO || kernel > ATTN_KERNEL_TWO_TILE) return ATTN_ERR_SHAPE;
-  if (kernel == ATTN_KERNEL_TWO_TILE && causal && !ATTN_PAIR_CAUSAL) return ATTN_ERR_SHAPE;
   attn_status st = check_args(q, k, v, o, lse, B, H, Sq, Sk, D, scale, kv_lens, 1);
   if (st != ATTN_OK || B == 0 || H == 0 || Sq == 0) return st;
   DeviceInfo* dev = nullptr;
@@ -1798,7 +1780,6 @@ attn_status attn_selftest_fwd_abort(const void* q, const void* k, const void* v,
                                     int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens,
                                     int kernel, int skip_fill, int64_t limit_ns, attn_stream_t stream) {
   if (kernel < ATTN_KERNEL_AUTO || kernel > ATTN_KERNEL_TWO_TILE) return ATTN_ERR_SHAPE;
-  if (kernel == ATTN_KERNEL_TWO_TILE && causal && !ATTN_PAIR_CAUSAL) return ATTN_ERR_SHAPE;
   attn_status st = check_args(q, k, v, o, lse, B, H, Sq, Sk, D, scale, kv_lens, 1);
   if (st != ATTN_OK) return st;
   if (limit_ns < 1000 || limit_ns > 2000000000LL || skip_fill < 0) return ATTN_ERR_SHAPE;
@@ -1832,9 +1813,14 @@ attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t 
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-int attn_fwd_kernel_choice(int B, int H, int Sq, int causal, int num_sms) {
-  if (B < 0 || H < 0 || Sq < 0 || num_sms < 0) return -1;
-  return use_pair_kernel(B, H, Sq, causal != 0, num_sms) ? 1 : 0;
+int64_t attn_fwd_pair_schedule(int B, int H, int Sq, int Sk, int head_group, int grid, uint8_t* owner,
+                               int64_t max_units) {
+  return attn_pair_host::build_schedule(B, H, Sq, Sk, head_group, grid, owner, max_units);
+}
+
+int attn_fwd_kernel_choice(int B, int H, int Sq, int Sk, int causal, int num_sms) {
+  if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || num_sms < 0) return -1;
+  return attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, num_sms) ? 1 : 0;
 }
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }

@@ -37,7 +37,14 @@
 // has in flight, frees TMEM and returns.  The softmax threads never use a
 // named barrier, so no role can be left waiting for another that has left.
 
+#include <algorithm>
 #include <atomic>
+#include <cstring>
+#include <functional>
+#include <mutex>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include "attn_common.cuh"
 #include "attn_pair_host.h"
@@ -94,6 +101,19 @@ struct UnitPair {
   int kv;       // valid keys of the batch entry
   int n[2];     // K tiles tile A / B processes
   int n_max;
+};
+
+// A static deal of the causal units to the blocks, computed on the host
+// (attn_pair_host::build_schedule: longest processing time first, from a
+// cost model of each unit) and passed by value with the launch: byte t of
+// `owner` is the block that runs unit t of the units' order; n == 0: the
+// round-robin deal of unit_at instead.  The non-causal kernel's units are all
+// of one length and take the round-robin deal (a one-word placeholder).
+constexpr int kSchedMaxUnits = 4096;
+template <bool ON>
+struct UnitSched {
+  int n;
+  uint32_t owner[ON ? kSchedMaxUnits / 4 : 1];
 };
 
 // Unit t: (b, h, pair of query tiles), ordered as attn_fwd_kernel's units
@@ -196,7 +216,8 @@ __device__ __forceinline__ void load_s128(uint32_t tS, uint32_t (&sp)[128]) {
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
-                         const __grid_constant__ CUtensorMap map_v, const Params p) {
+                         const __grid_constant__ CUtensorMap map_v, const Params p,
+                         const __grid_constant__ UnitSched<CAUSAL> sched) {
   using G = GeoPair<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_addr(smem_raw);
@@ -274,13 +295,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t pol_once = l2_policy_evict_first();  // Q: read once
         uint32_t pos = 0, qcount = 0, kq = 0;               // pos: ring positions filled (K_t at 2t, V_t at 2t+1)
         int t_static = blockIdx.x;
+        int t_sched = 0;  // static deal: next unit of the order to look at
         bool ok = true;
         while (ok) {
           int unit = -1;
           UnitPair u;
-          while (t_static < t_end) {
-            const int cand = unit_at<CAUSAL>(p, t_static);
-            t_static += gridDim.x;
+          for (;;) {
+            int cand;
+            if (CAUSAL && sched.n > 0) {
+              // the next unit this block owns in the host's deal
+              while (t_sched < sched.n &&
+                     ((sched.owner[t_sched >> 2] >> (8 * (t_sched & 3))) & 0xffu) != blockIdx.x)
+                ++t_sched;
+              if (t_sched >= sched.n) break;
+              cand = t_sched++;
+            } else {
+              if (t_static >= t_end) break;
+              cand = unit_at<CAUSAL>(p, t_static);
+              t_static += gridDim.x;
+            }
             if (cand >= p.total_units) continue;
             u = decode_pair<CAUSAL>(p, cand);
             if (u.rows[0] > 0) {
@@ -618,6 +651,72 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kMaxDevicesPair = 64;
 std::atomic<bool> g_pair_smem_set[kMaxDevicesPair][4];
 
+// Cost model of a unit, in hundredths of the time one 128-key tile takes the
+// one-tile kernel: a key tile that both query tiles of a pair process costs
+// 184 (measured: 1527 against 1390 TFLOP/s on the S = 8192 workload), one
+// that only tile B processes (the last of a causal pair) 130, and the fixed
+// part of a unit (Q load, first tile, epilogue) 150 for a single tile and
+// 200 for a pair (both estimates from a clock trace of the one-tile kernel).
+constexpr int64_t kCostTile = 100, kCostUnit = 150, kCostBoth = 184, kCostAlone = 130, kCostPairUnit = 200;
+
+int64_t key_tiles(int64_t q0, int64_t rows, int64_t Sk, bool causal) {
+  if (rows <= 0) return 0;
+  const int64_t lim = causal ? std::min(Sk, q0 + rows) : Sk;
+  return (lim + kBK - 1) / kBK;
+}
+
+// modelled time of single-tile unit `qt` and of pair unit `pr`
+int64_t tile_cost(int64_t qt, int64_t Sq, int64_t Sk, bool causal) {
+  const int64_t q0 = qt * kBQ;
+  return key_tiles(q0, std::min<int64_t>(kBQ, Sq - q0), Sk, causal) * kCostTile + kCostUnit;
+}
+
+int64_t pair_cost(int64_t pr, int64_t Sq, int64_t Sk, bool causal) {
+  const int64_t q0 = pr * 2 * kBQ;
+  const int64_t na = key_tiles(q0, std::min<int64_t>(kBQ, Sq - q0), Sk, causal);
+  const int64_t nb = key_tiles(q0 + kBQ, std::min<int64_t>(kBQ, Sq - q0 - kBQ), Sk, causal);
+  const int64_t both = std::min(na, nb);
+  return both * kCostBoth + (std::max(na, nb) - both) * kCostAlone + kCostPairUnit;
+}
+
+struct CachedSchedule {
+  int B = -1, H = 0, Sq = 0, Sk = 0, head_group = 0, grid = 0;
+  int64_t n = 0;
+  uint8_t owner[kSchedMaxUnits];
+};
+constexpr int kScheduleCacheSize = 8;
+std::mutex g_sched_mutex;
+CachedSchedule g_sched_cache[kScheduleCacheSize];
+int g_sched_next = 0;
+
+// The schedule for a causal launch, built once per shape and kept in a small
+// cache (the deal of up to 4096 units costs tens of microseconds of host time).
+bool causal_schedule(const Params& p, int grid, UnitSched<true>& out) {
+  std::lock_guard<std::mutex> lock(g_sched_mutex);
+  CachedSchedule* hit = nullptr;
+  for (CachedSchedule& c : g_sched_cache)
+    if (c.B == p.B && c.H == p.H && c.Sq == p.Sq && c.Sk == p.Sk && c.head_group == p.head_group && c.grid == grid)
+      hit = &c;
+  if (hit == nullptr) {
+    CachedSchedule& c = g_sched_cache[g_sched_next];
+    c.B = -1;
+    c.n = attn_pair_host::build_schedule(p.B, p.H, p.Sq, p.Sk, p.head_group, grid, c.owner, kSchedMaxUnits);
+    if (c.n < 0) return false;
+    c.B = p.B;
+    c.H = p.H;
+    c.Sq = p.Sq;
+    c.Sk = p.Sk;
+    c.head_group = p.head_group;
+    c.grid = grid;
+    g_sched_next = (g_sched_next + 1) % kScheduleCacheSize;
+    hit = &c;
+  }
+  out.n = static_cast<int>(hit->n);
+  std::memset(out.owner, 0, sizeof(out.owner));
+  std::memcpy(out.owner, hit->owner, static_cast<size_t>(hit->n));  // little-endian bytes: entry t is byte t
+  return true;
+}
+
 template <int D, bool CAUSAL>
 attn_status launch_pair(int dev, int idx, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk,
                         const CUtensorMap& mv, const Params& p0, cudaStream_t stream) {
@@ -630,7 +729,12 @@ attn_status launch_pair(int dev, int idx, int num_sms, const CUtensorMap& mq, co
     g_pair_smem_set[dev][idx].store(true, std::memory_order_release);
   }
   const int grid = p0.total_units < num_sms ? p0.total_units : num_sms;
-  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, with_divisors(p0, grid));
+  UnitSched<CAUSAL> sched;
+  sched.n = 0;
+  if constexpr (CAUSAL) {
+    if (!causal_schedule(p0, grid, sched)) sched.n = 0;  // too many units: the round-robin deal
+  }
+  kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, with_divisors(p0, grid), sched);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -638,17 +742,71 @@ attn_status launch_pair(int dev, int idx, int num_sms, const CUtensorMap& mq, co
 
 namespace attn_pair_host {
 
+bool use_pair(int B, int H, int Sq, int Sk, bool causal, int num_sms) {
+  if (B <= 0 || H <= 0 || Sq <= kBQ || Sk < 0 || num_sms < 1) return false;
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  const int64_t g = num_sms;
+  const int64_t n_tiles = (static_cast<int64_t>(Sq) + kBQ - 1) / kBQ;
+  const int64_t n_pairs = (static_cast<int64_t>(Sq) + 2 * kBQ - 1) / (2 * kBQ);
+  if (!causal) {
+    // units of one length: waves of units over the SMs
+    return kCostBoth * ((bh * n_pairs + g - 1) / g) < kCostTile * ((bh * n_tiles + g - 1) / g);
+  }
+  // causal units of many lengths, dealt longest first: the time is about the
+  // larger of the longest unit and the mean work per SM; the pair kernel
+  // needs its static deal (at most 4096 units) to balance
+  if (bh * n_pairs > kSchedMaxUnits) return false;
+  int64_t one_total = 0, one_max = 0, pair_total = 0, pair_max = 0;
+  for (int64_t t = 0; t < n_tiles; ++t) {
+    const int64_t c = tile_cost(t, Sq, Sk, true);
+    one_total += c;
+    one_max = std::max(one_max, c);
+  }
+  for (int64_t t = 0; t < n_pairs; ++t) {
+    const int64_t c = pair_cost(t, Sq, Sk, true);
+    pair_total += c;
+    pair_max = std::max(pair_max, c);
+  }
+  const int64_t one = std::max(one_max, (bh * one_total + g - 1) / g);
+  const int64_t pair = std::max(pair_max, (bh * pair_total + g - 1) / g);
+  return pair < one;
+}
+
+int64_t build_schedule(int B, int H, int Sq, int Sk, int head_group, int grid, uint8_t* owner, int64_t max_units) {
+  if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || head_group < 1 || grid < 1 || grid > 256 || owner == nullptr)
+    return -1;
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  const int64_t n_pairs = (static_cast<int64_t>(Sq) + 2 * kBQ - 1) / (2 * kBQ);
+  const int64_t n = bh * n_pairs;
+  if (n > max_units) return -1;
+  // the kernel's unit order (decode_pair<true>): groups of head_group heads,
+  // within a group the pairs from the last one down, each over the group's heads
+  using Load = std::pair<int64_t, int>;
+  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> free_at;
+  for (int b = 0; b < grid; ++b) free_at.push({0, b});
+  int64_t t = 0;
+  for (int64_t g0 = 0; g0 < bh; g0 += head_group) {
+    const int64_t heads = std::min<int64_t>(head_group, bh - g0);
+    for (int64_t wq = 0; wq < n_pairs; ++wq) {
+      const int64_t c = pair_cost(n_pairs - 1 - wq, Sq, Sk, true);
+      for (int64_t h = 0; h < heads; ++h, ++t) {
+        const Load l = free_at.top();
+        free_at.pop();
+        owner[t] = static_cast<uint8_t>(l.second);
+        free_at.push({l.first + c, l.second});
+      }
+    }
+  }
+  return n;
+}
+
 attn_status launch(int D, bool causal, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk,
                    const CUtensorMap& mv, const attn_detail::Params& p, cudaStream_t s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
-#if ATTN_PAIR_CAUSAL
   if (causal)
     return D == 64 ? launch_pair<64, true>(dev, 0, num_sms, mq, mk, mv, p, s)
                    : launch_pair<128, true>(dev, 2, num_sms, mq, mk, mv, p, s);
-#else
-  if (causal) return ATTN_ERR_SHAPE;  // not reached: causal batches take attn_fwd_kernel then
-#endif
   return D == 64 ? launch_pair<64, false>(dev, 1, num_sms, mq, mk, mv, p, s)
                  : launch_pair<128, false>(dev, 3, num_sms, mq, mk, mv, p, s);
 }

@@ -10,24 +10,33 @@
 
 #include "attn.h"
 
-// 1: causal padded batches also take the two-tile kernel (a build option; the
-// causal instantiations are compiled only then)
-#ifndef ATTN_PAIR_CAUSAL
-#define ATTN_PAIR_CAUSAL 0
-#endif
-
 namespace attn_detail {
 struct Params;
 }
 
 namespace attn_pair_host {
 
+// Whether a padded batch of B x H heads (Sq queries, Sk keys) runs faster on
+// the two-tile kernel than on the one-tile kernel of attn_fwd.cu, on a device
+// with num_sms SMs.  A cost model of each work unit, host arithmetic only;
+// false for arguments out of range.
+bool use_pair(int B, int H, int Sq, int Sk, bool causal, int num_sms);
+
 // Launches the padded forward over units of two 128-row query tiles
 // (p.n_qtiles = tile pairs per head, p.total_units = B * H * pairs; every
 // other field as for attn_fwd_kernel, without key ranges) on `stream`, with
-// one block per SM up to the number of units.
+// one block per SM up to the number of units.  Causal batches get a static
+// longest-first deal of their units (see build_schedule).
 attn_status launch(int D, bool causal, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk,
                    const CUtensorMap& mv, const attn_detail::Params& p, cudaStream_t stream);
+
+// The static deal of a causal batch's pair units to `grid` blocks, in the
+// kernel's unit order (head groups of `head_group` heads, longest units first
+// within a group): owner[t] is the block that runs unit t.  Each unit in
+// turn goes to the block with the least modelled work so far (the lowest
+// index among equals).  Returns the number of units (B * H * pairs), or -1
+// when it exceeds max_units or an argument is out of range (owner untouched).
+int64_t build_schedule(int B, int H, int Sq, int Sk, int head_group, int grid, uint8_t* owner, int64_t max_units);
 
 // Reads this translation unit's device status word into host[3] ([0]: a wait
 // gave up, [1]: its site, [2]: its block) and clears it if it was set.

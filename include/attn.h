@@ -92,8 +92,9 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
  *   ATTN_KERNEL_AUTO (-1)     the kernel attn_fwd would run;
  *   ATTN_KERNEL_ONE_TILE (0)  work units of 128 query rows;
  *   ATTN_KERNEL_TWO_TILE (1)  work units of two 128-row query tiles that share
- *                             every K/V tile (non-causal batches only: with
- *                             causal != 0 it returns ATTN_ERR_SHAPE).
+ *                             every K/V tile (causal batches: dealt to the
+ *                             SMs by a static longest-first schedule when
+ *                             they have at most 4096 such units).
  * Both kernels compute the same function within the forward's tolerance;
  * they split a row's sums differently over threads, so their results are not
  * bit-identical to each other.
@@ -394,18 +395,36 @@ attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t 
 
 /*
  * attn_fwd_kernel_choice — which kernel attn_fwd runs for a padded batch of
- * B x H heads of Sq queries, causal or not, on a device with `num_sms` SMs.
- * Returns 1 for the two-query-tile kernel (units of 256 query rows), 0 for
- * the one-tile kernel (units of 128 rows), -1 for a negative argument.  The
- * two compute the same function; the choice is a performance model (waves of
- * units over the SMs) and never depends on the data.  Host only: no CUDA call.
+ * B x H heads of Sq queries and Sk keys, causal or not, on a device with
+ * `num_sms` SMs.  Returns 1 for the two-query-tile kernel (units of 256 query
+ * rows), 0 for the one-tile kernel (units of 128 rows), -1 for a negative
+ * argument.  The two compute the same function; the choice is a cost model
+ * of the work units (non-causal: waves of equal units over the SMs; causal:
+ * the larger of the longest unit and the mean work per SM, with at most 4096
+ * two-tile units) and never depends on the data.  Host only: no CUDA call.
  */
-int attn_fwd_kernel_choice(int B, int H, int Sq, int causal, int num_sms);
+int attn_fwd_kernel_choice(int B, int H, int Sq, int Sk, int causal, int num_sms);
+
+/*
+ * attn_fwd_pair_schedule — the static deal of a causal batch's two-tile units
+ * that attn_fwd uses on the two-tile kernel: owner[t] (host memory, at least
+ * max_units bytes, caller-owned) receives the block that runs unit t, t in
+ * the kernel's unit order: groups of `head_group` (b, h) heads in b-major
+ * order, within a group the 256-row query pairs from the last one down, each
+ * over the group's heads.  Each unit in turn goes to the block with the least
+ * modelled work so far (lowest index among equals); the model counts a unit's
+ * key tiles ("Attention softmax fusion", section "The tile loop": one key
+ * tile per step) plus a fixed part.  Returns the number of units
+ * (B * H * ceil(Sq / 256)), or -1 when that exceeds max_units, grid is not
+ * 1 .. 256, head_group < 1 or an argument is negative.  Host only.
+ */
+int64_t attn_fwd_pair_schedule(int B, int H, int Sq, int Sk, int head_group, int grid, uint8_t* owner,
+                               int64_t max_units);
 
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 12
+#define ATTN_ABI_VERSION 13
 
 #ifdef __cplusplus
 }

@@ -292,19 +292,24 @@ def test_launch_floor_argument_checks(lib):
 def test_kernel_choice(lib):
     # host-only model of which padded-forward kernel runs (no device call)
     f = attn.attn_fwd_kernel_choice
-    assert f(2, 16, 8192, 0, 152) == 1      # 1024 pairs: 7 waves against 14 of single tiles
-    assert f(8, 16, 2048, 0, 152) == 1
-    assert f(2, 16, 8192, 1, 152) == 0      # causal: one-tile kernel
-    assert f(1, 8, 128, 0, 152) == 0        # one query tile per head: pairs half empty
-    assert f(1, 1, 128, 0, 152) == 0
-    assert f(1, 1, 8192, 0, 152) == 0       # 64 single tiles fit one wave
-    assert f(0, 16, 8192, 0, 152) == 0
-    assert f(-1, 16, 8192, 0, 152) == -1
-    assert f(2, 16, 8192, 0, -1) == -1
+    assert f(2, 16, 8192, 8192, 0, 152) == 1      # 1024 pairs: 7 waves against 14 of single tiles
+    assert f(8, 16, 2048, 2048, 0, 152) == 1
+    assert f(2, 16, 8192, 8192, 1, 152) == 1      # causal, 1024 pair units dealt statically
+    assert f(1, 8, 32768, 32768, 1, 152) == 1
+    assert f(4, 8, 1024, 1024, 1, 152) == 0       # causal, short: the longest pair unit sets the time
+    assert f(16, 16, 8192, 8192, 1, 152) == 0     # causal, 8192 pair units: more than the static deal holds
+    assert f(1, 8, 128, 32768, 0, 152) == 0       # one query tile per head: pairs half empty
+    assert f(1, 1, 128, 128, 0, 152) == 0
+    assert f(1, 1, 8192, 8192, 0, 152) == 0       # 64 single tiles fit one wave
+    assert f(0, 16, 8192, 8192, 0, 152) == 0
+    assert f(-1, 16, 8192, 8192, 0, 152) == -1
+    assert f(2, 16, 8192, -1, 0, 152) == -1
+    assert f(2, 16, 8192, 8192, 0, -1) == -1
     # never for a single query tile, whatever the batch
     for bh in (1, 7, 152, 153, 10_000):
-        assert f(1, bh, 100, 0, 152) == 0
-        assert f(1, bh, 128, 0, 152) == 0
+        for causal in (0, 1):
+            assert f(1, bh, 100, 100, causal, 152) == 0
+            assert f(1, bh, 128, 4096, causal, 152) == 0
 
 
 def test_fwd_abort_selftest_argument_checks(lib):
@@ -318,7 +323,6 @@ def test_fwd_abort_selftest_argument_checks(lib):
     assert f(*a, 256, 96, 0.1, 0, None, -1, 0, 10_000, None) == attn.ATTN_ERR_UNSUPPORTED_D
     assert f(A + 8, *a[1:], 256, 128, 0.1, 0, None, -1, 0, 10_000, None) == attn.ATTN_ERR_ALIGN
     assert f(*a, 256, 128, 0.1, 0, None, 2, 0, 10_000, None) == attn.ATTN_ERR_SHAPE    # unknown kernel
-    assert f(*a, 256, 128, 0.1, 1, None, 1, 0, 10_000, None) == attn.ATTN_ERR_SHAPE    # two-tile, causal
 
 
 def test_variant_argument_checks(lib):
@@ -327,7 +331,6 @@ def test_variant_argument_checks(lib):
     a = (A, A, A, A, A, 1, 2, 256, 256)
     assert f(*a, 128, 0.1, 0, None, 2, None) == attn.ATTN_ERR_SHAPE
     assert f(*a, 128, 0.1, 0, None, -2, None) == attn.ATTN_ERR_SHAPE
-    assert f(*a, 128, 0.1, 1, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_SHAPE
     assert f(*a, 96, 0.1, 0, None, attn.ATTN_KERNEL_ONE_TILE, None) == attn.ATTN_ERR_UNSUPPORTED_D
     assert f(*a, 128, float("inf"), 0, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_SCALE
     assert f(A, None, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, -1, None) == attn.ATTN_ERR_NULLPTR

@@ -89,16 +89,11 @@ SMALL = [
 ]
 
 
-# both padded-forward kernels on every non-causal case (the automatic choice
-# takes the one-tile kernel for most small batches); causal: one-tile only
+# both padded-forward kernels on every case (the automatic choice takes the
+# one-tile kernel for most small batches)
 KERNELS = [attn.ATTN_KERNEL_ONE_TILE, attn.ATTN_KERNEL_TWO_TILE]
 
-
-def _kernels(causal):
-    return [attn.ATTN_KERNEL_ONE_TILE] if causal else KERNELS
-
-
-SMALL_CASES = [(s, kern) for s in SMALL for kern in _kernels(s[5])]
+SMALL_CASES = [(s, kern) for s in SMALL for kern in KERNELS]
 
 
 @pytest.mark.parametrize("shape,kernel", SMALL_CASES,
@@ -111,7 +106,7 @@ def test_small_shapes(shape, kernel):
 
 
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("causal,kernel", [(False, 0), (False, 1), (True, 0)])
+@pytest.mark.parametrize("causal,kernel", [(False, 0), (False, 1), (True, 0), (True, 1)])
 def test_kv_lens_edges(D, causal, kernel):
     Sk = 400
     kv = [0, 1, 127, 128, 129, Sk, 255, 257]
@@ -127,7 +122,7 @@ def test_kv_lens_out_of_range_are_clamped():
 
 
 @pytest.mark.parametrize("std", [2.0, 4.0])
-@pytest.mark.parametrize("causal,kernel", [(False, 0), (False, 1), (True, 0)])
+@pytest.mark.parametrize("causal,kernel", [(False, 0), (False, 1), (True, 0), (True, 1)])
 def test_large_scores_stress_rescale(std, causal, kernel):
     # Scores with std ~ std^2 * sqrt(D) * scale: the running max moves often.
     q, k, v, _ = _inputs(1, 2, 512, 1024, 128, seed=11, std=std)
@@ -145,11 +140,11 @@ def test_increasing_scores_force_rescale_every_tile():
     q, k, v = (t.to(torch.bfloat16).contiguous() for t in (q, k, v))
     for kernel in KERNELS:
         _full_check(q, k, v, 2.0, False, None, f"rescale every tile, kernel {kernel}", kernel)
-    _full_check(q, k, v, 2.0, True, None, "rescale every tile, causal")
+        _full_check(q, k, v, 2.0, True, None, f"rescale every tile, causal, kernel {kernel}", kernel)
 
 
 @pytest.mark.parametrize("scale", [-0.125, 0.0, 1e-3, 0.5])
-@pytest.mark.parametrize("causal,kernel", [(False, 1), (True, 0)])
+@pytest.mark.parametrize("causal,kernel", [(False, 1), (True, 0), (True, 1)])
 def test_scale_values(scale, causal, kernel):
     q, k, v, _ = _inputs(1, 2, 300, 300, 64, seed=21)
     _full_check(q, k, v, scale, causal, None, f"scale {scale}", kernel)
@@ -177,7 +172,7 @@ def test_empty_query_is_a_no_op():
     assert o.numel() == 0 and lse.numel() == 0
 
 
-@pytest.mark.parametrize("causal,kernel", [(False, 1), (True, 0)])
+@pytest.mark.parametrize("causal,kernel", [(False, 1), (True, 0), (True, 1)])
 def test_output_guard_bands_untouched(causal, kernel):
     # Canary words around O and LSE catch out-of-bounds writes.
     B, H, Sq, Sk, D = 2, 3, 300, 333, 128
@@ -197,7 +192,7 @@ def test_output_guard_bands_untouched(causal, kernel):
     check(o_view.float().cpu().numpy(), l_view.cpu().numpy(), o_ref, lse_ref, "guard bands")
 
 
-@pytest.mark.parametrize("causal,kernel", [(False, 1), (True, 0)])
+@pytest.mark.parametrize("causal,kernel", [(False, 1), (True, 0), (True, 1)])
 def test_deterministic(causal, kernel):
     q, k, v, _ = _inputs(2, 4, 1000, 1000, 128, seed=13)
     dev = torch.device("cuda:0")
@@ -225,7 +220,8 @@ WAIT_SITES = set(range(1, 14)) - {8, 12}
 
 
 @pytest.mark.parametrize("D,causal,kernel,skip", [(128, False, 1, 5), (128, False, 0, 5), (128, True, 0, 0),
-                                                  (64, False, 1, 3), (64, False, 0, 2), (64, True, 0, 10)])
+                                                  (128, True, 1, 2), (64, False, 1, 3), (64, False, 0, 2),
+                                                  (64, True, 0, 10), (64, True, 1, 4)])
 def test_forward_kernel_gives_up_drains_and_recovers(D, causal, kernel, skip):
     """The attention kernel's own give-up path: block 0's producer leaves out
     one K fill, so a bounded wait (1 ms) in block 0 runs out; every role of
