@@ -57,6 +57,11 @@ SIGNATURES = {
                                        ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_float,
                                        ctypes.c_float, ctypes.c_float, ctypes.c_int, ctypes.c_void_p]),
+    "attn_fwd_fp8_variant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                            ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_void_p,
+                                            ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_void_p]),
     "attn_fwd_varlen": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
@@ -141,6 +146,13 @@ def attn_fwd_fp8(q: int, k: int, v_t: int, o: int, lse: int, B: int, H: int, Sq:
                  v_descale: float, stream: Optional[int]) -> int:
     return lib().attn_fwd_fp8(q, k, v_t, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, q_descale, k_descale,
                               v_descale, stream)
+
+
+def attn_fwd_fp8_variant(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
+                         scale: float, causal: int, kv_lens: Optional[int], q_descale: float, k_descale: float,
+                         v_descale: float, v_layout: int, kernel: int, stream: Optional[int]) -> int:
+    return lib().attn_fwd_fp8_variant(q, k, v, o, lse, B, H, Sq, Sk, D, scale, int(causal), kv_lens, q_descale,
+                                      k_descale, v_descale, v_layout, kernel, stream)
 
 
 def attn_fwd_fp8_ex(q: int, k: int, v: int, o: int, lse: int, B: int, H: int, Sq: int, Sk: int, D: int,
@@ -327,13 +339,13 @@ def forward_splitkv(q, k, v, num_splits: Optional[int] = None, scale: Optional[f
 
 def forward_fp8(q8, k8, v8, q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0,
                 scale: Optional[float] = None, causal: bool = False, kv_lens=None, out=None, lse=None,
-                v_layout: int = ATTN_V_TRANSPOSED):
+                v_layout: int = ATTN_V_TRANSPOSED, kernel: int = ATTN_KERNEL_AUTO):
     """FP8 forward on torch CUDA tensors of E4M3 codes (``torch.uint8`` or
     ``torch.float8_e4m3fn``): ``q8 [B,H,Sq,D]``, ``k8 [B,H,Sk,D]`` and ``v8``,
     which is ``[B,H,D,Sk]`` (V transposed) with ``v_layout=ATTN_V_TRANSPOSED``
-    (the default) or ``[B,H,Sk,D]`` with ``v_layout=ATTN_V_ROWS``.  Returns
-    ``(o bf16 [B,H,Sq,D], lse fp32 [B,H,Sq])``, written into ``out`` / ``lse``
-    when given."""
+    (the default) or ``[B,H,Sk,D]`` with ``v_layout=ATTN_V_ROWS``.  ``kernel``
+    as for ``forward``.  Returns ``(o bf16 [B,H,Sq,D], lse fp32 [B,H,Sq])``,
+    written into ``out`` / ``lse`` when given."""
     import torch
 
     for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
@@ -351,10 +363,10 @@ def forward_fp8(q8, k8, v8, q_descale: float = 1.0, k_descale: float = 1.0, v_de
     out, lse = _outputs(out, lse, (B, H, Sq, D), (B, H, Sq), q8.device)
     with torch.cuda.device(q8.device):
         stream = torch.cuda.current_stream(q8.device).cuda_stream
-        st = attn_fwd_fp8_ex(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H,
-                             Sq, Sk, D, float(scale), int(bool(causal)),
-                             None if kv_lens is None else kv_lens.data_ptr(), float(q_descale), float(k_descale),
-                             float(v_descale), int(v_layout), stream)
+        st = attn_fwd_fp8_variant(q8.data_ptr(), k8.data_ptr(), v8.data_ptr(), out.data_ptr(), lse.data_ptr(), B,
+                                  H, Sq, Sk, D, float(scale), int(bool(causal)),
+                                  None if kv_lens is None else kv_lens.data_ptr(), float(q_descale),
+                                  float(k_descale), float(v_descale), int(v_layout), int(kernel), stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_fp8")
     return out, lse

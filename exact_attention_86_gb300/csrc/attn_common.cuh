@@ -114,6 +114,16 @@ struct Params {
 };
 
 
+// Lazy rescale threshold (log2 units) and the shift of P (log2 units): each P
+// term is 2^(x - m + shift) <= 2^(tau + shift).  bf16 P: tau 16, shift 0.
+// E4M3 P (largest finite value 448): tau 4.5, shift 4, so terms stay <= 2^8.5
+// and terms down to 2^-13 of the reference keep a nonzero code.
+template <bool FP8>
+struct Prec {
+  static constexpr float kTau = FP8 ? 4.5f : 16.0f;
+  static constexpr float kShift = FP8 ? 4.0f : 0.0f;
+  static constexpr float kSumLimit = FP8 ? 362.03867196751236f : 65536.0f;  // 2^(kTau + kShift)
+};
 // ---------------------------------------------------------------- host side
 
 inline FastDiv make_fastdiv(int divisor) {

@@ -52,16 +52,6 @@ using namespace attn_sm103;
 
 namespace {
 
-// Lazy rescale threshold (log2 units) and the shift of P (log2 units): each P
-// term is 2^(x - m + shift) <= 2^(tau + shift).  bf16 P: tau 16, shift 0.
-// E4M3 P (largest finite value 448): tau 4.5, shift 4, so terms stay <= 2^8.5
-// and terms down to 2^-13 of the reference keep a nonzero code.
-template <bool FP8>
-struct Prec {
-  static constexpr float kTau = FP8 ? 4.5f : 16.0f;
-  static constexpr float kShift = FP8 ? 4.0f : 0.0f;
-  static constexpr float kSumLimit = FP8 ? 362.03867196751236f : 65536.0f;  // 2^(kTau + kShift)
-};
 // Fixed split-KV scratch of attn_fwd_splitkv_noalloc: a static device array,
 // instantiated once in every device context that loads the library, so that
 // entry point needs neither an allocation nor a caller workspace.
@@ -1420,7 +1410,7 @@ attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const voi
     const uint64_t n_pairs = (static_cast<uint64_t>(Sq) + 2 * kBQ - 1) / (2 * kBQ);
     pp.n_qtiles = static_cast<int>(n_pairs);
     pp.total_units = static_cast<int>(static_cast<uint64_t>(B) * H * n_pairs);
-    return attn_pair_host::launch(D, causal != 0, dev.num_sms, mq, mk, mv, pp, s);
+    return attn_pair_host::launch(D, causal != 0, false, dev.num_sms, mq, mk, mv, pp, s);
   }
 #endif
   if (D == 64) {
@@ -1459,10 +1449,12 @@ attn_status attn_fwd_variant(const void* q, const void* k, const void* v, void* 
                      reinterpret_cast<cudaStream_t>(stream), kernel);
 }
 
-attn_status attn_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
-                            int Sk, int D, float scale, int causal, const int32_t* kv_lens, float q_descale,
-                            float k_descale, float v_descale, int v_layout, attn_stream_t stream) {
+attn_status attn_fwd_fp8_variant(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                 int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens,
+                                 float q_descale, float k_descale, float v_descale, int v_layout, int kernel,
+                                 attn_stream_t stream) {
   if (v_layout != ATTN_V_ROWS && v_layout != ATTN_V_TRANSPOSED) return ATTN_ERR_SHAPE;
+  if (kernel < ATTN_KERNEL_AUTO || kernel > ATTN_KERNEL_TWO_TILE) return ATTN_ERR_SHAPE;
   const bool v_rows = v_layout == ATTN_V_ROWS;
   const void* v_t = v;
   if (B < 0 || H < 0 || Sq < 0 || Sk < 0) return ATTN_ERR_SHAPE;
@@ -1523,9 +1515,28 @@ attn_status attn_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o
   p.v_rows = v_rows ? 1 : 0;
   p.wait_limit_ns = kWaitLimitNs;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // E4M3 takes the one-tile kernel unless the caller forces the other: with
+  // half-time products its double-buffered scores matter more than the
+  // two-tile kernel's shared K/V tiles (measured on the S = 8192 workloads:
+  // 1416 against 1025 TFLOP/s, causal 1335 against 1016)
+  if (kernel == ATTN_KERNEL_TWO_TILE) {
+    // units of two query tiles (attn_fwd_pair_kernel)
+    Params pp = p;
+    const uint64_t n_pairs = (static_cast<uint64_t>(Sq) + 2 * kBQ - 1) / (2 * kBQ);
+    pp.n_qtiles = static_cast<int>(n_pairs);
+    pp.total_units = static_cast<int>(static_cast<uint64_t>(B) * H * n_pairs);
+    return attn_pair_host::launch(D, causal != 0, true, dev->num_sms, mq, mk, mv, pp, s);
+  }
   if (D == 64)
     return causal ? launch<64, true, true>(*dev, 12, mq, mk, mv, p, s) : launch<64, false, true>(*dev, 13, mq, mk, mv, p, s);
   return causal ? launch<128, true, true>(*dev, 4, mq, mk, mv, p, s) : launch<128, false, true>(*dev, 5, mq, mk, mv, p, s);
+}
+
+attn_status attn_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Sq,
+                            int Sk, int D, float scale, int causal, const int32_t* kv_lens, float q_descale,
+                            float k_descale, float v_descale, int v_layout, attn_stream_t stream) {
+  return attn_fwd_fp8_variant(q, k, v, o, lse, B, H, Sq, Sk, D, scale, causal, kv_lens, q_descale, k_descale,
+                              v_descale, v_layout, ATTN_KERNEL_AUTO, stream);
 }
 
 attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o, float* lse, int B, int H, int Sq,

@@ -53,18 +53,33 @@ using namespace attn_sm103;
 
 namespace {
 
-template <int D>
+template <int D, bool FP8>
 struct GeoPair {
   static_assert(D == 64 || D == 128, "head dim");
-  static constexpr int kTileBytes = 128 * D * 2;      // one Q, K or V tile (128 rows of bf16)
-  static constexpr int kChunkBytes = 128 * 128;       // 128 rows x 128 B (one 128-B swizzle column)
-  static constexpr int kChunks = D / 64;
-  static constexpr int kKSteps = D / 16;              // QK^T instructions (16 columns of D each)
+  static constexpr int kElem = FP8 ? 1 : 2;           // bytes per element of Q, K, V
+  static constexpr int kRowBytes = D * kElem;         // one row of a Q or K tile (and of V in rows)
+  static constexpr int kTileBytes = 128 * kRowBytes;  // one Q, K or V tile (128 rows)
+  // Rows of 128 bytes (bf16 D = 64, E4M3 D = 128) or 256 bytes (bf16 D =
+  // 128, two 64-column chunks) use the 128-byte swizzle; the 64-byte rows of
+  // E4M3 at D = 64 the 64-byte swizzle (8-row atoms of 64 bytes, 512 apart).
+  static constexpr bool kSw64 = kRowBytes == 64;
+  static constexpr int kChunkBytes = kSw64 ? 128 * 64 : 128 * 128;  // 128 rows of one swizzle column
+  static constexpr int kChunks = kSw64 ? 1 : kRowBytes / 128;
+  static constexpr int kChunkElems = kSw64 ? 64 : 128 / kElem;      // elements per row of a chunk
+  static constexpr uint32_t kSwMode = kSw64 ? kSmemSwizzle64B : kSmemSwizzle128B;
+  static constexpr uint32_t kSbo = kSw64 ? 512 : 1024;               // 8-row groups of a chunk
+  static constexpr int kKSteps = kRowBytes / 32;      // QK^T instructions: 32 bytes of D each
+  static constexpr int kPCols = 128 * kElem / 4;      // TMEM columns of one tile's P (128 keys)
   static constexpr int kOffQ = 1024;                  // after the control block
   static constexpr int kOffRing = kOffQ + 2 * kTileBytes;
-  // as many K/V slots as the 227 KB a block may use leave (D = 128: 5, D = 64: 12)
-  static constexpr int kSlots = (232448 - kOffRing) / kTileBytes;
-  static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes;
+  // E4M3 at D = 64 keeps an unused tile-sized pad after the ring, as the
+  // one-tile kernel does, so that no read of the last slot leaves the block
+  static constexpr int kPadBytes = kSw64 ? kTileBytes : 0;
+  // as many K/V slots as the 227 KB a block may use leave, at most 16 (bf16
+  // D = 128: 5, bf16 D = 64 and E4M3 D = 128: 12, E4M3 D = 64: 16)
+  static constexpr int kSlotsFit = (232448 - kOffRing - kPadBytes) / kTileBytes;
+  static constexpr int kSlots = kSlotsFit < 16 ? kSlotsFit : 16;
+  static constexpr int kSmemBytes = kOffRing + kSlots * kTileBytes + kPadBytes;
   static_assert(kSlots >= 2 && kSlots <= 16, "ring depth");
   static_assert(2 * kSmemBytes > 233472, "one block per SM (the TMEM allocation is the whole of it)");
   static constexpr uint32_t kTmemS = 0;               // + 128 * x
@@ -151,14 +166,17 @@ __device__ __forceinline__ UnitPair decode_pair(const Params& p, int t) {
   return u;
 }
 
-// p = 2^(s*c - mb) for a thread's 128 scores, packed to bf16 pairs IN PLACE
-// (pair e goes to sp[e], whose score was read at pair e / 2 <= e); masked
-// columns (>= climit) give 0.  Returns the fp32 sum of the unrounded terms.
-template <bool MASKED>
+// p = 2^(s*c - mb) for a thread's 128 scores, packed IN PLACE: bf16 pairs
+// (pair e to sp[e]) or, FP8, four E4M3 values a word (pairs 2 w and 2 w + 1
+// to sp[w]); each word goes to an index whose scores were already read.
+// Masked columns (>= climit) give 0.  Returns the fp32 sum of the unrounded
+// terms.
+template <bool MASKED, bool FP8>
 __device__ __forceinline__ float row_exp128(uint32_t (&sp)[128], float c, float mb, int climit) {
   const uint64_t c2 = f2_pack(c, c);
   const uint64_t nmb2 = f2_pack(-mb, -mb);
   uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+  float pprev0 = 0.0f, pprev1 = 0.0f;  // FP8: the previous pair, packed with the next
 #pragma unroll
   for (int e = 0; e < 64; ++e) {
     const int col = 2 * e;
@@ -171,7 +189,13 @@ __device__ __forceinline__ float row_exp128(uint32_t (&sp)[128], float c, float 
       p1 = (col + 1 < climit) ? p1 : 0.0f;
     }
     acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
-    sp[e] = pack_bf16x2(p0, p1);
+    if constexpr (FP8) {
+      if (e & 1) sp[e >> 1] = pack_e4m3x4(pprev0, pprev1, p0, p1);
+      pprev0 = p0;
+      pprev1 = p1;
+    } else {
+      sp[e] = pack_bf16x2(p0, p1);
+    }
   }
   const uint64_t a01 = f2_add(acc[0], acc[1]);
   const uint64_t a23 = f2_add(acc[2], acc[3]);
@@ -213,12 +237,13 @@ __device__ __forceinline__ void load_s128(uint32_t tS, uint32_t (&sp)[128]) {
   tmem_ld_wait_x32(d);
 }
 
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                          const __grid_constant__ CUtensorMap map_v, const Params p,
                          const __grid_constant__ UnitSched<CAUSAL> sched) {
-  using G = GeoPair<D>;
+  using G = GeoPair<D, FP8>;
+  using PR = Prec<FP8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t base = smem_addr(smem_raw);
   CtrlPair& ctl = *reinterpret_cast<CtrlPair*>(smem_raw);
@@ -338,8 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar_q_full, 2 * G::kTileBytes);
           for (int x = 0; x < 2; ++x)
             for (int c = 0; c < G::kChunks; ++c)
-              tma_load_4d_hint(base + G::kOffQ + x * G::kTileBytes + c * G::kChunkBytes, &map_q, bar_q_full, c * 64,
-                               u.q0 + kBQ * x, u.h, u.b, pol_once);
+              tma_load_4d_hint(base + G::kOffQ + x * G::kTileBytes + c * G::kChunkBytes, &map_q, bar_q_full,
+                               c * G::kChunkElems, u.q0 + kBQ * x, u.h, u.b, pol_once);
           ++qcount;
           for (int j = 0; ok && j < u.n_max; ++j) {
             for (int sel = 0; sel < 2; ++sel) {  // K_j, then V_j
@@ -356,8 +381,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(full, G::kTileBytes);
                 const CUtensorMap* m = sel ? &map_v : &map_k;
                 const uint32_t dst = base + G::kOffRing + f.slot * G::kTileBytes;
-                for (int c = 0; c < G::kChunks; ++c)
-                  tma_load_4d_hint(dst + c * G::kChunkBytes, m, full, c * 64, j * kBK, u.h, u.b, pol_keep);
+                if (FP8 && sel && !p.v_rows) {
+                  // E4M3 V given transposed, (Sk, D, H, B): the tile is D rows,
+                  // each 128 keys long (K-major for the P V product)
+                  tma_load_4d_hint(dst, m, full, j * kBK, 0, u.h, u.b, pol_keep);
+                } else {
+                  for (int c = 0; c < G::kChunks; ++c)
+                    tma_load_4d_hint(dst + c * G::kChunkBytes, m, full, c * G::kChunkElems, j * kBK, u.h, u.b,
+                                     pol_keep);
+                }
               }
               ++pos;
             }
@@ -412,8 +444,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < G::kKSteps; ++kk) {
               const uint32_t off = (kk >> 2) * G::kChunkBytes + (kk & 3) * 32;
-              mma_ss_elect(tmem + G::kTmemS + 128u * x, sdesc_sw128(qa + off, 16, 1024),
-                           sdesc_sw128(ka + off, 16, 1024), p.idesc_qk, kk > 0 ? 1u : 0u);
+              const uint64_t qdesc = sdesc_sw(qa + off, 16, G::kSbo, G::kSwMode);
+              const uint64_t kdesc = sdesc_sw(ka + off, 16, G::kSbo, G::kSwMode);
+              if constexpr (FP8)
+                mma_ss_f8_elect(tmem + G::kTmemS + 128u * x, qdesc, kdesc, p.idesc_qk, kk > 0 ? 1u : 0u);
+              else
+                mma_ss_elect(tmem + G::kTmemS + 128u * x, qdesc, kdesc, p.idesc_qk, kk > 0 ? 1u : 0u);
             }
             mma_commit_elect(bar_s_full0 + 8 * x);
             if (x == 0) {  // a plain arrive right after the issue
@@ -477,10 +513,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // chunks of D, SBO = 8 keys x 128 B)
             const uint32_t tO = tmem + G::kTmemO + static_cast<uint32_t>(D) * x;
             const uint32_t tP = tmem + G::kTmemS + 128u * x;
+            if constexpr (FP8) {
+              // E4M3 P (32 keys = 8 columns per MMA, four per column).  V
+              // transposed: K-major (D rows of 128 keys, 128-byte swizzle), 32
+              // keys = 32 bytes along each row per MMA.  V in rows: MN-major
+              // (rows of keys, D contiguous: one swizzle atom wide), 32 keys =
+              // 32 rows per MMA.
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_ts_elect(tO, tP + 8u * kk, sdesc_sw128(va + kk * 16 * 128, G::kChunkBytes, 1024), p.idesc_pv,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kBK / 32; ++kk) {
+                const uint64_t vdesc = p.v_rows ? sdesc_sw(va + kk * 32 * G::kRowBytes, 16, G::kSbo, G::kSwMode)
+                                                : sdesc_sw(va + kk * 32, 16, 1024, kSmemSwizzle128B);
+                mma_ts_f8_elect(tO, tP + 8u * kk, vdesc, p.idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < kBK / 16; ++kk)
+                mma_ts_elect(tO, tP + 8u * kk, sdesc_sw128(va + kk * 16 * 128, G::kChunkBytes, 1024), p.idesc_pv,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+            }
             mma_commit_elect(bar_p_free0 + 8 * x);
             ++pc[x];
             if (j == u.n[x] - 1) mma_commit_elect(bar_o_full0 + 8 * x);
@@ -557,8 +607,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sum = 0.0f;
         bool suspect = true;  // the first tile always takes its exact max
         if (j > 0) {
-          sum = masked ? row_exp128<true>(sp, c, m_used, climit) : row_exp128<false>(sp, c, m_used, climit);
-          suspect = !(sum <= 65536.0f);
+          // each term 2^(x - m_used + shift); a sum <= 2^(tau + shift) proves
+          // that no score of the row grew past the reference by more than tau
+          // (also false for NaN / inf)
+          sum = masked ? row_exp128<true, FP8>(sp, c, m_used - PR::kShift, climit)
+                       : row_exp128<false, FP8>(sp, c, m_used - PR::kShift, climit);
+          suspect = !(sum <= PR::kSumLimit);
         }
         // (warp-uniform decisions: the TMEM loads and stores below are
         // warp-wide instructions)
@@ -566,12 +620,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j > 0) load_s128(tS, sp);  // the raw scores again (P is not stored yet)
           const float mx = masked ? row_max128<true>(sp, climit) : row_max128<false>(sp, climit);
           const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
-          bool grow = (j == 0) || m_tile > m_used + 16.0f;
+          bool grow = (j == 0) || m_tile > m_used + PR::kTau;
           float alpha = 1.0f;
           if (grow && j > 0) alpha = ex2_approx(m_used - m_tile);
           if (grow) m_used = m_tile;
-          const float mb = (m_used == -INFINITY) ? 0.0f : m_used;
-          sum = masked ? row_exp128<true>(sp, c, mb, climit) : row_exp128<false>(sp, c, mb, climit);
+          const float mb = (m_used == -INFINITY) ? 0.0f : m_used - PR::kShift;
+          sum = masked ? row_exp128<true, FP8>(sp, c, mb, climit) : row_exp128<false, FP8>(sp, c, mb, climit);
           if (j > 0 && __any_sync(0xffffffffu, grow)) {
             // O_x holds the products of the tiles before (all completed: this
             // S_x was written after the last of them): rescale this row
@@ -593,9 +647,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        // P over the first 64 columns of S_x (their scores are in registers)
+        // P over the first columns of S_x (their scores are in registers):
+        // 64 columns of bf16 pairs, or 32 of four E4M3 values
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < G::kPCols / 16; ++q)
           tmem_st_32x32b_x16(tS + 16 * q, *reinterpret_cast<const uint32_t(*)[16]>(&sp[16 * q]));
         tmem_st_wait();
         warp_arrive_after_tc(bar_p_full, lane);
@@ -607,8 +662,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++oc;
       tc_fence_after_sync();
       const bool has_key = l > 0.0f;
-      const float inv_l = has_key ? rcp_approx(l) : 0.0f;
-      const float lse_row = has_key ? (m_used + lg2_approx(l)) * kLn2 : -INFINITY;
+      const float inv_l = has_key ? p.v_scale * rcp_approx(l) : 0.0f;  // (v_scale: 1, or the E4M3 V descale)
+      const float lse_row = has_key ? (m_used - PR::kShift + lg2_approx(l)) * kLn2 : -INFINITY;
 #pragma unroll
       for (int q = 0; q < D / 32; ++q) {
         uint32_t o[32];
@@ -649,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // dynamic shared memory attribute set, per device and instantiation
 constexpr int kMaxDevicesPair = 64;
-std::atomic<bool> g_pair_smem_set[kMaxDevicesPair][4];
+std::atomic<bool> g_pair_smem_set[kMaxDevicesPair][8];
 
 // Cost model of a unit, in hundredths of the time one 128-key tile takes the
 // one-tile kernel: a key tile that both query tiles of a pair process costs
@@ -717,11 +772,12 @@ bool causal_schedule(const Params& p, int grid, UnitSched<true>& out) {
   return true;
 }
 
-template <int D, bool CAUSAL>
-attn_status launch_pair(int dev, int idx, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk,
-                        const CUtensorMap& mv, const Params& p0, cudaStream_t stream) {
-  auto kern = attn_fwd_pair_kernel<D, CAUSAL>;
-  constexpr int smem = GeoPair<D>::kSmemBytes;
+template <int D, bool CAUSAL, bool FP8>
+attn_status launch_pair(int dev, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                        const Params& p0, cudaStream_t stream) {
+  auto kern = attn_fwd_pair_kernel<D, CAUSAL, FP8>;
+  constexpr int smem = GeoPair<D, FP8>::kSmemBytes;
+  constexpr int idx = (D == 64 ? 0 : 4) + (CAUSAL ? 2 : 0) + (FP8 ? 1 : 0);
   if (dev < 0 || dev >= kMaxDevicesPair) return ATTN_ERR_UNSUPPORTED_DEVICE;
   if (!g_pair_smem_set[dev][idx].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -800,15 +856,22 @@ int64_t build_schedule(int B, int H, int Sq, int Sk, int head_group, int grid, u
   return n;
 }
 
-attn_status launch(int D, bool causal, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk,
+attn_status launch(int D, bool causal, bool fp8, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk,
                    const CUtensorMap& mv, const attn_detail::Params& p, cudaStream_t s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (fp8) {
+    if (causal)
+      return D == 64 ? launch_pair<64, true, true>(dev, num_sms, mq, mk, mv, p, s)
+                     : launch_pair<128, true, true>(dev, num_sms, mq, mk, mv, p, s);
+    return D == 64 ? launch_pair<64, false, true>(dev, num_sms, mq, mk, mv, p, s)
+                   : launch_pair<128, false, true>(dev, num_sms, mq, mk, mv, p, s);
+  }
   if (causal)
-    return D == 64 ? launch_pair<64, true>(dev, 0, num_sms, mq, mk, mv, p, s)
-                   : launch_pair<128, true>(dev, 2, num_sms, mq, mk, mv, p, s);
-  return D == 64 ? launch_pair<64, false>(dev, 1, num_sms, mq, mk, mv, p, s)
-                 : launch_pair<128, false>(dev, 3, num_sms, mq, mk, mv, p, s);
+    return D == 64 ? launch_pair<64, true, false>(dev, num_sms, mq, mk, mv, p, s)
+                   : launch_pair<128, true, false>(dev, num_sms, mq, mk, mv, p, s);
+  return D == 64 ? launch_pair<64, false, false>(dev, num_sms, mq, mk, mv, p, s)
+                 : launch_pair<128, false, false>(dev, num_sms, mq, mk, mv, p, s);
 }
 
 attn_status status_read_clear(uint32_t host[3]) {

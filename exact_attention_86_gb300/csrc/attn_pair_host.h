@@ -24,10 +24,11 @@ bool use_pair(int B, int H, int Sq, int Sk, bool causal, int num_sms);
 
 // Launches the padded forward over units of two 128-row query tiles
 // (p.n_qtiles = tile pairs per head, p.total_units = B * H * pairs; every
-// other field as for attn_fwd_kernel, without key ranges) on `stream`, with
-// one block per SM up to the number of units.  Causal batches get a static
-// longest-first deal of their units (see build_schedule).
-attn_status launch(int D, bool causal, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk,
+// other field as for attn_fwd_kernel, without key ranges; fp8: E4M3 inputs,
+// with the tensor maps, descriptors and descales attn_fwd_fp8_ex builds) on
+// `stream`, with one block per SM up to the number of units.  Causal batches
+// get a static longest-first deal of their units (see build_schedule).
+attn_status launch(int D, bool causal, bool fp8, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk,
                    const CUtensorMap& mv, const attn_detail::Params& p, cudaStream_t stream);
 
 // The static deal of a causal batch's pair units to `grid` blocks, in the

@@ -151,6 +151,20 @@ attn_status attn_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o
                             float k_descale, float v_descale, int v_layout, attn_stream_t stream);
 
 /*
+ * attn_fwd_fp8_variant — attn_fwd_fp8_ex with the kernel chosen by the
+ * caller: `kernel` as in attn_fwd_variant (ATTN_KERNEL_AUTO: the kernel
+ * attn_fwd_fp8_ex runs, always the one-tile kernel for E4M3, measured faster
+ * there; ATTN_KERNEL_ONE_TILE or ATTN_KERNEL_TWO_TILE forced).  Both compute the same function within the
+ * E4M3 forward's tolerance; they are not bit-identical to each other (their
+ * row sums split differently over threads).  Any other `kernel`:
+ * ATTN_ERR_SHAPE.  Everything else as attn_fwd_fp8_ex.
+ */
+attn_status attn_fwd_fp8_variant(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                                 int Sq, int Sk, int D, float scale, int causal, const int32_t* kv_lens,
+                                 float q_descale, float k_descale, float v_descale, int v_layout, int kernel,
+                                 attn_stream_t stream);
+
+/*
  * attn_fwd_varlen — the same forward over a packed batch of variable-length
  * sequences (the ragged tensors of continuous batching, "Fused Multi-Head
  * Attention", section on continuous batching): no padding is stored or read.
@@ -394,7 +408,7 @@ attn_status attn_selftest_fwd_abort(const void* q, const void* k, const void* v,
 attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t stream);
 
 /*
- * attn_fwd_kernel_choice — which kernel attn_fwd runs for a padded batch of
+ * attn_fwd_kernel_choice — which kernel attn_fwd runs for a padded bf16 batch of
  * B x H heads of Sq queries and Sk keys, causal or not, on a device with
  * `num_sms` SMs.  Returns 1 for the two-query-tile kernel (units of 256 query
  * rows), 0 for the one-tile kernel (units of 128 rows), -1 for a negative
@@ -424,7 +438,7 @@ int64_t attn_fwd_pair_schedule(int B, int H, int Sq, int Sk, int head_group, int
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 13
+#define ATTN_ABI_VERSION 14
 
 #ifdef __cplusplus
 }

@@ -349,3 +349,16 @@ def test_fp8_ex_argument_checks(lib):
     assert f(A, A, A, A, A, 1, 2, 256, 100, 128, 0.1, 0, None, 1.0, 1.0, 1.0, 1, None) == attn.ATTN_ERR_SHAPE
     assert f(*args, 128, float("nan"), 0, None, 1.0, 1.0, 1.0, 0, None) == attn.ATTN_ERR_SCALE
     assert f(A + 8, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, 1.0, 1.0, 1.0, 0, None) == attn.ATTN_ERR_ALIGN
+
+
+def test_fp8_variant_argument_checks(lib):
+    # each call ends at a host-side check (no device query, no launch)
+    f = attn.attn_fwd_fp8_variant
+    args = (A, A, A, A, A, 1, 2, 256, 256, 128, 0.1, 0, None, 1.0, 1.0, 1.0)
+    assert f(*args, attn.ATTN_V_ROWS, 2, None) == attn.ATTN_ERR_SHAPE                   # unknown kernel
+    assert f(*args, attn.ATTN_V_ROWS, -2, None) == attn.ATTN_ERR_SHAPE
+    assert f(*args, 5, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_SHAPE         # unknown layout
+    assert f(A, A, A, A, A, 1, 2, 256, 256, 96, 0.1, 0, None, 1.0, 1.0, 1.0, attn.ATTN_V_ROWS,
+             attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_UNSUPPORTED_D
+    assert f(A, A, A, A, A, 0, 2, 256, 256, 128, 0.1, 0, None, 1.0, 1.0, 1.0, attn.ATTN_V_ROWS,
+             attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_OK                             # nothing to compute

@@ -50,9 +50,13 @@ def _inputs(B, H, Sq, Sk, seed, std=1.0, D=128):
 
 ROWS, TRANSPOSED = attn.ATTN_V_ROWS, attn.ATTN_V_TRANSPOSED
 LAYOUTS = pytest.mark.parametrize("layout", [ROWS, TRANSPOSED], ids=["v_rows", "v_transposed"])
+# both padded-forward kernels (small batches take the one-tile kernel unless forced)
+KERNELS = pytest.mark.parametrize("kernel", [attn.ATTN_KERNEL_ONE_TILE, attn.ATTN_KERNEL_TWO_TILE],
+                                  ids=["one", "two"])
 
 
-def _run(q, k, v, scale, causal=False, kv=None, qd=1.0, kd=1.0, vd=1.0, layout=TRANSPOSED):
+def _run(q, k, v, scale, causal=False, kv=None, qd=1.0, kd=1.0, vd=1.0, layout=TRANSPOSED,
+         kernel=attn.ATTN_KERNEL_AUTO):
     """The E4M3 forward with V in the given layout, into NaN-filled outputs."""
     dev = torch.device("cuda:0")
     vl = v if layout == ROWS else v.transpose(-1, -2).contiguous()
@@ -61,7 +65,7 @@ def _run(q, k, v, scale, causal=False, kv=None, qd=1.0, kd=1.0, vd=1.0, layout=T
     lse = nan_filled((B, H, Sq), torch.float32, dev)
     attn.forward_fp8(q.to(dev), k.to(dev), vl.to(dev), qd, kd, vd, scale=scale, causal=causal,
                      kv_lens=None if kv is None else torch.tensor(kv, dtype=torch.int32, device=dev), out=o, lse=lse,
-                     v_layout=layout)
+                     v_layout=layout, kernel=kernel)
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
     assert_no_nan(o, lse, what="fp8")
@@ -108,83 +112,90 @@ SHAPES = [
 ]
 
 
+@KERNELS
 @LAYOUTS
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("shape", SHAPES)
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_matches_oracle(shape, causal, layout, D):
+def test_fp8_matches_oracle(shape, causal, layout, D, kernel):
     B, H, Sq, Sk = shape
     q, k, v = _inputs(B, H, Sq, Sk, seed=Sq + Sk + int(causal) + D, D=D)
     scale = 1.0 / math.sqrt(D)
-    o, lse = _run(q, k, v, scale, causal, layout=layout)
+    o, lse = _run(q, k, v, scale, causal, layout=layout, kernel=kernel)
     o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, scale, causal)
     check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax,
               f"fp8 {shape} causal={causal} layout={layout}")
 
 
+@KERNELS
 @LAYOUTS
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("kv", [[0, 1], [16, 143], [128, 129], [255, 256]])
-def test_fp8_key_lengths(kv, layout, D):
+def test_fp8_key_lengths(kv, layout, D, kernel):
     q, k, v = _inputs(2, 2, 200, 256, seed=sum(kv) + D, D=D)
-    o, lse = _run(q, k, v, 0.09, kv=kv, layout=layout)
+    o, lse = _run(q, k, v, 0.09, kv=kv, layout=layout, kernel=kernel)
     o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, 0.09, kv=kv)
     check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax, f"fp8 kv={kv} layout={layout}")
 
 
+@KERNELS
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("shape", [(1, 1, 1, 1), (1, 2, 100, 100), (2, 1, 300, 333), (1, 2, 129, 1000)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_v_rows_any_key_count(shape, causal, D):
+def test_fp8_v_rows_any_key_count(shape, causal, D, kernel):
     """V in rows has no key-count restriction (the transposed layout needs a
     multiple of 16): ragged key counts against the oracle."""
     B, H, Sq, Sk = shape
     q, k, v = _inputs(B, H, Sq, Sk, seed=Sq * 3 + Sk + int(causal) + D, D=D)
     scale = 1.0 / math.sqrt(D)
-    o, lse = _run(q, k, v, scale, causal, layout=ROWS)
+    o, lse = _run(q, k, v, scale, causal, layout=ROWS, kernel=kernel)
     o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, scale, causal)
     check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax, f"fp8 rows {shape}")
 
 
+@KERNELS
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("shape", [(1, 2, 100, 144), (2, 2, 300, 1024), (1, 4, 1000, 2048)])
 @pytest.mark.parametrize("causal", [False, True])
-def test_fp8_v_layouts_bitwise_identical(shape, causal, D):
+def test_fp8_v_layouts_bitwise_identical(shape, causal, D, kernel):
     """The two V layouts feed the products the same values in the same order:
-    identical bits."""
+    identical bits (on either kernel)."""
     B, H, Sq, Sk = shape
     q, k, v = _inputs(B, H, Sq, Sk, seed=Sq + 7 * Sk + int(causal), std=2.0, D=D)
-    o_r, l_r = _run(q, k, v, 0.07, causal, layout=ROWS)
-    o_t, l_t = _run(q, k, v, 0.07, causal, layout=TRANSPOSED)
+    o_r, l_r = _run(q, k, v, 0.07, causal, layout=ROWS, kernel=kernel)
+    o_t, l_t = _run(q, k, v, 0.07, causal, layout=TRANSPOSED, kernel=kernel)
     assert torch.equal(o_r.view(torch.int16), o_t.view(torch.int16))
     assert torch.equal(l_r.view(torch.int32), l_t.view(torch.int32))
 
 
-def test_fp8_descales_and_large_scores():
+@KERNELS
+def test_fp8_descales_and_large_scores(kernel):
     # std 4 inputs (scores std about 16 after scaling by q and k descales) move the max often
     q, k, v = _inputs(1, 2, 256, 512, seed=41, std=4.0)
     for layout in (ROWS, TRANSPOSED):
-        o, lse = _run(q, k, v, 0.05, qd=0.5, kd=2.0, vd=0.25, layout=layout)
+        o, lse = _run(q, k, v, 0.05, qd=0.5, kd=2.0, vd=0.25, layout=layout, kernel=kernel)
         o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, 0.05, qd=0.5, kd=2.0, vd=0.25)
         check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax, f"fp8 descales {layout}")
 
 
-def test_fp8_descale_laws_bitwise():
+@KERNELS
+def test_fp8_descale_laws_bitwise(kernel):
     q, k, v = _inputs(1, 2, 256, 512, seed=43)
-    o1, l1 = _run(q, k, v, 0.1)
-    o2, l2 = _run(q, k, v, 0.1, vd=2.0)          # V descale: O doubles exactly, LSE unchanged
+    o1, l1 = _run(q, k, v, 0.1, kernel=kernel)
+    o2, l2 = _run(q, k, v, 0.1, vd=2.0, kernel=kernel)  # V descale: O doubles exactly, LSE unchanged
     assert torch.equal(o2.view(torch.int16), (2 * o1).view(torch.int16))
     assert torch.equal(l2, l1)
-    o3, l3 = _run(q, k, v, 0.05, qd=2.0)         # only scale * q_descale * k_descale matters
-    o4, l4 = _run(q, k, v, 0.2, kd=0.5)
+    o3, l3 = _run(q, k, v, 0.05, qd=2.0, kernel=kernel)  # only scale * q_descale * k_descale matters
+    o4, l4 = _run(q, k, v, 0.2, kd=0.5, kernel=kernel)
     for o, l in ((o3, l3), (o4, l4)):
         assert torch.equal(o.view(torch.int16), o1.view(torch.int16))
         assert torch.equal(l, l1)
 
 
-def test_fp8_negative_scale():
+@KERNELS
+def test_fp8_negative_scale(kernel):
     q, k, v = _inputs(1, 1, 130, 160, seed=47)
-    o, lse = _run(q, k, v, -0.1)
+    o, lse = _run(q, k, v, -0.1, kernel=kernel)
     o_ref, l_ref, a_ref, vmax = _oracle(q, k, v, -0.1)
     check_fp8(o.float().cpu().numpy(), lse.cpu().numpy(), o_ref, l_ref, a_ref, vmax, "fp8 negative scale")
 
