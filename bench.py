@@ -281,11 +281,11 @@ def is_fp8(w) -> bool:
 
 def forward_kernel(w, splits: int, num_sms: int) -> str:
     """The kernel that does the forward's work for this workload, as the
-    library chooses it: padded bf16 batches without key ranges may run the
-    two-query-tile kernel (attn_fwd_kernel_choice), every other mode (E4M3,
-    packed, paged, split) the one-tile kernel."""
+    library chooses it: padded batches (bf16 or E4M3) without key ranges may
+    run the two-query-tile kernel (attn_fwd_kernel_choice), packed, paged and
+    split batches the one-tile kernel."""
     from exact_attention_86_gb300 import attn
-    if not is_varlen(w) and not is_fp8(w) and splits == 0:
+    if not is_varlen(w) and splits == 0:
         if attn.attn_fwd_kernel_choice(w.B, w.H, w.Sq, w.Sk, int(w.causal), num_sms) == 1:
             return "attn_fwd_pair_kernel"
     return "attn_fwd_kernel"

@@ -1515,12 +1515,9 @@ attn_status attn_fwd_fp8_variant(const void* q, const void* k, const void* v, vo
   p.v_rows = v_rows ? 1 : 0;
   p.wait_limit_ns = kWaitLimitNs;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // E4M3 takes the one-tile kernel unless the caller forces the other: with
-  // half-time products its double-buffered scores matter more than the
-  // two-tile kernel's shared K/V tiles (measured on the S = 8192 workloads:
-  // 1416 against 1025 TFLOP/s, causal 1335 against 1016)
-  if (kernel == ATTN_KERNEL_TWO_TILE) {
-    // units of two query tiles (attn_fwd_pair_kernel)
+  if (kernel == ATTN_KERNEL_TWO_TILE ||
+      (kernel == ATTN_KERNEL_AUTO && attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, dev->num_sms))) {
+    // units of two query tiles (attn_fwd_pair_kernel), chosen as for bf16
     Params pp = p;
     const uint64_t n_pairs = (static_cast<uint64_t>(Sq) + 2 * kBQ - 1) / (2 * kBQ);
     pp.n_qtiles = static_cast<int>(n_pairs);

@@ -170,12 +170,16 @@ __device__ __forceinline__ UnitPair decode_pair(const Params& p, int t) {
 // (pair e to sp[e]) or, FP8, four E4M3 values a word (pairs 2 w and 2 w + 1
 // to sp[w]); each word goes to an index whose scores were already read.
 // Masked columns (>= climit) give 0.  Returns the fp32 sum of the unrounded
-// terms.
+// terms, and in part_max the quantity the caller's growth test bounds: for
+// FP8 the largest of the four 32-column partial sums (a term above the bound
+// puts its part's sum above it; over a whole row of 128 terms the sum of
+// ordinary terms crossed the E4M3 bound, 2^8.5, on most tiles), for bf16
+// (bound 2^16) the sum itself.
 template <bool MASKED, bool FP8>
-__device__ __forceinline__ float row_exp128(uint32_t (&sp)[128], float c, float mb, int climit) {
+__device__ __forceinline__ float row_exp128(uint32_t (&sp)[128], float c, float mb, int climit, float& part_max) {
   const uint64_t c2 = f2_pack(c, c);
   const uint64_t nmb2 = f2_pack(-mb, -mb);
-  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+  uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};  // FP8: one per 32 columns; bf16: interleaved
   float pprev0 = 0.0f, pprev1 = 0.0f;  // FP8: the previous pair, packed with the next
 #pragma unroll
   for (int e = 0; e < 64; ++e) {
@@ -188,7 +192,8 @@ __device__ __forceinline__ float row_exp128(uint32_t (&sp)[128], float c, float 
       p0 = (col < climit) ? p0 : 0.0f;
       p1 = (col + 1 < climit) ? p1 : 0.0f;
     }
-    acc[e & 3] = f2_add(acc[e & 3], f2_pack(p0, p1));
+    const int a = FP8 ? (e >> 4) : (e & 3);
+    acc[a] = f2_add(acc[a], f2_pack(p0, p1));
     if constexpr (FP8) {
       if (e & 1) sp[e >> 1] = pack_e4m3x4(pprev0, pprev1, p0, p1);
       pprev0 = p0;
@@ -197,11 +202,28 @@ __device__ __forceinline__ float row_exp128(uint32_t (&sp)[128], float c, float 
       sp[e] = pack_bf16x2(p0, p1);
     }
   }
-  const uint64_t a01 = f2_add(acc[0], acc[1]);
-  const uint64_t a23 = f2_add(acc[2], acc[3]);
-  float lo, hi;
-  f2_unpack(f2_add(a01, a23), lo, hi);
-  return lo + hi;
+  if constexpr (FP8) {
+    float part[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float lo, hi;
+      f2_unpack(acc[q], lo, hi);
+      part[q] = lo + hi;
+    }
+    // (a NaN part must reach part_max, so that the caller's test fails as
+    // it would on the sum: fmaxf would drop it)
+    part_max = part[0];
+#pragma unroll
+    for (int q = 1; q < 4; ++q) part_max = (part[q] > part_max || part[q] != part[q]) ? part[q] : part_max;
+    return (part[0] + part[1]) + (part[2] + part[3]);
+  } else {
+    const uint64_t a01 = f2_add(acc[0], acc[1]);
+    const uint64_t a23 = f2_add(acc[2], acc[3]);
+    float lo, hi;
+    f2_unpack(f2_add(a01, a23), lo, hi);
+    part_max = lo + hi;
+    return part_max;
+  }
 }
 
 // Maximum of a thread's 128 raw scores (columns >= climit excluded when MASKED).
@@ -607,12 +629,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sum = 0.0f;
         bool suspect = true;  // the first tile always takes its exact max
         if (j > 0) {
-          // each term 2^(x - m_used + shift); a sum <= 2^(tau + shift) proves
-          // that no score of the row grew past the reference by more than tau
-          // (also false for NaN / inf)
-          sum = masked ? row_exp128<true, FP8>(sp, c, m_used - PR::kShift, climit)
-                       : row_exp128<false, FP8>(sp, c, m_used - PR::kShift, climit);
-          suspect = !(sum <= PR::kSumLimit);
+          // each term 2^(x - m_used + shift); partial sums <= 2^(tau + shift)
+          // prove that no score of the row grew past the reference by more
+          // than tau (the test is also false for NaN / inf)
+          float part_max;
+          sum = masked ? row_exp128<true, FP8>(sp, c, m_used - PR::kShift, climit, part_max)
+                       : row_exp128<false, FP8>(sp, c, m_used - PR::kShift, climit, part_max);
+          suspect = !(part_max <= PR::kSumLimit);
         }
         // (warp-uniform decisions: the TMEM loads and stores below are
         // warp-wide instructions)
@@ -625,7 +648,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (grow && j > 0) alpha = ex2_approx(m_used - m_tile);
           if (grow) m_used = m_tile;
           const float mb = (m_used == -INFINITY) ? 0.0f : m_used - PR::kShift;
-          sum = masked ? row_exp128<true, FP8>(sp, c, mb, climit) : row_exp128<false, FP8>(sp, c, mb, climit);
+          float unused;
+          sum = masked ? row_exp128<true, FP8>(sp, c, mb, climit, unused)
+                       : row_exp128<false, FP8>(sp, c, mb, climit, unused);
           if (j > 0 && __any_sync(0xffffffffu, grow)) {
             // O_x holds the products of the tiles before (all completed: this
             // S_x was written after the last of them): rescale this row

@@ -153,8 +153,8 @@ attn_status attn_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o
 /*
  * attn_fwd_fp8_variant — attn_fwd_fp8_ex with the kernel chosen by the
  * caller: `kernel` as in attn_fwd_variant (ATTN_KERNEL_AUTO: the kernel
- * attn_fwd_fp8_ex runs, always the one-tile kernel for E4M3, measured faster
- * there; ATTN_KERNEL_ONE_TILE or ATTN_KERNEL_TWO_TILE forced).  Both compute the same function within the
+ * attn_fwd_fp8_ex runs, which attn_fwd_kernel_choice names; ATTN_KERNEL_ONE_TILE
+ * or ATTN_KERNEL_TWO_TILE forced).  Both compute the same function within the
  * E4M3 forward's tolerance; they are not bit-identical to each other (their
  * row sums split differently over threads).  Any other `kernel`:
  * ATTN_ERR_SHAPE.  Everything else as attn_fwd_fp8_ex.
@@ -408,9 +408,9 @@ attn_status attn_selftest_fwd_abort(const void* q, const void* k, const void* v,
 attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t stream);
 
 /*
- * attn_fwd_kernel_choice — which kernel attn_fwd runs for a padded bf16 batch of
- * B x H heads of Sq queries and Sk keys, causal or not, on a device with
- * `num_sms` SMs.  Returns 1 for the two-query-tile kernel (units of 256 query
+ * attn_fwd_kernel_choice — which kernel attn_fwd and attn_fwd_fp8_ex run for
+ * a padded batch of B x H heads of Sq queries and Sk keys, causal or not, on
+ * a device with `num_sms` SMs.  Returns 1 for the two-query-tile kernel (units of 256 query
  * rows), 0 for the one-tile kernel (units of 128 rows), -1 for a negative
  * argument.  The two compute the same function; the choice is a cost model
  * of the work units (non-causal: waves of equal units over the SMs; causal:
