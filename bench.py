@@ -282,12 +282,14 @@ def is_fp8(w) -> bool:
 def forward_kernel(w, splits: int, num_sms: int) -> str:
     """The kernel that does the forward's work for this workload, as the
     library chooses it: padded batches (bf16 or E4M3) without key ranges may
-    run the two-query-tile kernel (attn_fwd_kernel_choice), packed, paged and
-    split batches the one-tile kernel."""
+    run the two-query-tile kernel (attn_fwd_kernel_choice); packed and paged
+    batches run it when a sequence may hold more than one query tile; split
+    batches run the one-tile kernel."""
     from exact_attention_86_gb300 import attn
-    if not is_varlen(w) and splits == 0:
-        if attn.attn_fwd_kernel_choice(w.B, w.H, w.Sq, w.Sk, int(w.causal), num_sms) == 1:
-            return "attn_fwd_pair_kernel"
+    if is_varlen(w):
+        return "attn_fwd_pair_kernel" if w.max_len > 128 else "attn_fwd_kernel"
+    if splits == 0 and attn.attn_fwd_kernel_choice(w.B, w.H, w.Sq, w.Sk, int(w.causal), num_sms) == 1:
+        return "attn_fwd_pair_kernel"
     return "attn_fwd_kernel"
 
 
@@ -758,8 +760,8 @@ def main():
                        "parallelism": f"weak: {world} replica(s) of the workload, one per GPU",
                        "splits": args.splits,
                        "v_layout": (w.v_layout if is_fp8(w) else "rows"),
-                       "schedule": ("static" if args.static_schedule or w.causal else "dynamic") if varlen
-                                   else "static"},
+                       "schedule": ("static" if args.static_schedule or (w.causal and kernel == "attn_fwd_kernel")
+                                    else "dynamic") if varlen else "static"},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": whole_job_rate(step_flops, world, e2e_ms) / 1e12, "unit": "TFLOP/s",

@@ -66,11 +66,21 @@ SIGNATURES = {
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float,
                                        ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "attn_fwd_varlen_variant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_float, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                               ctypes.c_void_p]),
     "attn_fwd_paged": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                       ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
                                       ctypes.c_void_p, ctypes.c_void_p]),
+    "attn_fwd_paged_variant": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int,
+                                              ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]),
     "attn_fwd_splitkv_workspace_size": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                           ctypes.c_int]),
     "attn_fwd_splitkv_suggest_splits": (ctypes.c_int, [ctypes.c_int] * 5),
@@ -167,6 +177,13 @@ def attn_fwd_varlen(q: int, k: int, v: int, o: int, lse: int, cu_q: int, cu_k: i
                     tile_counter: Optional[int], stream: Optional[int]) -> int:
     return lib().attn_fwd_varlen(q, k, v, o, lse, cu_q, cu_k, batch, max_seqlen_q, total_q, total_k, H, D, scale,
                                  int(causal), tile_counter, stream)
+
+
+def attn_fwd_varlen_variant(q: int, k: int, v: int, o: int, lse: int, cu_q: int, cu_k: int, batch: int,
+                            max_seqlen_q: int, total_q: int, total_k: int, H: int, D: int, scale: float, causal: int,
+                            tile_counter: Optional[int], kernel: int, stream: Optional[int]) -> int:
+    return lib().attn_fwd_varlen_variant(q, k, v, o, lse, cu_q, cu_k, batch, max_seqlen_q, total_q, total_k, H, D,
+                                         scale, int(causal), tile_counter, kernel, stream)
 
 
 def attn_fwd_paged(q: int, k_cache: int, v_cache: int, o: int, lse: int, cu_q: int, seqlens_k: int,
@@ -390,11 +407,12 @@ def tile_counter(device, stream: int):
 
 
 def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, scale: Optional[float] = None,
-                   causal: bool = False, dynamic: bool = True, out=None, lse=None):
+                   causal: bool = False, dynamic: bool = True, out=None, lse=None, kernel: int = ATTN_KERNEL_AUTO):
     """Packed variable-length forward on torch CUDA tensors: ``q [total_q, H, D]``,
     ``k``/``v [total_k, H, D]`` bf16, ``cu_seqlens_q``/``cu_seqlens_k`` int32
-    ``[batch + 1]`` on the same device.  Returns ``(o [total_q, H, D], lse [H, total_q])``,
-    written into ``out`` / ``lse`` when given."""
+    ``[batch + 1]`` on the same device.  ``kernel`` as for ``forward``.
+    Returns ``(o [total_q, H, D], lse [H, total_q])``, written into ``out`` /
+    ``lse`` when given."""
     import torch
 
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -416,16 +434,18 @@ def forward_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, scale
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         counter = tile_counter(q.device, stream).data_ptr() if dynamic else None
-        st = attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                             cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), batch, int(max_seqlen_q), total_q,
-                             total_k, H, D, float(scale), int(bool(causal)), counter, stream)
+        st = attn_fwd_varlen_variant(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                     cu_seqlens_q.data_ptr(), cu_seqlens_k.data_ptr(), batch, int(max_seqlen_q),
+                                     total_q, total_k, H, D, float(scale), int(bool(causal)), counter, int(kernel),
+                                     stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_varlen")
     return out, lse
 
 
 def forward_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, max_seqlen_q: int,
-                  scale: Optional[float] = None, causal: bool = False, dynamic: bool = True, out=None, lse=None):
+                  scale: Optional[float] = None, causal: bool = False, dynamic: bool = True, out=None, lse=None,
+                  kernel: int = ATTN_KERNEL_AUTO):
     """Packed queries ``q [total_q, H, D]`` against a paged KV cache
     ``k_cache``/``v_cache [num_pages, page_size, H, D]`` (bf16 CUDA tensors);
     ``cu_seqlens_q`` int32 ``[batch + 1]``, ``seqlens_k`` int32 ``[batch]``,
@@ -456,10 +476,11 @@ def forward_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, max
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         counter = tile_counter(q.device, stream).data_ptr() if dynamic else None
-        st = attn_fwd_paged(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                            cu_seqlens_q.data_ptr(), seqlens_k.data_ptr(), block_table.data_ptr(), batch,
-                            int(max_seqlen_q), total_q, num_pages, page_size, block_table.shape[1], H, D,
-                            float(scale), int(bool(causal)), counter, stream)
+        st = lib().attn_fwd_paged_variant(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                                          lse.data_ptr(), cu_seqlens_q.data_ptr(), seqlens_k.data_ptr(),
+                                          block_table.data_ptr(), batch, int(max_seqlen_q), total_q, num_pages,
+                                          page_size, block_table.shape[1], H, D, float(scale), int(bool(causal)),
+                                          counter, int(kernel), stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_paged")
     return out, lse

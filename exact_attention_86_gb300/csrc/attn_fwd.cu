@@ -1543,10 +1543,11 @@ attn_status attn_fwd_fp8(const void* q, const void* k, const void* v_t, void* o,
                          ATTN_V_TRANSPOSED, stream);
 }
 
-attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
-                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int max_seqlen_q,
-                            int total_q, int total_k, int H, int D, float scale, int causal, uint32_t* tile_counter,
-                            attn_stream_t stream) {
+attn_status attn_fwd_varlen_variant(const void* q, const void* k, const void* v, void* o, float* lse,
+                                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
+                                    int max_seqlen_q, int total_q, int total_k, int H, int D, float scale, int causal,
+                                    uint32_t* tile_counter, int kernel, attn_stream_t stream) {
+  if (kernel < ATTN_KERNEL_AUTO || kernel > ATTN_KERNEL_TWO_TILE) return ATTN_ERR_SHAPE;
   if (batch < 0 || max_seqlen_q < 0 || total_q < 0 || total_k < 0 || H < 0) return ATTN_ERR_SHAPE;
   if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED_D;
   if (!std::isfinite(scale)) return ATTN_ERR_SCALE;
@@ -1582,14 +1583,40 @@ attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o
   // longest-first order walks through the empty high query tiles of the short
   // sequences one atomic at a time (measured 8 % slower)
   p.sched = causal ? nullptr : tile_counter;
+  // Units of two query tiles of one (sequence, head) (attn_fwd_pair_kernel)
+  // whenever a sequence may hold more than one query tile, claimed from the
+  // counter when it is given (causal too), in longest-first order over all
+  // heads (measured on the packed workload, 32 sequences U[1,4096]: causal
+  // 1063 TFLOP/s claimed and 967 dealt, against 942 on the one-tile kernel;
+  // by head groups, as the one-tile kernel orders them, 984; non-causal
+  // claimed 1350-1409 against 1238).
+  if (kernel == ATTN_KERNEL_TWO_TILE || (kernel == ATTN_KERNEL_AUTO && max_seqlen_q > kBQ)) {
+    Params pp = p;
+    pp.sched = tile_counter;
+    pp.head_group = batch * H;
+    const uint64_t n_pairs = (static_cast<uint64_t>(max_seqlen_q) + 2 * kBQ - 1) / (2 * kBQ);
+    pp.n_qtiles = static_cast<int>(n_pairs);
+    pp.total_units = static_cast<int>(static_cast<uint64_t>(batch) * H * n_pairs);
+    return attn_pair_host::launch(D, causal != 0, false, dev->num_sms, mq, mk, mv, pp,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  }
   return launch_any(*dev, D, causal != 0, mq, mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
 }
 
-attn_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
-                           const int32_t* cu_seqlens_q, const int32_t* seqlens_k, const int32_t* block_table,
-                           int batch, int max_seqlen_q, int total_q, int num_pages, int page_size,
-                           int max_pages_per_seq, int H, int D, float scale, int causal, uint32_t* tile_counter,
-                           attn_stream_t stream) {
+attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                            const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int max_seqlen_q,
+                            int total_q, int total_k, int H, int D, float scale, int causal, uint32_t* tile_counter,
+                            attn_stream_t stream) {
+  return attn_fwd_varlen_variant(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, batch, max_seqlen_q, total_q, total_k, H,
+                                 D, scale, causal, tile_counter, ATTN_KERNEL_AUTO, stream);
+}
+
+attn_status attn_fwd_paged_variant(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                                   const int32_t* cu_seqlens_q, const int32_t* seqlens_k,
+                                   const int32_t* block_table, int batch, int max_seqlen_q, int total_q,
+                                   int num_pages, int page_size, int max_pages_per_seq, int H, int D, float scale,
+                                   int causal, uint32_t* tile_counter, int kernel, attn_stream_t stream) {
+  if (kernel < ATTN_KERNEL_AUTO || kernel > ATTN_KERNEL_TWO_TILE) return ATTN_ERR_SHAPE;
   if (batch < 0 || max_seqlen_q < 0 || total_q < 0 || H < 0) return ATTN_ERR_SHAPE;
   if (num_pages < 1 || max_pages_per_seq < 1 || page_size < 64 || page_size % 64 != 0) return ATTN_ERR_SHAPE;
   if (static_cast<uint64_t>(num_pages) * page_size + 64 > 0x7fffffffull ||
@@ -1629,7 +1656,30 @@ attn_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cac
   // causal paged batches keep the longest-first order over all heads: the
   // head groups that help the packed batch (+9 %) cost this one 5 % (measured)
   p.head_group = batch * H;
+  if (kernel == ATTN_KERNEL_TWO_TILE || (kernel == ATTN_KERNEL_AUTO && max_seqlen_q > kBQ)) {
+    // units of two query tiles of one (sequence, head) (attn_fwd_pair_kernel),
+    // claimed from the counter when it is given (measured on the paged
+    // workload, causal: 1045 TFLOP/s claimed and 965 dealt, against 807-813
+    // on the one-tile kernel)
+    Params pp = p;
+    pp.sched = tile_counter;
+    const uint64_t n_pairs = (static_cast<uint64_t>(max_seqlen_q) + 2 * kBQ - 1) / (2 * kBQ);
+    pp.n_qtiles = static_cast<int>(n_pairs);
+    pp.total_units = static_cast<int>(static_cast<uint64_t>(batch) * H * n_pairs);
+    return attn_pair_host::launch(D, causal != 0, false, dev->num_sms, mq, mk, mv, pp,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  }
   return launch_any(*dev, D, causal != 0, mq, mk, mv, p, reinterpret_cast<cudaStream_t>(stream));
+}
+
+attn_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                           const int32_t* cu_seqlens_q, const int32_t* seqlens_k, const int32_t* block_table,
+                           int batch, int max_seqlen_q, int total_q, int num_pages, int page_size,
+                           int max_pages_per_seq, int H, int D, float scale, int causal, uint32_t* tile_counter,
+                           attn_stream_t stream) {
+  return attn_fwd_paged_variant(q, k_cache, v_cache, o, lse, cu_seqlens_q, seqlens_k, block_table, batch,
+                                max_seqlen_q, total_q, num_pages, page_size, max_pages_per_seq, H, D, scale, causal,
+                                tile_counter, ATTN_KERNEL_AUTO, stream);
 }
 
 size_t attn_fwd_splitkv_workspace_size(int B, int H, int Sq, int D, int num_splits) {

@@ -111,11 +111,13 @@ static_assert(sizeof(CtrlPair) <= 1024, "control block");
 
 struct UnitPair {
   int b, h;
-  int q0;       // first row of tile A
+  int q0;       // first row of tile A within its sequence
   int rows[2];  // rows of tiles A and B that exist (0 .. 128)
   int kv;       // valid keys of the batch entry
   int n[2];     // K tiles tile A / B processes
   int n_max;
+  int q_tok0;   // packed mode: token of tile A's first row
+  int k_tok0;   // packed mode: token of the sequence's first key
 };
 
 // A static deal of the causal units to the blocks, computed on the host
@@ -131,9 +133,42 @@ struct UnitSched {
   uint32_t owner[ON ? kSchedMaxUnits / 4 : 1];
 };
 
+// Rows, keys and tile counts of a packed unit (u.b, u.h, u.q0 set): the
+// sequence's query and key ranges come from the offsets (clamped so that any
+// content stays in bounds), paged keys from the sequence's key count.  Kept
+// apart from the padded decode, whose code it would otherwise perturb
+// (measured: 2.4 % on the padded forward).
+template <bool CAUSAL>
+__device__ __forceinline__ void packed_extent(const Params& p, UnitPair& u) {
+  const int qs = min(max(__ldg(p.cu_q + u.b), 0), p.total_q);
+  const int qe = min(max(__ldg(p.cu_q + u.b + 1), qs), p.total_q);
+  const int q_len = qe - qs;
+  u.q_tok0 = qs + u.q0;
+  int kv;
+  if (p.block_table != nullptr) {  // paged keys: looked up page by page
+    kv = min(max(__ldg(p.seqlens_k + u.b), 0), p.max_pages * p.page_size);
+    u.k_tok0 = 0;
+  } else {
+    const int ks = min(max(__ldg(p.cu_k + u.b), 0), p.total_k);
+    const int ke = min(max(__ldg(p.cu_k + u.b + 1), ks), p.total_k);
+    kv = ke - ks;
+    u.k_tok0 = ks;
+  }
+  u.kv = kv;
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const int q0x = u.q0 + kBQ * x;
+    u.rows[x] = max(min(kBQ, q_len - q0x), 0);
+    int lim = kv;
+    if (CAUSAL) lim = min(lim, q0x + u.rows[x]);
+    u.n[x] = u.rows[x] > 0 ? (lim + kBK - 1) / kBK : 0;
+  }
+  u.n_max = max(u.n[0], u.n[1]);
+}
+
 // Unit t: (b, h, pair of query tiles), ordered as attn_fwd_kernel's units
 // (Params::n_qtiles counts tile pairs per head here).
-template <bool CAUSAL>
+template <bool CAUSAL, bool PACKED>
 __device__ __forceinline__ UnitPair decode_pair(const Params& p, int t) {
   UnitPair u;
   int pr, bh;
@@ -151,6 +186,10 @@ __device__ __forceinline__ UnitPair decode_pair(const Params& p, int t) {
   u.b = p.fd_H.div(bh);
   u.h = bh - u.b * p.H;
   u.q0 = pr * (2 * kBQ);
+  if constexpr (PACKED) {
+    packed_extent<CAUSAL>(p, u);
+    return u;
+  }
   int kv = p.Sk;
   if (p.kv_lens != nullptr) kv = min(max(__ldg(p.kv_lens + u.b), 0), p.Sk);
   u.kv = kv;
@@ -259,7 +298,7 @@ __device__ __forceinline__ void load_s128(uint32_t tS, uint32_t (&sp)[128]) {
   tmem_ld_wait_x32(d);
 }
 
-template <int D, bool CAUSAL, bool FP8>
+template <int D, bool CAUSAL, bool FP8, bool PACKED>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_pair_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                          const __grid_constant__ CUtensorMap map_v, const Params p,
@@ -349,7 +388,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           UnitPair u;
           for (;;) {
             int cand;
-            if (CAUSAL && sched.n > 0) {
+            if (PACKED && p.sched != nullptr) {
+              // claimed from the launch's counter (packed batches with a
+              // caller-owned counter): any block takes the next unit
+              cand = static_cast<int>(atomicAdd(p.sched, 1u));
+              if (cand >= p.total_units) break;
+            } else if (CAUSAL && sched.n > 0) {
               // the next unit this block owns in the host's deal
               while (t_sched < sched.n &&
                      ((sched.owner[t_sched >> 2] >> (8 * (t_sched & 3))) & 0xffu) != blockIdx.x)
@@ -362,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               t_static += gridDim.x;
             }
             if (cand >= p.total_units) continue;
-            u = decode_pair<CAUSAL>(p, cand);
+            u = decode_pair<CAUSAL, PACKED>(p, cand);
             if (u.rows[0] > 0) {
               unit = cand;
               break;
@@ -384,11 +428,36 @@ __global__ void __launch_bounds__(kThreads, 1)
           // both Q tiles (rows past Sq read as zeros and count as loaded)
           mbar_arrive_expect_tx(bar_q_full, 2 * G::kTileBytes);
           for (int x = 0; x < 2; ++x)
-            for (int c = 0; c < G::kChunks; ++c)
-              tma_load_4d_hint(base + G::kOffQ + x * G::kTileBytes + c * G::kChunkBytes, &map_q, bar_q_full,
-                               c * G::kChunkElems, u.q0 + kBQ * x, u.h, u.b, pol_once);
+            for (int c = 0; c < G::kChunks; ++c) {
+              if constexpr (PACKED)  // packed maps are (D, H, tokens, 1)
+                tma_load_4d_hint(base + G::kOffQ + x * G::kTileBytes + c * G::kChunkBytes, &map_q, bar_q_full,
+                                 c * G::kChunkElems, u.h, u.q_tok0 + kBQ * x, 0, pol_once);
+              else                   // padded maps are (D, S, H, B)
+                tma_load_4d_hint(base + G::kOffQ + x * G::kTileBytes + c * G::kChunkBytes, &map_q, bar_q_full,
+                                 c * G::kChunkElems, u.q0 + kBQ * x, u.h, u.b, pol_once);
+            }
           ++qcount;
           for (int j = 0; ok && j < u.n_max; ++j) {
+            // paged keys: the cache rows of the tile's two 64-key halves (a
+            // half wholly past the sequence's keys reads one row past the end
+            // of the cache: zeros)
+            int page_tok[2] = {0, 0};
+            if constexpr (PACKED) {
+              page_tok[0] = page_tok[1] = p.cache_tokens;
+            }
+            if (PACKED && p.block_table != nullptr) {
+              int pg[2] = {0, 0};
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const int pos = j * kBK + 64 * hf;
+                if (pos < u.kv) pg[hf] = __ldg(p.block_table + static_cast<size_t>(u.b) * p.max_pages + pos / p.page_size);
+              }
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const int pos = j * kBK + 64 * hf;
+                if (pos < u.kv) page_tok[hf] = min(max(pg[hf], 0), p.num_pages - 1) * p.page_size + pos % p.page_size;
+              }
+            }
             for (int sel = 0; sel < 2; ++sel) {  // K_j, then V_j
               const typename G::Fill f = G::fill_of(pos >> 1, sel != 0);
               if (!wait_phase(bar_kv_empty0 + 8 * f.slot, (f.empty_use & 1u) ^ 1u, abort_flag, kSiteKvEmpty,
@@ -407,6 +476,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                   // E4M3 V given transposed, (Sk, D, H, B): the tile is D rows,
                   // each 128 keys long (K-major for the P V product)
                   tma_load_4d_hint(dst, m, full, j * kBK, 0, u.h, u.b, pol_keep);
+                } else if (PACKED && p.block_table != nullptr) {
+                  // paged: two 64-key boxes, each inside one page (page_size is
+                  // a multiple of 64), landing as the two halves of the tile
+                  for (int hf = 0; hf < 2; ++hf)
+                    for (int c = 0; c < G::kChunks; ++c)
+                      tma_load_4d_hint(dst + c * G::kChunkBytes + hf * (G::kChunkBytes / 2), m, full, c * 64, u.h,
+                                       page_tok[hf], 0, pol_keep);
+                } else if constexpr (PACKED) {
+                  for (int c = 0; c < G::kChunks; ++c)
+                    tma_load_4d_hint(dst + c * G::kChunkBytes, m, full, c * G::kChunkElems, u.h,
+                                     u.k_tok0 + j * kBK, 0, pol_keep);
                 } else {
                   for (int c = 0; c < G::kChunks; ++c)
                     tma_load_4d_hint(dst + c * G::kChunkBytes, m, full, c * G::kChunkElems, j * kBK, u.h, u.b,
@@ -415,6 +495,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               ++pos;
             }
+          }
+        }
+        // Dynamic claims: this block makes no more.  The last block to get
+        // here (every block does, aborting or not) puts the counter back to 0
+        // for the next launch that uses it.
+        if (PACKED && p.sched != nullptr) {
+          __threadfence();
+          if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+            atomicExch(p.sched, 0u);
+            atomicExch(p.sched + 1, 0u);
           }
         }
         // Drains: after a failure every issued copy must land; in any case the
@@ -440,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
         if (unit == -2) { ok = false; break; }
         if (unit < 0) break;
-        const UnitPair u = decode_pair<CAUSAL>(p, unit);
+        const UnitPair u = decode_pair<CAUSAL, PACKED>(p, unit);
         if (u.n_max == 0) continue;
         if (!wait_warp(bar_q_full, qcount & 1u, abort_flag, kSiteQFull, limit)) { ok = false; break; }
         ++qcount;
@@ -500,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
         if (unit == -2) { ok = false; break; }
         if (unit < 0) break;
-        const UnitPair u = decode_pair<CAUSAL>(p, unit);
+        const UnitPair u = decode_pair<CAUSAL, PACKED>(p, unit);
         if (u.n_max == 0) continue;
         for (int j = 0; ok && j < u.n_max; ++j, ++tiles) {
           const typename G::Fill f = G::fill_of(tiles, true);
@@ -592,21 +682,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int unit = take_unit(kq, unit_q, bar_uq_full0, bar_uq_empty0, abort_flag, limit, lane);
       if (unit == -2) { ok = false; break; }
       if (unit < 0) break;
-      const UnitPair u = decode_pair<CAUSAL>(p, unit);
+      const UnitPair u = decode_pair<CAUSAL, PACKED>(p, unit);
       const int rows = x ? u.rows[1] : u.rows[0];  // (constant indices keep the unit in registers)
       const int nx = x ? u.n[1] : u.n[0];
       if (rows == 0) continue;  // tile B past the end of the sequence
       const int q0x = u.q0 + kBQ * x;
       const int row = q0x + r;
       const bool row_ok = r < rows;
-      const size_t row_index = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq) + row;
+      size_t row_index, lse_index;  // row of O (in units of D elements) and index into lse
+      if constexpr (PACKED) {       // packed: o [total_q, H, D], lse [H, total_q]
+        const size_t tok = static_cast<size_t>(u.q_tok0) + kBQ * x + r;
+        row_index = tok * p.H + u.h;
+        lse_index = static_cast<size_t>(u.h) * p.total_q + tok;
+      } else {                      // padded: o [B, H, Sq, D], lse [B, H, Sq]
+        row_index = (static_cast<size_t>(u.b) * p.H + u.h) * static_cast<size_t>(p.Sq) + row;
+        lse_index = row_index;
+      }
       uint16_t* o_dst = p.o + row_index * D;
       if (nx == 0) {  // no valid key for any row of this tile: O = 0, LSE = -inf
         if (row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(o_dst);
 #pragma unroll
           for (int q = 0; q < D / 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
-          p.lse[row_index] = -INFINITY;
+          p.lse[lse_index] = -INFINITY;
         }
         continue;
       }
@@ -712,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the next unit's first P V overwrites O_x only after this warpgroup's
       // p_full for it, which comes after these loads
       tc_fence_before_sync();
-      if (row_ok) p.lse[row_index] = lse_row;
+      if (row_ok) p.lse[lse_index] = lse_row;
     }
     // The commit of the last P_x V lands asynchronously and nothing else
     // waits for it: wait before exiting.
@@ -729,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // dynamic shared memory attribute set, per device and instantiation
 constexpr int kMaxDevicesPair = 64;
-std::atomic<bool> g_pair_smem_set[kMaxDevicesPair][8];
+std::atomic<bool> g_pair_smem_set[kMaxDevicesPair][12];
 
 // Cost model of a unit, in hundredths of the time one 128-key tile takes the
 // one-tile kernel: a key tile that both query tiles of a pair process costs
@@ -797,12 +895,14 @@ bool causal_schedule(const Params& p, int grid, UnitSched<true>& out) {
   return true;
 }
 
-template <int D, bool CAUSAL, bool FP8>
+template <int D, bool CAUSAL, bool FP8, bool PACKED = false>
 attn_status launch_pair(int dev, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         const Params& p0, cudaStream_t stream) {
-  auto kern = attn_fwd_pair_kernel<D, CAUSAL, FP8>;
+  static_assert(!(FP8 && PACKED), "packed batches are bf16");
+  auto kern = attn_fwd_pair_kernel<D, CAUSAL, FP8, PACKED>;
   constexpr int smem = GeoPair<D, FP8>::kSmemBytes;
-  constexpr int idx = (D == 64 ? 0 : 4) + (CAUSAL ? 2 : 0) + (FP8 ? 1 : 0);
+  constexpr int idx = PACKED ? 8 + (D == 64 ? 0 : 2) + (CAUSAL ? 1 : 0)
+                             : (D == 64 ? 0 : 4) + (CAUSAL ? 2 : 0) + (FP8 ? 1 : 0);
   if (dev < 0 || dev >= kMaxDevicesPair) return ATTN_ERR_UNSUPPORTED_DEVICE;
   if (!g_pair_smem_set[dev][idx].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -813,7 +913,9 @@ attn_status launch_pair(int dev, int num_sms, const CUtensorMap& mq, const CUten
   UnitSched<CAUSAL> sched;
   sched.n = 0;
   if constexpr (CAUSAL) {
-    if (!causal_schedule(p0, grid, sched)) sched.n = 0;  // too many units: the round-robin deal
+    // padded batches only: a packed batch's sequence lengths are on the
+    // device, so its units keep the round-robin deal
+    if (PACKED || !causal_schedule(p0, grid, sched)) sched.n = 0;
   }
   kern<<<grid, kThreads, smem, stream>>>(mq, mk, mv, with_divisors(p0, grid), sched);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -885,6 +987,14 @@ attn_status launch(int D, bool causal, bool fp8, int num_sms, const CUtensorMap&
                    const CUtensorMap& mv, const attn_detail::Params& p, cudaStream_t s) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (p.cu_q != nullptr) {  // packed or paged (bf16)
+    if (fp8) return ATTN_ERR_SHAPE;
+    if (causal)
+      return D == 64 ? launch_pair<64, true, false, true>(dev, num_sms, mq, mk, mv, p, s)
+                     : launch_pair<128, true, false, true>(dev, num_sms, mq, mk, mv, p, s);
+    return D == 64 ? launch_pair<64, false, false, true>(dev, num_sms, mq, mk, mv, p, s)
+                   : launch_pair<128, false, false, true>(dev, num_sms, mq, mk, mv, p, s);
+  }
   if (fp8) {
     if (causal)
       return D == 64 ? launch_pair<64, true, true>(dev, num_sms, mq, mk, mv, p, s)

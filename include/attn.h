@@ -183,19 +183,37 @@ attn_status attn_fwd_fp8_variant(const void* q, const void* k, const void* v, vo
  * last 128-key tile of a sequence also reads the next sequence's first keys
  * with weight zero (they must be finite); past total_k the tile reads zeros.
  * tile_counter NULL (work is dealt round-robin to the SMs) or device uint32
- *              [2], 8-byte aligned, both zero on entry: for a non-causal call
- *              the SMs then claim the units of work (128 query rows of one
- *              sequence and head) one by one, which balances ragged batches;
- *              causal calls keep the longest-first round-robin deal and do
- *              not touch it.  A launch leaves both words zero when it ends,
- *              so one counter serves consecutive calls on a stream; calls that
- *              share a counter must not overlap on the GPU.
+ *              [2], 8-byte aligned, both zero on entry: the SMs then claim
+ *              the units of work one by one, which balances ragged batches.
+ *              With max_seqlen_q > 128 the call runs the two-tile kernel
+ *              (units of 256 query rows of one sequence and head, claimed
+ *              when the counter is given, causal or not); otherwise the
+ *              one-tile kernel (units of 128 rows), which claims only for
+ *              non-causal calls.  A launch leaves both words zero when it
+ *              ends, so one counter serves consecutive calls on a stream;
+ *              calls that share a counter must not overlap on the GPU.
  * Asynchronous on `stream`; argument errors return before any launch.
  */
 attn_status attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch, int max_seqlen_q,
                             int total_q, int total_k, int H, int D, float scale, int causal, uint32_t* tile_counter,
                             attn_stream_t stream);
+
+/*
+ * attn_fwd_varlen_variant — attn_fwd_varlen with the kernel chosen by the
+ * caller: `kernel` as in attn_fwd_variant (ATTN_KERNEL_AUTO: the kernel
+ * attn_fwd_varlen runs: the two-tile kernel when max_seqlen_q > 128, else
+ * the one-tile kernel; ATTN_KERNEL_TWO_TILE: units of two query tiles of one
+ * (sequence, head), claimed from tile_counter when it is given, causal or
+ * not, else dealt round-robin).  Both compute the
+ * same function within the forward's tolerance; they are not bit-identical
+ * to each other.  Any other `kernel`: ATTN_ERR_SHAPE.  Everything else as
+ * attn_fwd_varlen.
+ */
+attn_status attn_fwd_varlen_variant(const void* q, const void* k, const void* v, void* o, float* lse,
+                                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int batch,
+                                    int max_seqlen_q, int total_q, int total_k, int H, int D, float scale, int causal,
+                                    uint32_t* tile_counter, int kernel, attn_stream_t stream);
 
 /*
  * attn_fwd_paged — the packed-query forward with keys and values read through
@@ -228,6 +246,21 @@ attn_status attn_fwd_paged(const void* q, const void* k_cache, const void* v_cac
                            int batch, int max_seqlen_q, int total_q, int num_pages, int page_size,
                            int max_pages_per_seq, int H, int D, float scale, int causal, uint32_t* tile_counter,
                            attn_stream_t stream);
+
+/*
+ * attn_fwd_paged_variant — attn_fwd_paged with the kernel chosen by the
+ * caller: `kernel` as in attn_fwd_varlen_variant (ATTN_KERNEL_AUTO: the
+ * kernel attn_fwd_paged runs, the two-tile kernel when max_seqlen_q > 128,
+ * else the one-tile kernel; ATTN_KERNEL_TWO_TILE: units of two query tiles
+ * of one (sequence, head), claimed from tile_counter when it is given, else
+ * dealt round-robin).  Any other
+ * `kernel`: ATTN_ERR_SHAPE.  Everything else as attn_fwd_paged.
+ */
+attn_status attn_fwd_paged_variant(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                                   const int32_t* cu_seqlens_q, const int32_t* seqlens_k,
+                                   const int32_t* block_table, int batch, int max_seqlen_q, int total_q,
+                                   int num_pages, int page_size, int max_pages_per_seq, int H, int D, float scale,
+                                   int causal, uint32_t* tile_counter, int kernel, attn_stream_t stream);
 
 /*
  * attn_fwd_splitkv — the same forward with the keys of every (b, h, 128-row
@@ -438,7 +471,7 @@ int64_t attn_fwd_pair_schedule(int B, int H, int Sq, int Sk, int head_group, int
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 14
+#define ATTN_ABI_VERSION 16
 
 #ifdef __cplusplus
 }

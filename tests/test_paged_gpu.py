@@ -58,10 +58,14 @@ def _np(t):
     return t.float().numpy().astype(np.float64)
 
 
-def _run(q, kc, vc, cu_q, sk, table, max_q, scale, causal):
+KERNELS = pytest.mark.parametrize("kernel", [attn.ATTN_KERNEL_ONE_TILE, attn.ATTN_KERNEL_TWO_TILE],
+                                  ids=["one", "two"])
+
+
+def _run(q, kc, vc, cu_q, sk, table, max_q, scale, causal, kernel=attn.ATTN_KERNEL_AUTO):
     dev = torch.device("cuda:0")
     o, lse = attn.forward_paged(q.to(dev), kc.to(dev), vc.to(dev), cu_q.to(dev), sk.to(dev), table.to(dev), max_q,
-                                scale=scale, causal=causal)
+                                scale=scale, causal=causal, kernel=kernel)
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
     return o.float().cpu().numpy(), lse.cpu().numpy()
@@ -75,25 +79,28 @@ CASES = [
 ]
 
 
+@KERNELS
 @pytest.mark.parametrize("case", range(len(CASES)))
 @pytest.mark.parametrize("page_size", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("D", [64, 128])
-def test_paged_matches_oracle(case, page_size, causal, D):
+def test_paged_matches_oracle(case, page_size, causal, D, kernel):
     lens_q, lens_k = CASES[case]
     H = 2
     q, kc, vc, cu_q, sk, table = _paged_case(lens_q, lens_k, H, D, page_size, seed=case * 13 + page_size + D)
     scale = 1.0 / math.sqrt(D)
-    o, lse = _run(q, kc, vc, cu_q, sk, table, max(lens_q), scale, causal)
+    o, lse = _run(q, kc, vc, cu_q, sk, table, max(lens_q), scale, causal, kernel)
     o_ref, l_ref = attention_paged_ref(_np(q), _np(kc), _np(vc), cu_q.numpy(), sk.numpy(), table.numpy(), scale,
                                        causal=causal)
     check(o.transpose(1, 0, 2), lse, o_ref.transpose(1, 0, 2), l_ref,
           f"paged case {case} page {page_size} causal={causal} D={D}")
 
 
-def test_paged_in_order_pages_equal_varlen_bitwise():
+@KERNELS
+def test_paged_in_order_pages_equal_varlen_bitwise(kernel):
     """Pages laid out in sequence order turn the cache into the packed keys:
-    the paged and variable-length forwards then compute identical bits."""
+    the paged and variable-length forwards then compute identical bits (on
+    the same kernel)."""
     H, D, ps = 4, 128, 128
     lens = [384, 256, 512]
     g = torch.Generator().manual_seed(21)
@@ -105,15 +112,16 @@ def test_paged_in_order_pages_equal_varlen_bitwise():
     cu = torch.tensor([0, 384, 640, 1152], dtype=torch.int32, device=dev)
     table = torch.tensor([[0, 1, 2, 0], [3, 4, 0, 0], [5, 6, 7, 8]], dtype=torch.int32, device=dev)
     sk = torch.tensor(lens, dtype=torch.int32, device=dev)
-    o_v, l_v = attn.forward_varlen(q, k, v, cu, cu, max(lens), causal=True)
+    o_v, l_v = attn.forward_varlen(q, k, v, cu, cu, max(lens), causal=True, kernel=kernel)
     o_p, l_p = attn.forward_paged(q, k.view(total // ps, ps, H, D), v.view(total // ps, ps, H, D), cu, sk, table,
-                                  max(lens), causal=True)
+                                  max(lens), causal=True, kernel=kernel)
     torch.cuda.synchronize()
     assert torch.equal(o_v.view(torch.int16), o_p.view(torch.int16))
     assert torch.equal(l_v, l_p)
 
 
-def test_paged_benchmark_workload_equals_varlen_bitwise():
+@KERNELS
+def test_paged_benchmark_workload_equals_varlen_bitwise(kernel):
     """The benchmarked paged batch at full size, in the benchmark's launch
     configuration: the shuffled pages hold the same tokens as the packed batch
     (whose parity against the oracle is tested at full size), and the kernel
@@ -133,8 +141,9 @@ def test_paged_benchmark_workload_equals_varlen_bitwise():
     o_p, o_v = (nan_filled((total, w.H, w.D), torch.bfloat16, dev) for _ in range(2))
     l_p, l_v = (nan_filled((w.H, total), torch.float32, dev) for _ in range(2))
     attn.forward_paged(qd, kc.to(dev), vc.to(dev), cud, sk.to(dev), table.to(dev), w.max_len, causal=w.causal,
-                       out=o_p, lse=l_p)
-    attn.forward_varlen(qd, k.to(dev), v.to(dev), cud, cud, w.max_len, causal=w.causal, out=o_v, lse=l_v)
+                       out=o_p, lse=l_p, kernel=kernel)
+    attn.forward_varlen(qd, k.to(dev), v.to(dev), cud, cud, w.max_len, causal=w.causal, out=o_v, lse=l_v,
+                        kernel=kernel)
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
     assert_no_nan(o_p, l_p, what="paged")
@@ -143,15 +152,16 @@ def test_paged_benchmark_workload_equals_varlen_bitwise():
     assert torch.equal(l_p, l_v)
 
 
-def test_paged_dynamic_and_static_scheduling_agree_bitwise():
+@KERNELS
+def test_paged_dynamic_and_static_scheduling_agree_bitwise(kernel):
     from exact_attention_86_gb300 import workloads
 
     w = workloads.PAGED_WORKLOADS["paged_b32_d128_causal"]
     q, kc, vc, cu, sk, table = workloads.generate_paged(w)
     dev = torch.device("cuda:0")
     args = [t.to(dev) for t in (q, kc, vc, cu, sk, table)]
-    o_s, l_s = attn.forward_paged(*args, w.max_len, causal=w.causal, dynamic=False)
-    o_d, l_d = attn.forward_paged(*args, w.max_len, causal=w.causal, dynamic=True)
+    o_s, l_s = attn.forward_paged(*args, w.max_len, causal=w.causal, dynamic=False, kernel=kernel)
+    o_d, l_d = attn.forward_paged(*args, w.max_len, causal=w.causal, dynamic=True, kernel=kernel)
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
     assert torch.equal(o_d.view(torch.int16), o_s.view(torch.int16))

@@ -36,10 +36,14 @@ def _np(t):
     return t.float().numpy().astype(np.float64)
 
 
-def _run(q, k, v, cu_q, cu_k, max_q, scale, causal):
+KERNELS = pytest.mark.parametrize("kernel", [attn.ATTN_KERNEL_ONE_TILE, attn.ATTN_KERNEL_TWO_TILE],
+                                  ids=["one", "two"])
+
+
+def _run(q, k, v, cu_q, cu_k, max_q, scale, causal, kernel=attn.ATTN_KERNEL_AUTO):
     dev = torch.device("cuda:0")
     o, lse = attn.forward_varlen(q.to(dev), k.to(dev), v.to(dev), cu_q.to(dev), cu_k.to(dev), max_q,
-                                 scale=scale, causal=causal)
+                                 scale=scale, causal=causal, kernel=kernel)
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
     return o.float().cpu().numpy(), lse.cpu().numpy()
@@ -53,21 +57,23 @@ CASES = [
 ]
 
 
+@KERNELS
 @pytest.mark.parametrize("case", range(len(CASES)))
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("D", [64, 128])
-def test_varlen_matches_oracle(case, causal, D):
+def test_varlen_matches_oracle(case, causal, D, kernel):
     lens_q, lens_k = CASES[case]
     H = 3
     q, k, v, cu_q, cu_k = _packed(lens_q, lens_k, H, D, seed=case * 7 + D + int(causal))
     scale = 1.0 / math.sqrt(D)
-    o, lse = _run(q, k, v, cu_q, cu_k, max(lens_q), scale, causal)
+    o, lse = _run(q, k, v, cu_q, cu_k, max(lens_q), scale, causal, kernel)
     o_ref, l_ref = attention_varlen_ref(_np(q), _np(k), _np(v), cu_q.numpy(), cu_k.numpy(), scale, causal=causal)
     # O [total_q, H, D] against LSE [H, total_q]: compare head-major
     check(o.transpose(1, 0, 2), lse, o_ref.transpose(1, 0, 2), l_ref, f"varlen case {case} causal={causal} D={D}")
 
 
-def test_varlen_guard_rows_untouched():
+@KERNELS
+def test_varlen_guard_rows_untouched(kernel):
     # query tiles that run past a sequence end must not write the next sequence's rows,
     # and nothing past total_q may be written
     lens = [130, 3, 250]
@@ -81,9 +87,9 @@ def test_varlen_guard_rows_untouched():
     o_view = o_buf[:tq * H * D].view(torch.bfloat16).view(tq, H, D)
     l_view = l_buf[:H * tq].view(H, tq)
     qd, kd, vd, cqd, ckd = (t.to(dev) for t in (q, k, v, cu_q, cu_k))  # keep alive across the async call
-    st = attn.attn_fwd_varlen(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o_view.data_ptr(), l_view.data_ptr(),
-                              cqd.data_ptr(), ckd.data_ptr(), 3, 250, tq, tq, H, D, 1 / math.sqrt(D), 1, None,
-                              torch.cuda.current_stream().cuda_stream)
+    st = attn.attn_fwd_varlen_variant(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o_view.data_ptr(),
+                                      l_view.data_ptr(), cqd.data_ptr(), ckd.data_ptr(), 3, 250, tq, tq, H, D,
+                                      1 / math.sqrt(D), 1, None, kernel, torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK
     torch.cuda.synchronize()
     assert torch.all(o_buf[tq * H * D:] == 777) and torch.all(l_buf[H * tq:] == 5.5)
@@ -93,32 +99,36 @@ def test_varlen_guard_rows_untouched():
           "varlen guard")
 
 
-def test_varlen_equals_padded_forward_for_equal_lengths():
+@KERNELS
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_equals_padded_forward_for_equal_lengths(kernel, causal):
+    """Equal lengths on the same kernel: the packed forward reads the same
+    tiles and does the same arithmetic as the padded one, so the bits agree;
+    both match the oracle."""
     B, H, S, D = 2, 4, 384, 128
     g = torch.Generator().manual_seed(11)
     q = torch.randn(B, H, S, D, generator=g).to(torch.bfloat16)
     k = torch.randn(B, H, S, D, generator=g).to(torch.bfloat16)
     v = torch.randn(B, H, S, D, generator=g).to(torch.bfloat16)
     dev = torch.device("cuda:0")
-    o_pad, l_pad = attn.forward(q.to(dev), k.to(dev), v.to(dev), causal=True)
+    o_pad, l_pad = attn.forward(q.to(dev), k.to(dev), v.to(dev), causal=causal, kernel=kernel)
     pack = lambda t: t.permute(0, 2, 1, 3).reshape(B * S, H, D).contiguous().to(dev)  # noqa: E731
     cu = torch.arange(0, (B + 1) * S, S, dtype=torch.int32, device=dev)
-    o_var, l_var = attn.forward_varlen(pack(q), pack(k), pack(v), cu, cu, S, causal=True)
+    o_var, l_var = attn.forward_varlen(pack(q), pack(k), pack(v), cu, cu, S, causal=causal, kernel=kernel)
     torch.cuda.synchronize()
-    # Different kernels (the padded forward runs two query tiles per unit and
-    # sums a row in one thread, the packed one in two halves): both against
-    # the oracle, and against each other within a rounding of the row sum.
-    o_ref, l_ref = attention_ref(_np(q), _np(k), _np(v), 1 / math.sqrt(D), causal=True)
+    o_var_p = o_var.view(B, S, H, D).permute(0, 2, 1, 3)
+    l_var_p = l_var.view(H, B, S).permute(1, 0, 2)
+    assert torch.equal(o_var_p.contiguous().view(torch.int16), o_pad.view(torch.int16))
+    assert torch.equal(l_var_p.contiguous(), l_pad)
+    o_ref, l_ref = attention_ref(_np(q), _np(k), _np(v), 1 / math.sqrt(D), causal=causal)
     check(o_pad.float().cpu().numpy(), l_pad.cpu().numpy(), o_ref, l_ref, "padded")
-    o_var_p = o_var.view(B, S, H, D).permute(0, 2, 1, 3).float().cpu().numpy()
-    l_var_p = l_var.view(H, B, S).permute(1, 0, 2).cpu().numpy()
-    check(o_var_p, l_var_p, o_ref, l_ref, "packed")
     assert float((o_var.float() - pack(o_pad).float()).abs().max()) <= 1e-2
     assert float((l_var - l_pad.permute(1, 0, 2).reshape(H, B * S)).abs().max()) <= 1e-5
 
 
+@KERNELS
 @pytest.mark.parametrize("name", ["varlen_b32_d128_causal", "varlen_b32_d128"])
-def test_varlen_benchmark_workload_every_tile(name):
+def test_varlen_benchmark_workload_every_tile(name, kernel):
     """The benchmarked packed batch at full size, in the benchmark's launch
     configuration (dynamic schedule for the non-causal batch), into NaN-filled
     outputs: no NaN may survive, and the first, last and one random row of
@@ -134,7 +144,7 @@ def test_varlen_benchmark_workload_every_tile(name):
     lse = nan_filled((w.H, total), torch.float32, dev)
     cud = cu.to(dev)
     attn.forward_varlen(q.to(dev), k.to(dev), v.to(dev), cud, cud, w.max_len, scale=w.scale, causal=w.causal,
-                        out=o, lse=lse)
+                        out=o, lse=lse, kernel=kernel)
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
     assert_no_nan(o, lse, what=name)
@@ -170,18 +180,21 @@ def test_varlen_repeated_launches_are_bitwise_identical():
         assert torch.equal(lse, l0), f"launch {i} LSE differs"
 
 
+@KERNELS
 @pytest.mark.parametrize("name", ["varlen_b32_d128_causal", "varlen_b32_d128"])
-def test_varlen_dynamic_and_static_scheduling_agree_bitwise(name):
+def test_varlen_dynamic_and_static_scheduling_agree_bitwise(name, kernel):
     """The claimed (dynamic) and dealt (static) schedules run the same units
-    with the same arithmetic: identical bits; the counter is zero afterwards."""
+    with the same arithmetic: identical bits; the counter is zero afterwards
+    (on either kernel)."""
     from exact_attention_86_gb300 import workloads
 
     w = workloads.VARLEN_WORKLOADS[name]
     q, k, v, cu = workloads.generate_varlen(w)
     dev = torch.device("cuda:0")
     qd, kd, vd, cud = q.to(dev), k.to(dev), v.to(dev), cu.to(dev)
-    o_s, l_s = attn.forward_varlen(qd, kd, vd, cud, cud, w.max_len, causal=w.causal, dynamic=False)
-    runs = [attn.forward_varlen(qd, kd, vd, cud, cud, w.max_len, causal=w.causal, dynamic=True) for _ in range(5)]
+    o_s, l_s = attn.forward_varlen(qd, kd, vd, cud, cud, w.max_len, causal=w.causal, dynamic=False, kernel=kernel)
+    runs = [attn.forward_varlen(qd, kd, vd, cud, cud, w.max_len, causal=w.causal, dynamic=True, kernel=kernel)
+            for _ in range(5)]
     st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
     assert st == attn.ATTN_OK, (st, site)
     for o_d, l_d in runs:
