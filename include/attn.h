@@ -176,8 +176,11 @@ attn_status attn_fwd_fp8_variant(const void* q, const void* k, const void* v, vo
  *              [cu_seqlens_q[b], cu_seqlens_q[b+1]); cu_seqlens_k likewise for
  *              keys and values.  Entries are clamped to [0, total] and to be
  *              non-decreasing, so any content keeps every access in bounds.
- * max_seqlen_q host upper bound of the query lengths (it sizes the grid); rows
- *              of a longer sequence past it are not computed.
+ * max_seqlen_q host upper bound of the query lengths (it sizes the launch).
+ *              Rows of a longer sequence are computed up to the end of the
+ *              work unit that holds row max_seqlen_q - 1 (units of 128 rows
+ *              on the one-tile kernel, 256 on the two-tile kernel); its later
+ *              rows of o and lse are left as they were.
  * Per sequence the operation is exactly attn_fwd's (causal masking top-left
  * within the sequence; a sequence with no key gives O = 0, LSE = -inf).  The
  * last 128-key tile of a sequence also reads the next sequence's first keys

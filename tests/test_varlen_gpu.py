@@ -101,6 +101,43 @@ def test_varlen_guard_rows_untouched(kernel):
 
 @KERNELS
 @pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("max_q", [100, 300, 1000])
+def test_varlen_max_seqlen_q_bounds_the_computed_rows(kernel, causal, max_q):
+    """max_seqlen_q sizes the launch.  Above the longest sequence the extra
+    units are empty; below a sequence's length the rows of the units it
+    covers (128 rows a unit on the one-tile kernel, 256 on the two-tile
+    kernel) are computed and every later row of O and LSE is left as it was."""
+    lens = [600, 50, 257]
+    H, D = 2, 64
+    q, k, v, cu_q, cu_k = _packed(lens, lens, H, D, seed=17 + max_q + int(causal))
+    unit = 128 if kernel == attn.ATTN_KERNEL_ONE_TILE else 256
+    covered = -(-max_q // unit) * unit
+    dev = torch.device("cuda:0")
+    tq = sum(lens)
+    o_buf = torch.full((tq, H, D), 777, dtype=torch.int16, device=dev)
+    l_buf = torch.full((H, tq), 5.5, dtype=torch.float32, device=dev)
+    qd, kd, vd, cqd, ckd = (t.to(dev) for t in (q, k, v, cu_q, cu_k))  # keep alive across the async call
+    st = attn.attn_fwd_varlen_variant(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o_buf.data_ptr(),
+                                      l_buf.data_ptr(), cqd.data_ptr(), ckd.data_ptr(), len(lens), max_q, tq, tq, H,
+                                      D, 1 / math.sqrt(D), int(causal), None, kernel,
+                                      torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, (st, site)
+    pos = np.concatenate([np.arange(n) for n in lens])  # row of each token within its sequence
+    done = pos < covered
+    o_raw = o_buf.cpu()
+    assert torch.all(o_raw[torch.from_numpy(~done)] == 777)
+    assert torch.all(l_buf.cpu()[:, torch.from_numpy(~done)] == 5.5)
+    o_ref, l_ref = attention_varlen_ref(_np(q), _np(k), _np(v), cu_q.numpy(), cu_k.numpy(), 1 / math.sqrt(D),
+                                        causal=causal)
+    o = o_raw.view(torch.bfloat16).float().numpy()
+    check(o[done].transpose(1, 0, 2), l_buf.cpu().numpy()[:, done], o_ref[done].transpose(1, 0, 2),
+          l_ref[:, done], f"varlen max_seqlen_q={max_q}")
+
+
+@KERNELS
+@pytest.mark.parametrize("causal", [False, True])
 def test_varlen_equals_padded_forward_for_equal_lengths(kernel, causal):
     """Equal lengths on the same kernel: the packed forward reads the same
     tiles and does the same arithmetic as the padded one, so the bits agree;
