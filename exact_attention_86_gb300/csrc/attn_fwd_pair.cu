@@ -1,16 +1,19 @@
-// The padded-batch bf16 forward with two query tiles per work unit.
+// The forward with two query tiles per work unit.
 //
 // Same operation as attn_fwd_kernel (softmax(scale * Q K^T + mask) V and the
 // row LSE; "Kernel Fusion and the Memory Wall", section "FlashAttention: avoid
 // the full score matrix", and the tile loop of "Attention softmax fusion"), for
-// padded [B, H, S, D] batches without key ranges.  A translation unit of its
+// padded [B, H, S, D] batches without key ranges (bf16 or E4M3, the FP8
+// template parameter) and for packed and paged bf16 batches (the PACKED
+// template parameter, instantiations of their own).  A translation unit of its
 // own (with the shared parameters, waits and unit order of attn_common.cuh),
 // so that its code leaves the register allocation of attn_fwd.cu's kernels
 // untouched: compiled into one file with them, it cost two of those kernels a
 // register spill.
 //
-// A work unit is 256 query rows of one (b, h): tiles A (rows q0 .. q0 + 127)
-// and B (q0 + 128 .. q0 + 255), which share every K/V tile the producer loads.
+// A work unit is 256 query rows of one (b, h) (packed: of one sequence and
+// head): tiles A (rows q0 .. q0 + 127) and B (q0 + 128 .. q0 + 255), which
+// share every K/V tile the producer loads.
 // Each tile has one softmax warpgroup with ONE thread per row (warps 0-3: A,
 // warps 4-7: B), so a row's max and sum never leave its thread: no barrier,
 // no exchange.  The two tiles' work interleaves on the tensor pipe: while
@@ -25,12 +28,12 @@
 //   warp 11    idle
 //
 // Tensor Memory (512 columns): S_A [0,128), S_B [128,256), O_A [256, 256+D),
-// O_B [256+D, 256+2D).  P_x (bf16 pairs, 64 columns) is written over the first
-// 64 columns of S_x once the softmax has read S_x; S_x is written again only
-// after the P V of its previous tile has consumed P_x (the QK^T issuer waits
-// for that product's commit).  So when the softmax of x sees a new S_x, the
-// P V of the previous tile has completed and O_x is stable: a rescale of O_x
-// never waits.
+// O_B [256+D, 256+2D).  P_x (bf16 pairs in 64 columns; E4M3, four a word, in
+// 32) is written over the first columns of S_x once the softmax has read S_x;
+// S_x is written again only after the P V of its previous tile has consumed
+// P_x (the QK^T issuer waits for that product's commit).  So when the
+// softmax of x sees a new S_x, the P V of the previous tile has completed and
+// O_x is stable: a rescale of O_x never waits.
 //
 // Every wait is bounded, as in attn_fwd_kernel; a wait that gives up records
 // its site and raises the block's abort flag, and every role drains what it

@@ -22,14 +22,15 @@ namespace attn_pair_host {
 // false for arguments out of range.
 bool use_pair(int B, int H, int Sq, int Sk, bool causal, int num_sms);
 
-// Launches the padded forward over units of two 128-row query tiles
-// (p.n_qtiles = tile pairs per head, p.total_units = B * H * pairs; every
-// other field as for attn_fwd_kernel, without key ranges; fp8: E4M3 inputs,
-// with the tensor maps, descriptors and descales attn_fwd_fp8_ex builds;
-// p.cu_q set: a packed or paged bf16 batch, with attn_fwd_varlen's or
-// attn_fwd_paged's maps and fields, p.sched its optional counter) on
-// `stream`, with one block per SM up to the number of units.  Causal batches
-// get a static longest-first deal of their units (see build_schedule).
+// Launches the forward over units of two 128-row query tiles (p.n_qtiles =
+// tile pairs per head, p.total_units = B * H * pairs; every other field as
+// for attn_fwd_kernel, without key ranges; fp8: E4M3 inputs, with the tensor
+// maps, descriptors and descales attn_fwd_fp8_ex builds; p.cu_q set: a packed
+// or paged bf16 batch, with attn_fwd_varlen's or attn_fwd_paged's maps and
+// fields, p.sched its optional counter) on `stream`, with one block per SM up
+// to the number of units.  Padded causal batches get a static longest-first
+// deal of their units (see build_schedule); packed batches claim their units
+// from p.sched when it is set; the rest take the round-robin deal.
 attn_status launch(int D, bool causal, bool fp8, int num_sms, const CUtensorMap& mq, const CUtensorMap& mk,
                    const CUtensorMap& mv, const attn_detail::Params& p, cudaStream_t stream);
 
