@@ -195,6 +195,15 @@ def attn_fwd_paged(q: int, k_cache: int, v_cache: int, o: int, lse: int, cu_q: i
                                 tile_counter, stream)
 
 
+def attn_fwd_paged_variant(q: int, k_cache: int, v_cache: int, o: int, lse: int, cu_q: int, seqlens_k: int,
+                           block_table: int, batch: int, max_seqlen_q: int, total_q: int, num_pages: int,
+                           page_size: int, max_pages_per_seq: int, H: int, D: int, scale: float, causal: int,
+                           tile_counter: Optional[int], kernel: int, stream: Optional[int]) -> int:
+    return lib().attn_fwd_paged_variant(q, k_cache, v_cache, o, lse, cu_q, seqlens_k, block_table, batch,
+                                        max_seqlen_q, total_q, num_pages, page_size, max_pages_per_seq, H, D, scale,
+                                        int(causal), tile_counter, kernel, stream)
+
+
 def attn_fwd_splitkv_workspace_size(B: int, H: int, Sq: int, D: int, num_splits: int) -> int:
     return lib().attn_fwd_splitkv_workspace_size(B, H, Sq, D, num_splits)
 
@@ -476,11 +485,11 @@ def forward_paged(q, k_cache, v_cache, cu_seqlens_q, seqlens_k, block_table, max
     with torch.cuda.device(q.device):
         stream = torch.cuda.current_stream(q.device).cuda_stream
         counter = tile_counter(q.device, stream).data_ptr() if dynamic else None
-        st = lib().attn_fwd_paged_variant(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
-                                          lse.data_ptr(), cu_seqlens_q.data_ptr(), seqlens_k.data_ptr(),
-                                          block_table.data_ptr(), batch, int(max_seqlen_q), total_q, num_pages,
-                                          page_size, block_table.shape[1], H, D, float(scale), int(bool(causal)),
-                                          counter, int(kernel), stream)
+        st = attn_fwd_paged_variant(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr(), cu_seqlens_q.data_ptr(), seqlens_k.data_ptr(),
+                                    block_table.data_ptr(), batch, int(max_seqlen_q), total_q, num_pages, page_size,
+                                    block_table.shape[1], H, D, float(scale), int(bool(causal)), counter,
+                                    int(kernel), stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_fwd_paged")
     return out, lse

@@ -338,6 +338,34 @@ def test_variant_argument_checks(lib):
     assert f(*a[:5], 0, 2, 256, 256, 128, 0.1, 0, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_OK
 
 
+def test_varlen_and_paged_variant_argument_checks(lib):
+    # each call ends at a host-side check (no device query, no launch)
+    f = attn.attn_fwd_varlen_variant
+    a = (A, A, A, A, A, A, A, 2, 256, 512, 512, 2)  # ... batch, max_seqlen_q, total_q, total_k, H
+    assert f(*a, 128, 0.1, 1, None, 2, None) == attn.ATTN_ERR_SHAPE                     # unknown kernel
+    assert f(*a, 128, 0.1, 1, None, -2, None) == attn.ATTN_ERR_SHAPE
+    assert f(*a, 96, 0.1, 1, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_UNSUPPORTED_D
+    assert f(*a, 128, float("nan"), 1, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_SCALE
+    assert f(A, A, A, None, *a[4:], 128, 0.1, 1, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_NULLPTR
+    assert f(A + 8, *a[1:], 128, 0.1, 1, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_ALIGN
+    assert f(*a, 128, 0.1, 1, A + 4, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_ALIGN  # counter
+    assert f(A, A, A, A, A, A, A, 0, 256, 512, 512, 2, 128, 0.1, 1, None,
+             attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_OK                                    # nothing to compute
+    g = attn.attn_fwd_paged_variant
+    b = (A, A, A, A, A, A, A, A, 2, 256, 512)  # ... block_table, batch, max_seqlen_q, total_q
+    assert g(*b, 4, 256, 2, 2, 128, 0.1, 1, None, 2, None) == attn.ATTN_ERR_SHAPE       # unknown kernel
+    assert g(*b, 4, 100, 2, 2, 128, 0.1, 1, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_SHAPE
+    assert g(*b, 0, 256, 2, 2, 128, 0.1, 1, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_SHAPE
+    assert g(*b, 4, 256, 2, 2, 96, 0.1, 1, None, attn.ATTN_KERNEL_ONE_TILE, None) == attn.ATTN_ERR_UNSUPPORTED_D
+    assert g(*b, 4, 256, 2, 2, 128, float("inf"), 1, None, attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_SCALE
+    assert g(*b[:7], None, *b[8:], 4, 256, 2, 2, 128, 0.1, 1, None,
+             attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_NULLPTR                           # no page table
+    assert g(A, A + 8, *b[2:], 4, 256, 2, 2, 128, 0.1, 1, None,
+             attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_ERR_ALIGN
+    assert g(*b[:8], 0, 256, 512, 4, 256, 2, 2, 128, 0.1, 1, None,
+             attn.ATTN_KERNEL_TWO_TILE, None) == attn.ATTN_OK                                    # nothing to compute
+
+
 def test_fp8_ex_argument_checks(lib):
     # each call ends at a host-side check (no device query, no launch)
     f = attn.attn_fwd_fp8_ex
