@@ -1181,12 +1181,22 @@ bool make_map_packed(CUtensorMap* m, const void* ptr, int H, int total, int D, i
 }
 
 // Heads per causal group: as many as keep their K and V within 48 MB of L2
-// (K/V bytes of one head = 2 * keys * D * element size).
+// (K/V bytes of one head = 2 * keys * D * element size).  Each group's units
+// come longest first, so a last group of less than half the others' size
+// would put its long units at the end of the launch; then the heads are
+// spread evenly over the same number of groups (measured, causal D = 128:
+// 32 heads at 4096 keys, 24 + 8 heads 968 TFLOP/s, 16 + 16 heads 1077; 64
+// heads at 8192 keys 1352 against 1401; evening out groups that were already
+// at least half full cost up to 5 %, so those stay as they are).
 int head_group_for(int bh_count, int keys, int D, int elem_bytes) {
+  const uint64_t bh = static_cast<uint64_t>(bh_count > 0 ? bh_count : 1);
   const uint64_t per_head = 2ull * static_cast<uint64_t>(keys > 0 ? keys : 1) * D * elem_bytes;
   uint64_t g = (48ull << 20) / per_head;
   if (g < 1) g = 1;
-  if (g > static_cast<uint64_t>(bh_count > 0 ? bh_count : 1)) g = bh_count > 0 ? bh_count : 1;
+  if (g > bh) g = bh;
+  const uint64_t groups = (bh + g - 1) / g;
+  const uint64_t last = bh - (groups - 1) * g;
+  if (groups > 1 && 2 * last < g) g = (bh + groups - 1) / groups;
   return static_cast<int>(g);
 }
 
