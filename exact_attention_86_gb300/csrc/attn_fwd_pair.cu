@@ -833,12 +833,23 @@ constexpr int kMaxDevicesPair = 64;
 std::atomic<bool> g_pair_smem_set[kMaxDevicesPair][12];
 
 // Cost model of a unit, in hundredths of the time one 128-key tile takes the
-// one-tile kernel: a key tile that both query tiles of a pair process costs
-// 184 (measured: 1527 against 1390 TFLOP/s on the S = 8192 workload), one
-// that only tile B processes (the last of a causal pair) 130, and the fixed
-// part of a unit (Q load, first tile, epilogue) 150 for a single tile and
-// 200 for a pair (both estimates from a clock trace of the one-tile kernel).
-constexpr int64_t kCostTile = 100, kCostUnit = 150, kCostBoth = 184, kCostAlone = 130, kCostPairUnit = 200;
+// one-tile kernel.  Which kernel runs: non-causal, a key tile that both query
+// tiles of a pair process costs 184 (measured: 1527 against 1390 TFLOP/s on
+// the S = 8192 workload); causal, constants fitted by least squares to the
+// launch times of both kernels on causal batches (D = 128, S = 1024 to 8192,
+// 128 to 4096 query tiles; within 3 us of every time): a key tile of both
+// query tiles 181, the fixed part of a single-tile unit (Q load, first tile,
+// epilogue) 298, and the fixed part of a pair together with its last key
+// tile, which only tile B processes, 996 (taken as 498 each; the fit cannot
+// tell the two apart, as every causal pair has one such tile).  The static
+// deal of causal pairs weighs them 184 (both tiles), 130 (tile B alone) and
+// 200 (fixed part): dealt with the fitted weights instead, batches of 32 and
+// 64 heads at 4096 and 8192 keys ran 1.6 % and 2 % slower.
+struct PairWeights {
+  int64_t both, alone, unit;
+};
+constexpr int64_t kCostTile = 100, kCostBothDense = 184, kCostUnit = 298;
+constexpr PairWeights kRouteWeights{181, 498, 498}, kDealWeights{184, 130, 200};
 
 int64_t key_tiles(int64_t q0, int64_t rows, int64_t Sk, bool causal) {
   if (rows <= 0) return 0;
@@ -852,12 +863,12 @@ int64_t tile_cost(int64_t qt, int64_t Sq, int64_t Sk, bool causal) {
   return key_tiles(q0, std::min<int64_t>(kBQ, Sq - q0), Sk, causal) * kCostTile + kCostUnit;
 }
 
-int64_t pair_cost(int64_t pr, int64_t Sq, int64_t Sk, bool causal) {
+int64_t pair_cost(int64_t pr, int64_t Sq, int64_t Sk, bool causal, const PairWeights& w) {
   const int64_t q0 = pr * 2 * kBQ;
   const int64_t na = key_tiles(q0, std::min<int64_t>(kBQ, Sq - q0), Sk, causal);
   const int64_t nb = key_tiles(q0 + kBQ, std::min<int64_t>(kBQ, Sq - q0 - kBQ), Sk, causal);
   const int64_t both = std::min(na, nb);
-  return both * kCostBoth + (std::max(na, nb) - both) * kCostAlone + kCostPairUnit;
+  return both * w.both + (std::max(na, nb) - both) * w.alone + w.unit;
 }
 
 struct CachedSchedule {
@@ -936,7 +947,7 @@ bool use_pair(int B, int H, int Sq, int Sk, bool causal, int num_sms) {
   const int64_t n_pairs = (static_cast<int64_t>(Sq) + 2 * kBQ - 1) / (2 * kBQ);
   if (!causal) {
     // units of one length: waves of units over the SMs
-    return kCostBoth * ((bh * n_pairs + g - 1) / g) < kCostTile * ((bh * n_tiles + g - 1) / g);
+    return kCostBothDense * ((bh * n_pairs + g - 1) / g) < kCostTile * ((bh * n_tiles + g - 1) / g);
   }
   // causal units of many lengths, dealt longest first: the time is about the
   // larger of the longest unit and the mean work per SM; the pair kernel
@@ -949,7 +960,7 @@ bool use_pair(int B, int H, int Sq, int Sk, bool causal, int num_sms) {
     one_max = std::max(one_max, c);
   }
   for (int64_t t = 0; t < n_pairs; ++t) {
-    const int64_t c = pair_cost(t, Sq, Sk, true);
+    const int64_t c = pair_cost(t, Sq, Sk, true, kRouteWeights);
     pair_total += c;
     pair_max = std::max(pair_max, c);
   }
@@ -974,7 +985,7 @@ int64_t build_schedule(int B, int H, int Sq, int Sk, int head_group, int grid, u
   for (int64_t g0 = 0; g0 < bh; g0 += head_group) {
     const int64_t heads = std::min<int64_t>(head_group, bh - g0);
     for (int64_t wq = 0; wq < n_pairs; ++wq) {
-      const int64_t c = pair_cost(n_pairs - 1 - wq, Sq, Sk, true);
+      const int64_t c = pair_cost(n_pairs - 1 - wq, Sq, Sk, true, kDealWeights);
       for (int64_t h = 0; h < heads; ++h, ++t) {
         const Load l = free_at.top();
         free_at.pop();

@@ -297,6 +297,9 @@ def test_kernel_choice(lib):
     assert f(2, 16, 8192, 8192, 1, 152) == 1      # causal, 1024 pair units dealt statically
     assert f(1, 8, 32768, 32768, 1, 152) == 1
     assert f(4, 8, 1024, 1024, 1, 152) == 0       # causal, short: the longest pair unit sets the time
+    assert f(2, 16, 2048, 2048, 1, 152) == 0      # causal, 8 pairs a head: unit costs favour single tiles
+    assert f(8, 16, 2048, 2048, 1, 152) == 0      # (measured 148 against 154 us)
+    assert f(2, 16, 4096, 4096, 1, 152) == 1      # (measured 128 against 132 us)
     assert f(16, 16, 8192, 8192, 1, 152) == 0     # causal, 8192 pair units: more than the static deal holds
     assert f(1, 8, 128, 32768, 0, 152) == 0       # one query tile per head: pairs half empty
     assert f(1, 1, 128, 128, 0, 152) == 0
