@@ -282,13 +282,15 @@ def is_fp8(w) -> bool:
 def forward_kernel(w, splits: int, num_sms: int) -> str:
     """The kernel that does the forward's work for this workload, as the
     library chooses it: padded batches (bf16 or E4M3) without key ranges may
-    run the two-query-tile kernel (attn_fwd_kernel_choice); packed and paged
+    run the two-query-tile kernel (attn_fwd_kernel_choice,
+    attn_fwd_fp8_kernel_choice); packed and paged
     batches run it when a sequence may hold more than one query tile; split
     batches run the one-tile kernel."""
     from exact_attention_86_gb300 import attn
     if is_varlen(w):
         return "attn_fwd_pair_kernel" if w.max_len > 128 else "attn_fwd_kernel"
-    if splits == 0 and attn.attn_fwd_kernel_choice(w.B, w.H, w.Sq, w.Sk, int(w.causal), num_sms) == 1:
+    choice = attn.attn_fwd_fp8_kernel_choice if is_fp8(w) else attn.attn_fwd_kernel_choice
+    if splits == 0 and choice(w.B, w.H, w.Sq, w.Sk, int(w.causal), num_sms) == 1:
         return "attn_fwd_pair_kernel"
     return "attn_fwd_kernel"
 

@@ -1413,7 +1413,7 @@ attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const voi
   p.selftest_skip_fill = selftest_skip_fill;
 #ifndef ATTN_NO_PAIR
   const bool pair = kernel == ATTN_KERNEL_TWO_TILE ||
-                    (kernel == ATTN_KERNEL_AUTO && attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, dev.num_sms));
+                    (kernel == ATTN_KERNEL_AUTO && attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, dev.num_sms, false));
   if (o_part == nullptr && pair) {
     // whole rows: units of two query tiles (attn_fwd_pair_kernel)
     Params pp = p;
@@ -1526,8 +1526,8 @@ attn_status attn_fwd_fp8_variant(const void* q, const void* k, const void* v, vo
   p.wait_limit_ns = kWaitLimitNs;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kernel == ATTN_KERNEL_TWO_TILE ||
-      (kernel == ATTN_KERNEL_AUTO && attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, dev->num_sms))) {
-    // units of two query tiles (attn_fwd_pair_kernel), chosen as for bf16
+      (kernel == ATTN_KERNEL_AUTO && attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, dev->num_sms, true))) {
+    // units of two query tiles (attn_fwd_pair_kernel), by the E4M3 cost model
     Params pp = p;
     const uint64_t n_pairs = (static_cast<uint64_t>(Sq) + 2 * kBQ - 1) / (2 * kBQ);
     pp.n_qtiles = static_cast<int>(n_pairs);
@@ -1888,7 +1888,12 @@ int64_t attn_fwd_pair_schedule(int B, int H, int Sq, int Sk, int head_group, int
 
 int attn_fwd_kernel_choice(int B, int H, int Sq, int Sk, int causal, int num_sms) {
   if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || num_sms < 0) return -1;
-  return attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, num_sms) ? 1 : 0;
+  return attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, num_sms, false) ? 1 : 0;
+}
+
+int attn_fwd_fp8_kernel_choice(int B, int H, int Sq, int Sk, int causal, int num_sms) {
+  if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || num_sms < 0) return -1;
+  return attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, num_sms, true) ? 1 : 0;
 }
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }

@@ -153,7 +153,7 @@ attn_status attn_fwd_fp8_ex(const void* q, const void* k, const void* v, void* o
 /*
  * attn_fwd_fp8_variant — attn_fwd_fp8_ex with the kernel chosen by the
  * caller: `kernel` as in attn_fwd_variant (ATTN_KERNEL_AUTO: the kernel
- * attn_fwd_fp8_ex runs, which attn_fwd_kernel_choice names; ATTN_KERNEL_ONE_TILE
+ * attn_fwd_fp8_ex runs, which attn_fwd_fp8_kernel_choice names; ATTN_KERNEL_ONE_TILE
  * or ATTN_KERNEL_TWO_TILE forced).  Both compute the same function within the
  * E4M3 forward's tolerance; they are not bit-identical to each other (their
  * row sums split differently over threads).  Any other `kernel`:
@@ -444,9 +444,9 @@ attn_status attn_selftest_fwd_abort(const void* q, const void* k, const void* v,
 attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t stream);
 
 /*
- * attn_fwd_kernel_choice — which kernel attn_fwd and attn_fwd_fp8_ex run for
- * a padded batch of B x H heads of Sq queries and Sk keys, causal or not, on
- * a device with `num_sms` SMs.  Returns 1 for the two-query-tile kernel (units of 256 query
+ * attn_fwd_kernel_choice — which kernel attn_fwd runs for a padded bf16 batch
+ * of B x H heads of Sq queries and Sk keys, causal or not, on a device with
+ * `num_sms` SMs.  Returns 1 for the two-query-tile kernel (units of 256 query
  * rows), 0 for the one-tile kernel (units of 128 rows), -1 for a negative
  * argument.  The two compute the same function; the choice is a cost model
  * of the work units (non-causal: waves of equal units over the SMs; causal:
@@ -454,6 +454,16 @@ attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t 
  * two-tile units) and never depends on the data.  Host only: no CUDA call.
  */
 int attn_fwd_kernel_choice(int B, int H, int Sq, int Sk, int causal, int num_sms);
+
+/*
+ * attn_fwd_fp8_kernel_choice — the same for attn_fwd_fp8_ex (E4M3 inputs):
+ * its products take half the bf16 time, so the softmax, which the two-tile
+ * kernel interleaves, weighs more and the two-tile kernel is chosen more
+ * often (non-causal: a cheaper pair in the wave model; causal: the two-tile
+ * kernel from 1024 queries on, within the 4096-unit limit).  Same results
+ * and errors as attn_fwd_kernel_choice.
+ */
+int attn_fwd_fp8_kernel_choice(int B, int H, int Sq, int Sk, int causal, int num_sms);
 
 /*
  * attn_fwd_pair_schedule — the static deal of a causal batch's two-tile units
@@ -474,7 +484,7 @@ int64_t attn_fwd_pair_schedule(int B, int H, int Sq, int Sk, int head_group, int
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 16
+#define ATTN_ABI_VERSION 17
 
 #ifdef __cplusplus
 }

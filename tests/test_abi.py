@@ -300,6 +300,16 @@ def test_kernel_choice(lib):
     assert f(2, 16, 2048, 2048, 1, 152) == 0      # causal, 8 pairs a head: unit costs favour single tiles
     assert f(8, 16, 2048, 2048, 1, 152) == 0      # (measured 148 against 154 us)
     assert f(2, 16, 4096, 4096, 1, 152) == 1      # (measured 128 against 132 us)
+    # E4M3: the two-tile kernel measured faster on every batch above one query tile timed
+    f8 = attn.attn_fwd_fp8_kernel_choice
+    assert f8(8, 16, 2048, 2048, 1, 152) == 1     # causal (136 against 156 us)
+    assert f8(8, 16, 1024, 1024, 1, 152) == 1     # causal (54 against 56 us)
+    assert f8(2, 16, 4096, 4096, 0, 152) == 1     # non-causal, 4 against 7 waves (201 against 214 us)
+    assert f8(2, 16, 8192, 8192, 0, 152) == 1
+    assert f8(1, 8, 128, 32768, 0, 152) == 0      # one query tile per head
+    assert f8(1, 1, 8192, 8192, 0, 152) == 0      # 64 single tiles fit one wave
+    assert f8(16, 16, 8192, 8192, 1, 152) == 0    # more units than the static deal holds
+    assert f8(-1, 16, 8192, 8192, 0, 152) == -1
     assert f(16, 16, 8192, 8192, 1, 152) == 0     # causal, 8192 pair units: more than the static deal holds
     assert f(1, 8, 128, 32768, 0, 152) == 0       # one query tile per head: pairs half empty
     assert f(1, 1, 128, 128, 0, 152) == 0
