@@ -290,7 +290,7 @@ def forward_kernel(w, splits: int, num_sms: int) -> str:
     if is_varlen(w):
         return "attn_fwd_pair_kernel" if w.max_len > 128 else "attn_fwd_kernel"
     choice = attn.attn_fwd_fp8_kernel_choice if is_fp8(w) else attn.attn_fwd_kernel_choice
-    if splits == 0 and choice(w.B, w.H, w.Sq, w.Sk, int(w.causal), num_sms) == 1:
+    if splits == 0 and choice(w.B, w.H, w.Sq, w.Sk, w.D, int(w.causal), num_sms) == 1:
         return "attn_fwd_pair_kernel"
     return "attn_fwd_kernel"
 

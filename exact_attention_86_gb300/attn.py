@@ -106,8 +106,8 @@ SIGNATURES = {
                                                                                           ctypes.c_void_p, ctypes.c_int,
                                                                                           ctypes.c_int, ctypes.c_int64,
                                                                                           ctypes.c_void_p]),
-    "attn_fwd_kernel_choice": (ctypes.c_int, [ctypes.c_int] * 6),
-    "attn_fwd_fp8_kernel_choice": (ctypes.c_int, [ctypes.c_int] * 6),
+    "attn_fwd_kernel_choice": (ctypes.c_int, [ctypes.c_int] * 7),
+    "attn_fwd_fp8_kernel_choice": (ctypes.c_int, [ctypes.c_int] * 7),
     "attn_fwd_pair_schedule": (ctypes.c_int64, [ctypes.c_int] * 6 + [ctypes.c_void_p, ctypes.c_int64]),
     "attn_abi_version": (ctypes.c_int, []),
 }
@@ -268,12 +268,12 @@ def attn_selftest_launch_floor(grid: int, D: int, mode: int, stream: Optional[in
     return lib().attn_selftest_launch_floor(grid, D, mode, stream)
 
 
-def attn_fwd_kernel_choice(B: int, H: int, Sq: int, Sk: int, causal: int, num_sms: int) -> int:
-    return lib().attn_fwd_kernel_choice(B, H, Sq, Sk, int(causal), num_sms)
+def attn_fwd_kernel_choice(B: int, H: int, Sq: int, Sk: int, D: int, causal: int, num_sms: int) -> int:
+    return lib().attn_fwd_kernel_choice(B, H, Sq, Sk, D, int(causal), num_sms)
 
 
-def attn_fwd_fp8_kernel_choice(B: int, H: int, Sq: int, Sk: int, causal: int, num_sms: int) -> int:
-    return lib().attn_fwd_fp8_kernel_choice(B, H, Sq, Sk, int(causal), num_sms)
+def attn_fwd_fp8_kernel_choice(B: int, H: int, Sq: int, Sk: int, D: int, causal: int, num_sms: int) -> int:
+    return lib().attn_fwd_fp8_kernel_choice(B, H, Sq, Sk, D, int(causal), num_sms)
 
 
 def attn_fwd_pair_schedule(B: int, H: int, Sq: int, Sk: int, head_group: int, grid: int, max_units: int = 4096):

@@ -1412,8 +1412,9 @@ attn_status run_forward(DeviceInfo& dev, const void* q, const void* k, const voi
   p.wait_limit_ns = wait_limit_ns;
   p.selftest_skip_fill = selftest_skip_fill;
 #ifndef ATTN_NO_PAIR
-  const bool pair = kernel == ATTN_KERNEL_TWO_TILE ||
-                    (kernel == ATTN_KERNEL_AUTO && attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, dev.num_sms, false));
+  const bool pair =
+      kernel == ATTN_KERNEL_TWO_TILE ||
+      (kernel == ATTN_KERNEL_AUTO && attn_pair_host::use_pair(B, H, Sq, Sk, D, causal != 0, dev.num_sms, false));
   if (o_part == nullptr && pair) {
     // whole rows: units of two query tiles (attn_fwd_pair_kernel)
     Params pp = p;
@@ -1526,7 +1527,7 @@ attn_status attn_fwd_fp8_variant(const void* q, const void* k, const void* v, vo
   p.wait_limit_ns = kWaitLimitNs;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (kernel == ATTN_KERNEL_TWO_TILE ||
-      (kernel == ATTN_KERNEL_AUTO && attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, dev->num_sms, true))) {
+      (kernel == ATTN_KERNEL_AUTO && attn_pair_host::use_pair(B, H, Sq, Sk, D, causal != 0, dev->num_sms, true))) {
     // units of two query tiles (attn_fwd_pair_kernel), by the E4M3 cost model
     Params pp = p;
     const uint64_t n_pairs = (static_cast<uint64_t>(Sq) + 2 * kBQ - 1) / (2 * kBQ);
@@ -1886,14 +1887,14 @@ int64_t attn_fwd_pair_schedule(int B, int H, int Sq, int Sk, int head_group, int
   return attn_pair_host::build_schedule(B, H, Sq, Sk, head_group, grid, owner, max_units);
 }
 
-int attn_fwd_kernel_choice(int B, int H, int Sq, int Sk, int causal, int num_sms) {
-  if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || num_sms < 0) return -1;
-  return attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, num_sms, false) ? 1 : 0;
+int attn_fwd_kernel_choice(int B, int H, int Sq, int Sk, int D, int causal, int num_sms) {
+  if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || num_sms < 0 || (D != 64 && D != 128)) return -1;
+  return attn_pair_host::use_pair(B, H, Sq, Sk, D, causal != 0, num_sms, false) ? 1 : 0;
 }
 
-int attn_fwd_fp8_kernel_choice(int B, int H, int Sq, int Sk, int causal, int num_sms) {
-  if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || num_sms < 0) return -1;
-  return attn_pair_host::use_pair(B, H, Sq, Sk, causal != 0, num_sms, true) ? 1 : 0;
+int attn_fwd_fp8_kernel_choice(int B, int H, int Sq, int Sk, int D, int causal, int num_sms) {
+  if (B < 0 || H < 0 || Sq < 0 || Sk < 0 || num_sms < 0 || (D != 64 && D != 128)) return -1;
+  return attn_pair_host::use_pair(B, H, Sq, Sk, D, causal != 0, num_sms, true) ? 1 : 0;
 }
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }

@@ -849,10 +849,12 @@ struct PairWeights {
   int64_t both, alone, unit;
 };
 constexpr int64_t kCostTile = 100, kCostBothDense = 184, kCostUnit = 298;
-// E4M3, non-causal: a key tile of both query tiles costs 170 (measured on the
-// S = 8192 workload: 656 against 773 us at 7 against 14 waves); its faster
-// products leave the softmax the longer part, which the pair interleaves.
-constexpr int64_t kCostBothDenseFp8 = 170;
+// E4M3 or D = 64, non-causal: a key tile of both query tiles costs 170
+// (measured on the E4M3 S = 8192 workload: 656 against 773 us at 7 against 14
+// waves; bf16 D = 64 S = 1024, 4 against 7 waves: 58 against 66 us): their
+// faster products leave the softmax the longer part, which the pair
+// interleaves.
+constexpr int64_t kCostBothDenseLight = 170;
 constexpr PairWeights kRouteWeights{181, 498, 498}, kDealWeights{184, 130, 200};
 
 int64_t key_tiles(int64_t q0, int64_t rows, int64_t Sk, bool causal) {
@@ -943,24 +945,29 @@ attn_status launch_pair(int dev, int num_sms, const CUtensorMap& mq, const CUten
 
 namespace attn_pair_host {
 
-bool use_pair(int B, int H, int Sq, int Sk, bool causal, int num_sms, bool fp8) {
-  if (B <= 0 || H <= 0 || Sq <= kBQ || Sk < 0 || num_sms < 1) return false;
+bool use_pair(int B, int H, int Sq, int Sk, int D, bool causal, int num_sms, bool fp8) {
+  if (B <= 0 || H <= 0 || Sq <= kBQ || Sk < 0 || num_sms < 1 || (D != 64 && D != 128)) return false;
+  // E4M3 or D = 64: products that take half the bf16 D = 128 time (or less),
+  // so the softmax, which the pair interleaves, weighs more
+  const bool light = fp8 || D == 64;
   const int64_t bh = static_cast<int64_t>(B) * H;
   const int64_t g = num_sms;
   const int64_t n_tiles = (static_cast<int64_t>(Sq) + kBQ - 1) / kBQ;
   const int64_t n_pairs = (static_cast<int64_t>(Sq) + 2 * kBQ - 1) / (2 * kBQ);
   if (!causal) {
     // units of one length: waves of units over the SMs
-    const int64_t both = fp8 ? kCostBothDenseFp8 : kCostBothDense;
+    const int64_t both = light ? kCostBothDenseLight : kCostBothDense;
     return both * ((bh * n_pairs + g - 1) / g) < kCostTile * ((bh * n_tiles + g - 1) / g);
   }
   // causal units of many lengths, dealt longest first: the time is about the
   // larger of the longest unit and the mean work per SM; the pair kernel
   // needs its static deal (at most 4096 units) to balance
   if (bh * n_pairs > kSchedMaxUnits) return false;
-  // E4M3 from 1024 queries on: the pair kernel measured 4-22 % faster on
-  // every causal batch timed (S = 1024 to 8192); shorter ones take the model
-  if (fp8 && Sq >= 1024) return true;
+  // light products from 1024 (E4M3) or 2048 (bf16 D = 64) queries on: the
+  // pair measured faster on every such causal batch timed (E4M3 S = 1024 to
+  // 8192: 4-26 %; D = 64 S = 2048 to 8192: 6-24 %, but 4 % slower at 1024);
+  // shorter ones take the model
+  if (light && Sq >= (fp8 ? 1024 : 2048)) return true;
   int64_t one_total = 0, one_max = 0, pair_total = 0, pair_max = 0;
   for (int64_t t = 0; t < n_tiles; ++t) {
     const int64_t c = tile_cost(t, Sq, Sk, true);

@@ -16,11 +16,11 @@ struct Params;
 
 namespace attn_pair_host {
 
-// Whether a padded batch of B x H heads (Sq queries, Sk keys; bf16, or E4M3
-// when fp8) runs faster on the two-tile kernel than on the one-tile kernel of
-// attn_fwd.cu, on a device with num_sms SMs.  A cost model of each work unit,
-// host arithmetic only; false for arguments out of range.
-bool use_pair(int B, int H, int Sq, int Sk, bool causal, int num_sms, bool fp8);
+// Whether a padded batch of B x H heads (Sq queries, Sk keys, head dimension
+// D; bf16, or E4M3 when fp8) runs faster on the two-tile kernel than on the
+// one-tile kernel of attn_fwd.cu, on a device with num_sms SMs.  A cost model
+// of each work unit, host arithmetic only; false for arguments out of range.
+bool use_pair(int B, int H, int Sq, int Sk, int D, bool causal, int num_sms, bool fp8);
 
 // Launches the forward over units of two 128-row query tiles (p.n_qtiles =
 // tile pairs per head, p.total_units = B * H * pairs; every other field as

@@ -445,25 +445,27 @@ attn_status attn_selftest_launch_floor(int grid, int D, int mode, attn_stream_t 
 
 /*
  * attn_fwd_kernel_choice — which kernel attn_fwd runs for a padded bf16 batch
- * of B x H heads of Sq queries and Sk keys, causal or not, on a device with
- * `num_sms` SMs.  Returns 1 for the two-query-tile kernel (units of 256 query
- * rows), 0 for the one-tile kernel (units of 128 rows), -1 for a negative
- * argument.  The two compute the same function; the choice is a cost model
- * of the work units (non-causal: waves of equal units over the SMs; causal:
- * the larger of the longest unit and the mean work per SM, with at most 4096
- * two-tile units) and never depends on the data.  Host only: no CUDA call.
+ * of B x H heads of Sq queries and Sk keys, head dimension D, causal or not,
+ * on a device with `num_sms` SMs.  Returns 1 for the two-query-tile kernel
+ * (units of 256 query rows), 0 for the one-tile kernel (units of 128 rows),
+ * -1 for a negative argument or D other than 64 and 128.  The two compute
+ * the same function; the choice is a cost model of the work units
+ * (non-causal: waves of equal units over the SMs; causal: the larger of the
+ * longest unit and the mean work per SM, with at most 4096 two-tile units)
+ * and never depends on the data.  At D = 64 the products take half the
+ * D = 128 time, so the softmax, which the two-tile kernel interleaves, weighs
+ * more and that kernel is chosen more often.  Host only: no CUDA call.
  */
-int attn_fwd_kernel_choice(int B, int H, int Sq, int Sk, int causal, int num_sms);
+int attn_fwd_kernel_choice(int B, int H, int Sq, int Sk, int D, int causal, int num_sms);
 
 /*
- * attn_fwd_fp8_kernel_choice — the same for attn_fwd_fp8_ex (E4M3 inputs):
- * its products take half the bf16 time, so the softmax, which the two-tile
- * kernel interleaves, weighs more and the two-tile kernel is chosen more
- * often (non-causal: a cheaper pair in the wave model; causal: the two-tile
- * kernel from 1024 queries on, within the 4096-unit limit).  Same results
- * and errors as attn_fwd_kernel_choice.
+ * attn_fwd_fp8_kernel_choice — the same for attn_fwd_fp8_ex (E4M3 inputs),
+ * whose products take half the bf16 time: the two-tile kernel is chosen as
+ * for bf16 D = 64 (non-causal: a cheaper pair in the wave model; causal: from
+ * 1024 queries on, within the 4096-unit limit).  Same results and errors as
+ * attn_fwd_kernel_choice.
  */
-int attn_fwd_fp8_kernel_choice(int B, int H, int Sq, int Sk, int causal, int num_sms);
+int attn_fwd_fp8_kernel_choice(int B, int H, int Sq, int Sk, int D, int causal, int num_sms);
 
 /*
  * attn_fwd_pair_schedule — the static deal of a causal batch's two-tile units
@@ -484,7 +486,7 @@ int64_t attn_fwd_pair_schedule(int B, int H, int Sq, int Sk, int head_group, int
 /* ABI version of this header (incremented on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 17
+#define ATTN_ABI_VERSION 18
 
 #ifdef __cplusplus
 }

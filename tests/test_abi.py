@@ -290,39 +290,47 @@ def test_launch_floor_argument_checks(lib):
 
 
 def test_kernel_choice(lib):
-    # host-only model of which padded-forward kernel runs (no device call)
+    # host-only model of which padded-forward kernel runs (no device call);
+    # arguments B, H, Sq, Sk, D, causal, num_sms
     f = attn.attn_fwd_kernel_choice
-    assert f(2, 16, 8192, 8192, 0, 152) == 1      # 1024 pairs: 7 waves against 14 of single tiles
-    assert f(8, 16, 2048, 2048, 0, 152) == 1
-    assert f(2, 16, 8192, 8192, 1, 152) == 1      # causal, 1024 pair units dealt statically
-    assert f(1, 8, 32768, 32768, 1, 152) == 1
-    assert f(4, 8, 1024, 1024, 1, 152) == 0       # causal, short: the longest pair unit sets the time
-    assert f(2, 16, 2048, 2048, 1, 152) == 0      # causal, 8 pairs a head: unit costs favour single tiles
-    assert f(8, 16, 2048, 2048, 1, 152) == 0      # (measured 148 against 154 us)
-    assert f(2, 16, 4096, 4096, 1, 152) == 1      # (measured 128 against 132 us)
-    # E4M3: the two-tile kernel measured faster on every batch above one query tile timed
-    f8 = attn.attn_fwd_fp8_kernel_choice
-    assert f8(8, 16, 2048, 2048, 1, 152) == 1     # causal (136 against 156 us)
-    assert f8(8, 16, 1024, 1024, 1, 152) == 1     # causal (54 against 56 us)
-    assert f8(2, 16, 4096, 4096, 0, 152) == 1     # non-causal, 4 against 7 waves (201 against 214 us)
-    assert f8(2, 16, 8192, 8192, 0, 152) == 1
-    assert f8(1, 8, 128, 32768, 0, 152) == 0      # one query tile per head
-    assert f8(1, 1, 8192, 8192, 0, 152) == 0      # 64 single tiles fit one wave
-    assert f8(16, 16, 8192, 8192, 1, 152) == 0    # more units than the static deal holds
-    assert f8(-1, 16, 8192, 8192, 0, 152) == -1
-    assert f(16, 16, 8192, 8192, 1, 152) == 0     # causal, 8192 pair units: more than the static deal holds
-    assert f(1, 8, 128, 32768, 0, 152) == 0       # one query tile per head: pairs half empty
-    assert f(1, 1, 128, 128, 0, 152) == 0
-    assert f(1, 1, 8192, 8192, 0, 152) == 0       # 64 single tiles fit one wave
-    assert f(0, 16, 8192, 8192, 0, 152) == 0
-    assert f(-1, 16, 8192, 8192, 0, 152) == -1
-    assert f(2, 16, 8192, -1, 0, 152) == -1
-    assert f(2, 16, 8192, 8192, 0, -1) == -1
+    assert f(2, 16, 8192, 8192, 128, 0, 152) == 1   # 1024 pairs: 7 waves against 14 of single tiles
+    assert f(8, 16, 2048, 2048, 128, 0, 152) == 1
+    assert f(2, 16, 8192, 8192, 128, 1, 152) == 1   # causal, 1024 pair units dealt statically
+    assert f(1, 8, 32768, 32768, 128, 1, 152) == 1
+    assert f(4, 8, 1024, 1024, 128, 1, 152) == 0    # causal, short: the longest pair unit sets the time
+    assert f(2, 16, 2048, 2048, 128, 1, 152) == 0   # causal, 8 pairs a head: unit costs favour single tiles
+    assert f(8, 16, 2048, 2048, 128, 1, 152) == 0   # (measured 148 against 154 us)
+    assert f(2, 16, 4096, 4096, 128, 1, 152) == 1   # (measured 128 against 132 us)
+    assert f(16, 16, 8192, 8192, 128, 1, 152) == 0  # causal, 8192 pair units: more than the static deal holds
+    assert f(1, 8, 128, 32768, 128, 0, 152) == 0    # one query tile per head: pairs half empty
+    assert f(1, 1, 128, 128, 128, 0, 152) == 0
+    assert f(1, 1, 8192, 8192, 128, 0, 152) == 0    # 64 single tiles fit one wave
+    assert f(0, 16, 8192, 8192, 128, 0, 152) == 0
+    # D = 64: lighter products, so the pair more often (measured)
+    assert f(8, 16, 1024, 1024, 64, 0, 152) == 1    # 4 against 7 waves (58 against 66 us)
+    assert f(8, 16, 1024, 1024, 128, 0, 152) == 0   # the same waves at D = 128 favour single tiles
+    assert f(8, 16, 2048, 2048, 64, 1, 152) == 1    # causal (130 against 138 us)
+    assert f(8, 16, 1024, 1024, 64, 1, 152) == 0    # causal (52 against 50 us)
+    assert f(-1, 16, 8192, 8192, 128, 0, 152) == -1
+    assert f(2, 16, 8192, -1, 128, 0, 152) == -1
+    assert f(2, 16, 8192, 8192, 128, 0, -1) == -1
+    assert f(2, 16, 8192, 8192, 96, 0, 152) == -1   # unsupported D
     # never for a single query tile, whatever the batch
     for bh in (1, 7, 152, 153, 10_000):
         for causal in (0, 1):
-            assert f(1, bh, 100, 100, causal, 152) == 0
-            assert f(1, bh, 128, 4096, causal, 152) == 0
+            for D in (64, 128):
+                assert f(1, bh, 100, 100, D, causal, 152) == 0
+                assert f(1, bh, 128, 4096, D, causal, 152) == 0
+    # E4M3: the two-tile kernel measured faster on every batch above one query tile timed
+    f8 = attn.attn_fwd_fp8_kernel_choice
+    assert f8(8, 16, 2048, 2048, 128, 1, 152) == 1  # causal (136 against 156 us)
+    assert f8(8, 16, 1024, 1024, 128, 1, 152) == 1  # causal (54 against 56 us)
+    assert f8(2, 16, 4096, 4096, 128, 0, 152) == 1  # non-causal, 4 against 7 waves (201 against 214 us)
+    assert f8(2, 16, 8192, 8192, 128, 0, 152) == 1
+    assert f8(1, 8, 128, 32768, 128, 0, 152) == 0   # one query tile per head
+    assert f8(1, 1, 8192, 8192, 128, 0, 152) == 0   # 64 single tiles fit one wave
+    assert f8(16, 16, 8192, 8192, 128, 1, 152) == 0  # more units than the static deal holds
+    assert f8(-1, 16, 8192, 8192, 128, 0, 152) == -1
 
 
 def test_fwd_abort_selftest_argument_checks(lib):
