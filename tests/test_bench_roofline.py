@@ -88,3 +88,29 @@ def test_suggested_splits_against_a_direct_search(_lib):
             even = max(s for s in range(1, s_max + 1) if tiles % s == 0)
             want = even if 2 * even >= s_max else s_max
         assert attn.suggest_num_splits(B, H, Sq, Sk, sms) == want, (B, H, Sq, Sk, sms)
+
+
+# ------------------------------------------- the kernel a bench line names
+@pytest.mark.parametrize("name,kernel", [
+    ("s8192_d128", "attn_fwd_pair_kernel"),          # 7 pair waves against 14 single-tile waves
+    ("s8192_d128_causal", "attn_fwd_pair_kernel"),
+    ("s32768_d128_causal", "attn_fwd_pair_kernel"),
+    ("s2048_d128_padded", "attn_fwd_pair_kernel"),
+    ("s1024_d64_causal", "attn_fwd_kernel"),         # short causal: single tiles
+    ("s128_d64", "attn_fwd_kernel"),                 # one query tile
+    ("q128_k32768_d128", "attn_fwd_kernel"),         # one query tile per head
+    ("varlen_b32_d128_causal", "attn_fwd_pair_kernel"),
+    ("paged_b32_d128_causal", "attn_fwd_pair_kernel"),
+    ("s8192_d128_fp8", "attn_fwd_pair_kernel"),
+    ("s8192_d128_causal_fp8", "attn_fwd_pair_kernel"),
+    ("s8192_d64_fp8", "attn_fwd_pair_kernel"),
+])
+def test_forward_kernel_names_the_routed_kernel(_lib, name, kernel):
+    # the kernel the roofline object attributes its launch time to is the one
+    # the library's host-only choice functions route the workload to
+    assert bench.forward_kernel(bench.lookup(name), 0, 152) == kernel
+
+
+def test_split_workloads_run_the_one_tile_kernel(_lib):
+    assert bench.forward_kernel(bench.lookup("q128_k32768_d128"), 16, 152) == "attn_fwd_kernel"
+    assert bench.forward_kernel(bench.lookup("s8192_d128"), 4, 152) == "attn_fwd_kernel"
