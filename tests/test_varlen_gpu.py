@@ -101,6 +101,25 @@ def test_varlen_guard_rows_untouched(kernel):
 
 @KERNELS
 @pytest.mark.parametrize("causal", [False, True])
+def test_varlen_batch_without_any_key(kernel, causal):
+    """total_k = 0: no K or V tensor is read (the key maps are never
+    dereferenced) and every row gives exactly O = +0, LSE = -inf."""
+    lens_q = [130, 5, 300]
+    H, D = 2, 128
+    q, _, _, cu_q, _ = _packed(lens_q, [1, 1, 1], H, D, seed=29)
+    dev = torch.device("cuda:0")
+    k = torch.empty(0, H, D, dtype=torch.bfloat16, device=dev)
+    v = torch.empty(0, H, D, dtype=torch.bfloat16, device=dev)
+    cu_k = torch.zeros(len(lens_q) + 1, dtype=torch.int32, device=dev)
+    o, lse = attn.forward_varlen(q.to(dev), k, v, cu_q.to(dev), cu_k, max(lens_q), causal=causal, kernel=kernel)
+    st, site = attn.attn_check_device_status(torch.cuda.current_stream().cuda_stream)
+    assert st == attn.ATTN_OK, (st, site)
+    assert torch.all(o.view(torch.int16) == 0)
+    assert torch.all(lse == float("-inf"))
+
+
+@KERNELS
+@pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("max_q", [100, 300, 1000])
 def test_varlen_max_seqlen_q_bounds_the_computed_rows(kernel, causal, max_q):
     """max_seqlen_q sizes the launch.  Above the longest sequence the extra
